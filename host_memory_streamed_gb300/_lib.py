@@ -1,0 +1,110 @@
+"""ctypes loader of libmt.so and the prototypes of its C-ABI (include/mt.h, include/mt_ops.h).
+
+The product path has no fallback: if the library is missing this raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmt.so")
+
+MT_OK, MT_EINVAL, MT_ENOMEM, MT_ECUDA, MT_ETIMEDOUT, MT_ESTATE, MT_ENONFINITE, MT_EINTERNAL = 0, -1, -2, -3, -4, -5, -6, -7
+ERROR_NAMES = {0: "MT_OK", -1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_ECUDA", -4: "MT_ETIMEDOUT",
+               -5: "MT_ESTATE", -6: "MT_ENONFINITE", -7: "MT_EINTERNAL"}
+
+MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS = 1, 2, 4, 8, 16
+MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
+
+EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE = range(6)
+
+
+class MtConfig(C.Structure):
+    _fields_ = [
+        ("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+        ("head_dim", C.c_int32), ("ffn", C.c_int32), ("vocab", C.c_int32),
+        ("rms_eps", C.c_float), ("rope_theta", C.c_float),
+        ("batch", C.c_int32), ("seq", C.c_int32), ("ckpt_every", C.c_int32),
+        ("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float), ("adam_eps", C.c_float),
+        ("weight_decay", C.c_float),
+        ("n_adam_threads", C.c_int32), ("n_pack_threads", C.c_int32), ("n_grad_slabs", C.c_int32),
+        ("grad_slab_bytes", C.c_int64), ("stage_bytes", C.c_int64), ("timeout_ms", C.c_int64),
+        ("flags", C.c_uint32),
+    ]
+
+
+class MtTensorDesc(C.Structure):
+    _fields_ = [("name", C.c_char * 16), ("ndim", C.c_int32), ("shape", C.c_int64 * 2),
+                ("offset", C.c_int64), ("numel", C.c_int64)]
+
+
+class MtTileDesc(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("n_tensors", C.c_int32), ("n_params", C.c_int64),
+                ("w_bytes", C.c_int64), ("tile_bytes", C.c_int64), ("tensors", MtTensorDesc * 8)]
+
+
+class MtStepStats(C.Structure):
+    _fields_ = [
+        ("loss", C.c_double), ("step_ms", C.c_double), ("gpu_compute_ms", C.c_double),
+        ("h2d_ms", C.c_double), ("d2h_ms", C.c_double), ("wait_weights_ms", C.c_double),
+        ("adam_ms", C.c_double), ("adam_tail_ms", C.c_double), ("gemm_ms", C.c_double),
+        ("gemm_flops", C.c_double), ("gemm_launches", C.c_int64), ("kernel_launches", C.c_int64),
+        ("h2d_bytes", C.c_int64), ("d2h_bytes", C.c_int64), ("flops_executed", C.c_int64),
+        ("flops_model", C.c_int64), ("arena_high_water", C.c_int64), ("step", C.c_int64),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmt.so once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with host_memory_streamed_gb300.build.build()")
+    L = C.CDLL(LIB_PATH)
+    vp, i32, i64, sz, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float
+    fp = C.POINTER(C.c_float)
+    sig = {
+        "mt_required_device_bytes": (i64, [C.POINTER(MtConfig)]),
+        "mt_init_model": (C.c_int, [C.POINTER(MtConfig), vp, sz, vp, vp, vp, C.POINTER(vp)]),
+        "mt_tile_count": (C.c_int, [vp]),
+        "mt_tile_info": (C.c_int, [vp, C.c_int, C.POINTER(MtTileDesc)]),
+        "mt_load_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
+        "mt_train_step": (C.c_int, [vp, vp, sz, fp]),
+        "mt_train_step_device_tokens": (C.c_int, [vp, vp, sz, fp]),
+        "mt_get_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
+        "mt_get_step_stats": (C.c_int, [vp, C.POINTER(MtStepStats)]),
+        "mt_get_step": (i64, [vp]),
+        "mt_set_step": (C.c_int, [vp, i64]),
+        "mt_last_error": (C.c_char_p, [vp]),
+        "mt_free": (None, [vp]),
+        "mt_adam_host": (C.c_int, [vp, vp, vp, vp, sz, i64, f32, f32, f32, f32, f32]),
+        "mt_op_last_error": (C.c_char_p, []),
+        "mt_op_gemm": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, vp, i64, vp, i64, vp, i64,
+                                 vp, vp, i32, i32, i32, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name, None)
+        if f is None:
+            continue
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def declared_symbols():
+    """Every function name declared in include/*.h (parsed from the headers)."""
+    import re
+    inc = os.path.join(os.path.dirname(HERE), "include")
+    names = []
+    for fn in sorted(os.listdir(inc)):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(inc, fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"\b(mt_\w+)\s*\(", txt)
+    return sorted(set(names))

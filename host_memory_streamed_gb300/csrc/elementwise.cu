@@ -1,0 +1,473 @@
+// HBM-bound kernels of the decoder step: RMSNorm forward/backward, SwiGLU
+// backward, transposes, embedding gather / deterministic scatter, row-wise
+// cross-entropy, reductions.  128-bit (8 x BF16) vectorised, coalesced access;
+// FP32 arithmetic; every reduction runs in a fixed order so results are
+// bit-reproducible run to run.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mt {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& w, float* f) {
+  f[0] = __uint_as_float(w.x << 16);
+  f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(w.y << 16);
+  f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(w.z << 16);
+  f[5] = __uint_as_float(w.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(w.w << 16);
+  f[7] = __uint_as_float(w.w & 0xFFFF0000u);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum with a fixed reduction tree (deterministic).
+template <int THREADS>
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (w == 0) {
+    t = l < THREADS / 32 ? red[l] : 0.f;
+    t = warp_sum(t);
+    if (l == 0) red[0] = t;
+  }
+  __syncthreads();
+  t = red[0];
+  __syncthreads();
+  return t;
+}
+
+// ---------------------------------------------------------------- RMSNorm
+// One block per row; d % 8 == 0; each thread owns d/8/THREADS (ceil) vectors.
+constexpr int RMS_THREADS = 256;
+
+__global__ void __launch_bounds__(RMS_THREADS) rmsnorm_fwd_kernel(const bf16* __restrict__ x, const bf16* __restrict__ g,
+                                                              bf16* __restrict__ y, float* __restrict__ rstd, int d,
+                                                              float eps) {
+  __shared__ float red[32];
+  const long row = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * d);
+  const int nv = d / 8;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < nv; i += RMS_THREADS) {
+    float f[8];
+    unpack8(xr[i], f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+  }
+  ss = block_sum<RMS_THREADS>(ss, red);
+  const float r = rsqrtf(ss / (float)d + eps);
+  if (threadIdx.x == 0) rstd[row] = r;
+  for (int i = threadIdx.x; i < nv; i += RMS_THREADS) {
+    float f[8], w[8];
+    unpack8(xr[i], f);
+    unpack8(gr[i], w);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = f[j] * r * w[j];
+    yr[i] = pack8(f);
+  }
+}
+
+// Backward: one block handles kRmsRowsPerBlock rows; per-column dg partials of
+// the block go to dg_partial[blockIdx.x, :] (summed later in fixed order).
+__global__ void __launch_bounds__(RMS_THREADS) rmsnorm_bwd_kernel(const bf16* __restrict__ dy,
+                                                              const bf16* __restrict__ x, const bf16* __restrict__ g,
+                                                              const float* __restrict__ rstd,
+                                                              const bf16* __restrict__ dres, bf16* __restrict__ dx,
+                                                              float* __restrict__ dg_partial, long rows, int d) {
+  __shared__ float red[32];
+  extern __shared__ float dg_acc[];  // d floats
+  const int nv = d / 8;
+  for (int c = threadIdx.x; c < d; c += RMS_THREADS) dg_acc[c] = 0.f;
+  __syncthreads();
+  const long r0 = (long)blockIdx.x * kRmsRowsPerBlock;
+  const long r1 = min(rows, r0 + kRmsRowsPerBlock);
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  for (long row = r0; row < r1; ++row) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
+    const uint4* dyr = reinterpret_cast<const uint4*>(dy + row * d);
+    const float r = rstd[row];
+    float dot = 0.f;
+    for (int i = threadIdx.x; i < nv; i += RMS_THREADS) {
+      float xf[8], df[8], wf[8];
+      unpack8(xr[i], xf);
+      unpack8(dyr[i], df);
+      unpack8(gr[i], wf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float xh = xf[j] * r;
+        dot += df[j] * wf[j] * xh;
+        dg_acc[i * 8 + j] += df[j] * xh;  // each column owned by one thread: no race
+      }
+    }
+    dot = block_sum<RMS_THREADS>(dot, red) / (float)d;
+    uint4* dxr = reinterpret_cast<uint4*>(dx + row * d);
+    const uint4* rr = dres ? reinterpret_cast<const uint4*>(dres + row * d) : nullptr;
+    for (int i = threadIdx.x; i < nv; i += RMS_THREADS) {
+      float xf[8], df[8], wf[8], out[8];
+      unpack8(xr[i], xf);
+      unpack8(dyr[i], df);
+      unpack8(gr[i], wf);
+      float rf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (rr) unpack8(rr[i], rf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) out[j] = rf[j] + r * (df[j] * wf[j] - xf[j] * r * dot);
+      dxr[i] = pack8(out);
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < d; c += RMS_THREADS) dg_partial[(long)blockIdx.x * d + c] = dg_acc[c];
+}
+
+// out[c] = sum_p partial[p, c], p ascending; one thread per column.
+__global__ void colsum_bf16_kernel(const float* __restrict__ partial, long nparts, int d, bf16* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= d) return;
+  float s = 0.f;
+  for (long p = 0; p < nparts; ++p) s += partial[p * d + c];
+  out[c] = __float2bfloat16_rn(s);
+}
+
+// ---------------------------------------------------------------- SwiGLU backward
+// gu: [rows, 2f] with (gate, up) interleaved; da: [rows, f]; dgu like gu.
+__global__ void swiglu_bwd_kernel(const bf16* __restrict__ da, const bf16* __restrict__ gu, bf16* __restrict__ dgu,
+                                  long rows, int f) {
+  // one thread per 8 outputs of `da` (16 interleaved values)
+  const long nvec_row = f / 8;
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows * nvec_row) return;
+  const long row = i / nvec_row, v = i % nvec_row;
+  float a8[8], g16[16];
+  unpack8(reinterpret_cast<const uint4*>(da + row * f)[v], a8);
+  const uint4* gp = reinterpret_cast<const uint4*>(gu + row * 2L * f) + 2 * v;
+  unpack8(gp[0], g16);
+  unpack8(gp[1], g16 + 8);
+  float out[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float gt = g16[2 * j], up = g16[2 * j + 1];
+    const float sg = 1.0f / (1.0f + __expf(-gt));
+    const float silu = gt * sg;
+    out[2 * j] = a8[j] * up * sg * (1.0f + gt * (1.0f - sg));
+    out[2 * j + 1] = a8[j] * silu;
+  }
+  uint4* dp = reinterpret_cast<uint4*>(dgu + row * 2L * f) + 2 * v;
+  dp[0] = pack8(out);
+  dp[1] = pack8(out + 8);
+}
+
+// Scalar tail for f % 8 != 0 columns (used when f is not a multiple of 8).
+__global__ void swiglu_bwd_scalar_kernel(const bf16* __restrict__ da, const bf16* __restrict__ gu,
+                                         bf16* __restrict__ dgu, long rows, int f) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows * f) return;
+  const long row = i / f, j = i % f;
+  const float a = __bfloat162float(da[row * f + j]);
+  const float gt = __bfloat162float(gu[row * 2L * f + 2 * j]);
+  const float up = __bfloat162float(gu[row * 2L * f + 2 * j + 1]);
+  const float sg = 1.0f / (1.0f + __expf(-gt));
+  dgu[row * 2L * f + 2 * j] = __float2bfloat16_rn(a * up * sg * (1.0f + gt * (1.0f - sg)));
+  dgu[row * 2L * f + 2 * j + 1] = __float2bfloat16_rn(a * gt * sg);
+}
+
+// ---------------------------------------------------------------- transpose
+// 64 x 64 tiles through shared memory; 256 threads; 16-byte loads/stores when
+// the tile is interior and aligned, element-wise at the edges.
+constexpr int TP = 64;
+__global__ void __launch_bounds__(256) transpose_kernel(const bf16* __restrict__ src, long rows, long cols, long lds,
+                                                        bf16* __restrict__ dst, long ldd) {
+  __shared__ bf16 tile[TP][TP + 8];
+  const long r0 = (long)blockIdx.y * TP, c0 = (long)blockIdx.x * TP;
+  const bool interior = (r0 + TP <= rows) && (c0 + TP <= cols) && (lds % 8 == 0) && (ldd % 8 == 0);
+  if (interior) {
+    for (int i = threadIdx.x; i < TP * TP / 8; i += 256) {
+      const int r = i / (TP / 8), cv = i % (TP / 8);
+      const uint4 w = *reinterpret_cast<const uint4*>(src + (r0 + r) * lds + c0 + cv * 8);
+      const bf16* e = reinterpret_cast<const bf16*>(&w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[r][cv * 8 + j] = e[j];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < TP * TP / 8; i += 256) {
+      const int c = i / (TP / 8), rv = i % (TP / 8);
+      uint4 w;
+      bf16* e = reinterpret_cast<bf16*>(&w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = tile[rv * 8 + j][c];
+      *reinterpret_cast<uint4*>(dst + (c0 + c) * ldd + r0 + rv * 8) = w;
+    }
+  } else {
+    for (int i = threadIdx.x; i < TP * TP; i += 256) {
+      const int r = i / TP, c = i % TP;
+      if (r0 + r < rows && c0 + c < cols) tile[r][c] = src[(r0 + r) * lds + c0 + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < TP * TP; i += 256) {
+      const int c = i / TP, r = i % TP;
+      if (r0 + r < rows && c0 + c < cols) dst[(c0 + c) * ldd + r0 + r] = tile[r][c];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- embedding
+__global__ void embed_fwd_kernel(const int32_t* __restrict__ tok, const bf16* __restrict__ E, bf16* __restrict__ x,
+                                 long T, int d, int V, int* status) {
+  const long t = blockIdx.x;
+  const int id = tok[t];
+  const bool ok = id >= 0 && id < V;
+  if (!ok && threadIdx.x == 0) set_status(status, kStatusIndexOutOfRange);
+  const uint4* src = reinterpret_cast<const uint4*>(E + (long)(ok ? id : 0) * d);
+  uint4* dst = reinterpret_cast<uint4*>(x + t * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
+}
+
+// dE[v] = sum of dx rows listed for v (ascending positions), written for every v.
+__global__ void embed_bwd_kernel(const int32_t* __restrict__ off, const int32_t* __restrict__ pos,
+                                 const bf16* __restrict__ dx, bf16* __restrict__ dE, int V, int d) {
+  const long v = blockIdx.x;
+  const int b = off[v], e = off[v + 1];
+  uint4* out = reinterpret_cast<uint4*>(dE + v * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int k = b; k < e; ++k) {
+      float f[8];
+      unpack8(reinterpret_cast<const uint4*>(dx + (long)pos[k] * d)[i], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += f[j];
+    }
+    out[i] = pack8(acc);
+  }
+}
+
+// ---------------------------------------------------------------- cross-entropy
+constexpr int CE_THREADS = 512;
+// One block per row.  Pass 1: per-thread online (max, sum) over a strided
+// slice, combined in a fixed tree; pass 2: dz = (exp(z - lse) - onehot) * inv_n.
+__global__ void __launch_bounds__(CE_THREADS) cross_entropy_kernel(const float* __restrict__ z, int V,
+                                                                   const int32_t* __restrict__ tgt, float inv_n,
+                                                                   bf16* __restrict__ dz, float* __restrict__ loss_rows,
+                                                                   int* status) {
+  __shared__ float sm[CE_THREADS / 32], ss[CE_THREADS / 32];
+  const long row = blockIdx.x;
+  const float* zr = z + row * (long)V;
+  float m = -FLT_MAX, s = 0.f;
+  const bool vec = (V % 4) == 0;
+  if (vec) {
+    const float4* z4 = reinterpret_cast<const float4*>(zr);
+    for (int i = threadIdx.x; i < V / 4; i += CE_THREADS) {
+      const float4 q = z4[i];
+      const float mx = fmaxf(fmaxf(q.x, q.y), fmaxf(q.z, q.w));
+      if (mx > m) {
+        s *= __expf(m - mx);
+        m = mx;
+      }
+      s += __expf(q.x - m) + __expf(q.y - m) + __expf(q.z - m) + __expf(q.w - m);
+    }
+  } else {
+    for (int i = threadIdx.x; i < V; i += CE_THREADS) {
+      const float q = zr[i];
+      if (q > m) {
+        s *= __expf(m - q);
+        m = q;
+      }
+      s += __expf(q - m);
+    }
+  }
+  // warp combine
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, m2);
+    s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
+    m = mm;
+  }
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  if (l == 0) {
+    sm[w] = m;
+    ss[w] = s;
+  }
+  __syncthreads();
+  if (w == 0) {
+    m = l < CE_THREADS / 32 ? sm[l] : -FLT_MAX;
+    s = l < CE_THREADS / 32 ? ss[l] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      const float mm = fmaxf(m, m2);
+      s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
+      m = mm;
+    }
+    if (l == 0) {
+      sm[0] = m;
+      ss[0] = s;
+    }
+  }
+  __syncthreads();
+  const float lse = sm[0] + __logf(ss[0]);
+  int y = tgt[row];
+  if (y < 0 || y >= V) {
+    if (threadIdx.x == 0) set_status(status, kStatusIndexOutOfRange);
+    y = 0;
+  }
+  if (threadIdx.x == 0) loss_rows[row] = lse - zr[y];
+  bf16* dr = dz + row * (long)V;
+  if (vec && (V % 8) == 0) {
+    const float4* z4 = reinterpret_cast<const float4*>(zr);
+    for (int i = threadIdx.x; i < V / 8; i += CE_THREADS) {
+      const float4 a = z4[2 * i], b = z4[2 * i + 1];
+      float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        f[j] = __expf(f[j] - lse);
+        if (i * 8 + j == y) f[j] -= 1.0f;
+        f[j] *= inv_n;
+      }
+      reinterpret_cast<uint4*>(dr)[i] = pack8(f);
+    }
+  } else {
+    for (int i = threadIdx.x; i < V; i += CE_THREADS) {
+      float p = __expf(zr[i] - lse);
+      if (i == y) p -= 1.0f;
+      dr[i] = __float2bfloat16_rn(p * inv_n);
+    }
+  }
+}
+
+constexpr int LOSS_THREADS = 1024;
+__global__ void __launch_bounds__(LOSS_THREADS) mean_loss_kernel(const float* __restrict__ loss_rows, long n,
+                                                                 float inv_n, float* out) {
+  __shared__ float red[32];
+  // FP64 would be nicer but is slow on this part; pairwise-ish fixed order in FP32 is plenty for a mean.
+  float s = 0.f;
+  for (long i = threadIdx.x; i < n; i += LOSS_THREADS) s += loss_rows[i];
+  s = block_sum<LOSS_THREADS>(s, red);
+  if (threadIdx.x == 0) out[0] = s * inv_n;
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst, long n) {
+  const long i = ((long)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (i + 8 <= n) {
+    const float4 a = reinterpret_cast<const float4*>(src + i)[0], b = reinterpret_cast<const float4*>(src + i)[1];
+    float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    *reinterpret_cast<uint4*>(dst + i) = pack8(f);
+  } else {
+    for (long j = i; j < n; ++j) dst[j] = __float2bfloat16_rn(src[j]);
+  }
+}
+
+__global__ void check_finite_kernel(const bf16* __restrict__ p, long n, int* status) {
+  long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  bool bad = false;
+  for (; i < n; i += (long)gridDim.x * blockDim.x) {
+    const unsigned short b = reinterpret_cast<const unsigned short*>(p)[i];
+    if ((b & 0x7F80u) == 0x7F80u) bad = true;  // exponent all ones: Inf or NaN
+  }
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x % 32) == 0) set_status(status, kStatusNonFinite);
+}
+
+inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
+
+}  // namespace
+
+void launch_rmsnorm_fwd(const bf16* x, const bf16* g, bf16* y, float* rstd, long rows, int d, float eps,
+                        cudaStream_t s) {
+  if (rows <= 0) return;
+  rmsnorm_fwd_kernel<<<(unsigned)rows, RMS_THREADS, 0, s>>>(x, g, y, rstd, d, eps);
+}
+
+void launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
+                        bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s) {
+  if (rows <= 0) return;
+  const unsigned nb = blocks_for(rows, kRmsRowsPerBlock);
+  const size_t shm = (size_t)d * sizeof(float);
+  if (shm > 48 * 1024) cudaFuncSetAttribute(rmsnorm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
+  rmsnorm_bwd_kernel<<<nb, RMS_THREADS, shm, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+}
+
+void launch_colsum_bf16(const float* partial, long nparts, int d, bf16* out, cudaStream_t s) {
+  colsum_bf16_kernel<<<blocks_for(d, 256), 256, 0, s>>>(partial, nparts, d, out);
+}
+
+void launch_swiglu_bwd(const bf16* da, const bf16* gu, bf16* dgu, long rows, int f, cudaStream_t s) {
+  if (rows <= 0) return;
+  if (f % 8 == 0) {
+    const long n = rows * (f / 8);
+    swiglu_bwd_kernel<<<blocks_for(n, 256), 256, 0, s>>>(da, gu, dgu, rows, f);
+  } else {
+    const long n = rows * (long)f;
+    swiglu_bwd_scalar_kernel<<<blocks_for(n, 256), 256, 0, s>>>(da, gu, dgu, rows, f);
+  }
+}
+
+void launch_transpose(const bf16* src, long rows, long cols, long lds, bf16* dst, long ldd, cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return;
+  dim3 grid(blocks_for(cols, TP), blocks_for(rows, TP));
+  transpose_kernel<<<grid, 256, 0, s>>>(src, rows, cols, lds, dst, ldd);
+}
+
+void launch_embed_fwd(const int32_t* tok, const bf16* E, bf16* x, long T, int d, int V, int* status,
+                      cudaStream_t s) {
+  if (T <= 0) return;
+  embed_fwd_kernel<<<(unsigned)T, 128, 0, s>>>(tok, E, x, T, d, V, status);
+}
+
+void launch_embed_bwd(const int32_t* off, const int32_t* pos, const bf16* dx, bf16* dE, int V, int d,
+                      cudaStream_t s) {
+  embed_bwd_kernel<<<(unsigned)V, 128, 0, s>>>(off, pos, dx, dE, V, d);
+}
+
+void launch_cross_entropy(const float* z, long rows, int V, const int32_t* tgt, float inv_n, bf16* dz,
+                          float* loss_rows, int* status, cudaStream_t s) {
+  if (rows <= 0) return;
+  cross_entropy_kernel<<<(unsigned)rows, CE_THREADS, 0, s>>>(z, V, tgt, inv_n, dz, loss_rows, status);
+}
+
+void launch_mean_loss(const float* loss_rows, long n, float inv_n, float* out, cudaStream_t s) {
+  mean_loss_kernel<<<1, LOSS_THREADS, 0, s>>>(loss_rows, n, inv_n, out);
+}
+
+void launch_f32_to_bf16(const float* src, bf16* dst, long n, cudaStream_t s) {
+  if (n <= 0) return;
+  f32_to_bf16_kernel<<<blocks_for((n + 7) / 8, 256), 256, 0, s>>>(src, dst, n);
+}
+
+void launch_zero(void* p, size_t bytes, cudaStream_t s) {
+  if (bytes) cudaMemsetAsync(p, 0, bytes, s);
+}
+
+void launch_check_finite(const bf16* p, long n, int* status, cudaStream_t s) {
+  if (n <= 0) return;
+  unsigned nb = blocks_for(n, 256);
+  if (nb > 152u * 16u) nb = 152u * 16u;
+  check_finite_kernel<<<nb, 256, 0, s>>>(p, n, status);
+}
+
+}  // namespace mt

@@ -1,0 +1,494 @@
+// BF16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+//   C[M, N] = epilogue( A[M, K] * B[N, K]^T )      (both operands K-major)
+//
+// This is the one dense contraction of the decoder step: the QKV, O, gate-up
+// and down projections in forward, their data and weight gradients in
+// backward, and the LM head (MegaTrain paper summary (paperlayer.ai), §A.4
+// "GPU Compute Dispatch": the layer templates hold the attention and MLP
+// kernels; the kernels themselves are this library's own design).
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: 128x64 A box + 256x64 B box per stage, 128-byte
+//               swizzle, STAGES-deep ring of shared-memory stages.
+//   warp 1      MMA issuer: one elected thread issues tcgen05.mma (M=128,
+//               N=256, K=16) into one of two TMEM accumulators (2 x 256 FP32
+//               columns), commits stage release and accumulator-ready.
+//   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread, fused
+//               epilogue (bf16 / fp32 store, residual add, SwiGLU on
+//               interleaved gate/up columns, rotate-half RoPE, fp32 +=),
+//               16-byte stores.  The second accumulator lets the epilogue of
+//               tile i overlap the main loop of tile i+1.
+// Every mbarrier wait is bounded (2 s); on expiry the kernel records
+// kStatusGemmTimeout in the status word and unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mt {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE = BN * BK * 2;  // 32 KB
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;  // two FP32 accumulators
+constexpr int GROUP_M = 16;        // tile raster: 16 M-tiles share each B panel
+constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+
+struct EpiParams {
+  int M, N, K;
+  int mode;
+  void* C;
+  long ldc;
+  const __nv_bfloat16* R;
+  long ldr;
+  __nv_bfloat16* C2;
+  long ldc2;
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_cols;
+  int head_dim;
+  int seq;
+  int* status;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& tm, int& tn) {
+  const int per_group = GROUP_M * num_n;
+  const int group = tile / per_group;
+  const int first_m = group * GROUP_M;
+  const int gsize = min(num_m - first_m, GROUP_M);
+  const int r = tile - group * per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Store 32 FP32 values as BF16 at dst[0..31] (dst 16-byte aligned) for the
+// columns that are < ncols_valid.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int ncols_valid) {
+  if (ncols_valid >= 32) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16(v[q * 8 + 0], v[q * 8 + 1]);
+      w.y = pack_bf16(v[q * 8 + 2], v[q * 8 + 3]);
+      w.z = pack_bf16(v[q * 8 + 4], v[q * 8 + 5]);
+      w.w = pack_bf16(v[q * 8 + 6], v[q * 8 + 7]);
+      d[q] = w;
+    }
+  } else {
+    for (int j = 0; j < ncols_valid; ++j) dst[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+__device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int col0, float* v) {
+  // `v` holds accumulator columns col0 .. col0+31 of output row `row`.
+  const int nvalid = min(32, p.N - col0);
+  if (row >= p.M || nvalid <= 0) return;
+  switch (p.mode) {
+    case kEpiStoreBf16: {
+      store_bf16x32(reinterpret_cast<__nv_bfloat16*>(p.C) + (long)row * p.ldc + col0, v, nvalid);
+      break;
+    }
+    case kEpiResidualBf16: {
+      const __nv_bfloat16* r = p.R + (long)row * p.ldr + col0;
+      if (nvalid >= 32) {
+        const uint4* r4 = reinterpret_cast<const uint4*>(r);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w = r4[q];
+          v[q * 8 + 0] += bf16_lo(w.x); v[q * 8 + 1] += bf16_hi(w.x);
+          v[q * 8 + 2] += bf16_lo(w.y); v[q * 8 + 3] += bf16_hi(w.y);
+          v[q * 8 + 4] += bf16_lo(w.z); v[q * 8 + 5] += bf16_hi(w.z);
+          v[q * 8 + 6] += bf16_lo(w.w); v[q * 8 + 7] += bf16_hi(w.w);
+        }
+      } else {
+        for (int j = 0; j < nvalid; ++j) v[j] += __bfloat162float(r[j]);
+      }
+      store_bf16x32(reinterpret_cast<__nv_bfloat16*>(p.C) + (long)row * p.ldc + col0, v, nvalid);
+      break;
+    }
+    case kEpiF32: {
+      float* c = reinterpret_cast<float*>(p.C) + (long)row * p.ldc + col0;
+      if (nvalid >= 32) {
+        float4* c4 = reinterpret_cast<float4*>(c);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c4[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+      } else {
+        for (int j = 0; j < nvalid; ++j) c[j] = v[j];
+      }
+      break;
+    }
+    case kEpiF32Accumulate: {
+      float* c = reinterpret_cast<float*>(p.C) + (long)row * p.ldc + col0;
+      if (nvalid >= 32) {
+        float4* c4 = reinterpret_cast<float4*>(c);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float4 o = c4[q];
+          c4[q] = make_float4(o.x + v[q * 4], o.y + v[q * 4 + 1], o.z + v[q * 4 + 2], o.w + v[q * 4 + 3]);
+        }
+      } else {
+        for (int j = 0; j < nvalid; ++j) c[j] += v[j];
+      }
+      break;
+    }
+    case kEpiSwiGLU: {
+      // Columns alternate gate, up: output a[row, col/2] = silu(gate) * up.
+      if (p.C2) store_bf16x32(p.C2 + (long)row * p.ldc2 + col0, v, nvalid);
+      float a[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float g = v[2 * j], u = v[2 * j + 1];
+        a[j] = g / (1.0f + __expf(-g)) * u;
+      }
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + (long)row * p.ldc + col0 / 2;
+      const int na = nvalid / 2;
+      if (na >= 16) {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint4 w;
+          w.x = pack_bf16(a[q * 8 + 0], a[q * 8 + 1]);
+          w.y = pack_bf16(a[q * 8 + 2], a[q * 8 + 3]);
+          w.z = pack_bf16(a[q * 8 + 4], a[q * 8 + 5]);
+          w.w = pack_bf16(a[q * 8 + 6], a[q * 8 + 7]);
+          d[q] = w;
+        }
+      } else {
+        for (int j = 0; j < na; ++j) dst[j] = __float2bfloat16_rn(a[j]);
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_bf16_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                             EpiParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int num_m = (p.M + BM - 1) / BM;
+  const int num_n = (p.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_k = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int pending[STAGES];
+      for (int s = 0; s < STAGES; ++s) pending[s] = -1;
+      for (int tile = blockIdx.x; tile < num_tiles && !abort_flag; tile += gridDim.x) {
+        int tm, tn;
+        tile_coords(tile, num_m, num_n, tm, tn);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            set_status(p.status, kStatusGemmTimeout);
+            abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], A_STAGE + B_STAGE);
+          tma_load_2d(sA + stage * A_STAGE, &tmap_a, kb * BK, tm * BM, &full[stage]);
+          tma_load_2d(sB + stage * B_STAGE, &tmap_b, kb * BK, tn * BN, &full[stage]);
+          pending[stage] = (int)phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain: a load issued into a stage the MMA warp never consumed (abort
+      // path) must still land before the CTA exits.
+      for (int s = 0; s < STAGES; ++s)
+        if (pending[s] >= 0 && !mbar_wait(&full[s], (uint32_t)pending[s])) set_status(p.status, kStatusGemmTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !abort_flag; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1)) {
+          set_status(p.status, kStatusGemmTimeout);
+          abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            set_status(p.status, kStatusGemmTimeout);
+            abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_kmajor_sw128(sA + stage * A_STAGE);
+          const uint64_t bdesc = smem_desc_kmajor_sw128(sB + stage * B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // advance 16 elements = 32 bytes along K inside the swizzle atom
+            tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
+                        (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+  } else {
+    // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31.
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      int tm, tn;
+      tile_coords(tile, num_m, num_n, tm, tn);
+      if (!mbar_wait(&tfull[acc], acc_phase)) {
+        set_status(p.status, kStatusGemmTimeout);
+        abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = tm * BM + row_in_tile;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (p.mode == kEpiRope && tn * BN < p.rope_cols) {
+        // rotate-half RoPE: columns j and j + hd/2 of each head form a pair.
+        const int hd = p.head_dim;
+        const int s = row % p.seq;
+        for (int h0 = 0; h0 < BN; h0 += hd) {
+          for (int j = 0; j < hd / 2; j += 32) {
+            uint32_t lo_r[32], hi_r[32];
+            tmem_ld_32x32b_x32(tbase + h0 + j, lo_r);
+            tmem_ld_32x32b_x32(tbase + h0 + hd / 2 + j, hi_r);
+            tmem_wait_ld();
+            float lo[32], hi[32];
+            const int gcol = tn * BN + h0 + j;
+            if (row < p.M && gcol < p.rope_cols) {
+              const float* cs = p.rope_cos + (long)s * (hd / 2) + j;
+              const float* sn = p.rope_sin + (long)s * (hd / 2) + j;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float x1 = __uint_as_float(lo_r[e]), x2 = __uint_as_float(hi_r[e]);
+                const float c = cs[e], si = sn[e];
+                lo[e] = x1 * c - x2 * si;
+                hi[e] = x2 * c + x1 * si;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                lo[e] = __uint_as_float(lo_r[e]);
+                hi[e] = __uint_as_float(hi_r[e]);
+              }
+            }
+            EpiParams q = p;
+            q.mode = kEpiStoreBf16;
+            epilogue_chunk(q, row, gcol, lo);
+            epilogue_chunk(q, row, gcol + hd / 2, hi);
+          }
+        }
+      } else {
+        EpiParams q = p;
+        if (q.mode == kEpiRope) q.mode = kEpiStoreBf16;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+          epilogue_chunk(q, row, tn * BN + c * 32, v);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major BF16 matrix [rows, cols] with leading dimension ld (elements),
+// boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill outside.
+bool make_tmap(CUtensorMap* m, const void* base, long rows, long cols, long ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+}  // namespace
+
+const char* gemm_check(const GemmArgs& g) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return "gemm: M, N and K must be positive";
+  if (g.K % 8) return "gemm: K must be a multiple of 8 (16-byte TMA rows)";
+  if (g.lda % 8 || g.ldb % 8) return "gemm: lda/ldb must be multiples of 8 elements";
+  if (g.lda < g.K || g.ldb < g.K) return "gemm: lda/ldb smaller than K";
+  if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.B)) & 15) return "gemm: A/B not 16-byte aligned";
+  if (!g.C) return "gemm: null output";
+  if (reinterpret_cast<uintptr_t>(g.C) & 15) return "gemm: C not 16-byte aligned";
+  if (g.ldc % 8) return "gemm: ldc must be a multiple of 8";
+  switch (g.epi) {
+    case kEpiStoreBf16:
+    case kEpiF32:
+    case kEpiF32Accumulate:
+      break;
+    case kEpiResidualBf16:
+      if (!g.R || (reinterpret_cast<uintptr_t>(g.R) & 15) || g.ldr % 8) return "gemm: bad residual operand";
+      break;
+    case kEpiSwiGLU:
+      if (g.N % 2) return "gemm: SwiGLU needs an even N";
+      if (g.C2 && ((reinterpret_cast<uintptr_t>(g.C2) & 15) || g.ldc2 % 8)) return "gemm: bad SwiGLU gu output";
+      break;
+    case kEpiRope:
+      if (!(g.head_dim == 64 || g.head_dim == 128)) return "gemm: RoPE head_dim must be 64 or 128";
+      if (g.rope_cols % g.head_dim) return "gemm: rope_cols must be a multiple of head_dim";
+      if (!g.rope_cos || !g.rope_sin || g.seq <= 0) return "gemm: RoPE tables missing";
+      break;
+    default:
+      return "gemm: unknown epilogue";
+  }
+  return nullptr;
+}
+
+int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+  if (gemm_check(g)) return -1;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
+      return -2;
+    attr_done = true;
+  }
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, g.A, g.M, g.K, g.lda, BM)) return -3;
+  if (!make_tmap(&tb, g.B, g.N, g.K, g.ldb, BN)) return -3;
+  EpiParams p;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.mode = g.epi;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.R = g.R;
+  p.ldr = g.ldr;
+  p.C2 = g.C2;
+  p.ldc2 = g.ldc2;
+  p.rope_cos = g.rope_cos;
+  p.rope_sin = g.rope_sin;
+  p.rope_cols = g.rope_cols;
+  p.head_dim = g.head_dim;
+  p.seq = g.seq;
+  p.status = g.status;
+  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  gemm_bf16_tcgen05_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace mt

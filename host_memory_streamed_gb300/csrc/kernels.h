@@ -1,0 +1,105 @@
+// Launch interfaces of the sm_103a kernels that make up one decoder layer's
+// forward, recompute and backward, plus the embedding and LM-head steps.
+// All tensors are row-major; BF16 unless stated; `rows` counts tokens.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mt {
+
+using bf16 = __nv_bfloat16;
+
+// ----------------------------------------------------------------- GEMM
+enum EpiMode : int {
+  kEpiStoreBf16 = 0,      // C(bf16) = acc
+  kEpiResidualBf16 = 1,   // C(bf16) = R + acc
+  kEpiF32 = 2,            // C(f32) = acc
+  kEpiF32Accumulate = 3,  // C(f32) += acc
+  kEpiSwiGLU = 4,         // columns (2j, 2j+1) = (gate, up): C[:, j] = silu(gate) * up; C2 = gu (optional)
+  kEpiRope = 5,           // C(bf16) = acc, rotate-half RoPE on columns < rope_cols
+};
+
+struct GemmArgs {
+  const bf16* A = nullptr;  // [M, K], leading dimension lda
+  long lda = 0;
+  const bf16* B = nullptr;  // [N, K], leading dimension ldb
+  long ldb = 0;
+  int M = 0, N = 0, K = 0;
+  int epi = kEpiStoreBf16;
+  void* C = nullptr;
+  long ldc = 0;
+  const bf16* R = nullptr;
+  long ldr = 0;
+  bf16* C2 = nullptr;
+  long ldc2 = 0;
+  const float* rope_cos = nullptr;  // [seq, head_dim/2]
+  const float* rope_sin = nullptr;
+  int rope_cols = 0;
+  int head_dim = 0;
+  int seq = 1;
+  int* status = nullptr;
+};
+
+// Returns a message when the arguments are unsupported, else nullptr.
+const char* gemm_check(const GemmArgs& g);
+// 0 on success; negative on a launch or descriptor error.
+int launch_gemm(const GemmArgs& g, cudaStream_t stream);
+
+// ----------------------------------------------------------------- attention
+struct AttnArgs {
+  const bf16* qkv = nullptr;  // [B*S, ldqkv]: q heads, then k heads, then v heads (head_dim each)
+  long ldqkv = 0;
+  int batch = 0, seq = 0, n_heads = 0, n_kv_heads = 0, head_dim = 0;
+  bf16* o = nullptr;  // [B*S, ldo], head h at column h*head_dim
+  long ldo = 0;
+  float* lse = nullptr;  // [B, n_heads, S] natural-log row sums of exp(scores)
+  // backward
+  const bf16* dout = nullptr;  // dO, layout of o
+  float* delta = nullptr;      // [B, n_heads, S] scratch: rowsum(dO * O)
+  bf16* dqkv = nullptr;        // gradient w.r.t. the rotated q, k and v, layout of qkv
+  // rotate-half RoPE tables [seq, head_dim/2]; when set, the backward applies
+  // the inverse rotation so dqkv holds gradients w.r.t. the unrotated q, k.
+  const float* rope_cos = nullptr;
+  const float* rope_sin = nullptr;
+  int* status = nullptr;
+};
+const char* attn_check(const AttnArgs& a);
+int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
+int launch_attn_bwd(const AttnArgs& a, cudaStream_t stream);
+
+// ----------------------------------------------------------------- elementwise
+// y = x * rsqrt(mean(x^2) + eps) * g ; rstd[r] saved for the backward.
+void launch_rmsnorm_fwd(const bf16* x, const bf16* g, bf16* y, float* rstd, long rows, int d, float eps,
+                        cudaStream_t s);
+// dx = dres + rstd * (dy*g - xhat * mean(dy*g*xhat)), xhat = x*rstd.
+// dg_partial[blk, d] = sum over the rows of block blk of dy * xhat
+// (blocks of kRmsRowsPerBlock rows); reduce with launch_colsum_bf16.
+constexpr int kRmsRowsPerBlock = 64;
+void launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
+                        bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s);
+// out[c] = bf16(sum_p partial[p, c]) in a fixed order.
+void launch_colsum_bf16(const float* partial, long nparts, int d, bf16* out, cudaStream_t s);
+// gu [rows, 2f] interleaved (gate, up); da [rows, f] -> dgu [rows, 2f] interleaved.
+void launch_swiglu_bwd(const bf16* da, const bf16* gu, bf16* dgu, long rows, int f, cudaStream_t s);
+// dst[c, r] = src[r, c]
+void launch_transpose(const bf16* src, long rows, long cols, long lds, bf16* dst, long ldd, cudaStream_t s);
+// x[t] = E[tok[t]]; out-of-range ids set status and produce zeros.
+void launch_embed_fwd(const int32_t* tok, const bf16* E, bf16* x, long T, int d, int V, int* status,
+                      cudaStream_t s);
+// dE[v] = sum over t in pos[off[v] .. off[v+1]) of dx[t] (ascending t), zeros elsewhere.
+void launch_embed_bwd(const int32_t* off, const int32_t* pos, const bf16* dx, bf16* dE, int V, int d,
+                      cudaStream_t s);
+// Row-wise cross-entropy on FP32 logits z [rows, V]:
+// loss_rows[r] = logsumexp(z_r) - z_r[tgt_r];  dz_r = (softmax(z_r) - onehot(tgt_r)) * inv_n  (bf16)
+void launch_cross_entropy(const float* z, long rows, int V, const int32_t* tgt, float inv_n, bf16* dz,
+                          float* loss_rows, int* status, cudaStream_t s);
+// out[0] = sum(loss_rows[0..n)) * inv_n, fixed-order reduction.
+void launch_mean_loss(const float* loss_rows, long n, float inv_n, float* out, cudaStream_t s);
+void launch_f32_to_bf16(const float* src, bf16* dst, long n, cudaStream_t s);
+void launch_zero(void* p, size_t bytes, cudaStream_t s);
+// status |= kStatusNonFinite when any of the n BF16 values is NaN or Inf.
+void launch_check_finite(const bf16* p, long n, int* status, cudaStream_t s);
+
+}  // namespace mt

@@ -1,0 +1,196 @@
+/*
+ * mt.h -- C-ABI of libmt.so: one layer-streamed decoder training step on one
+ * GPU with the host as the authoritative store (MegaTrain).
+ *
+ * Where each operation comes from (page titles of the MegaTrain sources):
+ *  - host memory holds all persistent state; the GPU is a transient compute
+ *    engine: paperlayer.ai summary "MegaTrain: Full Precision Training of
+ *    100B+ Parameter Large Language Models on a Single GPU", Abstract and §3
+ *    "Execution workflow";
+ *  - one contiguous 4 KB-aligned tile per layer holding BF16 weights, BF16
+ *    gradients and FP32 Adam moments (12 bytes/parameter): paperlayer.ai §2
+ *    "Training memory", §A.1 "Layer-Contiguous Tiling"; hyper.ai summary,
+ *    方法 (Method) ¶5;
+ *  - streaming through two device buffers on three CUDA streams ordered by
+ *    Weights-Ready / Buffer-Free / Grads-Done events, a CPU packer thread
+ *    filling pinned staging buffers, gradient slabs with a background
+ *    accumulator: paperlayer.ai §A.2, §A.3; hyper.ai 方法 ¶3-5;
+ *  - stateless layer templates bound to streamed buffers (Bind):
+ *    paperlayer.ai §A.4; hyper.ai 方法 ¶6;
+ *  - block checkpoints and recompute in backward: paperlayer.ai §3; hyper.ai
+ *    方法 ¶2; author's blog "How to Train 100B+ Large Models on a Single GPU",
+ *    the F/W/G block figure;
+ *  - Adam on CPU threads: paperlayer.ai §3 "Execution workflow", §A.
+ *
+ * Conventions
+ *  - Tiles: index 0 = embedding (E [V, d]), 1..L = decoder layers,
+ *    L+1 = head (final RMSNorm gain g_f [d], LM head W_h [V, d]).
+ *  - Each tile is one page-aligned host block with four sections in this
+ *    order: W (BF16), G (BF16), M (FP32), V (FP32); each section starts on a
+ *    4096-byte boundary.  Inside W (and identically inside G) the tensors of
+ *    the tile follow in the order given by mt_tile_info, each on a 256-byte
+ *    boundary.  M and V hold one FP32 per parameter in the same order and
+ *    offsets x2.
+ *  - Layer tile tensors: g1 [d], wqkv [(Hq+2Hkv)*hd, d] (rows: all q heads,
+ *    then k heads, then v heads), wo [d, Hq*hd], g2 [d], wgu [2f, d] whose row
+ *    2j is gate row j and row 2j+1 is up row j, wd [d, f].  Matrices are
+ *    nn.Linear [out, in], row-major.
+ *  - Tokens: int32 [B, S+1]; row b trains on inputs tokens[b, :S] and targets
+ *    tokens[b, 1:]; the loss is the mean over the B*S targets.
+ *
+ * Ownership: the caller owns every pointer it passes (config, tokens, src,
+ * dst, device arena, streams) and keeps the arena and streams alive until
+ * mt_free.  The library copies what it needs and keeps no caller pointer
+ * except the arena and the streams.  The library owns the host tiles, the
+ * pinned staging buffers, the gradient slabs, its events and its threads.
+ *
+ * Errors: every call returns 0 (MT_OK) or a negative MT_E* code; the text is
+ * in mt_last_error(handle) (or mt_last_error(NULL) for failures before a
+ * handle exists).  No C++ exception crosses this boundary.  After MT_ECUDA or
+ * MT_EINTERNAL the handle accepts only mt_get_layer_tile, mt_last_error and
+ * mt_free.
+ */
+#ifndef MT_H
+#define MT_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MT_OK = 0,
+  MT_EINVAL = -1,      /* bad config, size, tile index or argument */
+  MT_ENOMEM = -2,      /* host allocation / pinning failed, or the arena is too small */
+  MT_ECUDA = -3,       /* a CUDA call failed */
+  MT_ETIMEDOUT = -4,   /* a bounded wait (host event poll or device mbarrier) expired */
+  MT_ESTATE = -5,      /* call not allowed in the handle's state */
+  MT_ENONFINITE = -6,  /* the loss or a gradient is NaN/Inf; the step's update was not applied */
+  MT_EINTERNAL = -7    /* a worker thread failed */
+};
+
+/* mt_config.flags */
+enum {
+  MT_RESIDENT = 1u << 0,          /* upload every tile's W once; no streaming (test path) */
+  MT_STORE_ACTS = 1u << 1,        /* keep every layer's internals from forward; no recompute (test path) */
+  MT_NO_DOUBLE_BUFFER = 1u << 2,  /* one device weight buffer: no H2D/compute overlap (ablation) */
+  MT_DEBUG_CHECKS = 1u << 3,      /* NaN/Inf scan of every gradient tile; host event-order asserts */
+  MT_TIME_KERNELS = 1u << 4       /* CUDA-event timing of every GEMM launch (mt_get_step_stats) */
+};
+
+/* Tile parts for load/get. */
+enum { MT_PART_W = 0, MT_PART_G = 1, MT_PART_M = 2, MT_PART_V = 3 };
+
+typedef struct {
+  int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rms_eps, rope_theta; /* 1e-5, 1e4 */
+  int32_t batch, seq;        /* tokens per step = batch * seq */
+  int32_t ckpt_every;        /* K: keep the input of every K-th layer; recompute inside blocks of K */
+  float lr, beta1, beta2, adam_eps, weight_decay;
+  int32_t n_adam_threads;    /* CPU Adam workers (0 = hardware threads) */
+  int32_t n_pack_threads;    /* CPU threads copying pageable tiles into pinned staging (0 = 4) */
+  int32_t n_grad_slabs;      /* pinned gradient slabs (0 = 12) */
+  int64_t grad_slab_bytes;   /* bytes per gradient slab (0 = 64 MiB) */
+  int64_t stage_bytes;       /* bytes per pinned H2D staging chunk (0 = 64 MiB); two chunks ping-pong */
+  int64_t timeout_ms;        /* bound of every host wait (0 = 60000) */
+  uint32_t flags;
+} mt_config;
+
+typedef struct mt_model mt_model;
+
+typedef struct {
+  char name[16];
+  int32_t ndim;
+  int64_t shape[2];
+  int64_t offset; /* byte offset inside the W (or G) section */
+  int64_t numel;
+} mt_tensor_desc;
+
+typedef struct {
+  int32_t kind;      /* 0 embed, 1 layer, 2 head */
+  int32_t n_tensors;
+  int64_t n_params;
+  int64_t w_bytes;   /* bytes of the W section (== G section); M, V sections are 2x */
+  int64_t tile_bytes;/* whole host tile */
+  mt_tensor_desc tensors[8];
+} mt_tile_desc;
+
+typedef struct {
+  double loss;
+  double step_ms;          /* host wall time of mt_train_step */
+  double gpu_compute_ms;   /* compute-stream time between the first and last event of the step */
+  double h2d_ms, d2h_ms;   /* summed copy time on the H2D / D2H streams (events) */
+  double wait_weights_ms;  /* compute-stream time spent waiting for Weights-Ready */
+  double adam_ms;          /* summed wall time of Adam tasks (all workers) */
+  double adam_tail_ms;     /* wall time from the last Grads-Done to the end of Adam */
+  double gemm_ms;          /* summed GEMM kernel time (MT_TIME_KERNELS) */
+  double gemm_flops;       /* FLOPs of those GEMM launches */
+  int64_t gemm_launches;
+  int64_t kernel_launches; /* kernels launched by the step */
+  int64_t h2d_bytes, d2h_bytes;
+  int64_t flops_executed;  /* all matmul FLOPs the step ran, recompute included */
+  int64_t flops_model;     /* 6 * N_linear * T + causal-attention FLOPs (3x forward) */
+  int64_t arena_high_water;
+  int64_t step;            /* Adam step counter after this step */
+} mt_step_stats;
+
+/* Device bytes the handle needs in its arena for this config (>0), or a negative MT_E* code. */
+int64_t mt_required_device_bytes(const mt_config* cfg);
+
+/*
+ * Create a handle.  device_arena: a device allocation of at least
+ * mt_required_device_bytes(cfg) bytes, 256-byte aligned; stream_*:
+ * cudaStream_t values (compute, host-to-device, device-to-host), distinct and
+ * non-blocking w.r.t. each other.  Allocates the host tiles (zeroed), the
+ * pinned staging buffers and gradient slabs, starts the worker threads.
+ * Every tile's W must be loaded (mt_load_layer_tile, part W) before the
+ * first mt_train_step.
+ */
+int mt_init_model(const mt_config* cfg, void* device_arena, size_t arena_bytes, void* stream_comp,
+                  void* stream_h2d, void* stream_d2h, mt_model** out);
+
+int mt_tile_count(const mt_model* m);                                /* L + 2 */
+int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out);
+
+/*
+ * Copy nbytes from host memory `src` into part `part` of tile `tile`;
+ * nbytes must equal the part's size (w_bytes for W and G, 2*w_bytes for M
+ * and V) in the tile's internal layout (see Conventions).
+ */
+int mt_load_layer_tile(mt_model* m, int tile, int part, const void* src, size_t nbytes);
+
+/*
+ * One synchronous training step: forward, backward with block recompute,
+ * gradient evacuation, and Adam on every tile.  tokens: host int32
+ * [batch, seq+1] (n_tokens = batch*(seq+1)); or, with tokens_on_device = 1,
+ * a device pointer to the same array.  On success *loss_out holds the mean
+ * cross-entropy of the step (computed before the update).
+ */
+int mt_train_step(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out);
+int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n_tokens, float* loss_out);
+
+/* Copy part `part` of tile `tile` into host memory `dst` (nbytes as in load). */
+int mt_get_layer_tile(mt_model* m, int tile, int part, void* dst, size_t nbytes);
+
+int mt_get_step_stats(const mt_model* m, mt_step_stats* out);
+int64_t mt_get_step(const mt_model* m);       /* Adam step counter t (0 before the first step) */
+int mt_set_step(mt_model* m, int64_t step);  /* for resume */
+const char* mt_last_error(const mt_model* m);
+void mt_free(mt_model* m);
+
+/*
+ * Host-only Adam on one tile-shaped range (used by the step's CPU workers;
+ * exported for checking against the oracle without a GPU).
+ * w, g: BF16 bit patterns (uint16); m, v: FP32; n elements; t >= 1.
+ * m <- b1 m + (1-b1) g; v <- b2 v + (1-b2) g^2;
+ * w <- bf16_rne(w - lr (m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps) - lr wd w),
+ * arithmetic in FP32.
+ */
+int mt_adam_host(uint16_t* w, const uint16_t* g, float* m, float* v, size_t n, int64_t t, float lr, float beta1,
+                 float beta2, float eps, float weight_decay);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
