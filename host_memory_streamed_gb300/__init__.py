@@ -1,0 +1,229 @@
+"""GB300-native layer-streamed decoder training step (MegaTrain's hot path).
+
+Thin Python binding over ``libmt.so`` (C-ABI in ``include/mt.h`` and
+``include/mt_ops.h``): argument marshalling only.  Every step of the training
+path runs in the library's CUDA kernels and C++ runtime; PyTorch provides the
+device arena and the three CUDA streams.  There is no CPU fallback: if the
+library is missing or no GPU is present, constructing a model raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib
+from ._lib import (MT_DEBUG_CHECKS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V, MT_PART_W,
+                   MT_RESIDENT, MT_STORE_ACTS, MT_TIME_KERNELS, ERROR_NAMES)
+
+__all__ = ["StreamedDecoder", "MtError", "ops", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
+           "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_PART_W", "MT_PART_G", "MT_PART_M", "MT_PART_V"]
+
+LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
+
+
+class MtError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _bf16_bytes(t: torch.Tensor) -> torch.Tensor:
+    return t.contiguous().view(torch.uint8).reshape(-1)
+
+
+class StreamedDecoder:
+    """One model handle: host tiles, device arena, three streams, worker threads."""
+
+    def __init__(self, n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, batch, seq, *,
+                 ckpt_every=1, rms_eps=1e-5, rope_theta=1e4, lr=1e-4, beta1=0.9, beta2=0.95, adam_eps=1e-8,
+                 weight_decay=0.0, n_adam_threads=0, n_pack_threads=0, n_grad_slabs=0, grad_slab_bytes=0,
+                 stage_bytes=0, timeout_ms=0, flags=0, device=None):
+        if not torch.cuda.is_available():
+            raise RuntimeError("a CUDA device is required (the library has no CPU path)")
+        self._L = _lib.lib()
+        cfg = _lib.MtConfig()
+        for k, v in dict(n_layers=n_layers, d_model=d_model, n_heads=n_heads, n_kv_heads=n_kv_heads,
+                         head_dim=head_dim, ffn=ffn, vocab=vocab, rms_eps=rms_eps, rope_theta=rope_theta,
+                         batch=batch, seq=seq, ckpt_every=ckpt_every, lr=lr, beta1=beta1, beta2=beta2,
+                         adam_eps=adam_eps, weight_decay=weight_decay, n_adam_threads=n_adam_threads,
+                         n_pack_threads=n_pack_threads, n_grad_slabs=n_grad_slabs,
+                         grad_slab_bytes=grad_slab_bytes, stage_bytes=stage_bytes, timeout_ms=timeout_ms,
+                         flags=flags).items():
+            setattr(cfg, k, v)
+        self.cfg = cfg
+        self.device = torch.device(device or "cuda")
+        need = self._L.mt_required_device_bytes(C.byref(cfg))
+        if need < 0:
+            raise MtError(need, self._L.mt_last_error(None).decode())
+        self.arena_bytes = int(need)
+        self.arena = torch.empty(self.arena_bytes, dtype=torch.uint8, device=self.device)
+        self.streams = [torch.cuda.Stream(self.device) for _ in range(3)]
+        h = C.c_void_p()
+        rc = self._L.mt_init_model(C.byref(cfg), self.arena.data_ptr(), self.arena_bytes,
+                                   *(s.cuda_stream for s in self.streams), C.byref(h))
+        if rc != 0:
+            raise MtError(rc, self._L.mt_last_error(None).decode())
+        self._h = h
+        self.n_tiles = self._L.mt_tile_count(h)
+        self.infos = [self.tile_info(i) for i in range(self.n_tiles)]
+
+    @classmethod
+    def from_shape(cls, s, **kw):
+        return cls(s.n_layers, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.ffn, s.vocab, s.batch, s.seq,
+                   ckpt_every=s.ckpt_every, rms_eps=s.rms_eps, rope_theta=s.rope_theta, lr=s.lr, beta1=s.beta1,
+                   beta2=s.beta2, adam_eps=s.adam_eps, weight_decay=s.weight_decay, **kw)
+
+    # ------------------------------------------------------------------ plumbing
+    def _check(self, rc):
+        if rc != 0:
+            raise MtError(rc, self._L.mt_last_error(self._h).decode())
+
+    def close(self):
+        if getattr(self, "_h", None):
+            for s in self.streams:
+                s.synchronize()
+            self._L.mt_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def tile_info(self, i):
+        d = _lib.MtTileDesc()
+        self._check(self._L.mt_tile_info(self._h, i, C.byref(d)))
+        tensors = {}
+        for k in range(d.n_tensors):
+            t = d.tensors[k]
+            shape = (t.shape[0], t.shape[1]) if t.ndim == 2 else (t.shape[0],)
+            tensors[t.name.decode()] = dict(shape=shape, offset=t.offset, numel=t.numel)
+        return dict(kind=d.kind, n_params=d.n_params, w_bytes=d.w_bytes, tile_bytes=d.tile_bytes, tensors=tensors)
+
+    def _part_bytes(self, i, part):
+        w = self.infos[i]["w_bytes"]
+        return w if part in (MT_PART_W, MT_PART_G) else 2 * w
+
+    def load_tile(self, i, part, buf: torch.Tensor):
+        buf = buf.contiguous()
+        assert buf.device.type == "cpu" and buf.numel() * buf.element_size() == self._part_bytes(i, part)
+        self._check(self._L.mt_load_layer_tile(self._h, i, part, buf.data_ptr(), self._part_bytes(i, part)))
+
+    def get_tile(self, i, part) -> torch.Tensor:
+        out = torch.empty(self._part_bytes(i, part), dtype=torch.uint8)
+        self._check(self._L.mt_get_layer_tile(self._h, i, part, out.data_ptr(), out.numel()))
+        return out
+
+    # ------------------------------------------------------------------ named <-> tile layout
+    def _named_to_slots(self, i, named):
+        kind = self.infos[i]["kind"]
+        if kind == 0:
+            return {"E": named["E"]}
+        if kind == 2:
+            return {"gf": named["gf"], "wh": named["wh"]}
+        wgu = torch.stack([named["wg"], named["wu"]], dim=1).reshape(-1, named["wg"].shape[1])
+        return {"g1": named["g1"], "wqkv": torch.cat([named["wq"], named["wk"], named["wv"]], 0),
+                "wo": named["wo"], "g2": named["g2"], "wgu": wgu, "wd": named["wd"]}
+
+    def _slots_to_named(self, i, slots):
+        kind = self.infos[i]["kind"]
+        if kind != 1:
+            return slots
+        c = self.cfg
+        q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
+        wqkv, wgu = slots["wqkv"], slots["wgu"]
+        return {"g1": slots["g1"], "wq": wqkv[:q], "wk": wqkv[q:q + kv], "wv": wqkv[q + kv:],
+                "wo": slots["wo"], "g2": slots["g2"], "wg": wgu[0::2], "wu": wgu[1::2], "wd": slots["wd"]}
+
+    def pack(self, i, named, dtype=torch.bfloat16) -> torch.Tensor:
+        """Named tensors of tile i -> the tile section bytes (W/G for BF16, M/V for FP32)."""
+        slots = self._named_to_slots(i, named)
+        esz = 2 if dtype == torch.bfloat16 else 4
+        out = torch.zeros(self.infos[i]["w_bytes"] * esz // 2, dtype=torch.uint8)
+        for name, meta in self.infos[i]["tensors"].items():
+            t = slots[name].to(dtype).contiguous().reshape(-1)
+            assert t.numel() == meta["numel"], (name, t.numel(), meta["numel"])
+            o = meta["offset"] * esz // 2
+            out[o:o + meta["numel"] * esz] = t.view(torch.uint8)
+        return out
+
+    def unpack(self, i, raw: torch.Tensor, dtype=torch.bfloat16):
+        esz = 2 if dtype == torch.bfloat16 else 4
+        slots = {}
+        for name, meta in self.infos[i]["tensors"].items():
+            o = meta["offset"] * esz // 2
+            slots[name] = raw[o:o + meta["numel"] * esz].view(dtype).reshape(meta["shape"]).clone()
+        return self._slots_to_named(i, slots)
+
+    def _tile_named(self, params, i):
+        if i == 0:
+            return params["embed"]
+        if i == self.n_tiles - 1:
+            return params["head"]
+        return params["layers"][i - 1]
+
+    def load_weights(self, params):
+        """params: {'embed': {'E'}, 'layers': [{g1,wq,...}], 'head': {'gf','wh'}} of BF16 tensors."""
+        for i in range(self.n_tiles):
+            self.load_tile(i, MT_PART_W, self.pack(i, self._tile_named(params, i)))
+
+    def _collect(self, part, dtype):
+        out = {"embed": None, "layers": [], "head": None}
+        for i in range(self.n_tiles):
+            named = self.unpack(i, self.get_tile(i, part), dtype)
+            if i == 0:
+                out["embed"] = named
+            elif i == self.n_tiles - 1:
+                out["head"] = named
+            else:
+                out["layers"].append(named)
+        return out
+
+    def weights(self):
+        return self._collect(MT_PART_W, torch.bfloat16)
+
+    def grads(self):
+        return self._collect(MT_PART_G, torch.bfloat16)
+
+    def moments(self):
+        return self._collect(MT_PART_M, torch.float32), self._collect(MT_PART_V, torch.float32)
+
+    # ------------------------------------------------------------------ the step
+    def train_step(self, tokens: torch.Tensor) -> float:
+        """tokens: int32 [B, S+1] on the host (or on the GPU). Returns the loss."""
+        loss = C.c_float()
+        tok = tokens.to(torch.int32).contiguous()
+        if tok.is_cuda:
+            rc = self._L.mt_train_step_device_tokens(self._h, tok.data_ptr(), tok.numel(), C.byref(loss))
+        else:
+            rc = self._L.mt_train_step(self._h, tok.data_ptr(), tok.numel(), C.byref(loss))
+        self._check(rc)
+        return loss.value
+
+    def stats(self) -> dict:
+        st = _lib.MtStepStats()
+        self._check(self._L.mt_get_step_stats(self._h, C.byref(st)))
+        return {k: getattr(st, k) for k, _ in st._fields_}
+
+    @property
+    def step(self) -> int:
+        return int(self._L.mt_get_step(self._h))
+
+    @step.setter
+    def step(self, v):
+        self._check(self._L.mt_set_step(self._h, int(v)))
+
+
+def adam_host(w_bits: torch.Tensor, g_bits: torch.Tensor, m: torch.Tensor, v: torch.Tensor, t: int, lr: float,
+              beta1: float, beta2: float, eps: float, weight_decay: float = 0.0):
+    """The library's CPU Adam (in place) on BF16 w/g (as int16 bit views) and FP32 m/v."""
+    L = _lib.lib()
+    rc = L.mt_adam_host(w_bits.data_ptr(), g_bits.data_ptr(), m.data_ptr(), v.data_ptr(), w_bits.numel(), t,
+                        lr, beta1, beta2, eps, weight_decay)
+    if rc != 0:
+        raise MtError(rc, "mt_adam_host rejected its arguments")
+
+
+from . import ops  # noqa: E402

@@ -86,6 +86,16 @@ def lib():
         "mt_op_last_error": (C.c_char_p, []),
         "mt_op_gemm": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, vp, i64, vp, i64, vp, i64,
                                  vp, vp, i32, i32, i32, vp, vp]),
+        "mt_op_attention_fwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp]),
+        "mt_op_attention_bwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp]),
+        "mt_op_rmsnorm_fwd": (C.c_int, [vp, vp, vp, vp, i64, i32, f32, vp]),
+        "mt_op_rmsnorm_bwd_scratch_floats": (i64, [i64, i32]),
+        "mt_op_rmsnorm_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp]),
+        "mt_op_swiglu_bwd": (C.c_int, [vp, vp, vp, i64, i32, vp]),
+        "mt_op_transpose": (C.c_int, [vp, i64, i64, i64, vp, i64, vp]),
+        "mt_op_cross_entropy": (C.c_int, [vp, i64, i32, vp, f32, vp, vp, vp, vp]),
+        "mt_op_embedding_fwd": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp]),
+        "mt_op_embedding_bwd": (C.c_int, [vp, vp, vp, vp, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name, None)

@@ -11,6 +11,15 @@ namespace mt {
 
 using bf16 = __nv_bfloat16;
 
+// Device status word codes (the first error sticks: written with atomicCAS).
+enum : int {
+  kStatusOk = 0,
+  kStatusGemmTimeout = 1,
+  kStatusAttnBadShape = 2,
+  kStatusIndexOutOfRange = 3,
+  kStatusNonFinite = 4,
+};
+
 // ----------------------------------------------------------------- GEMM
 enum EpiMode : int {
   kEpiStoreBf16 = 0,      // C(bf16) = acc

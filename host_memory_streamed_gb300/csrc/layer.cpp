@@ -1,0 +1,284 @@
+// Tile layouts and the stateless layer template.
+//
+// A template is the kernel sequence of one decoder layer (or of the
+// embedding / head) with no weight pointers of its own: Bind computes views
+// into whichever device buffer currently holds the tile (pointer arithmetic
+// over the tile's static offsets, no copy), and the same sequence runs on it
+// (MegaTrain paperlayer.ai summary §A.4 "GPU Compute Dispatch"; hyper.ai
+// summary 方法 ¶6: templates hold the compute kernels but no persistent
+// weight pointers; a Bind primitive maps views of the streaming buffer into
+// the template's input slots).  Because the host tile layout equals the
+// device view layout, Bind needs no gather kernel.
+#include <cstring>
+#include <stdexcept>
+
+#include "runtime.h"
+
+namespace mt {
+
+const TensorSlot& TileLayout::slot(const char* n) const {
+  for (const auto& t : tensors)
+    if (t.name == n) return t;
+  throw std::runtime_error(std::string("no tensor ") + n);
+}
+
+Dims dims_of(const mt_config& c) {
+  Dims d;
+  d.L = c.n_layers;
+  d.d = c.d_model;
+  d.Hq = c.n_heads;
+  d.Hkv = c.n_kv_heads;
+  d.hd = c.head_dim;
+  d.f = c.ffn;
+  d.V = c.vocab;
+  d.B = c.batch;
+  d.S = c.seq;
+  d.T = (long)c.batch * c.seq;
+  d.Dq = c.n_heads * c.head_dim;
+  d.Dqkv = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  return d;
+}
+
+TileLayout make_layout(TileKind kind, const Dims& d) {
+  TileLayout L;
+  L.kind = kind;
+  auto add = [&](const char* n, int64_t r, int64_t c) {
+    TensorSlot s;
+    s.name = n;
+    s.ndim = c ? 2 : 1;
+    s.shape[0] = r;
+    s.shape[1] = c;
+    s.numel = c ? r * c : r;
+    L.tensors.push_back(s);
+  };
+  if (kind == kTileEmbed) {
+    add("E", d.V, d.d);
+  } else if (kind == kTileLayer) {
+    add("g1", d.d, 0);
+    add("wqkv", d.Dqkv, d.d);
+    add("wo", d.d, d.Dq);
+    add("g2", d.d, 0);
+    add("wgu", 2L * d.f, d.d);
+    add("wd", d.d, d.f);
+  } else {
+    add("gf", d.d, 0);
+    add("wh", d.V, d.d);
+  }
+  int64_t off = 0;
+  for (auto& t : L.tensors) {
+    t.offset = off;
+    off = align_up(off + t.numel * 2, kTensorAlign);
+    L.n_params += t.numel;
+  }
+  L.w_bytes = align_up(off, kPage);
+  L.mv_bytes = 2 * L.w_bytes;
+  L.off_w = 0;
+  L.off_g = L.w_bytes;
+  L.off_m = 2 * L.w_bytes;
+  L.off_v = 2 * L.w_bytes + L.mv_bytes;
+  L.tile_bytes = 2 * L.w_bytes + 2 * L.mv_bytes;
+  return L;
+}
+
+LayerView bind_layer(const TileLayout& lay, void* base) {
+  auto p = [&](const char* n) { return reinterpret_cast<bf16*>(static_cast<uint8_t*>(base) + lay.slot(n).offset); };
+  return LayerView{p("g1"), p("wqkv"), p("wo"), p("g2"), p("wgu"), p("wd")};
+}
+
+HeadView bind_head(const TileLayout& lay, void* base) {
+  auto p = [&](const char* n) { return reinterpret_cast<bf16*>(static_cast<uint8_t*>(base) + lay.slot(n).offset); };
+  return HeadView{p("gf"), p("wh")};
+}
+
+// ------------------------------------------------------------------ template
+int LayerTemplate::gemm(const GemmArgs& g) const {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (stats->time_gemms) {
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0, s);
+  }
+  const int rc = launch_gemm(g, s);
+  if (stats->time_gemms) {
+    cudaEventRecord(e1, s);
+    stats->gemm_events->push_back(e0);
+    stats->gemm_events->push_back(e1);
+    stats->gemm_event_flops->push_back(2.0 * g.M * g.N * g.K);
+  }
+  stats->kernels += 1;
+  stats->gemms += 1;
+  stats->gemm_flops += 2.0 * g.M * g.N * g.K;
+  return rc;
+}
+
+namespace {
+GemmArgs mk(const bf16* A, long lda, const bf16* B, long ldb, int M, int N, int K, int epi, void* C, long ldc,
+            int* status) {
+  GemmArgs g;
+  g.A = A;
+  g.lda = lda;
+  g.B = B;
+  g.ldb = ldb;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.epi = epi;
+  g.C = C;
+  g.ldc = ldc;
+  g.status = status;
+  return g;
+}
+}  // namespace
+
+int LayerTemplate::forward(const LayerView& w, LayerActs& a, bf16* x_out, bool keep_gu) const {
+  const Dims& D = dm;
+  const long T = D.T;
+  int rc = 0;
+  launch_rmsnorm_fwd(a.x, w.g1, a.n1, a.rstd1, T, D.d, eps, s);
+  // qkv = n1 Wqkv^T with rotate-half RoPE on the q and k columns
+  GemmArgs g = mk(a.n1, D.d, w.wqkv, D.d, (int)T, D.Dqkv, D.d, kEpiRope, a.qkv, D.Dqkv, ws->status);
+  g.rope_cos = ws->rope_cos;
+  g.rope_sin = ws->rope_sin;
+  g.rope_cols = (D.Hq + D.Hkv) * D.hd;
+  g.head_dim = D.hd;
+  g.seq = D.S;
+  rc |= gemm(g);
+  AttnArgs at;
+  at.qkv = a.qkv;
+  at.ldqkv = D.Dqkv;
+  at.batch = D.B;
+  at.seq = D.S;
+  at.n_heads = D.Hq;
+  at.n_kv_heads = D.Hkv;
+  at.head_dim = D.hd;
+  at.o = a.o;
+  at.ldo = D.Dq;
+  at.lse = a.lse;
+  at.status = ws->status;
+  rc |= launch_attn_fwd(at, s);
+  // h = x + o Wo^T
+  g = mk(a.o, D.Dq, w.wo, D.Dq, (int)T, D.d, D.Dq, kEpiResidualBf16, a.h, D.d, ws->status);
+  g.R = a.x;
+  g.ldr = D.d;
+  rc |= gemm(g);
+  launch_rmsnorm_fwd(a.h, w.g2, a.n2, a.rstd2, T, D.d, eps, s);
+  // a = silu(n2 Wg^T) * (n2 Wu^T) from interleaved gate/up rows
+  g = mk(a.n2, D.d, w.wgu, D.d, (int)T, 2 * D.f, D.d, kEpiSwiGLU, a.a, D.f, ws->status);
+  if (keep_gu) {
+    g.C2 = a.gu;
+    g.ldc2 = 2L * D.f;
+  }
+  rc |= gemm(g);
+  // x_out = h + a Wd^T (skipped when only the internals are recomputed for backward)
+  if (x_out) {
+    g = mk(a.a, D.f, w.wd, D.f, (int)T, D.d, D.f, kEpiResidualBf16, x_out, D.d, ws->status);
+    g.R = a.h;
+    g.ldr = D.d;
+    rc |= gemm(g);
+  }
+  stats->kernels += 3;
+  return rc;
+}
+
+int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, bf16* dx_in,
+                            const LayerView& gv) const {
+  const Dims& D = dm;
+  const long T = D.T;
+  const Workspace& W = *ws;
+  int rc = 0;
+  // Weight gradient dW[N, K] = dY[T, N]^T X[T, K]: both operands transposed to K-major (T contiguous).
+  auto wgrad = [&](const bf16* dY, int N, const bf16* X, int K, bf16* dW) {
+    launch_transpose(dY, T, N, N, W.tr_y, T, s);
+    launch_transpose(X, T, K, K, W.tr_x, T, s);
+    stats->kernels += 2;
+    rc |= gemm(mk(W.tr_y, T, W.tr_x, T, N, K, (int)T, kEpiStoreBf16, dW, K, W.status));
+  };
+  // Data gradient dX[T, K] = dY[T, N] W[N, K]: W transposed to [K, N].
+  auto dgrad = [&](const bf16* dY, int N, const bf16* Wm, int K, bf16* dX) {
+    launch_transpose(Wm, N, K, K, W.tr_w, N, s);
+    stats->kernels += 1;
+    rc |= gemm(mk(dY, N, W.tr_w, N, (int)T, K, N, kEpiStoreBf16, dX, K, W.status));
+  };
+
+  // x_out = h + a Wd^T
+  wgrad(dx_out, D.d, a.a, D.f, gv.wd);
+  dgrad(dx_out, D.d, w.wd, D.f, W.da);
+  launch_swiglu_bwd(W.da, a.gu, W.dgu, T, D.f, s);
+  wgrad(W.dgu, 2 * D.f, a.n2, D.d, gv.wgu);
+  dgrad(W.dgu, 2 * D.f, w.wgu, D.d, W.dn);
+  // dh = dx_out + RMSNorm2^T dn2 ; dg2
+  launch_rmsnorm_bwd(W.dn, a.h, w.g2, a.rstd2, dx_out, W.dh, W.dg_partial, T, D.d, s);
+  launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g2, s);
+  // h = x + o Wo^T
+  wgrad(W.dh, D.d, a.o, D.Dq, gv.wo);
+  dgrad(W.dh, D.d, w.wo, D.Dq, W.dout);
+  AttnArgs at;
+  at.qkv = a.qkv;
+  at.ldqkv = D.Dqkv;
+  at.batch = D.B;
+  at.seq = D.S;
+  at.n_heads = D.Hq;
+  at.n_kv_heads = D.Hkv;
+  at.head_dim = D.hd;
+  at.o = a.o;
+  at.ldo = D.Dq;
+  at.lse = a.lse;
+  at.dout = W.dout;
+  at.delta = W.delta;
+  at.dqkv = W.dqkv;
+  at.rope_cos = W.rope_cos;
+  at.rope_sin = W.rope_sin;
+  at.status = W.status;
+  rc |= launch_attn_bwd(at, s);
+  wgrad(W.dqkv, D.Dqkv, a.n1, D.d, gv.wqkv);
+  dgrad(W.dqkv, D.Dqkv, w.wqkv, D.d, W.dn);
+  launch_rmsnorm_bwd(W.dn, a.x, w.g1, a.rstd1, W.dh, dx_in, W.dg_partial, T, D.d, s);
+  launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g1, s);
+  stats->kernels += 3 + 4;
+  return rc;
+}
+
+int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const HeadView& gv) const {
+  const Dims& D = dm;
+  const long T = D.T;
+  const Workspace& W = *ws;
+  int rc = 0;
+  launch_rmsnorm_fwd(x_L, w.gf, W.nf, W.rstd_f, T, D.d, eps, s);
+  launch_transpose(w.wh, D.V, D.d, D.d, W.tr_w, D.V, s);  // W_h^T [d, V]
+  launch_zero(W.dwh_f32, sizeof(float) * (size_t)D.V * D.d, s);
+  stats->kernels += 2;
+  const float inv_n = 1.0f / (float)T;
+  for (long r0 = 0; r0 < T; r0 += W.head_chunk) {
+    const long rows = (T - r0) < W.head_chunk ? (T - r0) : W.head_chunk;
+    const bf16* nf = W.nf + r0 * D.d;
+    rc |= gemm(mk(nf, D.d, w.wh, D.d, (int)rows, D.V, D.d, kEpiF32, W.z, D.V, W.status));
+    launch_cross_entropy(W.z, rows, D.V, W.tgt + r0, inv_n, W.dz, W.loss_rows + r0, W.status, s);
+    // d nf = dz W_h
+    rc |= gemm(mk(W.dz, D.V, W.tr_w, D.V, (int)rows, D.d, D.V, kEpiStoreBf16, W.dnf + r0 * D.d, D.d, W.status));
+    // dW_h += dz^T nf
+    launch_transpose(W.dz, rows, D.V, D.V, W.tr_y, rows, s);
+    launch_transpose(nf, rows, D.d, D.d, W.tr_x, rows, s);
+    rc |= gemm(mk(W.tr_y, rows, W.tr_x, rows, D.V, D.d, (int)rows, kEpiF32Accumulate, W.dwh_f32, D.d, W.status));
+    stats->kernels += 3;
+  }
+  launch_f32_to_bf16(W.dwh_f32, gv.wh, (long)D.V * D.d, s);
+  launch_mean_loss(W.loss_rows, T, inv_n, W.loss, s);
+  launch_rmsnorm_bwd(W.dnf, x_L, w.gf, W.rstd_f, nullptr, dx_L, W.dg_partial, T, D.d, s);
+  launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.gf, s);
+  stats->kernels += 4;
+  return rc;
+}
+
+int LayerTemplate::embed_fwd(const bf16* E, bf16* x0) const {
+  launch_embed_fwd(ws->inp, E, x0, dm.T, dm.d, dm.V, ws->status, s);
+  stats->kernels += 1;
+  return 0;
+}
+
+int LayerTemplate::embed_bwd(const bf16* dx0, bf16* dE) const {
+  launch_embed_bwd(ws->emb_off, ws->emb_pos, dx0, dE, dm.V, dm.d, s);
+  stats->kernels += 1;
+  return 0;
+}
+
+}  // namespace mt

@@ -57,3 +57,112 @@ int mt_op_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M
 }
 
 }  // extern "C"
+
+extern "C" {
+
+int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, void* o, int64_t ldo, float* lse, void* stream) {
+  mt::AttnArgs a;
+  a.qkv = static_cast<const mt::bf16*>(qkv);
+  a.ldqkv = ldqkv;
+  a.batch = batch;
+  a.seq = seq;
+  a.n_heads = n_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.o = static_cast<mt::bf16*>(o);
+  a.ldo = ldo;
+  a.lse = lse;
+  if (const char* e = mt::attn_check(a)) return op_fail(e);
+  return op_cuda(mt::launch_attn_fwd(a, static_cast<cudaStream_t>(stream)), "attention forward");
+}
+
+int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, const void* o, int64_t ldo, const float* lse,
+                        const void* dout, float* delta, void* dqkv, const float* rope_cos, const float* rope_sin,
+                        void* stream) {
+  mt::AttnArgs a;
+  a.qkv = static_cast<const mt::bf16*>(qkv);
+  a.ldqkv = ldqkv;
+  a.batch = batch;
+  a.seq = seq;
+  a.n_heads = n_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.o = const_cast<mt::bf16*>(static_cast<const mt::bf16*>(o));
+  a.ldo = ldo;
+  a.lse = const_cast<float*>(lse);
+  a.dout = static_cast<const mt::bf16*>(dout);
+  a.delta = delta;
+  a.dqkv = static_cast<mt::bf16*>(dqkv);
+  a.rope_cos = rope_cos;
+  a.rope_sin = rope_sin;
+  if (const char* e = mt::attn_check(a)) return op_fail(e);
+  if (!dout || !delta || !dqkv) return op_fail("attention backward: null dout, delta or dqkv");
+  if ((rope_cos == nullptr) != (rope_sin == nullptr)) return op_fail("attention backward: cos and sin go together");
+  return op_cuda(mt::launch_attn_bwd(a, static_cast<cudaStream_t>(stream)), "attention backward");
+}
+
+int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_t rows, int32_t d, float eps,
+                      void* stream) {
+  if (d <= 0 || d % 8) return op_fail("rmsnorm: d must be a positive multiple of 8");
+  mt::launch_rmsnorm_fwd(static_cast<const mt::bf16*>(x), static_cast<const mt::bf16*>(g),
+                         static_cast<mt::bf16*>(y), rstd, rows, d, eps, static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "rmsnorm forward");
+}
+
+int64_t mt_op_rmsnorm_bwd_scratch_floats(int64_t rows, int32_t d) {
+  return ((rows + mt::kRmsRowsPerBlock - 1) / mt::kRmsRowsPerBlock) * (int64_t)d;
+}
+
+int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float* rstd, const void* dres, void* dx,
+                      void* dg, float* scratch, int64_t rows, int32_t d, void* stream) {
+  if (d <= 0 || d % 8) return op_fail("rmsnorm: d must be a positive multiple of 8");
+  auto s = static_cast<cudaStream_t>(stream);
+  mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
+                         static_cast<const mt::bf16*>(g), rstd, static_cast<const mt::bf16*>(dres),
+                         static_cast<mt::bf16*>(dx), scratch, rows, d, s);
+  mt::launch_colsum_bf16(scratch, (rows + mt::kRmsRowsPerBlock - 1) / mt::kRmsRowsPerBlock, d,
+                         static_cast<mt::bf16*>(dg), s);
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "rmsnorm backward");
+}
+
+int mt_op_swiglu_bwd(const void* da, const void* gu, void* dgu, int64_t rows, int32_t f, void* stream) {
+  if (f <= 0) return op_fail("swiglu: f must be positive");
+  mt::launch_swiglu_bwd(static_cast<const mt::bf16*>(da), static_cast<const mt::bf16*>(gu),
+                        static_cast<mt::bf16*>(dgu), rows, f, static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "swiglu backward");
+}
+
+int mt_op_transpose(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd,
+                    void* stream) {
+  mt::launch_transpose(static_cast<const mt::bf16*>(src), rows, cols, lds, static_cast<mt::bf16*>(dst), ldd,
+                       static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "transpose");
+}
+
+int mt_op_cross_entropy(const float* z, int64_t rows, int32_t vocab, const int32_t* tgt, float inv_n, void* dz,
+                        float* loss_rows, int32_t* status, void* stream) {
+  if (vocab <= 0) return op_fail("cross entropy: vocab must be positive");
+  mt::launch_cross_entropy(z, rows, vocab, tgt, inv_n, static_cast<mt::bf16*>(dz), loss_rows, status,
+                           static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "cross entropy");
+}
+
+int mt_op_embedding_fwd(const int32_t* tok, const void* E, void* x, int64_t T, int32_t d, int32_t V,
+                        int32_t* status, void* stream) {
+  if (d % 8) return op_fail("embedding: d must be a multiple of 8");
+  mt::launch_embed_fwd(tok, static_cast<const mt::bf16*>(E), static_cast<mt::bf16*>(x), T, d, V, status,
+                       static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "embedding forward");
+}
+
+int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, const void* dx, void* dE, int32_t V,
+                        int32_t d, void* stream) {
+  if (d % 8) return op_fail("embedding: d must be a multiple of 8");
+  mt::launch_embed_bwd(row_offsets, positions, static_cast<const mt::bf16*>(dx), static_cast<mt::bf16*>(dE), V, d,
+                       static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "embedding backward");
+}
+
+}  // extern "C"

@@ -8,19 +8,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "kernels.h"
+
 namespace mt {
 
 // Wait budget for one mbarrier wait (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
-// Device status word codes (written with atomicCAS so the first error sticks).
-enum : int {
-  kStatusOk = 0,
-  kStatusGemmTimeout = 1,
-  kStatusAttnBadShape = 2,
-  kStatusIndexOutOfRange = 3,
-  kStatusNonFinite = 4,
-};
 
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);

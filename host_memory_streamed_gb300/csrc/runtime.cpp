@@ -1,0 +1,1274 @@
+// The layer-streamed training step: host-authoritative tiles, two device
+// weight buffers, three CUDA streams ordered by events, CPU worker threads.
+//
+//   caller thread   compute stream: waits Weights-Ready[v], binds the tile in
+//                   buffer b, launches the template's kernels, records
+//                   Buffer-Free[v] and (for backward visits) Grads-Done[v].
+//   loader thread   H2D stream: for each visit that needs a tile, waits for the
+//                   buffer's previous user to be done (Buffer-Free), then has
+//                   the packer threads copy the pageable tile into one of two
+//                   pinned staging chunks while the other chunk's DMA runs,
+//                   and records Weights-Ready[v].
+//   d2h thread      D2H stream: after Grads-Done[v], copies the gradient buffer
+//                   into free pinned slabs (12 by default) and records
+//                   Grads-Evacuated[v] so the compute stream may reuse it.
+//   accumulator     copies each landed slab into the tile's G section, returns
+//                   the slab, and hands a completed tile to the Adam pool.
+//   Adam pool       updates W, M, V of finished tiles while the GPU keeps
+//                   working on earlier layers.
+//
+// MegaTrain sources: paperlayer.ai summary §3 (execution workflow, three
+// streams, background gradient evacuation), §A.1 (layer-contiguous tiles,
+// pinned slab recycling, two pinned staging buffers), §A.2 (ComputeStream /
+// WeightStream / GradStream; weights-ready, backward-done and buffer-free
+// events), §A.3 (flat-buffer streaming with one copy per layer, K=12 pinned
+// gradient slabs with a background accumulator, preallocated workspaces),
+// §A.4 (stateless templates, ping-pong binding, no CUDA graphs); hyper.ai
+// summary 方法 ¶2-6 (block recompute order, JIT packer thread, Weights-Ready
+// event before Bind); author's blog (per-block F/W/G figure).
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <condition_variable>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <deque>
+#include <functional>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "runtime.h"
+
+namespace mt {
+namespace {
+
+using Clock = std::chrono::steady_clock;
+
+double ms_since(Clock::time_point t0) {
+  return std::chrono::duration<double, std::milli>(Clock::now() - t0).count();
+}
+
+struct MtError {
+  int code;
+  std::string msg;
+};
+
+// ------------------------------------------------------------------ small thread pool
+class Pool {
+ public:
+  explicit Pool(int n) {
+    for (int i = 0; i < n; ++i) th_.emplace_back([this] { run(); });
+  }
+  ~Pool() {
+    {
+      std::lock_guard<std::mutex> g(mu_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : th_) t.join();
+  }
+  void submit(std::function<void()> f) {
+    {
+      std::lock_guard<std::mutex> g(mu_);
+      q_.push_back(std::move(f));
+      ++pending_;
+    }
+    cv_.notify_one();
+  }
+  // Wait until every submitted task finished; false on timeout.
+  bool wait_idle(int64_t timeout_ms) {
+    std::unique_lock<std::mutex> g(mu_);
+    return done_cv_.wait_for(g, std::chrono::milliseconds(timeout_ms), [this] { return pending_ == 0; });
+  }
+  int size() const { return (int)th_.size(); }
+
+ private:
+  void run() {
+    while (true) {
+      std::function<void()> f;
+      {
+        std::unique_lock<std::mutex> g(mu_);
+        cv_.wait(g, [this] { return stop_ || !q_.empty(); });
+        if (stop_ && q_.empty()) return;
+        f = std::move(q_.front());
+        q_.pop_front();
+      }
+      f();
+      {
+        std::lock_guard<std::mutex> g(mu_);
+        if (--pending_ == 0) done_cv_.notify_all();
+      }
+    }
+  }
+  std::vector<std::thread> th_;
+  std::deque<std::function<void()>> q_;
+  std::mutex mu_;
+  std::condition_variable cv_, done_cv_;
+  int64_t pending_ = 0;
+  bool stop_ = false;
+};
+
+// ------------------------------------------------------------------ schedule
+enum VisitKind { kEmbedFwd, kLayerFwd, kHead, kRecompute, kLayerBwd, kEmbedBwd };
+
+struct Visit {
+  VisitKind kind;
+  int tile;
+  int layer;
+  int buf = -1;        // device weight buffer (-1: none)
+  bool h2d = false;    // stream the tile into buf before this visit
+  int prev_user = -1;  // previous visit that used buf
+  bool grads = false;
+  int gbuf = -1;
+  int prev_gbuf_user = -1;
+};
+
+std::vector<Visit> build_schedule(int L, int K, bool store_acts, bool single_buffer) {
+  std::vector<Visit> v;
+  v.push_back({kEmbedFwd, 0, -1});
+  for (int i = 0; i < L; ++i) v.push_back({kLayerFwd, i + 1, i});
+  v.push_back({kHead, L + 1, -1});
+  const int nblk = (L + K - 1) / K;
+  for (int b = nblk - 1; b >= 0; --b) {
+    const int s = b * K, e = std::min(L, s + K);
+    if (!store_acts)
+      for (int j = s; j < e - 1; ++j) v.push_back({kRecompute, j + 1, j});
+    for (int j = e - 1; j >= s; --j) v.push_back({kLayerBwd, j + 1, j});
+  }
+  v.push_back({kEmbedBwd, 0, -1});
+  // buffer assignment with residency reuse
+  int held[2] = {-1, -1}, last_user[2] = {-1, -1}, prev_buf = 1;
+  int glast[2] = {-1, -1}, gnext = 0;
+  for (int i = 0; i < (int)v.size(); ++i) {
+    Visit& x = v[i];
+    if (x.kind != kEmbedBwd) {
+      int b = -1;
+      for (int c = 0; c < (single_buffer ? 1 : 2); ++c)
+        if (held[c] == x.tile) b = c;
+      if (b < 0) {
+        b = single_buffer ? 0 : (prev_buf ^ 1);
+        x.h2d = true;
+        held[b] = x.tile;
+      }
+      x.buf = b;
+      x.prev_user = last_user[b];
+      last_user[b] = i;
+      prev_buf = b;
+    }
+    x.grads = (x.kind == kHead || x.kind == kLayerBwd || x.kind == kEmbedBwd);
+    if (x.grads) {
+      x.gbuf = gnext;
+      x.prev_gbuf_user = glast[gnext];
+      glast[gnext] = i;
+      gnext ^= 1;
+    }
+  }
+  return v;
+}
+
+// ------------------------------------------------------------------ device arena plan
+struct Plan {
+  int64_t total = 0;
+  int64_t add(int64_t bytes) {
+    const int64_t off = total;
+    total = align_up(total + std::max<int64_t>(bytes, 1), 256);
+    return off;
+  }
+};
+
+struct ActsSizes {
+  int64_t n1, rstd, qkv, o, lse, h, n2, gu, a, x;
+  int64_t total;
+};
+
+ActsSizes acts_sizes(const Dims& D) {
+  ActsSizes s;
+  s.x = align_up(D.T * D.d * 2, 256);
+  s.n1 = s.x;
+  s.rstd = align_up(D.T * 4, 256);
+  s.qkv = align_up(D.T * D.Dqkv * 2, 256);
+  s.o = align_up(D.T * D.Dq * 2, 256);
+  s.lse = align_up((int64_t)D.B * D.Hq * D.S * 4, 256);
+  s.h = s.x;
+  s.n2 = s.x;
+  s.gu = align_up(D.T * 2L * D.f * 2, 256);
+  s.a = align_up(D.T * (int64_t)D.f * 2, 256);
+  s.total = s.n1 + 2 * s.rstd + s.qkv + s.o + s.lse + s.h + s.n2 + s.gu + s.a;
+  return s;
+}
+
+LayerActs carve_acts(uint8_t* p, const Dims& D, bf16* x) {
+  const ActsSizes s = acts_sizes(D);
+  LayerActs a;
+  a.x = x;
+  a.n1 = reinterpret_cast<bf16*>(p);
+  p += s.n1;
+  a.rstd1 = reinterpret_cast<float*>(p);
+  p += s.rstd;
+  a.qkv = reinterpret_cast<bf16*>(p);
+  p += s.qkv;
+  a.o = reinterpret_cast<bf16*>(p);
+  p += s.o;
+  a.lse = reinterpret_cast<float*>(p);
+  p += s.lse;
+  a.h = reinterpret_cast<bf16*>(p);
+  p += s.h;
+  a.n2 = reinterpret_cast<bf16*>(p);
+  p += s.n2;
+  a.rstd2 = reinterpret_cast<float*>(p);
+  p += s.rstd;
+  a.gu = reinterpret_cast<bf16*>(p);
+  p += s.gu;
+  a.a = reinterpret_cast<bf16*>(p);
+  return a;
+}
+
+long head_chunk_rows(const Dims& D) {
+  // keep the FP32 logits of one chunk near 2 GiB, at most T, a multiple of 128
+  long rows = (long)((2LL << 30) / ((int64_t)D.V * 4));
+  rows = std::max(128L, rows / 128 * 128);
+  return std::min(rows, D.T);
+}
+
+// Workspace layout (shared by the byte count and by init).
+Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
+  const long T = D.T;
+  const long hc = head_chunk_rows(D);
+  const int64_t td = T * D.d * 2;
+  const int64_t maxN = std::max<int64_t>({(int64_t)2 * D.f, D.Dqkv, D.d});
+  const int64_t maxK = std::max<int64_t>({(int64_t)D.f, D.Dq, D.d});
+  const int64_t maxW = std::max<int64_t>({(int64_t)2 * D.f * D.d, (int64_t)D.Dqkv * D.d, (int64_t)D.d * D.Dq,
+                                          (int64_t)D.d * D.f, (int64_t)D.V * D.d});
+  auto at = [&](int64_t bytes) { return base ? base + P.add(bytes) : (P.add(bytes), nullptr); };
+  Workspace w{};
+  w.dx_a = reinterpret_cast<bf16*>(at(td));
+  w.dx_b = reinterpret_cast<bf16*>(at(td));
+  w.dh = reinterpret_cast<bf16*>(at(td));
+  w.da = reinterpret_cast<bf16*>(at(T * (int64_t)D.f * 2));
+  w.dgu = reinterpret_cast<bf16*>(at(T * 2L * D.f * 2));
+  w.dn = reinterpret_cast<bf16*>(at(td));
+  w.dout = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dq * 2));
+  w.dqkv = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dqkv * 2));
+  w.delta = reinterpret_cast<float*>(at((int64_t)D.B * D.Hq * D.S * 4));
+  w.dg_partial = reinterpret_cast<float*>(at(((T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock) * (int64_t)D.d * 4));
+  w.tr_y = reinterpret_cast<bf16*>(at(std::max<int64_t>(maxN * T, (int64_t)D.V * hc) * 2));
+  w.tr_x = reinterpret_cast<bf16*>(at(std::max<int64_t>(maxK * T, (int64_t)D.d * hc) * 2));
+  w.tr_w = reinterpret_cast<bf16*>(at(maxW * 2));
+  w.nf = reinterpret_cast<bf16*>(at(td));
+  w.rstd_f = reinterpret_cast<float*>(at(T * 4));
+  w.z = reinterpret_cast<float*>(at(hc * (int64_t)D.V * 4));
+  w.dz = reinterpret_cast<bf16*>(at(hc * (int64_t)D.V * 2));
+  w.dnf = reinterpret_cast<bf16*>(at(td));
+  w.dwh_f32 = reinterpret_cast<float*>(at((int64_t)D.V * D.d * 4));
+  w.loss_rows = reinterpret_cast<float*>(at(T * 4));
+  w.loss = reinterpret_cast<float*>(at(256));
+  w.inp = reinterpret_cast<int32_t*>(at(T * 4));
+  w.tgt = reinterpret_cast<int32_t*>(at(T * 4));
+  w.emb_off = reinterpret_cast<int32_t*>(at(((int64_t)D.V + 1) * 4));
+  w.emb_pos = reinterpret_cast<int32_t*>(at(T * 4));
+  w.tokens_dev = reinterpret_cast<int32_t*>(at((int64_t)D.B * (D.S + 1) * 4));
+  w.rope_cos = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
+  w.rope_sin = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
+  w.status = reinterpret_cast<int*>(at(256));
+  w.head_chunk = hc;
+  return w;
+}
+
+}  // namespace
+}  // namespace mt
+
+// ====================================================================== the handle
+struct mt_model {
+  mt_config cfg{};
+  mt::Dims D{};
+  int K = 1;
+  bool resident_mode = false, store_acts = false, single_buffer = false, debug = false, time_kernels = false;
+  std::vector<mt::TileLayout> layouts;  // per tile
+  std::vector<uint8_t*> tiles;
+  std::vector<uint8_t> w_loaded;
+  int64_t step = 0;
+  std::string err;
+  bool broken = false;
+
+  // device
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  int64_t arena_used = 0;
+  cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
+  uint8_t* wbuf[2] = {nullptr, nullptr};
+  uint8_t* gbuf[2] = {nullptr, nullptr};
+  uint8_t* resident = nullptr;
+  std::vector<int64_t> resident_off;
+  std::vector<mt::bf16*> ckpt, blockbuf;
+  mt::bf16* xtmp[2] = {nullptr, nullptr};
+  std::vector<mt::LayerActs> stored;
+  mt::LayerActs acts{};
+  mt::Workspace ws{};
+  int64_t max_w_bytes = 0;
+
+  // host pinned
+  uint8_t* stage[2] = {nullptr, nullptr};
+  int64_t stage_bytes = 0;
+  std::vector<uint8_t*> slabs;
+  int64_t slab_bytes = 0;
+  float* pinned_scalars = nullptr;  // [0] loss, [1] status bits
+  int32_t* pinned_tok = nullptr;    // inp | tgt | emb_off | emb_pos | raw tokens
+
+  // schedule + events
+  std::vector<mt::Visit> visits;
+  int n_grad_visits = 0;
+  int last_grad_visit = -1;
+  std::vector<cudaEvent_t> ev_ready, ev_free, ev_grads, ev_d2h;
+  std::vector<cudaEvent_t> ev_wait_a, ev_wait_b, ev_h2d_a, ev_h2d_b, ev_d2h_a, ev_d2h_b;
+  cudaEvent_t ev_stage[2] = {nullptr, nullptr};
+  std::vector<cudaEvent_t> ev_slab;
+  cudaEvent_t ev_t0 = nullptr, ev_t1 = nullptr;
+
+  // host handshakes
+  std::mutex mu;
+  std::condition_variable cv;
+  std::vector<char> rec_ready, rec_free, rec_d2h, rec_h2d_timed, rec_d2h_timed, rec_wait_timed;
+  std::atomic<bool> abort_flag{false};
+  std::atomic<bool> nonfinite{false};
+  std::atomic<int> worker_code{0};
+  std::string worker_msg;
+
+  // threads
+  std::unique_ptr<mt::Pool> adam_pool, pack_pool;
+  std::thread loader, d2h, accum;
+  bool stop_threads = false;
+  int64_t step_gen = 0;
+  std::deque<int> d2h_q;
+  struct AccJob {
+    int slab, visit, tile;
+    int64_t off, bytes;
+    bool last;
+  };
+  std::deque<AccJob> acc_q;
+  std::vector<int> free_slabs;
+  int acc_tiles_done = 0;
+  std::atomic<int64_t> adam_us{0};
+  std::chrono::steady_clock::time_point last_grads_landed;
+
+  // stats
+  mt_step_stats stats{};
+  mt::LaunchStats ls;
+  std::vector<cudaEvent_t> gemm_events;
+  std::vector<double> gemm_event_flops;
+};
+
+namespace mt {
+namespace {
+
+thread_local std::string g_init_error;
+
+#define MT_CK(call)                                                                                    \
+  do {                                                                                                 \
+    cudaError_t e__ = (call);                                                                          \
+    if (e__ != cudaSuccess) throw MtError{MT_ECUDA, std::string(#call) + ": " + cudaGetErrorString(e__)}; \
+  } while (0)
+
+void worker_fail(mt_model* m, const MtError& e) {
+  {
+    std::lock_guard<std::mutex> g(m->mu);
+    if (m->worker_code == 0) {
+      m->worker_code = e.code;
+      m->worker_msg = e.msg;
+    }
+    m->abort_flag = true;
+  }
+  m->cv.notify_all();
+}
+
+void check_abort(mt_model* m) {
+  if (m->abort_flag) {
+    std::lock_guard<std::mutex> g(m->mu);
+    throw MtError{m->worker_code ? m->worker_code.load() : MT_EINTERNAL, "step aborted: " + m->worker_msg};
+  }
+}
+
+void wait_event(mt_model* m, cudaEvent_t e, const char* what) {
+  const auto t0 = Clock::now();
+  while (true) {
+    const cudaError_t r = cudaEventQuery(e);
+    if (r == cudaSuccess) return;
+    if (r != cudaErrorNotReady) throw MtError{MT_ECUDA, std::string(what) + ": " + cudaGetErrorString(r)};
+    check_abort(m);
+    if (ms_since(t0) > (double)m->cfg.timeout_ms) throw MtError{MT_ETIMEDOUT, std::string("timed out waiting for ") + what};
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+void wait_flag(mt_model* m, std::vector<char>& vec, int i, const char* what) {
+  std::unique_lock<std::mutex> g(m->mu);
+  const bool ok = m->cv.wait_for(g, std::chrono::milliseconds(m->cfg.timeout_ms),
+                                 [&] { return vec[i] != 0 || m->abort_flag.load(); });
+  if (m->abort_flag)
+    throw MtError{m->worker_code ? m->worker_code.load() : MT_EINTERNAL,
+                  std::string("aborted while waiting for ") + what + ": " + m->worker_msg};
+  if (!ok) throw MtError{MT_ETIMEDOUT, std::string("timed out waiting for ") + what};
+}
+
+void set_flag(mt_model* m, std::vector<char>& vec, int i) {
+  {
+    std::lock_guard<std::mutex> g(m->mu);
+    vec[i] = 1;
+  }
+  m->cv.notify_all();
+}
+
+// Multi-threaded pageable -> pinned copy (the JIT packer).
+void pack_copy(mt_model* m, uint8_t* dst, const uint8_t* src, int64_t n) {
+  const int nt = m->pack_pool->size();
+  const int64_t piece = align_up((n + nt - 1) / nt, 4096);
+  if (nt <= 1 || n < (8 << 20)) {
+    std::memcpy(dst, src, (size_t)n);
+    return;
+  }
+  for (int64_t off = 0; off < n; off += piece) {
+    const int64_t c = std::min(piece, n - off);
+    m->pack_pool->submit([=] { std::memcpy(dst + off, src + off, (size_t)c); });
+  }
+  if (!m->pack_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "packer copy timed out"};
+}
+
+// ------------------------------------------------------------------ loader (H2D stream)
+void loader_main(mt_model* m) {
+  int64_t gen = 0;
+  while (true) {
+    {
+      std::unique_lock<std::mutex> g(m->mu);
+      m->cv.wait(g, [&] { return m->stop_threads || m->step_gen > gen; });
+      if (m->stop_threads) return;
+      gen = m->step_gen;
+    }
+    try {
+      int si = 0;
+      for (int v = 0; v < (int)m->visits.size(); ++v) {
+        const Visit& x = m->visits[v];
+        if (!x.h2d) continue;
+        if (x.prev_user >= 0) {
+          wait_flag(m, m->rec_free, x.prev_user, "buffer free");
+          MT_CK(cudaStreamWaitEvent(m->s_h2d, m->ev_free[x.prev_user], 0));
+        }
+        MT_CK(cudaEventRecord(m->ev_h2d_a[v], m->s_h2d));
+        const TileLayout& lay = m->layouts[x.tile];
+        const uint8_t* src = m->tiles[x.tile] + lay.off_w;
+        uint8_t* dst = m->wbuf[x.buf];
+        const int64_t n = lay.w_bytes;
+        for (int64_t off = 0; off < n; off += m->stage_bytes) {
+          const int64_t c = std::min(m->stage_bytes, n - off);
+          const int k = si++ & 1;
+          wait_event(m, m->ev_stage[k], "pinned staging buffer");
+          pack_copy(m, m->stage[k], src + off, c);
+          MT_CK(cudaMemcpyAsync(dst + off, m->stage[k], (size_t)c, cudaMemcpyHostToDevice, m->s_h2d));
+          MT_CK(cudaEventRecord(m->ev_stage[k], m->s_h2d));
+        }
+        MT_CK(cudaEventRecord(m->ev_h2d_b[v], m->s_h2d));
+        MT_CK(cudaEventRecord(m->ev_ready[v], m->s_h2d));
+        m->rec_h2d_timed[v] = 1;
+        set_flag(m, m->rec_ready, v);
+      }
+    } catch (const MtError& e) {
+      worker_fail(m, e);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ D2H stream + slabs
+int acquire_slab(mt_model* m) {
+  std::unique_lock<std::mutex> g(m->mu);
+  const bool ok = m->cv.wait_for(g, std::chrono::milliseconds(m->cfg.timeout_ms),
+                                 [&] { return !m->free_slabs.empty() || m->abort_flag.load(); });
+  if (m->abort_flag) throw MtError{MT_EINTERNAL, "aborted"};
+  if (!ok) throw MtError{MT_ETIMEDOUT, "timed out waiting for a free gradient slab"};
+  const int s = m->free_slabs.back();
+  m->free_slabs.pop_back();
+  return s;
+}
+
+void d2h_main(mt_model* m) {
+  while (true) {
+    int v;
+    {
+      std::unique_lock<std::mutex> g(m->mu);
+      m->cv.wait(g, [&] { return m->stop_threads || !m->d2h_q.empty(); });
+      if (m->stop_threads) return;
+      v = m->d2h_q.front();
+      m->d2h_q.pop_front();
+    }
+    try {
+      check_abort(m);
+      const Visit& x = m->visits[v];
+      const TileLayout& lay = m->layouts[x.tile];
+      MT_CK(cudaStreamWaitEvent(m->s_d2h, m->ev_grads[v], 0));
+      MT_CK(cudaEventRecord(m->ev_d2h_a[v], m->s_d2h));
+      const uint8_t* src = m->gbuf[x.gbuf];
+      const int64_t n = lay.w_bytes;
+      for (int64_t off = 0; off < n; off += m->slab_bytes) {
+        const int64_t c = std::min(m->slab_bytes, n - off);
+        const int s = acquire_slab(m);
+        MT_CK(cudaMemcpyAsync(m->slabs[s], src + off, (size_t)c, cudaMemcpyDeviceToHost, m->s_d2h));
+        MT_CK(cudaEventRecord(m->ev_slab[s], m->s_d2h));
+        {
+          std::lock_guard<std::mutex> g(m->mu);
+          m->acc_q.push_back({s, v, x.tile, off, c, off + c >= n});
+        }
+        m->cv.notify_all();
+      }
+      MT_CK(cudaEventRecord(m->ev_d2h_b[v], m->s_d2h));
+      MT_CK(cudaEventRecord(m->ev_d2h[v], m->s_d2h));
+      m->rec_d2h_timed[v] = 1;
+      set_flag(m, m->rec_d2h, v);
+    } catch (const MtError& e) {
+      worker_fail(m, e);
+    }
+  }
+}
+
+void submit_adam(mt_model* m, int tile) {
+  const TileLayout& lay = m->layouts[tile];
+  uint8_t* base = m->tiles[tile];
+  const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
+  for (const auto& t : lay.tensors) {
+    const int64_t n = t.numel;
+    const int64_t piece = std::max<int64_t>(1 << 20, (n + m->adam_pool->size() - 1) / m->adam_pool->size());
+    for (int64_t b = 0; b < n; b += piece) {
+      const int64_t c = std::min(piece, n - b);
+      uint16_t* w = reinterpret_cast<uint16_t*>(base + lay.off_w + t.offset) + b;
+      const uint16_t* g = reinterpret_cast<const uint16_t*>(base + lay.off_g + t.offset) + b;
+      float* mm = reinterpret_cast<float*>(base + lay.off_m + 2 * t.offset) + b;
+      float* vv = reinterpret_cast<float*>(base + lay.off_v + 2 * t.offset) + b;
+      m->adam_pool->submit([=] {
+        const auto t0 = Clock::now();
+        adam_range(w, g, mm, vv, (size_t)c, h);
+        m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
+      });
+    }
+  }
+}
+
+void accum_main(mt_model* m) {
+  while (true) {
+    mt_model::AccJob j;
+    {
+      std::unique_lock<std::mutex> g(m->mu);
+      m->cv.wait(g, [&] { return m->stop_threads || !m->acc_q.empty(); });
+      if (m->stop_threads) return;
+      j = m->acc_q.front();
+      m->acc_q.pop_front();
+    }
+    try {
+      wait_event(m, m->ev_slab[j.slab], "gradient slab copy");
+      if (m->visits[j.visit].kind == kHead && j.off == 0 && !std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
+      const TileLayout& lay = m->layouts[j.tile];
+      uint16_t* dst = reinterpret_cast<uint16_t*>(m->tiles[j.tile] + lay.off_g + j.off);
+      const bool fin = copy_grad_check_finite(dst, reinterpret_cast<const uint16_t*>(m->slabs[j.slab]),
+                                              (size_t)(j.bytes / 2));
+      if (!fin) m->nonfinite = true;
+      {
+        std::lock_guard<std::mutex> g(m->mu);
+        m->free_slabs.push_back(j.slab);
+      }
+      m->cv.notify_all();
+      if (j.last) {
+        if (!m->nonfinite) submit_adam(m, j.tile);
+        {
+          std::lock_guard<std::mutex> g(m->mu);
+          m->acc_tiles_done += 1;
+          m->last_grads_landed = Clock::now();
+        }
+        m->cv.notify_all();
+      }
+    } catch (const MtError& e) {
+      worker_fail(m, e);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host token preprocessing
+// tokens [B, S+1] -> inp [T], tgt [T], and the positions of every token id in
+// ascending order (counting sort) for the deterministic embedding scatter.
+void prepare_tokens(mt_model* m, const int32_t* tokens) {
+  const Dims& D = m->D;
+  const long T = D.T;
+  int32_t* inp = m->pinned_tok;
+  int32_t* tgt = inp + T;
+  int32_t* off = tgt + T;
+  int32_t* pos = off + D.V + 1;
+  for (int b = 0; b < D.B; ++b)
+    for (int s = 0; s < D.S; ++s) {
+      inp[(long)b * D.S + s] = tokens[(long)b * (D.S + 1) + s];
+      tgt[(long)b * D.S + s] = tokens[(long)b * (D.S + 1) + s + 1];
+    }
+  for (long t = 0; t < T; ++t)
+    if (inp[t] < 0 || inp[t] >= D.V || tgt[t] < 0 || tgt[t] >= D.V)
+      throw MtError{MT_EINVAL, "token id out of range [0, vocab)"};
+  std::memset(off, 0, sizeof(int32_t) * (D.V + 1));
+  for (long t = 0; t < T; ++t) off[inp[t] + 1] += 1;
+  for (int v = 0; v < D.V; ++v) off[v + 1] += off[v];
+  std::vector<int32_t> cur(off, off + D.V);
+  for (long t = 0; t < T; ++t) pos[cur[inp[t]]++] = (int32_t)t;
+  const size_t bytes = sizeof(int32_t) * (size_t)(2 * T + D.V + 1 + T);
+  // ws.inp, tgt, emb_off, emb_pos are not contiguous in the arena: copy each.
+  MT_CK(cudaMemcpyAsync(m->ws.inp, inp, sizeof(int32_t) * T, cudaMemcpyHostToDevice, m->s_comp));
+  MT_CK(cudaMemcpyAsync(m->ws.tgt, tgt, sizeof(int32_t) * T, cudaMemcpyHostToDevice, m->s_comp));
+  MT_CK(cudaMemcpyAsync(m->ws.emb_off, off, sizeof(int32_t) * (D.V + 1), cudaMemcpyHostToDevice, m->s_comp));
+  MT_CK(cudaMemcpyAsync(m->ws.emb_pos, pos, sizeof(int32_t) * T, cudaMemcpyHostToDevice, m->s_comp));
+  (void)bytes;
+}
+
+// ------------------------------------------------------------------ FLOP accounting
+struct Flops {
+  double layer_fwd, head_fwd;
+};
+Flops flop_model(const Dims& D) {
+  const double T = (double)D.T;
+  const double lin = (double)D.d * D.Dqkv + (double)D.Dq * D.d + (double)D.d * 2.0 * D.f + (double)D.f * D.d;
+  const double attn = 4.0 * D.B * D.Hq * D.hd * ((double)D.S * (D.S + 1) / 2.0);
+  return Flops{2.0 * T * lin + attn, 2.0 * T * (double)D.d * D.V};
+}
+
+// ------------------------------------------------------------------ the step
+bf16* x_fwd_loc(mt_model* m, int i) {
+  if (m->store_acts) return i < m->D.L ? m->stored[i].x : m->xtmp[m->D.L % 2];
+  return (i < m->D.L && i % m->K == 0) ? m->ckpt[i / m->K] : m->xtmp[i % 2];
+}
+
+int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev, size_t n_tokens, float* loss_out) {
+  const Dims& D = m->D;
+  if (m->broken) {
+    m->err = "handle is unusable after an earlier CUDA or internal error: " + m->err;
+    return MT_ESTATE;
+  }
+  if (n_tokens != (size_t)D.B * (D.S + 1)) {
+    m->err = "n_tokens must equal batch * (seq + 1)";
+    return MT_EINVAL;
+  }
+  for (size_t t = 0; t < m->tiles.size(); ++t)
+    if (!m->w_loaded[t]) {
+      m->err = "tile " + std::to_string(t) + " has no weights loaded";
+      return MT_ESTATE;
+    }
+  const auto wall0 = Clock::now();
+  int code = MT_OK;
+  try {
+    MT_CK(cudaSetDevice(0) == cudaSuccess ? cudaSuccess : cudaGetLastError());
+    std::vector<int32_t> host_tok;
+    if (tokens_dev) {
+      host_tok.resize(n_tokens);
+      MT_CK(cudaMemcpyAsync(host_tok.data(), tokens_dev, n_tokens * 4, cudaMemcpyDeviceToHost, m->s_comp));
+      MT_CK(cudaStreamSynchronize(m->s_comp));
+      tokens_host = host_tok.data();
+    }
+    // reset per-step state
+    {
+      std::lock_guard<std::mutex> g(m->mu);
+      std::fill(m->rec_ready.begin(), m->rec_ready.end(), 0);
+      std::fill(m->rec_free.begin(), m->rec_free.end(), 0);
+      std::fill(m->rec_d2h.begin(), m->rec_d2h.end(), 0);
+      std::fill(m->rec_h2d_timed.begin(), m->rec_h2d_timed.end(), 0);
+      std::fill(m->rec_d2h_timed.begin(), m->rec_d2h_timed.end(), 0);
+      std::fill(m->rec_wait_timed.begin(), m->rec_wait_timed.end(), 0);
+      m->abort_flag = false;
+      m->worker_code = 0;
+      m->worker_msg.clear();
+      m->acc_tiles_done = 0;
+      m->d2h_q.clear();
+      m->acc_q.clear();
+    }
+    m->nonfinite = false;
+    m->adam_us = 0;
+    m->ls = LaunchStats{};
+    m->ls.time_gemms = m->time_kernels;
+    m->ls.gemm_events = &m->gemm_events;
+    m->ls.gemm_event_flops = &m->gemm_event_flops;
+    m->pinned_scalars[0] = 0.f;
+    m->pinned_scalars[1] = 0.f;
+
+    prepare_tokens(m, tokens_host);
+    MT_CK(cudaMemsetAsync(m->ws.status, 0, sizeof(int), m->s_comp));
+    if (m->resident_mode)
+      for (size_t t = 0; t < m->tiles.size(); ++t)
+        MT_CK(cudaMemcpyAsync(m->resident + m->resident_off[t], m->tiles[t] + m->layouts[t].off_w,
+                              (size_t)m->layouts[t].w_bytes, cudaMemcpyHostToDevice, m->s_comp));
+    MT_CK(cudaEventRecord(m->ev_t0, m->s_comp));
+    {
+      std::lock_guard<std::mutex> g(m->mu);
+      m->step_gen += 1;
+    }
+    m->cv.notify_all();
+
+    LayerTemplate tmpl{D, m->cfg.rms_eps, m->s_comp, &m->ws, &m->ls};
+    bf16* dx_cur = m->ws.dx_a;
+    bf16* dx_nxt = m->ws.dx_b;
+    for (int v = 0; v < (int)m->visits.size(); ++v) {
+      check_abort(m);
+      const Visit& x = m->visits[v];
+      uint8_t* wb = nullptr;
+      if (x.buf >= 0) {
+        if (m->resident_mode) {
+          wb = m->resident + m->resident_off[x.tile];
+        } else {
+          if (x.h2d) {
+            wait_flag(m, m->rec_ready, v, "weights ready");
+            MT_CK(cudaEventRecord(m->ev_wait_a[v], m->s_comp));
+            MT_CK(cudaStreamWaitEvent(m->s_comp, m->ev_ready[v], 0));
+            MT_CK(cudaEventRecord(m->ev_wait_b[v], m->s_comp));
+            m->rec_wait_timed[v] = 1;
+          }
+          wb = m->wbuf[x.buf];
+        }
+      }
+      uint8_t* gb = nullptr;
+      if (x.grads) {
+        if (x.prev_gbuf_user >= 0) {
+          wait_flag(m, m->rec_d2h, x.prev_gbuf_user, "gradient buffer evacuated");
+          MT_CK(cudaStreamWaitEvent(m->s_comp, m->ev_d2h[x.prev_gbuf_user], 0));
+        }
+        gb = m->gbuf[x.gbuf];
+      }
+      const TileLayout& lay = m->layouts[x.tile];
+      int rc = 0;
+      switch (x.kind) {
+        case kEmbedFwd:
+          rc = tmpl.embed_fwd(reinterpret_cast<bf16*>(wb + lay.slot("E").offset), x_fwd_loc(m, 0));
+          break;
+        case kLayerFwd: {
+          const int i = x.layer;
+          LayerActs a = m->store_acts ? m->stored[i] : m->acts;
+          a.x = x_fwd_loc(m, i);
+          rc = tmpl.forward(bind_layer(lay, wb), a, x_fwd_loc(m, i + 1), m->store_acts);
+          break;
+        }
+        case kHead:
+          rc = tmpl.head(bind_head(lay, wb), x_fwd_loc(m, D.L), dx_cur, bind_head(lay, gb));
+          MT_CK(cudaMemcpyAsync(m->pinned_scalars, m->ws.loss, sizeof(float), cudaMemcpyDeviceToHost, m->s_comp));
+          break;
+        case kRecompute: {
+          const int j = x.layer, s = j / m->K * m->K;
+          LayerActs a = m->acts;
+          a.x = (j == s) ? m->ckpt[s / m->K] : m->blockbuf[j - s - 1];
+          rc = tmpl.forward(bind_layer(lay, wb), a, m->blockbuf[j - s], false);
+          break;
+        }
+        case kLayerBwd: {
+          const int j = x.layer;
+          LayerActs a;
+          if (m->store_acts) {
+            a = m->stored[j];
+          } else {
+            const int s = j / m->K * m->K;
+            a = m->acts;
+            a.x = (j == s) ? m->ckpt[s / m->K] : m->blockbuf[j - s - 1];
+            rc = tmpl.forward(bind_layer(lay, wb), a, nullptr, true);  // internals only
+          }
+          rc |= tmpl.backward(bind_layer(lay, wb), a, dx_cur, dx_nxt, bind_layer(lay, gb));
+          std::swap(dx_cur, dx_nxt);
+          break;
+        }
+        case kEmbedBwd:
+          rc = tmpl.embed_bwd(dx_cur, reinterpret_cast<bf16*>(gb + lay.slot("E").offset));
+          break;
+      }
+      if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(cudaGetLastError())};
+      MT_CK(cudaPeekAtLastError());
+      if (x.buf >= 0 && !m->resident_mode) {
+        MT_CK(cudaEventRecord(m->ev_free[v], m->s_comp));
+        set_flag(m, m->rec_free, v);
+      }
+      if (x.grads) {
+        if (m->debug) launch_check_finite(reinterpret_cast<bf16*>(gb), lay.w_bytes / 2, m->ws.status, m->s_comp);
+        MT_CK(cudaEventRecord(m->ev_grads[v], m->s_comp));
+        {
+          std::lock_guard<std::mutex> g(m->mu);
+          m->d2h_q.push_back(v);
+        }
+        m->cv.notify_all();
+      }
+    }
+    MT_CK(cudaEventRecord(m->ev_t1, m->s_comp));
+    MT_CK(cudaMemcpyAsync(m->pinned_scalars + 1, m->ws.status, sizeof(int), cudaMemcpyDeviceToHost, m->s_comp));
+    wait_event(m, m->ev_t1, "compute stream");
+    MT_CK(cudaStreamSynchronize(m->s_comp));
+    const int status = *reinterpret_cast<int*>(m->pinned_scalars + 1);
+    // drain the gradient path and Adam
+    wait_flag(m, m->rec_d2h, m->last_grad_visit, "last gradient evacuation");
+    {
+      std::unique_lock<std::mutex> g(m->mu);
+      const bool ok = m->cv.wait_for(g, std::chrono::milliseconds(m->cfg.timeout_ms),
+                                     [&] { return m->acc_tiles_done >= m->n_grad_visits || m->abort_flag.load(); });
+      if (m->abort_flag) throw MtError{m->worker_code ? m->worker_code.load() : MT_EINTERNAL, m->worker_msg};
+      if (!ok) throw MtError{MT_ETIMEDOUT, "timed out waiting for gradient accumulation"};
+    }
+    if (!m->adam_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "timed out waiting for Adam"};
+    const auto adam_end = Clock::now();
+    check_abort(m);
+    MT_CK(cudaStreamSynchronize(m->s_h2d));
+    MT_CK(cudaStreamSynchronize(m->s_d2h));
+
+    // statistics
+    mt_step_stats& st = m->stats;
+    st = mt_step_stats{};
+    st.loss = m->pinned_scalars[0];
+    float f = 0.f;
+    MT_CK(cudaEventElapsedTime(&f, m->ev_t0, m->ev_t1));
+    st.gpu_compute_ms = f;
+    for (int v = 0; v < (int)m->visits.size(); ++v) {
+      if (m->rec_h2d_timed[v] && cudaEventElapsedTime(&f, m->ev_h2d_a[v], m->ev_h2d_b[v]) == cudaSuccess) st.h2d_ms += f;
+      if (m->rec_d2h_timed[v] && cudaEventElapsedTime(&f, m->ev_d2h_a[v], m->ev_d2h_b[v]) == cudaSuccess) st.d2h_ms += f;
+      if (m->rec_wait_timed[v] && cudaEventElapsedTime(&f, m->ev_wait_a[v], m->ev_wait_b[v]) == cudaSuccess)
+        st.wait_weights_ms += f;
+      const Visit& x = m->visits[v];
+      if (x.h2d && !m->resident_mode) st.h2d_bytes += m->layouts[x.tile].w_bytes;
+      if (x.grads) st.d2h_bytes += m->layouts[x.tile].w_bytes;
+    }
+    cudaGetLastError();
+    for (size_t i = 0; i + 1 < m->gemm_events.size(); i += 2) {
+      if (cudaEventElapsedTime(&f, m->gemm_events[i], m->gemm_events[i + 1]) == cudaSuccess) st.gemm_ms += f;
+      cudaEventDestroy(m->gemm_events[i]);
+      cudaEventDestroy(m->gemm_events[i + 1]);
+    }
+    for (double fl : m->gemm_event_flops) st.gemm_flops += fl;
+    m->gemm_events.clear();
+    m->gemm_event_flops.clear();
+    st.gemm_launches = m->ls.gemms;
+    st.kernel_launches = m->ls.kernels;
+    st.adam_ms = m->adam_us.load() / 1000.0;
+    st.adam_tail_ms = std::chrono::duration<double, std::milli>(adam_end - m->last_grads_landed).count();
+    const Flops fm = flop_model(D);
+    int n_fwd = 0;
+    for (const auto& x : m->visits)
+      if (x.kind == kLayerFwd || x.kind == kRecompute || (x.kind == kLayerBwd && !m->store_acts)) ++n_fwd;
+    st.flops_model = (int64_t)(3.0 * (D.L * fm.layer_fwd + fm.head_fwd));
+    st.flops_executed = (int64_t)(n_fwd * fm.layer_fwd + 2.0 * D.L * fm.layer_fwd + 3.0 * fm.head_fwd);
+    st.arena_high_water = m->arena_used;
+    if (status != 0) {
+      if (status == kStatusGemmTimeout)
+        throw MtError{MT_ETIMEDOUT, "a device-side bounded wait expired (GEMM pipeline)"};
+      if (status == kStatusNonFinite) {
+        m->nonfinite = true;
+      } else {
+        throw MtError{MT_EINVAL, "device status " + std::to_string(status) + " (index out of range)"};
+      }
+    }
+    m->step += 1;
+    st.step = m->step;
+    st.step_ms = ms_since(wall0);
+    if (loss_out) *loss_out = m->pinned_scalars[0];
+    if (m->nonfinite) {
+      m->err = "non-finite loss or gradient; Adam skipped from the first affected tile on";
+      code = MT_ENONFINITE;
+    }
+  } catch (const MtError& e) {
+    m->err = e.msg;
+    code = e.code;
+    // stop the workers' part of this step and bring the streams to rest
+    worker_fail(m, e);
+    cudaStreamSynchronize(m->s_comp);
+    cudaStreamSynchronize(m->s_h2d);
+    cudaStreamSynchronize(m->s_d2h);
+    m->adam_pool->wait_idle(m->cfg.timeout_ms);
+    if (code != MT_EINVAL) m->broken = true;
+  }
+  return code;
+}
+
+// ------------------------------------------------------------------ init helpers
+const char* validate(const mt_config& c) {
+  if (c.n_layers < 1 || c.d_model < 8 || c.n_heads < 1 || c.n_kv_heads < 1 || c.ffn < 8 || c.vocab < 8 ||
+      c.batch < 1 || c.seq < 1)
+    return "dimensions must be positive";
+  if (c.head_dim != 64 && c.head_dim != 128) return "head_dim must be 64 or 128";
+  if (c.n_heads % c.n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (c.d_model % 8 || c.ffn % 8 || c.vocab % 8) return "d_model, ffn and vocab must be multiples of 8";
+  if (((int64_t)c.batch * c.seq) % 8) return "batch * seq must be a multiple of 8";
+  if (c.ckpt_every < 1) return "ckpt_every must be >= 1";
+  if (!(c.rms_eps > 0) || !(c.rope_theta > 0) || !(c.lr >= 0) || !(c.beta1 >= 0 && c.beta1 < 1) ||
+      !(c.beta2 >= 0 && c.beta2 < 1) || !(c.adam_eps >= 0))
+    return "bad hyper-parameter";
+  return nullptr;
+}
+
+mt_config with_defaults(const mt_config& in) {
+  mt_config c = in;
+  if (c.n_adam_threads <= 0) c.n_adam_threads = std::max(1u, std::thread::hardware_concurrency());
+  if (c.n_pack_threads <= 0) c.n_pack_threads = 4;
+  if (c.n_grad_slabs <= 0) c.n_grad_slabs = 12;
+  if (c.grad_slab_bytes <= 0) c.grad_slab_bytes = 64ll << 20;
+  if (c.stage_bytes <= 0) c.stage_bytes = 64ll << 20;
+  if (c.timeout_ms <= 0) c.timeout_ms = 60000;
+  c.grad_slab_bytes = align_up(c.grad_slab_bytes, kPage);
+  c.stage_bytes = align_up(c.stage_bytes, kPage);
+  return c;
+}
+
+// Lay out the device arena; with base == nullptr only the byte count is computed.
+int64_t plan_arena(mt_model* m, uint8_t* base) {
+  const Dims& D = m->D;
+  Plan P;
+  auto at = [&](int64_t bytes) -> uint8_t* {
+    const int64_t off = P.add(bytes);
+    return base ? base + off : nullptr;
+  };
+  const int64_t xb = D.T * D.d * 2;
+  for (int b = 0; b < 2; ++b) m->wbuf[b] = at(m->max_w_bytes);
+  for (int b = 0; b < 2; ++b) m->gbuf[b] = at(m->max_w_bytes);
+  if (m->resident_mode) {
+    int64_t tot = 0;
+    m->resident_off.assign(m->layouts.size(), 0);
+    for (size_t t = 0; t < m->layouts.size(); ++t) {
+      m->resident_off[t] = tot;
+      tot += m->layouts[t].w_bytes;
+    }
+    m->resident = at(tot);
+  }
+  const ActsSizes as = acts_sizes(D);
+  m->ckpt.clear();
+  m->blockbuf.clear();
+  m->stored.clear();
+  if (m->store_acts) {
+    for (int i = 0; i < D.L; ++i) {
+      uint8_t* x = at(xb);
+      uint8_t* p = at(as.total);
+      m->stored.push_back(base ? carve_acts(p, D, reinterpret_cast<bf16*>(x)) : LayerActs{});
+    }
+  } else {
+    for (int i = 0; i < (D.L + m->K - 1) / m->K; ++i) m->ckpt.push_back(reinterpret_cast<bf16*>(at(xb)));
+    for (int i = 0; i < m->K - 1; ++i) m->blockbuf.push_back(reinterpret_cast<bf16*>(at(xb)));
+    uint8_t* p = at(as.total);
+    if (base) m->acts = carve_acts(p, D, nullptr);
+  }
+  for (int b = 0; b < 2; ++b) m->xtmp[b] = reinterpret_cast<bf16*>(at(xb));
+  uint8_t* wsbase = base ? base + P.total : nullptr;
+  Plan Pw;
+  Workspace w = carve_ws(wsbase, D, Pw);
+  P.total += Pw.total;
+  if (base) m->ws = w;
+  return P.total;
+}
+
+void build_layouts(mt_model* m) {
+  m->layouts.clear();
+  m->layouts.push_back(make_layout(kTileEmbed, m->D));
+  for (int i = 0; i < m->D.L; ++i) m->layouts.push_back(make_layout(kTileLayer, m->D));
+  m->layouts.push_back(make_layout(kTileHead, m->D));
+  m->max_w_bytes = 0;
+  for (const auto& l : m->layouts) m->max_w_bytes = std::max(m->max_w_bytes, l.w_bytes);
+}
+
+void parallel_zero(uint8_t* p, int64_t n, int nthreads) {
+  std::vector<std::thread> th;
+  const int64_t piece = align_up((n + nthreads - 1) / nthreads, kPage);
+  for (int64_t off = 0; off < n; off += piece) {
+    const int64_t c = std::min(piece, n - off);
+    th.emplace_back([=] { std::memset(p + off, 0, (size_t)c); });
+  }
+  for (auto& t : th) t.join();
+}
+
+void destroy(mt_model* m) {
+  if (!m) return;
+  {
+    std::lock_guard<std::mutex> g(m->mu);
+    m->stop_threads = true;
+    m->abort_flag = true;
+  }
+  m->cv.notify_all();
+  if (m->loader.joinable()) m->loader.join();
+  if (m->d2h.joinable()) m->d2h.join();
+  if (m->accum.joinable()) m->accum.join();
+  m->adam_pool.reset();
+  m->pack_pool.reset();
+  if (m->s_comp) cudaStreamSynchronize(m->s_comp);
+  if (m->s_h2d) cudaStreamSynchronize(m->s_h2d);
+  if (m->s_d2h) cudaStreamSynchronize(m->s_d2h);
+  auto kill = [](std::vector<cudaEvent_t>& v) {
+    for (auto e : v)
+      if (e) cudaEventDestroy(e);
+    v.clear();
+  };
+  kill(m->ev_ready);
+  kill(m->ev_free);
+  kill(m->ev_grads);
+  kill(m->ev_d2h);
+  kill(m->ev_wait_a);
+  kill(m->ev_wait_b);
+  kill(m->ev_h2d_a);
+  kill(m->ev_h2d_b);
+  kill(m->ev_d2h_a);
+  kill(m->ev_d2h_b);
+  kill(m->ev_slab);
+  kill(m->gemm_events);
+  for (auto& e : m->ev_stage)
+    if (e) cudaEventDestroy(e);
+  if (m->ev_t0) cudaEventDestroy(m->ev_t0);
+  if (m->ev_t1) cudaEventDestroy(m->ev_t1);
+  for (auto& s : m->stage)
+    if (s) cudaFreeHost(s);
+  for (auto s : m->slabs)
+    if (s) cudaFreeHost(s);
+  if (m->pinned_scalars) cudaFreeHost(m->pinned_scalars);
+  if (m->pinned_tok) cudaFreeHost(m->pinned_tok);
+  for (auto t : m->tiles) std::free(t);
+  delete m;
+}
+
+void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_bytes, void* sc, void* sh, void* sd) {
+  if (const char* e = validate(cin)) throw MtError{MT_EINVAL, e};
+  m->cfg = with_defaults(cin);
+  m->D = dims_of(m->cfg);
+  m->K = m->cfg.ckpt_every;
+  m->resident_mode = m->cfg.flags & MT_RESIDENT;
+  m->store_acts = m->cfg.flags & MT_STORE_ACTS;
+  m->single_buffer = m->cfg.flags & MT_NO_DOUBLE_BUFFER;
+  m->debug = m->cfg.flags & MT_DEBUG_CHECKS;
+  m->time_kernels = m->cfg.flags & MT_TIME_KERNELS;
+  if (!sc || !sh || !sd || sc == sh || sc == sd || sh == sd)
+    throw MtError{MT_EINVAL, "three distinct CUDA streams are required"};
+  m->s_comp = static_cast<cudaStream_t>(sc);
+  m->s_h2d = static_cast<cudaStream_t>(sh);
+  m->s_d2h = static_cast<cudaStream_t>(sd);
+  build_layouts(m);
+  const int64_t need = plan_arena(m, nullptr);
+  if (!arena || (reinterpret_cast<uintptr_t>(arena) & 255)) throw MtError{MT_EINVAL, "device arena must be 256-byte aligned"};
+  if ((int64_t)arena_bytes < need)
+    throw MtError{MT_ENOMEM, "device arena too small: need " + std::to_string(need) + " bytes"};
+  m->arena = static_cast<uint8_t*>(arena);
+  m->arena_bytes = arena_bytes;
+  m->arena_used = plan_arena(m, m->arena);
+
+  // visit schedule
+  m->visits = build_schedule(m->D.L, m->K, m->store_acts, m->single_buffer);
+  if (m->resident_mode)
+    for (auto& x : m->visits) x.h2d = false;
+  const int nv = (int)m->visits.size();
+  m->n_grad_visits = 0;
+  for (int v = 0; v < nv; ++v)
+    if (m->visits[v].grads) {
+      ++m->n_grad_visits;
+      m->last_grad_visit = v;
+    }
+  auto mk = [&](std::vector<cudaEvent_t>& vec, bool timing) {
+    vec.assign(nv, nullptr);
+    for (auto& e : vec) MT_CK(cudaEventCreateWithFlags(&e, timing ? cudaEventDefault : cudaEventDisableTiming));
+  };
+  mk(m->ev_ready, false);
+  mk(m->ev_free, false);
+  mk(m->ev_grads, false);
+  mk(m->ev_d2h, false);
+  mk(m->ev_wait_a, true);
+  mk(m->ev_wait_b, true);
+  mk(m->ev_h2d_a, true);
+  mk(m->ev_h2d_b, true);
+  mk(m->ev_d2h_a, true);
+  mk(m->ev_d2h_b, true);
+  for (auto& e : m->ev_stage) MT_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  MT_CK(cudaEventCreate(&m->ev_t0));
+  MT_CK(cudaEventCreate(&m->ev_t1));
+  m->rec_ready.assign(nv, 0);
+  m->rec_free.assign(nv, 0);
+  m->rec_d2h.assign(nv, 0);
+  m->rec_h2d_timed.assign(nv, 0);
+  m->rec_d2h_timed.assign(nv, 0);
+  m->rec_wait_timed.assign(nv, 0);
+
+  // host tiles: pageable, page aligned, zeroed (first touch spread over threads)
+  m->tiles.assign(m->layouts.size(), nullptr);
+  m->w_loaded.assign(m->layouts.size(), 0);
+  for (size_t t = 0; t < m->layouts.size(); ++t) {
+    m->tiles[t] = static_cast<uint8_t*>(std::aligned_alloc(kPage, (size_t)m->layouts[t].tile_bytes));
+    if (!m->tiles[t]) throw MtError{MT_ENOMEM, "host tile allocation failed"};
+    parallel_zero(m->tiles[t], m->layouts[t].tile_bytes, std::min(16, m->cfg.n_adam_threads));
+  }
+  // pinned staging, slabs, scalars, token buffers
+  m->stage_bytes = std::min<int64_t>(m->cfg.stage_bytes, m->max_w_bytes);
+  for (auto& s : m->stage)
+    if (cudaHostAlloc(reinterpret_cast<void**>(&s), (size_t)m->stage_bytes, cudaHostAllocDefault) != cudaSuccess)
+      throw MtError{MT_ENOMEM, "pinned staging allocation failed"};
+  m->slab_bytes = std::min<int64_t>(m->cfg.grad_slab_bytes, m->max_w_bytes);
+  m->slabs.assign(m->cfg.n_grad_slabs, nullptr);
+  m->ev_slab.assign(m->cfg.n_grad_slabs, nullptr);
+  for (int i = 0; i < m->cfg.n_grad_slabs; ++i) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&m->slabs[i]), (size_t)m->slab_bytes, cudaHostAllocDefault) !=
+        cudaSuccess)
+      throw MtError{MT_ENOMEM, "pinned gradient slab allocation failed"};
+    MT_CK(cudaEventCreateWithFlags(&m->ev_slab[i], cudaEventDisableTiming));
+    m->free_slabs.push_back(i);
+  }
+  MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_scalars), 256, cudaHostAllocDefault));
+  const size_t ntok = (size_t)(3 * m->D.T + m->D.V + 1);
+  MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_tok), ntok * sizeof(int32_t), cudaHostAllocDefault));
+
+  // RoPE tables (rotate-half; angle = s * theta^(-2i/hd)), computed in double
+  {
+    const int half = m->D.hd / 2;
+    std::vector<float> c((size_t)m->D.S * half), s((size_t)m->D.S * half);
+    for (int p = 0; p < m->D.S; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * std::pow((double)m->cfg.rope_theta, -2.0 * i / m->D.hd);
+        c[(size_t)p * half + i] = (float)std::cos(ang);
+        s[(size_t)p * half + i] = (float)std::sin(ang);
+      }
+    MT_CK(cudaMemcpy(m->ws.rope_cos, c.data(), c.size() * 4, cudaMemcpyHostToDevice));
+    MT_CK(cudaMemcpy(m->ws.rope_sin, s.data(), s.size() * 4, cudaMemcpyHostToDevice));
+  }
+  // zero the gradient buffers once (alignment padding is never written)
+  MT_CK(cudaMemset(m->gbuf[0], 0, (size_t)m->max_w_bytes));
+  MT_CK(cudaMemset(m->gbuf[1], 0, (size_t)m->max_w_bytes));
+  MT_CK(cudaDeviceSynchronize());
+
+  m->adam_pool.reset(new Pool(m->cfg.n_adam_threads));
+  m->pack_pool.reset(new Pool(m->cfg.n_pack_threads));
+  m->loader = std::thread(loader_main, m);
+  m->d2h = std::thread(d2h_main, m);
+  m->accum = std::thread(accum_main, m);
+}
+
+}  // namespace
+}  // namespace mt
+
+// ====================================================================== C-ABI
+using mt::MtError;
+
+extern "C" {
+
+int64_t mt_required_device_bytes(const mt_config* cfg) {
+  if (!cfg) return MT_EINVAL;
+  if (const char* e = mt::validate(*cfg)) {
+    mt::g_init_error = e;
+    return MT_EINVAL;
+  }
+  mt_model tmp;
+  tmp.cfg = mt::with_defaults(*cfg);
+  tmp.D = mt::dims_of(tmp.cfg);
+  tmp.K = tmp.cfg.ckpt_every;
+  tmp.resident_mode = tmp.cfg.flags & MT_RESIDENT;
+  tmp.store_acts = tmp.cfg.flags & MT_STORE_ACTS;
+  mt::build_layouts(&tmp);
+  return mt::plan_arena(&tmp, nullptr);
+}
+
+int mt_init_model(const mt_config* cfg, void* device_arena, size_t arena_bytes, void* stream_comp, void* stream_h2d,
+                  void* stream_d2h, mt_model** out) {
+  if (!cfg || !out) {
+    mt::g_init_error = "null argument";
+    return MT_EINVAL;
+  }
+  *out = nullptr;
+  mt_model* m = new (std::nothrow) mt_model();
+  if (!m) return MT_ENOMEM;
+  try {
+    mt::init_model(m, *cfg, device_arena, arena_bytes, stream_comp, stream_h2d, stream_d2h);
+  } catch (const MtError& e) {
+    mt::g_init_error = e.msg;
+    mt::destroy(m);
+    return e.code;
+  } catch (const std::exception& e) {
+    mt::g_init_error = e.what();
+    mt::destroy(m);
+    return MT_EINTERNAL;
+  }
+  *out = m;
+  return MT_OK;
+}
+
+int mt_tile_count(const mt_model* m) { return m ? (int)m->layouts.size() : MT_EINVAL; }
+
+int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out) {
+  if (!m || !out || tile < 0 || tile >= (int)m->layouts.size()) return MT_EINVAL;
+  const auto& L = m->layouts[tile];
+  std::memset(out, 0, sizeof(*out));
+  out->kind = L.kind;
+  out->n_tensors = (int)L.tensors.size();
+  out->n_params = L.n_params;
+  out->w_bytes = L.w_bytes;
+  out->tile_bytes = L.tile_bytes;
+  for (size_t i = 0; i < L.tensors.size() && i < 8; ++i) {
+    const auto& t = L.tensors[i];
+    std::strncpy(out->tensors[i].name, t.name.c_str(), 15);
+    out->tensors[i].ndim = t.ndim;
+    out->tensors[i].shape[0] = t.shape[0];
+    out->tensors[i].shape[1] = t.shape[1];
+    out->tensors[i].offset = t.offset;
+    out->tensors[i].numel = t.numel;
+  }
+  return MT_OK;
+}
+
+static int part_span(mt_model* m, int tile, int part, size_t nbytes, int64_t* off, int64_t* n) {
+  if (!m || tile < 0 || tile >= (int)m->layouts.size()) {
+    if (m) m->err = "tile index out of range";
+    return MT_EINVAL;
+  }
+  const auto& L = m->layouts[tile];
+  switch (part) {
+    case MT_PART_W: *off = L.off_w; *n = L.w_bytes; break;
+    case MT_PART_G: *off = L.off_g; *n = L.w_bytes; break;
+    case MT_PART_M: *off = L.off_m; *n = L.mv_bytes; break;
+    case MT_PART_V: *off = L.off_v; *n = L.mv_bytes; break;
+    default: m->err = "bad part"; return MT_EINVAL;
+  }
+  if ((int64_t)nbytes != *n) {
+    m->err = "nbytes must equal the part size " + std::to_string(*n);
+    return MT_EINVAL;
+  }
+  return MT_OK;
+}
+
+int mt_load_layer_tile(mt_model* m, int tile, int part, const void* src, size_t nbytes) {
+  int64_t off, n;
+  if (int rc = part_span(m, tile, part, nbytes, &off, &n)) return rc;
+  if (!src) {
+    m->err = "null source";
+    return MT_EINVAL;
+  }
+  std::memcpy(m->tiles[tile] + off, src, (size_t)n);
+  if (part == MT_PART_W) m->w_loaded[tile] = 1;
+  return MT_OK;
+}
+
+int mt_get_layer_tile(mt_model* m, int tile, int part, void* dst, size_t nbytes) {
+  int64_t off, n;
+  if (int rc = part_span(m, tile, part, nbytes, &off, &n)) return rc;
+  if (!dst) {
+    m->err = "null destination";
+    return MT_EINVAL;
+  }
+  std::memcpy(dst, m->tiles[tile] + off, (size_t)n);
+  return MT_OK;
+}
+
+int mt_train_step(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out) {
+  if (!m || !tokens) return MT_EINVAL;
+  return mt::run_step(m, tokens, nullptr, n_tokens, loss_out);
+}
+
+int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n_tokens, float* loss_out) {
+  if (!m || !tokens_dev) return MT_EINVAL;
+  return mt::run_step(m, nullptr, tokens_dev, n_tokens, loss_out);
+}
+
+int mt_get_step_stats(const mt_model* m, mt_step_stats* out) {
+  if (!m || !out) return MT_EINVAL;
+  *out = m->stats;
+  return MT_OK;
+}
+
+int64_t mt_get_step(const mt_model* m) { return m ? m->step : MT_EINVAL; }
+
+int mt_set_step(mt_model* m, int64_t step) {
+  if (!m || step < 0) return MT_EINVAL;
+  m->step = step;
+  return MT_OK;
+}
+
+const char* mt_last_error(const mt_model* m) { return m ? m->err.c_str() : mt::g_init_error.c_str(); }
+
+void mt_free(mt_model* m) { mt::destroy(m); }
+
+}  // extern "C"

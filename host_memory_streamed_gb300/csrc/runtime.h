@@ -1,0 +1,146 @@
+// Host-side structures of the layer-streamed training runtime.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/mt.h"
+#include "kernels.h"
+
+namespace mt {
+
+constexpr int64_t kPage = 4096;     // tile section alignment (single-burst DMA of page-aligned blocks)
+constexpr int64_t kTensorAlign = 256;  // sub-tensor alignment inside a section
+
+inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+struct AdamHyper {
+  float lr, beta1, beta2, eps, weight_decay;
+  int64_t step;
+};
+void adam_range(uint16_t* w, const uint16_t* g, float* m, float* v, size_t n, const AdamHyper& h);
+bool copy_grad_check_finite(uint16_t* dst, const uint16_t* src, size_t n);
+
+// ------------------------------------------------------------------ tiles
+enum TileKind { kTileEmbed = 0, kTileLayer = 1, kTileHead = 2 };
+
+struct TensorSlot {
+  std::string name;
+  int ndim;
+  int64_t shape[2];
+  int64_t offset;  // bytes inside the W section
+  int64_t numel;
+};
+
+struct TileLayout {
+  TileKind kind;
+  std::vector<TensorSlot> tensors;
+  int64_t n_params = 0;
+  int64_t w_bytes = 0;  // W section bytes (page multiple); G section identical
+  int64_t mv_bytes = 0; // M (and V) section bytes (page multiple)
+  int64_t off_w = 0, off_g = 0, off_m = 0, off_v = 0;
+  int64_t tile_bytes = 0;
+  const TensorSlot& slot(const char* n) const;
+};
+
+struct Dims {
+  int L, d, Hq, Hkv, hd, f, V, B, S;
+  long T;       // B*S
+  int Dq;       // Hq*hd
+  int Dqkv;     // (Hq + 2 Hkv) * hd
+};
+
+Dims dims_of(const mt_config& c);
+TileLayout make_layout(TileKind kind, const Dims& d);
+
+// ------------------------------------------------------------------ device workspace
+// Bound views of one layer tile (weights in a streamed buffer, or gradients
+// in a gradient buffer): pointers only, no storage (the "Bind" of a template).
+struct LayerView {
+  bf16 *g1, *wqkv, *wo, *g2, *wgu, *wd;
+};
+struct HeadView {
+  bf16 *gf, *wh;
+};
+LayerView bind_layer(const TileLayout& lay, void* base);
+HeadView bind_head(const TileLayout& lay, void* base);
+
+// Activations of one layer pass.
+struct LayerActs {
+  bf16* x;       // input (not owned: checkpoint or block buffer)
+  bf16* n1;
+  float* rstd1;
+  bf16* qkv;
+  bf16* o;
+  float* lse;
+  bf16* h;
+  bf16* n2;
+  float* rstd2;
+  bf16* gu;      // may be null in plain forward
+  bf16* a;
+};
+
+struct Workspace {
+  // backward scratch
+  bf16 *dx_a, *dx_b;    // ping-pong dx between layers
+  bf16 *dh, *da, *dgu, *dn, *dout, *dqkv;
+  float* delta;
+  float* dg_partial;
+  bf16 *tr_y, *tr_x, *tr_w;  // transposes: dY^T, X^T, W^T
+  // head
+  bf16* nf;
+  float* rstd_f;
+  float* z;        // [chunk, V] FP32 logits
+  bf16* dz;        // [chunk, V]
+  bf16* dnf;       // [T, d]
+  float* dwh_f32;  // [V, d]
+  float* loss_rows;
+  float* loss;     // [1]
+  // tokens
+  int32_t* inp;    // [T]
+  int32_t* tgt;    // [T]
+  int32_t* emb_off;  // [V+1]
+  int32_t* emb_pos;  // [T]
+  int32_t* tokens_dev;  // [B, S+1] (device-token entry point)
+  float *rope_cos, *rope_sin;  // [S, hd/2]
+  int* status;
+  long head_chunk;  // rows per LM-head chunk
+};
+
+// Counts what the launch sequences issued (for the step statistics).
+struct LaunchStats {
+  int64_t kernels = 0;
+  int64_t gemms = 0;
+  double gemm_flops = 0;
+  double gemm_ms = 0;
+  bool time_gemms = false;
+  std::vector<cudaEvent_t>* gemm_events = nullptr;  // pairs
+  std::vector<double>* gemm_event_flops = nullptr;
+};
+
+// The stateless layer template: the kernel sequences of one decoder layer,
+// parameterised only by bound views and workspace pointers.
+struct LayerTemplate {
+  Dims dm;
+  float eps;
+  cudaStream_t s;
+  const Workspace* ws;
+  LaunchStats* stats;
+
+  int gemm(const GemmArgs& g) const;
+  // x -> x_out (x_out == nullptr: stop after the MLP activation).  keep_gu: also
+  // store the gate/up pre-activations (needed by backward).
+  int forward(const LayerView& w, LayerActs& a, bf16* x_out, bool keep_gu) const;
+  // Given the layer's forward activations and dx_out, write dx_in and the
+  // layer's gradients into gv (BF16, tile layout).
+  int backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, bf16* dx_in, const LayerView& gv) const;
+  // Final norm + LM head + cross-entropy, forward and backward in chunks.
+  int head(const HeadView& w, const bf16* x_L, bf16* dx_L, const HeadView& gv) const;
+  int embed_fwd(const bf16* E, bf16* x0) const;
+  int embed_bwd(const bf16* dx0, bf16* dE) const;
+};
+
+}  // namespace mt

@@ -50,6 +50,66 @@ int mt_op_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M
                const float* rope_cos, const float* rope_sin, int32_t rope_cols, int32_t head_dim, int32_t seq,
                int32_t* status, void* stream);
 
+
+/*
+ * Causal grouped-query attention forward (flash style, one pass over keys).
+ * qkv: [batch*seq, ldqkv] BF16 rows (token t = b*seq + s) holding n_heads query
+ * heads, then n_kv_heads key heads, then n_kv_heads value heads, head_dim
+ * columns each (q, k already rotated).  Query head h reads kv head
+ * h*n_kv_heads/n_heads.  o: [batch*seq, ldo] BF16; lse: FP32
+ * [batch, n_heads, seq] natural-log log-sum-exp of each score row (scores
+ * scaled by 1/sqrt(head_dim)).  head_dim 64 or 128; n_heads % n_kv_heads == 0.
+ */
+int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, void* o, int64_t ldo, float* lse, void* stream);
+
+/*
+ * Attention backward: given o, lse from the forward and dout (layout of o),
+ * writes dqkv (layout of qkv) = gradients w.r.t. q, k, v.  delta: FP32 scratch
+ * [batch, n_heads, seq] (overwritten).  When rope_cos/rope_sin ([seq,
+ * head_dim/2] FP32) are given, dq and dk are passed back through the inverse
+ * rotate-half rotation (gradient w.r.t. the unrotated projections).
+ * Deterministic: no atomics, fixed accumulation order.
+ */
+int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, const void* o, int64_t ldo, const float* lse,
+                        const void* dout, float* delta, void* dqkv, const float* rope_cos, const float* rope_sin,
+                        void* stream);
+
+/* y = x * rsqrt(mean(x^2) + eps) * g over rows of d (d % 8 == 0); rstd: FP32 [rows]. */
+int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_t rows, int32_t d, float eps,
+                      void* stream);
+/* FP32 scratch elements mt_op_rmsnorm_bwd needs. */
+int64_t mt_op_rmsnorm_bwd_scratch_floats(int64_t rows, int32_t d);
+/*
+ * dx = dres + d(rmsnorm)/dx^T dy (dres may be NULL); dg [d] BF16 = sum over rows
+ * of dy * x * rstd, reduced in a fixed order.
+ */
+int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float* rstd, const void* dres, void* dx,
+                      void* dg, float* scratch, int64_t rows, int32_t d, void* stream);
+/* SwiGLU backward on interleaved (gate, up) columns: gu, dgu [rows, 2f]; da [rows, f]. */
+int mt_op_swiglu_bwd(const void* da, const void* gu, void* dgu, int64_t rows, int32_t f, void* stream);
+/* dst[c, r] = src[r, c] (BF16). */
+int mt_op_transpose(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd,
+                    void* stream);
+/*
+ * Row-wise cross-entropy of FP32 logits z [rows, vocab] against tgt [rows]:
+ * loss_rows[r] = logsumexp(z_r) - z_r[tgt_r]; dz (BF16) = (softmax(z_r) -
+ * onehot(tgt_r)) * inv_n.  An out-of-range target sets *status.
+ */
+int mt_op_cross_entropy(const float* z, int64_t rows, int32_t vocab, const int32_t* tgt, float inv_n, void* dz,
+                        float* loss_rows, int32_t* status, void* stream);
+/* x[t] = E[tok[t]] ([V, d] BF16); out-of-range ids give zeros and set *status. */
+int mt_op_embedding_fwd(const int32_t* tok, const void* E, void* x, int64_t T, int32_t d, int32_t V,
+                        int32_t* status, void* stream);
+/*
+ * dE[v] = sum of dx[positions[k]] for k in [row_offsets[v], row_offsets[v+1])
+ * in ascending k, for every v < V (rows with no token become zero): a
+ * deterministic scatter-add given the token positions grouped by id.
+ */
+int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, const void* dx, void* dE, int32_t V,
+                        int32_t d, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,120 @@
+"""Host-side checks of libmt.so that need no GPU: the library loads and exports
+every symbol the headers declare, the CPU Adam matches the oracle, the tile
+layout keeps the 12-bytes-per-parameter accounting, and bad configurations are
+rejected with MT_EINVAL."""
+import ctypes as C
+import os
+
+import pytest
+import torch
+
+import mt_inputs
+import oracle
+from oracle import OracleConfig
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from host_memory_streamed_gb300 import _lib, build
+    build.build()
+    return _lib.lib()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from host_memory_streamed_gb300 import _lib
+    names = _lib.declared_symbols()
+    assert "mt_init_model" in names and "mt_train_step" in names and "mt_op_gemm" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def _cfg(shape, **kw):
+    from host_memory_streamed_gb300 import _lib
+    c = _lib.MtConfig()
+    for k in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "batch", "seq",
+              "ckpt_every", "rms_eps", "rope_theta", "lr", "beta1", "beta2", "adam_eps", "weight_decay"):
+        setattr(c, k, getattr(shape, k))
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("name", ["tiny", "1.3b", "14b", "70b", "7b-512k"])
+def test_required_device_bytes_positive_and_bounded(lib, name):
+    s = mt_inputs.PRESETS[name]
+    need = lib.mt_required_device_bytes(C.byref(_cfg(s)))
+    assert need > 0
+    # the device footprint is bounded by activations + two tile buffers, far below the model
+    assert need < 280e9
+    if name == "14b":
+        assert need < 80e9
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=690), dict(ckpt_every=0),
+                                 dict(vocab=0), dict(batch=0), dict(seq=3, batch=1)])
+def test_bad_config_rejected(lib, bad):
+    s = mt_inputs.PRESETS["tiny"]
+    assert lib.mt_required_device_bytes(C.byref(_cfg(s, **bad))) == -1
+    assert lib.mt_last_error(None)
+
+
+def _adam_ref(w, g, m, v, t, cfg):
+    return oracle.adam_update(w, g, m, v, t, cfg)
+
+
+@pytest.mark.parametrize("t", [1, 2, 7])
+def test_cpu_adam_matches_oracle(lib, t):
+    cfg = OracleConfig.from_shape(mt_inputs.PRESETS["tiny"])
+    gen = torch.Generator().manual_seed(10 + t)
+    n = 200003
+    w = (torch.randn(n, generator=gen) * 0.05).to(torch.bfloat16)
+    g = (torch.randn(n, generator=gen) * torch.exp(torch.randn(n, generator=gen) * 3) * 1e-4).to(torch.bfloat16)
+    g[::97] = 0.0
+    m = (torch.randn(n, generator=gen) * 1e-5).float() if t > 1 else torch.zeros(n)
+    v = (torch.rand(n, generator=gen) * 1e-9).float() if t > 1 else torch.zeros(n)
+    wb, mb, vb = w.clone(), m.clone(), v.clone()
+    rc = lib.mt_adam_host(wb.view(torch.int16).data_ptr(), g.view(torch.int16).data_ptr(), mb.data_ptr(),
+                          vb.data_ptr(), n, t, cfg.lr, cfg.beta1, cfg.beta2, cfg.adam_eps, cfg.weight_decay)
+    assert rc == 0
+    we, me, ve = _adam_ref(w, g, m, v, t, cfg)
+    diff = (wb.double() - we).abs()
+    from tests.parity import bf16_ulp
+    assert torch.all(diff <= bf16_ulp(we)), int((diff > bf16_ulp(we)).sum())
+    assert torch.allclose(mb.double(), me, rtol=2e-6, atol=0)
+    assert torch.allclose(vb.double(), ve, rtol=2e-6, atol=0)
+    # zero gradient at t = 1 leaves the weight untouched
+    if t == 1:
+        assert torch.equal(wb[::97], w[::97])
+
+
+def test_cpu_adam_rejects_bad_step(lib):
+    x = torch.zeros(4, dtype=torch.int16)
+    f = torch.zeros(4)
+    assert lib.mt_adam_host(x.data_ptr(), x.data_ptr(), f.data_ptr(), f.data_ptr(), 4, 0, 1e-4, 0.9, 0.95, 1e-8,
+                            0.0) != 0
+
+
+def test_tile_layout_accounting():
+    """Layer tiles hold W (BF16) | G (BF16) | M (FP32) | V (FP32), each section
+    page aligned: 12 bytes per parameter plus padding (the pages' 12P
+    accounting, 70B -> at least 840 GB)."""
+    for name in ("1.3b", "14b", "70b"):
+        s = mt_inputs.PRESETS[name]
+        shapes = mt_inputs.layer_tensor_shapes(s)
+        n = sum(int(torch.tensor(v).prod()) for v in shapes.values())
+        per_layer = 12 * n
+        total = s.n_layers * per_layer + 12 * (2 * s.vocab * s.d_model + s.d_model)
+        if name == "70b":
+            assert total >= 840e9
+        if name == "14b":
+            assert abs(n - 275261440) == 0
+
+
+def test_header_documents_every_entry_point():
+    """Every declared function has a comment block in its header."""
+    from host_memory_streamed_gb300 import _lib
+    txt = "".join(open(os.path.join(ROOT, "include", f)).read() for f in os.listdir(os.path.join(ROOT, "include")))
+    for n in _lib.declared_symbols():
+        assert n in txt

@@ -1,0 +1,150 @@
+"""GPU training step through the C-ABI against the CPU oracle, and the
+schedule's bit-exact self-consistency (streamed == resident, recompute ==
+stored activations, K=1 == K=2 == no double buffer, repeat runs, resume)."""
+import pytest
+import torch
+
+import mt_inputs
+import oracle
+from oracle import OracleConfig
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+hms = pytest.importorskip("host_memory_streamed_gb300")
+
+
+def _run(shape, steps=1, flags=0, jitter=0.1, **kw):
+    m = hms.StreamedDecoder.from_shape(shape, flags=flags, **kw)
+    params = mt_inputs.model_weights(shape, gain_jitter=jitter)
+    m.load_weights(params)
+    out = {"params0": params, "loss": [], "w": [], "g": [], "mv": []}
+    for n in range(1, steps + 1):
+        out["loss"].append(m.train_step(mt_inputs.step_tokens(shape, n)))
+        out["w"].append(m.weights())
+        out["g"].append(m.grads())
+        out["mv"].append(m.moments())
+    out["stats"] = m.stats()
+    m.close()
+    return out
+
+
+def _equal_trees(a, b):
+    for (n, x), (_, y) in zip(parity.flat_named(a), parity.flat_named(b)):
+        assert torch.equal(x, y), n
+
+
+SHAPES = {
+    "tiny": mt_inputs.PRESETS["tiny"],
+    # GQA, head_dim 128, ragged sequence (not a multiple of 64/128), 3 layers
+    "gqa128": mt_inputs.PRESETS["tiny"].with_(n_layers=3, d_model=256, n_heads=4, n_kv_heads=2, head_dim=128,
+                                              ffn=344, vocab=520, batch=2, seq=180),
+}
+
+
+@pytest.mark.parametrize("name", ["tiny", "gqa128"])
+def test_step_matches_oracle(name):
+    s = SHAPES[name]
+    cfg = OracleConfig.from_shape(s)
+    r = _run(s)
+    tokens = mt_inputs.step_tokens(s, 1)
+    loss, grads = oracle.model_loss_and_grads(r["params0"], tokens, cfg)
+    assert abs(r["loss"][0] - loss) <= parity.LOSS_RTOL * abs(loss)
+    parity.assert_grads_close(r["g"][0], grads)
+    m, v = r["mv"][0]
+    parity.assert_adam_matches(r["w"][0], r["params0"], r["g"][0], m, v, 1, cfg)
+    ok, total, excluded, worst = parity.adam_vs_oracle_grads(r["w"][0], r["params0"], grads, 1, cfg)
+    assert ok >= 0.99 * total, (ok, total, worst[:5])
+
+
+def test_three_step_loss_trajectory_matches_oracle():
+    s = SHAPES["tiny"]
+    cfg = OracleConfig.from_shape(s)
+    r = _run(s, steps=3)
+    params, state = r["params0"], None
+    for n in range(1, 4):
+        loss, grads, params, state = oracle.train_step(params, state, mt_inputs.step_tokens(s, n), n, cfg)
+        assert abs(r["loss"][n - 1] - loss) <= parity.LOSS_RTOL * abs(loss), (n, r["loss"][n - 1], loss)
+        parity.assert_grads_close(r["g"][n - 1], grads)
+
+
+def test_streamed_equals_resident_bitexact():
+    s = SHAPES["gqa128"]
+    a = _run(s, steps=2)
+    b = _run(s, steps=2, flags=hms.MT_RESIDENT)
+    assert a["loss"] == b["loss"]
+    _equal_trees(a["w"][-1], b["w"][-1])
+    _equal_trees(a["g"][-1], b["g"][-1])
+
+
+def test_recompute_equals_stored_activations_bitexact():
+    s = SHAPES["gqa128"]
+    a = _run(s, steps=2)
+    b = _run(s, steps=2, flags=hms.MT_STORE_ACTS)
+    assert a["loss"] == b["loss"]
+    _equal_trees(a["w"][-1], b["w"][-1])
+    _equal_trees(a["g"][-1], b["g"][-1])
+
+
+@pytest.mark.parametrize("variant", ["ckpt2", "ckpt3", "single_buffer", "small_chunks"])
+def test_schedule_variants_bitexact(variant):
+    s = SHAPES["gqa128"]
+    a = _run(s, steps=2)
+    if variant == "ckpt2":
+        b = _run(s.with_(ckpt_every=2), steps=2)
+    elif variant == "ckpt3":
+        b = _run(s.with_(ckpt_every=3), steps=2)
+    elif variant == "single_buffer":
+        b = _run(s, steps=2, flags=hms.MT_NO_DOUBLE_BUFFER)
+    else:  # many staging chunks and gradient slabs per tile, 2 slabs only
+        b = _run(s, steps=2, stage_bytes=64 << 10, grad_slab_bytes=32 << 10, n_grad_slabs=2, n_pack_threads=3)
+    assert a["loss"] == b["loss"]
+    _equal_trees(a["w"][-1], b["w"][-1])
+    _equal_trees(a["g"][-1], b["g"][-1])
+
+
+def test_repeat_runs_bitexact():
+    s = SHAPES["tiny"]
+    a = _run(s, steps=2)
+    b = _run(s, steps=2)
+    assert a["loss"] == b["loss"]
+    _equal_trees(a["w"][-1], b["w"][-1])
+    for x, y in zip(a["mv"][-1], b["mv"][-1]):
+        _equal_trees(x, y)
+
+
+def test_save_reload_continue_bitexact():
+    s = SHAPES["tiny"]
+    full = _run(s, steps=3)
+    m = hms.StreamedDecoder.from_shape(s)
+    m.load_weights(mt_inputs.model_weights(s, gain_jitter=0.1))
+    m.train_step(mt_inputs.step_tokens(s, 1))
+    saved = [[m.get_tile(i, p) for p in range(4)] for i in range(m.n_tiles)]
+    step = m.step
+    m.close()
+    m2 = hms.StreamedDecoder.from_shape(s)
+    for i in range(m2.n_tiles):
+        for p in range(4):
+            m2.load_tile(i, p, saved[i][p])
+    m2.step = step
+    l2 = m2.train_step(mt_inputs.step_tokens(s, 2))
+    l3 = m2.train_step(mt_inputs.step_tokens(s, 3))
+    assert [l2, l3] == full["loss"][1:]
+    _equal_trees(m2.weights(), full["w"][-1])
+    m2.close()
+
+
+def test_statistics_account_for_streamed_bytes():
+    s = SHAPES["gqa128"]
+    r = _run(s, steps=1)
+    st = r["stats"]
+    m = hms.StreamedDecoder.from_shape(s)
+    infos = m.infos
+    m.close()
+    layer_w = infos[1]["w_bytes"]
+    # K = 1: every layer is streamed for forward and again for backward, except
+    # the last layer, whose weights are still resident when backward starts.
+    expect_h2d = infos[0]["w_bytes"] + infos[-1]["w_bytes"] + (2 * s.n_layers - 1) * layer_w
+    assert st["h2d_bytes"] == expect_h2d
+    assert st["d2h_bytes"] == sum(i["w_bytes"] for i in infos)
+    assert st["step"] == 1 and st["gemm_launches"] > 0
