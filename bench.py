@@ -1,0 +1,422 @@
+"""Benchmark of the layer-streamed decoder training step on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 14b] [--impl reference]
+
+Prints ONE JSON line (rank 0).  A step is one full call of the library's
+training step: forward over every layer streamed from host tiles, LM head and
+loss, backward with block recompute, gradient evacuation and Adam on every
+host tile.  `value` is tokens/s with the tokens already in device memory;
+`e2e` is the same step through the host-token C-ABI call with the tokens in
+pinned host memory and the loss read back on the host.  Both include the
+host<->device weight/gradient streaming, which is the method itself.
+
+The default workload is the 14B-shaped GQA decoder (48 layers, d 5120, 40/8
+heads x 128, ffn 13824, vocab 152064, batch 8 x seq 4096).  When the host
+cannot hold all 48 layers' tiles the depth is truncated to what fits and the
+JSON says so.  With `--impl reference` the CPU oracle is timed instead on a
+bounded sample of the same workload (see `cpu_sample`).
+
+N > 1 (torchrun): one independent replica per GPU, no collective on the data
+path (the method is single-GPU); value = all ranks' tokens / the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mt_inputs  # noqa: E402
+
+METRIC = "streamed train tokens/s and MFU on 1 GB300; % of step roofline; H2D/D2H overlap"
+NOMINAL_BF16_PFLOPS = 2.25
+
+
+def _env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def tile_bytes(s):
+    """Host bytes of every tile kind (12 B/param + page padding), from the layout rules."""
+    def sect(numels):
+        off = 0
+        for n in numels:
+            off = (off + n * 2 + 255) // 256 * 256
+        w = (off + 4095) // 4096 * 4096
+        return 6 * w  # W + G (BF16) + M + V (FP32)
+    q, kv = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
+    layer = sect([s.d_model, (q + 2 * kv) * s.d_model, s.d_model * q, s.d_model, 2 * s.ffn * s.d_model,
+                  s.d_model * s.ffn])
+    embed = sect([s.vocab * s.d_model])
+    head = sect([s.d_model, s.vocab * s.d_model])
+    return layer, embed, head
+
+
+def fit_depth(s, n_replicas=1, margin=14 << 30):
+    """Most layers whose host tiles fit in MemAvailable (per replica)."""
+    avail = mem_available_bytes()
+    layer, embed, head = tile_bytes(s)
+    if avail is None:
+        return s.n_layers
+    per = (avail - margin) // max(1, n_replicas)
+    L = int((per - embed - head) // layer)
+    return max(1, min(s.n_layers, L))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6], swt=f[7],
+                                 swp=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("swp", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def link_bandwidth(device, nbytes=1 << 30):
+    """Pinned H2D and D2H GB/s, each measured while the other direction runs."""
+    h1 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h2 = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d1 = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    best = (0.0, 0.0)
+    for _ in range(3):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        torch.cuda.synchronize(device)
+        with torch.cuda.stream(s1):
+            e[0].record()
+            d1.copy_(h1, non_blocking=True)
+            e[1].record()
+        with torch.cuda.stream(s2):
+            e[2].record()
+            h2.copy_(d2, non_blocking=True)
+            e[3].record()
+        torch.cuda.synchronize(device)
+        h2d = nbytes / (e[0].elapsed_time(e[1]) * 1e-3) / 1e9
+        d2h = nbytes / (e[2].elapsed_time(e[3]) * 1e-3) / 1e9
+        best = (max(best[0], h2d), max(best[1], d2h))
+    del h1, h2, d1, d2
+    return best
+
+
+def load_synthetic_weights(model, s, device):
+    """N(0, 0.02) BF16 weights drawn on the GPU from per-tile seeds (1000 + tile), gains 1."""
+    for i in range(model.n_tiles):
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 + i)
+        info = model.infos[i]
+        raw = torch.zeros(info["w_bytes"], dtype=torch.uint8, device=device)
+        for name, meta in info["tensors"].items():
+            n = meta["numel"]
+            o = meta["offset"]
+            if name in ("g1", "g2", "gf"):
+                t = torch.ones(n, dtype=torch.bfloat16, device=device)
+            else:
+                t = (torch.randn(n, generator=g, device=device, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+            raw[o:o + 2 * n] = t.view(torch.uint8)
+        model.load_tile(i, 0, raw.cpu())
+        del raw
+
+
+def token_batches(s, steps, device):
+    gen = torch.Generator(device=device)
+    out = []
+    for n in range(steps):
+        gen.manual_seed(2000 + n + 1)
+        out.append(torch.randint(0, s.vocab, (s.batch, s.seq + 1), generator=gen, device=device, dtype=torch.int32))
+    return out
+
+
+def cpu_sample(s, repeats=1):
+    """Time the oracle (FP32, all host cores) on one decoder layer of the workload.
+
+    Sample: forward + backward of one full-width layer on one sequence of up to
+    2048 tokens, plus Adam on that layer's parameters; the whole-model time is
+    that layer time x (layers + the LM head's FLOPs in layer units), giving
+    tokens/s for the full model at the sample's tokens per step.
+    """
+    import oracle
+    from oracle import OracleConfig
+    torch.set_num_threads(os.cpu_count() or 1)
+    seq = min(s.seq, 2048)
+    cfg = OracleConfig.from_shape(s)
+    lw = {k: v.float() for k, v in mt_inputs.layer_weights(s, 0).items()}
+    gen = torch.Generator().manual_seed(7)
+    x = torch.randn(1, seq, s.d_model, generator=gen)
+    dy = torch.randn(1, seq, s.d_model, generator=gen) * 1e-3
+    cos, sin = oracle.rope_cos_sin(seq, s.head_dim, s.rope_theta, torch.float32)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        y, c = oracle.layer_forward(x, lw, cfg, cos, sin)
+        _, grads = oracle.layer_backward(dy, c, lw, cfg, cos, sin)
+        for k, w in lw.items():
+            z = torch.zeros_like(w)
+            oracle.adam_update(w.to(torch.bfloat16), grads[k].to(torch.bfloat16), z, z, 1, cfg)
+        times.append(time.perf_counter() - t0)
+    t_layer = statistics.median(times)
+    q, kv = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
+    lin = s.d_model * (q + 2 * kv) + q * s.d_model + 3 * s.d_model * s.ffn
+    head_in_layers = (s.d_model * s.vocab) / lin
+    t_model = t_layer * (s.n_layers + head_in_layers)
+    return {"value": seq / t_model, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": (f"oracle FP32 fwd+bwd+Adam of one {s.name} layer on 1x{seq} tokens "
+                       f"({t_layer:.2f} s), scaled to the full model as {s.n_layers} layers + "
+                       f"{head_in_layers:.2f} layer-equivalents of LM head"),
+            "layer_seconds": t_layer}
+
+
+def run_reference(args, s, rank):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_sample(s)
+    vals = [cpu_sample(s) for _ in range(args.steps)]
+    v = statistics.median(x["value"] for x in vals)
+    t = statistics.median(x["layer_seconds"] for x in vals)
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * s.batch * s.seq / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": s.name, "layers": s.n_layers, "batch": s.batch, "seq": s.seq},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "layer_seconds": t}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="14b", choices=sorted(mt_inputs.PRESETS))
+    ap.add_argument("--layers", type=int, default=0, help="override the depth (0 = preset, truncated to host RAM)")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    s = mt_inputs.PRESETS[args.config]
+    full_layers = s.n_layers
+    if args.layers:
+        s = s.with_(n_layers=args.layers)
+    if args.impl == "reference":
+        run_reference(args, s, rank)
+        return
+
+    import host_memory_streamed_gb300 as hms
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    L = fit_depth(s, n_replicas=world) if not args.layers else s.n_layers
+    s = s.with_(n_layers=L)
+
+    peaks, peak_kind = measured_peaks()
+    h2d_bw, d2h_bw = link_bandwidth(device)
+
+    t_init = time.perf_counter()
+    model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device)
+    load_synthetic_weights(model, s, device)
+    init_s = time.perf_counter() - t_init
+    toks = token_batches(s, args.warmup + args.steps, device)
+    host_toks = [t.cpu().pin_memory() for t in toks]
+    s_comp = model.streams[0]
+
+    for i in range(args.warmup):
+        model.train_step(toks[i])
+    # ---- timed region: device-resident tokens
+    stats = []
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(s_comp)
+        losses = []
+        for i in range(args.steps):
+            losses.append(model.train_step(toks[args.warmup + i]))
+            stats.append(model.stats())
+        e1.record(s_comp)
+        torch.cuda.synchronize(device)
+    if pg:
+        pg.barrier()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if pg:
+        t = torch.tensor([elapsed], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed = float(t[0])
+    tokens_per_step = s.batch * s.seq
+    value = world * args.steps * tokens_per_step / elapsed
+
+    # ---- e2e: host tokens through the C-ABI, loss read on the host
+    torch.cuda.synchronize(device)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(s_comp)
+    for i in range(args.steps):
+        model.train_step(host_toks[args.warmup + i])
+    f1.record(s_comp)
+    torch.cuda.synchronize(device)
+    e2e_elapsed = f0.elapsed_time(f1) / 1e3
+    if pg:
+        t = torch.tensor([e2e_elapsed], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_elapsed = float(t[0])
+    e2e = world * args.steps * tokens_per_step / e2e_elapsed
+    model.close()
+    del model
+
+    st = stats[-1]
+    ms_step = 1e3 * elapsed / args.steps
+    gemm_ms = sum(x["gemm_ms"] for x in stats)
+    gemm_flops = sum(x["gemm_flops"] for x in stats)
+    gemm_launches = sum(x["gemm_launches"] for x in stats)
+    kernels = sum(x["kernel_launches"] for x in stats)
+    p_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    flops_exec = st["flops_executed"]
+    flops_model = st["flops_model"]
+    t_flops = flops_exec / (p_sust * 1e12)
+    t_h2d = st["h2d_bytes"] / (h2d_bw * 1e9)
+    t_d2h = st["d2h_bytes"] / (d2h_bw * 1e9)
+    step_roof = max(t_flops, t_h2d, t_d2h)
+    lin_bytes = st["h2d_bytes"] + st["d2h_bytes"]
+    copy_ms = sum(x["h2d_ms"] + x["d2h_ms"] for x in stats)
+    stall_ms = sum(x["wait_weights_ms"] for x in stats)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": s.name, "layers": s.n_layers, "layers_preset": full_layers, "d_model": s.d_model,
+                   "heads": f"{s.n_heads}q/{s.n_kv_heads}kv x {s.head_dim}", "ffn": s.ffn, "vocab": s.vocab,
+                   "batch": s.batch, "seq": s.seq, "ckpt_every": s.ckpt_every,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (weights streamed per layer, activations > 129 MB)",
+                   "truncated": s.n_layers < full_layers,
+                   "truncation_reason": ("host RAM: tiles of all layers do not fit" if s.n_layers < full_layers
+                                         and not args.layers else None)},
+        "mfu": flops_model / (ms_step * 1e-3) / (NOMINAL_BF16_PFLOPS * 1e15),
+        "mfu_vs_measured_peak": flops_model / (ms_step * 1e-3) / (peaks["bf16_tflops"] * 1e12),
+        "executed_tflops": flops_exec / (ms_step * 1e-3) / 1e12,
+        "step_roofline": {"flops_executed": flops_exec, "flops_model": flops_model, "t_flops_ms": 1e3 * t_flops,
+                          "h2d_bytes": st["h2d_bytes"], "d2h_bytes": st["d2h_bytes"],
+                          "h2d_gbs_measured": h2d_bw, "d2h_gbs_measured": d2h_bw, "t_h2d_ms": 1e3 * t_h2d,
+                          "t_d2h_ms": 1e3 * t_d2h, "bound": "tensor" if t_flops >= max(t_h2d, t_d2h) else "link",
+                          "frac": step_roof / (ms_step * 1e-3),
+                          "peak": p_sust, "peak_kind": f"bf16_tflops_sustained ({peak_kind})"},
+        "overlap": {"copy_ms_per_step": copy_ms / args.steps, "compute_stall_on_weights_ms_per_step":
+                    stall_ms / args.steps,
+                    "hidden_frac": (1.0 - stall_ms / copy_ms) if copy_ms else None,
+                    "method": "CUDA events: copy windows on the H2D/D2H streams vs compute-stream waits"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_bf16_tcgen05", "achieved": achieved, "peak": p_sust,
+                     "unit": "TFLOP/s", "frac": (achieved / p_sust) if achieved else None,
+                     "traffic": None, "peak_kind": f"bf16_tflops_sustained ({peak_kind}) -- timed inside a long step",
+                     "launches": gemm_launches, "flops_per_launch": gemm_flops / max(1, gemm_launches),
+                     "ms_per_launch": gemm_ms / max(1, gemm_launches)},
+        "e2e": {"value": e2e, "unit": "tokens/s",
+                "h2d_bytes_per_step": 4 * (3 * tokens_per_step + s.vocab + 1) + st["h2d_bytes"],
+                "d2h_bytes_per_step": 4 + st["d2h_bytes"]},
+        "gpu_launches": kernels,
+        "step_breakdown_ms": {k: st[k] for k in ("step_ms", "gpu_compute_ms", "h2d_ms", "d2h_ms", "wait_weights_ms",
+                                                 "adam_ms", "adam_tail_ms", "gemm_ms")},
+        "losses": losses, "init_seconds": init_s,
+    }
+    line["clocks"] = clk.summary()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k: v for k, v in cpu_sample(s).items() if k != "layer_seconds"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

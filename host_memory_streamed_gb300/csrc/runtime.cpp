@@ -285,6 +285,7 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
 struct mt_model {
   mt_config cfg{};
   mt::Dims D{};
+  int device = 0;
   int K = 1;
   bool resident_mode = false, store_acts = false, single_buffer = false, debug = false, time_kernels = false;
   std::vector<mt::TileLayout> layouts;  // per tile
@@ -438,6 +439,7 @@ void pack_copy(mt_model* m, uint8_t* dst, const uint8_t* src, int64_t n) {
 
 // ------------------------------------------------------------------ loader (H2D stream)
 void loader_main(mt_model* m) {
+  cudaSetDevice(m->device);
   int64_t gen = 0;
   while (true) {
     {
@@ -492,6 +494,7 @@ int acquire_slab(mt_model* m) {
 }
 
 void d2h_main(mt_model* m) {
+  cudaSetDevice(m->device);
   while (true) {
     int v;
     {
@@ -553,6 +556,7 @@ void submit_adam(mt_model* m, int tile) {
 }
 
 void accum_main(mt_model* m) {
+  cudaSetDevice(m->device);
   while (true) {
     mt_model::AccJob j;
     {
@@ -657,7 +661,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
   const auto wall0 = Clock::now();
   int code = MT_OK;
   try {
-    MT_CK(cudaSetDevice(0) == cudaSuccess ? cudaSuccess : cudaGetLastError());
+    MT_CK(cudaSetDevice(m->device));
     std::vector<int32_t> host_tok;
     if (tokens_dev) {
       host_tok.resize(n_tokens);
@@ -1030,6 +1034,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->time_kernels = m->cfg.flags & MT_TIME_KERNELS;
   if (!sc || !sh || !sd || sc == sh || sc == sd || sh == sd)
     throw MtError{MT_EINVAL, "three distinct CUDA streams are required"};
+  MT_CK(cudaGetDevice(&m->device));
   m->s_comp = static_cast<cudaStream_t>(sc);
   m->s_h2d = static_cast<cudaStream_t>(sh);
   m->s_d2h = static_cast<cudaStream_t>(sd);

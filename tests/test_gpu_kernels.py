@@ -1,0 +1,279 @@
+"""Each sm_103a kernel through the C-ABI (include/mt_ops.h) against the CPU
+oracle's function for the same step (FP64) on the same seeded BF16 inputs."""
+import math
+
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+hms = pytest.importorskip("host_memory_streamed_gb300")
+from host_memory_streamed_gb300 import _lib, ops  # noqa: E402
+
+D = torch.float64
+DEV = "cuda"
+
+
+def rel(a, b):
+    a = a.to(D).cpu()
+    b = b.to(D).cpu()
+    return float((a - b).norm() / b.norm().clamp_min(1e-300))
+
+
+def rnd(shape, gen, scale=1.0):
+    return (torch.randn(shape, generator=gen) * scale).to(torch.bfloat16)
+
+
+def rope_tables(S, hd, theta=1e4):
+    c, s = oracle.rope_cos_sin(S, hd, theta)
+    return c.float().to(DEV).contiguous(), s.float().to(DEV).contiguous()
+
+
+# ------------------------------------------------------------------ GEMM
+GEMM_SHAPES = [(128, 256, 64), (300, 688, 256), (129, 264, 72), (1, 8, 8), (513, 1032, 1376), (2048, 1536, 512)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_store_and_fp32(M, N, K):
+    g = torch.Generator().manual_seed(M * 7 + N)
+    A, B = rnd((M, K), g), rnd((N, K), g)
+    ref = A.to(D) @ B.to(D).T
+    C32 = torch.empty(M, N, device=DEV)
+    ops.gemm(A.to(DEV), B.to(DEV), C32, _lib.EPI_F32)
+    Cb = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
+    ops.gemm(A.to(DEV), B.to(DEV), Cb, _lib.EPI_STORE_BF16)
+    torch.cuda.synchronize()
+    # FP32 accumulation of K exact BF16 products: error ~ sqrt(K) * 2^-24 * |terms|
+    bound = 1e-5 * math.sqrt(K) * (A.to(D).abs() @ B.to(D).abs().T) + 1e-30
+    assert torch.all((C32.cpu().to(D) - ref).abs() <= bound)
+    assert torch.equal(Cb.cpu(), C32.cpu().to(torch.bfloat16))  # BF16 output = RNE of the FP32 accumulator
+
+
+def test_gemm_residual_accumulate_swiglu_rope():
+    g = torch.Generator().manual_seed(3)
+    M, N, K, S, hd = 384, 512, 256, 96, 128
+    A, B, R = rnd((M, K), g), rnd((N, K), g), rnd((M, N), g)
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    ref = A.to(D) @ B.to(D).T
+    out = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
+    ops.gemm(Ad, Bd, out, _lib.EPI_RESIDUAL_BF16, residual=R.to(DEV))
+    assert rel(out, ref + R.to(D)) < 4e-3
+    acc = torch.full((M, N), 0.5, device=DEV)
+    ops.gemm(Ad, Bd, acc, _lib.EPI_F32_ACCUMULATE)
+    assert rel(acc, ref + 0.5) < 1e-6
+    a = torch.empty(M, N // 2, device=DEV, dtype=torch.bfloat16)
+    gu = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
+    ops.gemm(Ad, Bd, a, _lib.EPI_SWIGLU, out2=gu)
+    assert rel(a, oracle.swiglu(ref[:, 0::2], ref[:, 1::2])) < 4e-3
+    assert rel(gu, ref) < 4e-3
+    cos, sin = rope_tables(S, hd)
+    ro = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
+    ops.gemm(Ad, Bd, ro, _lib.EPI_ROPE, rope_cos=cos, rope_sin=sin, rope_cols=3 * hd, head_dim=hd, seq=S)
+    torch.cuda.synchronize()
+    c64, s64 = oracle.rope_cos_sin(S, hd, 1e4)
+    B_, S_ = M // S, S
+    x = ref[:, :3 * hd].reshape(B_, S_, 3, hd)
+    expect = torch.cat([oracle.rope(x, c64, s64).reshape(M, 3 * hd), ref[:, 3 * hd:]], 1)
+    assert rel(ro, expect) < 4e-3
+
+
+def test_gemm_rejects_bad_arguments():
+    A = torch.zeros(16, 12, device=DEV, dtype=torch.bfloat16)
+    C = torch.zeros(16, 16, device=DEV, dtype=torch.bfloat16)
+    with pytest.raises(RuntimeError, match="multiple of 8"):
+        ops.gemm(A, A[:, :12], C)
+
+
+def test_gemm_deterministic():
+    g = torch.Generator().manual_seed(5)
+    A, B = rnd((1000, 2048), g).to(DEV), rnd((3000, 2048), g).to(DEV)
+    c1 = torch.empty(1000, 3000, device=DEV)
+    c2 = torch.empty(1000, 3000, device=DEV)
+    ops.gemm(A, B, c1, _lib.EPI_F32)
+    ops.gemm(A, B, c2, _lib.EPI_F32)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+# ------------------------------------------------------------------ attention
+ATTN = [(2, 128, 4, 4, 64), (1, 200, 4, 2, 128), (2, 333, 6, 2, 64), (1, 1, 2, 1, 128), (1, 257, 10, 2, 128),
+        (1, 64, 8, 1, 64)]
+
+
+def _attn_inputs(B, S, Hq, Hkv, hd, seed):
+    g = torch.Generator().manual_seed(seed)
+    ld = (Hq + 2 * Hkv) * hd
+    qkv = rnd((B * S, ld), g)
+    do = rnd((B * S, Hq * hd), g)
+    return qkv, do
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,hd", ATTN)
+def test_attention_forward_backward_vs_oracle(B, S, Hq, Hkv, hd):
+    qkv, do = _attn_inputs(B, S, Hq, Hkv, hd, seed=B * 1000 + S + Hq)
+    T, ld = B * S, qkv.shape[1]
+    qd = qkv.to(DEV)
+    o = torch.empty(T, Hq * hd, device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty(B * Hq * S, device=DEV)
+    ops.attention_fwd(qd, B, S, Hq, Hkv, hd, o, lse)
+    delta = torch.empty(B * Hq * S, device=DEV)
+    dqkv = torch.zeros(T, ld, device=DEV, dtype=torch.bfloat16)
+    ops.attention_bwd(qd, B, S, Hq, Hkv, hd, o, lse, do.to(DEV), delta, dqkv)
+    torch.cuda.synchronize()
+    x = qkv.to(D)
+    q = x[:, :Hq * hd].reshape(B, S, Hq, hd)
+    k = x[:, Hq * hd:(Hq + Hkv) * hd].reshape(B, S, Hkv, hd)
+    v = x[:, (Hq + Hkv) * hd:].reshape(B, S, Hkv, hd)
+    o_ref, probs = oracle.causal_gqa_attention(q, k, v)
+    assert rel(o, o_ref.reshape(T, -1)) < 5e-3
+    # log-sum-exp of each score row, from the oracle's scores
+    scale = 1 / math.sqrt(hd)
+    lse_ref = torch.empty(B, Hq, S, dtype=D)
+    for b in range(B):
+        for h in range(Hq):
+            j = h * Hkv // Hq
+            sc = (q[b, :, h] @ k[b, :, j].T) * scale
+            sc = sc.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+            lse_ref[b, h] = torch.logsumexp(sc, -1)
+    assert (lse.cpu().to(D) - lse_ref.reshape(-1)).abs().max() < 1e-4
+    dq, dk, dv = oracle.causal_gqa_attention_backward(do.to(D).reshape(B, S, Hq, hd), q, k, v, probs)
+    got = dqkv.cpu().to(D)
+    for name, a, b_ in (("dq", got[:, :Hq * hd], dq), ("dk", got[:, Hq * hd:(Hq + Hkv) * hd], dk),
+                        ("dv", got[:, (Hq + Hkv) * hd:], dv)):
+        b_ = b_.reshape(T, -1)
+        if float(b_.norm()) < 1e-12:  # S = 1: the softmax is constant, dq = dk = 0 exactly
+            assert float(a.abs().max()) < 1e-2 * float(do.to(D).abs().max()), name
+        else:
+            assert rel(a, b_) < 1e-2, (name, rel(a, b_))
+
+
+def test_attention_backward_with_rope_gives_unrotated_grads():
+    B, S, Hq, Hkv, hd = 2, 150, 4, 2, 128
+    qkv, do = _attn_inputs(B, S, Hq, Hkv, hd, seed=11)
+    T, ld = B * S, qkv.shape[1]
+    cos, sin = rope_tables(S, hd)
+    qd = qkv.to(DEV)
+    o = torch.empty(T, Hq * hd, device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty(B * Hq * S, device=DEV)
+    ops.attention_fwd(qd, B, S, Hq, Hkv, hd, o, lse)
+    dqkv = torch.zeros(T, ld, device=DEV, dtype=torch.bfloat16)
+    ops.attention_bwd(qd, B, S, Hq, Hkv, hd, o, lse, do.to(DEV), torch.empty(B * Hq * S, device=DEV), dqkv,
+                      cos, sin)
+    torch.cuda.synchronize()
+    x = qkv.to(D)
+    q = x[:, :Hq * hd].reshape(B, S, Hq, hd)
+    k = x[:, Hq * hd:(Hq + Hkv) * hd].reshape(B, S, Hkv, hd)
+    v = x[:, (Hq + Hkv) * hd:].reshape(B, S, Hkv, hd)
+    _, probs = oracle.causal_gqa_attention(q, k, v)
+    dq, dk, _ = oracle.causal_gqa_attention_backward(do.to(D).reshape(B, S, Hq, hd), q, k, v, probs)
+    c64, s64 = oracle.rope_cos_sin(S, hd, 1e4)
+    got = dqkv.cpu().to(D)
+    assert rel(got[:, :Hq * hd], oracle.rope_backward(dq, c64, s64).reshape(T, -1)) < 1e-2
+    assert rel(got[:, Hq * hd:(Hq + Hkv) * hd], oracle.rope_backward(dk, c64, s64).reshape(T, -1)) < 1e-2
+
+
+def test_attention_backward_deterministic():
+    B, S, Hq, Hkv, hd = 1, 700, 10, 2, 128
+    qkv, do = _attn_inputs(B, S, Hq, Hkv, hd, seed=12)
+    T, ld = B * S, qkv.shape[1]
+    qd, dod = qkv.to(DEV), do.to(DEV)
+    o = torch.empty(T, Hq * hd, device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty(B * Hq * S, device=DEV)
+    ops.attention_fwd(qd, B, S, Hq, Hkv, hd, o, lse)
+    outs = []
+    for _ in range(2):
+        d = torch.zeros(T, ld, device=DEV, dtype=torch.bfloat16)
+        ops.attention_bwd(qd, B, S, Hq, Hkv, hd, o, lse, dod, torch.empty(B * Hq * S, device=DEV), d)
+        outs.append(d)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+
+
+# ------------------------------------------------------------------ RMSNorm / SwiGLU / CE / embedding / transpose
+@pytest.mark.parametrize("rows,d", [(256, 256), (1000, 5120), (77, 64), (130, 8192)])
+def test_rmsnorm_vs_oracle(rows, d):
+    g = torch.Generator().manual_seed(rows + d)
+    x, w = rnd((rows, d), g), (1 + 0.1 * torch.randn(d, generator=g)).to(torch.bfloat16)
+    dy, dres = rnd((rows, d), g), rnd((rows, d), g)
+    y = torch.empty(rows, d, device=DEV, dtype=torch.bfloat16)
+    rstd = torch.empty(rows, device=DEV)
+    ops.rmsnorm_fwd(x.to(DEV), w.to(DEV), y, rstd, 1e-5)
+    dx = torch.empty_like(y)
+    dg = torch.empty(d, device=DEV, dtype=torch.bfloat16)
+    ops.rmsnorm_bwd(dy.to(DEV), x.to(DEV), w.to(DEV), rstd, dres.to(DEV), dx, dg)
+    torch.cuda.synchronize()
+    yr, rr = oracle.rms_norm(x.to(D), w.to(D), 1e-5)
+    dxr, dgr = oracle.rms_norm_backward(dy.to(D), x.to(D), w.to(D), rr)
+    assert rel(y, yr) < 4e-3
+    assert rel(rstd, rr.reshape(-1)) < 1e-6
+    assert rel(dx, dxr + dres.to(D)) < 4e-3
+    assert rel(dg, dgr) < 4e-3
+
+
+@pytest.mark.parametrize("rows,f", [(256, 688), (300, 5632), (5, 7)])
+def test_swiglu_backward_vs_oracle(rows, f):
+    g = torch.Generator().manual_seed(rows + f)
+    gu, da = rnd((rows, 2 * f), g, 2.0), rnd((rows, f), g)
+    dgu = torch.empty(rows, 2 * f, device=DEV, dtype=torch.bfloat16)
+    ops.swiglu_bwd(da.to(DEV), gu.to(DEV), dgu)
+    torch.cuda.synchronize()
+    dg, du = oracle.swiglu_backward(da.to(D), gu.to(D)[:, 0::2], gu.to(D)[:, 1::2])
+    assert rel(dgu.cpu()[:, 0::2], dg) < 4e-3
+    assert rel(dgu.cpu()[:, 1::2], du) < 4e-3
+
+
+@pytest.mark.parametrize("rows,V", [(256, 1024), (64, 152064), (10, 40)])
+def test_cross_entropy_vs_oracle(rows, V):
+    g = torch.Generator().manual_seed(rows + V)
+    z = torch.randn(rows, V, generator=g) * 3
+    y = torch.randint(0, V, (rows,), generator=g, dtype=torch.int32)
+    dz = torch.empty(rows, V, device=DEV, dtype=torch.bfloat16)
+    lr = torch.empty(rows, device=DEV)
+    st = torch.zeros(1, device=DEV, dtype=torch.int32)
+    ops.cross_entropy(z.to(DEV), y.to(DEV), 1.0 / rows, dz, lr, st)
+    torch.cuda.synchronize()
+    zd = z.to(D)
+    lref = torch.logsumexp(zd, -1) - zd.gather(1, y.long()[:, None])[:, 0]
+    assert (lr.cpu().to(D) - lref).abs().max() < 1e-5 * max(1.0, float(lref.abs().max()))
+    p = torch.softmax(zd, -1)
+    p[torch.arange(rows), y.long()] -= 1
+    assert rel(dz, p / rows) < 4e-3
+    assert int(st.item()) == 0
+
+
+def test_embedding_forward_exact_backward_deterministic_sum():
+    g = torch.Generator().manual_seed(21)
+    V, d, T = 1000, 256, 512
+    E = rnd((V, d), g)
+    tok = torch.randint(0, V, (T,), generator=g, dtype=torch.int32)
+    x = torch.empty(T, d, device=DEV, dtype=torch.bfloat16)
+    st = torch.zeros(1, device=DEV, dtype=torch.int32)
+    ops.embedding_fwd(tok.to(DEV), E.to(DEV), x, st)
+    dx = rnd((T, d), g)
+    order = torch.argsort(tok.long() * T + torch.arange(T))
+    off = torch.zeros(V + 1, dtype=torch.int32)
+    off[1:] = torch.cumsum(torch.bincount(tok.long(), minlength=V), 0).int()
+    dE = torch.empty(V, d, device=DEV, dtype=torch.bfloat16)
+    ops.embedding_bwd(off.to(DEV), order.int().to(DEV), dx.to(DEV), dE)
+    torch.cuda.synchronize()
+    assert torch.equal(x.cpu(), E[tok.long()])
+    ref = torch.zeros(V, d, dtype=D).index_add_(0, tok.long(), dx.to(D))
+    assert rel(dE, ref) < 4e-3
+    assert torch.all(dE.cpu()[torch.bincount(tok.long(), minlength=V) == 0] == 0)
+    bad = tok.clone()
+    bad[3] = V + 5
+    ops.embedding_fwd(bad.to(DEV), E.to(DEV), x, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) != 0
+
+
+@pytest.mark.parametrize("r,c", [(100, 70), (4096, 5120), (64, 64), (1, 9), (130, 257)])
+def test_transpose_exact(r, c):
+    g = torch.Generator().manual_seed(r + c)
+    x = rnd((r, c), g).to(DEV)
+    y = torch.empty(c, r, device=DEV, dtype=torch.bfloat16)
+    ops.transpose(x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x.T)
