@@ -30,11 +30,20 @@ def _need(t, dtype, name):
         raise TypeError(f"{name} must be a CUDA {dtype} tensor")
 
 
+F32, BF16, I32 = torch.float32, torch.bfloat16, torch.int32
+
+
 def gemm(A, B, out, epilogue=_lib.EPI_STORE_BF16, residual=None, out2=None, rope_cos=None, rope_sin=None,
          rope_cols=0, head_dim=0, seq=1, status=None):
     """out = epilogue(A @ B^T); A [M, K], B [N, K] BF16 (row strides may exceed K)."""
-    _need(A, torch.bfloat16, "A")
-    _need(B, torch.bfloat16, "B")
+    _need(A, BF16, "A")
+    _need(B, BF16, "B")
+    _need(out, F32 if epilogue in (_lib.EPI_F32, _lib.EPI_F32_ACCUMULATE) else BF16, "out")
+    _need(residual, BF16, "residual")
+    _need(out2, BF16, "out2")
+    _need(rope_cos, F32, "rope_cos")
+    _need(rope_sin, F32, "rope_sin")
+    _need(status, I32, "status")
     M, K = A.shape
     N = B.shape[0]
     _chk(_lib.lib().mt_op_gemm(A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), M, N, K, epilogue,
@@ -45,25 +54,36 @@ def gemm(A, B, out, epilogue=_lib.EPI_STORE_BF16, residual=None, out2=None, rope
 
 
 def attention_fwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse):
-    _need(qkv, torch.bfloat16, "qkv")
+    _need(qkv, BF16, "qkv")
+    _need(o, BF16, "o")
+    _need(lse, F32, "lse")
     _chk(_lib.lib().mt_op_attention_fwd(qkv.data_ptr(), qkv.stride(0), batch, seq, n_heads, n_kv_heads, head_dim,
                                         o.data_ptr(), o.stride(0), lse.data_ptr(), _stream()))
 
 
 def attention_bwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse, dout, delta, dqkv, rope_cos=None,
                   rope_sin=None):
+    for t, dt, n in ((qkv, BF16, "qkv"), (o, BF16, "o"), (lse, F32, "lse"), (dout, BF16, "dout"),
+                     (delta, F32, "delta"), (dqkv, BF16, "dqkv"), (rope_cos, F32, "rope_cos"),
+                     (rope_sin, F32, "rope_sin")):
+        _need(t, dt, n)
     _chk(_lib.lib().mt_op_attention_bwd(qkv.data_ptr(), qkv.stride(0), batch, seq, n_heads, n_kv_heads, head_dim,
                                         o.data_ptr(), o.stride(0), lse.data_ptr(), dout.data_ptr(), delta.data_ptr(),
                                         dqkv.data_ptr(), _ptr(rope_cos), _ptr(rope_sin), _stream()))
 
 
 def rmsnorm_fwd(x, g, y, rstd, eps):
+    for t, dt, n in ((x, BF16, "x"), (g, BF16, "g"), (y, BF16, "y"), (rstd, F32, "rstd")):
+        _need(t, dt, n)
     rows, d = x.shape
     _chk(_lib.lib().mt_op_rmsnorm_fwd(x.data_ptr(), g.data_ptr(), y.data_ptr(), rstd.data_ptr(), rows, d, eps,
                                       _stream()))
 
 
 def rmsnorm_bwd(dy, x, g, rstd, dres, dx, dg):
+    for t, dt, n in ((dy, BF16, "dy"), (x, BF16, "x"), (g, BF16, "g"), (rstd, F32, "rstd"), (dres, BF16, "dres"),
+                     (dx, BF16, "dx"), (dg, BF16, "dg")):
+        _need(t, dt, n)
     rows, d = x.shape
     L = _lib.lib()
     scratch = torch.empty(L.mt_op_rmsnorm_bwd_scratch_floats(rows, d), dtype=torch.float32, device=x.device)
@@ -72,28 +92,40 @@ def rmsnorm_bwd(dy, x, g, rstd, dres, dx, dg):
 
 
 def swiglu_bwd(da, gu, dgu):
+    for t, n in ((da, "da"), (gu, "gu"), (dgu, "dgu")):
+        _need(t, BF16, n)
     rows, f = da.shape
     _chk(_lib.lib().mt_op_swiglu_bwd(da.data_ptr(), gu.data_ptr(), dgu.data_ptr(), rows, f, _stream()))
 
 
 def transpose(src, dst):
+    _need(src, BF16, "src")
+    _need(dst, BF16, "dst")
     r, c = src.shape
     _chk(_lib.lib().mt_op_transpose(src.data_ptr(), r, c, src.stride(0), dst.data_ptr(), dst.stride(0), _stream()))
 
 
 def cross_entropy(z, tgt, inv_n, dz, loss_rows, status=None):
+    for t, dt, n in ((z, F32, "z"), (tgt, I32, "tgt"), (dz, BF16, "dz"), (loss_rows, F32, "loss_rows"),
+                     (status, I32, "status")):
+        _need(t, dt, n)
     rows, V = z.shape
     _chk(_lib.lib().mt_op_cross_entropy(z.data_ptr(), rows, V, tgt.data_ptr(), inv_n, dz.data_ptr(),
                                         loss_rows.data_ptr(), _ptr(status), _stream()))
 
 
 def embedding_fwd(tok, E, x, status=None):
+    for t, dt, n in ((tok, I32, "tok"), (E, BF16, "E"), (x, BF16, "x"), (status, I32, "status")):
+        _need(t, dt, n)
     V, d = E.shape
     _chk(_lib.lib().mt_op_embedding_fwd(tok.data_ptr(), E.data_ptr(), x.data_ptr(), tok.numel(), d, V, _ptr(status),
                                         _stream()))
 
 
 def embedding_bwd(row_offsets, positions, dx, dE):
+    for t, dt, n in ((row_offsets, I32, "row_offsets"), (positions, I32, "positions"), (dx, BF16, "dx"),
+                     (dE, BF16, "dE")):
+        _need(t, dt, n)
     V, d = dE.shape
     _chk(_lib.lib().mt_op_embedding_bwd(row_offsets.data_ptr(), positions.data_ptr(), dx.data_ptr(), dE.data_ptr(),
                                         V, d, _stream()))

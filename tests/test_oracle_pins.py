@@ -17,8 +17,16 @@ import mt_inputs
 import oracle
 from oracle import OracleConfig
 
-torch.set_default_dtype(torch.float64)
 D = torch.float64
+
+
+@pytest.fixture(autouse=True)
+def _fp64_default_dtype():
+    """The pins build FP64 tensors by default; restore the caller's default after each test."""
+    old = torch.get_default_dtype()
+    torch.set_default_dtype(torch.float64)
+    yield
+    torch.set_default_dtype(old)
 
 
 def _tiny(**kw):
