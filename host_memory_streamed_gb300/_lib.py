@@ -96,6 +96,7 @@ def lib():
         "mt_op_cross_entropy": (C.c_int, [vp, i64, i32, vp, f32, vp, vp, vp, vp]),
         "mt_op_embedding_fwd": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp]),
         "mt_op_embedding_bwd": (C.c_int, [vp, vp, vp, vp, i32, i32, vp]),
+        "mt_op_rmsnorm_bwd_noalloc": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name, None)

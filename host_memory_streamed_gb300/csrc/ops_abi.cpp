@@ -23,6 +23,10 @@ int op_cuda(int rc, const char* what) {
 }
 }  // namespace
 
+namespace mt {
+void set_op_error(const std::string& msg) { g_op_error = msg; }
+}  // namespace mt
+
 extern "C" {
 
 const char* mt_op_last_error(void) { return g_op_error.c_str(); }

@@ -110,6 +110,29 @@ int mt_op_embedding_fwd(const int32_t* tok, const void* E, void* x, int64_t T, i
 int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, const void* dx, void* dE, int32_t V,
                         int32_t d, void* stream);
 
+/*
+ * RMSNorm backward that allocates nothing (no counterpart in the MegaTrain
+ * pages: it exists for callers of this library).  Same inputs, outputs and
+ * results as mt_op_rmsnorm_bwd, but without the caller-provided scratch
+ * buffer.  It is meant for callers that cannot allocate device memory: code
+ * embedded in a host application that reserves the GPU's memory budget up
+ * front and forbids further allocation, or latency-critical loops where a
+ * cudaMalloc/cudaFree (which can synchronise the device) is not acceptable.
+ *
+ * The gain-gradient partial sums go to a fixed array in the library's own
+ * device memory (16 MiB, 4,194,304 floats) that every GPU loading the library
+ * keeps until the process exits.  The call requires ceil(rows/64) * d <=
+ * 4,194,304 and returns MT_EINVAL otherwise (message in mt_op_last_error()).
+ * It calls no cudaMalloc, cudaFree or allocating library routine.  The first
+ * call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array: each overwrites
+ * the part it reads, but calls that overlap on the GPU (other streams, or
+ * other host threads without ordering) race and must be serialised.
+ */
+int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* g, const float* rstd, const void* dres,
+                              void* dx, void* dg, int64_t rows, int32_t d, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
