@@ -86,6 +86,7 @@ def lib():
         "mt_op_last_error": (C.c_char_p, []),
         "mt_op_gemm": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, vp, i64, vp, i64, vp, i64,
                                  vp, vp, i32, i32, i32, vp, vp]),
+        "mt_op_gemm_layout": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, i64, vp, vp]),
         "mt_op_attention_fwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp]),
         "mt_op_attention_bwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp]),
         "mt_op_rmsnorm_fwd": (C.c_int, [vp, vp, vp, vp, i64, i32, f32, vp]),

@@ -25,7 +25,7 @@ NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                      f"-I{INCLUDE}", f"-I{CSRC}"]
-CXX_FLAGS = ["-O3", "-fPIC", "-std=c++17", "-pthread", "-fno-fast-math", "-Wall", "-Wno-unused-function",
+CXX_FLAGS = ["-O3", "-fPIC", "-std=c++17", "-pthread", "-fno-fast-math", "-fno-math-errno", "-Wall", "-Wno-unused-function",
              f"-I{INCLUDE}", f"-I{CSRC}", f"-I{os.path.join(CUDA_HOME, 'include')}"]
 
 
@@ -61,11 +61,19 @@ def build(verbose: bool = False, jobs: int | None = None) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     hdr_mtime = max([os.path.getmtime(h) for h in _headers()] + [0.0])
+    stamp = os.path.join(BUILD, "flags.txt")
+    flags = " ".join(NVCC_FLAGS + CXX_FLAGS)
+    if not os.path.exists(stamp) or open(stamp).read() != flags:
+        verbose_all = True
+        with open(stamp, "w") as f:
+            f.write(flags)
+    else:
+        verbose_all = False
     objs, todo = [], []
     for s in srcs:
         o = os.path.join(BUILD, os.path.basename(s) + ".o")
         objs.append(o)
-        if verbose or _stale(s, o, hdr_mtime):
+        if verbose or verbose_all or _stale(s, o, hdr_mtime):
             todo.append((s, o))
     if todo:
         with cf.ThreadPoolExecutor(max_workers=jobs or min(len(todo), os.cpu_count() or 4)) as ex:

@@ -45,7 +45,11 @@ constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;  // two FP32 accumulators
 constexpr int GROUP_M = 16;        // tile raster: 16 M-tiles share each B panel
-constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int SMEM_USED = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+// Launch with the whole 227 KB (one CTA per SM either way); the unused tail
+// keeps every tensor-core read of the last stage inside the allocation.
+constexpr int SMEM_BYTES = 232448;
+static_assert(SMEM_USED <= SMEM_BYTES, "shared memory plan exceeds 227 KB");
 
 struct EpiParams {
   int M, N, K;
@@ -184,6 +188,10 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
   }
 }
 
+// A_MN / B_MN: the operand is stored MN-major ([K][M] resp. [K][N], M or N
+// contiguous) instead of K-major.  MN-major tiles arrive as 64-column TMA
+// boxes (8 KB each, 128-byte swizzle) stacked along M/N.
+template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                              EpiParams p) {
@@ -244,8 +252,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], A_STAGE + B_STAGE);
-          tma_load_2d(sA + stage * A_STAGE, &tmap_a, kb * BK, tm * BM, &full[stage]);
-          tma_load_2d(sB + stage * B_STAGE, &tmap_b, kb * BK, tn * BN, &full[stage]);
+          if (A_MN) {
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i)
+              tma_load_2d(sA + stage * A_STAGE + i * (64 * BK * 2), &tmap_a, tm * BM + 64 * i, kb * BK, &full[stage]);
+          } else {
+            tma_load_2d(sA + stage * A_STAGE, &tmap_a, kb * BK, tm * BM, &full[stage]);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(sB + stage * B_STAGE + i * (64 * BK * 2), &tmap_b, tn * BN + 64 * i, kb * BK, &full[stage]);
+          } else {
+            tma_load_2d(sB + stage * B_STAGE, &tmap_b, kb * BK, tn * BN, &full[stage]);
+          }
           pending[stage] = (int)phase;
           if (++stage == STAGES) {
             stage = 0;
@@ -260,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      const uint32_t idesc = idesc_bf16_f32(BM, BN) | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -282,13 +302,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = smem_desc_kmajor_sw128(sA + stage * A_STAGE);
-          const uint64_t bdesc = smem_desc_kmajor_sw128(sB + stage * B_STAGE);
+          const uint64_t adesc = A_MN ? smem_desc_mnmajor_sw128(sA + stage * A_STAGE, 64 * BK * 2)
+                                      : smem_desc_kmajor_sw128(sA + stage * A_STAGE);
+          const uint64_t bdesc = B_MN ? smem_desc_mnmajor_sw128(sB + stage * B_STAGE, 64 * BK * 2)
+                                      : smem_desc_kmajor_sw128(sB + stage * B_STAGE);
+          // one K step of 16: K-major advances 32 bytes inside the swizzle
+          // atom; MN-major advances two 8-row groups (2048 bytes)
+          constexpr uint64_t a_step = A_MN ? (2048 >> 4) : (32 >> 4);
+          constexpr uint64_t b_step = B_MN ? (2048 >> 4) : (32 >> 4);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // advance 16 elements = 32 bytes along K inside the swizzle atom
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -398,6 +422,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Row-major BF16 matrix [rows, cols] with leading dimension ld (elements),
 // boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill outside.
+// K-major operands use rows = M/N, cols = K, box_rows = BM/BN; MN-major
+// operands use rows = K, cols = M/N, box_rows = BK.
 bool make_tmap(CUtensorMap* m, const void* base, long rows, long cols, long ld, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -428,7 +454,7 @@ const char* gemm_check(const GemmArgs& g) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return "gemm: M, N and K must be positive";
   if (g.K % 8) return "gemm: K must be a multiple of 8 (16-byte TMA rows)";
   if (g.lda % 8 || g.ldb % 8) return "gemm: lda/ldb must be multiples of 8 elements";
-  if (g.lda < g.K || g.ldb < g.K) return "gemm: lda/ldb smaller than K";
+  if (g.lda < (g.a_mn ? g.M : g.K) || g.ldb < (g.b_mn ? g.N : g.K)) return "gemm: lda/ldb smaller than a row";
   if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.B)) & 15) return "gemm: A/B not 16-byte aligned";
   if (!g.C) return "gemm: null output";
   if (reinterpret_cast<uintptr_t>(g.C) & 15) return "gemm: C not 16-byte aligned";
@@ -460,14 +486,20 @@ int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (gemm_check(g)) return -1;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
-      return -2;
+    bool ok = cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<false, false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) == cudaSuccess;
+    if (!ok) return -2;
     attr_done = true;
   }
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, g.A, g.M, g.K, g.lda, BM)) return -3;
-  if (!make_tmap(&tb, g.B, g.N, g.K, g.ldb, BN)) return -3;
+  if (g.a_mn ? !make_tmap(&ta, g.A, g.K, g.M, g.lda, BK) : !make_tmap(&ta, g.A, g.M, g.K, g.lda, BM)) return -3;
+  if (g.b_mn ? !make_tmap(&tb, g.B, g.K, g.N, g.ldb, BK) : !make_tmap(&tb, g.B, g.N, g.K, g.ldb, BN)) return -3;
   EpiParams p;
   p.M = g.M;
   p.N = g.N;
@@ -487,7 +519,14 @@ int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   p.status = g.status;
   const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_bf16_tcgen05_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  if (!g.a_mn && !g.b_mn)
+    gemm_bf16_tcgen05_kernel<false, false><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  else if (g.a_mn && !g.b_mn)
+    gemm_bf16_tcgen05_kernel<true, false><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  else if (!g.a_mn && g.b_mn)
+    gemm_bf16_tcgen05_kernel<false, true><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  else
+    gemm_bf16_tcgen05_kernel<true, true><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

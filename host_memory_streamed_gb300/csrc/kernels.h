@@ -31,10 +31,11 @@ enum EpiMode : int {
 };
 
 struct GemmArgs {
-  const bf16* A = nullptr;  // [M, K], leading dimension lda
+  const bf16* A = nullptr;  // [M, K] (a_mn: stored [K, M]), leading dimension lda
   long lda = 0;
-  const bf16* B = nullptr;  // [N, K], leading dimension ldb
+  const bf16* B = nullptr;  // [N, K] (b_mn: stored [K, N]), leading dimension ldb
   long ldb = 0;
+  bool a_mn = false, b_mn = false;
   int M = 0, N = 0, K = 0;
   int epi = kEpiStoreBf16;
   void* C = nullptr;

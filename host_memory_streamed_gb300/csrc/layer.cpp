@@ -234,7 +234,7 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   dgrad(W.dqkv, D.Dqkv, w.wqkv, D.d, W.dn);
   launch_rmsnorm_bwd(W.dn, a.x, w.g1, a.rstd1, W.dh, dx_in, W.dg_partial, T, D.d, s);
   launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g1, s);
-  stats->kernels += 3 + 4;
+  stats->kernels += 8;  // swiglu, 2 x (rmsnorm bwd + colsum), attention delta + dK/dV + dQ
   return rc;
 }
 

@@ -60,6 +60,31 @@ int mt_op_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M
   return op_cuda(mt::launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
 }
 
+int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M, int32_t N, int32_t K,
+                      int32_t layout, int32_t epilogue, void* C, int64_t ldc, const void* R, int64_t ldr,
+                      int32_t* status, void* stream) {
+  mt::GemmArgs g;
+  g.A = static_cast<const mt::bf16*>(A);
+  g.lda = lda;
+  g.B = static_cast<const mt::bf16*>(B);
+  g.ldb = ldb;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.a_mn = (layout & 1) != 0;
+  g.b_mn = (layout & 2) != 0;
+  g.epi = epilogue;
+  g.C = C;
+  g.ldc = ldc;
+  g.R = static_cast<const mt::bf16*>(R);
+  g.ldr = ldr;
+  g.status = status;
+  if (layout & ~3) return op_fail("gemm: layout must be a combination of MT_GEMM_A_MN and MT_GEMM_B_MN");
+  if (epilogue == MT_EPI_SWIGLU || epilogue == MT_EPI_ROPE) return op_fail("gemm_layout: use mt_op_gemm for SwiGLU/RoPE");
+  if (const char* e = mt::gemm_check(g)) return op_fail(e);
+  return op_cuda(mt::launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
+}
+
 }  // extern "C"
 
 extern "C" {

@@ -150,6 +150,22 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(const void* tile) {
   return d;
 }
 
+// Descriptor for an MN-major operand tile (M or N contiguous) written by TMA
+// as 64-element-wide boxes with 128-byte swizzling: each box is rows of 128
+// bytes (one K index per row), 8-row swizzle atoms 1024 bytes apart along K
+// (stride byte offset); boxes adjacent along M/N are lbo_bytes apart
+// (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(const void* tile, uint32_t lbo_bytes) {
+  const uint64_t addr = smem_u32(tile);
+  uint64_t d = 0;
+  d |= (addr & 0x3FFFFull) >> 4;
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor: kind::f16 with BF16 A/B, FP32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4)                      // D format FP32

@@ -339,7 +339,7 @@ struct mt_model {
   std::string worker_msg;
 
   // threads
-  std::unique_ptr<mt::Pool> adam_pool, pack_pool;
+  std::unique_ptr<mt::Pool> adam_pool, pack_pool, acc_pool;
   std::thread loader, d2h, accum;
   bool stop_threads = false;
   int64_t step_gen = 0;
@@ -571,8 +571,19 @@ void accum_main(mt_model* m) {
       if (m->visits[j.visit].kind == kHead && j.off == 0 && !std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
       const TileLayout& lay = m->layouts[j.tile];
       uint16_t* dst = reinterpret_cast<uint16_t*>(m->tiles[j.tile] + lay.off_g + j.off);
-      const bool fin = copy_grad_check_finite(dst, reinterpret_cast<const uint16_t*>(m->slabs[j.slab]),
-                                              (size_t)(j.bytes / 2));
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
+      // the copy (and NaN/Inf scan) of one slab is split over the accumulator pool
+      const int64_t n = j.bytes / 2;
+      const int nt = m->acc_pool->size();
+      const int64_t piece = std::max<int64_t>(1 << 18, align_up((n + nt - 1) / nt, 2048));
+      std::atomic<bool> fin{true};
+      for (int64_t b = 0; b < n; b += piece) {
+        const int64_t c = std::min(piece, n - b);
+        m->acc_pool->submit([=, &fin] {
+          if (!copy_grad_check_finite(dst + b, src + b, (size_t)c)) fin = false;
+        });
+      }
+      if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
       if (!fin) m->nonfinite = true;
       {
         std::lock_guard<std::mutex> g(m->mu);
@@ -988,6 +999,7 @@ void destroy(mt_model* m) {
   if (m->accum.joinable()) m->accum.join();
   m->adam_pool.reset();
   m->pack_pool.reset();
+  m->acc_pool.reset();
   if (m->s_comp) cudaStreamSynchronize(m->s_comp);
   if (m->s_h2d) cudaStreamSynchronize(m->s_h2d);
   if (m->s_d2h) cudaStreamSynchronize(m->s_d2h);
@@ -1129,6 +1141,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
 
   m->adam_pool.reset(new Pool(m->cfg.n_adam_threads));
   m->pack_pool.reset(new Pool(m->cfg.n_pack_threads));
+  m->acc_pool.reset(new Pool(std::max(1, m->cfg.n_pack_threads)));
   m->loader = std::thread(loader_main, m);
   m->d2h = std::thread(d2h_main, m);
   m->accum = std::thread(accum_main, m);

@@ -51,6 +51,21 @@ int mt_op_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M
                int32_t* status, void* stream);
 
 
+/* Operand layouts of mt_op_gemm_layout. */
+enum { MT_GEMM_A_MN = 1, /* A stored [K, M] (M contiguous), leading dimension lda >= M */
+       MT_GEMM_B_MN = 2  /* B stored [K, N] (N contiguous), leading dimension ldb >= N */ };
+
+/*
+ * mt_op_gemm with either operand stored MN-major, read as such by the tensor
+ * cores (no transpose pass): the backward GEMMs of a linear layer,
+ * dW = dY^T X (both operands MN-major) and dX = dY W (B MN-major).
+ * Epilogues MT_EPI_STORE_BF16, MT_EPI_RESIDUAL_BF16, MT_EPI_F32,
+ * MT_EPI_F32_ACCUMULATE.  Same alignment rules as mt_op_gemm.
+ */
+int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M, int32_t N, int32_t K,
+                      int32_t layout, int32_t epilogue, void* C, int64_t ldc, const void* R, int64_t ldr,
+                      int32_t* status, void* stream);
+
 /*
  * Causal grouped-query attention forward (flash style, one pass over keys).
  * qkv: [batch*seq, ldqkv] BF16 rows (token t = b*seq + s) holding n_heads query
