@@ -675,7 +675,7 @@ const char* attn_check(const AttnArgs& x) {
 
 int launch_attn_fwd(const AttnArgs& x, cudaStream_t s) {
   if (attn_check(x)) return -1;
-  return x.head_dim == 128 ? fwd_impl<128>(x, s) : fwd_impl<64>(x, s);
+  return launch_attn_fwd_tc(x, s);
 }
 
 int launch_attn_bwd(const AttnArgs& x, cudaStream_t s) {

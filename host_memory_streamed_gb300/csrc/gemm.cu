@@ -48,7 +48,7 @@ constexpr int GROUP_M = 16;        // tile raster: 16 M-tiles share each B panel
 constexpr int SMEM_USED = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
 // Launch with the whole 227 KB (one CTA per SM either way); the unused tail
 // keeps every tensor-core read of the last stage inside the allocation.
-constexpr int SMEM_BYTES = 232448;
+constexpr int SMEM_BYTES = 232448 - 256;  // 227 KB less room for the static shared variables
 static_assert(SMEM_USED <= SMEM_BYTES, "shared memory plan exceeds 227 KB");
 
 struct EpiParams {
@@ -449,6 +449,10 @@ int num_sms() {
 }
 
 }  // namespace
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, long rows, long cols, long ld, int box_rows) {
+  return make_tmap(m, base, rows, cols, ld, box_rows);
+}
 
 const char* gemm_check(const GemmArgs& g) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return "gemm: M, N and K must be positive";

@@ -77,6 +77,8 @@ struct AttnArgs {
 };
 const char* attn_check(const AttnArgs& a);
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
+// tcgen05/TMEM forward (attention_tc.cu); same contract as launch_attn_fwd.
+int launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t stream);
 int launch_attn_bwd(const AttnArgs& a, cudaStream_t stream);
 
 // ----------------------------------------------------------------- elementwise

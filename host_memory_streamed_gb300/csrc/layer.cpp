@@ -186,18 +186,19 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   const long T = D.T;
   const Workspace& W = *ws;
   int rc = 0;
-  // Weight gradient dW[N, K] = dY[T, N]^T X[T, K]: both operands transposed to K-major (T contiguous).
+  // Weight gradient dW[N, K] = dY[T, N]^T X[T, K]: both operands read MN-major
+  // (T is the contraction, N and K contiguous), no transpose pass.
   auto wgrad = [&](const bf16* dY, int N, const bf16* X, int K, bf16* dW) {
-    launch_transpose(dY, T, N, N, W.tr_y, T, s);
-    launch_transpose(X, T, K, K, W.tr_x, T, s);
-    stats->kernels += 2;
-    rc |= gemm(mk(W.tr_y, T, W.tr_x, T, N, K, (int)T, kEpiStoreBf16, dW, K, W.status));
+    GemmArgs g = mk(dY, N, X, K, N, K, (int)T, kEpiStoreBf16, dW, K, W.status);
+    g.a_mn = true;
+    g.b_mn = true;
+    rc |= gemm(g);
   };
-  // Data gradient dX[T, K] = dY[T, N] W[N, K]: W transposed to [K, N].
+  // Data gradient dX[T, K] = dY[T, N] W[N, K]: W read MN-major.
   auto dgrad = [&](const bf16* dY, int N, const bf16* Wm, int K, bf16* dX) {
-    launch_transpose(Wm, N, K, K, W.tr_w, N, s);
-    stats->kernels += 1;
-    rc |= gemm(mk(dY, N, W.tr_w, N, (int)T, K, N, kEpiStoreBf16, dX, K, W.status));
+    GemmArgs g = mk(dY, N, Wm, K, (int)T, K, N, kEpiStoreBf16, dX, K, W.status);
+    g.b_mn = true;
+    rc |= gemm(g);
   };
 
   // x_out = h + a Wd^T
@@ -244,22 +245,24 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
   const Workspace& W = *ws;
   int rc = 0;
   launch_rmsnorm_fwd(x_L, w.gf, W.nf, W.rstd_f, T, D.d, eps, s);
-  launch_transpose(w.wh, D.V, D.d, D.d, W.tr_w, D.V, s);  // W_h^T [d, V]
   launch_zero(W.dwh_f32, sizeof(float) * (size_t)D.V * D.d, s);
-  stats->kernels += 2;
+  stats->kernels += 1;
   const float inv_n = 1.0f / (float)T;
   for (long r0 = 0; r0 < T; r0 += W.head_chunk) {
     const long rows = (T - r0) < W.head_chunk ? (T - r0) : W.head_chunk;
     const bf16* nf = W.nf + r0 * D.d;
     rc |= gemm(mk(nf, D.d, w.wh, D.d, (int)rows, D.V, D.d, kEpiF32, W.z, D.V, W.status));
     launch_cross_entropy(W.z, rows, D.V, W.tgt + r0, inv_n, W.dz, W.loss_rows + r0, W.status, s);
-    // d nf = dz W_h
-    rc |= gemm(mk(W.dz, D.V, W.tr_w, D.V, (int)rows, D.d, D.V, kEpiStoreBf16, W.dnf + r0 * D.d, D.d, W.status));
-    // dW_h += dz^T nf
-    launch_transpose(W.dz, rows, D.V, D.V, W.tr_y, rows, s);
-    launch_transpose(nf, rows, D.d, D.d, W.tr_x, rows, s);
-    rc |= gemm(mk(W.tr_y, rows, W.tr_x, rows, D.V, D.d, (int)rows, kEpiF32Accumulate, W.dwh_f32, D.d, W.status));
-    stats->kernels += 3;
+    // d nf = dz W_h  (W_h [V, d] read MN-major)
+    GemmArgs g = mk(W.dz, D.V, w.wh, D.d, (int)rows, D.d, D.V, kEpiStoreBf16, W.dnf + r0 * D.d, D.d, W.status);
+    g.b_mn = true;
+    rc |= gemm(g);
+    // dW_h += dz^T nf  (both operands MN-major, the chunk's tokens are the contraction)
+    g = mk(W.dz, D.V, nf, D.d, D.V, D.d, (int)rows, kEpiF32Accumulate, W.dwh_f32, D.d, W.status);
+    g.a_mn = true;
+    g.b_mn = true;
+    rc |= gemm(g);
+    stats->kernels += 1;
   }
   launch_f32_to_bf16(W.dwh_f32, gv.wh, (long)D.V * D.d, s);
   launch_mean_loss(W.loss_rows, T, inv_n, W.loss, s);

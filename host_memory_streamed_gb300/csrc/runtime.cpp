@@ -239,10 +239,6 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   const long T = D.T;
   const long hc = head_chunk_rows(D);
   const int64_t td = T * D.d * 2;
-  const int64_t maxN = std::max<int64_t>({(int64_t)2 * D.f, D.Dqkv, D.d});
-  const int64_t maxK = std::max<int64_t>({(int64_t)D.f, D.Dq, D.d});
-  const int64_t maxW = std::max<int64_t>({(int64_t)2 * D.f * D.d, (int64_t)D.Dqkv * D.d, (int64_t)D.d * D.Dq,
-                                          (int64_t)D.d * D.f, (int64_t)D.V * D.d});
   auto at = [&](int64_t bytes) { return base ? base + P.add(bytes) : (P.add(bytes), nullptr); };
   Workspace w{};
   w.dx_a = reinterpret_cast<bf16*>(at(td));
@@ -255,9 +251,6 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.dqkv = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dqkv * 2));
   w.delta = reinterpret_cast<float*>(at((int64_t)D.B * D.Hq * D.S * 4));
   w.dg_partial = reinterpret_cast<float*>(at(((T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock) * (int64_t)D.d * 4));
-  w.tr_y = reinterpret_cast<bf16*>(at(std::max<int64_t>(maxN * T, (int64_t)D.V * hc) * 2));
-  w.tr_x = reinterpret_cast<bf16*>(at(std::max<int64_t>(maxK * T, (int64_t)D.d * hc) * 2));
-  w.tr_w = reinterpret_cast<bf16*>(at(maxW * 2));
   w.nf = reinterpret_cast<bf16*>(at(td));
   w.rstd_f = reinterpret_cast<float*>(at(T * 4));
   w.z = reinterpret_cast<float*>(at(hc * (int64_t)D.V * 4));

@@ -89,7 +89,6 @@ struct Workspace {
   bf16 *dh, *da, *dgu, *dn, *dout, *dqkv;
   float* delta;
   float* dg_partial;
-  bf16 *tr_y, *tr_x, *tr_w;  // transposes: dY^T, X^T, W^T
   // head
   bf16* nf;
   float* rstd_f;
