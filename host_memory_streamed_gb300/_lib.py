@@ -14,7 +14,7 @@ MT_OK, MT_EINVAL, MT_ENOMEM, MT_ECUDA, MT_ETIMEDOUT, MT_ESTATE, MT_ENONFINITE, M
 ERROR_NAMES = {0: "MT_OK", -1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_ECUDA", -4: "MT_ETIMEDOUT",
                -5: "MT_ESTATE", -6: "MT_ENONFINITE", -7: "MT_EINTERNAL"}
 
-MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS = 1, 2, 4, 8, 16
+MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS, MT_TRACE = 1, 2, 4, 8, 16, 32
 MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
 EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE = range(6)
@@ -87,8 +87,8 @@ def lib():
         "mt_op_gemm": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, vp, i64, vp, i64, vp, i64,
                                  vp, vp, i32, i32, i32, vp, vp]),
         "mt_op_gemm_layout": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, i64, vp, vp]),
-        "mt_op_attention_fwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp]),
-        "mt_op_attention_bwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp]),
+        "mt_op_attention_fwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp]),
+        "mt_op_attention_bwd": (C.c_int, [vp, i64, i32, i32, i32, i32, i32, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]),
         "mt_op_rmsnorm_fwd": (C.c_int, [vp, vp, vp, vp, i64, i32, f32, vp]),
         "mt_op_rmsnorm_bwd_scratch_floats": (i64, [i64, i32]),
         "mt_op_rmsnorm_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, vp]),

@@ -24,7 +24,7 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-                     f"-I{INCLUDE}", f"-I{CSRC}"]
+                     f"-I{INCLUDE}", f"-I{CSRC}"] + os.environ.get("MT_NVCC_EXTRA", "").split()
 CXX_FLAGS = ["-O3", "-fPIC", "-std=c++17", "-pthread", "-fno-fast-math", "-fno-math-errno", "-Wall", "-Wno-unused-function",
              f"-I{INCLUDE}", f"-I{CSRC}", f"-I{os.path.join(CUDA_HOME, 'include')}"]
 

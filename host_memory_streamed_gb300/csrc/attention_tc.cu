@@ -16,7 +16,7 @@
 //               a factor 2^8, so O is rarely touched; the final O / l and the
 //               log-sum-exp use whichever maximum was kept.
 // Every mbarrier wait is bounded; on expiry the kernel records
-// kStatusGemmTimeout in the status word and unwinds.
+// kStatusAttnFwdTimeout in the status word and unwinds.
 //
 // MegaTrain's templates hold "Attention and MLP kernels" (paperlayer.ai
 // summary §A.4) without specifying them; this kernel is the library's own.
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       for (int j = 0; j < n_kb && !abort_flag; ++j) {
         const int s = j & 1;
         if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1)) {
-          set_status(p.status, kStatusGemmTimeout);
+          set_status(p.status, kStatusAttnFwdTimeout * 1000 + 100 + min(j, 99));
           abort_flag = 1;
           break;
         }
@@ -148,18 +148,24 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         pend[s] = (j >> 1) & 1;
       }
       // every issued load must land before exit
-      if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusGemmTimeout);
+      if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusAttnFwdTimeout * 1000 + 200);
       for (int s = 0; s < 2; ++s)
-        if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusGemmTimeout);
+        if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s]))
+          set_status(p.status, kStatusAttnFwdTimeout * 1000 + 300 + s);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, 128);
       const uint32_t id_pv = idesc_bf16_f32(128, HD) | (1u << 16);  // B (V) MN-major
+      int site = 0;
       bool ok = mbar_wait(q_full, 0);
+      if (!ok) site = 400;
       auto issue_qk = [&](int j) {
         const int s = j & 1;
-        if (!mbar_wait(&kv_full[s], (j >> 1) & 1)) return false;
+        if (!mbar_wait(&kv_full[s], (j >> 1) & 1)) {
+          site = 500 + min(j, 99);
+          return false;
+        }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -179,6 +185,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
           break;
         }
         if (!mbar_wait(&p_full[s], (j >> 1) & 1)) {
+          site = 600 + min(j, 99);
           ok = false;
           break;
         }
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       if (ok) {
         tc_commit(o_full);
       } else {
-        set_status(p.status, kStatusGemmTimeout);
+        set_status(p.status, kStatusAttnFwdTimeout * 1000 + site);
         abort_flag = 1;
       }
     }
@@ -208,9 +215,11 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    int site = 0;
     for (int j = 0; j < n_kb; ++j) {
       const int s = j & 1;
-      if (!mbar_wait(&s_full[s], (j >> 1) & 1)) {
+      if (!mbar_wait_warp(&s_full[s], (j >> 1) & 1)) {
+        site = 700 + min(j, 99);
         ok = false;
         break;
       }
@@ -242,7 +251,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       }
       const float base = (m == -INFINITY) ? 0.f : m;
       // the P buffer is free once PV_{j-2} completed
-      if (j >= 2 && !mbar_wait(&pv_done[s], ((j >> 1) - 1) & 1)) {
+      if (j >= 2 && !mbar_wait_warp(&pv_done[s], ((j >> 1) - 1) & 1)) {
+        site = 800 + min(j, 99);
         ok = false;
         break;
       }
@@ -262,9 +272,11 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         *reinterpret_cast<uint4*>(prow + box * C::BOX + ((cc ^ (r & 7)) << 4)) = w;
       }
       l = l * alpha + rs;
-      if (rescale && j > 0) {
-        // O holds sum_{i<j} P_i V_i: wait for PV_{j-1}, then scale this row in TMEM
-        if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+      // O holds sum_{i<j} P_i V_i.  tcgen05.ld/st are warp-collective, so the
+      // whole warp rescales when any of its rows must (alpha = 1 for the others).
+      if (__any_sync(0xffffffffu, rescale && j > 0)) {
+        if (!mbar_wait_warp(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+          site = 900 + min(j, 99);
           ok = false;
           break;
         }
@@ -284,7 +296,12 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       tc_fence_before();
       mbar_arrive(&p_full[s]);
     }
-    if (ok && mbar_wait(o_full, 0)) {
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !mbar_wait_warp(o_full, 0)) {
+      site = 999;
+      ok = false;
+    }
+    if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
       const bool valid = qrow < S;
@@ -306,7 +323,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       }
       if (valid) p.lse[((long)b * p.Hq + h) * S + qrow] = (m + log2f(l)) * kLn2F;
     } else {
-      set_status(p.status, kStatusGemmTimeout);
+      set_status(p.status, kStatusAttnFwdTimeout * 1000 + site);
       abort_flag = 1;
     }
   }
@@ -351,6 +368,605 @@ int launch_tc(const AttnArgs& x, cudaStream_t s) {
 int launch_attn_fwd_tc(const AttnArgs& x, cudaStream_t s) {
   if (attn_check(x)) return -1;
   return x.head_dim == 128 ? launch_tc<128>(x, s) : launch_tc<64>(x, s);
+}
+
+}  // namespace mt
+
+// ============================================================================
+// Backward on the tensor cores (deterministic, no atomics).
+//
+// dK/dV kernel: one CTA per (128-key block, kv head, batch).  K and V of the
+// block stay in shared memory; the TMA warp streams 64-query blocks of Q and
+// dO for every query head of the group, in a fixed order.  Per query block:
+//   S^T = K Q^T and dP^T = V dO^T      (TMEM, double-buffered)
+//   P^T = exp(S^T * scale - lse[q]), dS^T = P^T * (dP^T - delta[q])
+//                                       (softmax warps: thread = key row)
+//   dV += P^T dO, dK += dS^T Q          (TMEM accumulators; dO and Q are read
+//                                        MN-major from the very tiles used
+//                                        K-major for S^T and dP^T)
+// dQ kernel: one CTA per (128-query block, query head, batch), streaming
+// 64-key blocks: S = Q K^T, dP = dO V^T, dS = P * (dP - delta), dQ += dS K.
+// dK and dQ are scaled by 1/sqrt(hd) and leave through the inverse RoPE
+// rotation when tables are given.
+// ============================================================================
+namespace mt {
+namespace {
+
+constexpr int TB_THREADS = 192;
+
+struct TbParams {
+  int B, S, Hq, Hkv;
+  const float* lse;
+  const float* delta;
+  bf16* dqkv;
+  long ld;  // of dqkv (= ld of qkv)
+  const float* cos_t;
+  const float* sin_t;
+  float sl2;    // scale * log2(e)
+  float scale;  // 1/sqrt(hd)
+  int* status;
+};
+
+// Scale an accumulator row of HD floats, rotate it back through RoPE when
+// tables are given (pairs (c, c + HD/2) are both in this thread), store BF16.
+template <int HD>
+__device__ __forceinline__ void store_row(uint32_t taddr, float scale, bool rope, const float* cs, const float* sn,
+                                          bf16* dst) {
+  float v[HD];
+#pragma unroll
+  for (int c = 0; c < HD / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(r[e]) * scale;
+  }
+  if (rope) {
+#pragma unroll
+    for (int i = 0; i < HD / 2; ++i) {
+      const float c = cs[i], s = sn[i];
+      const float d1 = v[i], d2 = v[i + HD / 2];
+      v[i] = d1 * c + d2 * s;
+      v[i + HD / 2] = d2 * c - d1 * s;
+    }
+  }
+  if (dst) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < HD / 8; ++q)
+      d4[q] = make_uint4(pack2bf(v[q * 8], v[q * 8 + 1]), pack2bf(v[q * 8 + 2], v[q * 8 + 3]),
+                         pack2bf(v[q * 8 + 4], v[q * 8 + 5]), pack2bf(v[q * 8 + 6], v[q * 8 + 7]));
+  }
+}
+
+template <int HD>
+struct TkvCfg {
+  static constexpr int KBOX = 128 * 128;  // 64-column box of 128 key rows
+  static constexpr int QBOX = 64 * 128;   // 64-column box of 64 query rows
+  static constexpr int KV_BYTES = 128 * HD * 2;
+  static constexpr int Q_BYTES = 64 * HD * 2;
+  static constexpr int PT_BYTES = 128 * 64 * 2;  // [128 keys][64 queries] BF16, one box
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;        // 2 stages
+  static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;    // 2 stages
+  static constexpr int OFF_PT = OFF_DO + 2 * Q_BYTES;   // 2 buffers
+  static constexpr int OFF_DST = OFF_PT + 2 * PT_BYTES; // 2 buffers
+  static constexpr int OFF_BAR = OFF_DST + 2 * PT_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(TB_THREADS, 1)
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_do, TbParams p) {
+  using C = TkvCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sPt = smem + C::OFF_PT;
+  uint8_t* sdSt = smem + C::OFF_DST;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bar + 0;
+  uint64_t* qd_full = bar + 1;   // [2]
+  uint64_t* qd_empty = bar + 3;  // [2]
+  uint64_t* s_full = bar + 5;    // [2]
+  uint64_t* ds_full = bar + 7;   // [2]
+  uint64_t* pt_free = bar + 9;   // [2]
+  uint64_t* acc_full = bar + 11;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+  const int S = p.S;
+  const int k0 = blockIdx.x * 128;
+  const int row0 = b * S;
+  const int G = p.Hq / p.Hkv;
+  const int qb_first = k0 / 64;
+  const int n_qb = (S + 63) / 64;
+  const int per_head = n_qb - qb_first;
+  const int total = per_head * G;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qd_full[i], 1);
+      mbar_init(&qd_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&ds_full[i], 128);
+      mbar_init(&pt_free[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // TMEM columns: S^T[2] 0/64, dP^T[2] 128/192, dV 256.., dK 256+HD..
+  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
+
+  auto head_of = [&](int it) { return kvh * G + it / per_head; };
+  auto q0_of = [&](int it) { return (qb_first + it % per_head) * 64; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+#pragma unroll
+      for (int i = 0; i < HD / 64; ++i) {
+        tma_load_2d(sK + i * C::KBOX, &tm_kv, (p.Hq + kvh) * HD + 64 * i, row0 + k0, kv_full);
+        tma_load_2d(sV + i * C::KBOX, &tm_kv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + k0, kv_full);
+      }
+      int pend[2] = {-1, -1};
+      for (int it = 0; it < total && !abort_flag; ++it) {
+        const int st = it & 1;
+        if (it >= 2 && !mbar_wait(&qd_empty[st], ((it >> 1) - 1) & 1)) {
+          set_status(p.status, kStatusAttnBwdTimeout);
+          abort_flag = 1;
+          break;
+        }
+        const int h = head_of(it), q0 = q0_of(it);
+        mbar_arrive_expect_tx(&qd_full[st], 2 * C::Q_BYTES);
+#pragma unroll
+        for (int i = 0; i < HD / 64; ++i) {
+          tma_load_2d(sQ + st * C::Q_BYTES + i * C::QBOX, &tm_q, h * HD + 64 * i, row0 + q0, &qd_full[st]);
+          tma_load_2d(sdO + st * C::Q_BYTES + i * C::QBOX, &tm_do, h * HD + 64 * i, row0 + q0, &qd_full[st]);
+        }
+        pend[st] = (it >> 1) & 1;
+      }
+      if (!mbar_wait(kv_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
+      for (int s = 0; s < 2; ++s)
+        if (pend[s] >= 0 && !mbar_wait(&qd_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64);                 // K/V [keys][hd] x Q/dO [q][hd]^T
+      const uint32_t id_acc = idesc_bf16_f32(128, HD) | (1u << 16);  // P^T/dS^T x dO/Q (MN-major)
+      bool ok = mbar_wait(kv_full, 0);
+      auto issue_s = [&](int it) {
+        const int st = it & 1;
+        if (!mbar_wait(&qd_full[st], (it >> 1) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const int box = kk >> 2, off = (kk & 3) * 32;
+          const uint64_t ka = smem_desc_kmajor_sw128(sK + box * C::KBOX + off);
+          const uint64_t va = smem_desc_kmajor_sw128(sV + box * C::KBOX + off);
+          const uint64_t qb = smem_desc_kmajor_sw128(sQ + st * C::Q_BYTES + box * C::QBOX + off);
+          const uint64_t ob = smem_desc_kmajor_sw128(sdO + st * C::Q_BYTES + box * C::QBOX + off);
+          tc_mma_bf16(tmem + 64u * st, ka, qb, id_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + 128u + 64u * st, va, ob, id_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[st]);
+        return true;
+      };
+      auto issue_acc = [&](int it) {
+        const int st = it & 1;
+        if (!mbar_wait(&ds_full[st], (it >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t ob = smem_desc_mnmajor_sw128(sdO + st * C::Q_BYTES, C::QBOX);
+        const uint64_t qb = smem_desc_mnmajor_sw128(sQ + st * C::Q_BYTES, C::QBOX);
+#pragma unroll
+        for (int kk = 0; kk < 64 / 16; ++kk) {
+          const uint64_t pa = smem_desc_kmajor_sw128(sPt + st * C::PT_BYTES + kk * 32);
+          const uint64_t da = smem_desc_kmajor_sw128(sdSt + st * C::PT_BYTES + kk * 32);
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_bf16(tdV, pa, ob + (uint64_t)(kk * (2048 >> 4)), id_acc, acc);
+          tc_mma_bf16(tdK, da, qb + (uint64_t)(kk * (2048 >> 4)), id_acc, acc);
+        }
+        tc_commit(&qd_empty[st]);
+        tc_commit(&pt_free[st]);
+        return true;
+      };
+      for (int it = 0; ok && it < total; ++it) {
+        if (!issue_s(it)) ok = false;
+        if (ok && it > 0 && !issue_acc(it - 1)) ok = false;
+      }
+      if (ok && total > 0 && !issue_acc(total - 1)) ok = false;
+      if (ok) {
+        tc_commit(acc_full);
+      } else {
+        set_status(p.status, kStatusAttnBwdTimeout);
+        abort_flag = 1;
+      }
+    }
+  } else {
+    // softmax warps: thread <-> key row r
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int key = k0 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < total; ++it) {
+      const int st = it & 1;
+      const int h = head_of(it), q0 = q0_of(it);
+      if (!mbar_wait_warp(&s_full[st], (it >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64], dp[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32], w[32];
+        tmem_ld_32x32b_x32(tmem + 64u * st + lane_off + c * 32, v);
+        tmem_ld_32x32b_x32(tmem + 128u + 64u * st + lane_off + c * 32, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sv[c * 32 + e] = __uint_as_float(v[e]);
+          dp[c * 32 + e] = __uint_as_float(w[e]);
+        }
+      }
+      if (it >= 2 && !mbar_wait_warp(&pt_free[st], ((it >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const float* Lr = p.lse + ((long)b * p.Hq + h) * S;
+      const float* Dl = p.delta + ((long)b * p.Hq + h) * S;
+      uint8_t* prow = sPt + st * C::PT_BYTES + r * 128;
+      uint8_t* drow = sdSt + st * C::PT_BYTES + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float pv[8], dv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = c8 * 8 + e;
+          const int q = q0 + c;
+          float pr = 0.f, dsv = 0.f;
+          if (q < S && key <= q) {
+            pr = exp2f(sv[c] * p.sl2 - Lr[q] * kLog2eF);
+            dsv = pr * (dp[c] - Dl[q]);
+          }
+          pv[e] = pr;
+          dv[e] = dsv;
+        }
+        const int o = ((c8 ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(prow + o) = make_uint4(pack2bf(pv[0], pv[1]), pack2bf(pv[2], pv[3]),
+                                                         pack2bf(pv[4], pv[5]), pack2bf(pv[6], pv[7]));
+        *reinterpret_cast<uint4*>(drow + o) = make_uint4(pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]),
+                                                         pack2bf(dv[4], dv[5]), pack2bf(dv[6], dv[7]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ds_full[st]);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && mbar_wait_warp(acc_full, 0)) {
+      tc_fence_after();
+      const bool valid = key < S;
+      const bool rope = p.cos_t != nullptr;
+      const int pos = valid ? key : 0;
+      const float* cs = rope ? p.cos_t + (long)pos * (HD / 2) : nullptr;
+      const float* sn = rope ? p.sin_t + (long)pos * (HD / 2) : nullptr;
+      bf16* dk = valid ? p.dqkv + (long)(row0 + key) * p.ld + (long)(p.Hq + kvh) * HD : nullptr;
+      bf16* dv = valid ? p.dqkv + (long)(row0 + key) * p.ld + (long)(p.Hq + p.Hkv + kvh) * HD : nullptr;
+      store_row<HD>(tdK + lane_off, p.scale, rope, cs, sn, dk);
+      store_row<HD>(tdV + lane_off, 1.0f, false, nullptr, nullptr, dv);
+    } else {
+      set_status(p.status, kStatusAttnBwdTimeout);
+      abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD>
+struct TdqCfg {
+  static constexpr int QBOX = 128 * 128;  // 64 columns x 128 query rows
+  static constexpr int KBOX = 64 * 128;   // 64 columns x 64 key rows
+  static constexpr int Q_BYTES = 128 * HD * 2;
+  static constexpr int K_BYTES = 64 * HD * 2;
+  static constexpr int DS_BYTES = 128 * 64 * 2;  // [128 q][64 keys], one box
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + Q_BYTES;
+  static constexpr int OFF_K = OFF_DO + Q_BYTES;      // 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;   // 2 stages
+  static constexpr int OFF_DS = OFF_V + 2 * K_BYTES;  // 2 buffers
+  static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(TB_THREADS, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                          const __grid_constant__ CUtensorMap tm_do, TbParams p) {
+  using C = TdqCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sdS = smem + C::OFF_DS;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bar + 0;
+  uint64_t* kv_full = bar + 1;   // [2]
+  uint64_t* kv_empty = bar + 3;  // [2]
+  uint64_t* s_full = bar + 5;    // [2]
+  uint64_t* ds_full = bar + 7;   // [2]
+  uint64_t* ds_free = bar + 9;   // [2]
+  uint64_t* acc_full = bar + 11;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int qb = gridDim.x - 1 - blockIdx.x;
+  const int b = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
+  const int kvh = h * p.Hkv / p.Hq;
+  const int S = p.S;
+  const int q0 = qb * 128;
+  const int row0 = b * S;
+  const int n_kb = min((S + 63) / 64, (q0 + 128 + 63) / 64);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&ds_full[i], 128);
+      mbar_init(&ds_free[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // TMEM columns: S[2] 0/64, dP[2] 128/192, dQ 256..
+  const uint32_t tdQ = tmem + 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+#pragma unroll
+      for (int i = 0; i < HD / 64; ++i) {
+        tma_load_2d(sQ + i * C::QBOX, &tm_q, h * HD + 64 * i, row0 + q0, q_full);
+        tma_load_2d(sdO + i * C::QBOX, &tm_do, h * HD + 64 * i, row0 + q0, q_full);
+      }
+      int pend[2] = {-1, -1};
+      for (int j = 0; j < n_kb && !abort_flag; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1)) {
+          set_status(p.status, kStatusAttnBwdTimeout);
+          abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&kv_full[s], 2 * C::K_BYTES);
+#pragma unroll
+        for (int i = 0; i < HD / 64; ++i) {
+          tma_load_2d(sK + s * C::K_BYTES + i * C::KBOX, &tm_kv, (p.Hq + kvh) * HD + 64 * i, row0 + j * 64,
+                      &kv_full[s]);
+          tma_load_2d(sV + s * C::K_BYTES + i * C::KBOX, &tm_kv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + j * 64,
+                      &kv_full[s]);
+        }
+        pend[s] = (j >> 1) & 1;
+      }
+      if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
+      for (int s = 0; s < 2; ++s)
+        if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64);
+      const uint32_t id_dq = idesc_bf16_f32(128, HD) | (1u << 16);  // dS x K (MN-major)
+      bool ok = mbar_wait(q_full, 0);
+      auto issue_s = [&](int j) {
+        const int s = j & 1;
+        if (!mbar_wait(&kv_full[s], (j >> 1) & 1)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const int box = kk >> 2, off = (kk & 3) * 32;
+          const uint64_t qa = smem_desc_kmajor_sw128(sQ + box * C::QBOX + off);
+          const uint64_t oa = smem_desc_kmajor_sw128(sdO + box * C::QBOX + off);
+          const uint64_t kb = smem_desc_kmajor_sw128(sK + s * C::K_BYTES + box * C::KBOX + off);
+          const uint64_t vb = smem_desc_kmajor_sw128(sV + s * C::K_BYTES + box * C::KBOX + off);
+          tc_mma_bf16(tmem + 64u * s, qa, kb, id_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + 128u + 64u * s, oa, vb, id_s, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[s]);
+        return true;
+      };
+      auto issue_dq = [&](int j) {
+        const int s = j & 1;
+        if (!mbar_wait(&ds_full[s], (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint64_t kb = smem_desc_mnmajor_sw128(sK + s * C::K_BYTES, C::KBOX);
+#pragma unroll
+        for (int kk = 0; kk < 64 / 16; ++kk) {
+          const uint64_t a = smem_desc_kmajor_sw128(sdS + s * C::DS_BYTES + kk * 32);
+          tc_mma_bf16(tdQ, a, kb + (uint64_t)(kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&kv_empty[s]);
+        tc_commit(&ds_free[s]);
+        return true;
+      };
+      for (int j = 0; ok && j < n_kb; ++j) {
+        if (!issue_s(j)) ok = false;
+        if (ok && j > 0 && !issue_dq(j - 1)) ok = false;
+      }
+      if (ok && n_kb > 0 && !issue_dq(n_kb - 1)) ok = false;
+      if (ok) {
+        tc_commit(acc_full);
+      } else {
+        set_status(p.status, kStatusAttnBwdTimeout);
+        abort_flag = 1;
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qrow = q0 + r;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool valid = qrow < S;
+    const long li = ((long)b * p.Hq + h) * S + (valid ? qrow : 0);
+    const float L2 = valid ? p.lse[li] * kLog2eF : INFINITY;
+    const float Dr = valid ? p.delta[li] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kb; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait_warp(&s_full[s], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64], dp[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32], w[32];
+        tmem_ld_32x32b_x32(tmem + 64u * s + lane_off + c * 32, v);
+        tmem_ld_32x32b_x32(tmem + 128u + 64u * s + lane_off + c * 32, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sv[c * 32 + e] = __uint_as_float(v[e]);
+          dp[c * 32 + e] = __uint_as_float(w[e]);
+        }
+      }
+      if (j >= 2 && !mbar_wait_warp(&ds_free[s], ((j >> 1) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int k0 = j * 64;
+      uint8_t* drow = sdS + s * C::DS_BYTES + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float dv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = c8 * 8 + e;
+          float dsv = 0.f;
+          if (k0 + c <= qrow) {
+            const float pr = exp2f(sv[c] * p.sl2 - L2);
+            dsv = pr * (dp[c] - Dr);
+          }
+          dv[e] = dsv;
+        }
+        *reinterpret_cast<uint4*>(drow + ((c8 ^ (r & 7)) << 4)) = make_uint4(
+            pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]), pack2bf(dv[4], dv[5]), pack2bf(dv[6], dv[7]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&ds_full[s]);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && mbar_wait_warp(acc_full, 0)) {
+      tc_fence_after();
+      const bool rope = p.cos_t != nullptr;
+      const int pos = valid ? qrow : 0;
+      const float* cs = rope ? p.cos_t + (long)pos * (HD / 2) : nullptr;
+      const float* sn = rope ? p.sin_t + (long)pos * (HD / 2) : nullptr;
+      bf16* dq = valid ? p.dqkv + (long)(row0 + qrow) * p.ld + (long)h * HD : nullptr;
+      store_row<HD>(tdQ + lane_off, p.scale, rope, cs, sn, dq);
+    } else {
+      set_status(p.status, kStatusAttnBwdTimeout);
+      abort_flag = 1;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD>
+int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
+  using A = TkvCfg<HD>;
+  using Bq = TdqCfg<HD>;
+  static bool init = false;
+  if (!init) {
+    if (cudaFuncSetAttribute(attn_bwd_dkdv_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Bq::SMEM) !=
+            cudaSuccess)
+      return -2;
+    init = true;
+  }
+  const long T = (long)x.batch * x.seq;
+  const long cols = (long)(x.n_heads + 2 * x.n_kv_heads) * HD;
+  CUtensorMap tm_kv128, tm_q64, tm_q128, tm_kv64, tm_do64, tm_do128;
+  if (!make_tmap_bf16(&tm_kv128, x.qkv, T, cols, x.ldqkv, 128) ||
+      !make_tmap_bf16(&tm_q64, x.qkv, T, cols, x.ldqkv, 64) ||
+      !make_tmap_bf16(&tm_q128, x.qkv, T, cols, x.ldqkv, 128) ||
+      !make_tmap_bf16(&tm_kv64, x.qkv, T, cols, x.ldqkv, 64) ||
+      !make_tmap_bf16(&tm_do64, x.dout, T, (long)x.n_heads * HD, x.ldo, 64) ||
+      !make_tmap_bf16(&tm_do128, x.dout, T, (long)x.n_heads * HD, x.ldo, 128))
+    return -3;
+  TbParams p;
+  p.B = x.batch;
+  p.S = x.seq;
+  p.Hq = x.n_heads;
+  p.Hkv = x.n_kv_heads;
+  p.lse = x.lse;
+  p.delta = x.delta;
+  p.dqkv = x.dqkv;
+  p.ld = x.ldqkv;
+  p.cos_t = x.rope_cos;
+  p.sin_t = x.rope_sin;
+  p.scale = 1.0f / sqrtf((float)HD);
+  p.sl2 = p.scale * kLog2eF;
+  p.status = x.status;
+  dim3 g1((x.seq + 127) / 128, x.batch * x.n_kv_heads);
+  attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_kv128, tm_q64, tm_do64, p);
+  dim3 g2((x.seq + 127) / 128, x.batch * x.n_heads);
+  attn_bwd_dq_tc_kernel<HD><<<g2, TB_THREADS, Bq::SMEM, s>>>(tm_q128, tm_kv64, tm_do128, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace
+
+int launch_attn_bwd_tc_main(const AttnArgs& x, cudaStream_t s) {
+  return x.head_dim == 128 ? launch_bwd_tc<128>(x, s) : launch_bwd_tc<64>(x, s);
 }
 
 }  // namespace mt

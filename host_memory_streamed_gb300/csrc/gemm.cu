@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       int tm, tn;
       tile_coords(tile, num_m, num_n, tm, tn);
-      if (!mbar_wait(&tfull[acc], acc_phase)) {
+      if (!mbar_wait_warp(&tfull[acc], acc_phase)) {
         set_status(p.status, kStatusGemmTimeout);
         abort_flag = 1;
         break;

@@ -18,6 +18,8 @@ enum : int {
   kStatusAttnBadShape = 2,
   kStatusIndexOutOfRange = 3,
   kStatusNonFinite = 4,
+  kStatusAttnFwdTimeout = 5,
+  kStatusAttnBwdTimeout = 6,
 };
 
 // ----------------------------------------------------------------- GEMM
@@ -79,6 +81,8 @@ const char* attn_check(const AttnArgs& a);
 int launch_attn_fwd(const AttnArgs& a, cudaStream_t stream);
 // tcgen05/TMEM forward (attention_tc.cu); same contract as launch_attn_fwd.
 int launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t stream);
+// tcgen05/TMEM backward: dK/dV then dQ (attention_tc.cu); delta must already hold rowsum(dO * O).
+int launch_attn_bwd_tc_main(const AttnArgs& a, cudaStream_t stream);
 int launch_attn_bwd(const AttnArgs& a, cudaStream_t stream);
 
 // ----------------------------------------------------------------- elementwise

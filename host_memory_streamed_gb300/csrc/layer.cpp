@@ -108,6 +108,7 @@ int LayerTemplate::gemm(const GemmArgs& g) const {
   stats->kernels += 1;
   stats->gemms += 1;
   stats->gemm_flops += 2.0 * g.M * g.N * g.K;
+  trace(g.a_mn || g.b_mn ? "gemm (MN-major operand)" : "gemm");
   return rc;
 }
 
@@ -135,6 +136,7 @@ int LayerTemplate::forward(const LayerView& w, LayerActs& a, bf16* x_out, bool k
   const long T = D.T;
   int rc = 0;
   launch_rmsnorm_fwd(a.x, w.g1, a.n1, a.rstd1, T, D.d, eps, s);
+  trace("rmsnorm_fwd");
   // qkv = n1 Wqkv^T with rotate-half RoPE on the q and k columns
   GemmArgs g = mk(a.n1, D.d, w.wqkv, D.d, (int)T, D.Dqkv, D.d, kEpiRope, a.qkv, D.Dqkv, ws->status);
   g.rope_cos = ws->rope_cos;
@@ -156,12 +158,14 @@ int LayerTemplate::forward(const LayerView& w, LayerActs& a, bf16* x_out, bool k
   at.lse = a.lse;
   at.status = ws->status;
   rc |= launch_attn_fwd(at, s);
+  trace("attention_fwd");
   // h = x + o Wo^T
   g = mk(a.o, D.Dq, w.wo, D.Dq, (int)T, D.d, D.Dq, kEpiResidualBf16, a.h, D.d, ws->status);
   g.R = a.x;
   g.ldr = D.d;
   rc |= gemm(g);
   launch_rmsnorm_fwd(a.h, w.g2, a.n2, a.rstd2, T, D.d, eps, s);
+  trace("rmsnorm_fwd");
   // a = silu(n2 Wg^T) * (n2 Wu^T) from interleaved gate/up rows
   g = mk(a.n2, D.d, w.wgu, D.d, (int)T, 2 * D.f, D.d, kEpiSwiGLU, a.a, D.f, ws->status);
   if (keep_gu) {
@@ -205,10 +209,12 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   wgrad(dx_out, D.d, a.a, D.f, gv.wd);
   dgrad(dx_out, D.d, w.wd, D.f, W.da);
   launch_swiglu_bwd(W.da, a.gu, W.dgu, T, D.f, s);
+  trace("swiglu_bwd");
   wgrad(W.dgu, 2 * D.f, a.n2, D.d, gv.wgu);
   dgrad(W.dgu, 2 * D.f, w.wgu, D.d, W.dn);
   // dh = dx_out + RMSNorm2^T dn2 ; dg2
   launch_rmsnorm_bwd(W.dn, a.h, w.g2, a.rstd2, dx_out, W.dh, W.dg_partial, T, D.d, s);
+  trace("rmsnorm_bwd");
   launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g2, s);
   // h = x + o Wo^T
   wgrad(W.dh, D.d, a.o, D.Dq, gv.wo);
@@ -231,9 +237,11 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   at.rope_sin = W.rope_sin;
   at.status = W.status;
   rc |= launch_attn_bwd(at, s);
+  trace("attention_bwd");
   wgrad(W.dqkv, D.Dqkv, a.n1, D.d, gv.wqkv);
   dgrad(W.dqkv, D.Dqkv, w.wqkv, D.d, W.dn);
   launch_rmsnorm_bwd(W.dn, a.x, w.g1, a.rstd1, W.dh, dx_in, W.dg_partial, T, D.d, s);
+  trace("rmsnorm_bwd");
   launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g1, s);
   stats->kernels += 8;  // swiglu, 2 x (rmsnorm bwd + colsum), attention delta + dK/dV + dQ
   return rc;
@@ -253,6 +261,7 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
     const bf16* nf = W.nf + r0 * D.d;
     rc |= gemm(mk(nf, D.d, w.wh, D.d, (int)rows, D.V, D.d, kEpiF32, W.z, D.V, W.status));
     launch_cross_entropy(W.z, rows, D.V, W.tgt + r0, inv_n, W.dz, W.loss_rows + r0, W.status, s);
+    trace("cross_entropy");
     // d nf = dz W_h  (W_h [V, d] read MN-major)
     GemmArgs g = mk(W.dz, D.V, w.wh, D.d, (int)rows, D.d, D.V, kEpiStoreBf16, W.dnf + r0 * D.d, D.d, W.status);
     g.b_mn = true;
@@ -265,7 +274,9 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
     stats->kernels += 1;
   }
   launch_f32_to_bf16(W.dwh_f32, gv.wh, (long)D.V * D.d, s);
+  trace("f32_to_bf16");
   launch_mean_loss(W.loss_rows, T, inv_n, W.loss, s);
+  trace("mean_loss");
   launch_rmsnorm_bwd(W.dnf, x_L, w.gf, W.rstd_f, nullptr, dx_L, W.dg_partial, T, D.d, s);
   launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.gf, s);
   stats->kernels += 4;
@@ -274,12 +285,14 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
 
 int LayerTemplate::embed_fwd(const bf16* E, bf16* x0) const {
   launch_embed_fwd(ws->inp, E, x0, dm.T, dm.d, dm.V, ws->status, s);
+  trace("embed_fwd");
   stats->kernels += 1;
   return 0;
 }
 
 int LayerTemplate::embed_bwd(const bf16* dx0, bf16* dE) const {
   launch_embed_bwd(ws->emb_off, ws->emb_pos, dx0, dE, dm.V, dm.d, s);
+  trace("embed_bwd");
   stats->kernels += 1;
   return 0;
 }

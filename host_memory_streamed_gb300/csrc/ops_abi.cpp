@@ -90,7 +90,8 @@ int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, in
 extern "C" {
 
 int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
-                        int32_t n_kv_heads, int32_t head_dim, void* o, int64_t ldo, float* lse, void* stream) {
+                        int32_t n_kv_heads, int32_t head_dim, void* o, int64_t ldo, float* lse, int32_t* status,
+                        void* stream) {
   mt::AttnArgs a;
   a.qkv = static_cast<const mt::bf16*>(qkv);
   a.ldqkv = ldqkv;
@@ -102,6 +103,7 @@ int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
   a.o = static_cast<mt::bf16*>(o);
   a.ldo = ldo;
   a.lse = lse;
+  a.status = status;
   if (const char* e = mt::attn_check(a)) return op_fail(e);
   return op_cuda(mt::launch_attn_fwd(a, static_cast<cudaStream_t>(stream)), "attention forward");
 }
@@ -109,7 +111,7 @@ int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
 int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, const void* o, int64_t ldo, const float* lse,
                         const void* dout, float* delta, void* dqkv, const float* rope_cos, const float* rope_sin,
-                        void* stream) {
+                        int32_t* status, void* stream) {
   mt::AttnArgs a;
   a.qkv = static_cast<const mt::bf16*>(qkv);
   a.ldqkv = ldqkv;
@@ -126,6 +128,7 @@ int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
   a.dqkv = static_cast<mt::bf16*>(dqkv);
   a.rope_cos = rope_cos;
   a.rope_sin = rope_sin;
+  a.status = status;
   if (const char* e = mt::attn_check(a)) return op_fail(e);
   if (!dout || !delta || !dqkv) return op_fail("attention backward: null dout, delta or dqkv");
   if ((rope_cos == nullptr) != (rope_sin == nullptr)) return op_fail("attention backward: cos and sin go together");

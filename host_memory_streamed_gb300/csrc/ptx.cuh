@@ -12,8 +12,12 @@
 
 namespace mt {
 
-// Wait budget for one mbarrier wait (nanoseconds of %globaltimer).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Wait budget for one mbarrier wait (nanoseconds of %globaltimer); a debug
+// build may shorten it (-DMT_WAIT_LIMIT_NS=...).
+#ifndef MT_WAIT_LIMIT_NS
+#define MT_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MT_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
@@ -68,6 +72,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// The same bounded wait done by all 32 lanes of a warp, with a warp-uniform
+// result: warps that go on to warp-collective (.sync.aligned) tcgen05
+// instructions must never split on a wait's outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -281,6 +281,8 @@ struct mt_model {
   int device = 0;
   int K = 1;
   bool resident_mode = false, store_acts = false, single_buffer = false, debug = false, time_kernels = false;
+  bool trace = false;
+  bool undrained = false;
   std::vector<mt::TileLayout> layouts;  // per tile
   std::vector<uint8_t*> tiles;
   std::vector<uint8_t> w_loaded;
@@ -397,6 +399,22 @@ void wait_event(mt_model* m, cudaEvent_t e, const char* what) {
   }
 }
 
+// Wait (bounded) for everything enqueued on a stream so far; false on timeout or error.
+bool drain_stream(cudaStream_t st, int64_t timeout_ms) {
+  cudaEvent_t e;
+  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+  bool ok = cudaEventRecord(e, st) == cudaSuccess;
+  const auto t0 = Clock::now();
+  while (ok) {
+    const cudaError_t r = cudaEventQuery(e);
+    if (r == cudaSuccess) break;
+    if (r != cudaErrorNotReady || ms_since(t0) > (double)timeout_ms) ok = false;
+    else std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  cudaEventDestroy(e);
+  return ok;
+}
+
 void wait_flag(mt_model* m, std::vector<char>& vec, int i, const char* what) {
   std::unique_lock<std::mutex> g(m->mu);
   const bool ok = m->cv.wait_for(g, std::chrono::milliseconds(m->cfg.timeout_ms),
@@ -465,6 +483,7 @@ void loader_main(mt_model* m) {
         }
         MT_CK(cudaEventRecord(m->ev_h2d_b[v], m->s_h2d));
         MT_CK(cudaEventRecord(m->ev_ready[v], m->s_h2d));
+        if (m->trace) std::fprintf(stderr, "[mt trace] loader: tile %d for visit %d enqueued\n", x.tile, v);
         m->rec_h2d_timed[v] = 1;
         set_flag(m, m->rec_ready, v);
       }
@@ -712,11 +731,27 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     m->cv.notify_all();
 
     LayerTemplate tmpl{D, m->cfg.rms_eps, m->s_comp, &m->ws, &m->ls};
+    if (m->trace) {
+      tmpl.trace_ctx = m;
+      tmpl.trace_fn = [](void* ctx, const char* kernel) {
+        mt_model* mm = static_cast<mt_model*>(ctx);
+        const auto t0 = Clock::now();
+        MT_CK(cudaEventRecord(mm->ev_t1, mm->s_comp));
+        wait_event(mm, mm->ev_t1, kernel);
+        int st = 0;
+        MT_CK(cudaMemcpy(&st, mm->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
+        std::fprintf(stderr, "[mt trace]   %-26s %9.3f ms  status %d\n", kernel, ms_since(t0), st);
+        if (st != 0) throw MtError{MT_ETIMEDOUT, std::string("device status ") + std::to_string(st) + " after " + kernel};
+      };
+    }
     bf16* dx_cur = m->ws.dx_a;
     bf16* dx_nxt = m->ws.dx_b;
     for (int v = 0; v < (int)m->visits.size(); ++v) {
       check_abort(m);
       const Visit& x = m->visits[v];
+      if (m->trace)
+        std::fprintf(stderr, "[mt trace] visit %d (tile %d, layer %d, buffer %d, h2d %d) starts\n", v, x.tile,
+                     x.layer, x.buf, (int)x.h2d);
       uint8_t* wb = nullptr;
       if (x.buf >= 0) {
         if (m->resident_mode) {
@@ -789,6 +824,20 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
         MT_CK(cudaEventRecord(m->ev_free[v], m->s_comp));
         set_flag(m, m->rec_free, v);
       }
+      if (m->trace) {
+        // debugging: finish this visit, report its time and the device status
+        const auto t0 = Clock::now();
+        MT_CK(cudaEventRecord(m->ev_t1, m->s_comp));
+        wait_event(m, m->ev_t1, "traced visit");
+        int st = 0;
+        MT_CK(cudaMemcpy(&st, m->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
+        static const char* kind_name[] = {"embed_fwd", "layer_fwd", "head", "recompute", "layer_bwd", "embed_bwd"};
+        std::fprintf(stderr, "[mt trace] visit %d %s tile %d layer %d: %.3f ms after issue, status %d\n", v,
+                     kind_name[x.kind], x.tile, x.layer, ms_since(t0), st);
+        if (st != 0)
+          throw MtError{MT_ETIMEDOUT, "device status " + std::to_string(st) + " after visit " + std::to_string(v) +
+                                          " (" + kind_name[x.kind] + ", layer " + std::to_string(x.layer) + ")"};
+      }
       if (x.grads) {
         if (m->debug) launch_check_finite(reinterpret_cast<bf16*>(gb), lay.w_bytes / 2, m->ws.status, m->s_comp);
         MT_CK(cudaEventRecord(m->ev_grads[v], m->s_comp));
@@ -858,6 +907,10 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     if (status != 0) {
       if (status == kStatusGemmTimeout)
         throw MtError{MT_ETIMEDOUT, "a device-side bounded wait expired (GEMM pipeline)"};
+      if (status == kStatusAttnFwdTimeout || status == kStatusAttnBwdTimeout || status / 1000 == kStatusAttnFwdTimeout ||
+          status / 1000 == kStatusAttnBwdTimeout)
+        throw MtError{MT_ETIMEDOUT, "a device-side bounded wait expired (attention pipeline, code " +
+                                        std::to_string(status) + ")"};
       if (status == kStatusNonFinite) {
         m->nonfinite = true;
       } else {
@@ -877,9 +930,12 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     code = e.code;
     // stop the workers' part of this step and bring the streams to rest
     worker_fail(m, e);
-    cudaStreamSynchronize(m->s_comp);
-    cudaStreamSynchronize(m->s_h2d);
-    cudaStreamSynchronize(m->s_d2h);
+    const bool drained = drain_stream(m->s_comp, m->cfg.timeout_ms) & drain_stream(m->s_h2d, m->cfg.timeout_ms) &
+                         drain_stream(m->s_d2h, m->cfg.timeout_ms);
+    if (!drained) {
+      m->err += " (streams did not drain within the timeout; the handle keeps its buffers until mt_free)";
+      m->undrained = true;
+    }
     m->adam_pool->wait_idle(m->cfg.timeout_ms);
     if (code != MT_EINVAL) m->broken = true;
   }
@@ -993,9 +1049,18 @@ void destroy(mt_model* m) {
   m->adam_pool.reset();
   m->pack_pool.reset();
   m->acc_pool.reset();
-  if (m->s_comp) cudaStreamSynchronize(m->s_comp);
-  if (m->s_h2d) cudaStreamSynchronize(m->s_h2d);
-  if (m->s_d2h) cudaStreamSynchronize(m->s_d2h);
+  bool drained = true;
+  if (m->s_comp) drained &= drain_stream(m->s_comp, m->cfg.timeout_ms);
+  if (m->s_h2d) drained &= drain_stream(m->s_h2d, m->cfg.timeout_ms);
+  if (m->s_d2h) drained &= drain_stream(m->s_d2h, m->cfg.timeout_ms);
+  if (!drained || m->undrained) {
+    // work may still be running against the pinned buffers: leak them rather than free memory in use
+    std::fprintf(stderr, "mt_free: streams still busy after %lld ms; pinned buffers are leaked\n",
+                 (long long)m->cfg.timeout_ms);
+    for (auto t : m->tiles) std::free(t);
+    delete m;
+    return;
+  }
   auto kill = [](std::vector<cudaEvent_t>& v) {
     for (auto e : v)
       if (e) cudaEventDestroy(e);
@@ -1037,6 +1102,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->single_buffer = m->cfg.flags & MT_NO_DOUBLE_BUFFER;
   m->debug = m->cfg.flags & MT_DEBUG_CHECKS;
   m->time_kernels = m->cfg.flags & MT_TIME_KERNELS;
+  m->trace = m->cfg.flags & MT_TRACE;
   if (!sc || !sh || !sd || sc == sh || sc == sd || sh == sd)
     throw MtError{MT_EINVAL, "three distinct CUDA streams are required"};
   MT_CK(cudaGetDevice(&m->device));

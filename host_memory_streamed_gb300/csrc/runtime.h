@@ -129,6 +129,14 @@ struct LayerTemplate {
   const Workspace* ws;
   LaunchStats* stats;
 
+  // Optional debugging hook called after every kernel launch with its name
+  // (used by MT_TRACE to wait for and report each kernel).
+  void (*trace_fn)(void* ctx, const char* kernel) = nullptr;
+  void* trace_ctx = nullptr;
+  void trace(const char* kernel) const {
+    if (trace_fn) trace_fn(trace_ctx, kernel);
+  }
+
   int gemm(const GemmArgs& g) const;
   // x -> x_out (x_out == nullptr: stop after the MLP activation).  keep_gu: also
   // store the gate/up pre-activations (needed by backward).

@@ -53,23 +53,23 @@ def gemm(A, B, out, epilogue=_lib.EPI_STORE_BF16, residual=None, out2=None, rope
                                rope_cols, head_dim, seq, _ptr(status), _stream()))
 
 
-def attention_fwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse):
+def attention_fwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse, status=None):
     _need(qkv, BF16, "qkv")
     _need(o, BF16, "o")
     _need(lse, F32, "lse")
     _chk(_lib.lib().mt_op_attention_fwd(qkv.data_ptr(), qkv.stride(0), batch, seq, n_heads, n_kv_heads, head_dim,
-                                        o.data_ptr(), o.stride(0), lse.data_ptr(), _stream()))
+                                        o.data_ptr(), o.stride(0), lse.data_ptr(), _ptr(status), _stream()))
 
 
 def attention_bwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse, dout, delta, dqkv, rope_cos=None,
-                  rope_sin=None):
+                  rope_sin=None, status=None):
     for t, dt, n in ((qkv, BF16, "qkv"), (o, BF16, "o"), (lse, F32, "lse"), (dout, BF16, "dout"),
                      (delta, F32, "delta"), (dqkv, BF16, "dqkv"), (rope_cos, F32, "rope_cos"),
                      (rope_sin, F32, "rope_sin")):
         _need(t, dt, n)
     _chk(_lib.lib().mt_op_attention_bwd(qkv.data_ptr(), qkv.stride(0), batch, seq, n_heads, n_kv_heads, head_dim,
                                         o.data_ptr(), o.stride(0), lse.data_ptr(), dout.data_ptr(), delta.data_ptr(),
-                                        dqkv.data_ptr(), _ptr(rope_cos), _ptr(rope_sin), _stream()))
+                                        dqkv.data_ptr(), _ptr(rope_cos), _ptr(rope_sin), _ptr(status), _stream()))
 
 
 def rmsnorm_fwd(x, g, y, rstd, eps):

@@ -76,7 +76,10 @@ enum {
   MT_STORE_ACTS = 1u << 1,        /* keep every layer's internals from forward; no recompute (test path) */
   MT_NO_DOUBLE_BUFFER = 1u << 2,  /* one device weight buffer: no H2D/compute overlap (ablation) */
   MT_DEBUG_CHECKS = 1u << 3,      /* NaN/Inf scan of every gradient tile; host event-order asserts */
-  MT_TIME_KERNELS = 1u << 4       /* CUDA-event timing of every GEMM launch (mt_get_step_stats) */
+  MT_TIME_KERNELS = 1u << 4,      /* CUDA-event timing of every GEMM launch (mt_get_step_stats) */
+  MT_TRACE = 1u << 5              /* debugging: wait for every visit (layer pass) to finish, print its kind,
+                                     layer, time and the device status word to stderr, stop at the first
+                                     nonzero status */
 };
 
 /* Tile parts for load/get. */

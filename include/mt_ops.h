@@ -74,9 +74,11 @@ int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, in
  * h*n_kv_heads/n_heads.  o: [batch*seq, ldo] BF16; lse: FP32
  * [batch, n_heads, seq] natural-log log-sum-exp of each score row (scores
  * scaled by 1/sqrt(head_dim)).  head_dim 64 or 128; n_heads % n_kv_heads == 0.
+ * A wait inside the kernel that runs out writes a nonzero code to *status.
  */
 int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
-                        int32_t n_kv_heads, int32_t head_dim, void* o, int64_t ldo, float* lse, void* stream);
+                        int32_t n_kv_heads, int32_t head_dim, void* o, int64_t ldo, float* lse, int32_t* status,
+                        void* stream);
 
 /*
  * Attention backward: given o, lse from the forward and dout (layout of o),
@@ -89,7 +91,7 @@ int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
 int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, const void* o, int64_t ldo, const float* lse,
                         const void* dout, float* delta, void* dqkv, const float* rope_cos, const float* rope_sin,
-                        void* stream);
+                        int32_t* status, void* stream);
 
 /* y = x * rsqrt(mean(x^2) + eps) * g over rows of d (d % 8 == 0); rstd: FP32 [rows]. */
 int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_t rows, int32_t d, float eps,

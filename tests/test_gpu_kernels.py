@@ -277,3 +277,45 @@ def test_transpose_exact(r, c):
     ops.transpose(x, y)
     torch.cuda.synchronize()
     assert torch.equal(y, x.T)
+
+
+def _attention_vs_oracle(qkv, B, S, Hq, Hkv, hd):
+    T = B * S
+    qd = qkv.to(DEV)
+    o = torch.empty(T, Hq * hd, device=DEV, dtype=torch.bfloat16)
+    lse = torch.empty(B * Hq * S, device=DEV)
+    st = torch.zeros(1, device=DEV, dtype=torch.int32)
+    ops.attention_fwd(qd, B, S, Hq, Hkv, hd, o, lse, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    x = qkv.to(D)
+    q = x[:, :Hq * hd].reshape(B, S, Hq, hd)
+    k = x[:, Hq * hd:(Hq + Hkv) * hd].reshape(B, S, Hkv, hd)
+    v = x[:, (Hq + Hkv) * hd:].reshape(B, S, Hkv, hd)
+    o_ref, _ = oracle.causal_gqa_attention(q, k, v)
+    return rel(o, o_ref.reshape(T, -1))
+
+
+def test_attention_rescale_in_part_of_a_warp():
+    """Half of one warp's query rows meet a key, in a later key block, whose
+    score exceeds their running maximum by far more than 2^8, the other half
+    do not: the running-maximum rescale then happens for some lanes of a warp
+    only, which the kernel must handle as one warp."""
+    B, S, Hq, Hkv, hd = 1, 512, 2, 1, 128
+    g = torch.Generator().manual_seed(31)
+    qkv = torch.randn(B * S, (Hq + 2 * Hkv) * hd, generator=g) * 0.5
+    u = torch.randn(hd, generator=g)
+    u = u / u.norm()
+    for r in range(400, 416):  # query rows in key block 3, lanes 16..31 of the warp owning rows 384..415
+        qkv[r, :hd] = 4.0 * u
+    qkv[300, Hq * hd:(Hq + 1) * hd] = 4.0 * u  # key 300 (block 2) aligns with them: score 16/sqrt(128) * ... >> 2^8 in exp
+    qkv[300, Hq * hd:(Hq + 1) * hd] *= 8.0
+    assert _attention_vs_oracle(qkv.to(torch.bfloat16), B, S, Hq, Hkv, hd) < 5e-3
+
+
+def test_attention_long_sequence_step_scale():
+    """Activations at the scale the decoder produces (std ~1.4) over 16 key blocks."""
+    B, S, Hq, Hkv, hd = 1, 2048, 4, 2, 128
+    g = torch.Generator().manual_seed(32)
+    qkv = (torch.randn(B * S, (Hq + 2 * Hkv) * hd, generator=g) * 1.4).to(torch.bfloat16)
+    assert _attention_vs_oracle(qkv, B, S, Hq, Hkv, hd) < 5e-3
