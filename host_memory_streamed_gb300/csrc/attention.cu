@@ -642,21 +642,12 @@ int fwd_impl(const AttnArgs& x, cudaStream_t s) {
 
 template <int HD>
 int bwd_impl(const AttnArgs& x, cudaStream_t s) {
-  static bool init = false;
-  if (!init) {
-    cudaFuncSetAttribute(attn_bwd_dkdv_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkdv_smem<HD>());
-    cudaFuncSetAttribute(attn_bwd_dq_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem<HD>());
-    init = true;
-  }
   AttnDev a = to_dev(x);
   const long rows = (long)x.batch * x.seq * x.n_heads;
   const long threads = rows * (HD / 8);
   attn_delta_kernel<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a);
-  dim3 g1((x.seq + 127) / 128, x.batch * x.n_kv_heads);
-  attn_bwd_dkdv_kernel<HD><<<g1, 256, dkdv_smem<HD>(), s>>>(a);
-  dim3 g2((x.seq + 127) / 128, x.batch * x.n_heads);
-  attn_bwd_dq_kernel<HD><<<g2, 256, dq_smem<HD>(), s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  if (cudaPeekAtLastError() != cudaSuccess) return -4;
+  return launch_attn_bwd_tc_main(x, s);
 }
 
 }  // namespace
