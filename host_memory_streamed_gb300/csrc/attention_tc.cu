@@ -446,13 +446,15 @@ struct TkvCfg {
   static constexpr int KV_BYTES = 128 * HD * 2;
   static constexpr int Q_BYTES = 64 * HD * 2;
   static constexpr int PT_BYTES = 128 * 64 * 2;  // [128 keys][64 queries] BF16, one box
+  static constexpr int QSTAGES = 3;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;        // 2 stages
-  static constexpr int OFF_DO = OFF_Q + 2 * Q_BYTES;    // 2 stages
-  static constexpr int OFF_PT = OFF_DO + 2 * Q_BYTES;   // 2 buffers
-  static constexpr int OFF_DST = OFF_PT + 2 * PT_BYTES; // 2 buffers
-  static constexpr int OFF_BAR = OFF_DST + 2 * PT_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;              // QSTAGES stages
+  static constexpr int OFF_DO = OFF_Q + QSTAGES * Q_BYTES;    // QSTAGES stages
+  static constexpr int OFF_PT = OFF_DO + QSTAGES * Q_BYTES;   // 2 buffers
+  static constexpr int OFF_DST = OFF_PT + 2 * PT_BYTES;       // 2 buffers
+  static constexpr int OFF_LD = OFF_DST + 2 * PT_BYTES;       // lse*log2e | delta of a query block, 2 buffers
+  static constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
 
@@ -469,15 +471,17 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint8_t* sdO = smem + C::OFF_DO;
   uint8_t* sPt = smem + C::OFF_PT;
   uint8_t* sdSt = smem + C::OFF_DST;
+  float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;   // [2]
-  uint64_t* qd_empty = bar + 3;  // [2]
-  uint64_t* s_full = bar + 5;    // [2]
-  uint64_t* ds_full = bar + 7;   // [2]
-  uint64_t* pt_free = bar + 9;   // [2]
-  uint64_t* acc_full = bar + 11;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+  uint64_t* qd_full = bar + 1;   // [3]
+  uint64_t* qd_empty = bar + 4;  // [3]
+  uint64_t* s_full = bar + 7;    // [2]
+  uint64_t* ds_full = bar + 9;   // [2]
+  uint64_t* pt_free = bar + 11;  // [2]
+  uint64_t* acc_full = bar + 13;
+  uint64_t* ld_ready = bar + 14;  // [2]: the staged lse/delta of a query block (128 softmax threads)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 16);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -494,12 +498,15 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::QSTAGES; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&ds_full[i], 128);
       mbar_init(&pt_free[i], 1);
+      mbar_init(&ld_ready[i], 128);
     }
     mbar_init(acc_full, 1);
     fence_barrier_init();
@@ -529,10 +536,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         tma_load_2d(sK + i * C::KBOX, &tm_kv, (p.Hq + kvh) * HD + 64 * i, row0 + k0, kv_full);
         tma_load_2d(sV + i * C::KBOX, &tm_kv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + k0, kv_full);
       }
-      int pend[2] = {-1, -1};
+      int pend[C::QSTAGES] = {-1, -1, -1};
       for (int it = 0; it < total && !abort_flag; ++it) {
-        const int st = it & 1;
-        if (it >= 2 && !mbar_wait(&qd_empty[st], ((it >> 1) - 1) & 1)) {
+        const int st = it % C::QSTAGES;
+        if (it >= C::QSTAGES && !mbar_wait(&qd_empty[st], ((it / C::QSTAGES) - 1) & 1)) {
           set_status(p.status, kStatusAttnBwdTimeout);
           abort_flag = 1;
           break;
@@ -544,10 +551,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           tma_load_2d(sQ + st * C::Q_BYTES + i * C::QBOX, &tm_q, h * HD + 64 * i, row0 + q0, &qd_full[st]);
           tma_load_2d(sdO + st * C::Q_BYTES + i * C::QBOX, &tm_do, h * HD + 64 * i, row0 + q0, &qd_full[st]);
         }
-        pend[st] = (it >> 1) & 1;
+        pend[st] = (it / C::QSTAGES) & 1;
       }
       if (!mbar_wait(kv_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < C::QSTAGES; ++s)
         if (pend[s] >= 0 && !mbar_wait(&qd_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
     }
   } else if (warp == 1) {
@@ -556,38 +563,38 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       const uint32_t id_acc = idesc_bf16_f32(128, HD) | (1u << 16);  // P^T/dS^T x dO/Q (MN-major)
       bool ok = mbar_wait(kv_full, 0);
       auto issue_s = [&](int it) {
-        const int st = it & 1;
-        if (!mbar_wait(&qd_full[st], (it >> 1) & 1)) return false;
+        const int qs = it % C::QSTAGES, b2 = it & 1;
+        if (!mbar_wait(&qd_full[qs], (it / C::QSTAGES) & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const int box = kk >> 2, off = (kk & 3) * 32;
           const uint64_t ka = smem_desc_kmajor_sw128(sK + box * C::KBOX + off);
           const uint64_t va = smem_desc_kmajor_sw128(sV + box * C::KBOX + off);
-          const uint64_t qb = smem_desc_kmajor_sw128(sQ + st * C::Q_BYTES + box * C::QBOX + off);
-          const uint64_t ob = smem_desc_kmajor_sw128(sdO + st * C::Q_BYTES + box * C::QBOX + off);
-          tc_mma_bf16(tmem + 64u * st, ka, qb, id_s, kk > 0 ? 1u : 0u);
-          tc_mma_bf16(tmem + 128u + 64u * st, va, ob, id_s, kk > 0 ? 1u : 0u);
+          const uint64_t qb = smem_desc_kmajor_sw128(sQ + qs * C::Q_BYTES + box * C::QBOX + off);
+          const uint64_t ob = smem_desc_kmajor_sw128(sdO + qs * C::Q_BYTES + box * C::QBOX + off);
+          tc_mma_bf16(tmem + 64u * b2, ka, qb, id_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + 128u + 64u * b2, va, ob, id_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[st]);
+        tc_commit(&s_full[b2]);
         return true;
       };
       auto issue_acc = [&](int it) {
-        const int st = it & 1;
-        if (!mbar_wait(&ds_full[st], (it >> 1) & 1)) return false;
+        const int qs = it % C::QSTAGES, b2 = it & 1;
+        if (!mbar_wait(&ds_full[b2], (it >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t ob = smem_desc_mnmajor_sw128(sdO + st * C::Q_BYTES, C::QBOX);
-        const uint64_t qb = smem_desc_mnmajor_sw128(sQ + st * C::Q_BYTES, C::QBOX);
+        const uint64_t ob = smem_desc_mnmajor_sw128(sdO + qs * C::Q_BYTES, C::QBOX);
+        const uint64_t qb = smem_desc_mnmajor_sw128(sQ + qs * C::Q_BYTES, C::QBOX);
 #pragma unroll
         for (int kk = 0; kk < 64 / 16; ++kk) {
-          const uint64_t pa = smem_desc_kmajor_sw128(sPt + st * C::PT_BYTES + kk * 32);
-          const uint64_t da = smem_desc_kmajor_sw128(sdSt + st * C::PT_BYTES + kk * 32);
+          const uint64_t pa = smem_desc_kmajor_sw128(sPt + b2 * C::PT_BYTES + kk * 32);
+          const uint64_t da = smem_desc_kmajor_sw128(sdSt + b2 * C::PT_BYTES + kk * 32);
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           tc_mma_bf16(tdV, pa, ob + (uint64_t)(kk * (2048 >> 4)), id_acc, acc);
           tc_mma_bf16(tdK, da, qb + (uint64_t)(kk * (2048 >> 4)), id_acc, acc);
         }
-        tc_commit(&qd_empty[st]);
-        tc_commit(&pt_free[st]);
+        tc_commit(&qd_empty[qs]);
+        tc_commit(&pt_free[b2]);
         return true;
       };
       for (int it = 0; ok && it < total; ++it) {
@@ -612,7 +619,18 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     for (int it = 0; it < total; ++it) {
       const int st = it & 1;
       const int h = head_of(it), q0 = q0_of(it);
-      if (!mbar_wait_warp(&s_full[st], (it >> 1) & 1)) {
+      // stage lse (log2 units) and delta of the 64 queries once for all 128 rows
+      float* ld = sLD + st * 128;
+      {
+        const int t = r & 63, q = q0 + t;
+        const long idx = ((long)b * p.Hq + h) * S + q;
+        if (r < 64)
+          ld[t] = q < S ? p.lse[idx] * kLog2eF : INFINITY;
+        else
+          ld[64 + t] = q < S ? p.delta[idx] : 0.f;
+      }
+      mbar_arrive(&ld_ready[st]);
+      if (!mbar_wait_warp(&ld_ready[st], (it >> 1) & 1) || !mbar_wait_warp(&s_full[st], (it >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -634,8 +652,6 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         ok = false;
         break;
       }
-      const float* Lr = p.lse + ((long)b * p.Hq + h) * S;
-      const float* Dl = p.delta + ((long)b * p.Hq + h) * S;
       uint8_t* prow = sPt + st * C::PT_BYTES + r * 128;
       uint8_t* drow = sdSt + st * C::PT_BYTES + r * 128;
 #pragma unroll
@@ -647,8 +663,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           const int q = q0 + c;
           float pr = 0.f, dsv = 0.f;
           if (q < S && key <= q) {
-            pr = exp2f(sv[c] * p.sl2 - Lr[q] * kLog2eF);
-            dsv = pr * (dp[c] - Dl[q]);
+            pr = exp2f(sv[c] * p.sl2 - ld[c]);
+            dsv = pr * (dp[c] - ld[64 + c]);
           }
           pv[e] = pr;
           dv[e] = dsv;
@@ -695,11 +711,12 @@ struct TdqCfg {
   static constexpr int Q_BYTES = 128 * HD * 2;
   static constexpr int K_BYTES = 64 * HD * 2;
   static constexpr int DS_BYTES = 128 * 64 * 2;  // [128 q][64 keys], one box
+  static constexpr int KSTAGES = 4;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + Q_BYTES;
-  static constexpr int OFF_K = OFF_DO + Q_BYTES;      // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;   // 2 stages
-  static constexpr int OFF_DS = OFF_V + 2 * K_BYTES;  // 2 buffers
+  static constexpr int OFF_K = OFF_DO + Q_BYTES;            // KSTAGES stages
+  static constexpr int OFF_V = OFF_K + KSTAGES * K_BYTES;   // KSTAGES stages
+  static constexpr int OFF_DS = OFF_V + KSTAGES * K_BYTES;  // 2 buffers
   static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
@@ -718,13 +735,13 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint8_t* sdS = smem + C::OFF_DS;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_empty = bar + 3;  // [2]
-  uint64_t* s_full = bar + 5;    // [2]
-  uint64_t* ds_full = bar + 7;   // [2]
-  uint64_t* ds_free = bar + 9;   // [2]
-  uint64_t* acc_full = bar + 11;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+  uint64_t* kv_full = bar + 1;   // [4]
+  uint64_t* kv_empty = bar + 5;  // [4]
+  uint64_t* s_full = bar + 9;    // [2]
+  uint64_t* ds_full = bar + 11;  // [2]
+  uint64_t* ds_free = bar + 13;  // [2]
+  uint64_t* acc_full = bar + 15;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 16);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -739,9 +756,11 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::KSTAGES; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&ds_full[i], 128);
       mbar_init(&ds_free[i], 1);
@@ -771,10 +790,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         tma_load_2d(sQ + i * C::QBOX, &tm_q, h * HD + 64 * i, row0 + q0, q_full);
         tma_load_2d(sdO + i * C::QBOX, &tm_do, h * HD + 64 * i, row0 + q0, q_full);
       }
-      int pend[2] = {-1, -1};
+      int pend[C::KSTAGES] = {-1, -1, -1, -1};
       for (int j = 0; j < n_kb && !abort_flag; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1)) {
+        const int s = j % C::KSTAGES;
+        if (j >= C::KSTAGES && !mbar_wait(&kv_empty[s], ((j / C::KSTAGES) - 1) & 1)) {
           set_status(p.status, kStatusAttnBwdTimeout);
           abort_flag = 1;
           break;
@@ -787,10 +806,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           tma_load_2d(sV + s * C::K_BYTES + i * C::KBOX, &tm_kv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + j * 64,
                       &kv_full[s]);
         }
-        pend[s] = (j >> 1) & 1;
+        pend[s] = (j / C::KSTAGES) & 1;
       }
       if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < C::KSTAGES; ++s)
         if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
     }
   } else if (warp == 1) {
@@ -799,34 +818,34 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       const uint32_t id_dq = idesc_bf16_f32(128, HD) | (1u << 16);  // dS x K (MN-major)
       bool ok = mbar_wait(q_full, 0);
       auto issue_s = [&](int j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_full[s], (j >> 1) & 1)) return false;
+        const int ks = j % C::KSTAGES, b2 = j & 1;
+        if (!mbar_wait(&kv_full[ks], (j / C::KSTAGES) & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const int box = kk >> 2, off = (kk & 3) * 32;
           const uint64_t qa = smem_desc_kmajor_sw128(sQ + box * C::QBOX + off);
           const uint64_t oa = smem_desc_kmajor_sw128(sdO + box * C::QBOX + off);
-          const uint64_t kb = smem_desc_kmajor_sw128(sK + s * C::K_BYTES + box * C::KBOX + off);
-          const uint64_t vb = smem_desc_kmajor_sw128(sV + s * C::K_BYTES + box * C::KBOX + off);
-          tc_mma_bf16(tmem + 64u * s, qa, kb, id_s, kk > 0 ? 1u : 0u);
-          tc_mma_bf16(tmem + 128u + 64u * s, oa, vb, id_s, kk > 0 ? 1u : 0u);
+          const uint64_t kb = smem_desc_kmajor_sw128(sK + ks * C::K_BYTES + box * C::KBOX + off);
+          const uint64_t vb = smem_desc_kmajor_sw128(sV + ks * C::K_BYTES + box * C::KBOX + off);
+          tc_mma_bf16(tmem + 64u * b2, qa, kb, id_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + 128u + 64u * b2, oa, vb, id_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[s]);
+        tc_commit(&s_full[b2]);
         return true;
       };
       auto issue_dq = [&](int j) {
-        const int s = j & 1;
-        if (!mbar_wait(&ds_full[s], (j >> 1) & 1)) return false;
+        const int ks = j % C::KSTAGES, b2 = j & 1;
+        if (!mbar_wait(&ds_full[b2], (j >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t kb = smem_desc_mnmajor_sw128(sK + s * C::K_BYTES, C::KBOX);
+        const uint64_t kb = smem_desc_mnmajor_sw128(sK + ks * C::K_BYTES, C::KBOX);
 #pragma unroll
         for (int kk = 0; kk < 64 / 16; ++kk) {
-          const uint64_t a = smem_desc_kmajor_sw128(sdS + s * C::DS_BYTES + kk * 32);
+          const uint64_t a = smem_desc_kmajor_sw128(sdS + b2 * C::DS_BYTES + kk * 32);
           tc_mma_bf16(tdQ, a, kb + (uint64_t)(kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&kv_empty[s]);
-        tc_commit(&ds_free[s]);
+        tc_commit(&kv_empty[ks]);
+        tc_commit(&ds_free[b2]);
         return true;
       };
       for (int j = 0; ok && j < n_kb; ++j) {
