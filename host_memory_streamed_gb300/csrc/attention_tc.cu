@@ -392,7 +392,7 @@ int launch_attn_fwd_tc(const AttnArgs& x, cudaStream_t s) {
 namespace mt {
 namespace {
 
-constexpr int TB_THREADS = 192;
+constexpr int TB_THREADS = 320;  // TMA warp, MMA warp, 8 softmax warps (two per TMEM lane group)
 
 struct TbParams {
   int B, S, Hq, Hkv;
@@ -407,35 +407,66 @@ struct TbParams {
   int* status;
 };
 
-// Scale an accumulator row of HD floats, rotate it back through RoPE when
-// tables are given (pairs (c, c + HD/2) are both in this thread), store BF16.
+// 32 lanes x 16 consecutive 32-bit TMEM columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Half of an accumulator row held by one of the two warps that share a TMEM
+// lane group: columns [h*W, h*W+W) and [HD/2 + h*W, +W) with W = HD/4, so the
+// rotate-half pairs (i, i + HD/2) stay in one thread.  Scales, applies the
+// inverse RoPE rotation when tables are given, stores BF16.
 template <int HD>
-__device__ __forceinline__ void store_row(uint32_t taddr, float scale, bool rope, const float* cs, const float* sn,
-                                          bf16* dst) {
-  float v[HD];
-#pragma unroll
-  for (int c = 0; c < HD / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(taddr + c * 32, r);
+__device__ __forceinline__ void store_half_row(uint32_t taddr, int h, float scale, bool rope, const float* cs,
+                                               const float* sn, bf16* dst) {
+  constexpr int W = HD / 4;
+  float a[W], c2[W];
+  if constexpr (W == 32) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(taddr + h * W, r0);
+    tmem_ld_32x32b_x32(taddr + HD / 2 + h * W, r1);
     tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[c * 32 + e] = __uint_as_float(r[e]) * scale;
+    for (int e = 0; e < W; ++e) {
+      a[e] = __uint_as_float(r0[e]) * scale;
+      c2[e] = __uint_as_float(r1[e]) * scale;
+    }
+  } else {
+    uint32_t r0[16], r1[16];
+    tmem_ld_32x32b_x16(taddr + h * W, r0);
+    tmem_ld_32x32b_x16(taddr + HD / 2 + h * W, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < W; ++e) {
+      a[e] = __uint_as_float(r0[e]) * scale;
+      c2[e] = __uint_as_float(r1[e]) * scale;
+    }
   }
   if (rope) {
 #pragma unroll
-    for (int i = 0; i < HD / 2; ++i) {
-      const float c = cs[i], s = sn[i];
-      const float d1 = v[i], d2 = v[i + HD / 2];
-      v[i] = d1 * c + d2 * s;
-      v[i + HD / 2] = d2 * c - d1 * s;
+    for (int e = 0; e < W; ++e) {
+      const int i = h * W + e;
+      const float c = cs[i], sv = sn[i];
+      const float d1 = a[e], d2 = c2[e];
+      a[e] = d1 * c + d2 * sv;
+      c2[e] = d2 * c - d1 * sv;
     }
   }
   if (dst) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    uint4* d0 = reinterpret_cast<uint4*>(dst + h * W);
+    uint4* d1 = reinterpret_cast<uint4*>(dst + HD / 2 + h * W);
 #pragma unroll
-    for (int q = 0; q < HD / 8; ++q)
-      d4[q] = make_uint4(pack2bf(v[q * 8], v[q * 8 + 1]), pack2bf(v[q * 8 + 2], v[q * 8 + 3]),
-                         pack2bf(v[q * 8 + 4], v[q * 8 + 5]), pack2bf(v[q * 8 + 6], v[q * 8 + 7]));
+    for (int q = 0; q < W / 8; ++q) {
+      d0[q] = make_uint4(pack2bf(a[q * 8], a[q * 8 + 1]), pack2bf(a[q * 8 + 2], a[q * 8 + 3]),
+                         pack2bf(a[q * 8 + 4], a[q * 8 + 5]), pack2bf(a[q * 8 + 6], a[q * 8 + 7]));
+      d1[q] = make_uint4(pack2bf(c2[q * 8], c2[q * 8 + 1]), pack2bf(c2[q * 8 + 2], c2[q * 8 + 3]),
+                         pack2bf(c2[q * 8 + 4], c2[q * 8 + 5]), pack2bf(c2[q * 8 + 6], c2[q * 8 + 7]));
+    }
   }
 }
 
@@ -504,9 +535,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&ds_full[i], 128);
+      mbar_init(&ds_full[i], 256);
       mbar_init(&pt_free[i], 1);
-      mbar_init(&ld_ready[i], 128);
+      mbar_init(&ld_ready[i], 256);
     }
     mbar_init(acc_full, 1);
     fence_barrier_init();
@@ -610,21 +641,23 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
     }
   } else {
-    // softmax warps: thread <-> key row r
+    // softmax warps 2..9: thread <-> key row r, half hf of the 64 query columns
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
+    const int tid = (warp - 2) * 32 + lane;  // 0..255
     const int key = k0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
     for (int it = 0; it < total; ++it) {
       const int st = it & 1;
       const int h = head_of(it), q0 = q0_of(it);
-      // stage lse (log2 units) and delta of the 64 queries once for all 128 rows
+      // stage lse (log2 units) and delta of the 64 queries once for all rows
       float* ld = sLD + st * 128;
-      {
-        const int t = r & 63, q = q0 + t;
+      if (tid < 128) {
+        const int t = tid & 63, q = q0 + t;
         const long idx = ((long)b * p.Hq + h) * S + q;
-        if (r < 64)
+        if (tid < 64)
           ld[t] = q < S ? p.lse[idx] * kLog2eF : INFINITY;
         else
           ld[64 + t] = q < S ? p.delta[idx] : 0.f;
@@ -635,19 +668,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         break;
       }
       tc_fence_after();
-      float sv[64], dp[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32], w[32];
-        tmem_ld_32x32b_x32(tmem + 64u * st + lane_off + c * 32, v);
-        tmem_ld_32x32b_x32(tmem + 128u + 64u * st + lane_off + c * 32, w);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[c * 32 + e] = __uint_as_float(v[e]);
-          dp[c * 32 + e] = __uint_as_float(w[e]);
-        }
-      }
+      uint32_t sv[32], dp[32];
+      tmem_ld_32x32b_x32(tmem + 64u * st + lane_off + hf * 32, sv);
+      tmem_ld_32x32b_x32(tmem + 128u + 64u * st + lane_off + hf * 32, dp);
+      tmem_wait_ld();
       if (it >= 2 && !mbar_wait_warp(&pt_free[st], ((it >> 1) - 1) & 1)) {
         ok = false;
         break;
@@ -655,21 +679,21 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       uint8_t* prow = sPt + st * C::PT_BYTES + r * 128;
       uint8_t* drow = sdSt + st * C::PT_BYTES + r * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int k8 = 0; k8 < 4; ++k8) {
         float pv[8], dv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
+          const int cl = k8 * 8 + e, c = hf * 32 + cl;
           const int q = q0 + c;
           float pr = 0.f, dsv = 0.f;
           if (q < S && key <= q) {
-            pr = exp2f(sv[c] * p.sl2 - ld[c]);
-            dsv = pr * (dp[c] - ld[64 + c]);
+            pr = exp2f(__uint_as_float(sv[cl]) * p.sl2 - ld[c]);
+            dsv = pr * (__uint_as_float(dp[cl]) - ld[64 + c]);
           }
           pv[e] = pr;
           dv[e] = dsv;
         }
-        const int o = ((c8 ^ (r & 7)) << 4);
+        const int o = (((hf * 4 + k8) ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(prow + o) = make_uint4(pack2bf(pv[0], pv[1]), pack2bf(pv[2], pv[3]),
                                                          pack2bf(pv[4], pv[5]), pack2bf(pv[6], pv[7]));
         *reinterpret_cast<uint4*>(drow + o) = make_uint4(pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]),
@@ -689,8 +713,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       const float* sn = rope ? p.sin_t + (long)pos * (HD / 2) : nullptr;
       bf16* dk = valid ? p.dqkv + (long)(row0 + key) * p.ld + (long)(p.Hq + kvh) * HD : nullptr;
       bf16* dv = valid ? p.dqkv + (long)(row0 + key) * p.ld + (long)(p.Hq + p.Hkv + kvh) * HD : nullptr;
-      store_row<HD>(tdK + lane_off, p.scale, rope, cs, sn, dk);
-      store_row<HD>(tdV + lane_off, 1.0f, false, nullptr, nullptr, dv);
+      store_half_row<HD>(tdK + lane_off, hf, p.scale, rope, cs, sn, dk);
+      store_half_row<HD>(tdV + lane_off, hf, 1.0f, false, nullptr, nullptr, dv);
     } else {
       set_status(p.status, kStatusAttnBwdTimeout);
       abort_flag = 1;
@@ -762,7 +786,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&ds_full[i], 128);
+      mbar_init(&ds_full[i], 256);
       mbar_init(&ds_free[i], 1);
     }
     mbar_init(acc_full, 1);
@@ -861,7 +885,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
     }
   } else {
+    // softmax warps 2..9: thread <-> query row r, half hf of the 64 key columns
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = q0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -877,19 +903,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         break;
       }
       tc_fence_after();
-      float sv[64], dp[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32], w[32];
-        tmem_ld_32x32b_x32(tmem + 64u * s + lane_off + c * 32, v);
-        tmem_ld_32x32b_x32(tmem + 128u + 64u * s + lane_off + c * 32, w);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          sv[c * 32 + e] = __uint_as_float(v[e]);
-          dp[c * 32 + e] = __uint_as_float(w[e]);
-        }
-      }
+      uint32_t sv[32], dp[32];
+      tmem_ld_32x32b_x32(tmem + 64u * s + lane_off + hf * 32, sv);
+      tmem_ld_32x32b_x32(tmem + 128u + 64u * s + lane_off + hf * 32, dp);
+      tmem_wait_ld();
       if (j >= 2 && !mbar_wait_warp(&ds_free[s], ((j >> 1) - 1) & 1)) {
         ok = false;
         break;
@@ -897,19 +914,19 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       const int k0 = j * 64;
       uint8_t* drow = sdS + s * C::DS_BYTES + r * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int k8 = 0; k8 < 4; ++k8) {
         float dv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
+          const int cl = k8 * 8 + e, c = hf * 32 + cl;
           float dsv = 0.f;
           if (k0 + c <= qrow) {
-            const float pr = exp2f(sv[c] * p.sl2 - L2);
-            dsv = pr * (dp[c] - Dr);
+            const float pr = exp2f(__uint_as_float(sv[cl]) * p.sl2 - L2);
+            dsv = pr * (__uint_as_float(dp[cl]) - Dr);
           }
           dv[e] = dsv;
         }
-        *reinterpret_cast<uint4*>(drow + ((c8 ^ (r & 7)) << 4)) = make_uint4(
+        *reinterpret_cast<uint4*>(drow + (((hf * 4 + k8) ^ (r & 7)) << 4)) = make_uint4(
             pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]), pack2bf(dv[4], dv[5]), pack2bf(dv[6], dv[7]));
       }
       fence_proxy_async_smem();
@@ -924,7 +941,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       const float* cs = rope ? p.cos_t + (long)pos * (HD / 2) : nullptr;
       const float* sn = rope ? p.sin_t + (long)pos * (HD / 2) : nullptr;
       bf16* dq = valid ? p.dqkv + (long)(row0 + qrow) * p.ld + (long)h * HD : nullptr;
-      store_row<HD>(tdQ + lane_off, p.scale, rope, cs, sn, dq);
+      store_half_row<HD>(tdQ + lane_off, hf, p.scale, rope, cs, sn, dq);
     } else {
       set_status(p.status, kStatusAttnBwdTimeout);
       abort_flag = 1;
