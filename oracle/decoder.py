@@ -53,6 +53,8 @@ __all__ = [
     "rope_backward",
     "causal_gqa_attention",
     "causal_gqa_attention_backward",
+    "attention_rows",
+    "attention_key_grads",
     "swiglu",
     "swiglu_backward",
     "layer_forward",
@@ -227,6 +229,58 @@ def causal_gqa_attention_backward(do, q, k, v, probs):
             dk[b, :, j, :] += (ds.T @ q[b, :, h, :]) * scale
             dv[b, :, j, :] += p.T @ dob
     return dq, dk, dv
+
+
+def attention_rows(q, k, v, rows, do=None):
+    """The same causal attention for selected query rows of one head.
+
+    q [S, hd] (one query head), k, v [S, hd] (its kv head); for each row i in
+    ``rows``: scores over keys 0..i, o_i = softmax(scores) v, lse_i =
+    logsumexp(scores); with ``do`` [S, hd], also dq_i = (P * (dP - rowsum(P*dP))) k * scale.
+    Cost O(len(rows) * S * hd): usable at long sequences.  Returns (o, lse, dq)
+    stacked over ``rows`` (dq is None without ``do``).
+    """
+    hd = q.shape[-1]
+    scale = 1.0 / math.sqrt(hd)
+    os_, ls_, dq_ = [], [], []
+    for i in rows:
+        sc = (k[: i + 1] @ q[i]) * scale
+        lse = torch.logsumexp(sc, dim=0)
+        p = torch.exp(sc - lse)
+        os_.append(p @ v[: i + 1])
+        ls_.append(lse)
+        if do is not None:
+            dp = v[: i + 1] @ do[i]
+            ds = p * (dp - (p * dp).sum())
+            dq_.append((ds @ k[: i + 1]) * scale)
+    dq = torch.stack(dq_) if do is not None else None
+    return torch.stack(os_), torch.stack(ls_), dq
+
+
+def attention_key_grads(qs, k, v, dos, j):
+    """dk_j and dv_j of key position j of one kv head.
+
+    qs [G, S, hd] and dos [G, S, hd]: the query heads that read this kv head
+    and their output gradients; k, v [S, hd].  Sums over every query row
+    i >= j of every head in the group: dv_j = sum P_ij dO_i and
+    dk_j = sum dS_ij q_i * scale with P, dS of the full causal rows i.
+    Cost O(G * (S - j) * S * hd).
+    """
+    G, S, hd = qs.shape
+    scale = 1.0 / math.sqrt(hd)
+    mask = torch.arange(S)[None, :] > torch.arange(j, S)[:, None]  # key > query
+    dk = torch.zeros(hd, dtype=k.dtype)
+    dv = torch.zeros(hd, dtype=v.dtype)
+    for g in range(G):
+        qi = qs[g, j:]
+        sc = (qi @ k.T) * scale
+        sc = sc.masked_fill(mask, float("-inf"))
+        p = torch.softmax(sc, dim=-1)
+        dp = dos[g, j:] @ v.T
+        ds = p * (dp - (p * dp).sum(dim=-1, keepdim=True))
+        dv += p[:, j] @ dos[g, j:]
+        dk += (ds[:, j] @ qi) * scale
+    return dk, dv
 
 
 # ----------------------------------------------------------------------------

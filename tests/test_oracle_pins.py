@@ -171,6 +171,32 @@ def test_attention_special_cases():
     assert torch.allclose(o1[0, 0], v[0, 0].repeat_interleave(2, 0).reshape(6, 8), atol=1e-15)
 
 
+def test_attention_row_functions_agree_with_full_matrix():
+    """The per-row and per-key forms (for long sequences) give the full-matrix
+    oracle's output, lse, dq, dk and dv."""
+    g = torch.Generator().manual_seed(41)
+    S, hd, G = 37, 16, 3
+    q = torch.randn(1, S, G, hd, generator=g)
+    k = torch.randn(1, S, 1, hd, generator=g)
+    v = torch.randn(1, S, 1, hd, generator=g)
+    do = torch.randn(1, S, G, hd, generator=g)
+    o, probs = oracle.causal_gqa_attention(q, k, v)
+    dq, dk, dv = oracle.causal_gqa_attention_backward(do, q, k, v, probs)
+    rows = [0, 5, 36]
+    for h in range(G):
+        o_r, lse_r, dq_r = oracle.attention_rows(q[0, :, h], k[0, :, 0], v[0, :, 0], rows, do[0, :, h])
+        assert torch.allclose(o_r, o[0, rows, h], atol=1e-13)
+        assert torch.allclose(dq_r, dq[0, rows, h], atol=1e-12)
+        sc = (q[0, :, h] @ k[0, :, 0].T) / math.sqrt(hd)
+        sc = sc.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+        assert torch.allclose(lse_r, torch.logsumexp(sc, -1)[rows], atol=1e-13)
+    for j in (0, 20, 36):
+        dk_j, dv_j = oracle.attention_key_grads(q[0].permute(1, 0, 2), k[0, :, 0], v[0, :, 0],
+                                                do[0].permute(1, 0, 2), j)
+        assert torch.allclose(dk_j, dk[0, j, 0], atol=1e-12)
+        assert torch.allclose(dv_j, dv[0, j, 0], atol=1e-12)
+
+
 # ---------------------------------------------------------------- SwiGLU
 
 def test_swiglu_matches_library_and_autograd():
