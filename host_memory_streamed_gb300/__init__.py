@@ -202,6 +202,21 @@ class StreamedDecoder:
         self._check(rc)
         return loss.value
 
+    def layer_pass(self, layer, x_in, dx_out=None, x_out=None, dx_in=None):
+        """One decoder layer's forward (and backward, given dx_out) on device BF16
+        [batch*seq, d_model] activations; the layer's gradient lands in its host
+        tile's G section (see ``grads``).  Adam does not run."""
+        c = self.cfg
+        shape = (c.batch * c.seq, c.d_model)
+        for t, n in ((x_in, "x_in"), (dx_out, "dx_out"), (x_out, "x_out"), (dx_in, "dx_in")):
+            if t is None:
+                continue
+            if not t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != shape or not t.is_contiguous():
+                raise TypeError(f"{n} must be a contiguous CUDA bfloat16 tensor of shape {shape}")
+        p = lambda t: None if t is None else t.data_ptr()
+        torch.cuda.current_stream(self.device).synchronize()
+        self._check(self._L.mt_layer_pass(self._h, int(layer), p(x_in), p(dx_out), p(x_out), p(dx_in)))
+
     def stats(self) -> dict:
         st = _lib.MtStepStats()
         self._check(self._L.mt_get_step_stats(self._h, C.byref(st)))

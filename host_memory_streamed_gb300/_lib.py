@@ -76,6 +76,7 @@ def lib():
         "mt_load_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
         "mt_train_step": (C.c_int, [vp, vp, sz, fp]),
         "mt_train_step_device_tokens": (C.c_int, [vp, vp, sz, fp]),
+        "mt_layer_pass": (C.c_int, [vp, i32, vp, vp, vp, vp]),
         "mt_get_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
         "mt_get_step_stats": (C.c_int, [vp, C.POINTER(MtStepStats)]),
         "mt_get_step": (i64, [vp]),

@@ -1330,6 +1330,65 @@ int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n
   return mt::run_step(m, nullptr, tokens_dev, n_tokens, loss_out);
 }
 
+int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, void* x_out, void* dx_in) {
+  using namespace mt;
+  if (!m) return MT_EINVAL;
+  const Dims& D = m->D;
+  if (layer < 0 || layer >= D.L || !x_in) {
+    m->err = "mt_layer_pass: layer out of range or null x_in";
+    return MT_EINVAL;
+  }
+  if (m->broken) {
+    m->err = "handle is unusable after an earlier CUDA or internal error: " + m->err;
+    return MT_ESTATE;
+  }
+  const int tile = layer + 1;
+  if (!m->w_loaded[tile]) {
+    m->err = "tile " + std::to_string(tile) + " has no weights loaded";
+    return MT_ESTATE;
+  }
+  int code = MT_OK;
+  try {
+    MT_CK(cudaSetDevice(m->device));
+    const TileLayout& lay = m->layouts[tile];
+    uint8_t* wb = m->resident_mode ? m->resident + m->resident_off[tile] : m->wbuf[0];
+    MT_CK(cudaMemsetAsync(m->ws.status, 0, sizeof(int), m->s_comp));
+    MT_CK(cudaMemcpyAsync(wb, m->tiles[tile] + lay.off_w, (size_t)lay.w_bytes, cudaMemcpyHostToDevice, m->s_comp));
+    LaunchStats ls;
+    LayerTemplate tmpl{D, m->cfg.rms_eps, m->s_comp, &m->ws, &ls};
+    LayerActs a = m->store_acts ? m->stored[layer] : m->acts;
+    a.x = reinterpret_cast<bf16*>(const_cast<void*>(x_in));
+    int rc = tmpl.forward(bind_layer(lay, wb), a, reinterpret_cast<bf16*>(x_out), dx_out != nullptr);
+    if (dx_out) {
+      bf16* dxi = dx_in ? reinterpret_cast<bf16*>(dx_in) : m->ws.dx_b;
+      rc |= tmpl.backward(bind_layer(lay, wb), a, reinterpret_cast<const bf16*>(dx_out), dxi,
+                          bind_layer(lay, m->gbuf[0]));
+    }
+    if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(cudaGetLastError())};
+    // bounded wait for the kernels, then plain copies of the results
+    MT_CK(cudaEventRecord(m->ev_t1, m->s_comp));
+    wait_event(m, m->ev_t1, "layer pass");
+    MT_CK(cudaStreamSynchronize(m->s_comp));
+    int st = 0;
+    MT_CK(cudaMemcpy(&st, m->ws.status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (dx_out && st == 0)
+      MT_CK(cudaMemcpy(m->tiles[tile] + lay.off_g, m->gbuf[0], (size_t)lay.w_bytes, cudaMemcpyDeviceToHost));
+    if (st != 0) {
+      if (st == kStatusNonFinite) throw MtError{MT_ENONFINITE, "non-finite value in the layer pass"};
+      throw MtError{MT_ETIMEDOUT, "device status " + std::to_string(st) + " in the layer pass"};
+    }
+  } catch (const MtError& e) {
+    m->err = e.msg;
+    code = e.code;
+    if (!drain_stream(m->s_comp, m->cfg.timeout_ms)) {
+      m->err += " (compute stream did not drain within the timeout)";
+      m->undrained = true;
+    }
+    if (code != MT_EINVAL && code != MT_ENONFINITE) m->broken = true;
+  }
+  return code;
+}
+
 int mt_get_step_stats(const mt_model* m, mt_step_stats* out) {
   if (!m || !out) return MT_EINVAL;
   *out = m->stats;

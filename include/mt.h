@@ -173,6 +173,25 @@ int mt_load_layer_tile(mt_model* m, int tile, int part, const void* src, size_t 
 int mt_train_step(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out);
 int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n_tokens, float* loss_out);
 
+/*
+ * Per-layer check at the workload's full shape (a debugging hook for parity
+ * tests): run decoder layer `layer` (0-based; tile layer + 1) forward and
+ * backward once on caller-supplied activations, with the same template,
+ * kernels and launch shapes as a training step.
+ *   x_in    device BF16 [batch*seq, d_model], row-major: the layer input x_j
+ *   dx_out  device BF16 [batch*seq, d_model]: dL/dx_{j+1}; NULL = forward only
+ *   x_out   device BF16 [batch*seq, d_model]: receives x_{j+1}; may be NULL
+ *   dx_in   device BF16 [batch*seq, d_model]: receives dL/dx_j; may be NULL
+ * The layer's weight gradient (BF16, tile layout) replaces the G section of
+ * the host tile (read it back with mt_get_layer_tile, part G).  Adam does not
+ * run and the step counter does not change.  The four buffers are owned by
+ * the caller, must not overlap, and stay untouched after return.
+ * Synchronous on the compute stream.  Errors: MT_EINVAL (bad layer index or
+ * null x_in), MT_ESTATE (weights not loaded, or the handle is unusable),
+ * MT_ETIMEDOUT (a device-side bounded wait expired), MT_ECUDA.
+ */
+int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, void* x_out, void* dx_in);
+
 /* Copy part `part` of tile `tile` into host memory `dst` (nbytes as in load). */
 int mt_get_layer_tile(mt_model* m, int tile, int part, void* dst, size_t nbytes);
 

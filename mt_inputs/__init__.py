@@ -21,6 +21,7 @@ Per-tile seeds let any single layer be regenerated without the rest.
 """
 from __future__ import annotations
 
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, replace
 
 import torch
@@ -34,6 +35,7 @@ __all__ = [
     "head_weights",
     "model_weights",
     "step_tokens",
+    "normal_bf16",
 ]
 
 
@@ -145,3 +147,27 @@ def step_tokens(s: ModelShape, step: int) -> torch.Tensor:
     """int32 [B, S+1] uniform token ids for training step ``step`` (1-based)."""
     gen = torch.Generator().manual_seed(2000 + step)
     return torch.randint(0, s.vocab, (s.batch, s.seq + 1), generator=gen, dtype=torch.int64).to(torch.int32)
+
+
+def normal_bf16(shape, seed: int, std: float = 1.0, chunk: int = 1 << 24) -> torch.Tensor:
+    """Large BF16 arrays of N(0, std^2) values (activations, output gradients).
+
+    The flat array is cut into chunks of ``chunk`` elements; chunk c is
+    ``randn(fp32, generator seeded with seed * 1_000_003 + c) * std`` rounded
+    to BF16, drawn on parallel threads.  The values depend only on (shape,
+    seed, std, chunk).
+    """
+    n = 1
+    for x in shape:
+        n *= int(x)
+    out = torch.empty(n, dtype=torch.bfloat16)
+
+    def fill(c):
+        lo = c * chunk
+        hi = min(n, lo + chunk)
+        g = torch.Generator().manual_seed(seed * 1_000_003 + c)
+        out[lo:hi] = (torch.randn(hi - lo, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(16, torch.get_num_threads()))) as ex:
+        list(ex.map(fill, range((n + chunk - 1) // chunk)))
+    return out.reshape(shape)

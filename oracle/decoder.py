@@ -59,6 +59,7 @@ __all__ = [
     "swiglu_backward",
     "layer_forward",
     "layer_backward",
+    "layer_tail_rows",
     "head_loss_and_backward",
     "model_forward_loss",
     "model_loss_and_grads",
@@ -365,6 +366,81 @@ def layer_backward(dx_out, c, lw, cfg: OracleConfig, cos, sin):
     dn1 = dq @ lw["wq"] + dk @ lw["wk"] + dv @ lw["wv"]
     dx_n, g["g1"] = rms_norm_backward(dn1, c["x"], lw["g1"], c["rstd1"])
     return dh + dx_n, g
+
+
+def layer_tail_rows(x, dy_tail, lw, cfg: OracleConfig, cos, sin, t0):
+    """One decoder layer on one sequence whose output gradient is zero before row t0.
+
+    x [S, d]: the layer input of one sequence; dy_tail [S - t0, d]: dL/dx' on
+    rows t0..S-1 (rows before t0 carry no gradient).  By causality, rows t0..
+    of x' need the queries of those rows and the keys and values of every row,
+    and the gradient reaches rows before t0 only through their keys and
+    values, so the result equals ``layer_forward`` / ``layer_backward`` with
+    dy zero-padded, at a cost of O(S (d (2 Hkv hd) + (S - t0) Hq hd) +
+    (S - t0) d (Hq hd + 3 ffn)) instead of O(S^2 Hq hd + S d ffn).
+    ``cos``/``sin`` are the tables of all S positions.  Returns (x' on rows
+    t0.., dL/dx on all S rows, weight gradients named as in ``lw``).
+    """
+    S, d = x.shape
+    R = S - t0
+    Hq, Hkv, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    scale = 1.0 / math.sqrt(hd)
+    ct, st = cos[t0:], sin[t0:]
+    # forward: normalised input of every row, keys/values of every row
+    n1, rstd1 = rms_norm(x, lw["g1"], cfg.rms_eps)
+    k = rope((n1 @ lw["wk"].T).reshape(1, S, Hkv, hd), cos, sin)[0]
+    v = (n1 @ lw["wv"].T).reshape(S, Hkv, hd)
+    n1t = n1[t0:]
+    q = rope((n1t @ lw["wq"].T).reshape(1, R, Hq, hd), ct, st)[0]
+    mask = torch.arange(S)[None, :] > torch.arange(t0, S)[:, None]  # key index > query index
+    o = torch.empty(R, Hq, hd, dtype=x.dtype)
+    probs = []
+    for h in range(Hq):
+        j = _kv_head(h, Hq, Hkv)
+        sc = ((q[:, h] @ k[:, j].T) * scale).masked_fill(mask, float("-inf"))
+        p = torch.softmax(sc, dim=-1)
+        o[:, h] = p @ v[:, j]
+        probs.append(p)
+    o2 = o.reshape(R, Hq * hd)
+    hh = x[t0:] + o2 @ lw["wo"].T
+    n2, rstd2 = rms_norm(hh, lw["g2"], cfg.rms_eps)
+    gate = n2 @ lw["wg"].T
+    up = n2 @ lw["wu"].T
+    a = swiglu(gate, up)
+    y = hh + a @ lw["wd"].T
+    # backward
+    g = {}
+    dy = dy_tail
+    g["wd"] = dy.T @ a
+    dgate, dup = swiglu_backward(dy @ lw["wd"], gate, up)
+    g["wg"] = dgate.T @ n2
+    g["wu"] = dup.T @ n2
+    dh_n, g["g2"] = rms_norm_backward(dgate @ lw["wg"] + dup @ lw["wu"], hh, lw["g2"], rstd2)
+    dh = dy + dh_n
+    g["wo"] = dh.T @ o2
+    do = (dh @ lw["wo"]).reshape(R, Hq, hd)
+    dq = torch.empty(R, Hq, hd, dtype=x.dtype)
+    dk = torch.zeros(S, Hkv, hd, dtype=x.dtype)
+    dv = torch.zeros(S, Hkv, hd, dtype=x.dtype)
+    for h in range(Hq):
+        j = _kv_head(h, Hq, Hkv)
+        p = probs[h]
+        dp = do[:, h] @ v[:, j].T
+        ds = p * (dp - (p * dp).sum(dim=-1, keepdim=True))
+        dq[:, h] = (ds @ k[:, j]) * scale
+        dk[:, j] += (ds.T @ q[:, h]) * scale
+        dv[:, j] += p.T @ do[:, h]
+    dq = rope_backward(dq[None], ct, st)[0].reshape(R, Hq * hd)
+    dk = rope_backward(dk[None], cos, sin)[0].reshape(S, Hkv * hd)
+    dv = dv.reshape(S, Hkv * hd)
+    g["wq"] = dq.T @ n1t
+    g["wk"] = dk.T @ n1
+    g["wv"] = dv.T @ n1
+    dn1 = dk @ lw["wk"] + dv @ lw["wv"]
+    dn1[t0:] += dq @ lw["wq"]
+    dx, g["g1"] = rms_norm_backward(dn1, x, lw["g1"], rstd1)
+    dx[t0:] += dh
+    return y, dx, g
 
 
 # ----------------------------------------------------------------------------

@@ -197,6 +197,32 @@ def test_attention_row_functions_agree_with_full_matrix():
         assert torch.allclose(dv_j, dv[0, j, 0], atol=1e-12)
 
 
+@pytest.mark.parametrize("t0", [0, 23, 36])
+def test_layer_tail_rows_equals_full_layer_with_zero_padded_gradient(t0):
+    """The tail-rows layer (for long sequences) reproduces layer_forward and
+    layer_backward exactly when dL/dx' is zero before row t0."""
+    cfg = OracleConfig(n_layers=1, d_model=32, n_heads=4, n_kv_heads=2, head_dim=8, ffn=40, vocab=16,
+                       rms_eps=1e-5, rope_theta=1e4, lr=1e-4, beta1=0.9, beta2=0.95, adam_eps=1e-8,
+                       weight_decay=0.0)
+    g = torch.Generator().manual_seed(43)
+    S = 37
+    shapes = dict(g1=(32,), wq=(32, 32), wk=(16, 32), wv=(16, 32), wo=(32, 32), g2=(32,), wg=(40, 32),
+                  wu=(40, 32), wd=(32, 40))
+    lw = {k: (1 + 0.3 * torch.randn(sh, generator=g)) if len(sh) == 1 else 0.3 * torch.randn(sh, generator=g)
+          for k, sh in shapes.items()}
+    x = torch.randn(1, S, 32, generator=g)
+    dy = torch.randn(1, S, 32, generator=g)
+    dy[:, :t0] = 0
+    cos, sin = oracle.rope_cos_sin(S, 8, 1e4)
+    y_ref, c = oracle.layer_forward(x, lw, cfg, cos, sin)
+    dx_ref, g_ref = oracle.layer_backward(dy, c, lw, cfg, cos, sin)
+    y, dx, gr = oracle.layer_tail_rows(x[0], dy[0, t0:], lw, cfg, cos, sin, t0)
+    assert torch.allclose(y, y_ref[0, t0:], atol=1e-12)
+    assert torch.allclose(dx, dx_ref[0], atol=1e-12)
+    for k in shapes:
+        assert torch.allclose(gr[k], g_ref[k], atol=1e-11), k
+
+
 # ---------------------------------------------------------------- SwiGLU
 
 def test_swiglu_matches_library_and_autograd():
