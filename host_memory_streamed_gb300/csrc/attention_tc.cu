@@ -678,20 +678,28 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
       uint8_t* prow = sPt + st * C::PT_BYTES + r * 128;
       uint8_t* drow = sdSt + st * C::PT_BYTES + r * 128;
+      // Queries past the sequence end have lse = +inf (P = 0) and delta = 0;
+      // only a block that reaches the causal diagonal needs the key > query mask.
+      const bool diag = k0 + 127 > q0;
+      const float4* lse4 = reinterpret_cast<const float4*>(ld + hf * 32);
+      const float4* del4 = reinterpret_cast<const float4*>(ld + 64 + hf * 32);
 #pragma unroll
       for (int k8 = 0; k8 < 4; ++k8) {
+        const float4 la = lse4[2 * k8], lb = lse4[2 * k8 + 1], da = del4[2 * k8], db = del4[2 * k8 + 1];
+        const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+        const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
         float pv[8], dv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int cl = k8 * 8 + e, c = hf * 32 + cl;
-          const int q = q0 + c;
-          float pr = 0.f, dsv = 0.f;
-          if (q < S && key <= q) {
-            pr = exp2f(__uint_as_float(sv[cl]) * p.sl2 - ld[c]);
-            dsv = pr * (__uint_as_float(dp[cl]) - ld[64 + c]);
-          }
+          const int cl = k8 * 8 + e;
+          const float pr = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.sl2, -l8[e]));
           pv[e] = pr;
-          dv[e] = dsv;
+          dv[e] = pr * (__uint_as_float(dp[cl]) - d8[e]);
+        }
+        if (diag) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (key > q0 + hf * 32 + k8 * 8 + e) pv[e] = dv[e] = 0.f;
         }
         const int o = (((hf * 4 + k8) ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(prow + o) = make_uint4(pack2bf(pv[0], pv[1]), pack2bf(pv[2], pv[3]),
@@ -913,18 +921,22 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
       const int k0 = j * 64;
       uint8_t* drow = sdS + s * C::DS_BYTES + r * 128;
+      // Rows past the sequence end have L2 = +inf (P = 0); only a block that
+      // reaches the causal diagonal needs the key > query mask.
+      const bool diag = k0 + 63 > q0;
 #pragma unroll
       for (int k8 = 0; k8 < 4; ++k8) {
         float dv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int cl = k8 * 8 + e, c = hf * 32 + cl;
-          float dsv = 0.f;
-          if (k0 + c <= qrow) {
-            const float pr = exp2f(__uint_as_float(sv[cl]) * p.sl2 - L2);
-            dsv = pr * (__uint_as_float(dp[cl]) - Dr);
-          }
-          dv[e] = dsv;
+          const int cl = k8 * 8 + e;
+          const float pr = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.sl2, -L2));
+          dv[e] = pr * (__uint_as_float(dp[cl]) - Dr);
+        }
+        if (diag) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (k0 + hf * 32 + k8 * 8 + e > qrow) dv[e] = 0.f;
         }
         *reinterpret_cast<uint4*>(drow + (((hf * 4 + k8) ^ (r & 7)) << 4)) = make_uint4(
             pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]), pack2bf(dv[4], dv[5]), pack2bf(dv[6], dv[7]));
