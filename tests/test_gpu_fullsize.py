@@ -93,7 +93,7 @@ def test_layer_pass_full_shape_matches_oracle(name):
         y_o, dx_o, g_o = oracle.layer_tail_rows(x[rows].to(D), dy[b * S + t0:(b + 1) * S].to(D), lw64, cfg, cos,
                                                 sin, t0)
         c, r = cos_rel(y[b * S + t0:(b + 1) * S], y_o)
-        assert c >= 0.9999 and r <= 1e-2, ("x'", b, c, r)
+        assert c >= parity.GRAD_COS and r <= parity.GRAD_RTOL, ("x'", b, c, r)
         c, r = cos_rel(dx[rows], dx_o)
         assert c >= parity.GRAD_COS and r <= parity.GRAD_RTOL, ("dx", b, c, r)
         g_ref = g_o if g_ref is None else {k: g_ref[k] + g_o[k] for k in g_o}
@@ -220,7 +220,14 @@ def test_full_width_model_matches_oracle(name):
                 for sl in _row_chunks(wf):
                     z = torch.zeros(sl.stop - sl.start, dtype=D)
                     we, me, ve = oracle.adam_update(wof[sl], gf[sl], z, z, 1, hcfg)
-                    assert torch.all((wf[sl].to(D) - we).abs() <= parity.bf16_ulp(we)), (i, k)
+                    off = (wf[sl].to(D) - we).abs() > parity.adam_weight_tol(we, wof[sl])
+                    if bool(off.any()):
+                        ix = off.nonzero()[:6, 0]
+                        raise AssertionError(
+                            f"tile {i} {k}: {int(off.sum())} of {off.numel()} weights beyond 1 BF16 ulp of the "
+                            f"oracle's Adam on the library's gradient; first at {(sl.start + ix).tolist()}: "
+                            f"w0 {wof[sl][ix].tolist()} g {gf[sl][ix].tolist()} w_lib {wf[sl][ix].tolist()} "
+                            f"w_expect {we[ix].tolist()} m_lib {mf[sl][ix].tolist()} v_lib {vf[sl][ix].tolist()}")
                     gd = gf[sl].to(D)
                     assert torch.all((mf[sl].to(D) - me).abs() <= 4 * 2.0 ** -24 * (1 - hcfg.beta1) * gd.abs())
                     assert torch.all((vf[sl].to(D) - ve).abs() <= 4 * 2.0 ** -24 * (1 - hcfg.beta2) * gd * gd)
