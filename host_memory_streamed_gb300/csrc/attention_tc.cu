@@ -2,19 +2,24 @@
 // cores: S = Q K^T and O += P V with tcgen05.mma, S and O accumulated in
 // TMEM, Q/K/V tiles brought in by TMA.
 //
-// One CTA per (128 queries, query head, batch); 6 warps:
+// One CTA per (128 queries, query head, batch); 10 warps:
 //   warp 0      TMA: Q once; K and V blocks of 128 keys into a 2-stage ring
 //               (one tensor map over the packed q|k|v projection buffer).
 //   warp 1      MMA (one thread): S_j = Q K_j^T into TMEM buffer j%2, then,
 //               once the softmax has written P_j, O += P_j V_j (V read as an
 //               MN-major operand straight from its [keys][head_dim] tile).
-//   warps 2..5  softmax: each thread owns one query row (its TMEM lane), so
-//               the row max and row sum need no shuffles.  P_j is written to
-//               shared memory in the 128-byte-swizzled K-major layout the
-//               tensor core reads as its A operand.  The running maximum is
-//               only moved (and O rescaled in TMEM) when it grows by more than
-//               a factor 2^8, so O is rarely touched; the final O / l and the
-//               log-sum-exp use whichever maximum was kept.
+//   warps 2..9  softmax: two threads (one in each of two warps that share a
+//               TMEM lane group) own one query row.  Each reads the whole
+//               score row and takes its maximum itself, so the pair agrees on
+//               the running maximum without exchanging anything; each then
+//               exponentiates its half of the 128 keys and keeps its half of
+//               the row sum (the halves are added once, at the end).  P_j is
+//               written to shared memory in the 128-byte-swizzled K-major
+//               layout the tensor core reads as its A operand.  The running
+//               maximum is only moved (and O rescaled in TMEM, each thread of
+//               the pair scaling half of the columns) when it grows by more
+//               than a factor 2^8, so O is rarely touched; the final O / l and
+//               the log-sum-exp use whichever maximum was kept.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // kStatusAttnFwdTimeout in the status word and unwinds.
 //
@@ -27,6 +32,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -38,7 +44,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long rows, long cols, long
 
 namespace {
 
-constexpr int TA_BM = 128, TA_BN = 128, TA_THREADS = 192;
+constexpr int TA_BM = 128, TA_BN = 128, TA_THREADS = 320;
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 256);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(o_full, 1);
@@ -208,12 +214,14 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       }
     }
   } else {
-    // softmax warps: thread <-> query row r (TMEM lane r)
+    // softmax warps 2..9: thread <-> query row r (TMEM lane r), half hf of the
+    // 128 key columns for the exponentials and of the HD output columns
     const int quarter = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = q0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // running maximum (raw score units) and this half's row sum
     bool ok = true;
     int site = 0;
     for (int j = 0; j < n_kb; ++j) {
@@ -224,32 +232,32 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         break;
       }
       tc_fence_after();
-      float x[TA_BN];
+      uint32_t x[TA_BN];
 #pragma unroll
       for (int c = 0; c < TA_BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32((tmem + 128u * (uint32_t)s) + lane_off + c * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]) * p.sl2;
+        uint32_t* xc = x + c * 32;
+        tmem_ld_32x32b_x32((tmem + 128u * (uint32_t)s) + lane_off + c * 32,
+                           *reinterpret_cast<uint32_t(*)[32]>(xc));
       }
+      tmem_wait_ld_regs(x);
       const int k0 = j * TA_BN;
-      float mx = -INFINITY;
       if (k0 + TA_BN - 1 > q0) {  // block touches the diagonal
 #pragma unroll
         for (int c = 0; c < TA_BN; ++c)
-          if (k0 + c > qrow) x[c] = -INFINITY;
+          if (k0 + c > qrow) x[c] = __float_as_uint(-INFINITY);
       }
+      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < TA_BN; ++c) mx = fmaxf(mx, x[c]);
+      for (int c = 0; c < TA_BN; ++c) mx = fmaxf(mx, __uint_as_float(x[c]));
+      // scores are raw q.k; probabilities exp2((x - m) * scale * log2 e)
       const float m_new = fmaxf(m, mx);
-      const bool rescale = (m == -INFINITY) || (m_new > m + kRescaleThreshold);
+      const bool rescale = (m == -INFINITY) || ((m_new - m) * p.sl2 > kRescaleThreshold);
       float alpha = 1.f;
       if (rescale) {
-        alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+        alpha = (m == -INFINITY) ? 0.f : ex2_approx((m - m_new) * p.sl2);
         m = m_new;
       }
-      const float base = (m == -INFINITY) ? 0.f : m;
+      const float nb = (m == -INFINITY) ? 0.f : -m * p.sl2;
       // the P buffer is free once PV_{j-2} completed
       if (j >= 2 && !mbar_wait_warp(&pv_done[s], ((j >> 1) - 1) & 1)) {
         site = 800 + min(j, 99);
@@ -257,23 +265,31 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         break;
       }
       float rs = 0.f;
-      uint8_t* prow = sP + s * C::P_BYTES + r * 128;
+      uint8_t* prow = sP + s * C::P_BYTES + hf * C::BOX + r * 128;
+      // this half's 64 keys; the register array is indexed with constants only
+      auto exp_half = [&](auto half) {
+        constexpr int K0 = decltype(half)::value * 64;
 #pragma unroll
-      for (int c16 = 0; c16 < TA_BN / 8; ++c16) {  // 16-byte chunks of 8 keys
-        float e8[8];
+        for (int cc = 0; cc < 8; ++cc) {  // 16-byte chunks of 8 keys in the half's 64-key box
+          float e8[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          e8[e] = exp2f(x[c16 * 8 + e] - base);
-          rs += e8[e];
+          for (int e = 0; e < 8; ++e) {
+            e8[e] = ex2_approx(fmaf(__uint_as_float(x[K0 + cc * 8 + e]), p.sl2, nb));
+            rs += e8[e];
+          }
+          uint4 w = make_uint4(pack2bf(e8[0], e8[1]), pack2bf(e8[2], e8[3]), pack2bf(e8[4], e8[5]),
+                               pack2bf(e8[6], e8[7]));
+          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w;
         }
-        const int box = c16 >> 3, cc = c16 & 7;
-        uint4 w = make_uint4(pack2bf(e8[0], e8[1]), pack2bf(e8[2], e8[3]), pack2bf(e8[4], e8[5]),
-                             pack2bf(e8[6], e8[7]));
-        *reinterpret_cast<uint4*>(prow + box * C::BOX + ((cc ^ (r & 7)) << 4)) = w;
-      }
+      };
+      if (hf == 0)
+        exp_half(std::integral_constant<int, 0>{});
+      else
+        exp_half(std::integral_constant<int, 1>{});
       l = l * alpha + rs;
       // O holds sum_{i<j} P_i V_i.  tcgen05.ld/st are warp-collective, so the
-      // whole warp rescales when any of its rows must (alpha = 1 for the others).
+      // whole warp rescales when any of its rows must (alpha = 1 for the others);
+      // the two warps of a lane group see the same rows and scale one half each.
       if (__any_sync(0xffffffffu, rescale && j > 0)) {
         if (!mbar_wait_warp(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
           site = 900 + min(j, 99);
@@ -282,13 +298,14 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HD / 64; ++c) {
           uint32_t v[32];
-          tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
+          const uint32_t ta = tO + lane_off + hf * (HD / 2) + c * 32;
+          tmem_ld_32x32b_x32(ta, v);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st_32x32b_x32(tO + lane_off + c * 32, v);
+          tmem_st_32x32b_x32(ta, v);
         }
         tmem_wait_st();
       }
@@ -301,15 +318,27 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       site = 999;
       ok = false;
     }
+    // the two halves of each row sum meet in the (now idle) P buffer
+    float* lsum = reinterpret_cast<float*>(sP);
+    if (ok) {
+      lsum[hf * 128 + r] = l;
+      mbar_arrive(&p_full[0]);  // one more phase of p_full[0] collects all 256 halves
+      const int ph = ((n_kb + 1) >> 1) & 1;  // phases of p_full[0] completed so far: ceil(n_kb / 2)
+      if (!mbar_wait_warp(&p_full[0], (uint32_t)ph)) {
+        site = 998;
+        ok = false;
+      }
+    }
     if (ok) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float lt = lsum[r] + lsum[128 + r];
+      const float inv = 1.f / lt;
       const bool valid = qrow < S;
-      bf16* dst = p.o + (long)(row0 + qrow) * p.ldo + (long)h * HD;
+      bf16* dst = p.o + (long)(row0 + qrow) * p.ldo + (long)h * HD + hf * (HD / 2);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HD / 64; ++c) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tO + lane_off + c * 32, v);
+        tmem_ld_32x32b_x32(tO + lane_off + hf * (HD / 2) + c * 32, v);
         tmem_wait_ld();
         if (valid) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
@@ -321,7 +350,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
           }
         }
       }
-      if (valid) p.lse[((long)b * p.Hq + h) * S + qrow] = (m + log2f(l)) * kLn2F;
+      if (valid && hf == 0) p.lse[((long)b * p.Hq + h) * S + qrow] = m * (p.sl2 * kLn2F) + logf(lt);
     } else {
       set_status(p.status, kStatusAttnFwdTimeout * 1000 + site);
       abort_flag = 1;

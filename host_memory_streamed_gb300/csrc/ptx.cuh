@@ -169,6 +169,14 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tcgen05.wait::ld, then tie the loaded registers to it (an empty volatile asm
+// that "rewrites" each one) so that no use of them is scheduled above the wait.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[N]) {
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile whose rows are
 // 128 bytes (64 BF16) long, written by TMA with 128-byte swizzling: 8-row
