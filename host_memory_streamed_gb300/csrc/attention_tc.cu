@@ -404,17 +404,27 @@ int launch_attn_fwd_tc(const AttnArgs& x, cudaStream_t s) {
 // ============================================================================
 // Backward on the tensor cores (deterministic, no atomics).
 //
+// Both kernels work on 128 x 128 score blocks, so every tcgen05.mma has
+// N = 128 (narrower MMAs were bound by shared-memory operand bandwidth), and
+// keep the BF16 probabilities / score gradients in TMEM, written in place
+// over the FP32 scores they came from, where the tensor core reads them as
+// its A operand (tcgen05.mma with A in TMEM: lane = row, 32-bit column j =
+// elements 2j and 2j+1 of the row).
+//
 // dK/dV kernel: one CTA per (128-key block, kv head, batch).  K and V of the
-// block stay in shared memory; the TMA warp streams 64-query blocks of Q and
-// dO for every query head of the group, in a fixed order.  Per query block:
-//   S^T = K Q^T and dP^T = V dO^T      (TMEM, double-buffered)
-//   P^T = exp(S^T * scale - lse[q]), dS^T = P^T * (dP^T - delta[q])
-//                                       (softmax warps: thread = key row)
-//   dV += P^T dO, dK += dS^T Q          (TMEM accumulators; dO and Q are read
-//                                        MN-major from the very tiles used
-//                                        K-major for S^T and dP^T)
+// block stay in shared memory; the TMA warp streams 128-query blocks of Q and
+// dO (2 stages) for every query head of the group, in a fixed order.  Per
+// query block (TMEM: S^T 0..127, dP^T 128..255, dV, dK accumulators above):
+//   S^T = K Q^T, dP^T = V dO^T
+//   P^T = exp(S^T * scale - lse[q])          -> BF16 over S^T's columns
+//   dS^T = P^T * (dP^T - delta[q])           -> BF16 over dP^T's columns
+//   dV += P^T dO, dK += dS^T Q               (dO, Q read MN-major from the
+//                                             tiles used K-major above)
+// The tensor core runs dV_i, S^T_{i+1}, dK_i, dP^T_{i+1} in that order, so
+// each score block is overwritten only after its probabilities were used.
 // dQ kernel: one CTA per (128-query block, query head, batch), streaming
-// 64-key blocks: S = Q K^T, dP = dO V^T, dS = P * (dP - delta), dQ += dS K.
+// 128-key blocks of K and V (2 stages): S = Q K^T (double-buffered in TMEM),
+// dP = dO V^T, dS = P * (dP - delta) -> BF16 over S's columns, dQ += dS K.
 // dK and dQ are scaled by 1/sqrt(hd) and leave through the inverse RoPE
 // rotation when tables are given.
 // ============================================================================
@@ -499,29 +509,30 @@ __device__ __forceinline__ void store_half_row(uint32_t taddr, int h, float scal
   }
 }
 
+// Probabilities / score gradients of one half row (64 columns), packed BF16
+// pairs (even column in the low half), into TMEM columns [col, col + 32).
+__device__ __forceinline__ void tmem_st_packed32(uint32_t taddr, const uint32_t (&v)[32]) {
+  tmem_st_32x32b_x32(taddr, v);
+}
+
 template <int HD>
 struct TkvCfg {
-  static constexpr int KBOX = 128 * 128;  // 64-column box of 128 key rows
-  static constexpr int QBOX = 64 * 128;   // 64-column box of 64 query rows
-  static constexpr int KV_BYTES = 128 * HD * 2;
-  static constexpr int Q_BYTES = 64 * HD * 2;
-  static constexpr int PT_BYTES = 128 * 64 * 2;  // [128 keys][64 queries] BF16, one box
-  static constexpr int QSTAGES = 3;
+  static constexpr int BOX = 128 * 128;      // one 64-column box of 128 rows, bytes
+  static constexpr int TILE = 128 * HD * 2;  // 128 rows x HD columns (HD / 64 boxes)
+  static constexpr int QSTAGES = 2;
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;              // QSTAGES stages
-  static constexpr int OFF_DO = OFF_Q + QSTAGES * Q_BYTES;    // QSTAGES stages
-  static constexpr int OFF_PT = OFF_DO + QSTAGES * Q_BYTES;   // 2 buffers
-  static constexpr int OFF_DST = OFF_PT + 2 * PT_BYTES;       // 2 buffers
-  static constexpr int OFF_LD = OFF_DST + 2 * PT_BYTES;       // lse*log2e | delta of a query block, 2 buffers
-  static constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_Q = OFF_V + TILE;                 // QSTAGES tiles
+  static constexpr int OFF_DO = OFF_Q + QSTAGES * TILE;      // QSTAGES tiles
+  static constexpr int OFF_LD = OFF_DO + QSTAGES * TILE;     // [QSTAGES][lse*log2e 128 | delta 128]
+  static constexpr int OFF_BAR = OFF_LD + QSTAGES * 256 * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
 
 template <int HD>
 __global__ void __launch_bounds__(TB_THREADS, 1)
-    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
-                            const __grid_constant__ CUtensorMap tm_do, TbParams p) {
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                            TbParams p) {
   using C = TkvCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -529,19 +540,20 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sdO = smem + C::OFF_DO;
-  uint8_t* sPt = smem + C::OFF_PT;
-  uint8_t* sdSt = smem + C::OFF_DST;
   float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bar + 0;
-  uint64_t* qd_full = bar + 1;   // [3]
-  uint64_t* qd_empty = bar + 4;  // [3]
-  uint64_t* s_full = bar + 7;    // [2]
-  uint64_t* ds_full = bar + 9;   // [2]
-  uint64_t* pt_free = bar + 11;  // [2]
+  uint64_t* qd_full = bar + 1;    // [2]
+  uint64_t* qd_empty = bar + 3;   // [2]
+  uint64_t* st_full = bar + 5;    // S^T of the current block computed
+  uint64_t* dpt_full = bar + 6;   // dP^T of the current block computed
+  uint64_t* p_ready = bar + 7;    // P^T stored (256 softmax threads)
+  uint64_t* ds_ready = bar + 8;   // dS^T stored (256)
+  uint64_t* ld_ready = bar + 9;   // [2] lse/delta of a block staged (256)
+  uint64_t* st_read = bar + 11;   // every softmax thread has read its S^T columns (256)
+  uint64_t* dpt_read = bar + 12;  // ... and its dP^T columns (256)
   uint64_t* acc_full = bar + 13;
-  uint64_t* ld_ready = bar + 14;  // [2]: the staged lse/delta of a query block (128 softmax threads)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 16);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 14);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -550,28 +562,28 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   const int k0 = blockIdx.x * 128;
   const int row0 = b * S;
   const int G = p.Hq / p.Hkv;
-  const int qb_first = k0 / 64;
-  const int n_qb = (S + 63) / 64;
+  const int qb_first = blockIdx.x;
+  const int n_qb = (S + 127) / 128;
   const int per_head = n_qb - qb_first;
   const int total = per_head * G;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(kv_full, 1);
-    for (int i = 0; i < C::QSTAGES; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&ds_full[i], 256);
-      mbar_init(&pt_free[i], 1);
       mbar_init(&ld_ready[i], 256);
     }
+    mbar_init(st_full, 1);
+    mbar_init(dpt_full, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(st_read, 256);
+    mbar_init(dpt_read, 256);
     mbar_init(acc_full, 1);
     fence_barrier_init();
-    tma_prefetch_desc(&tm_kv);
-    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_do);
   }
   if (warp == 1) {
@@ -582,86 +594,103 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // TMEM columns: S^T[2] 0/64, dP^T[2] 128/192, dV 256.., dK 256+HD..
-  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + HD;
+  const uint32_t tST = tmem, tDPT = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + HD;
 
   auto head_of = [&](int it) { return kvh * G + it / per_head; };
-  auto q0_of = [&](int it) { return (qb_first + it % per_head) * 64; };
+  auto q0_of = [&](int it) { return (qb_first + it % per_head) * 128; };
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      mbar_arrive_expect_tx(kv_full, 2 * C::TILE);
 #pragma unroll
       for (int i = 0; i < HD / 64; ++i) {
-        tma_load_2d(sK + i * C::KBOX, &tm_kv, (p.Hq + kvh) * HD + 64 * i, row0 + k0, kv_full);
-        tma_load_2d(sV + i * C::KBOX, &tm_kv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + k0, kv_full);
+        tma_load_2d(sK + i * C::BOX, &tm_qkv, (p.Hq + kvh) * HD + 64 * i, row0 + k0, kv_full);
+        tma_load_2d(sV + i * C::BOX, &tm_qkv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + k0, kv_full);
       }
-      int pend[C::QSTAGES] = {-1, -1, -1};
+      int pend[2] = {-1, -1};
       for (int it = 0; it < total && !abort_flag; ++it) {
-        const int st = it % C::QSTAGES;
-        if (it >= C::QSTAGES && !mbar_wait(&qd_empty[st], ((it / C::QSTAGES) - 1) & 1)) {
+        const int st = it & 1;
+        if (it >= 2 && !mbar_wait(&qd_empty[st], ((it >> 1) - 1) & 1)) {
           set_status(p.status, kStatusAttnBwdTimeout);
           abort_flag = 1;
           break;
         }
         const int h = head_of(it), q0 = q0_of(it);
-        mbar_arrive_expect_tx(&qd_full[st], 2 * C::Q_BYTES);
+        mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE);
 #pragma unroll
         for (int i = 0; i < HD / 64; ++i) {
-          tma_load_2d(sQ + st * C::Q_BYTES + i * C::QBOX, &tm_q, h * HD + 64 * i, row0 + q0, &qd_full[st]);
-          tma_load_2d(sdO + st * C::Q_BYTES + i * C::QBOX, &tm_do, h * HD + 64 * i, row0 + q0, &qd_full[st]);
+          tma_load_2d(sQ + st * C::TILE + i * C::BOX, &tm_qkv, h * HD + 64 * i, row0 + q0, &qd_full[st]);
+          tma_load_2d(sdO + st * C::TILE + i * C::BOX, &tm_do, h * HD + 64 * i, row0 + q0, &qd_full[st]);
         }
-        pend[st] = (it / C::QSTAGES) & 1;
+        pend[st] = (it >> 1) & 1;
       }
       if (!mbar_wait(kv_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
-      for (int s = 0; s < C::QSTAGES; ++s)
+      for (int s = 0; s < 2; ++s)
         if (pend[s] >= 0 && !mbar_wait(&qd_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 64);                 // K/V [keys][hd] x Q/dO [q][hd]^T
-      const uint32_t id_acc = idesc_bf16_f32(128, HD) | (1u << 16);  // P^T/dS^T x dO/Q (MN-major)
+      const uint32_t id_s = idesc_bf16_f32(128, 128);                // K/V [keys][hd] x Q/dO [q][hd]^T
+      const uint32_t id_acc = idesc_bf16_f32(128, HD) | (1u << 16);  // P^T/dS^T (TMEM) x dO/Q (MN-major)
       bool ok = mbar_wait(kv_full, 0);
-      auto issue_s = [&](int it) {
-        const int qs = it % C::QSTAGES, b2 = it & 1;
-        if (!mbar_wait(&qd_full[qs], (it / C::QSTAGES) & 1)) return false;
-        tc_fence_after();
+      // S^T (or dP^T with V, dO) of block it into TMEM columns dst
+      auto issue_scores = [&](int it, const uint8_t* sA, const uint8_t* sB, uint32_t dst) {
+        const int qs = it & 1;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const int box = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t ka = smem_desc_kmajor_sw128(sK + box * C::KBOX + off);
-          const uint64_t va = smem_desc_kmajor_sw128(sV + box * C::KBOX + off);
-          const uint64_t qb = smem_desc_kmajor_sw128(sQ + qs * C::Q_BYTES + box * C::QBOX + off);
-          const uint64_t ob = smem_desc_kmajor_sw128(sdO + qs * C::Q_BYTES + box * C::QBOX + off);
-          tc_mma_bf16(tmem + 64u * b2, ka, qb, id_s, kk > 0 ? 1u : 0u);
-          tc_mma_bf16(tmem + 128u + 64u * b2, va, ob, id_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(dst, smem_desc_kmajor_sw128(sA + box * C::BOX + off),
+                      smem_desc_kmajor_sw128(sB + qs * C::TILE + box * C::BOX + off), id_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[b2]);
-        return true;
       };
-      auto issue_acc = [&](int it) {
-        const int qs = it % C::QSTAGES, b2 = it & 1;
-        if (!mbar_wait(&ds_full[b2], (it >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint64_t ob = smem_desc_mnmajor_sw128(sdO + qs * C::Q_BYTES, C::QBOX);
-        const uint64_t qb = smem_desc_mnmajor_sw128(sQ + qs * C::Q_BYTES, C::QBOX);
+      // acc += (TMEM operand at src) x (tile of block it, MN-major)
+      auto issue_acc = [&](int it, uint32_t src, const uint8_t* sB, uint32_t acc) {
+        const int qs = it & 1;
+        const uint64_t bd = smem_desc_mnmajor_sw128(sB + qs * C::TILE, C::BOX);
 #pragma unroll
-        for (int kk = 0; kk < 64 / 16; ++kk) {
-          const uint64_t pa = smem_desc_kmajor_sw128(sPt + b2 * C::PT_BYTES + kk * 32);
-          const uint64_t da = smem_desc_kmajor_sw128(sdSt + b2 * C::PT_BYTES + kk * 32);
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_bf16(tdV, pa, ob + (uint64_t)(kk * (2048 >> 4)), id_acc, acc);
-          tc_mma_bf16(tdK, da, qb + (uint64_t)(kk * (2048 >> 4)), id_acc, acc);
-        }
-        tc_commit(&qd_empty[qs]);
-        tc_commit(&pt_free[b2]);
-        return true;
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          tc_mma_bf16_ts(acc, src + kk * 8, bd + (uint64_t)(kk * (2048 >> 4)), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
       };
-      for (int it = 0; ok && it < total; ++it) {
-        if (!issue_s(it)) ok = false;
-        if (ok && it > 0 && !issue_acc(it - 1)) ok = false;
+      if (ok && total > 0) {
+        ok = mbar_wait(&qd_full[0], 0);
+        if (ok) {
+          tc_fence_after();
+          issue_scores(0, sK, sQ, tST);
+          tc_commit(st_full);
+          issue_scores(0, sV, sdO, tDPT);
+          tc_commit(dpt_full);
+        }
       }
-      if (ok && total > 0 && !issue_acc(total - 1)) ok = false;
+      for (int it = 0; ok && it < total; ++it) {
+        const uint32_t ph = it & 1;
+        if (!mbar_wait(p_ready, ph)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_acc(it, tST, sdO, tdV);  // dV += P^T dO
+        const bool more = it + 1 < total;
+        if (more) {
+          if (!mbar_wait(&qd_full[(it + 1) & 1], ((it + 1) >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_scores(it + 1, sK, sQ, tST);  // runs after dV_it has read P^T
+          tc_commit(st_full);
+        }
+        if (!mbar_wait(ds_ready, ph)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_acc(it, tDPT, sQ, tdK);  // dK += dS^T Q
+        tc_commit(&qd_empty[it & 1]);
+        if (more) {
+          issue_scores(it + 1, sV, sdO, tDPT);  // runs after dK_it has read dS^T
+          tc_commit(dpt_full);
+        }
+      }
       if (ok) {
         tc_commit(acc_full);
       } else {
@@ -670,7 +699,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
     }
   } else {
-    // softmax warps 2..9: thread <-> key row r, half hf of the 64 query columns
+    // softmax warps 2..9: thread <-> key row r, half hf of the 128 query columns
     const int quarter = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
@@ -680,65 +709,91 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     bool ok = true;
     for (int it = 0; it < total; ++it) {
       const int st = it & 1;
+      const uint32_t ph = it & 1;
       const int h = head_of(it), q0 = q0_of(it);
-      // stage lse (log2 units) and delta of the 64 queries once for all rows
-      float* ld = sLD + st * 128;
-      if (tid < 128) {
-        const int t = tid & 63, q = q0 + t;
+      // stage lse (log2 units) and delta of the 128 queries once for all rows
+      float* ld = sLD + st * 256;
+      {
+        const int t = tid & 127, q = q0 + t;
         const long idx = ((long)b * p.Hq + h) * S + q;
-        if (tid < 64)
+        if (tid < 128)
           ld[t] = q < S ? p.lse[idx] * kLog2eF : INFINITY;
         else
-          ld[64 + t] = q < S ? p.delta[idx] : 0.f;
+          ld[128 + t] = q < S ? p.delta[idx] : 0.f;
       }
       mbar_arrive(&ld_ready[st]);
-      if (!mbar_wait_warp(&ld_ready[st], (it >> 1) & 1) || !mbar_wait_warp(&s_full[st], (it >> 1) & 1)) {
+      if (!mbar_wait_warp(&ld_ready[st], (it >> 1) & 1) || !mbar_wait_warp(st_full, ph)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[32], dp[32];
-      tmem_ld_32x32b_x32(tmem + 64u * st + lane_off + hf * 32, sv);
-      tmem_ld_32x32b_x32(tmem + 128u + 64u * st + lane_off + hf * 32, dp);
-      tmem_wait_ld();
-      if (it >= 2 && !mbar_wait_warp(&pt_free[st], ((it >> 1) - 1) & 1)) {
+      uint32_t sv[64];
+      tmem_ld_32x32b_x32(tST + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld_32x32b_x32(tST + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_wait_ld_regs(sv);
+      mbar_arrive(st_read);
+      // Queries past the sequence end have lse = +inf (P = 0) and delta = 0;
+      // only the diagonal block (q0 == k0) needs the key > query mask.
+      const bool diag = q0 == k0;
+      const float4* lse4 = reinterpret_cast<const float4*>(ld + hf * 64);
+      float pf[64];
+      uint32_t pk[32];
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = lse4[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c4 * 4 + e;
+          float pr = ex2_approx(fmaf(__uint_as_float(sv[c]), p.sl2, -lv[e]));
+          if (diag && key > q0 + hf * 64 + c) pr = 0.f;
+          pf[c] = pr;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) pk[j] = pack2bf(pf[2 * j], pf[2 * j + 1]);
+      if (!mbar_wait_warp(st_read, ph)) {
         ok = false;
         break;
       }
-      uint8_t* prow = sPt + st * C::PT_BYTES + r * 128;
-      uint8_t* drow = sdSt + st * C::PT_BYTES + r * 128;
-      // Queries past the sequence end have lse = +inf (P = 0) and delta = 0;
-      // only a block that reaches the causal diagonal needs the key > query mask.
-      const bool diag = k0 + 127 > q0;
-      const float4* lse4 = reinterpret_cast<const float4*>(ld + hf * 32);
-      const float4* del4 = reinterpret_cast<const float4*>(ld + 64 + hf * 32);
-#pragma unroll
-      for (int k8 = 0; k8 < 4; ++k8) {
-        const float4 la = lse4[2 * k8], lb = lse4[2 * k8 + 1], da = del4[2 * k8], db = del4[2 * k8 + 1];
-        const float l8[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-        const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-        float pv[8], dv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int cl = k8 * 8 + e;
-          const float pr = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.sl2, -l8[e]));
-          pv[e] = pr;
-          dv[e] = pr * (__uint_as_float(dp[cl]) - d8[e]);
-        }
-        if (diag) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (key > q0 + hf * 32 + k8 * 8 + e) pv[e] = dv[e] = 0.f;
-        }
-        const int o = (((hf * 4 + k8) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(prow + o) = make_uint4(pack2bf(pv[0], pv[1]), pack2bf(pv[2], pv[3]),
-                                                         pack2bf(pv[4], pv[5]), pack2bf(pv[6], pv[7]));
-        *reinterpret_cast<uint4*>(drow + o) = make_uint4(pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]),
-                                                         pack2bf(dv[4], dv[5]), pack2bf(dv[6], dv[7]));
-      }
-      fence_proxy_async_smem();
+      tc_fence_after();
+      tmem_st_packed32(tST + lane_off + hf * 32, pk);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ds_full[st]);
+      mbar_arrive(p_ready);
+      // dS^T = P^T * (dP^T - delta)
+      if (!mbar_wait_warp(dpt_full, ph)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float4* del4 = reinterpret_cast<const float4*>(ld + 128 + hf * 64);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dp[32];
+        tmem_ld_32x32b_x32(tDPT + lane_off + hf * 64 + half * 32, dp);
+        tmem_wait_ld_regs(dp);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = del4[half * 8 + c4];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          const int c = half * 32 + c4 * 4;
+          pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[c4 * 4]) - dv[0]),
+                              pf[c + 1] * (__uint_as_float(dp[c4 * 4 + 1]) - dv[1]));
+          pk[c / 2 + 1] = pack2bf(pf[c + 2] * (__uint_as_float(dp[c4 * 4 + 2]) - dv[2]),
+                                  pf[c + 3] * (__uint_as_float(dp[c4 * 4 + 3]) - dv[3]));
+        }
+      }
+      mbar_arrive(dpt_read);
+      if (!mbar_wait_warp(dpt_read, ph)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_packed32(tDPT + lane_off + hf * 32, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(acc_full, 0)) {
@@ -767,25 +822,21 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
 
 template <int HD>
 struct TdqCfg {
-  static constexpr int QBOX = 128 * 128;  // 64 columns x 128 query rows
-  static constexpr int KBOX = 64 * 128;   // 64 columns x 64 key rows
-  static constexpr int Q_BYTES = 128 * HD * 2;
-  static constexpr int K_BYTES = 64 * HD * 2;
-  static constexpr int DS_BYTES = 128 * 64 * 2;  // [128 q][64 keys], one box
-  static constexpr int KSTAGES = 4;
+  static constexpr int BOX = 128 * 128;      // one 64-column box of 128 rows, bytes
+  static constexpr int TILE = 128 * HD * 2;  // 128 rows x HD columns
+  static constexpr int KSTAGES = 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_DO = OFF_Q + Q_BYTES;
-  static constexpr int OFF_K = OFF_DO + Q_BYTES;            // KSTAGES stages
-  static constexpr int OFF_V = OFF_K + KSTAGES * K_BYTES;   // KSTAGES stages
-  static constexpr int OFF_DS = OFF_V + KSTAGES * K_BYTES;  // 2 buffers
-  static constexpr int OFF_BAR = OFF_DS + 2 * DS_BYTES;
+  static constexpr int OFF_DO = OFF_Q + TILE;
+  static constexpr int OFF_K = OFF_DO + TILE;             // KSTAGES tiles
+  static constexpr int OFF_V = OFF_K + KSTAGES * TILE;    // KSTAGES tiles
+  static constexpr int OFF_BAR = OFF_V + KSTAGES * TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
 
 template <int HD>
 __global__ void __launch_bounds__(TB_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                          const __grid_constant__ CUtensorMap tm_do, TbParams p) {
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_do,
+                          TbParams p) {
   using C = TdqCfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -793,43 +844,44 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint8_t* sdO = smem + C::OFF_DO;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sdS = smem + C::OFF_DS;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [4]
-  uint64_t* kv_empty = bar + 5;  // [4]
-  uint64_t* s_full = bar + 9;    // [2]
-  uint64_t* ds_full = bar + 11;  // [2]
-  uint64_t* ds_free = bar + 13;  // [2]
-  uint64_t* acc_full = bar + 15;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 16);
+  uint64_t* kv_full = bar + 1;   // [2]
+  uint64_t* kv_empty = bar + 3;  // [2]
+  uint64_t* s_full = bar + 5;    // [2] S of block j in TMEM buffer j & 1
+  uint64_t* dp_full = bar + 7;
+  uint64_t* sd_read = bar + 8;   // every softmax thread has read its S and dP columns (256)
+  // [2] dS_j stored (256).  Two barriers: the softmax may finish block j + 1
+  // before the MMA thread starts waiting for block j (dP_{j+1} is issued first).
+  uint64_t* ds_ready = bar + 9;
+  uint64_t* acc_full = bar + 11;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qb = gridDim.x - 1 - blockIdx.x;
+  const int qb = gridDim.x - 1 - blockIdx.x;  // longest causal rows first
   const int b = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
   const int kvh = h * p.Hkv / p.Hq;
   const int S = p.S;
   const int q0 = qb * 128;
   const int row0 = b * S;
-  const int n_kb = min((S + 63) / 64, (q0 + 128 + 63) / 64);
+  const int n_kb = qb + 1;  // key blocks 0..qb (128-aligned, same as the query blocks)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(q_full, 1);
-    for (int i = 0; i < C::KSTAGES; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&ds_full[i], 256);
-      mbar_init(&ds_free[i], 1);
     }
+    mbar_init(dp_full, 1);
+    mbar_init(sd_read, 256);
+    mbar_init(&ds_ready[0], 256);
+    mbar_init(&ds_ready[1], 256);
     mbar_init(acc_full, 1);
     fence_barrier_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_do);
   }
   if (warp == 1) {
@@ -840,80 +892,93 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // TMEM columns: S[2] 0/64, dP[2] 128/192, dQ 256..
-  const uint32_t tdQ = tmem + 256;
+  // TMEM columns: S[2] 0 / 128, dP 256, dQ 384 (HD columns)
+  const uint32_t tDP = tmem + 256, tdQ = tmem + 384;
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, 2 * C::Q_BYTES);
+      mbar_arrive_expect_tx(q_full, 2 * C::TILE);
 #pragma unroll
       for (int i = 0; i < HD / 64; ++i) {
-        tma_load_2d(sQ + i * C::QBOX, &tm_q, h * HD + 64 * i, row0 + q0, q_full);
-        tma_load_2d(sdO + i * C::QBOX, &tm_do, h * HD + 64 * i, row0 + q0, q_full);
+        tma_load_2d(sQ + i * C::BOX, &tm_qkv, h * HD + 64 * i, row0 + q0, q_full);
+        tma_load_2d(sdO + i * C::BOX, &tm_do, h * HD + 64 * i, row0 + q0, q_full);
       }
-      int pend[C::KSTAGES] = {-1, -1, -1, -1};
+      int pend[2] = {-1, -1};
       for (int j = 0; j < n_kb && !abort_flag; ++j) {
-        const int s = j % C::KSTAGES;
-        if (j >= C::KSTAGES && !mbar_wait(&kv_empty[s], ((j / C::KSTAGES) - 1) & 1)) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1)) {
           set_status(p.status, kStatusAttnBwdTimeout);
           abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[s], 2 * C::K_BYTES);
+        mbar_arrive_expect_tx(&kv_full[s], 2 * C::TILE);
 #pragma unroll
         for (int i = 0; i < HD / 64; ++i) {
-          tma_load_2d(sK + s * C::K_BYTES + i * C::KBOX, &tm_kv, (p.Hq + kvh) * HD + 64 * i, row0 + j * 64,
+          tma_load_2d(sK + s * C::TILE + i * C::BOX, &tm_qkv, (p.Hq + kvh) * HD + 64 * i, row0 + j * 128,
                       &kv_full[s]);
-          tma_load_2d(sV + s * C::K_BYTES + i * C::KBOX, &tm_kv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + j * 64,
+          tma_load_2d(sV + s * C::TILE + i * C::BOX, &tm_qkv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + j * 128,
                       &kv_full[s]);
         }
-        pend[s] = (j / C::KSTAGES) & 1;
+        pend[s] = (j >> 1) & 1;
       }
       if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
-      for (int s = 0; s < C::KSTAGES; ++s)
+      for (int s = 0; s < 2; ++s)
         if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, 64);
-      const uint32_t id_dq = idesc_bf16_f32(128, HD) | (1u << 16);  // dS x K (MN-major)
+      const uint32_t id_s = idesc_bf16_f32(128, 128);
+      const uint32_t id_dq = idesc_bf16_f32(128, HD) | (1u << 16);  // dS (TMEM) x K (MN-major)
       bool ok = mbar_wait(q_full, 0);
-      auto issue_s = [&](int j) {
-        const int ks = j % C::KSTAGES, b2 = j & 1;
-        if (!mbar_wait(&kv_full[ks], (j / C::KSTAGES) & 1)) return false;
-        tc_fence_after();
+      auto issue_scores = [&](int j, const uint8_t* sA, const uint8_t* sB, uint32_t dst) {
+        const int ks = j & 1;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const int box = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t qa = smem_desc_kmajor_sw128(sQ + box * C::QBOX + off);
-          const uint64_t oa = smem_desc_kmajor_sw128(sdO + box * C::QBOX + off);
-          const uint64_t kb = smem_desc_kmajor_sw128(sK + ks * C::K_BYTES + box * C::KBOX + off);
-          const uint64_t vb = smem_desc_kmajor_sw128(sV + ks * C::K_BYTES + box * C::KBOX + off);
-          tc_mma_bf16(tmem + 64u * b2, qa, kb, id_s, kk > 0 ? 1u : 0u);
-          tc_mma_bf16(tmem + 128u + 64u * b2, oa, vb, id_s, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(dst, smem_desc_kmajor_sw128(sA + box * C::BOX + off),
+                      smem_desc_kmajor_sw128(sB + ks * C::TILE + box * C::BOX + off), id_s, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[b2]);
-        return true;
       };
-      auto issue_dq = [&](int j) {
-        const int ks = j % C::KSTAGES, b2 = j & 1;
-        if (!mbar_wait(&ds_full[b2], (j >> 1) & 1)) return false;
+      auto issue_s = [&](int j) {
+        if (!mbar_wait(&kv_full[j & 1], (j >> 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t kb = smem_desc_mnmajor_sw128(sK + ks * C::K_BYTES, C::KBOX);
-#pragma unroll
-        for (int kk = 0; kk < 64 / 16; ++kk) {
-          const uint64_t a = smem_desc_kmajor_sw128(sdS + b2 * C::DS_BYTES + kk * 32);
-          tc_mma_bf16(tdQ, a, kb + (uint64_t)(kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&kv_empty[ks]);
-        tc_commit(&ds_free[b2]);
+        issue_scores(j, sQ, sK, tmem + 128u * (uint32_t)(j & 1));
+        tc_commit(&s_full[j & 1]);
         return true;
       };
-      for (int j = 0; ok && j < n_kb; ++j) {
-        if (!issue_s(j)) ok = false;
-        if (ok && j > 0 && !issue_dq(j - 1)) ok = false;
+      if (ok) ok = issue_s(0);
+      if (ok) {
+        issue_scores(0, sdO, sV, tDP);
+        tc_commit(dp_full);
       }
-      if (ok && n_kb > 0 && !issue_dq(n_kb - 1)) ok = false;
+      for (int j = 0; ok && j < n_kb; ++j) {
+        const uint32_t ph = j & 1;
+        // S_{j+1} into the other buffer, whose dS_{j-1} the dQ MMAs issued before have read
+        if (j + 1 < n_kb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(sd_read, ph)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (j + 1 < n_kb) {
+          issue_scores(j + 1, sdO, sV, tDP);  // dP_{j+1}: every thread has read dP_j
+          tc_commit(dp_full);
+        }
+        if (!mbar_wait(&ds_ready[j & 1], (j >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t src = tmem + 128u * (uint32_t)(j & 1);
+        const uint64_t kd = smem_desc_mnmajor_sw128(sK + (j & 1) * C::TILE, C::BOX);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)
+          tc_mma_bf16_ts(tdQ, src + kk * 8, kd + (uint64_t)(kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&kv_empty[j & 1]);
+      }
       if (ok) {
         tc_commit(acc_full);
       } else {
@@ -922,7 +987,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
     }
   } else {
-    // softmax warps 2..9: thread <-> query row r, half hf of the 64 key columns
+    // softmax warps 2..9: thread <-> query row r, half hf of the 128 key columns
     const int quarter = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
@@ -934,45 +999,55 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     const float Dr = valid ? p.delta[li] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kb; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait_warp(&s_full[s], (j >> 1) & 1)) {
+      const uint32_t ph = j & 1;
+      const uint32_t tS = tmem + 128u * (uint32_t)(j & 1);
+      if (!mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[32], dp[32];
-      tmem_ld_32x32b_x32(tmem + 64u * s + lane_off + hf * 32, sv);
-      tmem_ld_32x32b_x32(tmem + 128u + 64u * s + lane_off + hf * 32, dp);
-      tmem_wait_ld();
-      if (j >= 2 && !mbar_wait_warp(&ds_free[s], ((j >> 1) - 1) & 1)) {
+      uint32_t sv[64];
+      tmem_ld_32x32b_x32(tS + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld_32x32b_x32(tS + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_wait_ld_regs(sv);
+      // Rows past the sequence end have L2 = +inf (P = 0); only the diagonal
+      // block (key block j == query block) needs the key > query mask.
+      const int k0 = j * 128;
+      const bool diag = j == qb;
+      float pf[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float pr = ex2_approx(fmaf(__uint_as_float(sv[c]), p.sl2, -L2));
+        if (diag && k0 + hf * 64 + c > qrow) pr = 0.f;
+        pf[c] = pr;
+      }
+      if (!mbar_wait_warp(dp_full, ph)) {
         ok = false;
         break;
       }
-      const int k0 = j * 64;
-      uint8_t* drow = sdS + s * C::DS_BYTES + r * 128;
-      // Rows past the sequence end have L2 = +inf (P = 0); only a block that
-      // reaches the causal diagonal needs the key > query mask.
-      const bool diag = k0 + 63 > q0;
+      tc_fence_after();
+      uint32_t pk[32];
 #pragma unroll
-      for (int k8 = 0; k8 < 4; ++k8) {
-        float dv[8];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dp[32];
+        tmem_ld_32x32b_x32(tDP + lane_off + hf * 64 + half * 32, dp);
+        tmem_wait_ld_regs(dp);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int cl = k8 * 8 + e;
-          const float pr = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.sl2, -L2));
-          dv[e] = pr * (__uint_as_float(dp[cl]) - Dr);
+        for (int e = 0; e < 16; ++e) {
+          const int c = half * 32 + 2 * e;
+          pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[2 * e]) - Dr), pf[c + 1] * (__uint_as_float(dp[2 * e + 1]) - Dr));
         }
-        if (diag) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (k0 + hf * 32 + k8 * 8 + e > qrow) dv[e] = 0.f;
-        }
-        *reinterpret_cast<uint4*>(drow + (((hf * 4 + k8) ^ (r & 7)) << 4)) = make_uint4(
-            pack2bf(dv[0], dv[1]), pack2bf(dv[2], dv[3]), pack2bf(dv[4], dv[5]), pack2bf(dv[6], dv[7]));
       }
-      fence_proxy_async_smem();
+      mbar_arrive(sd_read);
+      if (!mbar_wait_warp(sd_read, ph)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_packed32(tS + lane_off + hf * 32, pk);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ds_full[s]);
+      mbar_arrive(&ds_ready[j & 1]);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(acc_full, 0)) {
@@ -1011,13 +1086,9 @@ int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
   }
   const long T = (long)x.batch * x.seq;
   const long cols = (long)(x.n_heads + 2 * x.n_kv_heads) * HD;
-  CUtensorMap tm_kv128, tm_q64, tm_q128, tm_kv64, tm_do64, tm_do128;
-  if (!make_tmap_bf16(&tm_kv128, x.qkv, T, cols, x.ldqkv, 128) ||
-      !make_tmap_bf16(&tm_q64, x.qkv, T, cols, x.ldqkv, 64) ||
-      !make_tmap_bf16(&tm_q128, x.qkv, T, cols, x.ldqkv, 128) ||
-      !make_tmap_bf16(&tm_kv64, x.qkv, T, cols, x.ldqkv, 64) ||
-      !make_tmap_bf16(&tm_do64, x.dout, T, (long)x.n_heads * HD, x.ldo, 64) ||
-      !make_tmap_bf16(&tm_do128, x.dout, T, (long)x.n_heads * HD, x.ldo, 128))
+  CUtensorMap tm_qkv, tm_do;
+  if (!make_tmap_bf16(&tm_qkv, x.qkv, T, cols, x.ldqkv, 128) ||
+      !make_tmap_bf16(&tm_do, x.dout, T, (long)x.n_heads * HD, x.ldo, 128))
     return -3;
   TbParams p;
   p.B = x.batch;
@@ -1034,9 +1105,9 @@ int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
   p.sl2 = p.scale * kLog2eF;
   p.status = x.status;
   dim3 g1((x.seq + 127) / 128, x.batch * x.n_kv_heads);
-  attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_kv128, tm_q64, tm_do64, p);
+  attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_qkv, tm_do, p);
   dim3 g2((x.seq + 127) / 128, x.batch * x.n_heads);
-  attn_bwd_dq_tc_kernel<HD><<<g2, TB_THREADS, Bq::SMEM, s>>>(tm_q128, tm_kv64, tm_do128, p);
+  attn_bwd_dq_tc_kernel<HD><<<g2, TB_THREADS, Bq::SMEM, s>>>(tm_qkv, tm_do, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
