@@ -54,13 +54,13 @@ struct TaCfg {
   static constexpr int BOX = 128 * 128;          // one 64-column box of 128 rows, bytes
   static constexpr int Q_BYTES = 128 * HD * 2;   // HD/64 boxes
   static constexpr int KV_BYTES = 128 * HD * 2;  // K or V block
-  static constexpr int P_BYTES = 128 * 128 * 2;  // two 64-key boxes
+  static constexpr int STAGES = 3;               // K/V ring depth
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;            // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;       // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;       // 2 buffers
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;        // barriers + alignment slack
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;             // STAGES blocks
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;   // STAGES blocks
+  static constexpr int OFF_L = OFF_V + STAGES * KV_BYTES;   // [2][128] halves of the row sums
+  static constexpr int OFF_BAR = OFF_L + 2 * 128 * 4;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;         // barriers + alignment slack
 };
 
 struct TaParams {
@@ -81,21 +81,24 @@ template <int HD>
 __global__ void __launch_bounds__(TA_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, TaParams p) {
   using C = TaCfg<HD>;
+  constexpr int NS = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sP = smem + C::OFF_P;
+  float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_empty = bar + 3;  // [2]
-  uint64_t* s_full = bar + 5;    // [2]
-  uint64_t* p_full = bar + 7;    // [2]
-  uint64_t* pv_done = bar + 9;   // [2]
-  uint64_t* o_full = bar + 11;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+  uint64_t* kv_full = bar + 1;        // [NS]
+  uint64_t* kv_empty = bar + 1 + NS;  // [NS]
+  uint64_t* s_full = bar + 1 + 2 * NS;   // [2] S_j in TMEM buffer j & 1
+  uint64_t* p_full = bar + 3 + 2 * NS;   // [2] P_j stored over S_j, O rescaled (256 softmax threads)
+  uint64_t* pv_done = bar + 5 + 2 * NS;  // [2]
+  uint64_t* s_read = bar + 7 + 2 * NS;   // every softmax thread has read S_j (256)
+  uint64_t* o_full = bar + 8 + 2 * NS;
+  uint64_t* l_ready = bar + 9 + 2 * NS;  // both halves of every row sum written (256)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 10 + 2 * NS);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -111,14 +114,18 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 256);
       mbar_init(&pv_done[i], 1);
     }
+    mbar_init(s_read, 256);
     mbar_init(o_full, 1);
+    mbar_init(l_ready, 256);
     fence_barrier_init();
     tma_prefetch_desc(&tm_qkv);
   }
@@ -130,17 +137,18 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tO = tmem + 256;
+  const uint32_t tO = tmem + 256;  // S_j at 128 * (j & 1), O at 256
 
   if (warp == 0) {
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
       for (int i = 0; i < HD / 64; ++i) tma_load_2d(sQ + i * C::BOX, &tm_qkv, colQ + 64 * i, row0 + q0, q_full);
-      int pend[2] = {-1, -1};
+      int pend[NS];
+      for (int s = 0; s < NS; ++s) pend[s] = -1;
       for (int j = 0; j < n_kb && !abort_flag; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1)) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(&kv_empty[s], ((j / NS) - 1) & 1)) {
           set_status(p.status, kStatusAttnFwdTimeout * 1000 + 100 + min(j, 99));
           abort_flag = 1;
           break;
@@ -151,24 +159,24 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
           tma_load_2d(sK + s * C::KV_BYTES + i * C::BOX, &tm_qkv, colK + 64 * i, row0 + j * TA_BN, &kv_full[s]);
           tma_load_2d(sV + s * C::KV_BYTES + i * C::BOX, &tm_qkv, colV + 64 * i, row0 + j * TA_BN, &kv_full[s]);
         }
-        pend[s] = (j >> 1) & 1;
+        pend[s] = (j / NS) & 1;
       }
       // every issued load must land before exit
       if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusAttnFwdTimeout * 1000 + 200);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < NS; ++s)
         if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s]))
           set_status(p.status, kStatusAttnFwdTimeout * 1000 + 300 + s);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, 128);
-      const uint32_t id_pv = idesc_bf16_f32(128, HD) | (1u << 16);  // B (V) MN-major
+      const uint32_t id_pv = idesc_bf16_f32(128, HD) | (1u << 16);  // P (TMEM) x V (MN-major)
       int site = 0;
       bool ok = mbar_wait(q_full, 0);
       if (!ok) site = 400;
       auto issue_qk = [&](int j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_full[s], (j >> 1) & 1)) {
+        const int s = j % NS;
+        if (!mbar_wait(&kv_full[s], (j / NS) & 1)) {
           site = 500 + min(j, 99);
           return false;
         }
@@ -178,33 +186,32 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
           const int box = kk >> 2, off = (kk & 3) * 32;
           const uint64_t a = smem_desc_kmajor_sw128(sQ + box * C::BOX + off);
           const uint64_t bb = smem_desc_kmajor_sw128(sK + s * C::KV_BYTES + box * C::BOX + off);
-          tc_mma_bf16((tmem + 128u * (uint32_t)s), a, bb, id_qk, kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + 128u * (uint32_t)(j & 1), a, bb, id_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[s]);
+        tc_commit(&s_full[j & 1]);
         return true;
       };
       if (ok) ok = issue_qk(0);
       for (int j = 0; ok && j < n_kb; ++j) {
-        const int s = j & 1;
+        // S_{j+1} goes to the other buffer; the PV MMA that read P_{j-1} from it was issued before
         if (j + 1 < n_kb && !issue_qk(j + 1)) {
           ok = false;
           break;
         }
-        if (!mbar_wait(&p_full[s], (j >> 1) & 1)) {
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) {
           site = 600 + min(j, 99);
           ok = false;
           break;
         }
         tc_fence_after();
+        const int s = j % NS;
         const uint64_t vdesc = smem_desc_mnmajor_sw128(sV + s * C::KV_BYTES, C::BOX);
+        const uint32_t pa = tmem + 128u * (uint32_t)(j & 1);
 #pragma unroll
-        for (int kk = 0; kk < TA_BN / 16; ++kk) {
-          const int box = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t a = smem_desc_kmajor_sw128(sP + s * C::P_BYTES + box * C::BOX + off);
-          tc_mma_bf16(tO, a, vdesc + (uint64_t)(kk * (2048 >> 4)), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < TA_BN / 16; ++kk)
+          tc_mma_bf16_ts(tO, pa + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&kv_empty[s]);
-        tc_commit(&pv_done[s]);
+        tc_commit(&pv_done[j & 1]);
       }
       if (ok) {
         tc_commit(o_full);
@@ -225,8 +232,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     bool ok = true;
     int site = 0;
     for (int j = 0; j < n_kb; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait_warp(&s_full[s], (j >> 1) & 1)) {
+      const uint32_t tS = tmem + 128u * (uint32_t)(j & 1);
+      if (!mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1)) {
         site = 700 + min(j, 99);
         ok = false;
         break;
@@ -234,12 +241,10 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       tc_fence_after();
       uint32_t x[TA_BN];
 #pragma unroll
-      for (int c = 0; c < TA_BN / 32; ++c) {
-        uint32_t* xc = x + c * 32;
-        tmem_ld_32x32b_x32((tmem + 128u * (uint32_t)s) + lane_off + c * 32,
-                           *reinterpret_cast<uint32_t(*)[32]>(xc));
-      }
+      for (int c = 0; c < TA_BN / 32; ++c)
+        tmem_ld_32x32b_x32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(x + c * 32));
       tmem_wait_ld_regs(x);
+      mbar_arrive(s_read);
       const int k0 = j * TA_BN;
       if (k0 + TA_BN - 1 > q0) {  // block touches the diagonal
 #pragma unroll
@@ -258,28 +263,17 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         m = m_new;
       }
       const float nb = (m == -INFINITY) ? 0.f : -m * p.sl2;
-      // the P buffer is free once PV_{j-2} completed
-      if (j >= 2 && !mbar_wait_warp(&pv_done[s], ((j >> 1) - 1) & 1)) {
-        site = 800 + min(j, 99);
-        ok = false;
-        break;
-      }
+      // this half's 64 keys as packed BF16 pairs; the register array is indexed with constants only
       float rs = 0.f;
-      uint8_t* prow = sP + s * C::P_BYTES + hf * C::BOX + r * 128;
-      // this half's 64 keys; the register array is indexed with constants only
+      uint32_t pk[32];
       auto exp_half = [&](auto half) {
         constexpr int K0 = decltype(half)::value * 64;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {  // 16-byte chunks of 8 keys in the half's 64-key box
-          float e8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            e8[e] = ex2_approx(fmaf(__uint_as_float(x[K0 + cc * 8 + e]), p.sl2, nb));
-            rs += e8[e];
-          }
-          uint4 w = make_uint4(pack2bf(e8[0], e8[1]), pack2bf(e8[2], e8[3]), pack2bf(e8[4], e8[5]),
-                               pack2bf(e8[6], e8[7]));
-          *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = w;
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(x[K0 + 2 * e]), p.sl2, nb));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(x[K0 + 2 * e + 1]), p.sl2, nb));
+          rs += p0 + p1;
+          pk[e] = pack2bf(p0, p1);
         }
       };
       if (hf == 0)
@@ -287,6 +281,14 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       else
         exp_half(std::integral_constant<int, 1>{});
       l = l * alpha + rs;
+      // P_j over S_j's first 64 columns, once both halves of every row have read S_j
+      if (!mbar_wait_warp(s_read, j & 1)) {
+        site = 750 + min(j, 49);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_32x32b_x32(tS + lane_off + hf * 32, pk);
       // O holds sum_{i<j} P_i V_i.  tcgen05.ld/st are warp-collective, so the
       // whole warp rescales when any of its rows must (alpha = 1 for the others);
       // the two warps of a lane group see the same rows and scale one half each.
@@ -302,36 +304,33 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
           uint32_t v[32];
           const uint32_t ta = tO + lane_off + hf * (HD / 2) + c * 32;
           tmem_ld_32x32b_x32(ta, v);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tmem_st_32x32b_x32(ta, v);
         }
-        tmem_wait_st();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[s]);
+      mbar_arrive(&p_full[j & 1]);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !mbar_wait_warp(o_full, 0)) {
       site = 999;
       ok = false;
     }
-    // the two halves of each row sum meet in the (now idle) P buffer
-    float* lsum = reinterpret_cast<float*>(sP);
+    // the two halves of each row sum meet in shared memory
     if (ok) {
-      lsum[hf * 128 + r] = l;
-      mbar_arrive(&p_full[0]);  // one more phase of p_full[0] collects all 256 halves
-      const int ph = ((n_kb + 1) >> 1) & 1;  // phases of p_full[0] completed so far: ceil(n_kb / 2)
-      if (!mbar_wait_warp(&p_full[0], (uint32_t)ph)) {
+      sL[hf * 128 + r] = l;
+      mbar_arrive(l_ready);
+      if (!mbar_wait_warp(l_ready, 0)) {
         site = 998;
         ok = false;
       }
     }
     if (ok) {
       tc_fence_after();
-      const float lt = lsum[r] + lsum[128 + r];
+      const float lt = sL[r] + sL[128 + r];
       const float inv = 1.f / lt;
       const bool valid = qrow < S;
       bf16* dst = p.o + (long)(row0 + qrow) * p.ldo + (long)h * HD + hf * (HD / 2);
@@ -339,7 +338,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       for (int c = 0; c < HD / 64; ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tO + lane_off + hf * (HD / 2) + c * 32, v);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(v);
         if (valid) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
