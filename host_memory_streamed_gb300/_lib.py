@@ -17,7 +17,7 @@ ERROR_NAMES = {0: "MT_OK", -1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_ECUDA", -4:
 MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS, MT_TRACE = 1, 2, 4, 8, 16, 32
 MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
-EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE = range(6)
+EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE, EPI_SWIGLU_BWD = range(7)
 
 
 class MtConfig(C.Structure):
@@ -52,6 +52,7 @@ class MtStepStats(C.Structure):
         ("gemm_flops", C.c_double), ("gemm_launches", C.c_int64), ("kernel_launches", C.c_int64),
         ("h2d_bytes", C.c_int64), ("d2h_bytes", C.c_int64), ("flops_executed", C.c_int64),
         ("flops_model", C.c_int64), ("arena_high_water", C.c_int64), ("step", C.c_int64),
+        ("visit_gap_ms", C.c_double),
     ]
 
 

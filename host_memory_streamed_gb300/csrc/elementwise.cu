@@ -261,6 +261,27 @@ __global__ void embed_bwd_kernel(const int32_t* __restrict__ off, const int32_t*
   }
 }
 
+// Only the vocabulary rows that occur among the step's tokens: out[u] = sum of
+// the dx rows listed for rows[u] (ascending positions), u < U, packed densely.
+__global__ void embed_bwd_rows_kernel(const int32_t* __restrict__ off, const int32_t* __restrict__ pos,
+                                      const int32_t* __restrict__ rows, const bf16* __restrict__ dx,
+                                      bf16* __restrict__ out, int d) {
+  const long u = blockIdx.x;
+  const int v = rows[u];
+  const int b = off[v], e = off[v + 1];
+  uint4* o = reinterpret_cast<uint4*>(out + u * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int k = b; k < e; ++k) {
+      float f[8];
+      unpack8(reinterpret_cast<const uint4*>(dx + (long)pos[k] * d)[i], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += f[j];
+    }
+    o[i] = pack8(acc);
+  }
+}
+
 // ---------------------------------------------------------------- cross-entropy
 constexpr int CE_THREADS = 512;
 // One block per row.  Pass 1: per-thread online (max, sum) over a strided
@@ -431,6 +452,11 @@ void launch_embed_fwd(const int32_t* tok, const bf16* E, bf16* x, long T, int d,
                       cudaStream_t s) {
   if (T <= 0) return;
   embed_fwd_kernel<<<(unsigned)T, 128, 0, s>>>(tok, E, x, T, d, V, status);
+}
+
+void launch_embed_bwd_rows(const int32_t* off, const int32_t* pos, const int32_t* rows, int U, const bf16* dx,
+                           bf16* out, int d, cudaStream_t s) {
+  if (U > 0) embed_bwd_rows_kernel<<<(unsigned)U, 128, 0, s>>>(off, pos, rows, dx, out, d);
 }
 
 void launch_embed_bwd(const int32_t* off, const int32_t* pos, const bf16* dx, bf16* dE, int V, int d,

@@ -183,6 +183,41 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
       }
       break;
     }
+    case kEpiSwiGLUBwd: {
+      // v = da[row, col0 .. col0 + 31] (FP32); (gate, up) pairs from R; (dgate, dup) pairs to C.
+      const __nv_bfloat16* g = p.R + (long)row * p.ldr + 2 * col0;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + (long)row * p.ldc + 2 * col0;
+      auto grad = [](float da, float gt, float up, float& dg, float& du) {
+        const float sg = 1.0f / (1.0f + __expf(-gt));
+        dg = da * up * sg * (1.0f + gt * (1.0f - sg));
+        du = da * gt * sg;
+      };
+      if (nvalid >= 32) {
+        const uint4* g4 = reinterpret_cast<const uint4*>(g);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // 4 (gate, up) pairs per 16 bytes
+          const uint4 w = g4[q];
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float dg, du;
+            grad(v[q * 4 + e], bf16_lo(ws[e]), bf16_hi(ws[e]), dg, du);
+            o[e] = pack_bf16(dg, du);
+          }
+          d4[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      } else {
+        for (int j = 0; j < nvalid; ++j) {
+          float dg, du;
+          grad(v[j], __bfloat162float(g[2 * j]), __bfloat162float(g[2 * j + 1]), dg, du);
+          dst[2 * j] = __float2bfloat16_rn(dg);
+          dst[2 * j + 1] = __float2bfloat16_rn(du);
+        }
+      }
+      break;
+    }
     default:
       break;
   }
@@ -470,6 +505,11 @@ const char* gemm_check(const GemmArgs& g) {
       break;
     case kEpiResidualBf16:
       if (!g.R || (reinterpret_cast<uintptr_t>(g.R) & 15) || g.ldr % 8) return "gemm: bad residual operand";
+      break;
+    case kEpiSwiGLUBwd:
+      if (!g.R || (reinterpret_cast<uintptr_t>(g.R) & 15) || g.ldr % 8 || g.ldr < 2L * g.N)
+        return "gemm: SwiGLU backward needs the gate/up pairs R [M, 2N]";
+      if (g.ldc < 2L * g.N) return "gemm: SwiGLU backward writes C [M, 2N]";
       break;
     case kEpiSwiGLU:
       if (g.N % 2) return "gemm: SwiGLU needs an even N";

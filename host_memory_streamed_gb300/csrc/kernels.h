@@ -30,6 +30,7 @@ enum EpiMode : int {
   kEpiF32Accumulate = 3,  // C(f32) += acc
   kEpiSwiGLU = 4,         // columns (2j, 2j+1) = (gate, up): C[:, j] = silu(gate) * up; C2 = gu (optional)
   kEpiRope = 5,           // C(bf16) = acc, rotate-half RoPE on columns < rope_cols
+  kEpiSwiGLUBwd = 6,      // acc = da[:, j]; R = gu [M, 2N] (gate, up interleaved); C[:, 2j | 2j+1] = (dgate, dup)
 };
 
 struct GemmArgs {
@@ -105,6 +106,9 @@ void launch_transpose(const bf16* src, long rows, long cols, long lds, bf16* dst
 void launch_embed_fwd(const int32_t* tok, const bf16* E, bf16* x, long T, int d, int V, int* status,
                       cudaStream_t s);
 // dE[v] = sum over t in pos[off[v] .. off[v+1]) of dx[t] (ascending t), zeros elsewhere.
+// Compact embedding gradient: out[u] = sum of dx rows of token id rows[u], u < U.
+void launch_embed_bwd_rows(const int32_t* off, const int32_t* pos, const int32_t* rows, int U, const bf16* dx,
+                           bf16* out, int d, cudaStream_t s);
 void launch_embed_bwd(const int32_t* off, const int32_t* pos, const bf16* dx, bf16* dE, int V, int d,
                       cudaStream_t s);
 // Row-wise cross-entropy on FP32 logits z [rows, V]:

@@ -207,9 +207,15 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
 
   // x_out = h + a Wd^T
   wgrad(dx_out, D.d, a.a, D.f, gv.wd);
-  dgrad(dx_out, D.d, w.wd, D.f, W.da);
-  launch_swiglu_bwd(W.da, a.gu, W.dgu, T, D.f, s);
-  trace("swiglu_bwd");
+  // da = dx_out Wd (Wd read MN-major), and in the same epilogue the SwiGLU
+  // backward: dgu = (da * up * silu'(gate), da * silu(gate)) from the stored gate/up
+  {
+    GemmArgs g = mk(dx_out, D.d, w.wd, D.f, (int)T, D.f, D.d, kEpiSwiGLUBwd, W.dgu, 2L * D.f, W.status);
+    g.b_mn = true;
+    g.R = a.gu;
+    g.ldr = 2L * D.f;
+    rc |= gemm(g);
+  }
   wgrad(W.dgu, 2 * D.f, a.n2, D.d, gv.wgu);
   dgrad(W.dgu, 2 * D.f, w.wgu, D.d, W.dn);
   // dh = dx_out + RMSNorm2^T dn2 ; dg2
@@ -243,7 +249,7 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   launch_rmsnorm_bwd(W.dn, a.x, w.g1, a.rstd1, W.dh, dx_in, W.dg_partial, T, D.d, s);
   trace("rmsnorm_bwd");
   launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g1, s);
-  stats->kernels += 8;  // swiglu, 2 x (rmsnorm bwd + colsum), attention delta + dK/dV + dQ
+  stats->kernels += 7;  // 2 x (rmsnorm bwd + colsum), attention delta + dK/dV + dQ
   return rc;
 }
 
@@ -286,6 +292,13 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
 int LayerTemplate::embed_fwd(const bf16* E, bf16* x0) const {
   launch_embed_fwd(ws->inp, E, x0, dm.T, dm.d, dm.V, ws->status, s);
   trace("embed_fwd");
+  stats->kernels += 1;
+  return 0;
+}
+
+int LayerTemplate::embed_bwd_rows(const bf16* dx0, bf16* out, int U) const {
+  launch_embed_bwd_rows(ws->emb_off, ws->emb_pos, ws->emb_rows, U, dx0, out, dm.d, s);
+  trace("embed_bwd_rows");
   stats->kernels += 1;
   return 0;
 }

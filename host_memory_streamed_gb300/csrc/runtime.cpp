@@ -41,6 +41,10 @@
 #include <thread>
 #include <vector>
 
+#include <sys/resource.h>
+#include <sys/syscall.h>
+#include <unistd.h>
+
 #include "runtime.h"
 
 namespace mt {
@@ -60,8 +64,14 @@ struct MtError {
 // ------------------------------------------------------------------ small thread pool
 class Pool {
  public:
-  explicit Pool(int n) {
-    for (int i = 0; i < n; ++i) th_.emplace_back([this] { run(); });
+  // nice > 0 lowers the workers' scheduling priority (Linux niceness of each
+  // worker thread), so that work on the step's critical path preempts them.
+  explicit Pool(int n, int nice = 0) {
+    for (int i = 0; i < n; ++i)
+      th_.emplace_back([this, nice] {
+        if (nice > 0) setpriority(PRIO_PROCESS, (id_t)syscall(SYS_gettid), nice);
+        run();
+      });
   }
   ~Pool() {
     {
@@ -244,7 +254,6 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.dx_a = reinterpret_cast<bf16*>(at(td));
   w.dx_b = reinterpret_cast<bf16*>(at(td));
   w.dh = reinterpret_cast<bf16*>(at(td));
-  w.da = reinterpret_cast<bf16*>(at(T * (int64_t)D.f * 2));
   w.dgu = reinterpret_cast<bf16*>(at(T * 2L * D.f * 2));
   w.dn = reinterpret_cast<bf16*>(at(td));
   w.dout = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dq * 2));
@@ -263,6 +272,7 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.tgt = reinterpret_cast<int32_t*>(at(T * 4));
   w.emb_off = reinterpret_cast<int32_t*>(at(((int64_t)D.V + 1) * 4));
   w.emb_pos = reinterpret_cast<int32_t*>(at(T * 4));
+  w.emb_rows = reinterpret_cast<int32_t*>(at(std::min<int64_t>(T, D.V) * 4));
   w.tokens_dev = reinterpret_cast<int32_t*>(at((int64_t)D.B * (D.S + 1) * 4));
   w.rope_cos = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
   w.rope_sin = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
@@ -312,7 +322,8 @@ struct mt_model {
   std::vector<uint8_t*> slabs;
   int64_t slab_bytes = 0;
   float* pinned_scalars = nullptr;  // [0] loss, [1] status bits
-  int32_t* pinned_tok = nullptr;    // inp | tgt | emb_off | emb_pos | raw tokens
+  int32_t* pinned_tok = nullptr;    // inp | tgt | emb_off | emb_pos | emb_rows
+  int emb_u = 0;                    // number of distinct token ids of the step (rows of the compact dE)
 
   // schedule + events
   std::vector<mt::Visit> visits;
@@ -320,6 +331,7 @@ struct mt_model {
   int last_grad_visit = -1;
   std::vector<cudaEvent_t> ev_ready, ev_free, ev_grads, ev_d2h;
   std::vector<cudaEvent_t> ev_wait_a, ev_wait_b, ev_h2d_a, ev_h2d_b, ev_d2h_a, ev_d2h_b;
+  std::vector<cudaEvent_t> ev_vis_a, ev_vis_b;  // first / last kernel of each visit on the compute stream
   cudaEvent_t ev_stage[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ev_slab;
   cudaEvent_t ev_t0 = nullptr, ev_t1 = nullptr;
@@ -343,6 +355,7 @@ struct mt_model {
     int slab, visit, tile;
     int64_t off, bytes;
     bool last;
+    bool rows;  // compact embedding gradient: the slab holds whole rows of emb_rows, from row off / (2 d)
   };
   std::deque<AccJob> acc_q;
   std::vector<int> free_slabs;
@@ -523,15 +536,19 @@ void d2h_main(mt_model* m) {
       MT_CK(cudaStreamWaitEvent(m->s_d2h, m->ev_grads[v], 0));
       MT_CK(cudaEventRecord(m->ev_d2h_a[v], m->s_d2h));
       const uint8_t* src = m->gbuf[x.gbuf];
-      const int64_t n = lay.w_bytes;
-      for (int64_t off = 0; off < n; off += m->slab_bytes) {
-        const int64_t c = std::min(m->slab_bytes, n - off);
+      // the embedding gradient leaves compact (rows of the step's token ids), in whole rows per slab
+      const bool rows = x.kind == kEmbedBwd;
+      const int64_t row_b = 2LL * m->D.d;
+      const int64_t n = rows ? (int64_t)m->emb_u * row_b : lay.w_bytes;
+      const int64_t chunk = rows ? m->slab_bytes / row_b * row_b : m->slab_bytes;
+      for (int64_t off = 0; off < n; off += chunk) {
+        const int64_t c = std::min(chunk, n - off);
         const int s = acquire_slab(m);
         MT_CK(cudaMemcpyAsync(m->slabs[s], src + off, (size_t)c, cudaMemcpyDeviceToHost, m->s_d2h));
         MT_CK(cudaEventRecord(m->ev_slab[s], m->s_d2h));
         {
           std::lock_guard<std::mutex> g(m->mu);
-          m->acc_q.push_back({s, v, x.tile, off, c, off + c >= n});
+          m->acc_q.push_back({s, v, x.tile, off, c, off + c >= n, rows});
         }
         m->cv.notify_all();
       }
@@ -545,15 +562,23 @@ void d2h_main(mt_model* m) {
   }
 }
 
-void submit_adam(mt_model* m, int tile) {
+// Adam on the elements of tile `tile` whose BF16 gradients occupy bytes
+// [g_off, g_off + g_bytes) of its G section (one landed gradient slab): the
+// update is elementwise, so each slab is updated as soon as it lands.
+void submit_adam_range(mt_model* m, int tile, int64_t g_off, int64_t g_bytes) {
   const TileLayout& lay = m->layouts[tile];
   uint8_t* base = m->tiles[tile];
   const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
+  const int64_t lo_b = g_off, hi_b = g_off + g_bytes;
   for (const auto& t : lay.tensors) {
-    const int64_t n = t.numel;
-    const int64_t piece = std::max<int64_t>(1 << 20, (n + m->adam_pool->size() - 1) / m->adam_pool->size());
-    for (int64_t b = 0; b < n; b += piece) {
-      const int64_t c = std::min(piece, n - b);
+    // element range of this tensor inside [lo_b, hi_b)
+    const int64_t e0 = std::max<int64_t>(0, (lo_b - t.offset + 1) / 2);
+    const int64_t e1 = std::min<int64_t>(t.numel, (hi_b - t.offset) / 2);
+    if (e1 <= e0) continue;
+    const int64_t n = e1 - e0;
+    const int64_t piece = std::max<int64_t>(1 << 18, (n + m->adam_pool->size() - 1) / m->adam_pool->size());
+    for (int64_t b = e0; b < e1; b += piece) {
+      const int64_t c = std::min(piece, e1 - b);
       uint16_t* w = reinterpret_cast<uint16_t*>(base + lay.off_w + t.offset) + b;
       const uint16_t* g = reinterpret_cast<const uint16_t*>(base + lay.off_g + t.offset) + b;
       float* mm = reinterpret_cast<float*>(base + lay.off_m + 2 * t.offset) + b;
@@ -564,6 +589,74 @@ void submit_adam(mt_model* m, int tile) {
         m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
       });
     }
+  }
+}
+
+// Embedding rows whose gradient is zero this step (token ids that do not occur):
+// zero their G rows and, when the loss is finite, run Adam on them (g = 0).
+// Submitted once the loss is known (the head's gradient lands).  The embedding
+// W was streamed for the forward before the head ran and the backward does
+// not read it, so these rows may be updated mid-step.
+void submit_untouched_embed(mt_model* m) {
+  const TileLayout& lay = m->layouts[0];
+  const TensorSlot& E = lay.slot("E");
+  const int d = m->D.d, V = m->D.V;
+  uint8_t* base = m->tiles[0];
+  const int32_t* off = m->pinned_tok + 2 * m->D.T;  // emb_off [V + 1]
+  const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
+  constexpr int kRowsPerTask = 64;
+  for (int v0 = 0; v0 < V; v0 += kRowsPerTask) {
+    const int v1 = std::min(V, v0 + kRowsPerTask);
+    m->adam_pool->submit([=] {
+      const auto t0 = Clock::now();
+      for (int v = v0; v < v1; ++v) {
+        if (off[v + 1] > off[v]) continue;
+        const int64_t e = (int64_t)v * d;
+        uint16_t* g = reinterpret_cast<uint16_t*>(base + lay.off_g + E.offset) + e;
+        std::memset(g, 0, sizeof(uint16_t) * d);
+        if (m->nonfinite) continue;
+        adam_range(reinterpret_cast<uint16_t*>(base + lay.off_w + E.offset) + e, g,
+                   reinterpret_cast<float*>(base + lay.off_m + 2 * E.offset) + e,
+                   reinterpret_cast<float*>(base + lay.off_v + 2 * E.offset) + e, (size_t)d, h);
+      }
+      m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
+    });
+  }
+}
+
+// One slab of the compact embedding gradient: rows u0 .. u0 + nrows of the
+// step's token ids.  Scatter each row into the tile's G section, check it is
+// finite, and update the row (Adam) in the same task.
+void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<bool>& fin) {
+  const TileLayout& lay = m->layouts[j.tile];
+  const TensorSlot& E = lay.slot("E");
+  const int d = m->D.d;
+  const int64_t row_b = 2LL * d;
+  const int64_t u0 = j.off / row_b, nrows = j.bytes / row_b;
+  const int32_t* rows = m->pinned_tok + 3 * m->D.T + m->D.V + 1;  // emb_rows
+  uint8_t* base = m->tiles[j.tile];
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
+  const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
+  const int nt = m->acc_pool->size();
+  const int64_t per = std::max<int64_t>(16, (nrows + nt - 1) / nt);
+  for (int64_t a = 0; a < nrows; a += per) {
+    const int64_t b = std::min(nrows, a + per);
+    m->acc_pool->submit([=, &fin] {
+      for (int64_t k = a; k < b; ++k) {
+        const int64_t e = (int64_t)rows[u0 + k] * d;
+        uint16_t* g = reinterpret_cast<uint16_t*>(base + lay.off_g + E.offset) + e;
+        if (!copy_grad_check_finite(g, src + k * d, (size_t)d)) {
+          fin = false;
+          m->nonfinite = true;
+        }
+        if (m->nonfinite) continue;
+        const auto t0 = Clock::now();
+        adam_range(reinterpret_cast<uint16_t*>(base + lay.off_w + E.offset) + e, g,
+                   reinterpret_cast<float*>(base + lay.off_m + 2 * E.offset) + e,
+                   reinterpret_cast<float*>(base + lay.off_v + 2 * E.offset) + e, (size_t)d, h);
+        m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
+      }
+    });
   }
 }
 
@@ -580,7 +673,26 @@ void accum_main(mt_model* m) {
     }
     try {
       wait_event(m, m->ev_slab[j.slab], "gradient slab copy");
-      if (m->visits[j.visit].kind == kHead && j.off == 0 && !std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
+      if (m->visits[j.visit].kind == kHead && j.off == 0) {
+        if (!std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
+        submit_untouched_embed(m);
+      }
+      if (j.rows) {
+        std::atomic<bool> fin{true};
+        accumulate_embed_rows(m, j, fin);
+        if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
+        if (!fin) m->nonfinite = true;
+        {
+          std::lock_guard<std::mutex> g(m->mu);
+          m->free_slabs.push_back(j.slab);
+          if (j.last) {
+            m->acc_tiles_done += 1;
+            m->last_grads_landed = Clock::now();
+          }
+        }
+        m->cv.notify_all();
+        continue;
+      }
       const TileLayout& lay = m->layouts[j.tile];
       uint16_t* dst = reinterpret_cast<uint16_t*>(m->tiles[j.tile] + lay.off_g + j.off);
       const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
@@ -602,8 +714,8 @@ void accum_main(mt_model* m) {
         m->free_slabs.push_back(j.slab);
       }
       m->cv.notify_all();
+      if (!m->nonfinite) submit_adam_range(m, j.tile, j.off, j.bytes);
       if (j.last) {
-        if (!m->nonfinite) submit_adam(m, j.tile);
         {
           std::lock_guard<std::mutex> g(m->mu);
           m->acc_tiles_done += 1;
@@ -640,12 +752,19 @@ void prepare_tokens(mt_model* m, const int32_t* tokens) {
   for (int v = 0; v < D.V; ++v) off[v + 1] += off[v];
   std::vector<int32_t> cur(off, off + D.V);
   for (long t = 0; t < T; ++t) pos[cur[inp[t]]++] = (int32_t)t;
+  // token ids that occur in the step: the only rows of dE that can be nonzero
+  int32_t* rows = pos + T;
+  int u = 0;
+  for (int v = 0; v < D.V; ++v)
+    if (off[v + 1] > off[v]) rows[u++] = v;
+  m->emb_u = u;
   const size_t bytes = sizeof(int32_t) * (size_t)(2 * T + D.V + 1 + T);
   // ws.inp, tgt, emb_off, emb_pos are not contiguous in the arena: copy each.
   MT_CK(cudaMemcpyAsync(m->ws.inp, inp, sizeof(int32_t) * T, cudaMemcpyHostToDevice, m->s_comp));
   MT_CK(cudaMemcpyAsync(m->ws.tgt, tgt, sizeof(int32_t) * T, cudaMemcpyHostToDevice, m->s_comp));
   MT_CK(cudaMemcpyAsync(m->ws.emb_off, off, sizeof(int32_t) * (D.V + 1), cudaMemcpyHostToDevice, m->s_comp));
   MT_CK(cudaMemcpyAsync(m->ws.emb_pos, pos, sizeof(int32_t) * T, cudaMemcpyHostToDevice, m->s_comp));
+  MT_CK(cudaMemcpyAsync(m->ws.emb_rows, rows, sizeof(int32_t) * u, cudaMemcpyHostToDevice, m->s_comp));
   (void)bytes;
 }
 
@@ -777,6 +896,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       }
       const TileLayout& lay = m->layouts[x.tile];
       int rc = 0;
+      MT_CK(cudaEventRecord(m->ev_vis_a[v], m->s_comp));
       switch (x.kind) {
         case kEmbedFwd:
           rc = tmpl.embed_fwd(reinterpret_cast<bf16*>(wb + lay.slot("E").offset), x_fwd_loc(m, 0));
@@ -814,12 +934,13 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
           std::swap(dx_cur, dx_nxt);
           break;
         }
-        case kEmbedBwd:
-          rc = tmpl.embed_bwd(dx_cur, reinterpret_cast<bf16*>(gb + lay.slot("E").offset));
+        case kEmbedBwd:  // compact: the rows of the step's token ids, packed from the buffer start
+          rc = tmpl.embed_bwd_rows(dx_cur, reinterpret_cast<bf16*>(gb), m->emb_u);
           break;
       }
       if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(cudaGetLastError())};
       MT_CK(cudaPeekAtLastError());
+      MT_CK(cudaEventRecord(m->ev_vis_b[v], m->s_comp));
       if (x.buf >= 0 && !m->resident_mode) {
         MT_CK(cudaEventRecord(m->ev_free[v], m->s_comp));
         set_flag(m, m->rec_free, v);
@@ -839,7 +960,10 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
                                           " (" + kind_name[x.kind] + ", layer " + std::to_string(x.layer) + ")"};
       }
       if (x.grads) {
-        if (m->debug) launch_check_finite(reinterpret_cast<bf16*>(gb), lay.w_bytes / 2, m->ws.status, m->s_comp);
+        if (m->debug)
+          launch_check_finite(reinterpret_cast<bf16*>(gb),
+                              x.kind == kEmbedBwd ? (int64_t)m->emb_u * D.d : lay.w_bytes / 2, m->ws.status,
+                              m->s_comp);
         MT_CK(cudaEventRecord(m->ev_grads[v], m->s_comp));
         {
           std::lock_guard<std::mutex> g(m->mu);
@@ -880,9 +1004,10 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       if (m->rec_d2h_timed[v] && cudaEventElapsedTime(&f, m->ev_d2h_a[v], m->ev_d2h_b[v]) == cudaSuccess) st.d2h_ms += f;
       if (m->rec_wait_timed[v] && cudaEventElapsedTime(&f, m->ev_wait_a[v], m->ev_wait_b[v]) == cudaSuccess)
         st.wait_weights_ms += f;
+      if (v > 0 && cudaEventElapsedTime(&f, m->ev_vis_b[v - 1], m->ev_vis_a[v]) == cudaSuccess) st.visit_gap_ms += f;
       const Visit& x = m->visits[v];
       if (x.h2d && !m->resident_mode) st.h2d_bytes += m->layouts[x.tile].w_bytes;
-      if (x.grads) st.d2h_bytes += m->layouts[x.tile].w_bytes;
+      if (x.grads) st.d2h_bytes += x.kind == kEmbedBwd ? 2LL * m->emb_u * D.d : m->layouts[x.tile].w_bytes;
     }
     cudaGetLastError();
     for (size_t i = 0; i + 1 < m->gemm_events.size(); i += 2) {
@@ -952,6 +1077,8 @@ const char* validate(const mt_config& c) {
   if (c.d_model % 8 || c.ffn % 8 || c.vocab % 8) return "d_model, ffn and vocab must be multiples of 8";
   if (((int64_t)c.batch * c.seq) % 8) return "batch * seq must be a multiple of 8";
   if (c.ckpt_every < 1) return "ckpt_every must be >= 1";
+  if (c.grad_slab_bytes > 0 && align_up(c.grad_slab_bytes, kPage) < 2LL * c.d_model)
+    return "grad_slab_bytes must hold one embedding row (2 * d_model bytes)";
   if (!(c.rms_eps > 0) || !(c.rope_theta > 0) || !(c.lr >= 0) || !(c.beta1 >= 0 && c.beta1 < 1) ||
       !(c.beta2 >= 0 && c.beta2 < 1) || !(c.adam_eps >= 0))
     return "bad hyper-parameter";
@@ -1076,6 +1203,8 @@ void destroy(mt_model* m) {
   kill(m->ev_h2d_b);
   kill(m->ev_d2h_a);
   kill(m->ev_d2h_b);
+  kill(m->ev_vis_a);
+  kill(m->ev_vis_b);
   kill(m->ev_slab);
   kill(m->gemm_events);
   for (auto& e : m->ev_stage)
@@ -1143,6 +1272,8 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   mk(m->ev_h2d_b, true);
   mk(m->ev_d2h_a, true);
   mk(m->ev_d2h_b, true);
+  mk(m->ev_vis_a, true);
+  mk(m->ev_vis_b, true);
   for (auto& e : m->ev_stage) MT_CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   MT_CK(cudaEventCreate(&m->ev_t0));
   MT_CK(cudaEventCreate(&m->ev_t1));
@@ -1177,7 +1308,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
     m->free_slabs.push_back(i);
   }
   MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_scalars), 256, cudaHostAllocDefault));
-  const size_t ntok = (size_t)(3 * m->D.T + m->D.V + 1);
+  const size_t ntok = (size_t)(3 * m->D.T + m->D.V + 1 + std::min<int64_t>(m->D.T, m->D.V));
   MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_tok), ntok * sizeof(int32_t), cudaHostAllocDefault));
 
   // RoPE tables (rotate-half; angle = s * theta^(-2i/hd)), computed in double
@@ -1198,9 +1329,11 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   MT_CK(cudaMemset(m->gbuf[1], 0, (size_t)m->max_w_bytes));
   MT_CK(cudaDeviceSynchronize());
 
-  m->adam_pool.reset(new Pool(m->cfg.n_adam_threads));
+  // Adam is background work for the step (it only has to finish by its end);
+  // packing weights and draining gradient slabs gate the GPU, so they win.
+  m->adam_pool.reset(new Pool(m->cfg.n_adam_threads, 10));
   m->pack_pool.reset(new Pool(m->cfg.n_pack_threads));
-  m->acc_pool.reset(new Pool(std::max(1, m->cfg.n_pack_threads)));
+  m->acc_pool.reset(new Pool(std::max(1, std::min(8, m->cfg.n_adam_threads))));
   m->loader = std::thread(loader_main, m);
   m->d2h = std::thread(d2h_main, m);
   m->accum = std::thread(accum_main, m);

@@ -86,7 +86,7 @@ struct LayerActs {
 struct Workspace {
   // backward scratch
   bf16 *dx_a, *dx_b;    // ping-pong dx between layers
-  bf16 *dh, *da, *dgu, *dn, *dout, *dqkv;
+  bf16 *dh, *dgu, *dn, *dout, *dqkv;
   float* delta;
   float* dg_partial;
   // head
@@ -103,6 +103,7 @@ struct Workspace {
   int32_t* tgt;    // [T]
   int32_t* emb_off;  // [V+1]
   int32_t* emb_pos;  // [T]
+  int32_t* emb_rows; // [min(T, V)] token ids that occur in the step, ascending
   int32_t* tokens_dev;  // [B, S+1] (device-token entry point)
   float *rope_cos, *rope_sin;  // [S, hd/2]
   int* status;
@@ -148,6 +149,8 @@ struct LayerTemplate {
   int head(const HeadView& w, const bf16* x_L, bf16* dx_L, const HeadView& gv) const;
   int embed_fwd(const bf16* E, bf16* x0) const;
   int embed_bwd(const bf16* dx0, bf16* dE) const;
+  // Gradient rows of the U token ids in ws->emb_rows only, packed [U, d].
+  int embed_bwd_rows(const bf16* dx0, bf16* out, int U) const;
 };
 
 }  // namespace mt

@@ -66,7 +66,9 @@ enum {
   MT_ECUDA = -3,       /* a CUDA call failed */
   MT_ETIMEDOUT = -4,   /* a bounded wait (host event poll or device mbarrier) expired */
   MT_ESTATE = -5,      /* call not allowed in the handle's state */
-  MT_ENONFINITE = -6,  /* the loss or a gradient is NaN/Inf; the step's update was not applied */
+  MT_ENONFINITE = -6,  /* the loss or a gradient is NaN/Inf: Adam is not applied to any gradient chunk
+                          that lands after the first non-finite value is seen; a non-finite loss is seen
+                          before any gradient lands, so then no weight is updated */
   MT_EINTERNAL = -7    /* a worker thread failed */
 };
 
@@ -136,6 +138,8 @@ typedef struct {
   int64_t flops_model;     /* 6 * N_linear * T + causal-attention FLOPs (3x forward) */
   int64_t arena_high_water;
   int64_t step;            /* Adam step counter after this step */
+  double visit_gap_ms;     /* compute-stream time between the end of one visit's kernels and the start of
+                              the next one's: stream waits plus idle time while the host was behind */
 } mt_step_stats;
 
 /* Device bytes the handle needs in its arena for this config (>0), or a negative MT_E* code. */

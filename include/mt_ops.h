@@ -31,8 +31,11 @@ enum {
   MT_EPI_F32_ACCUMULATE = 3,/* C += acc (FP32) */
   MT_EPI_SWIGLU = 4,       /* columns (2j, 2j+1) are (gate, up): C[:, j] = silu(gate)*up (BF16, N/2 cols);
                               C2, when not NULL, receives the BF16 gate/up values themselves */
-  MT_EPI_ROPE = 5          /* C = acc (BF16) with rotate-half RoPE applied to columns < rope_cols,
+  MT_EPI_ROPE = 5,         /* C = acc (BF16) with rotate-half RoPE applied to columns < rope_cols,
                               heads of head_dim columns, position = row % seq */
+  MT_EPI_SWIGLU_BWD = 6    /* acc = da, the gradient of a = silu(gate) * up (N columns); R = the BF16
+                              (gate, up) pairs [M, 2N] interleaved; C (BF16, [M, 2N]) receives
+                              (da * up * silu'(gate), da * silu(gate)) at columns (2j, 2j+1) */
 };
 
 const char* mt_op_last_error(void);

@@ -79,6 +79,22 @@ def test_gemm_residual_accumulate_swiglu_rope():
     assert rel(ro, expect) < 4e-3
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 344, 256), (256, 688, 512), (33, 40, 64)])
+def test_gemm_swiglu_backward_epilogue(M, N, K):
+    """da = dY W (FP32 accumulator) and, in the same epilogue, the SwiGLU
+    backward against the stored (gate, up) pairs."""
+    g = torch.Generator().manual_seed(M + N + K)
+    dY, W = rnd((M, K), g), rnd((N, K), g, 0.1)
+    gu = rnd((M, 2 * N), g, 2.0)
+    dgu = torch.empty(M, 2 * N, device=DEV, dtype=torch.bfloat16)
+    ops.gemm(dY.to(DEV), W.to(DEV), dgu, _lib.EPI_SWIGLU_BWD, residual=gu.to(DEV))
+    torch.cuda.synchronize()
+    da = dY.to(D) @ W.to(D).T
+    dg, du = oracle.swiglu_backward(da, gu.to(D)[:, 0::2], gu.to(D)[:, 1::2])
+    assert rel(dgu.cpu()[:, 0::2], dg) < 4e-3
+    assert rel(dgu.cpu()[:, 1::2], du) < 4e-3
+
+
 def test_gemm_rejects_bad_arguments():
     A = torch.zeros(16, 12, device=DEV, dtype=torch.bfloat16)
     C = torch.zeros(16, 16, device=DEV, dtype=torch.bfloat16)

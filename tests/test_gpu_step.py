@@ -63,9 +63,14 @@ def test_three_step_loss_trajectory_matches_oracle():
     r = _run(s, steps=3)
     params, state = r["params0"], None
     for n in range(1, 4):
-        loss, grads, params, state = oracle.train_step(params, state, mt_inputs.step_tokens(s, n), n, cfg)
+        tok = mt_inputs.step_tokens(s, n)
+        loss, grads, params, state = oracle.train_step(params, state, tok, n, cfg)
         assert abs(r["loss"][n - 1] - loss) <= parity.LOSS_RTOL * abs(loss), (n, r["loss"][n - 1], loss)
         parity.assert_grads_close(r["g"][n - 1], grads)
+        # embedding rows of token ids absent from this step hold exactly zero
+        untouched = torch.ones(s.vocab, dtype=torch.bool)
+        untouched[tok[:, :-1].reshape(-1).long()] = False
+        assert torch.all(r["g"][n - 1]["embed"]["E"][untouched] == 0)
 
 
 def test_streamed_equals_resident_bitexact():
@@ -146,5 +151,23 @@ def test_statistics_account_for_streamed_bytes():
     # the last layer, whose weights are still resident when backward starts.
     expect_h2d = infos[0]["w_bytes"] + infos[-1]["w_bytes"] + (2 * s.n_layers - 1) * layer_w
     assert st["h2d_bytes"] == expect_h2d
-    assert st["d2h_bytes"] == sum(i["w_bytes"] for i in infos)
+    # gradients: every layer tile and the head whole; the embedding only for the
+    # token ids that occur in the step (its other rows are zero)
+    distinct = int(torch.unique(mt_inputs.step_tokens(s, 1)[:, :-1]).numel())
+    assert st["d2h_bytes"] == sum(i["w_bytes"] for i in infos[1:]) + 2 * distinct * s.d_model
     assert st["step"] == 1 and st["gemm_launches"] > 0
+
+
+def test_nonfinite_loss_skips_every_update():
+    """A non-finite loss is seen before any gradient lands: the step reports
+    MT_ENONFINITE and no weight is updated."""
+    s = SHAPES["tiny"]
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    params["head"]["wh"][3, 5] = float("inf")
+    m = hms.StreamedDecoder.from_shape(s)
+    m.load_weights(params)
+    with pytest.raises(hms.MtError) as e:
+        m.train_step(mt_inputs.step_tokens(s, 1))
+    assert e.value.code == hms._lib.MT_ENONFINITE
+    _equal_trees(m.weights(), params)
+    m.close()

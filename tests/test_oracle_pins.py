@@ -320,7 +320,7 @@ def test_model_grads_match_autograd_of_library_forward(which):
     p = _as_f64(params, requires_grad=True)
     ref = _library_model_loss(p, tokens, cfg)
     ref.backward()
-    assert abs(loss - float(ref)) < 1e-12 * abs(loss)
+    assert abs(loss - float(ref.detach())) < 1e-12 * abs(loss)
     for mine, theirs in zip(_flat(grads), _flat(p)):
         err = (mine - theirs.grad).norm() / theirs.grad.norm()
         assert err < 1e-10, err
@@ -483,3 +483,22 @@ def test_train_step_applies_adam_to_bf16_rounded_grads():
     used[tokens[:, :-1].long().reshape(-1)] = True
     E0 = params["embed"]["E"].to(D)
     assert torch.equal(new_p["embed"]["E"][~used], E0[~used])
+
+
+def test_precision_model_without_rounding_is_the_oracle_in_fp32():
+    """The storage-precision model (tests/precision_model.py) with every
+    rounding point off is the same step in FP32: its loss and gradients match
+    the FP64 oracle to FP32 accuracy, and switching all points on moves the
+    gradients by about the BF16 scale."""
+    from tests import parity, precision_model as pm
+    s = mt_inputs.PRESETS["tiny"].with_(batch=1, seq=48)
+    cfg = OracleConfig.from_shape(s)
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    tokens = mt_inputs.step_tokens(s, 1)
+    loss_ref, gref = oracle.model_loss_and_grads(params, tokens, cfg)
+    loss, g = pm.Model(()).loss_and_grads(params, tokens, cfg)
+    assert abs(loss - loss_ref) < 1e-5 * abs(loss_ref)
+    assert max(r for _, _, r in parity.grad_report(g, gref)) < 1e-4
+    _, gb = pm.Model(pm.ALL).loss_and_grads(params, tokens, cfg)
+    worst = max(r for _, _, r in parity.grad_report(gb, gref))
+    assert 1e-3 < worst < 5e-2
