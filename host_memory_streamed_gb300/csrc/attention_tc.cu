@@ -45,6 +45,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long rows, long cols, long
 namespace {
 
 constexpr int TA_BM = 128, TA_BN = 128, TA_THREADS = 320;
+constexpr int kSoftmaxWarps = 8;  // barriers the softmax warps arrive on count warps (one arrival each)
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
@@ -120,12 +121,12 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 256);
+      mbar_init(&p_full[i], kSoftmaxWarps);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(s_read, 256);
+    mbar_init(s_read, kSoftmaxWarps);
     mbar_init(o_full, 1);
-    mbar_init(l_ready, 256);
+    mbar_init(l_ready, kSoftmaxWarps);
     fence_barrier_init();
     tma_prefetch_desc(&tm_qkv);
   }
@@ -244,7 +245,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       for (int c = 0; c < TA_BN / 32; ++c)
         tmem_ld_32x32b_x32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(x + c * 32));
       tmem_wait_ld_regs(x);
-      mbar_arrive(s_read);
+      tc_fence_before();
+      mbar_arrive_warp(s_read);
       const int k0 = j * TA_BN;
       if (k0 + TA_BN - 1 > q0) {  // block touches the diagonal
 #pragma unroll
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive_warp(&p_full[j & 1]);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !mbar_wait_warp(o_full, 0)) {
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     // the two halves of each row sum meet in shared memory
     if (ok) {
       sL[hf * 128 + r] = l;
-      mbar_arrive(l_ready);
+      mbar_arrive_warp(l_ready);
       if (!mbar_wait_warp(l_ready, 0)) {
         site = 998;
         ok = false;
@@ -572,14 +574,14 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
-      mbar_init(&ld_ready[i], 256);
+      mbar_init(&ld_ready[i], kSoftmaxWarps);
     }
     mbar_init(st_full, 1);
     mbar_init(dpt_full, 1);
-    mbar_init(p_ready, 256);
-    mbar_init(ds_ready, 256);
-    mbar_init(st_read, 256);
-    mbar_init(dpt_read, 256);
+    mbar_init(p_ready, kSoftmaxWarps);
+    mbar_init(ds_ready, kSoftmaxWarps);
+    mbar_init(st_read, kSoftmaxWarps);
+    mbar_init(dpt_read, kSoftmaxWarps);
     mbar_init(acc_full, 1);
     fence_barrier_init();
     tma_prefetch_desc(&tm_qkv);
@@ -720,7 +722,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         else
           ld[128 + t] = q < S ? p.delta[idx] : 0.f;
       }
-      mbar_arrive(&ld_ready[st]);
+      mbar_arrive_warp(&ld_ready[st]);
       if (!mbar_wait_warp(&ld_ready[st], (it >> 1) & 1) || !mbar_wait_warp(st_full, ph)) {
         ok = false;
         break;
@@ -730,7 +732,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       tmem_ld_32x32b_x32(tST + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_ld_32x32b_x32(tST + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld_regs(sv);
-      mbar_arrive(st_read);
+      tc_fence_before();
+      mbar_arrive_warp(st_read);
       // Queries past the sequence end have lse = +inf (P = 0) and delta = 0;
       // only the diagonal block (q0 == k0) needs the key > query mask.
       const bool diag = q0 == k0;
@@ -759,7 +762,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       tmem_st_packed32(tST + lane_off + hf * 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive_warp(p_ready);
       // dS^T = P^T * (dP^T - delta)
       if (!mbar_wait_warp(dpt_full, ph)) {
         ok = false;
@@ -783,7 +786,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
                                   pf[c + 3] * (__uint_as_float(dp[c4 * 4 + 3]) - dv[3]));
         }
       }
-      mbar_arrive(dpt_read);
+      tc_fence_before();
+      mbar_arrive_warp(dpt_read);
       if (!mbar_wait_warp(dpt_read, ph)) {
         ok = false;
         break;
@@ -792,7 +796,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       tmem_st_packed32(tDPT + lane_off + hf * 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(ds_ready);
+      mbar_arrive_warp(ds_ready);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(acc_full, 0)) {
@@ -823,12 +827,15 @@ template <int HD>
 struct TdqCfg {
   static constexpr int BOX = 128 * 128;      // one 64-column box of 128 rows, bytes
   static constexpr int TILE = 128 * HD * 2;  // 128 rows x HD columns
-  static constexpr int KSTAGES = 2;
+  // K is read by S_j and, last, by dQ_j; V only by dP_j, which runs a whole
+  // score block earlier.  Separate rings let V_j be refilled as soon as dP_j
+  // is done, and give K a third stage.
+  static constexpr int KSTAGES = 3, VSTAGES = 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + TILE;
   static constexpr int OFF_K = OFF_DO + TILE;             // KSTAGES tiles
-  static constexpr int OFF_V = OFF_K + KSTAGES * TILE;    // KSTAGES tiles
-  static constexpr int OFF_BAR = OFF_V + KSTAGES * TILE;
+  static constexpr int OFF_V = OFF_K + KSTAGES * TILE;    // VSTAGES tiles
+  static constexpr int OFF_BAR = OFF_V + VSTAGES * TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
 
@@ -844,17 +851,20 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  constexpr int NK = C::KSTAGES, NV = C::VSTAGES;
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_empty = bar + 3;  // [2]
-  uint64_t* s_full = bar + 5;    // [2] S of block j in TMEM buffer j & 1
-  uint64_t* dp_full = bar + 7;
-  uint64_t* sd_read = bar + 8;   // every softmax thread has read its S and dP columns (256)
-  // [2] dS_j stored (256).  Two barriers: the softmax may finish block j + 1
-  // before the MMA thread starts waiting for block j (dP_{j+1} is issued first).
-  uint64_t* ds_ready = bar + 9;
-  uint64_t* acc_full = bar + 11;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 12);
+  uint64_t* k_full = bar + 1;                 // [NK]
+  uint64_t* k_empty = bar + 1 + NK;           // [NK]
+  uint64_t* v_full = bar + 1 + 2 * NK;        // [NV]
+  uint64_t* v_empty = bar + 1 + 2 * NK + NV;  // [NV]
+  uint64_t* s_full = bar + 1 + 2 * NK + 2 * NV;  // [2] S of block j in TMEM buffer j & 1
+  uint64_t* dp_full = bar + 3 + 2 * NK + 2 * NV;
+  uint64_t* sd_read = bar + 4 + 2 * NK + 2 * NV;  // every softmax warp has read its S and dP columns
+  // [2] dS_j stored.  Two barriers: the softmax may finish block j + 1 before
+  // the MMA thread starts waiting for block j (dP_{j+1} is issued first).
+  uint64_t* ds_ready = bar + 5 + 2 * NK + 2 * NV;
+  uint64_t* acc_full = bar + 7 + 2 * NK + 2 * NV;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 8 + 2 * NK + 2 * NV);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -869,15 +879,19 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     mbar_init(dp_full, 1);
-    mbar_init(sd_read, 256);
-    mbar_init(&ds_ready[0], 256);
-    mbar_init(&ds_ready[1], 256);
+    mbar_init(sd_read, kSoftmaxWarps);
+    mbar_init(&ds_ready[0], kSoftmaxWarps);
+    mbar_init(&ds_ready[1], kSoftmaxWarps);
     mbar_init(acc_full, 1);
     fence_barrier_init();
     tma_prefetch_desc(&tm_qkv);
@@ -902,54 +916,71 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         tma_load_2d(sQ + i * C::BOX, &tm_qkv, h * HD + 64 * i, row0 + q0, q_full);
         tma_load_2d(sdO + i * C::BOX, &tm_do, h * HD + 64 * i, row0 + q0, q_full);
       }
-      int pend[2] = {-1, -1};
+      int pk[NK], pv[NV];
+      for (int s = 0; s < NK; ++s) pk[s] = -1;
+      for (int s = 0; s < NV; ++s) pv[s] = -1;
       for (int j = 0; j < n_kb && !abort_flag; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&kv_empty[s], ((j >> 1) - 1) & 1)) {
+        const int sk = j % NK, sv = j % NV;
+        if (j >= NK && !mbar_wait(&k_empty[sk], ((j / NK) - 1) & 1)) {
           set_status(p.status, kStatusAttnBwdTimeout);
           abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[s], 2 * C::TILE);
+        mbar_arrive_expect_tx(&k_full[sk], C::TILE);
 #pragma unroll
-        for (int i = 0; i < HD / 64; ++i) {
-          tma_load_2d(sK + s * C::TILE + i * C::BOX, &tm_qkv, (p.Hq + kvh) * HD + 64 * i, row0 + j * 128,
-                      &kv_full[s]);
-          tma_load_2d(sV + s * C::TILE + i * C::BOX, &tm_qkv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + j * 128,
-                      &kv_full[s]);
+        for (int i = 0; i < HD / 64; ++i)
+          tma_load_2d(sK + sk * C::TILE + i * C::BOX, &tm_qkv, (p.Hq + kvh) * HD + 64 * i, row0 + j * 128,
+                      &k_full[sk]);
+        pk[sk] = (j / NK) & 1;
+        if (j >= NV && !mbar_wait(&v_empty[sv], ((j / NV) - 1) & 1)) {
+          set_status(p.status, kStatusAttnBwdTimeout);
+          abort_flag = 1;
+          break;
         }
-        pend[s] = (j >> 1) & 1;
+        mbar_arrive_expect_tx(&v_full[sv], C::TILE);
+#pragma unroll
+        for (int i = 0; i < HD / 64; ++i)
+          tma_load_2d(sV + sv * C::TILE + i * C::BOX, &tm_qkv, (p.Hq + p.Hkv + kvh) * HD + 64 * i, row0 + j * 128,
+                      &v_full[sv]);
+        pv[sv] = (j / NV) & 1;
       }
       if (!mbar_wait(q_full, 0)) set_status(p.status, kStatusAttnBwdTimeout);
-      for (int s = 0; s < 2; ++s)
-        if (pend[s] >= 0 && !mbar_wait(&kv_full[s], (uint32_t)pend[s])) set_status(p.status, kStatusAttnBwdTimeout);
+      for (int s = 0; s < NK; ++s)
+        if (pk[s] >= 0 && !mbar_wait(&k_full[s], (uint32_t)pk[s])) set_status(p.status, kStatusAttnBwdTimeout);
+      for (int s = 0; s < NV; ++s)
+        if (pv[s] >= 0 && !mbar_wait(&v_full[s], (uint32_t)pv[s])) set_status(p.status, kStatusAttnBwdTimeout);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 128);
       const uint32_t id_dq = idesc_bf16_f32(128, HD) | (1u << 16);  // dS (TMEM) x K (MN-major)
       bool ok = mbar_wait(q_full, 0);
-      auto issue_scores = [&](int j, const uint8_t* sA, const uint8_t* sB, uint32_t dst) {
-        const int ks = j & 1;
+      // scores of block j: A (Q or dO) x B-tile^T into TMEM columns dst
+      auto issue_scores = [&](const uint8_t* sA, const uint8_t* sBt, uint32_t dst) {
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const int box = kk >> 2, off = (kk & 3) * 32;
           tc_mma_bf16(dst, smem_desc_kmajor_sw128(sA + box * C::BOX + off),
-                      smem_desc_kmajor_sw128(sB + ks * C::TILE + box * C::BOX + off), id_s, kk > 0 ? 1u : 0u);
+                      smem_desc_kmajor_sw128(sBt + box * C::BOX + off), id_s, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_s = [&](int j) {
-        if (!mbar_wait(&kv_full[j & 1], (j >> 1) & 1)) return false;
+        if (!mbar_wait(&k_full[j % NK], (j / NK) & 1)) return false;
         tc_fence_after();
-        issue_scores(j, sQ, sK, tmem + 128u * (uint32_t)(j & 1));
+        issue_scores(sQ, sK + (j % NK) * C::TILE, tmem + 128u * (uint32_t)(j & 1));
         tc_commit(&s_full[j & 1]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok) {
-        issue_scores(0, sdO, sV, tDP);
+      auto issue_dp = [&](int j) {
+        if (!mbar_wait(&v_full[j % NV], (j / NV) & 1)) return false;
+        tc_fence_after();
+        issue_scores(sdO, sV + (j % NV) * C::TILE, tDP);
         tc_commit(dp_full);
-      }
+        tc_commit(&v_empty[j % NV]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < n_kb; ++j) {
         const uint32_t ph = j & 1;
         // S_{j+1} into the other buffer, whose dS_{j-1} the dQ MMAs issued before have read
@@ -962,9 +993,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           break;
         }
         tc_fence_after();
-        if (j + 1 < n_kb) {
-          issue_scores(j + 1, sdO, sV, tDP);  // dP_{j+1}: every thread has read dP_j
-          tc_commit(dp_full);
+        if (j + 1 < n_kb && !issue_dp(j + 1)) {  // dP_{j+1}: every thread has read dP_j
+          ok = false;
+          break;
         }
         if (!mbar_wait(&ds_ready[j & 1], (j >> 1) & 1)) {
           ok = false;
@@ -972,11 +1003,11 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t src = tmem + 128u * (uint32_t)(j & 1);
-        const uint64_t kd = smem_desc_mnmajor_sw128(sK + (j & 1) * C::TILE, C::BOX);
+        const uint64_t kd = smem_desc_mnmajor_sw128(sK + (j % NK) * C::TILE, C::BOX);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)
           tc_mma_bf16_ts(tdQ, src + kk * 8, kd + (uint64_t)(kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&kv_empty[j & 1]);
+        tc_commit(&k_empty[j % NK]);
       }
       if (ok) {
         tc_commit(acc_full);
@@ -1037,7 +1068,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[2 * e]) - Dr), pf[c + 1] * (__uint_as_float(dp[2 * e + 1]) - Dr));
         }
       }
-      mbar_arrive(sd_read);
+      tc_fence_before();
+      mbar_arrive_warp(sd_read);
       if (!mbar_wait_warp(sd_read, ph)) {
         ok = false;
         break;
@@ -1046,7 +1078,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       tmem_st_packed32(tS + lane_off + hf * 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ds_ready[j & 1]);
+      mbar_arrive_warp(&ds_ready[j & 1]);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(acc_full, 0)) {

@@ -86,6 +86,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// One arrival per warp on a barrier that counts warps: every lane's prior work
+// (generic shared-memory writes, completed TMEM loads/stores with their
+// tcgen05 fences) is ordered before lane 0's release-arrive by the warp barrier.
+// One shared-memory atomic per warp instead of one per thread.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
