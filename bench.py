@@ -406,7 +406,8 @@ def main():
                 "d2h_bytes_per_step": 4 + st["d2h_bytes"]},
         "gpu_launches": kernels,
         "step_breakdown_ms": {k: st[k] for k in ("step_ms", "gpu_compute_ms", "h2d_ms", "d2h_ms", "wait_weights_ms",
-                                                 "visit_gap_ms", "adam_ms", "adam_tail_ms", "gemm_ms")},
+                                                 "visit_gap_ms", "host_pre_ms", "tail_grads_ms", "tail_adam_ms",
+                                                 "tail_rest_ms", "adam_ms", "adam_tail_ms", "gemm_ms")},
         "losses": losses, "init_seconds": init_s,
     }
     line["clocks"] = clk.summary()

@@ -52,7 +52,8 @@ class MtStepStats(C.Structure):
         ("gemm_flops", C.c_double), ("gemm_launches", C.c_int64), ("kernel_launches", C.c_int64),
         ("h2d_bytes", C.c_int64), ("d2h_bytes", C.c_int64), ("flops_executed", C.c_int64),
         ("flops_model", C.c_int64), ("arena_high_water", C.c_int64), ("step", C.c_int64),
-        ("visit_gap_ms", C.c_double),
+        ("visit_gap_ms", C.c_double), ("host_pre_ms", C.c_double), ("tail_grads_ms", C.c_double),
+        ("tail_adam_ms", C.c_double), ("tail_rest_ms", C.c_double),
     ]
 
 

@@ -39,14 +39,17 @@ void adam_range(uint16_t* __restrict__ w, const uint16_t* __restrict__ g, float*
   const float bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(b1), t));
   const float bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(b2), t));
   const float lr = h.lr, eps = h.eps, wd = h.weight_decay;
+  // bias corrections as multiplications (1/(1-b^t) once per call): two fewer
+  // divisions per element; the rounding differs from dividing by < 1 FP32 ulp
+  const float ibc1 = 1.0f / bc1, ibc2 = 1.0f / bc2;
   for (size_t i = 0; i < n; ++i) {
     const float gi = bf16_bits_to_f32(g[i]);
     const float mi = b1 * m[i] + omb1 * gi;
     const float vi = b2 * v[i] + omb2 * gi * gi;
     m[i] = mi;
     v[i] = vi;
-    const float mhat = mi / bc1;
-    const float vhat = vi / bc2;
+    const float mhat = mi * ibc1;
+    const float vhat = vi * ibc2;
     const float wi = bf16_bits_to_f32(w[i]);
     const float upd = mhat / (std::sqrt(vhat) + eps) + wd * wi;
     w[i] = f32_to_bf16_bits(wi - lr * upd);

@@ -59,7 +59,7 @@ int bwd_impl(const AttnArgs& x, cudaStream_t s) {
   const long threads = rows * (HD / 8);
   attn_delta_kernel<HD><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(x.dout, x.o, x.ldo, x.batch, x.seq,
                                                                          x.n_heads, x.delta);
-  if (cudaPeekAtLastError() != cudaSuccess) return -4;
+  if (launch_result() != 0) return -4;
   return launch_attn_bwd_tc_main(x, s);
 }
 

@@ -270,13 +270,16 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       uint32_t pk[32];
       auto exp_half = [&](auto half) {
         constexpr int K0 = decltype(half)::value * 64;
+        // four partial row sums: no 64-long chain of dependent adds
+        float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(x[K0 + 2 * e]), p.sl2, nb));
           const float p1 = ex2_approx(fmaf(__uint_as_float(x[K0 + 2 * e + 1]), p.sl2, nb));
-          rs += p0 + p1;
+          r4[e & 3] += p0 + p1;
           pk[e] = pack2bf(p0, p1);
         }
+        rs = (r4[0] + r4[1]) + (r4[2] + r4[3]);
       };
       if (hf == 0)
         exp_half(std::integral_constant<int, 0>{});
@@ -390,7 +393,7 @@ int launch_tc(const AttnArgs& x, cudaStream_t s) {
   p.status = x.status;
   dim3 grid((x.seq + TA_BM - 1) / TA_BM, x.batch * x.n_heads);
   attn_fwd_tc_kernel<HD><<<grid, TA_THREADS, C::SMEM, s>>>(tm, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  return launch_result();
 }
 
 }  // namespace
@@ -1139,7 +1142,7 @@ int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
   attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_qkv, tm_do, p);
   dim3 g2((x.seq + 127) / 128, x.batch * x.n_heads);
   attn_bwd_dq_tc_kernel<HD><<<g2, TB_THREADS, Bq::SMEM, s>>>(tm_qkv, tm_do, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  return launch_result();
 }
 
 }  // namespace

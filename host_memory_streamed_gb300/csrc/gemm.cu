@@ -485,6 +485,19 @@ int num_sms() {
 
 }  // namespace
 
+namespace {
+thread_local const char* g_launch_err = "no error";
+}
+
+int launch_result() {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return 0;
+  g_launch_err = cudaGetErrorString(e);
+  return -4;
+}
+
+const char* last_launch_error() { return g_launch_err; }
+
 bool make_tmap_bf16(CUtensorMap* m, const void* base, long rows, long cols, long ld, int box_rows) {
   return make_tmap(m, base, rows, cols, ld, box_rows);
 }
@@ -571,7 +584,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     gemm_bf16_tcgen05_kernel<false, true><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
   else
     gemm_bf16_tcgen05_kernel<true, true><<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  return launch_result();
 }
 
 }  // namespace mt

@@ -55,6 +55,11 @@ struct GemmArgs {
   int* status = nullptr;
 };
 
+// 0 when the launches just issued succeeded; otherwise -4, keeping the CUDA
+// error's text for last_launch_error() (thread-local).
+int launch_result();
+const char* last_launch_error();
+
 // Returns a message when the arguments are unsupported, else nullptr.
 const char* gemm_check(const GemmArgs& g);
 // 0 on success; negative on a launch or descriptor error.

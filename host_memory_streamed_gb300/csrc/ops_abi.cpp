@@ -18,7 +18,7 @@ int op_fail(const char* msg) {
 }
 int op_cuda(int rc, const char* what) {
   if (rc == 0) return MT_OK;
-  g_op_error = std::string(what) + ": launch failed (" + cudaGetErrorString(cudaGetLastError()) + ")";
+  g_op_error = std::string(what) + ": launch failed (" + (rc == -4 ? mt::last_launch_error() : "bad descriptor or attributes") + ")";
   return MT_ECUDA;
 }
 }  // namespace

@@ -625,8 +625,8 @@ void submit_untouched_embed(mt_model* m) {
 }
 
 // One slab of the compact embedding gradient: rows u0 .. u0 + nrows of the
-// step's token ids.  Scatter each row into the tile's G section, check it is
-// finite, and update the row (Adam) in the same task.
+// step's token ids.  Scatter each row into the tile's G section and check it
+// is finite (accumulator pool); the rows' Adam then goes to the Adam pool.
 void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<bool>& fin) {
   const TileLayout& lay = m->layouts[j.tile];
   const TensorSlot& E = lay.slot("E");
@@ -636,26 +636,40 @@ void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<b
   const int32_t* rows = m->pinned_tok + 3 * m->D.T + m->D.V + 1;  // emb_rows
   uint8_t* base = m->tiles[j.tile];
   const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
-  const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
   const int nt = m->acc_pool->size();
   const int64_t per = std::max<int64_t>(16, (nrows + nt - 1) / nt);
   for (int64_t a = 0; a < nrows; a += per) {
     const int64_t b = std::min(nrows, a + per);
     m->acc_pool->submit([=, &fin] {
       for (int64_t k = a; k < b; ++k) {
+        uint16_t* g = reinterpret_cast<uint16_t*>(base + lay.off_g + E.offset) + (int64_t)rows[u0 + k] * d;
+        if (!copy_grad_check_finite(g, src + k * d, (size_t)d)) fin = false;
+      }
+    });
+  }
+}
+
+// Adam on the embedding rows rows[u0 .. u0 + nrows) whose gradients just landed.
+void submit_adam_embed_rows(mt_model* m, int tile, int64_t u0, int64_t nrows) {
+  const TileLayout& lay = m->layouts[tile];
+  const TensorSlot& E = lay.slot("E");
+  const int d = m->D.d;
+  const int32_t* rows = m->pinned_tok + 3 * m->D.T + m->D.V + 1;
+  uint8_t* base = m->tiles[tile];
+  const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
+  const int64_t per = std::max<int64_t>(8, (1 << 18) / d);
+  for (int64_t a = 0; a < nrows; a += per) {
+    const int64_t b = std::min(nrows, a + per);
+    m->adam_pool->submit([=] {
+      const auto t0 = Clock::now();
+      for (int64_t k = a; k < b; ++k) {
         const int64_t e = (int64_t)rows[u0 + k] * d;
-        uint16_t* g = reinterpret_cast<uint16_t*>(base + lay.off_g + E.offset) + e;
-        if (!copy_grad_check_finite(g, src + k * d, (size_t)d)) {
-          fin = false;
-          m->nonfinite = true;
-        }
-        if (m->nonfinite) continue;
-        const auto t0 = Clock::now();
-        adam_range(reinterpret_cast<uint16_t*>(base + lay.off_w + E.offset) + e, g,
+        adam_range(reinterpret_cast<uint16_t*>(base + lay.off_w + E.offset) + e,
+                   reinterpret_cast<const uint16_t*>(base + lay.off_g + E.offset) + e,
                    reinterpret_cast<float*>(base + lay.off_m + 2 * E.offset) + e,
                    reinterpret_cast<float*>(base + lay.off_v + 2 * E.offset) + e, (size_t)d, h);
-        m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
       }
+      m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
     });
   }
 }
@@ -682,6 +696,7 @@ void accum_main(mt_model* m) {
         accumulate_embed_rows(m, j, fin);
         if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
         if (!fin) m->nonfinite = true;
+        if (!m->nonfinite) submit_adam_embed_rows(m, j.tile, j.off / (2LL * m->D.d), j.bytes / (2LL * m->D.d));
         {
           std::lock_guard<std::mutex> g(m->mu);
           m->free_slabs.push_back(j.slab);
@@ -843,6 +858,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
         MT_CK(cudaMemcpyAsync(m->resident + m->resident_off[t], m->tiles[t] + m->layouts[t].off_w,
                               (size_t)m->layouts[t].w_bytes, cudaMemcpyHostToDevice, m->s_comp));
     MT_CK(cudaEventRecord(m->ev_t0, m->s_comp));
+    const auto t_ev0 = Clock::now();
     {
       std::lock_guard<std::mutex> g(m->mu);
       m->step_gen += 1;
@@ -938,7 +954,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
           rc = tmpl.embed_bwd_rows(dx_cur, reinterpret_cast<bf16*>(gb), m->emb_u);
           break;
       }
-      if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(cudaGetLastError())};
+      if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + last_launch_error()};
       MT_CK(cudaPeekAtLastError());
       MT_CK(cudaEventRecord(m->ev_vis_b[v], m->s_comp));
       if (x.buf >= 0 && !m->resident_mode) {
@@ -976,6 +992,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     MT_CK(cudaMemcpyAsync(m->pinned_scalars + 1, m->ws.status, sizeof(int), cudaMemcpyDeviceToHost, m->s_comp));
     wait_event(m, m->ev_t1, "compute stream");
     MT_CK(cudaStreamSynchronize(m->s_comp));
+    const auto t_compute_done = Clock::now();
     const int status = *reinterpret_cast<int*>(m->pinned_scalars + 1);
     // drain the gradient path and Adam
     wait_flag(m, m->rec_d2h, m->last_grad_visit, "last gradient evacuation");
@@ -986,6 +1003,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       if (m->abort_flag) throw MtError{m->worker_code ? m->worker_code.load() : MT_EINTERNAL, m->worker_msg};
       if (!ok) throw MtError{MT_ETIMEDOUT, "timed out waiting for gradient accumulation"};
     }
+    const auto t_grads_done = Clock::now();
     if (!m->adam_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "timed out waiting for Adam"};
     const auto adam_end = Clock::now();
     check_abort(m);
@@ -1045,6 +1063,13 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     m->step += 1;
     st.step = m->step;
     st.step_ms = ms_since(wall0);
+    auto span = [](Clock::time_point a, Clock::time_point b) {
+      return std::chrono::duration<double, std::milli>(b - a).count();
+    };
+    st.host_pre_ms = span(wall0, t_ev0);
+    st.tail_grads_ms = span(t_compute_done, t_grads_done);
+    st.tail_adam_ms = span(t_grads_done, adam_end);
+    st.tail_rest_ms = span(adam_end, Clock::now());
     if (loss_out) *loss_out = m->pinned_scalars[0];
     if (m->nonfinite) {
       m->err = "non-finite loss or gradient; Adam skipped from the first affected tile on";
@@ -1088,7 +1113,7 @@ const char* validate(const mt_config& c) {
 mt_config with_defaults(const mt_config& in) {
   mt_config c = in;
   if (c.n_adam_threads <= 0) c.n_adam_threads = std::max(1u, std::thread::hardware_concurrency());
-  if (c.n_pack_threads <= 0) c.n_pack_threads = 4;
+  if (c.n_pack_threads <= 0) c.n_pack_threads = 8;
   if (c.n_grad_slabs <= 0) c.n_grad_slabs = 12;
   if (c.grad_slab_bytes <= 0) c.grad_slab_bytes = 64ll << 20;
   if (c.stage_bytes <= 0) c.stage_bytes = 64ll << 20;
@@ -1497,7 +1522,7 @@ int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, 
       rc |= tmpl.backward(bind_layer(lay, wb), a, reinterpret_cast<const bf16*>(dx_out), dxi,
                           bind_layer(lay, m->gbuf[0]));
     }
-    if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + cudaGetErrorString(cudaGetLastError())};
+    if (rc != 0) throw MtError{MT_ECUDA, std::string("kernel launch failed: ") + last_launch_error()};
     // bounded wait for the kernels, then plain copies of the results
     MT_CK(cudaEventRecord(m->ev_t1, m->s_comp));
     wait_event(m, m->ev_t1, "layer pass");

@@ -94,7 +94,7 @@ typedef struct {
   int32_t ckpt_every;        /* K: keep the input of every K-th layer; recompute inside blocks of K */
   float lr, beta1, beta2, adam_eps, weight_decay;
   int32_t n_adam_threads;    /* CPU Adam workers (0 = hardware threads) */
-  int32_t n_pack_threads;    /* CPU threads copying pageable tiles into pinned staging (0 = 4) */
+  int32_t n_pack_threads;    /* CPU threads copying pageable tiles into pinned staging (0 = 8) */
   int32_t n_grad_slabs;      /* pinned gradient slabs (0 = 12) */
   int64_t grad_slab_bytes;   /* bytes per gradient slab (0 = 64 MiB) */
   int64_t stage_bytes;       /* bytes per pinned H2D staging chunk (0 = 64 MiB); two chunks ping-pong */
@@ -140,6 +140,10 @@ typedef struct {
   int64_t step;            /* Adam step counter after this step */
   double visit_gap_ms;     /* compute-stream time between the end of one visit's kernels and the start of
                               the next one's: stream waits plus idle time while the host was behind */
+  double host_pre_ms;      /* host wall time from the call to the first compute-stream event */
+  double tail_grads_ms;    /* from the compute stream's end to the last gradient landing in its tile */
+  double tail_adam_ms;     /* from there to the end of the last Adam task */
+  double tail_rest_ms;     /* from there to the return (stream drains, statistics) */
 } mt_step_stats;
 
 /* Device bytes the handle needs in its arena for this config (>0), or a negative MT_E* code. */
