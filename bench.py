@@ -58,6 +58,26 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def gemm_traffic_per_launch():
+    """DRAM bytes per GEMM launch of the 14B step from the committed ncu summary
+    (profiles/gemm_dram_14b_step.md), or None when gemm.cu has changed since
+    the counters were taken (the summary records the source's SHA-256)."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "gemm_dram_14b_step.md")
+    src = os.path.join(ROOT, "host_memory_streamed_gb300", "csrc", "gemm.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    fields = {}
+    for line in open(prof):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if fields.get("gemm.cu sha256") != digest or "traffic bytes per launch" not in fields:
+        return None
+    return float(fields["traffic bytes per launch"])
+
+
 def mem_available_bytes():
     try:
         with open("/proc/meminfo") as f:
@@ -271,6 +291,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="14b", choices=sorted(mt_inputs.PRESETS))
     ap.add_argument("--layers", type=int, default=0, help="override the depth (0 = preset, truncated to host RAM)")
+    ap.add_argument("--mlp-chunk-rows", type=int, default=-1,
+                    help="MLP row chunk (0 = whole step; default: chunk only when the device arena would not fit)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -303,8 +325,12 @@ def main():
     peaks, peak_kind = measured_peaks()
     h2d_bw, d2h_bw = link_bandwidth(device)
 
+    chunk = args.mlp_chunk_rows
+    if chunk < 0:
+        free, _ = torch.cuda.mem_get_info(device)
+        chunk = 0 if hms.StreamedDecoder.required_device_bytes(s) < 0.9 * free else 65536
     t_init = time.perf_counter()
-    model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device)
+    model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device, mlp_chunk_rows=chunk)
     load_synthetic_weights(model, s, device)
     init_s = time.perf_counter() - t_init
     toks = token_batches(s, args.warmup + args.steps, device)
@@ -337,6 +363,9 @@ def main():
     tokens_per_step = s.batch * s.seq
     value = world * args.steps * tokens_per_step / elapsed
 
+    free_b, total_b = torch.cuda.mem_get_info(device)
+    dev_mem = {"arena_bytes": model.arena_bytes, "device_used_bytes": total_b - free_b,
+               "torch_max_allocated_bytes": torch.cuda.max_memory_allocated(device)}
     # ---- e2e: host tokens through the C-ABI, loss read on the host
     torch.cuda.synchronize(device)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -380,6 +409,7 @@ def main():
                    "batch": s.batch, "seq": s.seq, "ckpt_every": s.ckpt_every,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (weights streamed per layer, activations > 129 MB)",
+                   "mlp_chunk_rows": chunk or None,
                    "truncated": s.n_layers < full_layers,
                    "truncation_reason": ("host RAM: tiles of all layers do not fit" if s.n_layers < full_layers
                                          and not args.layers else None)},
@@ -398,7 +428,8 @@ def main():
                     "method": "CUDA events: copy windows on the H2D/D2H streams vs compute-stream waits"},
         "roofline": {"bound": "tensor", "kernel": "gemm_bf16_tcgen05", "achieved": achieved, "peak": p_sust,
                      "unit": "TFLOP/s", "frac": (achieved / p_sust) if achieved else None,
-                     "traffic": None, "peak_kind": f"bf16_tflops_sustained ({peak_kind}) -- timed inside a long step",
+                     "traffic": gemm_traffic_per_launch() if s.name == "14b" else None,
+                     "peak_kind": f"bf16_tflops_sustained ({peak_kind}) -- timed inside a long step",
                      "launches": gemm_launches, "flops_per_launch": gemm_flops / max(1, gemm_launches),
                      "ms_per_launch": gemm_ms / max(1, gemm_launches)},
         "e2e": {"value": e2e, "unit": "tokens/s",
@@ -409,6 +440,7 @@ def main():
                                                  "visit_gap_ms", "host_pre_ms", "tail_grads_ms", "tail_adam_ms",
                                                  "tail_rest_ms", "adam_ms", "adam_tail_ms", "gemm_ms")},
         "losses": losses, "init_seconds": init_s,
+        "device_memory": dev_mem,
     }
     line["clocks"] = clk.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -38,7 +38,7 @@ class StreamedDecoder:
     def __init__(self, n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, batch, seq, *,
                  ckpt_every=1, rms_eps=1e-5, rope_theta=1e4, lr=1e-4, beta1=0.9, beta2=0.95, adam_eps=1e-8,
                  weight_decay=0.0, n_adam_threads=0, n_pack_threads=0, n_grad_slabs=0, grad_slab_bytes=0,
-                 stage_bytes=0, timeout_ms=0, flags=0, device=None):
+                 stage_bytes=0, timeout_ms=0, flags=0, mlp_chunk_rows=0, device=None):
         if not torch.cuda.is_available():
             raise RuntimeError("a CUDA device is required (the library has no CPU path)")
         self._L = _lib.lib()
@@ -49,7 +49,7 @@ class StreamedDecoder:
                          adam_eps=adam_eps, weight_decay=weight_decay, n_adam_threads=n_adam_threads,
                          n_pack_threads=n_pack_threads, n_grad_slabs=n_grad_slabs,
                          grad_slab_bytes=grad_slab_bytes, stage_bytes=stage_bytes, timeout_ms=timeout_ms,
-                         flags=flags).items():
+                         flags=flags, mlp_chunk_rows=mlp_chunk_rows).items():
             setattr(cfg, k, v)
         self.cfg = cfg
         self.device = torch.device(device or "cuda")
@@ -67,6 +67,20 @@ class StreamedDecoder:
         self._h = h
         self.n_tiles = self._L.mt_tile_count(h)
         self.infos = [self.tile_info(i) for i in range(self.n_tiles)]
+
+    @staticmethod
+    def required_device_bytes(s, **kw) -> int:
+        """Device arena bytes a model of shape ``s`` (and the given options) needs."""
+        cfg = _lib.MtConfig()
+        for k in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "batch", "seq",
+                  "ckpt_every", "rms_eps", "rope_theta", "lr", "beta1", "beta2", "adam_eps", "weight_decay"):
+            setattr(cfg, k, getattr(s, k))
+        for k, v in kw.items():
+            setattr(cfg, k, v)
+        need = _lib.lib().mt_required_device_bytes(C.byref(cfg))
+        if need < 0:
+            raise MtError(need, _lib.lib().mt_last_error(None).decode())
+        return int(need)
 
     @classmethod
     def from_shape(cls, s, **kw):
@@ -200,6 +214,16 @@ class StreamedDecoder:
         else:
             rc = self._L.mt_train_step(self._h, tok.data_ptr(), tok.numel(), C.byref(loss))
         self._check(rc)
+        return loss.value
+
+    def train_step_micro(self, tokens: torch.Tensor) -> float:
+        """tokens: int32 [n_micro, B, S+1] on the host; one step with gradient
+        accumulation over the n_micro micro-batches.  Returns the mean loss."""
+        tok = tokens.to(torch.int32).contiguous()
+        if tok.dim() != 3 or tok.is_cuda:
+            raise TypeError("tokens must be a host tensor [n_micro, batch, seq + 1]")
+        loss = C.c_float()
+        self._check(self._L.mt_train_step_micro(self._h, tok.data_ptr(), tok.numel(), tok.shape[0], C.byref(loss)))
         return loss.value
 
     def layer_pass(self, layer, x_in, dx_out=None, x_out=None, dx_in=None):

@@ -30,7 +30,7 @@ class MtConfig(C.Structure):
         ("weight_decay", C.c_float),
         ("n_adam_threads", C.c_int32), ("n_pack_threads", C.c_int32), ("n_grad_slabs", C.c_int32),
         ("grad_slab_bytes", C.c_int64), ("stage_bytes", C.c_int64), ("timeout_ms", C.c_int64),
-        ("flags", C.c_uint32),
+        ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64),
     ]
 
 
@@ -79,6 +79,7 @@ def lib():
         "mt_train_step": (C.c_int, [vp, vp, sz, fp]),
         "mt_train_step_device_tokens": (C.c_int, [vp, vp, sz, fp]),
         "mt_layer_pass": (C.c_int, [vp, i32, vp, vp, vp, vp]),
+        "mt_train_step_micro": (C.c_int, [vp, vp, sz, i32, fp]),
         "mt_get_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
         "mt_get_step_stats": (C.c_int, [vp, C.POINTER(MtStepStats)]),
         "mt_get_step": (i64, [vp]),

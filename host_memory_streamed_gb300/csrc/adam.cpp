@@ -68,6 +68,18 @@ bool copy_grad_check_finite(uint16_t* __restrict__ dst, const uint16_t* __restri
   return bad == 0;
 }
 
+// dst += src (BF16 gradients of another micro-batch): the sum in FP32, rounded
+// to nearest even; reports whether src holds a NaN or Inf.
+bool add_grad_check_finite(uint16_t* __restrict__ dst, const uint16_t* __restrict__ src, size_t n) {
+  uint32_t bad = 0;
+  for (size_t i = 0; i < n; ++i) {
+    const uint16_t b = src[i];
+    bad |= static_cast<uint32_t>((b & 0x7F80u) == 0x7F80u);
+    dst[i] = f32_to_bf16_bits(bf16_bits_to_f32(dst[i]) + bf16_bits_to_f32(b));
+  }
+  return bad == 0;
+}
+
 }  // namespace mt
 
 extern "C" int mt_adam_host(uint16_t* w, const uint16_t* g, float* m, float* v, size_t n, int64_t t, float lr,

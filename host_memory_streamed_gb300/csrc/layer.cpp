@@ -9,6 +9,7 @@
 // weight pointers; a Bind primitive maps views of the streaming buffer into
 // the template's input slots).  Because the host tile layout equals the
 // device view layout, Bind needs no gather kernel.
+#include <algorithm>
 #include <cstring>
 #include <stdexcept>
 
@@ -34,6 +35,7 @@ Dims dims_of(const mt_config& c) {
   d.B = c.batch;
   d.S = c.seq;
   d.T = (long)c.batch * c.seq;
+  d.Tc = (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < d.T) ? (long)c.mlp_chunk_rows : d.T;
   d.Dq = c.n_heads * c.head_dim;
   d.Dqkv = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   return d;
@@ -166,6 +168,24 @@ int LayerTemplate::forward(const LayerView& w, LayerActs& a, bf16* x_out, bool k
   rc |= gemm(g);
   launch_rmsnorm_fwd(a.h, w.g2, a.n2, a.rstd2, T, D.d, eps, s);
   trace("rmsnorm_fwd");
+  if (D.Tc < T) {
+    // chunked MLP: the gate/up activations of one row chunk at a time.  An
+    // internals-only pass (for backward) stops here: backward recomputes the
+    // MLP chunk by chunk.
+    if (x_out) {
+      for (long c0 = 0; c0 < T; c0 += D.Tc) {
+        const int rows = (int)std::min(D.Tc, T - c0);
+        g = mk(a.n2 + c0 * D.d, D.d, w.wgu, D.d, rows, 2 * D.f, D.d, kEpiSwiGLU, a.a, D.f, ws->status);
+        rc |= gemm(g);
+        g = mk(a.a, D.f, w.wd, D.f, rows, D.d, D.f, kEpiResidualBf16, x_out + c0 * D.d, D.d, ws->status);
+        g.R = a.h + c0 * D.d;
+        g.ldr = D.d;
+        rc |= gemm(g);
+      }
+    }
+    stats->kernels += 3;
+    return rc;
+  }
   // a = silu(n2 Wg^T) * (n2 Wu^T) from interleaved gate/up rows
   g = mk(a.n2, D.d, w.wgu, D.d, (int)T, 2 * D.f, D.d, kEpiSwiGLU, a.a, D.f, ws->status);
   if (keep_gu) {
@@ -205,6 +225,9 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
     rc |= gemm(g);
   };
 
+  if (D.Tc < T) {
+    rc |= mlp_backward_chunked(w, a, dx_out, gv);
+  } else {
   // x_out = h + a Wd^T
   wgrad(dx_out, D.d, a.a, D.f, gv.wd);
   // da = dx_out Wd (Wd read MN-major), and in the same epilogue the SwiGLU
@@ -218,6 +241,7 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   }
   wgrad(W.dgu, 2 * D.f, a.n2, D.d, gv.wgu);
   dgrad(W.dgu, 2 * D.f, w.wgu, D.d, W.dn);
+  }
   // dh = dx_out + RMSNorm2^T dn2 ; dg2
   launch_rmsnorm_bwd(W.dn, a.h, w.g2, a.rstd2, dx_out, W.dh, W.dg_partial, T, D.d, s);
   trace("rmsnorm_bwd");
@@ -253,6 +277,53 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   return rc;
 }
 
+// MLP backward over row chunks (long sequences): per chunk, recompute the
+// gate/up GEMM (the forward kept no [T, 2 ffn] activations), then
+//   dW_d  += dx_out^T a          (FP32, accumulated across chunks)
+//   dgu    = SwiGLU'(dx_out W_d)  (fused into the GEMM epilogue)
+//   dW_gu += dgu^T n2             (FP32)
+//   dn2    = dgu W_gu
+// and finally the two FP32 gradients are rounded into the BF16 tile.
+int LayerTemplate::mlp_backward_chunked(const LayerView& w, const LayerActs& a, const bf16* dx_out,
+                                        const LayerView& gv) const {
+  const Dims& D = dm;
+  const long T = D.T;
+  const Workspace& W = *ws;
+  int rc = 0;
+  for (long c0 = 0; c0 < T; c0 += D.Tc) {
+    const int rows = (int)std::min(D.Tc, T - c0);
+    const int acc = c0 == 0 ? kEpiF32 : kEpiF32Accumulate;
+    const bf16* n2 = a.n2 + c0 * D.d;
+    const bf16* dy = dx_out + c0 * D.d;
+    GemmArgs g = mk(n2, D.d, w.wgu, D.d, rows, 2 * D.f, D.d, kEpiSwiGLU, a.a, D.f, W.status);
+    g.C2 = a.gu;
+    g.ldc2 = 2L * D.f;
+    rc |= gemm(g);
+    g = mk(dy, D.d, a.a, D.f, D.d, D.f, rows, acc, W.dwd_f32, D.f, W.status);
+    g.a_mn = true;
+    g.b_mn = true;
+    rc |= gemm(g);
+    g = mk(dy, D.d, w.wd, D.f, rows, D.f, D.d, kEpiSwiGLUBwd, W.dgu, 2L * D.f, W.status);
+    g.b_mn = true;
+    g.R = a.gu;
+    g.ldr = 2L * D.f;
+    rc |= gemm(g);
+    g = mk(W.dgu, 2L * D.f, n2, D.d, 2 * D.f, D.d, rows, acc, W.dwgu_f32, D.d, W.status);
+    g.a_mn = true;
+    g.b_mn = true;
+    rc |= gemm(g);
+    g = mk(W.dgu, 2L * D.f, w.wgu, D.d, rows, D.d, 2 * D.f, kEpiStoreBf16, W.dn + c0 * D.d, D.d, W.status);
+    g.b_mn = true;
+    rc |= gemm(g);
+  }
+  launch_f32_to_bf16(W.dwd_f32, gv.wd, (long)D.d * D.f, s);
+  trace("f32_to_bf16");
+  launch_f32_to_bf16(W.dwgu_f32, gv.wgu, 2L * D.f * D.d, s);
+  trace("f32_to_bf16");
+  stats->kernels += 2;
+  return rc;
+}
+
 int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const HeadView& gv) const {
   const Dims& D = dm;
   const long T = D.T;
@@ -261,7 +332,7 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
   launch_rmsnorm_fwd(x_L, w.gf, W.nf, W.rstd_f, T, D.d, eps, s);
   launch_zero(W.dwh_f32, sizeof(float) * (size_t)D.V * D.d, s);
   stats->kernels += 1;
-  const float inv_n = 1.0f / (float)T;
+  const float inv_n = loss_scale / (float)T;
   for (long r0 = 0; r0 < T; r0 += W.head_chunk) {
     const long rows = (T - r0) < W.head_chunk ? (T - r0) : W.head_chunk;
     const bf16* nf = W.nf + r0 * D.d;

@@ -205,8 +205,8 @@ ActsSizes acts_sizes(const Dims& D) {
   s.lse = align_up((int64_t)D.B * D.Hq * D.S * 4, 256);
   s.h = s.x;
   s.n2 = s.x;
-  s.gu = align_up(D.T * 2L * D.f * 2, 256);
-  s.a = align_up(D.T * (int64_t)D.f * 2, 256);
+  s.gu = align_up(D.Tc * 2L * D.f * 2, 256);  // one MLP row chunk (the whole step when unchunked)
+  s.a = align_up(D.Tc * (int64_t)D.f * 2, 256);
   s.total = s.n1 + 2 * s.rstd + s.qkv + s.o + s.lse + s.h + s.n2 + s.gu + s.a;
   return s;
 }
@@ -254,12 +254,15 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.dx_a = reinterpret_cast<bf16*>(at(td));
   w.dx_b = reinterpret_cast<bf16*>(at(td));
   w.dh = reinterpret_cast<bf16*>(at(td));
-  w.dgu = reinterpret_cast<bf16*>(at(T * 2L * D.f * 2));
+  w.dgu = reinterpret_cast<bf16*>(at(D.Tc * 2L * D.f * 2));
   w.dn = reinterpret_cast<bf16*>(at(td));
   w.dout = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dq * 2));
   w.dqkv = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dqkv * 2));
   w.delta = reinterpret_cast<float*>(at((int64_t)D.B * D.Hq * D.S * 4));
   w.dg_partial = reinterpret_cast<float*>(at(((T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock) * (int64_t)D.d * 4));
+  const bool chunked = D.Tc < T;
+  w.dwd_f32 = chunked ? reinterpret_cast<float*>(at((int64_t)D.d * D.f * 4)) : nullptr;
+  w.dwgu_f32 = chunked ? reinterpret_cast<float*>(at(2LL * D.f * D.d * 4)) : nullptr;
   w.nf = reinterpret_cast<bf16*>(at(td));
   w.rstd_f = reinterpret_cast<float*>(at(T * 4));
   w.z = reinterpret_cast<float*>(at(hc * (int64_t)D.V * 4));
@@ -324,6 +327,10 @@ struct mt_model {
   float* pinned_scalars = nullptr;  // [0] loss, [1] status bits
   int32_t* pinned_tok = nullptr;    // inp | tgt | emb_off | emb_pos | emb_rows
   int emb_u = 0;                    // number of distinct token ids of the step (rows of the compact dE)
+  // micro-batches of the current step: pass micro_index of micro_count; gradients
+  // of later passes add into the tile's G, Adam runs on the last pass only
+  int micro_index = 0, micro_count = 1;
+  bool last_pass() const { return micro_index + 1 == micro_count; }
 
   // schedule + events
   std::vector<mt::Visit> visits;
@@ -598,6 +605,8 @@ void submit_adam_range(mt_model* m, int tile, int64_t g_off, int64_t g_bytes) {
 // W was streamed for the forward before the head ran and the backward does
 // not read it, so these rows may be updated mid-step.
 void submit_untouched_embed(mt_model* m) {
+  if (m->micro_index > 0) return;  // later micro-batches add into the rows the first one set
+  const bool update = m->micro_count == 1;  // with micro-batches, one dense embedding update at the end
   const TileLayout& lay = m->layouts[0];
   const TensorSlot& E = lay.slot("E");
   const int d = m->D.d, V = m->D.V;
@@ -614,7 +623,7 @@ void submit_untouched_embed(mt_model* m) {
         const int64_t e = (int64_t)v * d;
         uint16_t* g = reinterpret_cast<uint16_t*>(base + lay.off_g + E.offset) + e;
         std::memset(g, 0, sizeof(uint16_t) * d);
-        if (m->nonfinite) continue;
+        if (!update || m->nonfinite) continue;
         adam_range(reinterpret_cast<uint16_t*>(base + lay.off_w + E.offset) + e, g,
                    reinterpret_cast<float*>(base + lay.off_m + 2 * E.offset) + e,
                    reinterpret_cast<float*>(base + lay.off_v + 2 * E.offset) + e, (size_t)d, h);
@@ -636,6 +645,7 @@ void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<b
   const int32_t* rows = m->pinned_tok + 3 * m->D.T + m->D.V + 1;  // emb_rows
   uint8_t* base = m->tiles[j.tile];
   const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
+  const bool add = m->micro_index > 0;
   const int nt = m->acc_pool->size();
   const int64_t per = std::max<int64_t>(16, (nrows + nt - 1) / nt);
   for (int64_t a = 0; a < nrows; a += per) {
@@ -643,7 +653,9 @@ void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<b
     m->acc_pool->submit([=, &fin] {
       for (int64_t k = a; k < b; ++k) {
         uint16_t* g = reinterpret_cast<uint16_t*>(base + lay.off_g + E.offset) + (int64_t)rows[u0 + k] * d;
-        if (!copy_grad_check_finite(g, src + k * d, (size_t)d)) fin = false;
+        const bool okr = add ? add_grad_check_finite(g, src + k * d, (size_t)d)
+                             : copy_grad_check_finite(g, src + k * d, (size_t)d);
+        if (!okr) fin = false;
       }
     });
   }
@@ -696,7 +708,14 @@ void accum_main(mt_model* m) {
         accumulate_embed_rows(m, j, fin);
         if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
         if (!fin) m->nonfinite = true;
-        if (!m->nonfinite) submit_adam_embed_rows(m, j.tile, j.off / (2LL * m->D.d), j.bytes / (2LL * m->D.d));
+        if (!m->nonfinite && m->last_pass()) {
+          if (m->micro_count == 1) {
+            submit_adam_embed_rows(m, j.tile, j.off / (2LL * m->D.d), j.bytes / (2LL * m->D.d));
+          } else if (j.last) {  // every row may have been touched by some micro-batch: one dense update
+            const TensorSlot& E = m->layouts[j.tile].slot("E");
+            submit_adam_range(m, j.tile, E.offset, 2 * E.numel);
+          }
+        }
         {
           std::lock_guard<std::mutex> g(m->mu);
           m->free_slabs.push_back(j.slab);
@@ -714,12 +733,15 @@ void accum_main(mt_model* m) {
       // the copy (and NaN/Inf scan) of one slab is split over the accumulator pool
       const int64_t n = j.bytes / 2;
       const int nt = m->acc_pool->size();
+      const bool add = m->micro_index > 0;
       const int64_t piece = std::max<int64_t>(1 << 18, align_up((n + nt - 1) / nt, 2048));
       std::atomic<bool> fin{true};
       for (int64_t b = 0; b < n; b += piece) {
         const int64_t c = std::min(piece, n - b);
         m->acc_pool->submit([=, &fin] {
-          if (!copy_grad_check_finite(dst + b, src + b, (size_t)c)) fin = false;
+          const bool okc = add ? add_grad_check_finite(dst + b, src + b, (size_t)c)
+                               : copy_grad_check_finite(dst + b, src + b, (size_t)c);
+          if (!okc) fin = false;
         });
       }
       if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
@@ -729,7 +751,7 @@ void accum_main(mt_model* m) {
         m->free_slabs.push_back(j.slab);
       }
       m->cv.notify_all();
-      if (!m->nonfinite) submit_adam_range(m, j.tile, j.off, j.bytes);
+      if (!m->nonfinite && m->last_pass()) submit_adam_range(m, j.tile, j.off, j.bytes);
       if (j.last) {
         {
           std::lock_guard<std::mutex> g(m->mu);
@@ -842,7 +864,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       m->d2h_q.clear();
       m->acc_q.clear();
     }
-    m->nonfinite = false;
+    if (m->micro_index == 0) m->nonfinite = false;
     m->adam_us = 0;
     m->ls = LaunchStats{};
     m->ls.time_gemms = m->time_kernels;
@@ -866,6 +888,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     m->cv.notify_all();
 
     LayerTemplate tmpl{D, m->cfg.rms_eps, m->s_comp, &m->ws, &m->ls};
+    tmpl.loss_scale = 1.0f / (float)m->micro_count;  // the loss is the mean over every micro-batch's tokens
     if (m->trace) {
       tmpl.trace_ctx = m;
       tmpl.trace_fn = [](void* ctx, const char* kernel) {
@@ -1060,7 +1083,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
         throw MtError{MT_EINVAL, "device status " + std::to_string(status) + " (index out of range)"};
       }
     }
-    m->step += 1;
+    if (m->last_pass()) m->step += 1;
     st.step = m->step;
     st.step_ms = ms_since(wall0);
     auto span = [](Clock::time_point a, Clock::time_point b) {
@@ -1102,6 +1125,9 @@ const char* validate(const mt_config& c) {
   if (c.d_model % 8 || c.ffn % 8 || c.vocab % 8) return "d_model, ffn and vocab must be multiples of 8";
   if (((int64_t)c.batch * c.seq) % 8) return "batch * seq must be a multiple of 8";
   if (c.ckpt_every < 1) return "ckpt_every must be >= 1";
+  if (c.mlp_chunk_rows < 0 || c.mlp_chunk_rows % 128) return "mlp_chunk_rows must be a multiple of 128 (0 = unchunked)";
+  if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq && (c.flags & MT_STORE_ACTS))
+    return "a chunked MLP keeps no per-layer gate/up activations: not combinable with MT_STORE_ACTS";
   if (c.grad_slab_bytes > 0 && align_up(c.grad_slab_bytes, kPage) < 2LL * c.d_model)
     return "grad_slab_bytes must hold one embedding row (2 * d_model bytes)";
   if (!(c.rms_eps > 0) || !(c.rope_theta > 0) || !(c.lr >= 0) || !(c.beta1 >= 0 && c.beta1 < 1) ||
@@ -1486,6 +1512,46 @@ int mt_train_step(mt_model* m, const int32_t* tokens, size_t n_tokens, float* lo
 int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n_tokens, float* loss_out) {
   if (!m || !tokens_dev) return MT_EINVAL;
   return mt::run_step(m, nullptr, tokens_dev, n_tokens, loss_out);
+}
+
+int mt_train_step_micro(mt_model* m, const int32_t* tokens, size_t n_tokens, int32_t n_micro, float* loss_out) {
+  if (!m || !tokens || n_micro < 1) return MT_EINVAL;
+  const size_t per = (size_t)m->D.B * (m->D.S + 1);
+  if (n_tokens != per * (size_t)n_micro) {
+    m->err = "n_tokens must equal n_micro * batch * (seq + 1)";
+    return MT_EINVAL;
+  }
+  mt_step_stats tot{};
+  float loss = 0.f;
+  int code = MT_OK;
+  for (int k = 0; k < n_micro; ++k) {
+    m->micro_index = k;
+    m->micro_count = n_micro;
+    float l = 0.f;
+    code = mt::run_step(m, tokens + (size_t)k * per, nullptr, per, &l);
+    const mt_step_stats& s = m->stats;
+    for (double mt_step_stats::*f : {&mt_step_stats::step_ms, &mt_step_stats::gpu_compute_ms, &mt_step_stats::h2d_ms,
+                                     &mt_step_stats::d2h_ms, &mt_step_stats::wait_weights_ms, &mt_step_stats::adam_ms,
+                                     &mt_step_stats::gemm_ms, &mt_step_stats::gemm_flops, &mt_step_stats::visit_gap_ms,
+                                     &mt_step_stats::host_pre_ms, &mt_step_stats::tail_grads_ms,
+                                     &mt_step_stats::tail_adam_ms, &mt_step_stats::tail_rest_ms})
+      tot.*f += s.*f;
+    for (int64_t mt_step_stats::*f : {&mt_step_stats::gemm_launches, &mt_step_stats::kernel_launches,
+                                      &mt_step_stats::h2d_bytes, &mt_step_stats::d2h_bytes,
+                                      &mt_step_stats::flops_executed, &mt_step_stats::flops_model})
+      tot.*f += s.*f;
+    tot.adam_tail_ms = s.adam_tail_ms;
+    tot.arena_high_water = s.arena_high_water;
+    if (code != MT_OK) break;
+    loss += l;
+  }
+  m->micro_index = 0;
+  m->micro_count = 1;
+  tot.loss = loss;
+  tot.step = m->step;
+  m->stats = tot;
+  if (loss_out) *loss_out = loss;
+  return code;
 }
 
 int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, void* x_out, void* dx_in) {

@@ -23,6 +23,7 @@ struct AdamHyper {
 };
 void adam_range(uint16_t* w, const uint16_t* g, float* m, float* v, size_t n, const AdamHyper& h);
 bool copy_grad_check_finite(uint16_t* dst, const uint16_t* src, size_t n);
+bool add_grad_check_finite(uint16_t* dst, const uint16_t* src, size_t n);
 
 // ------------------------------------------------------------------ tiles
 enum TileKind { kTileEmbed = 0, kTileLayer = 1, kTileHead = 2 };
@@ -49,6 +50,7 @@ struct TileLayout {
 struct Dims {
   int L, d, Hq, Hkv, hd, f, V, B, S;
   long T;       // B*S
+  long Tc;      // rows per MLP chunk (T when the MLP runs on the whole step at once)
   int Dq;       // Hq*hd
   int Dqkv;     // (Hq + 2 Hkv) * hd
 };
@@ -89,6 +91,7 @@ struct Workspace {
   bf16 *dh, *dgu, *dn, *dout, *dqkv;
   float* delta;
   float* dg_partial;
+  float *dwd_f32, *dwgu_f32;  // FP32 W_d / W_gu gradients accumulated over MLP row chunks (chunked MLP only)
   // head
   bf16* nf;
   float* rstd_f;
@@ -132,6 +135,7 @@ struct LayerTemplate {
 
   // Optional debugging hook called after every kernel launch with its name
   // (used by MT_TRACE to wait for and report each kernel).
+  float loss_scale = 1.f;  // the head's cross-entropy is scaled by loss_scale / tokens (micro-batches)
   void (*trace_fn)(void* ctx, const char* kernel) = nullptr;
   void* trace_ctx = nullptr;
   void trace(const char* kernel) const {
@@ -145,6 +149,7 @@ struct LayerTemplate {
   // Given the layer's forward activations and dx_out, write dx_in and the
   // layer's gradients into gv (BF16, tile layout).
   int backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, bf16* dx_in, const LayerView& gv) const;
+  int mlp_backward_chunked(const LayerView& w, const LayerActs& a, const bf16* dx_out, const LayerView& gv) const;
   // Final norm + LM head + cross-entropy, forward and backward in chunks.
   int head(const HeadView& w, const bf16* x_L, bf16* dx_L, const HeadView& gv) const;
   int embed_fwd(const bf16* E, bf16* x0) const;

@@ -100,6 +100,11 @@ typedef struct {
   int64_t stage_bytes;       /* bytes per pinned H2D staging chunk (0 = 64 MiB); two chunks ping-pong */
   int64_t timeout_ms;        /* bound of every host wait (0 = 60000) */
   uint32_t flags;
+  int64_t mlp_chunk_rows;    /* run the MLP (gate/up, SwiGLU, down and their backward) over row chunks of
+                                this many tokens, a multiple of 128, so that its [tokens, 2 ffn]
+                                activations exist one chunk at a time (long sequences); the W_gu and W_d
+                                gradients then accumulate in FP32 across chunks.  0 = the whole step at
+                                once.  Not combinable with MT_STORE_ACTS. */
 } mt_config;
 
 typedef struct mt_model mt_model;
@@ -180,6 +185,19 @@ int mt_load_layer_tile(mt_model* m, int tile, int part, const void* src, size_t 
  */
 int mt_train_step(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out);
 int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n_tokens, float* loss_out);
+
+/*
+ * One training step over n_micro micro-batches (gradient accumulation): host
+ * int32 tokens [n_micro, batch, seq+1] (n_tokens = n_micro*batch*(seq+1)).
+ * Each micro-batch is a full streamed forward/backward pass; the gradient of
+ * the mean loss over all n_micro*batch*seq targets accumulates in the host
+ * tiles' G sections (BF16, the first pass writes, later passes add), and Adam
+ * runs once, as the last pass's gradients land.  *loss_out: the mean loss.
+ * n_micro = 1 is mt_train_step.  The step statistics sum over the passes.
+ * Errors as mt_train_step; a non-finite loss or gradient stops the step
+ * before any weight is updated.
+ */
+int mt_train_step_micro(mt_model* m, const int32_t* tokens, size_t n_tokens, int32_t n_micro, float* loss_out);
 
 /*
  * Per-layer check at the workload's full shape (a debugging hook for parity

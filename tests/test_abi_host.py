@@ -53,7 +53,8 @@ def test_required_device_bytes_positive_and_bounded(lib, name):
 
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=690), dict(ckpt_every=0),
-                                 dict(vocab=0), dict(batch=0), dict(seq=3, batch=1)])
+                                 dict(vocab=0), dict(batch=0), dict(seq=3, batch=1), dict(mlp_chunk_rows=100),
+                                 dict(mlp_chunk_rows=128, flags=2)])
 def test_bad_config_rejected(lib, bad):
     s = mt_inputs.PRESETS["tiny"]
     assert lib.mt_required_device_bytes(C.byref(_cfg(s, **bad))) == -1
@@ -145,3 +146,13 @@ def test_cpu_adam_cancellation_within_fp32_bound(lib):
     assert torch.all(diff <= adam_weight_tol(we, w))
     assert float(we[:2].abs().max()) < 1e-3 * float(w[:2].double().abs().min())  # the update cancels w
     assert diff[2] <= bf16_ulp(we[2:])[0]  # an ordinary weight stays within 1 BF16 ulp
+
+
+def test_chunked_mlp_shrinks_the_device_arena(lib):
+    """Row-chunked MLP: the [tokens, 2 ffn] activations and their gradient exist
+    one chunk at a time, so the long-sequence step fits the GPU."""
+    s = mt_inputs.PRESETS["7b-512k"]
+    whole = lib.mt_required_device_bytes(C.byref(_cfg(s)))
+    chunked = lib.mt_required_device_bytes(C.byref(_cfg(s, mlp_chunk_rows=65536)))
+    assert chunked > 0 and whole - chunked > 40e9
+    assert chunked < 240e9

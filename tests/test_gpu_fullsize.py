@@ -9,7 +9,7 @@
     rows, dL/dx on every row of those sequences and the layer's full weight
     gradients.  Every other sequence must receive dL/dx = 0 exactly.
 (2) The attention kernels at the workloads' sequence lengths (4K with GQA,
-    32K and 128K with MHA): output, log-sum-exp and dq on sampled query rows,
+    32K, 128K and 512K with MHA): output, log-sum-exp and dq on sampled query rows,
     dk and dv on sampled keys, each computed by the oracle one at a time.
 (3) Full-width models of reduced depth against the whole oracle: loss, every
     gradient and the Adam update.  The oracle needs O(T) host work per layer
@@ -113,6 +113,7 @@ ATTN_CASES = {
     "14b": (8, 4096, 40, 8, (0, 7), (0, 17, 39), (0, 1, 127, 128, 1000, 2049, 4094, 4095), (0, 64, 2047, 4000, 4095)),
     "7b-32k": (1, 32768, 32, 32, (0,), (0, 31), (0, 1, 4095, 16383, 16384, 32767), (32767, 32700, 32100)),
     "7b-128k": (1, 131072, 32, 32, (0,), (0, 31), (0, 127, 65536, 131071), (131071, 131000, 130900)),
+    "7b-512k": (1, 524288, 32, 32, (0,), (0, 31), (0, 4095, 262144, 524287), (524287, 524200)),
 }
 
 

@@ -171,3 +171,55 @@ def test_nonfinite_loss_skips_every_update():
     assert e.value.code == hms._lib.MT_ENONFINITE
     _equal_trees(m.weights(), params)
     m.close()
+
+
+def test_chunked_mlp_matches_oracle_and_repeats():
+    """The MLP over row chunks (long-sequence mode: 128-row chunks of a
+    360-token step, the last one ragged) against the oracle, and bit-exact
+    across repeat runs."""
+    s = SHAPES["gqa128"]
+    cfg = OracleConfig.from_shape(s)
+    r = _run(s, mlp_chunk_rows=128)
+    tokens = mt_inputs.step_tokens(s, 1)
+    loss, grads = oracle.model_loss_and_grads(r["params0"], tokens, cfg)
+    assert abs(r["loss"][0] - loss) <= parity.LOSS_RTOL * abs(loss)
+    parity.assert_grads_close(r["g"][0], grads)
+    m, v = r["mv"][0]
+    parity.assert_adam_matches(r["w"][0], r["params0"], r["g"][0], m, v, 1, cfg)
+    r2 = _run(s, mlp_chunk_rows=128)
+    assert r["loss"] == r2["loss"]
+    _equal_trees(r["g"][0], r2["g"][0])
+    _equal_trees(r["w"][0], r2["w"][0])
+
+
+def test_micro_batch_accumulation_matches_oracle():
+    """Two micro-batches in one step: the loss and every gradient are those of
+    the mean over both micro-batches' targets (the oracle on the concatenated
+    batch), and Adam runs once on the accumulated gradient."""
+    s = SHAPES["gqa128"]
+    cfg = OracleConfig.from_shape(s)
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    t1, t2 = mt_inputs.step_tokens(s, 1), mt_inputs.step_tokens(s, 2)
+    m = hms.StreamedDecoder.from_shape(s)
+    m.load_weights(params)
+    loss = m.train_step_micro(torch.stack([t1, t2]))
+    g, w = m.grads(), m.weights()
+    mm, vv = m.moments()
+    assert m.step == 1
+    m.close()
+    loss_ref, grads = oracle.model_loss_and_grads(params, torch.cat([t1, t2]), cfg)
+    assert abs(loss - loss_ref) <= parity.LOSS_RTOL * abs(loss_ref)
+    parity.assert_grads_close(g, grads)
+    parity.assert_adam_matches(w, params, g, mm, vv, 1, cfg)
+
+
+def test_one_micro_batch_is_the_plain_step():
+    s = SHAPES["tiny"]
+    a = _run(s, steps=1)
+    m = hms.StreamedDecoder.from_shape(s)
+    m.load_weights(mt_inputs.model_weights(s, gain_jitter=0.1))
+    loss = m.train_step_micro(mt_inputs.step_tokens(s, 1)[None])
+    assert loss == a["loss"][0]
+    _equal_trees(m.weights(), a["w"][0])
+    _equal_trees(m.grads(), a["g"][0])
+    m.close()
