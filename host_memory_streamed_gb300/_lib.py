@@ -18,6 +18,7 @@ MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNEL
 MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
 EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE, EPI_SWIGLU_BWD = range(7)
+GEMM_A_MN, GEMM_B_MN = 1, 2  # operand layouts of mt_op_gemm_layout
 
 
 class MtConfig(C.Structure):

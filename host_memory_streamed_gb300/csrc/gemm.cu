@@ -51,6 +51,21 @@ constexpr int SMEM_USED = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*
 constexpr int SMEM_BYTES = 232448 - 256;  // 227 KB less room for the static shared variables
 static_assert(SMEM_USED <= SMEM_BYTES, "shared memory plan exceeds 227 KB");
 
+// CTA-pair variant (cta_group::2): a cluster of two CTAs on two SMs computes
+// one 256 x 256 output tile.  Each CTA stages its 128 rows of A and its 128
+// rows (half) of B per K block; the leading CTA's single MMA thread issues
+// M = 256, N = 256 MMAs that read both CTAs' stages, and each CTA's TMEM
+// receives its 128 rows of the tile.  Per SM this moves 32 KB of operands per
+// K block instead of 48 KB for the same 128 x 256 x 64 of work.
+constexpr int PM = 256;                // pair tile rows (128 per CTA)
+constexpr int PHALF = 128;             // rows of A and of B staged per CTA
+constexpr int P_STAGES = 6;
+constexpr int P_A_STAGE = PHALF * BK * 2;  // 16 KB
+constexpr int P_B_STAGE = PHALF * BK * 2;  // 16 KB
+constexpr int P_GROUP_M = 8;           // pair-tile raster: 8 M-tiles share each B panel
+constexpr int P_SMEM_USED = P_STAGES * (P_A_STAGE + P_B_STAGE) + 1024 + 256;
+static_assert(P_SMEM_USED <= SMEM_BYTES, "pair shared memory plan exceeds 227 KB");
+
 struct EpiParams {
   int M, N, K;
   int mode;
@@ -68,11 +83,11 @@ struct EpiParams {
   int* status;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& tm, int& tn) {
-  const int per_group = GROUP_M * num_n;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& tm, int& tn, int group_m = GROUP_M) {
+  const int per_group = group_m * num_n;
   const int group = tile / per_group;
-  const int first_m = group * GROUP_M;
-  const int gsize = min(num_m - first_m, GROUP_M);
+  const int first_m = group * group_m;
+  const int gsize = min(num_m - first_m, group_m);
   const int r = tile - group * per_group;
   tm = first_m + r % gsize;
   tn = r / gsize;
@@ -220,6 +235,70 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
     }
     default:
       break;
+  }
+}
+
+// Epilogue of one output tile: thread `row` of the tile reads its TMEM lane
+// (tbase already points at lane quarter*32, accumulator column 0), applies the
+// epilogue mode and stores columns tn*BN .. tn*BN + BN - 1.
+__device__ __forceinline__ void store_tile(const EpiParams& p, uint32_t tbase, int row, int tn) {
+  if (p.mode == kEpiRope && tn * BN < p.rope_cols) {
+    // rotate-half RoPE: columns j and j + hd/2 of each head form a pair.
+    // The row's cos/sin for frequencies j .. j+31 are loaded once (16-byte
+    // loads) and serve every head of the tile.
+    const int hd = p.head_dim;
+    const int s = row % p.seq;
+    for (int j = 0; j < hd / 2; j += 32) {
+      float cs[32], sn[32];
+      if (row < p.M) {
+        const float4* c4 = reinterpret_cast<const float4*>(p.rope_cos + (long)s * (hd / 2) + j);
+        const float4* s4 = reinterpret_cast<const float4*>(p.rope_sin + (long)s * (hd / 2) + j);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 a = c4[q], b = s4[q];
+          cs[4 * q] = a.x, cs[4 * q + 1] = a.y, cs[4 * q + 2] = a.z, cs[4 * q + 3] = a.w;
+          sn[4 * q] = b.x, sn[4 * q + 1] = b.y, sn[4 * q + 2] = b.z, sn[4 * q + 3] = b.w;
+        }
+      }
+      for (int h0 = 0; h0 < BN; h0 += hd) {
+        uint32_t lo_r[32], hi_r[32];
+        tmem_ld_32x32b_x32(tbase + h0 + j, lo_r);
+        tmem_ld_32x32b_x32(tbase + h0 + hd / 2 + j, hi_r);
+        tmem_wait_ld();
+        float lo[32], hi[32];
+        const int gcol = tn * BN + h0 + j;
+        if (row < p.M && gcol < p.rope_cols) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x1 = __uint_as_float(lo_r[e]), x2 = __uint_as_float(hi_r[e]);
+            lo[e] = x1 * cs[e] - x2 * sn[e];
+            hi[e] = x2 * cs[e] + x1 * sn[e];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            lo[e] = __uint_as_float(lo_r[e]);
+            hi[e] = __uint_as_float(hi_r[e]);
+          }
+        }
+        EpiParams q = p;
+        q.mode = kEpiStoreBf16;
+        epilogue_chunk(q, row, gcol, lo);
+        epilogue_chunk(q, row, gcol + hd / 2, hi);
+      }
+    }
+  } else {
+    EpiParams q = p;
+    if (q.mode == kEpiRope) q.mode = kEpiStoreBf16;
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tbase + c * 32, r);
+      tmem_wait_ld();
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+      epilogue_chunk(q, row, tn * BN + c * 32, v);
+    }
   }
 }
 
@@ -378,54 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int row = tm * BM + row_in_tile;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (p.mode == kEpiRope && tn * BN < p.rope_cols) {
-        // rotate-half RoPE: columns j and j + hd/2 of each head form a pair.
-        const int hd = p.head_dim;
-        const int s = row % p.seq;
-        for (int h0 = 0; h0 < BN; h0 += hd) {
-          for (int j = 0; j < hd / 2; j += 32) {
-            uint32_t lo_r[32], hi_r[32];
-            tmem_ld_32x32b_x32(tbase + h0 + j, lo_r);
-            tmem_ld_32x32b_x32(tbase + h0 + hd / 2 + j, hi_r);
-            tmem_wait_ld();
-            float lo[32], hi[32];
-            const int gcol = tn * BN + h0 + j;
-            if (row < p.M && gcol < p.rope_cols) {
-              const float* cs = p.rope_cos + (long)s * (hd / 2) + j;
-              const float* sn = p.rope_sin + (long)s * (hd / 2) + j;
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float x1 = __uint_as_float(lo_r[e]), x2 = __uint_as_float(hi_r[e]);
-                const float c = cs[e], si = sn[e];
-                lo[e] = x1 * c - x2 * si;
-                hi[e] = x2 * c + x1 * si;
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                lo[e] = __uint_as_float(lo_r[e]);
-                hi[e] = __uint_as_float(hi_r[e]);
-              }
-            }
-            EpiParams q = p;
-            q.mode = kEpiStoreBf16;
-            epilogue_chunk(q, row, gcol, lo);
-            epilogue_chunk(q, row, gcol + hd / 2, hi);
-          }
-        }
-      } else {
-        EpiParams q = p;
-        if (q.mode == kEpiRope) q.mode = kEpiStoreBf16;
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, r);
-          tmem_wait_ld();
-          float v[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-          epilogue_chunk(q, row, tn * BN + c * 32, v);
-        }
-      }
+      store_tile(p, tbase, row, tn);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -439,6 +471,193 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// The CTA-pair kernel.  Roles per CTA as in gemm_bf16_tcgen05_kernel; the
+// MMA warp of the odd CTA only takes part in the TMEM allocation.
+//   full[s]    leading CTA only: the leader's producer arms it with both
+//              CTAs' bytes, both producers' loads complete on it.
+//   empty[s]   both CTAs: the MMA commit arrives on both (multicast).
+//   tfull[a]   both CTAs: accumulator a ready (multicast commit).
+//   tempty[a]  leading CTA only: the 8 epilogue warps of the pair arrive.
+// Every wait is bounded; after a timeout each role stops, records
+// kStatusGemmTimeout and both CTAs still meet at the final cluster barrier.
+template <bool A_MN, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    gemm_bf16_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                  const __grid_constant__ CUtensorMap tmap_b, EpiParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * P_A_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + P_STAGES * P_B_STAGE);
+  uint64_t* empty = full + P_STAGES;
+  uint64_t* tfull = empty + P_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+  const int num_m = (p.M + PM - 1) / PM;
+  const int num_n = (p.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_k = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers initialised in both CTAs before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int pending[P_STAGES];
+      for (int s = 0; s < P_STAGES; ++s) pending[s] = -1;
+      const int row0 = (int)rank * PHALF;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
+        int tm, tn;
+        tile_coords(tile, num_m, num_n, tm, tn, P_GROUP_M);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            set_status(p.status, kStatusGemmTimeout);
+            ok = false;
+            break;
+          }
+          const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_STAGE + P_B_STAGE));
+          uint8_t* a_dst = sA + stage * P_A_STAGE;
+          uint8_t* b_dst = sB + stage * P_B_STAGE;
+          if (A_MN) {
+#pragma unroll
+            for (int i = 0; i < PHALF / 64; ++i)
+              tma_load_2d_pair(a_dst + i * (64 * BK * 2), &tmap_a, tm * PM + row0 + 64 * i, kb * BK, bar);
+          } else {
+            tma_load_2d_pair(a_dst, &tmap_a, kb * BK, tm * PM + row0, bar);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int i = 0; i < PHALF / 64; ++i)
+              tma_load_2d_pair(b_dst + i * (64 * BK * 2), &tmap_b, tn * BN + row0 + 64 * i, kb * BK, bar);
+          } else {
+            tma_load_2d_pair(b_dst, &tmap_b, kb * BK, tn * BN + row0, bar);
+          }
+          pending[stage] = (int)phase;
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Tail: every load of this CTA has landed once the MMA released its
+      // stage.  After a timeout here the remaining loads were issued more
+      // than the wait limit ago.
+      for (int s = 0; s < P_STAGES; ++s)
+        if (pending[s] >= 0 && !mbar_wait(&empty[s], (uint32_t)pending[s])) {
+          set_status(p.status, kStatusGemmTimeout);
+          break;
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(PM, BN) | (A_MN ? (1u << 15) : 0u) | (B_MN ? (1u << 16) : 0u);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
+        if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1)) {
+          set_status(p.status, kStatusGemmTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], phase)) {
+            set_status(p.status, kStatusGemmTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = A_MN ? smem_desc_mnmajor_sw128(sA + stage * P_A_STAGE, 64 * BK * 2)
+                                      : smem_desc_kmajor_sw128(sA + stage * P_A_STAGE);
+          const uint64_t bdesc = B_MN ? smem_desc_mnmajor_sw128(sB + stage * P_B_STAGE, 64 * BK * 2)
+                                      : smem_desc_kmajor_sw128(sB + stage * P_B_STAGE);
+          constexpr uint64_t a_step = A_MN ? (2048 >> 4) : (32 >> 4);
+          constexpr uint64_t b_step = B_MN ? (2048 >> 4) : (32 >> 4);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_pair_mc(&empty[stage], 0x3);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&tfull[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // Every MMA issued above has completed (and stopped reading both CTAs'
+      // shared memory and writing their TMEM) once this commit arrives.
+      tc_commit_pair(done);
+      if (!mbar_wait(done, 0)) set_status(p.status, kStatusGemmTimeout);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row_in_tile = (int)rank * PHALF + quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster; tile < num_tiles; tile += num_clusters) {
+      int tm, tn;
+      tile_coords(tile, num_m, num_n, tm, tn, P_GROUP_M);
+      if (!mbar_wait_warp(&tfull[acc], acc_phase)) {
+        set_status(p.status, kStatusGemmTimeout);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      store_tile(p, tbase, tm * PM + row_in_tile, tn);
+      tc_fence_before();
+      if (leader)
+        mbar_arrive_warp(&tempty[acc]);
+      else
+        mbar_arrive_warp_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -532,12 +751,58 @@ const char* gemm_check(const GemmArgs& g) {
       if (!(g.head_dim == 64 || g.head_dim == 128)) return "gemm: RoPE head_dim must be 64 or 128";
       if (g.rope_cols % g.head_dim) return "gemm: rope_cols must be a multiple of head_dim";
       if (!g.rope_cos || !g.rope_sin || g.seq <= 0) return "gemm: RoPE tables missing";
+      if ((reinterpret_cast<uintptr_t>(g.rope_cos) | reinterpret_cast<uintptr_t>(g.rope_sin)) & 15)
+        return "gemm: RoPE tables must be 16-byte aligned";
       break;
     default:
       return "gemm: unknown epilogue";
   }
   return nullptr;
 }
+
+namespace {
+
+// Clusters of two that fit on the device at once (one CTA per SM; SMs left
+// over by an odd GPC stay idle), or 0 when no pair can be placed.
+template <bool A_MN, bool B_MN>
+int pair_clusters() {
+  static int n = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    auto* k = gemm_bf16_tcgen05_pair_kernel<A_MN, B_MN>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
+      n = 0;
+      return;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * num_sms(), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    int c = 0;
+    n = cudaOccupancyMaxActiveClusters(&c, k, &cfg) == cudaSuccess ? c : 0;
+    cudaGetLastError();
+  });
+  return n;
+}
+
+template <bool A_MN, bool B_MN>
+int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& p, int clusters, cudaStream_t s) {
+  gemm_bf16_tcgen05_pair_kernel<A_MN, B_MN><<<2 * clusters, THREADS, SMEM_BYTES, s>>>(ta, tb, p);
+  return launch_result();
+}
+
+template <bool A_MN, bool B_MN>
+int gemm_pair(const GemmArgs& g, const EpiParams& p, cudaStream_t s) {
+  const int avail = pair_clusters<A_MN, B_MN>();
+  if (avail <= 0) return 1;  // not placeable: the caller uses the single-CTA kernel
+  CUtensorMap ta, tb;
+  if (A_MN ? !make_tmap(&ta, g.A, g.K, g.M, g.lda, BK) : !make_tmap(&ta, g.A, g.M, g.K, g.lda, PHALF)) return -3;
+  if (B_MN ? !make_tmap(&tb, g.B, g.K, g.N, g.ldb, BK) : !make_tmap(&tb, g.B, g.N, g.K, g.ldb, PHALF)) return -3;
+  const int tiles = ((g.M + PM - 1) / PM) * ((g.N + BN - 1) / BN);
+  return launch_pair<A_MN, B_MN>(ta, tb, p, tiles < avail ? tiles : avail, s);
+}
+
+}  // namespace
 
 int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (gemm_check(g)) return -1;
@@ -554,9 +819,6 @@ int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
     if (!ok) return -2;
     attr_done = true;
   }
-  CUtensorMap ta, tb;
-  if (g.a_mn ? !make_tmap(&ta, g.A, g.K, g.M, g.lda, BK) : !make_tmap(&ta, g.A, g.M, g.K, g.lda, BM)) return -3;
-  if (g.b_mn ? !make_tmap(&tb, g.B, g.K, g.N, g.ldb, BK) : !make_tmap(&tb, g.B, g.N, g.K, g.ldb, BN)) return -3;
   EpiParams p;
   p.M = g.M;
   p.N = g.N;
@@ -574,6 +836,22 @@ int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   p.head_dim = g.head_dim;
   p.seq = g.seq;
   p.status = g.status;
+  // More than one 128-row tile of M: CTA pairs (256 x 256 tiles).
+  if (g.M > BM) {
+    int rc;
+    if (!g.a_mn && !g.b_mn)
+      rc = gemm_pair<false, false>(g, p, stream);
+    else if (g.a_mn && !g.b_mn)
+      rc = gemm_pair<true, false>(g, p, stream);
+    else if (!g.a_mn && g.b_mn)
+      rc = gemm_pair<false, true>(g, p, stream);
+    else
+      rc = gemm_pair<true, true>(g, p, stream);
+    if (rc <= 0) return rc;
+  }
+  CUtensorMap ta, tb;
+  if (g.a_mn ? !make_tmap(&ta, g.A, g.K, g.M, g.lda, BK) : !make_tmap(&ta, g.A, g.M, g.K, g.lda, BM)) return -3;
+  if (g.b_mn ? !make_tmap(&tb, g.B, g.K, g.N, g.ldb, BK) : !make_tmap(&tb, g.B, g.N, g.K, g.ldb, BN)) return -3;
   const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   if (!g.a_mn && !g.b_mn)

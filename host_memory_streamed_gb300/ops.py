@@ -53,6 +53,23 @@ def gemm(A, B, out, epilogue=_lib.EPI_STORE_BF16, residual=None, out2=None, rope
                                rope_cols, head_dim, seq, _ptr(status), _stream()))
 
 
+def gemm_layout(A, B, out, a_mn=False, b_mn=False, epilogue=_lib.EPI_STORE_BF16, residual=None, status=None):
+    """out = epilogue(op(A) @ op(B)^T) with A stored [M, K] (or [K, M] when a_mn)
+    and B stored [N, K] (or [K, N] when b_mn): the weight-gradient and
+    data-gradient layouts of the backward pass."""
+    _need(A, BF16, "A")
+    _need(B, BF16, "B")
+    _need(out, F32 if epilogue in (_lib.EPI_F32, _lib.EPI_F32_ACCUMULATE) else BF16, "out")
+    _need(residual, BF16, "residual")
+    _need(status, I32, "status")
+    M, K = (A.shape[1], A.shape[0]) if a_mn else (A.shape[0], A.shape[1])
+    N = B.shape[1] if b_mn else B.shape[0]
+    layout = (_lib.GEMM_A_MN if a_mn else 0) | (_lib.GEMM_B_MN if b_mn else 0)
+    _chk(_lib.lib().mt_op_gemm_layout(A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), M, N, K, layout,
+                                      epilogue, out.data_ptr(), out.stride(0), _ptr(residual),
+                                      residual.stride(0) if residual is not None else 0, _ptr(status), _stream()))
+
+
 def attention_fwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse, status=None):
     _need(qkv, BF16, "qkv")
     _need(o, BF16, "o")

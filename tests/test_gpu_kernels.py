@@ -95,6 +95,36 @@ def test_gemm_swiglu_backward_epilogue(M, N, K):
     assert rel(dgu.cpu()[:, 1::2], du) < 4e-3
 
 
+# Both kernels (single CTA for M <= 128, CTA pairs with 256 x 256 tiles above)
+# in all four operand layouts, with ragged M, N and K tails and partial tiles
+# (MN-major operands need M resp. N to be a multiple of 8).
+LAYOUT_SHAPES = [(128, 264, 72), (120, 136, 64), (296, 520, 200), (256, 256, 64), (1000, 776, 1032),
+                 (2304, 2048, 512)]
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, False), (False, True), (True, True)])
+@pytest.mark.parametrize("M,N,K", LAYOUT_SHAPES)
+def test_gemm_operand_layouts(M, N, K, a_mn, b_mn):
+    g = torch.Generator().manual_seed(M + 3 * N + 7 * K + 2 * a_mn + b_mn)
+    A, B = rnd((M, K), g), rnd((N, K), g)
+    ref = A.to(D) @ B.to(D).T
+    Ad = (A.T.contiguous() if a_mn else A).to(DEV)
+    Bd = (B.T.contiguous() if b_mn else B).to(DEV)
+    C32 = torch.empty(M, N, device=DEV)
+    ops.gemm_layout(Ad, Bd, C32, a_mn=a_mn, b_mn=b_mn, epilogue=_lib.EPI_F32)
+    acc = torch.full((M, N), 0.25, device=DEV)
+    ops.gemm_layout(Ad, Bd, acc, a_mn=a_mn, b_mn=b_mn, epilogue=_lib.EPI_F32_ACCUMULATE)
+    status = torch.zeros(1, device=DEV, dtype=torch.int32)
+    Cb = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
+    ops.gemm_layout(Ad, Bd, Cb, a_mn=a_mn, b_mn=b_mn, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    bound = 1e-5 * math.sqrt(K) * (A.to(D).abs() @ B.to(D).abs().T) + 1e-30
+    assert torch.all((C32.cpu().to(D) - ref).abs() <= bound)
+    assert torch.all((acc.cpu().to(D) - (ref + 0.25)).abs() <= bound + 1e-7)
+    assert torch.equal(Cb.cpu(), C32.cpu().to(torch.bfloat16))
+
+
 def test_gemm_rejects_bad_arguments():
     A = torch.zeros(16, 12, device=DEV, dtype=torch.bfloat16)
     C = torch.zeros(16, 16, device=DEV, dtype=torch.bfloat16)
