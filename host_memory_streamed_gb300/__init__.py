@@ -14,10 +14,11 @@ import torch
 
 from . import _lib
 from ._lib import (MT_DEBUG_CHECKS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V, MT_PART_W,
-                   MT_RESIDENT, MT_STORE_ACTS, MT_TIME_KERNELS, MT_TRACE, ERROR_NAMES)
+                   MT_RESIDENT, MT_STORE_ACTS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG, ERROR_NAMES)
 
 __all__ = ["StreamedDecoder", "MtError", "ops", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
-           "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_PART_W", "MT_PART_G", "MT_PART_M", "MT_PART_V"]
+           "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_VISIT_LOG", "MT_PART_W", "MT_PART_G", "MT_PART_M",
+           "MT_PART_V"]
 
 LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
 

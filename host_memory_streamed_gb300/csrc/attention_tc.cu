@@ -3,23 +3,24 @@
 // TMEM, Q/K/V tiles brought in by TMA.
 //
 // One CTA per (128 queries, query head, batch); 10 warps:
-//   warp 0      TMA: Q once; K and V blocks of 128 keys into a 2-stage ring
+//   warp 0      TMA: Q once; K and V blocks of 128 keys into a 3-stage ring
 //               (one tensor map over the packed q|k|v projection buffer).
-//   warp 1      MMA (one thread): S_j = Q K_j^T into TMEM buffer j%2, then,
-//               once the softmax has written P_j, O += P_j V_j (V read as an
-//               MN-major operand straight from its [keys][head_dim] tile).
-//   warps 2..9  softmax: two threads (one in each of two warps that share a
-//               TMEM lane group) own one query row.  Each reads the whole
-//               score row and takes its maximum itself, so the pair agrees on
-//               the running maximum without exchanging anything; each then
-//               exponentiates its half of the 128 keys and keeps its half of
-//               the row sum (the halves are added once, at the end).  P_j is
-//               written to shared memory in the 128-byte-swizzled K-major
-//               layout the tensor core reads as its A operand.  The running
-//               maximum is only moved (and O rescaled in TMEM, each thread of
-//               the pair scaling half of the columns) when it grows by more
-//               than a factor 2^8, so O is rarely touched; the final O / l and
-//               the log-sum-exp use whichever maximum was kept.
+//   warp 1      MMA (one thread): S_j = Q K_j^T into TMEM buffer j%2; once
+//               the softmax has written P_j (BF16, over S_j's first 64
+//               columns) O_{j%2} += P_j V_j with P read from TMEM as the A
+//               operand and V as an MN-major operand straight from its
+//               [keys][head_dim] tile; then S_{j+2} into the same buffer.
+//   warps 2..9  softmax in two groups of four warps: group 0 takes the even
+//               key blocks, group 1 the odd ones, each with its own running
+//               maximum, row sum and O accumulator in TMEM, so that one
+//               group's exponentials overlap the tensor core's work on the
+//               other group's block.  Thread <-> query row (TMEM lane); each
+//               thread reads its whole score row, takes the maximum and
+//               exponentiates all 128 keys (f32x2 arithmetic, SFU exp2).  A
+//               group's maximum is only moved (and its O rescaled in TMEM)
+//               when it grows by more than a factor 2^8.  At the end the two
+//               groups' (max, sum) pairs meet in shared memory and each group
+//               writes half of the output columns from both accumulators.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // kStatusAttnFwdTimeout in the status word and unwinds.
 //
@@ -78,6 +79,31 @@ __device__ __forceinline__ uint32_t pack2bf(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// ---- FP32 pairs: one f32x2 instruction does the work of two scalar ones.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(TA_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, TaParams p) {
@@ -88,18 +114,16 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  float* sL = reinterpret_cast<float*>(smem + C::OFF_L);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;        // [NS]
-  uint64_t* kv_empty = bar + 1 + NS;  // [NS]
+  uint64_t* kv_full = bar + 1;           // [NS]
+  uint64_t* kv_empty = bar + 1 + NS;     // [NS]
   uint64_t* s_full = bar + 1 + 2 * NS;   // [2] S_j in TMEM buffer j & 1
-  uint64_t* p_full = bar + 3 + 2 * NS;   // [2] P_j stored over S_j, O rescaled (256 softmax threads)
-  uint64_t* pv_done = bar + 5 + 2 * NS;  // [2]
-  uint64_t* s_read = bar + 7 + 2 * NS;   // every softmax thread has read S_j (256)
-  uint64_t* o_full = bar + 8 + 2 * NS;
-  uint64_t* l_ready = bar + 9 + 2 * NS;  // both halves of every row sum written (256)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 10 + 2 * NS);
+  uint64_t* p_full = bar + 3 + 2 * NS;   // [2] P_j stored over S_j, O_{j&1} rescaled (the group's 4 warps)
+  uint64_t* pv_done = bar + 5 + 2 * NS;  // [2] O_{j&1} += P_j V_j done
+  uint64_t* o_full = bar + 7 + 2 * NS;   // every MMA done
+  uint64_t* ml_ready = bar + 8 + 2 * NS; // both groups' (m, l) of every row in shared memory (8 warps)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 9 + 2 * NS);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -121,12 +145,11 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kSoftmaxWarps);
+      mbar_init(&p_full[i], kSoftmaxWarps / 2);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(s_read, kSoftmaxWarps);
     mbar_init(o_full, 1);
-    mbar_init(l_ready, kSoftmaxWarps);
+    mbar_init(ml_ready, kSoftmaxWarps);
     fence_barrier_init();
     tma_prefetch_desc(&tm_qkv);
   }
@@ -138,7 +161,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tO = tmem + 256;  // S_j at 128 * (j & 1), O at 256
+  // S_j at 128 * (j & 1); the two groups' O accumulators at 256 and 256 + HD
+  auto tO = [&](int g) { return tmem + 256u + (uint32_t)(g * HD); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -193,13 +217,10 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         return true;
       };
       if (ok) ok = issue_qk(0);
+      if (ok && n_kb > 1) ok = issue_qk(1);
       for (int j = 0; ok && j < n_kb; ++j) {
-        // S_{j+1} goes to the other buffer; the PV MMA that read P_{j-1} from it was issued before
-        if (j + 1 < n_kb && !issue_qk(j + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1)) {
+        const int g = j & 1;
+        if (!mbar_wait(&p_full[g], (j >> 1) & 1)) {
           site = 600 + min(j, 99);
           ok = false;
           break;
@@ -207,12 +228,17 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         tc_fence_after();
         const int s = j % NS;
         const uint64_t vdesc = smem_desc_mnmajor_sw128(sV + s * C::KV_BYTES, C::BOX);
-        const uint32_t pa = tmem + 128u * (uint32_t)(j & 1);
+        const uint32_t pa = tmem + 128u * (uint32_t)g;
 #pragma unroll
         for (int kk = 0; kk < TA_BN / 16; ++kk)
-          tc_mma_bf16_ts(tO, pa + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_bf16_ts(tO(g), pa + kk * 8, vdesc + (uint64_t)(kk * (2048 >> 4)), id_pv, (j >= 2 || kk > 0) ? 1u : 0u);
         tc_commit(&kv_empty[s]);
-        tc_commit(&pv_done[j & 1]);
+        tc_commit(&pv_done[g]);
+        // S_{j+2} overwrites P_j: issued after the MMAs that read it
+        if (j + 2 < n_kb && !issue_qk(j + 2)) {
+          ok = false;
+          break;
+        }
       }
       if (ok) {
         tc_commit(o_full);
@@ -222,19 +248,23 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       }
     }
   } else {
-    // softmax warps 2..9: thread <-> query row r (TMEM lane r), half hf of the
-    // 128 key columns for the exponentials and of the HD output columns
+    // softmax warps: group g = 0 (warps 2..5) takes the even key blocks, g = 1
+    // (warps 6..9) the odd ones; thread <-> query row r (TMEM lane r), all
+    // 128 keys of its group's blocks, its own running maximum, row sum and O
+    // accumulator.  While one group exponentiates, the tensor core works on
+    // the other group's blocks.
     const int quarter = warp & 3;
-    const int hf = (warp - 2) >> 2;
+    const int g = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = q0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float m = -INFINITY, l = 0.f;  // running maximum (raw score units) and this half's row sum
+    const uint32_t tOg = tO(g) + lane_off;
+    float m = -INFINITY, l = 0.f;  // running maximum (raw score units) and row sum of this group's blocks
     bool ok = true;
     int site = 0;
-    for (int j = 0; j < n_kb; ++j) {
-      const uint32_t tS = tmem + 128u * (uint32_t)(j & 1);
-      if (!mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1)) {
+    for (int j = g; j < n_kb; j += 2) {
+      const uint32_t tS = tmem + 128u * (uint32_t)g + lane_off;
+      if (!mbar_wait_warp(&s_full[g], (j >> 1) & 1)) {
         site = 700 + min(j, 99);
         ok = false;
         break;
@@ -243,19 +273,21 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       uint32_t x[TA_BN];
 #pragma unroll
       for (int c = 0; c < TA_BN / 32; ++c)
-        tmem_ld_32x32b_x32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(x + c * 32));
+        tmem_ld_32x32b_x32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(x + c * 32));
       tmem_wait_ld_regs(x);
-      tc_fence_before();
-      mbar_arrive_warp(s_read);
       const int k0 = j * TA_BN;
       if (k0 + TA_BN - 1 > q0) {  // block touches the diagonal
 #pragma unroll
         for (int c = 0; c < TA_BN; ++c)
           if (k0 + c > qrow) x[c] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < TA_BN; ++c) mx = fmaxf(mx, __uint_as_float(x[c]));
+      for (int c = 0; c < TA_BN; c += 4) {
+        mxa = fmax3(mxa, __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
+        mxb = fmax3(mxb, __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]));
+      }
+      const float mx = fmaxf(mxa, mxb);
       // scores are raw q.k; probabilities exp2((x - m) * scale * log2 e)
       const float m_new = fmaxf(m, mx);
       const bool rescale = (m == -INFINITY) || ((m_new - m) * p.sl2 > kRescaleThreshold);
@@ -265,96 +297,109 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         m = m_new;
       }
       const float nb = (m == -INFINITY) ? 0.f : -m * p.sl2;
-      // this half's 64 keys as packed BF16 pairs; the register array is indexed with constants only
-      float rs = 0.f;
-      uint32_t pk[32];
+      const uint64_t sl2x2 = f2(p.sl2, p.sl2), nbx2 = f2(nb, nb);
+      // two packed partial row sums: four independent chains of adds
+      uint64_t acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+      // P_j as packed BF16 pairs over the first 64 columns of S_j (this warp's
+      // own lanes, already read), one half of the keys at a time; the register
+      // arrays are indexed with constants only
       auto exp_half = [&](auto half) {
-        constexpr int K0 = decltype(half)::value * 64;
-        // four partial row sums: no 64-long chain of dependent adds
-        float r4[4] = {0.f, 0.f, 0.f, 0.f};
+        constexpr int K0 = decltype(half)::value * (TA_BN / 2);
+        uint32_t pk[TA_BN / 4];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(x[K0 + 2 * e]), p.sl2, nb));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(x[K0 + 2 * e + 1]), p.sl2, nb));
-          r4[e & 3] += p0 + p1;
+        for (int e = 0; e < TA_BN / 4; ++e) {
+          const uint64_t t =
+              fma2(f2(__uint_as_float(x[K0 + 2 * e]), __uint_as_float(x[K0 + 2 * e + 1])), sl2x2, nbx2);
+          float t0, t1;
+          f2split(t, t0, t1);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          acc[e & 1] = add2(acc[e & 1], f2(p0, p1));
           pk[e] = pack2bf(p0, p1);
         }
-        rs = (r4[0] + r4[1]) + (r4[2] + r4[3]);
+        tmem_st_32x32b_x32(tS + decltype(half)::value * 32, pk);
       };
-      if (hf == 0)
-        exp_half(std::integral_constant<int, 0>{});
-      else
-        exp_half(std::integral_constant<int, 1>{});
-      l = l * alpha + rs;
-      // P_j over S_j's first 64 columns, once both halves of every row have read S_j
-      if (!mbar_wait_warp(s_read, j & 1)) {
-        site = 750 + min(j, 49);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st_32x32b_x32(tS + lane_off + hf * 32, pk);
-      // O holds sum_{i<j} P_i V_i.  tcgen05.ld/st are warp-collective, so the
-      // whole warp rescales when any of its rows must (alpha = 1 for the others);
-      // the two warps of a lane group see the same rows and scale one half each.
-      if (__any_sync(0xffffffffu, rescale && j > 0)) {
-        if (!mbar_wait_warp(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1)) {
+      exp_half(std::integral_constant<int, 0>{});
+      exp_half(std::integral_constant<int, 1>{});
+      float a0, a1, b0, b1;
+      f2split(acc[0], a0, a1);
+      f2split(acc[1], b0, b1);
+      l = l * alpha + ((a0 + a1) + (b0 + b1));
+      // O_g holds the sum over this group's earlier blocks; tcgen05.ld/st are
+      // warp-collective, so the whole warp rescales when any of its rows must
+      // (alpha = 1 for the others), after the previous P V into O_g is done.
+      if (__any_sync(0xffffffffu, rescale && j >= 2)) {
+        if (!mbar_wait_warp(&pv_done[g], ((j - 2) >> 1) & 1)) {
           site = 900 + min(j, 99);
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t v[32];
-          const uint32_t ta = tO + lane_off + hf * (HD / 2) + c * 32;
-          tmem_ld_32x32b_x32(ta, v);
+          tmem_ld_32x32b_x32(tOg + c * 32, v);
           tmem_wait_ld_regs(v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st_32x32b_x32(ta, v);
+          tmem_st_32x32b_x32(tOg + c * 32, v);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&p_full[j & 1]);
+      mbar_arrive_warp(&p_full[g]);
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !mbar_wait_warp(o_full, 0)) {
       site = 999;
       ok = false;
     }
-    // the two halves of each row sum meet in shared memory
+    // The two groups' (m, l) meet in shared memory (the K ring is free once
+    // every MMA is done); each group then writes half of the output columns.
+    float* sML = reinterpret_cast<float*>(sK);  // [2 groups][m, l][128 rows]
     if (ok) {
-      sL[hf * 128 + r] = l;
-      mbar_arrive_warp(l_ready);
-      if (!mbar_wait_warp(l_ready, 0)) {
+      sML[g * 256 + r] = m;
+      sML[g * 256 + 128 + r] = l;
+      mbar_arrive_warp(ml_ready);
+      if (!mbar_wait_warp(ml_ready, 0)) {
         site = 998;
         ok = false;
       }
     }
     if (ok) {
       tc_fence_after();
-      const float lt = sL[r] + sL[128 + r];
+      const float m0 = sML[r], l0 = sML[128 + r], m1 = sML[256 + r], l1 = sML[384 + r];
+      const float mm = fmaxf(m0, m1);
+      // a group that saw no key of this row (or no block at all) contributes nothing
+      const float c0 = (m0 == -INFINITY) ? 0.f : ex2_approx((m0 - mm) * p.sl2);
+      const float c1 = (m1 == -INFINITY) ? 0.f : ex2_approx((m1 - mm) * p.sl2);
+      const float lt = l0 * c0 + l1 * c1;
       const float inv = 1.f / lt;
+      const float w0 = c0 * inv, w1 = c1 * inv;
       const bool valid = qrow < S;
-      bf16* dst = p.o + (long)(row0 + qrow) * p.ldo + (long)h * HD + hf * (HD / 2);
+      bf16* dst = p.o + (long)(row0 + qrow) * p.ldo + (long)h * HD + g * (HD / 2);
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tO + lane_off + hf * (HD / 2) + c * 32, v);
-        tmem_wait_ld_regs(v);
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32(tO(0) + lane_off + g * (HD / 2) + c * 32, va);
+        tmem_ld_32x32b_x32(tO(1) + lane_off + g * (HD / 2) + c * 32, vb);
+        tmem_wait_ld_regs(va);
+        tmem_wait_ld_regs(vb);
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          // select, not multiply: an O accumulator that was never written holds garbage
+          const float o0 = __uint_as_float(va[e]) * w0;
+          f[e] = (c1 != 0.f) ? fmaf(__uint_as_float(vb[e]), w1, o0) : o0;
+        }
         if (valid) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float* f = reinterpret_cast<const float*>(v + q * 8);
-            d4[q] = make_uint4(pack2bf(f[0] * inv, f[1] * inv), pack2bf(f[2] * inv, f[3] * inv),
-                               pack2bf(f[4] * inv, f[5] * inv), pack2bf(f[6] * inv, f[7] * inv));
-          }
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack2bf(f[8 * q], f[8 * q + 1]), pack2bf(f[8 * q + 2], f[8 * q + 3]),
+                               pack2bf(f[8 * q + 4], f[8 * q + 5]), pack2bf(f[8 * q + 6], f[8 * q + 7]));
         }
       }
-      if (valid && hf == 0) p.lse[((long)b * p.Hq + h) * S + qrow] = m * (p.sl2 * kLn2F) + logf(lt);
+      if (valid && g == 0) p.lse[((long)b * p.Hq + h) * S + qrow] = mm * (p.sl2 * kLn2F) + logf(lt);
     } else {
       set_status(p.status, kStatusAttnFwdTimeout * 1000 + site);
       abort_flag = 1;

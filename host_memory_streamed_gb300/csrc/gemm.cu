@@ -45,7 +45,9 @@ constexpr int B_STAGE = BN * BK * 2;  // 32 KB
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;  // two FP32 accumulators
 constexpr int GROUP_M = 16;        // tile raster: 16 M-tiles share each B panel
-constexpr int SMEM_USED = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/;
+// Per epilogue warp a 32 x 33 float block for transposing an accumulator chunk.
+constexpr int XPOSE_BYTES = 4 * 32 * 33 * 4;
+constexpr int SMEM_USED = STAGES * (A_STAGE + B_STAGE) + 1024 /*align*/ + 256 /*barriers*/ + XPOSE_BYTES;
 // Launch with the whole 227 KB (one CTA per SM either way); the unused tail
 // keeps every tensor-core read of the last stage inside the allocation.
 constexpr int SMEM_BYTES = 232448 - 256;  // 227 KB less room for the static shared variables
@@ -63,7 +65,7 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_STAGE = PHALF * BK * 2;  // 16 KB
 constexpr int P_B_STAGE = PHALF * BK * 2;  // 16 KB
 constexpr int P_GROUP_M = 8;           // pair-tile raster: 8 M-tiles share each B panel
-constexpr int P_SMEM_USED = P_STAGES * (P_A_STAGE + P_B_STAGE) + 1024 + 256;
+constexpr int P_SMEM_USED = P_STAGES * (P_A_STAGE + P_B_STAGE) + 1024 + 256 + XPOSE_BYTES;
 static_assert(P_SMEM_USED <= SMEM_BYTES, "pair shared memory plan exceeds 227 KB");
 
 struct EpiParams {
@@ -115,7 +117,9 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v
       d[q] = w;
     }
   } else {
-    for (int j = 0; j < ncols_valid; ++j) dst[j] = __float2bfloat16_rn(v[j]);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)  // constant indices keep v in registers
+      if (j < ncols_valid) dst[j] = __float2bfloat16_rn(v[j]);
   }
 }
 
@@ -141,7 +145,9 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
           v[q * 8 + 6] += bf16_lo(w.w); v[q * 8 + 7] += bf16_hi(w.w);
         }
       } else {
-        for (int j = 0; j < nvalid; ++j) v[j] += __bfloat162float(r[j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) v[j] += __bfloat162float(r[j]);
       }
       store_bf16x32(reinterpret_cast<__nv_bfloat16*>(p.C) + (long)row * p.ldc + col0, v, nvalid);
       break;
@@ -153,7 +159,9 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
 #pragma unroll
         for (int q = 0; q < 8; ++q) c4[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
       } else {
-        for (int j = 0; j < nvalid; ++j) c[j] = v[j];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) c[j] = v[j];
       }
       break;
     }
@@ -167,7 +175,9 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
           c4[q] = make_float4(o.x + v[q * 4], o.y + v[q * 4 + 1], o.z + v[q * 4 + 2], o.w + v[q * 4 + 3]);
         }
       } else {
-        for (int j = 0; j < nvalid; ++j) c[j] += v[j];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) c[j] += v[j];
       }
       break;
     }
@@ -194,42 +204,9 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
           d[q] = w;
         }
       } else {
-        for (int j = 0; j < na; ++j) dst[j] = __float2bfloat16_rn(a[j]);
-      }
-      break;
-    }
-    case kEpiSwiGLUBwd: {
-      // v = da[row, col0 .. col0 + 31] (FP32); (gate, up) pairs from R; (dgate, dup) pairs to C.
-      const __nv_bfloat16* g = p.R + (long)row * p.ldr + 2 * col0;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + (long)row * p.ldc + 2 * col0;
-      auto grad = [](float da, float gt, float up, float& dg, float& du) {
-        const float sg = 1.0f / (1.0f + __expf(-gt));
-        dg = da * up * sg * (1.0f + gt * (1.0f - sg));
-        du = da * gt * sg;
-      };
-      if (nvalid >= 32) {
-        const uint4* g4 = reinterpret_cast<const uint4*>(g);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // 4 (gate, up) pairs per 16 bytes
-          const uint4 w = g4[q];
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float dg, du;
-            grad(v[q * 4 + e], bf16_lo(ws[e]), bf16_hi(ws[e]), dg, du);
-            o[e] = pack_bf16(dg, du);
-          }
-          d4[q] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      } else {
-        for (int j = 0; j < nvalid; ++j) {
-          float dg, du;
-          grad(v[j], __bfloat162float(g[2 * j]), __bfloat162float(g[2 * j + 1]), dg, du);
-          dst[2 * j] = __float2bfloat16_rn(dg);
-          dst[2 * j + 1] = __float2bfloat16_rn(du);
-        }
+        for (int j = 0; j < 16; ++j)
+          if (j < na) dst[j] = __float2bfloat16_rn(a[j]);
       }
       break;
     }
@@ -241,8 +218,68 @@ __device__ __forceinline__ void epilogue_chunk(const EpiParams& p, int row, int 
 // Epilogue of one output tile: thread `row` of the tile reads its TMEM lane
 // (tbase already points at lane quarter*32, accumulator column 0), applies the
 // epilogue mode and stores columns tn*BN .. tn*BN + BN - 1.
-__device__ __forceinline__ void store_tile(const EpiParams& p, uint32_t tbase, int row, int tn) {
-  if (p.mode == kEpiRope && tn * BN < p.rope_cols) {
+__device__ __forceinline__ void store_tile(const EpiParams& p, uint32_t tbase, int row, int tn, float* xpose) {
+  if (p.mode == kEpiSwiGLUBwd) {
+    // One row per thread does not coalesce: each lane would read its row's
+    // gate/up pairs and write dgate/dup 64 KB away from its neighbours'.  The
+    // warp's 32 x 32 block of da goes through shared memory (row stride 33
+    // floats: conflict-free both ways) and comes back as 4 consecutive
+    // columns of one row per lane, so 8 lanes cover 128 contiguous bytes of
+    // R and of C.  All eight loads of a chunk are issued before any use.
+    const int lane = threadIdx.x & 31;
+    const int row0 = row - lane;
+    const int sub = lane & 7;
+    auto grad = [](float da, float gt, float up, float& dg, float& du) {
+      const float sg = 1.0f / (1.0f + __expf(-gt));
+      dg = da * up * sg * (1.0f + gt * (1.0f - sg));
+      du = da * gt * sg;
+    };
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tbase + c * 32, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xpose[lane * 33 + e] = __uint_as_float(r[e]);
+      __syncwarp();
+      const int col = tn * BN + c * 32 + 4 * sub;  // this lane's first da column
+      const int nv = min(4, p.N - col);
+      uint4 g[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int grow = row0 + 4 * i + (lane >> 3);
+        g[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (grow < p.M && nv == 4) g[i] = *reinterpret_cast<const uint4*>(p.R + (long)grow * p.ldr + 2 * col);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3);
+        const int grow = row0 + rr;
+        if (grow >= p.M || nv <= 0) continue;
+        const float* dav = xpose + rr * 33 + 4 * sub;
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + (long)grow * p.ldc + 2 * col;
+        if (nv == 4) {
+          const uint32_t ws[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float dg, du;
+            grad(dav[e], bf16_lo(ws[e]), bf16_hi(ws[e]), dg, du);
+            o[e] = pack_bf16(dg, du);
+          }
+          *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          const __nv_bfloat16* gp = p.R + (long)grow * p.ldr + 2 * col;
+          for (int e = 0; e < nv; ++e) {
+            float dg, du;
+            grad(dav[e], __bfloat162float(gp[2 * e]), __bfloat162float(gp[2 * e + 1]), dg, du);
+            dst[2 * e] = __float2bfloat16_rn(dg);
+            dst[2 * e + 1] = __float2bfloat16_rn(du);
+          }
+        }
+      }
+      __syncwarp();  // the next chunk overwrites this warp's block
+    }
+  } else if (p.mode == kEpiRope && tn * BN < p.rope_cols) {
     // rotate-half RoPE: columns j and j + hd/2 of each head form a pair.
     // The row's cos/sin for frequencies j .. j+31 are loaded once (16-byte
     // loads) and serve every head of the tile.
@@ -443,6 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // Epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31.
     const int quarter = warp & 3;
+    float* xpose = reinterpret_cast<float*>(sB + STAGES * B_STAGE + 256) + (warp - 2) * 32 * 33;
     const int row_in_tile = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -457,7 +495,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int row = tm * BM + row_in_tile;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      store_tile(p, tbase, row, tn);
+      store_tile(p, tbase, row, tn, xpose);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -632,6 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     const int quarter = warp & 3;
     const int row_in_tile = (int)rank * PHALF + quarter * 32 + lane;
+    float* xpose = reinterpret_cast<float*>(sB + P_STAGES * P_B_STAGE + 256) + (warp - 2) * 32 * 33;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cluster; tile < num_tiles; tile += num_clusters) {
@@ -643,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      store_tile(p, tbase, tm * PM + row_in_tile, tn);
+      store_tile(p, tbase, tm * PM + row_in_tile, tn, xpose);
       tc_fence_before();
       if (leader)
         mbar_arrive_warp(&tempty[acc]);

@@ -152,7 +152,7 @@ std::vector<Visit> build_schedule(int L, int K, bool store_acts, bool single_buf
   v.push_back({kEmbedBwd, 0, -1});
   // buffer assignment with residency reuse
   int held[2] = {-1, -1}, last_user[2] = {-1, -1}, prev_buf = 1;
-  int glast[2] = {-1, -1}, gnext = 0;
+  int glast[3] = {-1, -1, -1}, gnext = 0;
   for (int i = 0; i < (int)v.size(); ++i) {
     Visit& x = v[i];
     if (x.kind != kEmbedBwd) {
@@ -171,10 +171,15 @@ std::vector<Visit> build_schedule(int L, int K, bool store_acts, bool single_buf
     }
     x.grads = (x.kind == kHead || x.kind == kLayerBwd || x.kind == kEmbedBwd);
     if (x.grads) {
-      x.gbuf = gnext;
-      x.prev_gbuf_user = glast[gnext];
-      glast[gnext] = i;
-      gnext ^= 1;
+      // Layers alternate between gradient buffers 0 and 1; the head (its
+      // gradient is several layers' worth and takes that long to leave) and
+      // the compact embedding rows use buffer 2, so no layer waits for the
+      // head's gradient to be evacuated.
+      const int g = x.kind == kLayerBwd ? gnext : 2;
+      x.gbuf = g;
+      x.prev_gbuf_user = glast[g];
+      glast[g] = i;
+      if (x.kind == kLayerBwd) gnext ^= 1;
     }
   }
   return v;
@@ -295,6 +300,7 @@ struct mt_model {
   int K = 1;
   bool resident_mode = false, store_acts = false, single_buffer = false, debug = false, time_kernels = false;
   bool trace = false;
+  bool visit_log = false;
   bool undrained = false;
   std::vector<mt::TileLayout> layouts;  // per tile
   std::vector<uint8_t*> tiles;
@@ -309,7 +315,8 @@ struct mt_model {
   int64_t arena_used = 0;
   cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
   uint8_t* wbuf[2] = {nullptr, nullptr};
-  uint8_t* gbuf[2] = {nullptr, nullptr};
+  uint8_t* gbuf[3] = {nullptr, nullptr, nullptr};  // layers alternate 0/1; head and embedding rows use 2
+  int64_t gbuf_bytes[3] = {0, 0, 0};
   uint8_t* resident = nullptr;
   std::vector<int64_t> resident_off;
   std::vector<mt::bf16*> ckpt, blockbuf;
@@ -347,6 +354,7 @@ struct mt_model {
   std::mutex mu;
   std::condition_variable cv;
   std::vector<char> rec_ready, rec_free, rec_d2h, rec_h2d_timed, rec_d2h_timed, rec_wait_timed;
+  std::vector<double> host_wait_ready_ms, host_wait_gbuf_ms;  // compute thread's waits per visit (MT_VISIT_LOG)
   std::atomic<bool> abort_flag{false};
   std::atomic<bool> nonfinite{false};
   std::atomic<int> worker_code{0};
@@ -857,6 +865,8 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       std::fill(m->rec_h2d_timed.begin(), m->rec_h2d_timed.end(), 0);
       std::fill(m->rec_d2h_timed.begin(), m->rec_d2h_timed.end(), 0);
       std::fill(m->rec_wait_timed.begin(), m->rec_wait_timed.end(), 0);
+      std::fill(m->host_wait_ready_ms.begin(), m->host_wait_ready_ms.end(), 0.0);
+      std::fill(m->host_wait_gbuf_ms.begin(), m->host_wait_gbuf_ms.end(), 0.0);
       m->abort_flag = false;
       m->worker_code = 0;
       m->worker_msg.clear();
@@ -916,7 +926,9 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
           wb = m->resident + m->resident_off[x.tile];
         } else {
           if (x.h2d) {
+            const auto tw = Clock::now();
             wait_flag(m, m->rec_ready, v, "weights ready");
+            m->host_wait_ready_ms[v] = ms_since(tw);
             MT_CK(cudaEventRecord(m->ev_wait_a[v], m->s_comp));
             MT_CK(cudaStreamWaitEvent(m->s_comp, m->ev_ready[v], 0));
             MT_CK(cudaEventRecord(m->ev_wait_b[v], m->s_comp));
@@ -928,7 +940,9 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       uint8_t* gb = nullptr;
       if (x.grads) {
         if (x.prev_gbuf_user >= 0) {
+          const auto tw = Clock::now();
           wait_flag(m, m->rec_d2h, x.prev_gbuf_user, "gradient buffer evacuated");
+          m->host_wait_gbuf_ms[v] = ms_since(tw);
           MT_CK(cudaStreamWaitEvent(m->s_comp, m->ev_d2h[x.prev_gbuf_user], 0));
         }
         gb = m->gbuf[x.gbuf];
@@ -1045,7 +1059,25 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       if (m->rec_d2h_timed[v] && cudaEventElapsedTime(&f, m->ev_d2h_a[v], m->ev_d2h_b[v]) == cudaSuccess) st.d2h_ms += f;
       if (m->rec_wait_timed[v] && cudaEventElapsedTime(&f, m->ev_wait_a[v], m->ev_wait_b[v]) == cudaSuccess)
         st.wait_weights_ms += f;
-      if (v > 0 && cudaEventElapsedTime(&f, m->ev_vis_b[v - 1], m->ev_vis_a[v]) == cudaSuccess) st.visit_gap_ms += f;
+      float gap = 0.f;
+      if (v > 0 && cudaEventElapsedTime(&gap, m->ev_vis_b[v - 1], m->ev_vis_a[v]) == cudaSuccess) st.visit_gap_ms += gap;
+      if (m->visit_log) {
+        static const char* kind_name[] = {"embed_fwd", "layer_fwd", "head", "recompute", "layer_bwd", "embed_bwd"};
+        float run = 0.f, ww = 0.f, end = 0.f, d2h_a = -1.f, d2h_b = -1.f;
+        cudaEventElapsedTime(&run, m->ev_vis_a[v], m->ev_vis_b[v]);
+        cudaEventElapsedTime(&end, m->ev_t0, m->ev_vis_b[v]);
+        if (m->rec_wait_timed[v]) cudaEventElapsedTime(&ww, m->ev_wait_a[v], m->ev_wait_b[v]);
+        if (m->rec_d2h_timed[v]) {
+          cudaEventElapsedTime(&d2h_a, m->ev_t0, m->ev_d2h_a[v]);
+          cudaEventElapsedTime(&d2h_b, m->ev_t0, m->ev_d2h_b[v]);
+        }
+        std::fprintf(stderr,
+                     "[mt visit] %3d %-9s layer %3d  gap %7.3f ms  run %8.3f ms  stream wait weights %7.3f ms  "
+                     "host wait weights %7.3f ms  host wait grad buffer %7.3f ms  ends at %8.2f ms  "
+                     "gradient copy %8.2f .. %8.2f ms\n",
+                     v, kind_name[m->visits[v].kind], m->visits[v].layer, gap, run, ww, m->host_wait_ready_ms[v],
+                     m->host_wait_gbuf_ms[v], end, d2h_a, d2h_b);
+      }
       const Visit& x = m->visits[v];
       if (x.h2d && !m->resident_mode) st.h2d_bytes += m->layouts[x.tile].w_bytes;
       if (x.grads) st.d2h_bytes += x.kind == kEmbedBwd ? 2LL * m->emb_u * D.d : m->layouts[x.tile].w_bytes;
@@ -1091,6 +1123,10 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     };
     st.host_pre_ms = span(wall0, t_ev0);
     st.tail_grads_ms = span(t_compute_done, t_grads_done);
+    if (m->visit_log)
+      std::fprintf(stderr, "[mt visit] compute stream ends at %8.2f ms; host: all gradients accumulated %.2f ms "
+                           "and Adam done %.2f ms after the compute stream was seen finished\n",
+                   st.gpu_compute_ms, st.tail_grads_ms, span(t_compute_done, adam_end));
     st.tail_adam_ms = span(t_grads_done, adam_end);
     st.tail_rest_ms = span(adam_end, Clock::now());
     if (loss_out) *loss_out = m->pinned_scalars[0];
@@ -1159,7 +1195,7 @@ int64_t plan_arena(mt_model* m, uint8_t* base) {
   };
   const int64_t xb = D.T * D.d * 2;
   for (int b = 0; b < 2; ++b) m->wbuf[b] = at(m->max_w_bytes);
-  for (int b = 0; b < 2; ++b) m->gbuf[b] = at(m->max_w_bytes);
+  for (int b = 0; b < 3; ++b) m->gbuf[b] = at(m->gbuf_bytes[b]);
   if (m->resident_mode) {
     int64_t tot = 0;
     m->resident_off.assign(m->layouts.size(), 0);
@@ -1201,6 +1237,11 @@ void build_layouts(mt_model* m) {
   m->layouts.push_back(make_layout(kTileHead, m->D));
   m->max_w_bytes = 0;
   for (const auto& l : m->layouts) m->max_w_bytes = std::max(m->max_w_bytes, l.w_bytes);
+  int64_t layer_bytes = 0;
+  for (int i = 1; i <= m->D.L; ++i) layer_bytes = std::max(layer_bytes, m->layouts[i].w_bytes);
+  m->gbuf_bytes[0] = m->gbuf_bytes[1] = layer_bytes;
+  m->gbuf_bytes[2] =
+      std::max<int64_t>(m->layouts[m->D.L + 1].w_bytes, std::min<int64_t>(m->D.T, m->D.V) * 2LL * m->D.d);
 }
 
 void parallel_zero(uint8_t* p, int64_t n, int nthreads) {
@@ -1283,6 +1324,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->debug = m->cfg.flags & MT_DEBUG_CHECKS;
   m->time_kernels = m->cfg.flags & MT_TIME_KERNELS;
   m->trace = m->cfg.flags & MT_TRACE;
+  m->visit_log = m->cfg.flags & MT_VISIT_LOG;
   if (!sc || !sh || !sd || sc == sh || sc == sd || sh == sd)
     throw MtError{MT_EINVAL, "three distinct CUDA streams are required"};
   MT_CK(cudaGetDevice(&m->device));
@@ -1334,6 +1376,8 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->rec_h2d_timed.assign(nv, 0);
   m->rec_d2h_timed.assign(nv, 0);
   m->rec_wait_timed.assign(nv, 0);
+  m->host_wait_ready_ms.assign(nv, 0.0);
+  m->host_wait_gbuf_ms.assign(nv, 0.0);
 
   // host tiles: pageable, page aligned, zeroed (first touch spread over threads)
   m->tiles.assign(m->layouts.size(), nullptr);
@@ -1376,8 +1420,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
     MT_CK(cudaMemcpy(m->ws.rope_sin, s.data(), s.size() * 4, cudaMemcpyHostToDevice));
   }
   // zero the gradient buffers once (alignment padding is never written)
-  MT_CK(cudaMemset(m->gbuf[0], 0, (size_t)m->max_w_bytes));
-  MT_CK(cudaMemset(m->gbuf[1], 0, (size_t)m->max_w_bytes));
+  for (int b = 0; b < 3; ++b) MT_CK(cudaMemset(m->gbuf[b], 0, (size_t)m->gbuf_bytes[b]));
   MT_CK(cudaDeviceSynchronize());
 
   // Adam is background work for the step (it only has to finish by its end);

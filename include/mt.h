@@ -79,9 +79,12 @@ enum {
   MT_NO_DOUBLE_BUFFER = 1u << 2,  /* one device weight buffer: no H2D/compute overlap (ablation) */
   MT_DEBUG_CHECKS = 1u << 3,      /* NaN/Inf scan of every gradient tile; host event-order asserts */
   MT_TIME_KERNELS = 1u << 4,      /* CUDA-event timing of every GEMM launch (mt_get_step_stats) */
-  MT_TRACE = 1u << 5              /* debugging: wait for every visit (layer pass) to finish, print its kind,
+  MT_TRACE = 1u << 5,             /* debugging: wait for every visit (layer pass) to finish, print its kind,
                                      layer, time and the device status word to stderr, stop at the first
                                      nonzero status */
+  MT_VISIT_LOG = 1u << 6          /* after each step print one line per visit to stderr: the compute-stream
+                                     gap before it, its compute-stream time, and how long the stream and the
+                                     issuing host thread waited for its weights and its gradient buffer */
 };
 
 /* Tile parts for load/get. */

@@ -156,3 +156,4 @@ def test_chunked_mlp_shrinks_the_device_arena(lib):
     chunked = lib.mt_required_device_bytes(C.byref(_cfg(s, mlp_chunk_rows=65536)))
     assert chunked > 0 and whole - chunked > 40e9
     assert chunked < 240e9
+
