@@ -1174,9 +1174,12 @@ const char* validate(const mt_config& c) {
 
 mt_config with_defaults(const mt_config& in) {
   mt_config c = in;
-  if (c.n_adam_threads <= 0) c.n_adam_threads = std::max(1u, std::thread::hardware_concurrency());
+  // Adam is bound by host memory bandwidth well before every core is busy;
+  // three quarters of the hardware threads leave cores and bandwidth to the
+  // packers and the gradient accumulator.
+  if (c.n_adam_threads <= 0) c.n_adam_threads = std::max(1u, std::thread::hardware_concurrency() * 3 / 4);
   if (c.n_pack_threads <= 0) c.n_pack_threads = 8;
-  if (c.n_grad_slabs <= 0) c.n_grad_slabs = 12;
+  if (c.n_grad_slabs <= 0) c.n_grad_slabs = 24;  // 1.5 GiB pinned at 64 MiB: absorbs the LM head's gradient burst
   if (c.grad_slab_bytes <= 0) c.grad_slab_bytes = 64ll << 20;
   if (c.stage_bytes <= 0) c.stage_bytes = 64ll << 20;
   if (c.timeout_ms <= 0) c.timeout_ms = 60000;

@@ -96,9 +96,9 @@ typedef struct {
   int32_t batch, seq;        /* tokens per step = batch * seq */
   int32_t ckpt_every;        /* K: keep the input of every K-th layer; recompute inside blocks of K */
   float lr, beta1, beta2, adam_eps, weight_decay;
-  int32_t n_adam_threads;    /* CPU Adam workers (0 = hardware threads) */
+  int32_t n_adam_threads;    /* CPU Adam workers (0 = 3/4 of the hardware threads) */
   int32_t n_pack_threads;    /* CPU threads copying pageable tiles into pinned staging (0 = 8) */
-  int32_t n_grad_slabs;      /* pinned gradient slabs (0 = 12) */
+  int32_t n_grad_slabs;      /* pinned gradient slabs (0 = 24) */
   int64_t grad_slab_bytes;   /* bytes per gradient slab (0 = 64 MiB) */
   int64_t stage_bytes;       /* bytes per pinned H2D staging chunk (0 = 64 MiB); two chunks ping-pong */
   int64_t timeout_ms;        /* bound of every host wait (0 = 60000) */
