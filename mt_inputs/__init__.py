@@ -143,6 +143,12 @@ def model_weights(s: ModelShape, gain_jitter: float = 0.0) -> dict:
     }
 
 
+def tied(params: dict) -> dict:
+    """The same weights with the LM head tied to the embedding: ``head`` keeps
+    only the final norm gain and the embedding E serves as the head's weight."""
+    return {"embed": params["embed"], "layers": params["layers"], "head": {"gf": params["head"]["gf"]}}
+
+
 def step_tokens(s: ModelShape, step: int) -> torch.Tensor:
     """int32 [B, S+1] uniform token ids for training step ``step`` (1-based)."""
     gen = torch.Generator().manual_seed(2000 + step)

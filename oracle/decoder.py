@@ -12,7 +12,8 @@ paper summary (paperlayer.ai), §3 "Execution workflow"; hyper.ai summary,
 方法 "Method" ¶2):
 
 * a Llama-style decoder (RMSNorm, rotate-half RoPE, causal GQA attention,
-  SwiGLU MLP, untied embedding and LM head, no biases) on token ids
+  SwiGLU MLP, no biases; embedding and LM head untied, or tied: one matrix
+  used for both, see ``head_weight``) on token ids
   ``tokens[B, S+1]``; inputs ``tokens[:, :S]``, targets ``tokens[:, 1:]``;
 * the mean next-token cross-entropy over the B*S targets;
 * its gradient with respect to every weight, written out by hand;
@@ -61,6 +62,7 @@ __all__ = [
     "layer_backward",
     "layer_tail_rows",
     "head_loss_and_backward",
+    "head_weight",
     "model_forward_loss",
     "model_loss_and_grads",
     "adam_update",
@@ -473,6 +475,15 @@ def head_loss_and_backward(x, hw, tgt, cfg: OracleConfig):
 # Whole model
 # ----------------------------------------------------------------------------
 
+def head_weight(p):
+    """The LM head's weight: its own W_h, or the embedding E when the model ties
+    them (``params["head"]`` then holds only the final norm gain).  The pages'
+    host store keeps tied embedding and head states in one shared region
+    (paperlayer.ai summary §A.1, tied embeddings); mathematically the one
+    matrix E is used twice, as the token embedding and as W_h."""
+    return p["head"]["wh"] if "wh" in p["head"] else p["embed"]["E"]
+
+
 def _cast_params(params, dtype):
     return {
         "embed": {k: _f(v, dtype) for k, v in params["embed"].items()},
@@ -492,7 +503,7 @@ def model_forward_loss(params, tokens, cfg: OracleConfig, dtype=torch.float64):
     for lw in p["layers"]:
         x, _ = layer_forward(x, lw, cfg, cos, sin)
     nf, _ = rms_norm(x, p["head"]["gf"], cfg.rms_eps)
-    z = nf.reshape(-1, cfg.d_model) @ p["head"]["wh"].T
+    z = nf.reshape(-1, cfg.d_model) @ head_weight(p).T
     y = tgt.reshape(-1)
     return float((torch.logsumexp(z, dim=-1) - z.gather(1, y[:, None])[:, 0]).mean())
 
@@ -513,12 +524,15 @@ def model_loss_and_grads(params, tokens, cfg: OracleConfig, dtype=torch.float64)
     for lw in p["layers"]:
         x, c = layer_forward(x, lw, cfg, cos, sin)
         caches.append(c)
-    loss, dx, head_g = head_loss_and_backward(x, p["head"], tgt, cfg)
+    tied = "wh" not in p["head"]
+    loss, dx, head_g = head_loss_and_backward(x, {"gf": p["head"]["gf"], "wh": head_weight(p)}, tgt, cfg)
     layer_g = [None] * len(p["layers"])
     for i in reversed(range(len(p["layers"]))):
         dx, layer_g[i] = layer_backward(dx, caches[i], p["layers"][i], cfg, cos, sin)
     dE = torch.zeros_like(p["embed"]["E"])
     dE.index_add_(0, inp.reshape(-1), dx.reshape(-1, cfg.d_model))
+    if tied:  # E is used twice: its gradient is the sum of both uses' (chain rule)
+        dE += head_g.pop("wh")
     grads = {"embed": {"E": dE}, "layers": layer_g, "head": head_g}
     return float(loss), grads
 

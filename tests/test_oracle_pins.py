@@ -326,6 +326,58 @@ def test_model_grads_match_autograd_of_library_forward(which):
         assert err < 1e-10, err
 
 
+@pytest.mark.parametrize("which", ["tiny", "gqa"])
+def test_tied_model_grads_match_autograd_of_library_forward(which):
+    """Tied embedding and LM head: autograd through the library's forward with
+    one leaf tensor used both as the embedding table and as the head weight
+    accumulates both uses into its gradient; the oracle's tied dE must match."""
+    s, cfg = _tiny() if which == "tiny" else _gqa_tiny()
+    params = mt_inputs.tied(mt_inputs.model_weights(s, gain_jitter=0.1))
+    tokens = mt_inputs.step_tokens(s, 2)
+    loss, grads = oracle.model_loss_and_grads(params, tokens, cfg)
+    assert set(grads["head"]) == {"gf"}
+    p = _as_f64(params, requires_grad=True)
+    ref = _library_model_loss(dict(p, head={"gf": p["head"]["gf"], "wh": p["embed"]["E"]}), tokens, cfg)
+    ref.backward()
+    assert abs(loss - float(ref.detach())) < 1e-12 * abs(loss)
+    pairs = [(grads["embed"]["E"], p["embed"]["E"]), (grads["head"]["gf"], p["head"]["gf"])]
+    for gl, pl in zip(grads["layers"], p["layers"]):
+        pairs += [(gl[k], pl[k]) for k in mt_inputs.LAYER_TENSORS]
+    for mine, theirs in pairs:
+        err = (mine - theirs.grad).norm() / theirs.grad.norm()
+        assert err < 1e-10, err
+    # the tied gradient of E is the untied embedding gradient plus the untied head gradient
+    untied = dict(params, head={"gf": params["head"]["gf"], "wh": params["embed"]["E"]})
+    _, gu = oracle.model_loss_and_grads(untied, tokens, cfg)
+    assert torch.allclose(grads["embed"]["E"], gu["embed"]["E"] + gu["head"]["wh"], rtol=0, atol=1e-14)
+
+
+def test_tied_model_grad_finite_differences():
+    """Central differences along random directions of (E, gf) in the tied model:
+    a perturbation of E moves both the embedding lookups and the logits."""
+    s, cfg = _tiny(n_layers=1, d_model=64, n_heads=2, n_kv_heads=1, head_dim=32, ffn=96, vocab=61, seq=12)
+    params = _as_f64(mt_inputs.tied(mt_inputs.model_weights(s, gain_jitter=0.1)))
+    tokens = mt_inputs.step_tokens(s, 4)
+    _, grads = oracle.model_loss_and_grads(params, tokens, cfg)
+    gen = torch.Generator().manual_seed(13)
+    for trial in range(3):
+        uE = torch.randn(params["embed"]["E"].shape, generator=gen, dtype=D)
+        ug = torch.randn(params["head"]["gf"].shape, generator=gen, dtype=D)
+        nrm = math.sqrt(float((uE * uE).sum() + (ug * ug).sum()))
+        uE, ug = uE / nrm, ug / nrm
+        h = 1e-5
+
+        def at(sign):
+            q = _as_f64(params)
+            q["embed"]["E"].add_(sign * h * uE)
+            q["head"]["gf"].add_(sign * h * ug)
+            return oracle.model_forward_loss(q, tokens, cfg)
+
+        fd = (at(1) - at(-1)) / (2 * h)
+        an = float((grads["embed"]["E"] * uE).sum() + (grads["head"]["gf"] * ug).sum())
+        assert abs(fd - an) <= 1e-6 * abs(an) + 1e-11, (fd, an)
+
+
 def test_model_grad_finite_differences():
     """Central differences of the oracle's own forward, in FP64.
 
