@@ -14,11 +14,12 @@ import torch
 
 from . import _lib
 from ._lib import (MT_DEBUG_CHECKS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V, MT_PART_W,
-                   MT_RESIDENT, MT_STORE_ACTS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG, ERROR_NAMES)
+                   MT_RESIDENT, MT_STORE_ACTS, MT_TIE_EMBEDDINGS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG,
+                   ERROR_NAMES)
 
 __all__ = ["StreamedDecoder", "MtError", "ops", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
-           "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_VISIT_LOG", "MT_PART_W", "MT_PART_G", "MT_PART_M",
-           "MT_PART_V"]
+           "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_VISIT_LOG", "MT_TIE_EMBEDDINGS", "MT_PART_W",
+           "MT_PART_G", "MT_PART_M", "MT_PART_V"]
 
 LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
 
@@ -68,6 +69,8 @@ class StreamedDecoder:
         self._h = h
         self.n_tiles = self._L.mt_tile_count(h)
         self.infos = [self.tile_info(i) for i in range(self.n_tiles)]
+        # tied embeddings: tile 0 holds E and gf, and there is no head tile
+        self.tied = bool(flags & MT_TIE_EMBEDDINGS)
 
     @staticmethod
     def required_device_bytes(s, **kw) -> int:
@@ -135,7 +138,7 @@ class StreamedDecoder:
     def _named_to_slots(self, i, named):
         kind = self.infos[i]["kind"]
         if kind == 0:
-            return {"E": named["E"]}
+            return {"E": named["E"], "gf": named["gf"]} if self.tied else {"E": named["E"]}
         if kind == 2:
             return {"gf": named["gf"], "wh": named["wh"]}
         wgu = torch.stack([named["wg"], named["wu"]], dim=1).reshape(-1, named["wg"].shape[1])
@@ -174,13 +177,14 @@ class StreamedDecoder:
 
     def _tile_named(self, params, i):
         if i == 0:
-            return params["embed"]
-        if i == self.n_tiles - 1:
+            return dict(params["embed"], gf=params["head"]["gf"]) if self.tied else params["embed"]
+        if i == self.n_tiles - 1 and not self.tied:
             return params["head"]
         return params["layers"][i - 1]
 
     def load_weights(self, params):
-        """params: {'embed': {'E'}, 'layers': [{g1,wq,...}], 'head': {'gf','wh'}} of BF16 tensors."""
+        """params: {'embed': {'E'}, 'layers': [{g1,wq,...}], 'head': {'gf','wh'}} of BF16 tensors
+        ('head': {'gf'} alone with tied embeddings)."""
         for i in range(self.n_tiles):
             self.load_tile(i, MT_PART_W, self.pack(i, self._tile_named(params, i)))
 
@@ -189,8 +193,10 @@ class StreamedDecoder:
         for i in range(self.n_tiles):
             named = self.unpack(i, self.get_tile(i, part), dtype)
             if i == 0:
+                if self.tied:
+                    out["head"] = {"gf": named.pop("gf")}
                 out["embed"] = named
-            elif i == self.n_tiles - 1:
+            elif i == self.n_tiles - 1 and not self.tied:
                 out["head"] = named
             else:
                 out["layers"].append(named)

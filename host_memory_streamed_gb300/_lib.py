@@ -14,8 +14,8 @@ MT_OK, MT_EINVAL, MT_ENOMEM, MT_ECUDA, MT_ETIMEDOUT, MT_ESTATE, MT_ENONFINITE, M
 ERROR_NAMES = {0: "MT_OK", -1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_ECUDA", -4: "MT_ETIMEDOUT",
                -5: "MT_ESTATE", -6: "MT_ENONFINITE", -7: "MT_EINTERNAL"}
 
-MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG = \
-    1, 2, 4, 8, 16, 32, 64
+MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG, \
+    MT_TIE_EMBEDDINGS = 1, 2, 4, 8, 16, 32, 64, 128
 MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
 EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE, EPI_SWIGLU_BWD = range(7)

@@ -23,6 +23,12 @@ const TensorSlot& TileLayout::slot(const char* n) const {
   throw std::runtime_error(std::string("no tensor ") + n);
 }
 
+bool TileLayout::has(const char* n) const {
+  for (const auto& t : tensors)
+    if (t.name == n) return true;
+  return false;
+}
+
 Dims dims_of(const mt_config& c) {
   Dims d;
   d.L = c.n_layers;
@@ -41,7 +47,7 @@ Dims dims_of(const mt_config& c) {
   return d;
 }
 
-TileLayout make_layout(TileKind kind, const Dims& d) {
+TileLayout make_layout(TileKind kind, const Dims& d, bool tied) {
   TileLayout L;
   L.kind = kind;
   auto add = [&](const char* n, int64_t r, int64_t c) {
@@ -55,6 +61,7 @@ TileLayout make_layout(TileKind kind, const Dims& d) {
   };
   if (kind == kTileEmbed) {
     add("E", d.V, d.d);
+    if (tied) add("gf", d.d, 0);
   } else if (kind == kTileLayer) {
     add("g1", d.d, 0);
     add("wqkv", d.Dqkv, d.d);
@@ -89,7 +96,8 @@ LayerView bind_layer(const TileLayout& lay, void* base) {
 
 HeadView bind_head(const TileLayout& lay, void* base) {
   auto p = [&](const char* n) { return reinterpret_cast<bf16*>(static_cast<uint8_t*>(base) + lay.slot(n).offset); };
-  return HeadView{p("gf"), p("wh")};
+  // tied embeddings: the head's weight is the embedding table itself
+  return HeadView{p("gf"), lay.has("wh") ? p("wh") : p("E")};
 }
 
 // ------------------------------------------------------------------ template

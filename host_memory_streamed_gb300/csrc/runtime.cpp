@@ -137,11 +137,11 @@ struct Visit {
   int prev_gbuf_user = -1;
 };
 
-std::vector<Visit> build_schedule(int L, int K, bool store_acts, bool single_buffer) {
+std::vector<Visit> build_schedule(int L, int K, bool store_acts, bool single_buffer, int head_tile) {
   std::vector<Visit> v;
   v.push_back({kEmbedFwd, 0, -1});
   for (int i = 0; i < L; ++i) v.push_back({kLayerFwd, i + 1, i});
-  v.push_back({kHead, L + 1, -1});
+  v.push_back({kHead, head_tile, -1});
   const int nblk = (L + K - 1) / K;
   for (int b = nblk - 1; b >= 0; --b) {
     const int s = b * K, e = std::min(L, s + K);
@@ -301,6 +301,8 @@ struct mt_model {
   bool resident_mode = false, store_acts = false, single_buffer = false, debug = false, time_kernels = false;
   bool trace = false;
   bool visit_log = false;
+  bool tied = false;   // MT_TIE_EMBEDDINGS: the head's weight is tile 0's E
+  int head_tile = 0;   // tile the head visit streams (L + 1, or 0 when tied)
   bool undrained = false;
   std::vector<mt::TileLayout> layouts;  // per tile
   std::vector<uint8_t*> tiles;
@@ -641,10 +643,41 @@ void submit_untouched_embed(mt_model* m) {
   }
 }
 
+// Tied embeddings, once the head's gradient has landed in tile 0's G: Adam on
+// gf and on E's rows that no token of the step uses (their gradient is the
+// head's alone and is complete).  The other rows wait for their embedding
+// gradient (submit_adam_embed_rows).
+void submit_tied_head_adam(mt_model* m) {
+  const TileLayout& lay = m->layouts[0];
+  const TensorSlot& E = lay.slot("E");
+  const TensorSlot& gf = lay.slot("gf");
+  submit_adam_range(m, 0, gf.offset, 2 * gf.numel);
+  const int d = m->D.d, V = m->D.V;
+  uint8_t* base = m->tiles[0];
+  const int32_t* off = m->pinned_tok + 2 * m->D.T;  // emb_off [V + 1]
+  const AdamHyper h{m->cfg.lr, m->cfg.beta1, m->cfg.beta2, m->cfg.adam_eps, m->cfg.weight_decay, m->step + 1};
+  constexpr int kRowsPerTask = 64;
+  for (int v0 = 0; v0 < V; v0 += kRowsPerTask) {
+    const int v1 = std::min(V, v0 + kRowsPerTask);
+    m->adam_pool->submit([=] {
+      const auto t0 = Clock::now();
+      for (int v = v0; v < v1; ++v) {
+        if (off[v + 1] > off[v]) continue;
+        const int64_t e = (int64_t)v * d;
+        adam_range(reinterpret_cast<uint16_t*>(base + lay.off_w + E.offset) + e,
+                   reinterpret_cast<const uint16_t*>(base + lay.off_g + E.offset) + e,
+                   reinterpret_cast<float*>(base + lay.off_m + 2 * E.offset) + e,
+                   reinterpret_cast<float*>(base + lay.off_v + 2 * E.offset) + e, (size_t)d, h);
+      }
+      m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
+    });
+  }
+}
+
 // One slab of the compact embedding gradient: rows u0 .. u0 + nrows of the
 // step's token ids.  Scatter each row into the tile's G section and check it
 // is finite (accumulator pool); the rows' Adam then goes to the Adam pool.
-void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<bool>& fin) {
+void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<bool>& fin, bool add) {
   const TileLayout& lay = m->layouts[j.tile];
   const TensorSlot& E = lay.slot("E");
   const int d = m->D.d;
@@ -653,7 +686,6 @@ void accumulate_embed_rows(mt_model* m, const mt_model::AccJob& j, std::atomic<b
   const int32_t* rows = m->pinned_tok + 3 * m->D.T + m->D.V + 1;  // emb_rows
   uint8_t* base = m->tiles[j.tile];
   const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
-  const bool add = m->micro_index > 0;
   const int nt = m->acc_pool->size();
   const int64_t per = std::max<int64_t>(16, (nrows + nt - 1) / nt);
   for (int64_t a = 0; a < nrows; a += per) {
@@ -707,21 +739,26 @@ void accum_main(mt_model* m) {
     }
     try {
       wait_event(m, m->ev_slab[j.slab], "gradient slab copy");
-      if (m->visits[j.visit].kind == kHead && j.off == 0) {
+      const bool head = m->visits[j.visit].kind == kHead;
+      if (head && j.off == 0) {
         if (!std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
-        submit_untouched_embed(m);
+        if (!m->tied) submit_untouched_embed(m);
       }
       if (j.rows) {
         std::atomic<bool> fin{true};
-        accumulate_embed_rows(m, j, fin);
+        accumulate_embed_rows(m, j, fin, m->tied || m->micro_index > 0);
         if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
         if (!fin) m->nonfinite = true;
         if (!m->nonfinite && m->last_pass()) {
           if (m->micro_count == 1) {
             submit_adam_embed_rows(m, j.tile, j.off / (2LL * m->D.d), j.bytes / (2LL * m->D.d));
           } else if (j.last) {  // every row may have been touched by some micro-batch: one dense update
-            const TensorSlot& E = m->layouts[j.tile].slot("E");
-            submit_adam_range(m, j.tile, E.offset, 2 * E.numel);
+            if (m->tied) {  // E and gf: the whole tile
+              submit_adam_range(m, j.tile, 0, m->layouts[j.tile].w_bytes);
+            } else {
+              const TensorSlot& E = m->layouts[j.tile].slot("E");
+              submit_adam_range(m, j.tile, E.offset, 2 * E.numel);
+            }
           }
         }
         {
@@ -759,7 +796,15 @@ void accum_main(mt_model* m) {
         m->free_slabs.push_back(j.slab);
       }
       m->cv.notify_all();
-      if (!m->nonfinite && m->last_pass()) submit_adam_range(m, j.tile, j.off, j.bytes);
+      if (!m->nonfinite && m->last_pass()) {
+        if (!(head && m->tied)) {
+          submit_adam_range(m, j.tile, j.off, j.bytes);
+        } else if (j.last && m->micro_count == 1) {
+          // tied: E's rows wait for their embedding gradient unless no token
+          // of the step uses them; gf is complete with the head's gradient
+          submit_tied_head_adam(m);
+        }
+      }
       if (j.last) {
         {
           std::lock_guard<std::mutex> g(m->mu);
@@ -1235,16 +1280,18 @@ int64_t plan_arena(mt_model* m, uint8_t* base) {
 
 void build_layouts(mt_model* m) {
   m->layouts.clear();
-  m->layouts.push_back(make_layout(kTileEmbed, m->D));
+  m->tied = m->cfg.flags & MT_TIE_EMBEDDINGS;
+  m->layouts.push_back(make_layout(kTileEmbed, m->D, m->tied));
   for (int i = 0; i < m->D.L; ++i) m->layouts.push_back(make_layout(kTileLayer, m->D));
-  m->layouts.push_back(make_layout(kTileHead, m->D));
+  if (!m->tied) m->layouts.push_back(make_layout(kTileHead, m->D));
+  m->head_tile = m->tied ? 0 : m->D.L + 1;
   m->max_w_bytes = 0;
   for (const auto& l : m->layouts) m->max_w_bytes = std::max(m->max_w_bytes, l.w_bytes);
   int64_t layer_bytes = 0;
   for (int i = 1; i <= m->D.L; ++i) layer_bytes = std::max(layer_bytes, m->layouts[i].w_bytes);
   m->gbuf_bytes[0] = m->gbuf_bytes[1] = layer_bytes;
   m->gbuf_bytes[2] =
-      std::max<int64_t>(m->layouts[m->D.L + 1].w_bytes, std::min<int64_t>(m->D.T, m->D.V) * 2LL * m->D.d);
+      std::max<int64_t>(m->layouts[m->head_tile].w_bytes, std::min<int64_t>(m->D.T, m->D.V) * 2LL * m->D.d);
 }
 
 void parallel_zero(uint8_t* p, int64_t n, int nthreads) {
@@ -1344,7 +1391,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->arena_used = plan_arena(m, m->arena);
 
   // visit schedule
-  m->visits = build_schedule(m->D.L, m->K, m->store_acts, m->single_buffer);
+  m->visits = build_schedule(m->D.L, m->K, m->store_acts, m->single_buffer, m->head_tile);
   if (m->resident_mode)
     for (auto& x : m->visits) x.h2d = false;
   const int nv = (int)m->visits.size();

@@ -45,6 +45,7 @@ struct TileLayout {
   int64_t off_w = 0, off_g = 0, off_m = 0, off_v = 0;
   int64_t tile_bytes = 0;
   const TensorSlot& slot(const char* n) const;
+  bool has(const char* n) const;
 };
 
 struct Dims {
@@ -56,7 +57,9 @@ struct Dims {
 };
 
 Dims dims_of(const mt_config& c);
-TileLayout make_layout(TileKind kind, const Dims& d);
+// tied: the embedding tile also holds the final norm gain and serves as the LM
+// head's weight (there is no head tile).
+TileLayout make_layout(TileKind kind, const Dims& d, bool tied = false);
 
 // ------------------------------------------------------------------ device workspace
 // Bound views of one layer tile (weights in a streamed buffer, or gradients

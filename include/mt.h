@@ -82,9 +82,17 @@ enum {
   MT_TRACE = 1u << 5,             /* debugging: wait for every visit (layer pass) to finish, print its kind,
                                      layer, time and the device status word to stderr, stop at the first
                                      nonzero status */
-  MT_VISIT_LOG = 1u << 6          /* after each step print one line per visit to stderr: the compute-stream
+  MT_VISIT_LOG = 1u << 6,         /* after each step print one line per visit to stderr: the compute-stream
                                      gap before it, its compute-stream time, and how long the stream and the
                                      issuing host thread waited for its weights and its gradient buffer */
+  MT_TIE_EMBEDDINGS = 1u << 7     /* the LM head's weight is the embedding table E (paperlayer.ai summary
+                                     §A.1, tied embeddings: one shared host region, update readiness
+                                     tracked).  Tile 0 holds E and the final norm gain gf; there is no head
+                                     tile (mt_tile_count = L + 1).  The head's visit streams tile 0 and binds
+                                     W_h to its E (one device address); its dense dW_h lands in tile 0's G and
+                                     the embedding rows' gradient is added to it.  E's rows that no token of
+                                     the step uses are updated once the head's gradient has landed, the rest
+                                     once their embedding gradient has been added. */
 };
 
 /* Tile parts for load/get. */
@@ -169,7 +177,7 @@ int64_t mt_required_device_bytes(const mt_config* cfg);
 int mt_init_model(const mt_config* cfg, void* device_arena, size_t arena_bytes, void* stream_comp,
                   void* stream_h2d, void* stream_d2h, mt_model** out);
 
-int mt_tile_count(const mt_model* m);                                /* L + 2 */
+int mt_tile_count(const mt_model* m);                                /* L + 2 (L + 1 with MT_TIE_EMBEDDINGS) */
 int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out);
 
 /*

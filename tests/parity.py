@@ -32,7 +32,9 @@ def flat_named(tree):
     for i, lw in enumerate(tree["layers"]):
         for k in mt_inputs.LAYER_TENSORS:
             out.append((f"layers.{i}.{k}", lw[k]))
-    out += [("head.gf", tree["head"]["gf"]), ("head.wh", tree["head"]["wh"])]
+    out.append(("head.gf", tree["head"]["gf"]))
+    if "wh" in tree["head"]:  # absent with tied embeddings (E is the head's weight)
+        out.append(("head.wh", tree["head"]["wh"]))
     return out
 
 

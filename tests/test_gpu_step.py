@@ -223,3 +223,72 @@ def test_one_micro_batch_is_the_plain_step():
     _equal_trees(m.weights(), a["w"][0])
     _equal_trees(m.grads(), a["g"][0])
     m.close()
+
+
+# ------------------------------------------------------------------ tied embeddings
+def _run_tied(shape, tokens_list, flags=0, micro=False):
+    m = hms.StreamedDecoder.from_shape(shape, flags=flags | hms.MT_TIE_EMBEDDINGS)
+    assert m.n_tiles == shape.n_layers + 1
+    params = mt_inputs.tied(mt_inputs.model_weights(shape, gain_jitter=0.1))
+    m.load_weights(params)
+    out = {"params0": params, "loss": [], "w": [], "g": [], "mv": []}
+    for tok in tokens_list:
+        out["loss"].append(m.train_step_micro(tok) if micro else m.train_step(tok))
+        out["w"].append(m.weights())
+        out["g"].append(m.grads())
+        out["mv"].append(m.moments())
+    m.close()
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "one_layer", "gqa128"])
+def test_tied_embeddings_step_matches_oracle(name):
+    """MT_TIE_EMBEDDINGS: one host tile for E and the final gain; the head
+    streams it and uses E as W_h, E's gradient is the head's plus the
+    embedding's, Adam updates every row once.  With one layer the head's
+    visit finds the embedding tile still in a device buffer (no second
+    upload); with more layers it is streamed again."""
+    s = SHAPES["tiny"].with_(n_layers=1) if name == "one_layer" else SHAPES[name]
+    cfg = OracleConfig.from_shape(s)
+    tokens = mt_inputs.step_tokens(s, 1)
+    r = _run_tied(s, [tokens])
+    assert set(r["g"][0]["head"]) == {"gf"} and set(r["w"][0]["head"]) == {"gf"}
+    loss, grads = oracle.model_loss_and_grads(r["params0"], tokens, cfg)
+    assert abs(r["loss"][0] - loss) <= parity.LOSS_RTOL * abs(loss)
+    parity.assert_grads_close(r["g"][0], grads)
+    m, v = r["mv"][0]
+    parity.assert_adam_matches(r["w"][0], r["params0"], r["g"][0], m, v, 1, cfg)
+    # rows of token ids absent from the step carry the head's gradient alone
+    untouched = torch.ones(s.vocab, dtype=torch.bool)
+    untouched[tokens[:, :-1].reshape(-1).long()] = False
+    assert int(untouched.sum()) > 0
+    assert torch.any(r["g"][0]["embed"]["E"][untouched] != 0)
+
+
+def test_tied_embeddings_trajectory_and_resident_bitexact():
+    s = SHAPES["gqa128"]
+    cfg = OracleConfig.from_shape(s)
+    toks = [mt_inputs.step_tokens(s, n) for n in (1, 2)]
+    a = _run_tied(s, toks)
+    b = _run_tied(s, toks, flags=hms.MT_RESIDENT)
+    assert a["loss"] == b["loss"]
+    _equal_trees(a["w"][-1], b["w"][-1])
+    _equal_trees(a["g"][-1], b["g"][-1])
+    params, state = a["params0"], None
+    for n, tok in enumerate(toks, 1):
+        loss, grads, params, state = oracle.train_step(params, state, tok, n, cfg)
+        assert abs(a["loss"][n - 1] - loss) <= parity.LOSS_RTOL * abs(loss), (n, a["loss"][n - 1], loss)
+        parity.assert_grads_close(a["g"][n - 1], grads)
+
+
+def test_tied_embeddings_micro_batches_match_oracle():
+    s = SHAPES["gqa128"]
+    cfg = OracleConfig.from_shape(s)
+    t1, t2 = mt_inputs.step_tokens(s, 1), mt_inputs.step_tokens(s, 2)
+    r = _run_tied(s, [torch.stack([t1, t2])], micro=True)
+    loss_ref, grads = oracle.model_loss_and_grads(r["params0"], torch.cat([t1, t2]), cfg)
+    assert abs(r["loss"][0] - loss_ref) <= parity.LOSS_RTOL * abs(loss_ref)
+    parity.assert_grads_close(r["g"][0], grads)
+    m, v = r["mv"][0]
+    parity.assert_adam_matches(r["w"][0], r["params0"], r["g"][0], m, v, 1, cfg)
+
