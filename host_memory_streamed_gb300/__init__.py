@@ -233,6 +233,22 @@ class StreamedDecoder:
         self._check(self._L.mt_train_step_micro(self._h, tok.data_ptr(), tok.numel(), tok.shape[0], C.byref(loss)))
         return loss.value
 
+    def train_step_grads(self, tokens: torch.Tensor) -> float:
+        """Forward and backward of one step without the optimizer: the tiles'
+        G sections receive the gradient of the mean loss over these tokens
+        (host int32 [B, S+1]); weights, moments and the step are unchanged.
+        Returns the loss.  See ``apply_adam`` and ``replicas.replica_step``."""
+        loss = C.c_float()
+        tok = tokens.to(torch.int32).contiguous()
+        if tok.is_cuda:
+            raise TypeError("tokens must be a host tensor [batch, seq + 1]")
+        self._check(self._L.mt_train_step_grads(self._h, tok.data_ptr(), tok.numel(), C.byref(loss)))
+        return loss.value
+
+    def apply_adam(self):
+        """One Adam step of every tile from its G section as it stands; advances the step."""
+        self._check(self._L.mt_apply_adam(self._h))
+
     def layer_pass(self, layer, x_in, dx_out=None, x_out=None, dx_in=None):
         """One decoder layer's forward (and backward, given dx_out) on device BF16
         [batch*seq, d_model] activations; the layer's gradient lands in its host

@@ -82,6 +82,8 @@ def lib():
         "mt_train_step_device_tokens": (C.c_int, [vp, vp, sz, fp]),
         "mt_layer_pass": (C.c_int, [vp, i32, vp, vp, vp, vp]),
         "mt_train_step_micro": (C.c_int, [vp, vp, sz, i32, fp]),
+        "mt_train_step_grads": (C.c_int, [vp, vp, sz, fp]),
+        "mt_apply_adam": (C.c_int, [vp]),
         "mt_get_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
         "mt_get_step_stats": (C.c_int, [vp, C.POINTER(MtStepStats)]),
         "mt_get_step": (i64, [vp]),

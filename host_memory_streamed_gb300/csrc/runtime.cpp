@@ -339,7 +339,8 @@ struct mt_model {
   // micro-batches of the current step: pass micro_index of micro_count; gradients
   // of later passes add into the tile's G, Adam runs on the last pass only
   int micro_index = 0, micro_count = 1;
-  bool last_pass() const { return micro_index + 1 == micro_count; }
+  bool grads_only = false;  // mt_train_step_grads: no pass is the last (no Adam, no step advance)
+  bool last_pass() const { return !grads_only && micro_index + 1 == micro_count; }
 
   // schedule + events
   std::vector<mt::Visit> visits;
@@ -616,7 +617,8 @@ void submit_adam_range(mt_model* m, int tile, int64_t g_off, int64_t g_bytes) {
 // not read it, so these rows may be updated mid-step.
 void submit_untouched_embed(mt_model* m) {
   if (m->micro_index > 0) return;  // later micro-batches add into the rows the first one set
-  const bool update = m->micro_count == 1;  // with micro-batches, one dense embedding update at the end
+  // with micro-batches one dense embedding update at the end; none for gradients only
+  const bool update = m->micro_count == 1 && !m->grads_only;
   const TileLayout& lay = m->layouts[0];
   const TensorSlot& E = lay.slot("E");
   const int d = m->D.d, V = m->D.V;
@@ -1605,6 +1607,31 @@ int mt_train_step(mt_model* m, const int32_t* tokens, size_t n_tokens, float* lo
 int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n_tokens, float* loss_out) {
   if (!m || !tokens_dev) return MT_EINVAL;
   return mt::run_step(m, nullptr, tokens_dev, n_tokens, loss_out);
+}
+
+int mt_train_step_grads(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out) {
+  if (!m || !tokens) return MT_EINVAL;
+  m->grads_only = true;
+  const int code = mt::run_step(m, tokens, nullptr, n_tokens, loss_out);
+  m->grads_only = false;
+  return code;
+}
+
+int mt_apply_adam(mt_model* m) {
+  using namespace mt;
+  if (!m) return MT_EINVAL;
+  if (m->broken) {
+    m->err = "handle is unusable after an earlier CUDA or internal error: " + m->err;
+    return MT_ESTATE;
+  }
+  for (size_t t = 0; t < m->tiles.size(); ++t) submit_adam_range(m, (int)t, 0, m->layouts[t].w_bytes);
+  if (!m->adam_pool->wait_idle(m->cfg.timeout_ms)) {
+    m->err = "timed out waiting for Adam";
+    m->broken = true;
+    return MT_ETIMEDOUT;
+  }
+  m->step += 1;
+  return MT_OK;
 }
 
 int mt_train_step_micro(mt_model* m, const int32_t* tokens, size_t n_tokens, int32_t n_micro, float* loss_out) {

@@ -211,6 +211,27 @@ int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n
 int mt_train_step_micro(mt_model* m, const int32_t* tokens, size_t n_tokens, int32_t n_micro, float* loss_out);
 
 /*
+ * Data-parallel replicas (one handle per GPU, each on its own batch) combine
+ * their gradients on the host between these two calls:
+ *
+ * mt_train_step_grads: mt_train_step without the optimizer.  Afterwards every
+ * tile's G section holds the BF16 gradient of the mean loss over this batch's
+ * batch*seq targets (embedding rows of token ids the batch does not use are
+ * zero); weights, moments and the step counter are unchanged.  Arguments and
+ * errors as mt_train_step.
+ *
+ * mt_apply_adam: one Adam step of every tile from its G section as it stands
+ * (left by mt_train_step_grads or replaced through mt_load_layer_tile, part
+ * G), with step counter t + 1, on the host Adam workers; returns when every
+ * tile is updated, then advances the counter.  The caller checks that the
+ * gradients are finite.  MT_ESTATE on a handle that saw MT_ECUDA, MT_EINTERNAL
+ * or MT_ETIMEDOUT; MT_ETIMEDOUT when the workers do not finish within
+ * timeout_ms.
+ */
+int mt_train_step_grads(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out);
+int mt_apply_adam(mt_model* m);
+
+/*
  * Per-layer check at the workload's full shape (a debugging hook for parity
  * tests): run decoder layer `layer` (0-based; tile layer + 1) forward and
  * backward once on caller-supplied activations, with the same template,

@@ -292,3 +292,22 @@ def test_tied_embeddings_micro_batches_match_oracle():
     m, v = r["mv"][0]
     parity.assert_adam_matches(r["w"][0], r["params0"], r["g"][0], m, v, 1, cfg)
 
+
+
+def test_grads_only_then_adam_is_the_plain_step():
+    """mt_train_step_grads + mt_apply_adam (the data-parallel replica split)
+    reproduce mt_train_step bit for bit: loss, weights, gradients, moments."""
+    s = SHAPES["gqa128"]
+    a = _run(s, steps=2)
+    m = hms.StreamedDecoder.from_shape(s)
+    m.load_weights(mt_inputs.model_weights(s, gain_jitter=0.1))
+    for n in (1, 2):
+        assert m.train_step_grads(mt_inputs.step_tokens(s, n)) == a["loss"][n - 1]
+        assert m.step == n - 1
+        m.apply_adam()
+    assert m.step == 2
+    _equal_trees(m.weights(), a["w"][-1])
+    _equal_trees(m.grads(), a["g"][-1])
+    for x, y in zip(m.moments(), a["mv"][-1]):
+        _equal_trees(x, y)
+    m.close()
