@@ -1,0 +1,99 @@
+"""CPU oracle of a mixture-of-experts MLP block (FP64).
+
+TEST INFRASTRUCTURE ONLY, like the rest of ``oracle/``: only ``tests/`` may
+import it; the library never does.
+
+The pages name the model of MegaTrain's largest run (gpt-oss 120B, a
+mixture-of-experts decoder; author's blog, the single-H200 run; podcast
+transcript, the 120B GPT-OSS run), list dedicated MoE optimisations among
+planned work (author's blog, planned projects) and note that the stateless
+layer templates may need redesign for MoE (engineersofai.com breakdown,
+limitations), but give no formula for the MoE layer.  This file takes the
+plainest reading of a top-k MoE MLP, stated here so that the kernels have a
+definition to match:
+
+* router logits ``s = x W_r^T`` (``W_r`` [E, d], no bias);
+* per token, the k experts with the largest logits; ties go to the lower
+  expert index (a stable order, so the selection is a function of ``s``);
+* gates ``g = softmax`` over the k selected logits (they sum to 1);
+* ``y = sum_j g_j * f_{e_j}(x)`` with every expert a SwiGLU MLP,
+  ``f_e(x) = W_d[e] (silu(W_g[e] x) * W_u[e] x)``, no biases.
+
+The selection is piecewise constant, so the gradient flows through the gates
+and the experts only.  Everything is FP64 and unblocked: each expert runs on
+the rows routed to it, gathered with ``index_select`` and scattered back with
+``index_add_``.
+
+Parity status: pinned by ``tests/test_oracle_moe_pins.py`` (autograd of a
+separately written forward, finite differences, the single-expert case equal
+to the dense SwiGLU MLP, invariance under relabelling the experts).
+"""
+from __future__ import annotations
+
+import torch
+
+from .decoder import swiglu, swiglu_backward
+
+__all__ = ["moe_route", "moe_mlp_forward", "moe_mlp_backward"]
+
+
+def moe_route(x, wr, k):
+    """x [N, d], wr [E, d] -> (logits [N, E], expert ids [N, k], gates [N, k]).
+
+    Expert ids per token in descending logit order, ties to the lower id.
+    """
+    s = x @ wr.T
+    E = s.shape[1]
+    # stable descending order: sort by (-logit, id)
+    order = torch.sort(-s, dim=1, stable=True).indices
+    idx = order[:, :k]
+    sel = s.gather(1, idx)
+    gates = torch.softmax(sel, dim=1)
+    assert idx.shape[1] == k <= E
+    return s, idx, gates
+
+
+def moe_mlp_forward(x, wr, experts, k):
+    """y = sum_j g_j f_{e_j}(x) for x [N, d]; ``experts`` is a list of dicts
+    with 'wg', 'wu' [F, d] and 'wd' [d, F].  Returns (y, cache)."""
+    N, d = x.shape
+    s, idx, gates = moe_route(x, wr, k)
+    y = torch.zeros_like(x)
+    per_expert = []
+    for e, ew in enumerate(experts):
+        tok, slot = (idx == e).nonzero(as_tuple=True)  # rows routed to e, and which of their k slots
+        xe = x.index_select(0, tok)
+        gate, up = xe @ ew["wg"].T, xe @ ew["wu"].T
+        a = swiglu(gate, up)
+        fe = a @ ew["wd"].T
+        y.index_add_(0, tok, fe * gates[tok, slot][:, None])
+        per_expert.append((tok, slot, xe, gate, up, a, fe))
+    return y, {"s": s, "idx": idx, "gates": gates, "per_expert": per_expert}
+
+
+def moe_mlp_backward(dy, x, wr, experts, k, cache):
+    """Gradients of sum(dy * y): returns (dx, dwr, [{'wg','wu','wd'}] per expert)."""
+    idx, gates = cache["idx"], cache["gates"]
+    N, d = x.shape
+    dx = torch.zeros_like(x)
+    dg = torch.zeros_like(gates)  # d loss / d gate[n, j]
+    dexperts = []
+    for e, ew in enumerate(experts):
+        tok, slot, xe, gate, up, a, fe = cache["per_expert"][e]
+        dye = dy.index_select(0, tok)
+        dg[tok, slot] = (dye * fe).sum(1)
+        dfe = dye * gates[tok, slot][:, None]  # gradient of this expert's output
+        dwd = dfe.T @ a
+        da = dfe @ ew["wd"]
+        dgate, dup = swiglu_backward(da, gate, up)
+        dwg = dgate.T @ xe
+        dwu = dup.T @ xe
+        dx.index_add_(0, tok, dgate @ ew["wg"] + dup @ ew["wu"])
+        dexperts.append({"wg": dwg, "wu": dwu, "wd": dwd})
+    # softmax over the selected logits: ds_j = g_j (dg_j - sum_i g_i dg_i)
+    dsel = gates * (dg - (gates * dg).sum(1, keepdim=True))
+    ds = torch.zeros(N, wr.shape[0], dtype=x.dtype)
+    ds.scatter_(1, idx, dsel)
+    dwr = ds.T @ x
+    dx += ds @ wr
+    return dx, dwr, dexperts
