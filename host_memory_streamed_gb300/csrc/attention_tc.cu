@@ -60,8 +60,7 @@ struct TaCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;             // STAGES blocks
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;   // STAGES blocks
-  static constexpr int OFF_L = OFF_V + STAGES * KV_BYTES;   // [2][128] halves of the row sums
-  static constexpr int OFF_BAR = OFF_L + 2 * 128 * 4;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;  // the final (max, sum) exchange reuses the K ring
   static constexpr int SMEM = OFF_BAR + 256 + 1024;         // barriers + alignment slack
 };
 

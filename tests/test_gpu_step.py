@@ -311,3 +311,21 @@ def test_grads_only_then_adam_is_the_plain_step():
     for x, y in zip(m.moments(), a["mv"][-1]):
         _equal_trees(x, y)
     m.close()
+
+
+def test_visit_log_prints_one_line_per_visit(capfd):
+    """MT_VISIT_LOG: after the step, one '[mt visit]' line per visit of the
+    schedule (embedding, L layers forward, head, L layers backward, embedding
+    backward at K = 1) and the host-tail line, on stderr."""
+    s = SHAPES["tiny"]
+    m = hms.StreamedDecoder.from_shape(s, flags=hms.MT_VISIT_LOG)
+    m.load_weights(mt_inputs.model_weights(s, gain_jitter=0.1))
+    capfd.readouterr()
+    m.train_step(mt_inputs.step_tokens(s, 1))
+    m.close()
+    err = capfd.readouterr().err.splitlines()
+    visits = [l for l in err if l.startswith("[mt visit]") and " gap " in l]
+    tails = [l for l in err if l.startswith("[mt visit] compute stream ends")]
+    assert len(visits) == 2 * s.n_layers + 3, err[:5]
+    assert len(tails) == 1
+    assert "layer_bwd" in visits[-2] and "embed_bwd" in visits[-1]
