@@ -25,16 +25,19 @@ the rows routed to it, gathered with ``index_select`` and scattered back with
 ``index_add_``.
 
 Parity status: pinned by ``tests/test_oracle_moe_pins.py`` (autograd of a
-separately written forward, finite differences, the single-expert case equal
-to the dense SwiGLU MLP, invariance under relabelling the experts).
+separately written forward, finite differences of the block and of the whole
+MoE decoder layer, the single-expert block equal to the dense SwiGLU MLP and
+the single-expert layer equal to the dense decoder layer, invariance under
+relabelling the experts, the tie order).
 """
 from __future__ import annotations
 
 import torch
 
-from .decoder import swiglu, swiglu_backward
+from .decoder import (OracleConfig, causal_gqa_attention, causal_gqa_attention_backward, rms_norm,
+                      rms_norm_backward, rope, rope_backward, swiglu, swiglu_backward)
 
-__all__ = ["moe_route", "moe_mlp_forward", "moe_mlp_backward"]
+__all__ = ["moe_route", "moe_mlp_forward", "moe_mlp_backward", "moe_layer_forward", "moe_layer_backward"]
 
 
 def moe_route(x, wr, k):
@@ -97,3 +100,58 @@ def moe_mlp_backward(dy, x, wr, experts, k, cache):
     dwr = ds.T @ x
     dx += ds @ wr
     return dx, dwr, dexperts
+
+
+# ----------------------------------------------------------------------------
+# One MoE decoder layer: the dense layer's attention half, then the MoE MLP
+# ----------------------------------------------------------------------------
+
+def moe_layer_forward(x, lw, cfg: OracleConfig, cos, sin, k):
+    """x [B, S, d] -> x' = h + MoE(n2), h = x + W_o attn(n1), n2 = RMSNorm(h; g2).
+
+    ``lw``: g1, wq, wk, wv, wo, g2, wr [E, d] and ``experts`` (a list of
+    {wg, wu, wd}).  Returns x' and the cache for ``moe_layer_backward``.
+    """
+    B, S, d = x.shape
+    Hq, Hkv, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    n1, rstd1 = rms_norm(x, lw["g1"], cfg.rms_eps)
+    qr = rope((n1 @ lw["wq"].T).reshape(B, S, Hq, hd), cos, sin)
+    kr = rope((n1 @ lw["wk"].T).reshape(B, S, Hkv, hd), cos, sin)
+    v = (n1 @ lw["wv"].T).reshape(B, S, Hkv, hd)
+    o, probs = causal_gqa_attention(qr, kr, v)
+    o2 = o.reshape(B, S, Hq * hd)
+    h = x + o2 @ lw["wo"].T
+    n2, rstd2 = rms_norm(h, lw["g2"], cfg.rms_eps)
+    y, mc = moe_mlp_forward(n2.reshape(B * S, d), lw["wr"], lw["experts"], k)
+    x_out = h + y.reshape(B, S, d)
+    cache = dict(x=x, n1=n1, rstd1=rstd1, qr=qr, kr=kr, v=v, probs=probs, o2=o2, h=h, n2=n2, rstd2=rstd2, moe=mc)
+    return x_out, cache
+
+
+def moe_layer_backward(dx_out, c, lw, cfg: OracleConfig, cos, sin, k):
+    """Backward of ``moe_layer_forward``: (dx, grads named as in ``lw``, the
+    experts' gradients as a list under 'experts')."""
+    B, S, d = dx_out.shape
+    Hq, Hkv, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+
+    def wgrad(dy, xin):
+        return dy.reshape(-1, dy.shape[-1]).T @ xin.reshape(-1, xin.shape[-1])
+
+    g = {}
+    dn2, g["wr"], g["experts"] = moe_mlp_backward(dx_out.reshape(B * S, d), c["n2"].reshape(B * S, d), lw["wr"],
+                                                 lw["experts"], k, c["moe"])
+    dh_n, g["g2"] = rms_norm_backward(dn2.reshape(B, S, d), c["h"], lw["g2"], c["rstd2"])
+    dh = dx_out + dh_n
+    g["wo"] = wgrad(dh, c["o2"])
+    do = (dh @ lw["wo"]).reshape(B, S, Hq, hd)
+    dqr, dkr, dv = causal_gqa_attention_backward(do, c["qr"], c["kr"], c["v"], c["probs"])
+    dq = rope_backward(dqr, cos, sin).reshape(B, S, Hq * hd)
+    dk = rope_backward(dkr, cos, sin).reshape(B, S, Hkv * hd)
+    dv = dv.reshape(B, S, Hkv * hd)
+    g["wq"] = wgrad(dq, c["n1"])
+    g["wk"] = wgrad(dk, c["n1"])
+    g["wv"] = wgrad(dv, c["n1"])
+    dn1 = dq @ lw["wq"] + dk @ lw["wk"] + dv @ lw["wv"]
+    dx_n, g["g1"] = rms_norm_backward(dn1, c["x"], lw["g1"], c["rstd1"])
+    return dh + dx_n, g
+

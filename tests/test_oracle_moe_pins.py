@@ -119,3 +119,68 @@ def test_ties_go_to_the_lower_expert_id():
     assert idx.tolist() == [[1, 2, 3]]
     e = math.exp(-2.0)
     assert torch.allclose(gates, torch.tensor([[1 / (2 + e), 1 / (2 + e), e / (2 + e)]], dtype=D))
+
+
+def _layer_setup(E, k, seed):
+    import mt_inputs
+    from oracle import OracleConfig
+    s = mt_inputs.PRESETS["tiny"].with_(n_layers=1, d_model=64, n_heads=4, n_kv_heads=2, head_dim=16, ffn=48,
+                                        vocab=50, batch=2, seq=10)
+    cfg = OracleConfig.from_shape(s)
+    lw = {n: t.to(D) for n, t in mt_inputs.layer_weights(s, 0, gain_jitter=0.1).items()}
+    wr, experts = _weights(E, s.d_model, s.ffn, seed)
+    x = torch.randn(s.batch, s.seq, s.d_model, generator=torch.Generator().manual_seed(seed + 1), dtype=D)
+    cos, sin = oracle.rope_cos_sin(s.seq, s.head_dim, s.rope_theta)
+    return s, cfg, lw, wr, experts, x, cos, sin
+
+
+def test_moe_layer_with_one_expert_is_the_dense_layer():
+    """E = k = 1 with the dense layer's own MLP as the expert: the MoE layer's
+    output and every gradient equal the dense layer's."""
+    s, cfg, lw, wr, _, x, cos, sin = _layer_setup(1, 1, 51)
+    mw = {n: lw[n] for n in ("g1", "wq", "wk", "wv", "wo", "g2")}
+    mw["wr"] = wr
+    mw["experts"] = [{"wg": lw["wg"], "wu": lw["wu"], "wd": lw["wd"]}]
+    y_dense, c_dense = oracle.layer_forward(x, lw, cfg, cos, sin)
+    y_moe, c_moe = moe.moe_layer_forward(x, mw, cfg, cos, sin, 1)
+    assert torch.allclose(y_moe, y_dense, rtol=1e-13, atol=1e-14)
+    dy = torch.randn(x.shape, generator=torch.Generator().manual_seed(52), dtype=D)
+    dx_d, g_d = oracle.layer_backward(dy, c_dense, lw, cfg, cos, sin)
+    dx_m, g_m = moe.moe_layer_backward(dy, c_moe, mw, cfg, cos, sin, 1)
+    assert torch.allclose(dx_m, dx_d, rtol=1e-11, atol=1e-13)
+    for n in ("g1", "wq", "wk", "wv", "wo", "g2"):
+        assert torch.allclose(g_m[n], g_d[n], rtol=1e-11, atol=1e-13), n
+    for n in ("wg", "wu", "wd"):
+        assert torch.allclose(g_m["experts"][0][n], g_d[n], rtol=1e-11, atol=1e-13), n
+    assert torch.all(g_m["wr"] == 0)  # one expert, gate identically 1
+
+
+def test_moe_layer_finite_differences():
+    """Directional central differences of the MoE layer over all its weights
+    and its input, small enough that no token's expert selection moves."""
+    E, k = 5, 2
+    s, cfg, lw, wr, experts, x, cos, sin = _layer_setup(E, k, 61)
+    mw = {n: lw[n] for n in ("g1", "wq", "wk", "wv", "wo", "g2")}
+    mw["wr"], mw["experts"] = wr, experts
+    dy = torch.randn(x.shape, generator=torch.Generator().manual_seed(62), dtype=D)
+    _, c = moe.moe_layer_forward(x, mw, cfg, cos, sin, k)
+    dx, g = moe.moe_layer_backward(dy, c, mw, cfg, cos, sin, k)
+    gen = torch.Generator().manual_seed(63)
+    names = ("g1", "wq", "wk", "wv", "wo", "g2", "wr")
+    for _ in range(2):
+        ux = torch.randn(x.shape, generator=gen, dtype=D)
+        uw = {n: torch.randn(mw[n].shape, generator=gen, dtype=D) for n in names}
+        ue = [{n: torch.randn(t.shape, generator=gen, dtype=D) for n, t in e.items()} for e in experts]
+        h = 1e-6
+
+        def f(sign):
+            w2 = {n: mw[n] + sign * h * uw[n] for n in names}
+            w2["experts"] = [{n: t + sign * h * ue[i][n] for n, t in e.items()} for i, e in enumerate(experts)]
+            y, c2 = moe.moe_layer_forward(x + sign * h * ux, w2, cfg, cos, sin, k)
+            assert torch.equal(c2["moe"]["idx"], c["moe"]["idx"])
+            return float((y * dy).sum())
+
+        fd = (f(1) - f(-1)) / (2 * h)
+        an = float((dx * ux).sum()) + sum(float((g[n] * uw[n]).sum()) for n in names) + \
+            sum(float((g["experts"][i][n] * ue[i][n]).sum()) for i in range(E) for n in ("wg", "wu", "wd"))
+        assert abs(fd - an) <= 1e-6 * abs(an) + 1e-9, (fd, an)
