@@ -105,6 +105,13 @@ def lib():
         "mt_op_cross_entropy": (C.c_int, [vp, i64, i32, vp, f32, vp, vp, vp, vp]),
         "mt_op_embedding_fwd": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp]),
         "mt_op_embedding_bwd": (C.c_int, [vp, vp, vp, vp, i32, i32, vp]),
+        "mt_op_moe_sort_scratch_ints": (i64, [i64, i32]),
+        "mt_op_moe_route": (C.c_int, [vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "mt_op_moe_gather": (C.c_int, [vp, i64, vp, i32, i64, i32, vp, vp]),
+        "mt_op_moe_combine": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp, vp]),
+        "mt_op_moe_combine_bwd": (C.c_int, [vp, vp, vp, vp, i64, i32, i32, vp, vp, vp]),
+        "mt_op_moe_gate_bwd": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp]),
+        "mt_op_moe_scatter_bwd": (C.c_int, [vp, vp, i64, i32, i32, vp, vp, vp]),
         "mt_op_rmsnorm_bwd_noalloc": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp]),
     }
     for name, (res, args) in sig.items():

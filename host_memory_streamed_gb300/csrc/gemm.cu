@@ -762,7 +762,9 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, long rows, long cols, long
 
 const char* gemm_check(const GemmArgs& g) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return "gemm: M, N and K must be positive";
-  if (g.K % 8) return "gemm: K must be a multiple of 8 (16-byte TMA rows)";
+  // K is the contiguous dimension of a K-major operand; with both operands
+  // MN-major it is the outer one and any K works (the last block reads zeros)
+  if (g.K % 8 && !(g.a_mn && g.b_mn)) return "gemm: K must be a multiple of 8 (16-byte TMA rows)";
   if (g.lda % 8 || g.ldb % 8) return "gemm: lda/ldb must be multiples of 8 elements";
   if (g.lda < (g.a_mn ? g.M : g.K) || g.ldb < (g.b_mn ? g.N : g.K)) return "gemm: lda/ldb smaller than a row";
   if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.B)) & 15) return "gemm: A/B not 16-byte aligned";

@@ -127,4 +127,30 @@ void launch_zero(void* p, size_t bytes, cudaStream_t s);
 // status |= kStatusNonFinite when any of the n BF16 values is NaN or Inf.
 void launch_check_finite(const bf16* p, long n, int* status, cudaStream_t s);
 
+// ----------------------------------------------------------------- mixture of experts (moe.cu)
+// N tokens, E experts (<= 256), top k (<= 8), pairs p = n*k + j, P = N*k.
+const char* moe_check(long N, int E, int k, int d);
+// idx[n, j], gates[n, j] from FP32 router logits [N, E]: k largest, ties to the lower id; softmax over them.
+int launch_moe_topk(const float* logits, long N, int E, int k, int32_t* idx, float* gates, cudaStream_t s);
+// Stable counting sort of the pairs by expert: order[i] = pair at position i,
+// pos[p] = position of pair p, offsets[e] = first position of expert e (offsets[E] = P).
+long moe_sort_scratch_ints(long P, int E);
+int launch_moe_sort(const int32_t* idx, long P, int E, int32_t* scratch, int32_t* order, int32_t* pos,
+                    int32_t* offsets, cudaStream_t s);
+// xp[i] = x[order[i] / k] (rows of d BF16 values; x rows ldx apart).
+int launch_moe_gather(const bf16* x, long ldx, const int32_t* order, int k, long P, int d, bf16* xp,
+                      cudaStream_t s);
+// out[n] = res[n] + sum_j gates[n, j] yp[pos[n k + j]] (res may be null).
+int launch_moe_combine(const bf16* yp, const int32_t* pos, const float* gates, long N, int k, int d, const bf16* res,
+                       bf16* out, cudaStream_t s);
+// dyp[pos[p]] = gates[p] dy[n]; dgates[p] = <dy[n], yp[pos[p]]>.
+int launch_moe_combine_bwd(const bf16* dy, const bf16* yp, const int32_t* pos, const float* gates, long N, int k,
+                           int d, bf16* dyp, float* dgates, cudaStream_t s);
+// ds [N, E] (BF16): softmax backward over the selected logits, zero elsewhere.
+int launch_moe_gate_bwd(const int32_t* idx, const float* gates, const float* dgates, long N, int E, int k, bf16* ds,
+                        cudaStream_t s);
+// dx[n] = dres[n] + sum_j dxp[pos[n k + j]] (dres may be null).
+int launch_moe_scatter_bwd(const bf16* dxp, const int32_t* pos, long N, int k, int d, const bf16* dres, bf16* dx,
+                           cudaStream_t s);
+
 }  // namespace mt

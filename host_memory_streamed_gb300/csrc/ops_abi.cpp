@@ -197,4 +197,58 @@ int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, co
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "embedding backward");
 }
 
+int64_t mt_op_moe_sort_scratch_ints(int64_t P, int32_t E) { return mt::moe_sort_scratch_ints(P, E); }
+
+int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_t* idx, float* gates, int32_t* order,
+                    int32_t* pos, int32_t* offsets, int32_t* scratch, void* stream) {
+  if (const char* e = mt::moe_check(N, E, k, 8)) return op_fail(e);
+  if (!logits || !idx || !gates || !order || !pos || !offsets || !scratch) return op_fail("moe route: null pointer");
+  auto s = static_cast<cudaStream_t>(stream);
+  if (mt::launch_moe_topk(logits, N, E, k, idx, gates, s)) return op_cuda(-4, "moe top-k");
+  return op_cuda(mt::launch_moe_sort(idx, N * k, E, scratch, order, pos, offsets, s), "moe sort");
+}
+
+int mt_op_moe_gather(const void* x, int64_t ldx, const int32_t* order, int32_t k, int64_t P, int32_t d, void* xp,
+                     void* stream) {
+  if (P <= 0 || k < 1 || d <= 0 || d % 8 || ldx % 8 || ldx < d) return op_fail("moe gather: bad shape");
+  return op_cuda(mt::launch_moe_gather(static_cast<const mt::bf16*>(x), ldx, order, k, P, d,
+                                       static_cast<mt::bf16*>(xp), static_cast<cudaStream_t>(stream)),
+                 "moe gather");
+}
+
+int mt_op_moe_combine(const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k, int32_t d,
+                      const void* res, void* out, void* stream) {
+  if (const char* e = mt::moe_check(N, k, k, d)) return op_fail(e);
+  return op_cuda(mt::launch_moe_combine(static_cast<const mt::bf16*>(yp), pos, gates, N, k, d,
+                                        static_cast<const mt::bf16*>(res), static_cast<mt::bf16*>(out),
+                                        static_cast<cudaStream_t>(stream)),
+                 "moe combine");
+}
+
+int mt_op_moe_combine_bwd(const void* dy, const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k,
+                          int32_t d, void* dyp, float* dgates, void* stream) {
+  if (const char* e = mt::moe_check(N, k, k, d)) return op_fail(e);
+  return op_cuda(mt::launch_moe_combine_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(yp), pos,
+                                            gates, N, k, d, static_cast<mt::bf16*>(dyp), dgates,
+                                            static_cast<cudaStream_t>(stream)),
+                 "moe combine backward");
+}
+
+int mt_op_moe_gate_bwd(const int32_t* idx, const float* gates, const float* dgates, int64_t N, int32_t E, int32_t k,
+                       void* ds, void* stream) {
+  if (const char* e = mt::moe_check(N, E, k, 8)) return op_fail(e);
+  return op_cuda(mt::launch_moe_gate_bwd(idx, gates, dgates, N, E, k, static_cast<mt::bf16*>(ds),
+                                         static_cast<cudaStream_t>(stream)),
+                 "moe gate backward");
+}
+
+int mt_op_moe_scatter_bwd(const void* dxp, const int32_t* pos, int64_t N, int32_t k, int32_t d, const void* dres,
+                          void* dx, void* stream) {
+  if (const char* e = mt::moe_check(N, k, k, d)) return op_fail(e);
+  return op_cuda(mt::launch_moe_scatter_bwd(static_cast<const mt::bf16*>(dxp), pos, N, k, d,
+                                            static_cast<const mt::bf16*>(dres), static_cast<mt::bf16*>(dx),
+                                            static_cast<cudaStream_t>(stream)),
+                 "moe scatter backward");
+}
+
 }  // extern "C"

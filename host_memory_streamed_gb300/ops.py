@@ -146,3 +146,122 @@ def embedding_bwd(row_offsets, positions, dx, dE):
     V, d = dE.shape
     _chk(_lib.lib().mt_op_embedding_bwd(row_offsets.data_ptr(), positions.data_ptr(), dx.data_ptr(), dE.data_ptr(),
                                         V, d, _stream()))
+
+
+# ------------------------------------------------------------------ mixture of experts
+def moe_route(logits, k):
+    """FP32 router logits [N, E] -> (idx [N, k], gates [N, k], order [N k], pos [N k], offsets [E + 1])."""
+    _need(logits, F32, "logits")
+    N, E = logits.shape
+    dev = logits.device
+    idx = torch.empty(N, k, device=dev, dtype=I32)
+    gates = torch.empty(N, k, device=dev, dtype=F32)
+    order = torch.empty(N * k, device=dev, dtype=I32)
+    pos = torch.empty(N * k, device=dev, dtype=I32)
+    offsets = torch.empty(E + 1, device=dev, dtype=I32)
+    scratch = torch.empty(int(_lib.lib().mt_op_moe_sort_scratch_ints(N * k, E)), device=dev, dtype=I32)
+    _chk(_lib.lib().mt_op_moe_route(logits.data_ptr(), N, E, k, idx.data_ptr(), gates.data_ptr(), order.data_ptr(),
+                                    pos.data_ptr(), offsets.data_ptr(), scratch.data_ptr(), _stream()))
+    return idx, gates, order, pos, offsets
+
+
+def moe_gather(x, order, k):
+    _need(x, BF16, "x")
+    P, d = order.numel(), x.shape[1]
+    xp = torch.empty(P, d, device=x.device, dtype=BF16)
+    _chk(_lib.lib().mt_op_moe_gather(x.data_ptr(), x.stride(0), order.data_ptr(), k, P, d, xp.data_ptr(), _stream()))
+    return xp
+
+
+def moe_combine(yp, pos, gates, residual=None):
+    _need(yp, BF16, "yp")
+    N, k = gates.shape
+    d = yp.shape[1]
+    out = torch.empty(N, d, device=yp.device, dtype=BF16)
+    _chk(_lib.lib().mt_op_moe_combine(yp.data_ptr(), pos.data_ptr(), gates.data_ptr(), N, k, d, _ptr(residual),
+                                      out.data_ptr(), _stream()))
+    return out
+
+
+def moe_combine_bwd(dy, yp, pos, gates):
+    N, k = gates.shape
+    d = dy.shape[1]
+    dyp = torch.empty(N * k, d, device=dy.device, dtype=BF16)
+    dgates = torch.empty(N, k, device=dy.device, dtype=F32)
+    _chk(_lib.lib().mt_op_moe_combine_bwd(dy.data_ptr(), yp.data_ptr(), pos.data_ptr(), gates.data_ptr(), N, k, d,
+                                          dyp.data_ptr(), dgates.data_ptr(), _stream()))
+    return dyp, dgates
+
+
+def moe_gate_bwd(idx, gates, dgates, E):
+    N, k = gates.shape
+    ds = torch.empty(N, E, device=gates.device, dtype=BF16)
+    _chk(_lib.lib().mt_op_moe_gate_bwd(idx.data_ptr(), gates.data_ptr(), dgates.data_ptr(), N, E, k, ds.data_ptr(),
+                                       _stream()))
+    return ds
+
+
+def moe_scatter_bwd(dxp, pos, N, k, dres=None):
+    d = dxp.shape[1]
+    dx = torch.empty(N, d, device=dxp.device, dtype=BF16)
+    _chk(_lib.lib().mt_op_moe_scatter_bwd(dxp.data_ptr(), pos.data_ptr(), N, k, d, _ptr(dres), dx.data_ptr(),
+                                          _stream()))
+    return dx
+
+
+def moe_mlp_forward(x, wr, wgu, wd, k):
+    """The MoE MLP on the device from the pieces above and the tcgen05 GEMM:
+    x [N, d] BF16, wr [E, d], wgu [E, 2F, d] (gate/up rows interleaved),
+    wd [E, d, F].  Returns (y [N, d] BF16, saved tensors for the backward).
+    The expert loop reads the per-expert row counts on the host."""
+    N, d = x.shape
+    E, twoF, _ = wgu.shape
+    Fh = twoF // 2
+    logits = torch.empty(N, E, device=x.device, dtype=F32)
+    gemm(x, wr, logits, _lib.EPI_F32)
+    idx, gates, order, pos, offsets = moe_route(logits, k)
+    xp = moe_gather(x, order, k)
+    P = N * k
+    ap = torch.empty(P, Fh, device=x.device, dtype=BF16)
+    gup = torch.empty(P, twoF, device=x.device, dtype=BF16)
+    yp = torch.empty(P, d, device=x.device, dtype=BF16)
+    off = offsets.cpu().tolist()
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        gemm(xp[r0:r1], wgu[e], ap[r0:r1], _lib.EPI_SWIGLU, out2=gup[r0:r1])
+        gemm(ap[r0:r1], wd[e], yp[r0:r1])
+    y = moe_combine(yp, pos, gates)
+    return y, dict(idx=idx, gates=gates, order=order, pos=pos, off=off, xp=xp, ap=ap, gup=gup, yp=yp)
+
+
+def moe_mlp_backward(dy, x, wr, wgu, wd, k, saved):
+    """Gradients of the MoE MLP: (dx, dwr, dwgu [E, 2F, d], dwd [E, d, F])."""
+    N, d = x.shape
+    E, twoF, _ = wgu.shape
+    Fh = twoF // 2
+    dyp, dgates = moe_combine_bwd(dy, saved["yp"], saved["pos"], saved["gates"])
+    P = N * k
+    dgup = torch.empty(P, twoF, device=x.device, dtype=BF16)
+    dxp = torch.empty(P, d, device=x.device, dtype=BF16)
+    dwgu = torch.zeros_like(wgu)
+    dwd = torch.zeros_like(wd)
+    off = saved["off"]
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        if r1 == r0:
+            continue
+        gemm_layout(dyp[r0:r1], saved["ap"][r0:r1], dwd[e], a_mn=True, b_mn=True)
+        gemm_layout(dyp[r0:r1], wd[e], dgup[r0:r1], b_mn=True, epilogue=_lib.EPI_SWIGLU_BWD,
+                    residual=saved["gup"][r0:r1])
+        gemm_layout(dgup[r0:r1], saved["xp"][r0:r1], dwgu[e], a_mn=True, b_mn=True)
+        gemm_layout(dgup[r0:r1], wgu[e], dxp[r0:r1], b_mn=True)
+    ds = moe_gate_bwd(saved["idx"], saved["gates"], dgates, E)
+    dwr = torch.empty_like(wr)
+    gemm_layout(ds, x, dwr, a_mn=True, b_mn=True)
+    dx_router = torch.empty(N, d, device=x.device, dtype=BF16)
+    gemm_layout(ds, wr, dx_router, b_mn=True)
+    dx = moe_scatter_bwd(dxp, saved["pos"], N, k, dres=dx_router)
+    return dx, dwr, dwgu, dwd
+

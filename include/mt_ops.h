@@ -153,6 +153,40 @@ int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, co
 int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* g, const float* rstd, const void* dres,
                               void* dx, void* dg, int64_t rows, int32_t d, void* stream);
 
+/*
+ * Mixture-of-experts MLP pieces (the expert GEMMs run on mt_op_gemm /
+ * mt_op_gemm_layout over each expert's rows).  N tokens, E experts (1..256),
+ * top k (1..min(8, E)), pairs p = n*k + j (P = N*k), d a multiple of 8.
+ * Routing: per token the k largest router logits (ties to the lower expert
+ * id), gates = softmax over them; the pairs are then sorted by expert, stably.
+ *
+ * mt_op_moe_route: logits FP32 [N, E] -> idx int32 [N, k], gates FP32 [N, k],
+ *   order int32 [P] (pair at each position), pos int32 [P] (position of each
+ *   pair), offsets int32 [E + 1] (first position of each expert, offsets[E] =
+ *   P); scratch: mt_op_moe_sort_scratch_ints(P, E) int32 values.
+ * mt_op_moe_gather: xp[i] = x[order[i] / k] (BF16 rows, x rows ldx apart).
+ * mt_op_moe_combine: out[n] = res[n] + sum_j gates[n, j] yp[pos[n k + j]]
+ *   (BF16 rows, FP32 sums in slot order; res may be NULL).
+ * mt_op_moe_combine_bwd: dyp[pos[p]] = gates[p] dy[n] (BF16),
+ *   dgates[p] = <dy[n], yp[pos[p]]> (FP32).
+ * mt_op_moe_gate_bwd: ds [N, E] BF16 = softmax backward over the selected
+ *   logits (g_j (dg_j - sum_i g_i dg_i) at the selected experts, 0 elsewhere).
+ * mt_op_moe_scatter_bwd: dx[n] = dres[n] + sum_j dxp[pos[n k + j]] (dres may be NULL).
+ */
+int64_t mt_op_moe_sort_scratch_ints(int64_t P, int32_t E);
+int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_t* idx, float* gates, int32_t* order,
+                    int32_t* pos, int32_t* offsets, int32_t* scratch, void* stream);
+int mt_op_moe_gather(const void* x, int64_t ldx, const int32_t* order, int32_t k, int64_t P, int32_t d, void* xp,
+                     void* stream);
+int mt_op_moe_combine(const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k, int32_t d,
+                      const void* res, void* out, void* stream);
+int mt_op_moe_combine_bwd(const void* dy, const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k,
+                          int32_t d, void* dyp, float* dgates, void* stream);
+int mt_op_moe_gate_bwd(const int32_t* idx, const float* gates, const float* dgates, int64_t N, int32_t E, int32_t k,
+                       void* ds, void* stream);
+int mt_op_moe_scatter_bwd(const void* dxp, const int32_t* pos, int64_t N, int32_t k, int32_t d, const void* dres,
+                          void* dx, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

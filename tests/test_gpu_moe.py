@@ -1,0 +1,93 @@
+"""MoE MLP on the device (routing, counting sort, gather, expert GEMMs,
+combine and their backward) against the FP64 MoE oracle."""
+import pytest
+import torch
+
+from oracle import moe
+
+pytestmark = pytest.mark.gpu
+
+hms = pytest.importorskip("host_memory_streamed_gb300")
+from host_memory_streamed_gb300 import ops  # noqa: E402
+
+D = torch.float64
+DEV = "cuda"
+
+
+def rel(a, b):
+    a, b = a.to(D).cpu(), b.to(D).cpu()
+    return float((a - b).norm() / b.norm().clamp_min(1e-300))
+
+
+def cos(a, b):
+    a, b = a.to(D).cpu().reshape(-1), b.to(D).cpu().reshape(-1)
+    return float(a @ b / (a.norm() * b.norm()).clamp_min(1e-300))
+
+
+@pytest.mark.parametrize("N,E,k", [(300, 8, 2), (1000, 64, 4), (37, 5, 5), (128, 256, 8)])
+def test_route_and_sort(N, E, k):
+    g = torch.Generator().manual_seed(N + E + k)
+    logits = torch.randn(N, E, generator=g)
+    logits[0, :] = 0.5  # one token whose logits all tie: the lower ids win
+    idx, gates, order, pos, offsets = ops.moe_route(logits.to(DEV), k)
+    torch.cuda.synchronize()
+    _, idx_ref, gates_ref = moe.moe_route(logits.to(D), torch.eye(E, dtype=D), k)  # x = logits, W_r = I
+    assert torch.equal(idx.cpu().long(), idx_ref)
+    assert torch.allclose(gates.cpu().to(D), gates_ref, rtol=1e-5, atol=1e-7)
+    flat = idx.cpu().reshape(-1).long()
+    order, pos, offsets = order.cpu().long(), pos.cpu().long(), offsets.cpu().long()
+    assert torch.equal(offsets, torch.cat([torch.zeros(1, dtype=torch.long), torch.bincount(flat, minlength=E).cumsum(0)]))
+    assert torch.equal(pos[order], torch.arange(N * k))
+    for e in range(E):
+        seg = order[offsets[e]:offsets[e + 1]]
+        assert torch.all(flat[seg] == e) and torch.all(seg[1:] > seg[:-1])  # stable: pair order kept
+
+
+def _moe_weights(E, d, Fh, seed):
+    g = torch.Generator().manual_seed(seed)
+    wr = (torch.randn(E, d, generator=g) * 0.3).to(torch.bfloat16)
+    wg = (torch.randn(E, Fh, d, generator=g) * 0.05).to(torch.bfloat16)
+    wu = (torch.randn(E, Fh, d, generator=g) * 0.05).to(torch.bfloat16)
+    wd = (torch.randn(E, d, Fh, generator=g) * 0.05).to(torch.bfloat16)
+    wgu = torch.stack([wg, wu], dim=2).reshape(E, 2 * Fh, d)  # gate/up rows interleaved
+    experts = [{"wg": wg[e].to(D), "wu": wu[e].to(D), "wd": wd[e].to(D)} for e in range(E)]
+    return wr, wgu, wd, experts
+
+
+@pytest.mark.parametrize("N,E,k,d,Fh", [(256, 8, 2, 128, 96), (200, 16, 4, 64, 136)])
+def test_moe_mlp_matches_oracle(N, E, k, d, Fh):
+    wr, wgu, wd, experts = _moe_weights(E, d, Fh, N + E)
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(N, d, generator=g).to(torch.bfloat16)
+    dy = (torch.randn(N, d, generator=g) * 0.1).to(torch.bfloat16)
+    y, saved = ops.moe_mlp_forward(x.to(DEV), wr.to(DEV), wgu.to(DEV), wd.to(DEV), k)
+    dx, dwr, dwgu, dwd = ops.moe_mlp_backward(dy.to(DEV), x.to(DEV), wr.to(DEV), wgu.to(DEV), wd.to(DEV), k, saved)
+    torch.cuda.synchronize()
+    y_ref, cache = moe.moe_mlp_forward(x.to(D), wr.to(D), experts, k)
+    # the selection is an integer decision: both sides must have made the same one
+    assert torch.equal(saved["idx"].cpu().long(), cache["idx"])
+    dx_ref, dwr_ref, dex_ref = moe.moe_mlp_backward(dy.to(D), x.to(D), wr.to(D), experts, k, cache)
+    assert rel(y, y_ref) < 1e-2
+    for mine, ref in [(dx, dx_ref), (dwr, dwr_ref)]:
+        assert cos(mine, ref) > 0.999 and rel(mine, ref) < 2e-2
+    dwg_ref = torch.stack([e["wg"] for e in dex_ref])
+    dwu_ref = torch.stack([e["wu"] for e in dex_ref])
+    dwd_ref = torch.stack([e["wd"] for e in dex_ref])
+    dwgu_ref = torch.stack([dwg_ref, dwu_ref], dim=2).reshape(E, 2 * Fh, d)
+    for mine, ref in [(dwgu, dwgu_ref), (dwd, dwd_ref)]:
+        assert cos(mine, ref) > 0.999 and rel(mine, ref) < 2e-2
+
+
+def test_moe_mlp_deterministic():
+    N, E, k, d, Fh = 256, 8, 2, 128, 96
+    wr, wgu, wd, _ = _moe_weights(E, d, Fh, 77)
+    x = torch.randn(N, d, generator=torch.Generator().manual_seed(78)).to(torch.bfloat16).to(DEV)
+    dy = torch.randn(N, d, generator=torch.Generator().manual_seed(79)).to(torch.bfloat16).to(DEV)
+    outs = []
+    for _ in range(2):
+        y, saved = ops.moe_mlp_forward(x, wr.to(DEV), wgu.to(DEV), wd.to(DEV), k)
+        grads = ops.moe_mlp_backward(dy, x, wr.to(DEV), wgu.to(DEV), wd.to(DEV), k, saved)
+        outs.append([y] + list(grads))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
