@@ -8,15 +8,23 @@
 // "GPU Compute Dispatch": the layer templates hold the attention and MLP
 // kernels; the kernels themselves are this library's own design).
 //
-// Design (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: 128x64 A box + 256x64 B box per stage, 128-byte
-//               swizzle, STAGES-deep ring of shared-memory stages.
-//   warp 1      MMA issuer: one elected thread issues tcgen05.mma (M=128,
-//               N=256, K=16) into one of two TMEM accumulators (2 x 256 FP32
-//               columns), commits stage release and accumulator-ready.
+// Two kernels with the same warp roles, persistent over output tiles:
+//   gemm_bf16_tcgen05_pair_kernel (every GEMM with M > 128): clusters of two
+//     CTAs on two SMs share one 256 x 256 tile; each CTA stages its 128 rows
+//     of A and its half of B (6-stage ring), the even CTA issues
+//     tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and its commits arrive on
+//     both CTAs' barriers.  Per SM 32 KB of operands per 64-wide K block.
+//   gemm_bf16_tcgen05_kernel (M <= 128, or no pair placeable): one CTA per SM,
+//     128 x 256 tiles, tcgen05.mma M=128, N=256, K=16, 4-stage ring.
+// Warp roles (both):
+//   warp 0      TMA producer: 128-byte-swizzled boxes into the stage ring.
+//   warp 1      MMA issuer: one elected thread issues the MMAs into one of two
+//               TMEM accumulators (2 x 256 FP32 columns), commits stage
+//               release and accumulator-ready.
 //   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread, fused
 //               epilogue (bf16 / fp32 store, residual add, SwiGLU on
-//               interleaved gate/up columns, rotate-half RoPE, fp32 +=),
+//               interleaved gate/up columns, the SwiGLU backward through a
+//               per-warp shared-memory transpose, rotate-half RoPE, fp32 +=),
 //               16-byte stores.  The second accumulator lets the epilogue of
 //               tile i overlap the main loop of tile i+1.
 // Every mbarrier wait is bounded (2 s); on expiry the kernel records
