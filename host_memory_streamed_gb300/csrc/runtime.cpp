@@ -10,19 +10,22 @@
 //                   pinned staging chunks while the other chunk's DMA runs,
 //                   and records Weights-Ready[v].
 //   d2h thread      D2H stream: after Grads-Done[v], copies the gradient buffer
-//                   into free pinned slabs (12 by default) and records
-//                   Grads-Evacuated[v] so the compute stream may reuse it.
+//                   (layers alternate two; the head and the embedding rows use
+//                   a third) into free pinned slabs (24 x 64 MiB by default)
+//                   and records Grads-Evacuated[v] so the compute stream may
+//                   reuse the buffer.
 //   accumulator     copies each landed slab into the tile's G section, returns
-//                   the slab, and hands a completed tile to the Adam pool.
-//   Adam pool       updates W, M, V of finished tiles while the GPU keeps
+//                   the slab, and hands the slab's range to the Adam pool.
+//   Adam pool       updates W, M, V of each landed range while the GPU keeps
 //                   working on earlier layers.
 //
 // MegaTrain sources: paperlayer.ai summary §3 (execution workflow, three
 // streams, background gradient evacuation), §A.1 (layer-contiguous tiles,
 // pinned slab recycling, two pinned staging buffers), §A.2 (ComputeStream /
 // WeightStream / GradStream; weights-ready, backward-done and buffer-free
-// events), §A.3 (flat-buffer streaming with one copy per layer, K=12 pinned
-// gradient slabs with a background accumulator, preallocated workspaces),
+// events), §A.3 (flat-buffer streaming with one copy per layer, pinned
+// gradient slabs (12 there) with a background accumulator, preallocated
+// workspaces),
 // §A.4 (stateless templates, ping-pong binding, no CUDA graphs); hyper.ai
 // summary 方法 ¶2-6 (block recompute order, JIT packer thread, Weights-Ready
 // event before Bind); author's blog (per-block F/W/G figure).
