@@ -330,7 +330,11 @@ def main():
         free, _ = torch.cuda.mem_get_info(device)
         chunk = 0 if hms.StreamedDecoder.required_device_bytes(s) < 0.9 * free else 65536
     t_init = time.perf_counter()
-    model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device, mlp_chunk_rows=chunk)
+    # replicas share the host's cores: split the Adam workers (3/4 of the cores, the library's
+    # own default for one process) between them instead of oversubscribing
+    adam_threads = max(2, (os.cpu_count() or 4) * 3 // 4 // world) if world > 1 else 0
+    model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device, mlp_chunk_rows=chunk,
+                                           n_adam_threads=adam_threads)
     load_synthetic_weights(model, s, device)
     init_s = time.perf_counter() - t_init
     toks = token_batches(s, args.warmup + args.steps, device)
