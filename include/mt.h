@@ -212,7 +212,10 @@ int mt_train_step_micro(mt_model* m, const int32_t* tokens, size_t n_tokens, int
 
 /*
  * Data-parallel replicas (one handle per GPU, each on its own batch) combine
- * their gradients on the host between these two calls:
+ * their gradients on the host between these two calls.  The pages leave
+ * several GPUs as future work (engineersofai.com breakdown, limitations;
+ * author's blog, planned projects: single-machine multi-GPU training); this
+ * is the host-side gradient average that needs no device collective:
  *
  * mt_train_step_grads: mt_train_step without the optimizer.  Afterwards every
  * tile's G section holds the BF16 gradient of the mean loss over this batch's

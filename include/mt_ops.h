@@ -155,7 +155,10 @@ int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* g, cons
 
 /*
  * Mixture-of-experts MLP pieces (the expert GEMMs run on mt_op_gemm /
- * mt_op_gemm_layout over each expert's rows).  N tokens, E experts (1..256),
+ * mt_op_gemm_layout over each expert's rows).  MegaTrain's largest run
+ * trains an MoE model (author's blog, the single-H200 gpt-oss 120B run;
+ * podcast transcript, the 120B GPT-OSS run); the pages give no formula for
+ * the MoE layer, so this is the plainest top-k reading.  N tokens, E experts (1..256),
  * top k (1..min(8, E)), pairs p = n*k + j (P = N*k), d a multiple of 8.
  * Routing: per token the k largest router logits (ties to the lower expert
  * id), gates = softmax over them; the pairs are then sorted by expert, stably.
