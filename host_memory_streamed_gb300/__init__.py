@@ -17,11 +17,24 @@ from ._lib import (MT_DEBUG_CHECKS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, M
                    MT_RESIDENT, MT_STORE_ACTS, MT_TIE_EMBEDDINGS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG,
                    ERROR_NAMES)
 
-__all__ = ["StreamedDecoder", "MtError", "ops", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
+__all__ = ["StreamedDecoder", "MtError", "ops", "plan_schedule", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
            "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_VISIT_LOG", "MT_TIE_EMBEDDINGS", "MT_PART_W",
            "MT_PART_G", "MT_PART_M", "MT_PART_V"]
 
 LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
+
+
+def plan_schedule(n_layers: int, ckpt_every: int = 1, flags: int = 0) -> list[dict]:
+    """The visit order of one training step (``mt_plan_schedule``): a list of
+    dicts with kind, tile, layer, buf, h2d, buf_wait, gbuf, gbuf_wait.  Host
+    only; needs no GPU."""
+    lib = _lib.lib()
+    n = lib.mt_plan_schedule(n_layers, ckpt_every, flags, None, 0)
+    if n < 0:
+        raise MtError(n, "mt_plan_schedule: bad arguments")
+    out = (_lib.MtVisit * n)()
+    lib.mt_plan_schedule(n_layers, ckpt_every, flags, out, n)
+    return [{f: getattr(v, f) for f, _ in _lib.MtVisit._fields_} for v in out]
 
 
 class MtError(RuntimeError):

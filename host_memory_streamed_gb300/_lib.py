@@ -46,6 +46,13 @@ class MtTileDesc(C.Structure):
                 ("w_bytes", C.c_int64), ("tile_bytes", C.c_int64), ("tensors", MtTensorDesc * 8)]
 
 
+class MtVisit(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("kind", "tile", "layer", "buf", "h2d", "buf_wait", "gbuf", "gbuf_wait")]
+
+
+VISIT_EMBED_FWD, VISIT_LAYER_FWD, VISIT_HEAD, VISIT_RECOMPUTE, VISIT_LAYER_BWD, VISIT_EMBED_BWD = range(6)
+
+
 class MtStepStats(C.Structure):
     _fields_ = [
         ("loss", C.c_double), ("step_ms", C.c_double), ("gpu_compute_ms", C.c_double),
@@ -75,6 +82,7 @@ def lib():
     sig = {
         "mt_required_device_bytes": (i64, [C.POINTER(MtConfig)]),
         "mt_init_model": (C.c_int, [C.POINTER(MtConfig), vp, sz, vp, vp, vp, C.POINTER(vp)]),
+        "mt_plan_schedule": (i32, [i32, i32, C.c_uint32, C.POINTER(MtVisit), i32]),
         "mt_tile_count": (C.c_int, [vp]),
         "mt_tile_info": (C.c_int, [vp, C.c_int, C.POINTER(MtTileDesc)]),
         "mt_load_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),

@@ -127,6 +127,9 @@ class Pool {
 
 // ------------------------------------------------------------------ schedule
 enum VisitKind { kEmbedFwd, kLayerFwd, kHead, kRecompute, kLayerBwd, kEmbedBwd };
+static_assert(kEmbedFwd == MT_VISIT_EMBED_FWD && kLayerFwd == MT_VISIT_LAYER_FWD && kHead == MT_VISIT_HEAD &&
+                  kRecompute == MT_VISIT_RECOMPUTE && kLayerBwd == MT_VISIT_LAYER_BWD && kEmbedBwd == MT_VISIT_EMBED_BWD,
+              "visit kinds of the C-ABI");
 
 struct Visit {
   VisitKind kind;
@@ -1495,6 +1498,18 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
 using mt::MtError;
 
 extern "C" {
+
+int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, uint32_t flags, mt_visit* out, int32_t cap) {
+  if (n_layers < 1 || ckpt_every < 1 || cap < 0) return MT_EINVAL;
+  const bool tied = flags & MT_TIE_EMBEDDINGS;
+  const auto v = mt::build_schedule(n_layers, ckpt_every, flags & MT_STORE_ACTS, flags & MT_NO_DOUBLE_BUFFER,
+                                    tied ? 0 : n_layers + 1);
+  for (int i = 0; out && i < (int)v.size() && i < cap; ++i) {
+    const mt::Visit& x = v[i];
+    out[i] = mt_visit{(int32_t)x.kind, x.tile, x.layer, x.buf, x.h2d ? 1 : 0, x.prev_user, x.gbuf, x.prev_gbuf_user};
+  }
+  return (int32_t)v.size();
+}
 
 int64_t mt_required_device_bytes(const mt_config* cfg) {
   if (!cfg) return MT_EINVAL;

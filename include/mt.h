@@ -177,6 +177,41 @@ int64_t mt_required_device_bytes(const mt_config* cfg);
 int mt_init_model(const mt_config* cfg, void* device_arena, size_t arena_bytes, void* stream_comp,
                   void* stream_h2d, void* stream_d2h, mt_model** out);
 
+/* One visit of the streamed schedule (mt_plan_schedule). */
+enum {
+  MT_VISIT_EMBED_FWD = 0, /* embedding forward (tile 0) */
+  MT_VISIT_LAYER_FWD = 1, /* layer forward; x_i kept when i % ckpt_every == 0 */
+  MT_VISIT_HEAD = 2,      /* final norm + LM head + cross-entropy, forward and backward */
+  MT_VISIT_RECOMPUTE = 3, /* layer forward again inside a checkpoint block (backward pass) */
+  MT_VISIT_LAYER_BWD = 4, /* layer backward (its internals recomputed from x_i in the same visit) */
+  MT_VISIT_EMBED_BWD = 5  /* embedding gradient rows (no weights needed on the device) */
+};
+typedef struct {
+  int32_t kind;      /* MT_VISIT_* */
+  int32_t tile;      /* host tile whose weights the visit binds */
+  int32_t layer;     /* decoder layer, -1 for the embedding and the head */
+  int32_t buf;       /* device weight buffer (0 or 1), -1 for none */
+  int32_t h2d;       /* 1: the tile streams into buf before the visit; 0: buf still holds it */
+  int32_t buf_wait;  /* previous visit that used buf (the copy waits for its Buffer-Free event), -1 none */
+  int32_t gbuf;      /* device gradient buffer (layers alternate 0 and 1; head and embedding 2), -1 none */
+  int32_t gbuf_wait; /* previous visit that used gbuf (its gradients must have left first), -1 none */
+} mt_visit;
+
+/*
+ * The visit order one mt_train_step runs for n_layers decoder layers,
+ * checkpoint interval ckpt_every (K) and flags (MT_STORE_ACTS,
+ * MT_NO_DOUBLE_BUFFER and MT_TIE_EMBEDDINGS matter; MT_RESIDENT models use the
+ * same order with every tile resident).  Host only, no handle: the forward
+ * visits every layer in order, the head follows, then the checkpoint blocks
+ * run in reverse (per block [s, e): layers s .. e-2 recomputed, then layers
+ * e-1 .. s backward), then the embedding gradient (MegaTrain paperlayer.ai
+ * summary, §3 "Execution workflow" and §A.3 "Block-wise recomputation").  A
+ * tile still held by one of the two buffers is not streamed again.  Writes at
+ * most cap visits to out (out may be NULL) and returns the number of visits,
+ * or MT_EINVAL for n_layers < 1, ckpt_every < 1 or cap < 0.
+ */
+int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, uint32_t flags, mt_visit* out, int32_t cap);
+
 int mt_tile_count(const mt_model* m);                                /* L + 2 (L + 1 with MT_TIE_EMBEDDINGS) */
 int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out);
 
