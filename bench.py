@@ -228,58 +228,86 @@ def token_batches(s, steps, device):
 def cpu_sample(s, repeats=1):
     """Time the oracle (FP32, all host cores) on one decoder layer of the workload.
 
-    Sample: forward + backward of one full-width layer on one sequence of up to
-    2048 tokens, plus Adam on that layer's parameters; the whole-model time is
-    that layer time x (layers + the LM head's FLOPs in layer units), giving
-    tokens/s for the full model at the sample's tokens per step.
+    Sample: forward + backward of one full-width layer on one whole sequence
+    (the workload's S, capped at 4096 tokens: the oracle materialises the
+    S x S score matrix of every head), then FP32 Adam on that layer's
+    parameters.  The layer's time at the workload's T = B * S is B sequences
+    plus one Adam update; the whole-model time is that x (layers + the LM
+    head's FLOPs in layer units), giving tokens/s for the full model.
     """
     import oracle
     from oracle import OracleConfig
     torch.set_num_threads(os.cpu_count() or 1)
-    seq = min(s.seq, 2048)
+    seq = min(s.seq, 4096)
     cfg = OracleConfig.from_shape(s)
     lw = {k: v.float() for k, v in mt_inputs.layer_weights(s, 0).items()}
     gen = torch.Generator().manual_seed(7)
     x = torch.randn(1, seq, s.d_model, generator=gen)
     dy = torch.randn(1, seq, s.d_model, generator=gen) * 1e-3
     cos, sin = oracle.rope_cos_sin(seq, s.head_dim, s.rope_theta, torch.float32)
-    times = []
+    t_seq, t_adam = [], []
     for _ in range(repeats):
         t0 = time.perf_counter()
         y, c = oracle.layer_forward(x, lw, cfg, cos, sin)
         _, grads = oracle.layer_backward(dy, c, lw, cfg, cos, sin)
+        t1 = time.perf_counter()
         for k, w in lw.items():
             z = torch.zeros_like(w)
-            oracle.adam_update(w.to(torch.bfloat16), grads[k].to(torch.bfloat16), z, z, 1, cfg)
-        times.append(time.perf_counter() - t0)
-    t_layer = statistics.median(times)
+            oracle.adam_update(w.to(torch.bfloat16), grads[k].to(torch.bfloat16), z, z, 1, cfg,
+                               dtype=torch.float32)
+        t2 = time.perf_counter()
+        t_seq.append(t1 - t0)
+        t_adam.append(t2 - t1)
+    ts, ta = statistics.median(t_seq), statistics.median(t_adam)
+    n_seq = s.batch * s.seq / seq
+    t_layer = n_seq * ts + ta
     q, kv = s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim
     lin = s.d_model * (q + 2 * kv) + q * s.d_model + 3 * s.d_model * s.ffn
     head_in_layers = (s.d_model * s.vocab) / lin
     t_model = t_layer * (s.n_layers + head_in_layers)
-    return {"value": seq / t_model, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
-            "sample": (f"oracle FP32 fwd+bwd+Adam of one {s.name} layer on 1x{seq} tokens "
-                       f"({t_layer:.2f} s), scaled to the full model as {s.n_layers} layers + "
-                       f"{head_in_layers:.2f} layer-equivalents of LM head"),
-            "layer_seconds": t_layer}
+    cpu = ""
+    try:
+        import platform
+        cpu = platform.machine()
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    cpu += ", " + line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    short = " (shorter than the workload's sequence: attention's share is understated)" if seq < s.seq else ""
+    return {"value": s.batch * s.seq / t_model, "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": (f"oracle FP32 fwd+bwd of one {s.name} layer on 1x{seq} tokens ({ts:.2f} s){short} and "
+                       f"FP32 Adam of its parameters ({ta:.2f} s); layer at T = {s.batch * s.seq} = "
+                       f"{n_seq:g} x that sequence + one Adam ({t_layer:.1f} s), scaled to the full model as "
+                       f"{s.n_layers} layers + {head_in_layers:.2f} layer-equivalents of LM head"),
+            "cpu": cpu, "sample_seconds": ts + ta, "layer_seconds": t_layer}
 
 
 def run_reference(args, s, rank):
+    """The reference arm: the oracle timed on the host cores.  A step is one
+    bounded sample (cpu_sample); ms_per_step is its measured wall time and
+    value the whole-model tokens/s that sample gives."""
     if rank != 0:
         return
     for _ in range(args.warmup):
         cpu_sample(s)
+    t0 = time.perf_counter()
     vals = [cpu_sample(s) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
     v = statistics.median(x["value"] for x in vals)
     t = statistics.median(x["layer_seconds"] for x in vals)
     line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1e3 * s.batch * s.seq / v, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": s.name, "layers": s.n_layers, "batch": s.batch, "seq": s.seq},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": vals[0]["cores"], "kind": "oracle",
-                             "sample": vals[0]["sample"]},
+                             "sample": vals[0]["sample"], "cpu": vals[0]["cpu"]},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "model_ms_per_step_extrapolated": 1e3 * s.batch * s.seq / v,
             "layer_seconds": t}
     print(json.dumps(line), flush=True)
 
@@ -394,6 +422,7 @@ def main():
     gemm_launches = sum(x["gemm_launches"] for x in stats)
     kernels = sum(x["kernel_launches"] for x in stats)
     p_sust = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    p_burst = peaks["bf16_tflops"]
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
     flops_exec = st["flops_executed"]
     flops_model = st["flops_model"]
@@ -425,7 +454,9 @@ def main():
                           "h2d_gbs_measured": h2d_bw, "d2h_gbs_measured": d2h_bw, "t_h2d_ms": 1e3 * t_h2d,
                           "t_d2h_ms": 1e3 * t_d2h, "bound": "tensor" if t_flops >= max(t_h2d, t_d2h) else "link",
                           "frac": step_roof / (ms_step * 1e-3),
-                          "peak": p_sust, "peak_kind": f"bf16_tflops_sustained ({peak_kind})"},
+                          "peak": p_sust, "peak_kind": f"bf16_tflops_sustained ({peak_kind})",
+                          "frac_vs_burst_peak": max(flops_exec / (p_burst * 1e12), t_h2d, t_d2h) / (ms_step * 1e-3),
+                          "peak_burst": p_burst},
         "overlap": {"copy_ms_per_step": copy_ms / args.steps, "compute_stall_on_weights_ms_per_step":
                     stall_ms / args.steps,
                     "hidden_frac": (1.0 - stall_ms / copy_ms) if copy_ms else None,
@@ -448,7 +479,7 @@ def main():
     }
     line["clocks"] = clk.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = {k: v for k, v in cpu_sample(s).items() if k != "layer_seconds"}
+        line["cpu_baseline"] = {k: v for k, v in cpu_sample(s).items() if k not in ("layer_seconds", "sample_seconds")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

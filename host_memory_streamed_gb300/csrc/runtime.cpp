@@ -867,14 +867,21 @@ void prepare_tokens(mt_model* m, const int32_t* tokens) {
 }
 
 // ------------------------------------------------------------------ FLOP accounting
+// layer_fwd: one layer's forward; layer_internal: the internals that a
+// backward visit recomputes (the forward without the down projection, whose
+// output the backward does not need); head_fwd: the LM head's forward.
+// Attention counts the causal half of QK^T and PV; a backward counts as two
+// forwards (the usual convention for the model FLOPs).
 struct Flops {
-  double layer_fwd, head_fwd;
+  double layer_fwd, layer_internal, head_fwd;
 };
 Flops flop_model(const Dims& D) {
   const double T = (double)D.T;
+  const double down = 2.0 * T * (double)D.f * D.d;
   const double lin = (double)D.d * D.Dqkv + (double)D.Dq * D.d + (double)D.d * 2.0 * D.f + (double)D.f * D.d;
   const double attn = 4.0 * D.B * D.Hq * D.hd * ((double)D.S * (D.S + 1) / 2.0);
-  return Flops{2.0 * T * lin + attn, 2.0 * T * (double)D.d * D.V};
+  const double fwd = 2.0 * T * lin + attn;
+  return Flops{fwd, fwd - down, 2.0 * T * (double)D.d * D.V};
 }
 
 // ------------------------------------------------------------------ the step
@@ -1149,11 +1156,17 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     st.adam_ms = m->adam_us.load() / 1000.0;
     st.adam_tail_ms = std::chrono::duration<double, std::milli>(adam_end - m->last_grads_landed).count();
     const Flops fm = flop_model(D);
-    int n_fwd = 0;
-    for (const auto& x : m->visits)
-      if (x.kind == kLayerFwd || x.kind == kRecompute || (x.kind == kLayerBwd && !m->store_acts)) ++n_fwd;
+    // executed: every forward visit and boundary recompute in full, every
+    // backward visit's internal recompute (when activations are not stored),
+    // each layer's backward, and the head's forward and backward once
+    int n_fwd = 0, n_internal = 0;
+    for (const auto& x : m->visits) {
+      if (x.kind == kLayerFwd || x.kind == kRecompute) ++n_fwd;
+      if (x.kind == kLayerBwd && !m->store_acts) ++n_internal;
+    }
     st.flops_model = (int64_t)(3.0 * (D.L * fm.layer_fwd + fm.head_fwd));
-    st.flops_executed = (int64_t)(n_fwd * fm.layer_fwd + 2.0 * D.L * fm.layer_fwd + 3.0 * fm.head_fwd);
+    st.flops_executed = (int64_t)(n_fwd * fm.layer_fwd + n_internal * fm.layer_internal + 2.0 * D.L * fm.layer_fwd +
+                                  3.0 * fm.head_fwd);
     st.arena_high_water = m->arena_used;
     if (status != 0) {
       if (status == kStatusGemmTimeout)

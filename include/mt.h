@@ -150,7 +150,9 @@ typedef struct {
   int64_t gemm_launches;
   int64_t kernel_launches; /* kernels launched by the step */
   int64_t h2d_bytes, d2h_bytes;
-  int64_t flops_executed;  /* all matmul FLOPs the step ran, recompute included */
+  int64_t flops_executed;  /* matmul FLOPs of the schedule: forward visits and boundary recomputes in full,
+                              each backward visit's internal recompute without the down projection, each
+                              layer's backward at 2x its forward, the head's forward + backward once */
   int64_t flops_model;     /* 6 * N_linear * T + causal-attention FLOPs (3x forward) */
   int64_t arena_high_water;
   int64_t step;            /* Adam step counter after this step */
