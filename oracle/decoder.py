@@ -541,7 +541,7 @@ def model_loss_and_grads(params, tokens, cfg: OracleConfig, dtype=torch.float64)
 # Adam on the host tile (BF16 w, BF16 g, FP32 m and v)
 # ----------------------------------------------------------------------------
 
-def adam_update(w, g, m, v, step, cfg: OracleConfig):
+def adam_update(w, g, m, v, step, cfg: OracleConfig, dtype=torch.float64):
     """One bias-corrected Adam(W) step in the PyTorch convention.
 
     m <- b1 m + (1-b1) g;  v <- b2 v + (1-b2) g^2;
@@ -549,14 +549,15 @@ def adam_update(w, g, m, v, step, cfg: OracleConfig):
     w <- w - lr * (mhat / (sqrt(vhat) + eps) + wd * w)
 
     Inputs: w and g hold BF16 values, m and v FP32 values (any float dtype).
-    The arithmetic is FP64; the results are stored as the tile stores them:
-    m, v rounded to FP32 and w rounded to BF16 (ties to even).  Returns
-    (w_new, m_new, v_new) as FP64 tensors holding those rounded values.
+    The arithmetic is in ``dtype`` (FP64 for parity, FP32 for the timed CPU
+    baseline); the results are stored as the tile stores them: m, v rounded
+    to FP32 and w rounded to BF16 (ties to even).  Returns (w_new, m_new,
+    v_new) as FP64 tensors holding those rounded values.
     """
-    w = w.to(torch.float64)
-    g = g.to(torch.float64)
-    m = m.to(torch.float64)
-    v = v.to(torch.float64)
+    w = w.to(dtype)
+    g = g.to(dtype)
+    m = m.to(dtype)
+    v = v.to(dtype)
     t = float(step)
     m_new = cfg.beta1 * m + (1.0 - cfg.beta1) * g
     v_new = cfg.beta2 * v + (1.0 - cfg.beta2) * g * g

@@ -484,6 +484,22 @@ def test_adam_first_step_is_lr_times_sign():
     assert torch.allclose(v, 0.05 * g * g, rtol=1e-7)
 
 
+def test_adam_fp32_arithmetic_first_step_is_lr_times_sign():
+    """The FP32 arithmetic of the timed CPU baseline reaches the same closed
+    form at t = 1: update = lr * sign(g) where |g| >> eps, none where g = 0."""
+    s, cfg = _tiny()
+    w = torch.tensor([0.5, -0.25, 0.0078125, 3.0, 0.125]).to(torch.bfloat16).to(D)
+    g = torch.tensor([1e-3, -2e-5, 0.0, 7.0, -1e-6]).to(torch.bfloat16).to(D)
+    z = torch.zeros(5)
+    wn, m, v = oracle.adam_update(w, g, z, z, 1, cfg, dtype=torch.float32)
+    assert wn[2] == w[2]
+    big = g.abs() > 1e-4
+    assert torch.equal(wn[big], oracle.round_to_bf16(w - cfg.lr * torch.sign(g))[big])
+    w64, _, _ = oracle.adam_update(w, g, z, z, 1, cfg)
+    ulp = torch.ldexp(torch.ones_like(w64), torch.frexp(w64)[1] - 8)
+    assert ((wn - w64).abs() <= ulp).all()
+
+
 def test_adam_two_steps_exact_rationals():
     """Two Adam steps on three elements, worked in exact rational arithmetic
     (eps = 0 so the square roots are exact for these perfect-square inputs)."""
