@@ -110,6 +110,13 @@ class StreamedDecoder:
         if rc != 0:
             raise MtError(rc, self._L.mt_last_error(self._h).decode())
 
+    def debug_inject(self, what: int, visit: int = 0):
+        """Arm a host-side failure for the next step (``mt_debug_inject``):
+        one of the ``_lib.MT_INJECT_*`` kinds at the first visit >= ``visit``."""
+        rc = self._L.mt_debug_inject(self._h, what, visit)
+        if rc != 0:
+            raise MtError(rc, "mt_debug_inject: bad arguments")
+
     def close(self):
         if getattr(self, "_h", None):
             for s in self.streams:

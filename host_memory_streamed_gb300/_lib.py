@@ -50,6 +50,11 @@ class MtVisit(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("kind", "tile", "layer", "buf", "h2d", "buf_wait", "gbuf", "gbuf_wait")]
 
 
+# host-side fault injection (mt_debug_inject) and the device wait probe's status code
+(MT_INJECT_NONE, MT_INJECT_LOADER_FAIL, MT_INJECT_D2H_FAIL, MT_INJECT_ACCUM_FAIL, MT_INJECT_ADAM_FAIL,
+ MT_INJECT_LOADER_STALL) = range(6)
+MT_STATUS_WAIT_PROBE = 7
+
 VISIT_EMBED_FWD, VISIT_LAYER_FWD, VISIT_HEAD, VISIT_RECOMPUTE, VISIT_LAYER_BWD, VISIT_EMBED_BWD = range(6)
 
 
@@ -83,6 +88,8 @@ def lib():
         "mt_required_device_bytes": (i64, [C.POINTER(MtConfig)]),
         "mt_init_model": (C.c_int, [C.POINTER(MtConfig), vp, sz, vp, vp, vp, C.POINTER(vp)]),
         "mt_plan_schedule": (i32, [i32, i32, C.c_uint32, C.POINTER(MtVisit), i32]),
+        "mt_debug_inject": (C.c_int, [vp, i32, i32]),
+        "mt_op_wait_probe": (C.c_int, [vp, i64, vp]),
         "mt_tile_count": (C.c_int, [vp]),
         "mt_tile_info": (C.c_int, [vp, C.c_int, C.POINTER(MtTileDesc)]),
         "mt_load_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),

@@ -410,6 +410,19 @@ __global__ void check_finite_kernel(const bf16* __restrict__ p, long n, int* sta
 
 inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
 
+// Failure-detection probe (see launch_wait_probe): the barrier expects one
+// arrival and gets none, so phase 0 never completes and the bounded wait
+// must run out.
+__global__ void wait_probe_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait_for(&bar, 0, limit_ns)) set_status(status, kStatusWaitProbe);
+}
+
 }  // namespace
 
 void launch_rmsnorm_fwd(const bf16* x, const bf16* g, bf16* y, float* rstd, long rows, int d, float eps,
@@ -488,6 +501,11 @@ void launch_check_finite(const bf16* p, long n, int* status, cudaStream_t s) {
   unsigned nb = blocks_for(n, 256);
   if (nb > 152u * 16u) nb = 152u * 16u;
   check_finite_kernel<<<nb, 256, 0, s>>>(p, n, status);
+}
+
+int launch_wait_probe(int* status, uint64_t limit_ns, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return launch_result();
 }
 
 }  // namespace mt

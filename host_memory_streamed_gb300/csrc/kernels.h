@@ -20,7 +20,13 @@ enum : int {
   kStatusNonFinite = 4,
   kStatusAttnFwdTimeout = 5,
   kStatusAttnBwdTimeout = 6,
+  kStatusWaitProbe = 7,  // the wait probe's bounded wait ran out (its expected outcome)
 };
+
+// Failure-detection probe: one warp waits, bounded by limit_ns of
+// %globaltimer, on an mbarrier that nothing arrives on, then records
+// kStatusWaitProbe in *status and exits.
+int launch_wait_probe(int* status, uint64_t limit_ns, cudaStream_t s);
 
 // ----------------------------------------------------------------- GEMM
 enum EpiMode : int {

@@ -10,6 +10,8 @@
 #include "../../include/mt_ops.h"
 #include "kernels.h"
 
+static_assert((int)MT_STATUS_WAIT_PROBE == (int)mt::kStatusWaitProbe, "wait-probe status code");
+
 namespace {
 thread_local std::string g_op_error;
 int op_fail(const char* msg) {
@@ -195,6 +197,12 @@ int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, co
   mt::launch_embed_bwd(row_offsets, positions, static_cast<const mt::bf16*>(dx), static_cast<mt::bf16*>(dE), V, d,
                        static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "embedding backward");
+}
+
+int mt_op_wait_probe(int32_t* status, int64_t limit_ns, void* stream) {
+  if (!status || limit_ns < 1000000 || limit_ns > 5000000000LL)
+    return op_fail("wait probe: status required, limit between 1 ms and 5 s");
+  return op_cuda(mt::launch_wait_probe(status, (uint64_t)limit_ns, static_cast<cudaStream_t>(stream)), "wait probe");
 }
 
 int64_t mt_op_moe_sort_scratch_ints(int64_t P, int32_t E) { return mt::moe_sort_scratch_ints(P, E); }

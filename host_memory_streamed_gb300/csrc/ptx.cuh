@@ -105,6 +105,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Bounded wait with a caller-given limit (nanoseconds of %globaltimer).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
 // The same bounded wait done by all 32 lanes of a warp, with a warp-uniform
 // result: warps that go on to warp-collective (.sync.aligned) tcgen05
 // instructions must never split on a wait's outcome.

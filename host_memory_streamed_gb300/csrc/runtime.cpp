@@ -368,6 +368,9 @@ struct mt_model {
   std::atomic<bool> nonfinite{false};
   std::atomic<int> worker_code{0};
   std::string worker_msg;
+  // host-side fault injection (mt_debug_inject): fires once, in the next step
+  std::atomic<int> inject_what{MT_INJECT_NONE};
+  std::atomic<int> inject_visit{0};
 
   // threads
   std::unique_ptr<mt::Pool> adam_pool, pack_pool, acc_pool;
@@ -415,6 +418,17 @@ void worker_fail(mt_model* m, const MtError& e) {
     m->abort_flag = true;
   }
   m->cv.notify_all();
+}
+
+// True once for the armed injection `what` at the first visit >= its visit.
+bool inject_now(mt_model* m, int what, int visit) {
+  if (m->inject_what.load() != what || visit < m->inject_visit.load()) return false;
+  int expected = what;
+  return m->inject_what.compare_exchange_strong(expected, MT_INJECT_NONE);
+}
+
+MtError injected(const char* where, int visit) {
+  return MtError{MT_EINTERNAL, std::string("injected ") + where + " failure at visit " + std::to_string(visit)};
 }
 
 void check_abort(mt_model* m) {
@@ -501,6 +515,15 @@ void loader_main(mt_model* m) {
       for (int v = 0; v < (int)m->visits.size(); ++v) {
         const Visit& x = m->visits[v];
         if (!x.h2d) continue;
+        if (inject_now(m, MT_INJECT_LOADER_FAIL, v)) throw injected("loader", v);
+        if (inject_now(m, MT_INJECT_LOADER_STALL, v)) {
+          // stop without an error: the compute thread's Weights-Ready wait runs
+          // out; leave once the step has aborted (bounded in any case)
+          std::unique_lock<std::mutex> g(m->mu);
+          m->cv.wait_for(g, std::chrono::milliseconds(4 * m->cfg.timeout_ms),
+                         [&] { return m->abort_flag.load() || m->stop_threads; });
+          break;
+        }
         if (x.prev_user >= 0) {
           wait_flag(m, m->rec_free, x.prev_user, "buffer free");
           MT_CK(cudaStreamWaitEvent(m->s_h2d, m->ev_free[x.prev_user], 0));
@@ -555,6 +578,7 @@ void d2h_main(mt_model* m) {
     }
     try {
       check_abort(m);
+      if (inject_now(m, MT_INJECT_D2H_FAIL, v)) throw injected("D2H", v);
       const Visit& x = m->visits[v];
       const TileLayout& lay = m->layouts[x.tile];
       MT_CK(cudaStreamWaitEvent(m->s_d2h, m->ev_grads[v], 0));
@@ -747,6 +771,7 @@ void accum_main(mt_model* m) {
     }
     try {
       wait_event(m, m->ev_slab[j.slab], "gradient slab copy");
+      if (inject_now(m, MT_INJECT_ACCUM_FAIL, j.visit)) throw injected("accumulator", j.visit);
       const bool head = m->visits[j.visit].kind == kHead;
       if (head && j.off == 0) {
         if (!std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
@@ -805,7 +830,10 @@ void accum_main(mt_model* m) {
       }
       m->cv.notify_all();
       if (!m->nonfinite && m->last_pass()) {
-        if (!(head && m->tied)) {
+        if (inject_now(m, MT_INJECT_ADAM_FAIL, j.visit)) {
+          const int v = j.visit;
+          m->adam_pool->submit([m, v] { worker_fail(m, injected("Adam", v)); });
+        } else if (!(head && m->tied)) {
           submit_adam_range(m, j.tile, j.off, j.bytes);
         } else if (j.last && m->micro_count == 1) {
           // tied: E's rows wait for their embedding gradient unless no token
@@ -1214,6 +1242,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     m->adam_pool->wait_idle(m->cfg.timeout_ms);
     if (code != MT_EINVAL) m->broken = true;
   }
+  m->inject_what = MT_INJECT_NONE;  // an injection arms one step only
   return code;
 }
 
@@ -1561,6 +1590,13 @@ int mt_init_model(const mt_config* cfg, void* device_arena, size_t arena_bytes, 
     return MT_EINTERNAL;
   }
   *out = m;
+  return MT_OK;
+}
+
+int mt_debug_inject(mt_model* m, int32_t what, int32_t visit) {
+  if (!m || what < MT_INJECT_NONE || what > MT_INJECT_LOADER_STALL || visit < 0) return MT_EINVAL;
+  m->inject_visit = visit;
+  m->inject_what = what;
   return MT_OK;
 }
 

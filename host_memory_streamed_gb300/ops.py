@@ -70,6 +70,13 @@ def gemm_layout(A, B, out, a_mn=False, b_mn=False, epilogue=_lib.EPI_STORE_BF16,
                                       residual.stride(0) if residual is not None else 0, _ptr(status), _stream()))
 
 
+def wait_probe(status, limit_ns):
+    """Launch the failure-detection probe: a bounded wait that must run out
+    and record MT_STATUS_WAIT_PROBE in ``status`` (device int32)."""
+    _need(status, I32, "status")
+    _chk(_lib.lib().mt_op_wait_probe(status.data_ptr(), int(limit_ns), _stream()))
+
+
 def attention_fwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse, status=None):
     _need(qkv, BF16, "qkv")
     _need(o, BF16, "o")

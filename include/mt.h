@@ -214,6 +214,37 @@ typedef struct {
  */
 int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, uint32_t flags, mt_visit* out, int32_t cap);
 
+/*
+ * Host-side fault injection, for tests of failure detection that fault no
+ * GPU.  The next mt_train_step fails in the named host component at the
+ * first visit >= `visit` that the component works on:
+ *   MT_INJECT_LOADER_FAIL  the loader thread reports an error instead of
+ *                          streaming that visit's tile;
+ *   MT_INJECT_D2H_FAIL     the D2H thread reports an error instead of
+ *                          evacuating that visit's gradients;
+ *   MT_INJECT_ACCUM_FAIL   the accumulator reports an error on that visit's
+ *                          first gradient slab;
+ *   MT_INJECT_ADAM_FAIL    an Adam task of that visit's tile reports an error
+ *                          instead of updating;
+ *   MT_INJECT_LOADER_STALL the loader stops before that visit's copy without
+ *                          an error, so the compute thread's bounded wait for
+ *                          Weights-Ready runs out (MT_ETIMEDOUT after
+ *                          timeout_ms); the loader resumes its wait for the
+ *                          next step once the step has aborted.
+ * The failures return MT_EINTERNAL with "injected" in mt_last_error.  As after
+ * any such error, the handle then accepts only mt_get_layer_tile and
+ * mt_free.  Returns MT_EINVAL for an unknown kind or a negative visit.
+ */
+enum {
+  MT_INJECT_NONE = 0,
+  MT_INJECT_LOADER_FAIL = 1,
+  MT_INJECT_D2H_FAIL = 2,
+  MT_INJECT_ACCUM_FAIL = 3,
+  MT_INJECT_ADAM_FAIL = 4,
+  MT_INJECT_LOADER_STALL = 5
+};
+int mt_debug_inject(mt_model* m, int32_t what, int32_t visit);
+
 int mt_tile_count(const mt_model* m);                                /* L + 2 (L + 1 with MT_TIE_EMBEDDINGS) */
 int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out);
 

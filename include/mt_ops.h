@@ -154,6 +154,18 @@ int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* g, cons
                               void* dx, void* dg, int64_t rows, int32_t d, void* stream);
 
 /*
+ * Failure-detection probe.  Every spin-wait in the library's kernels is
+ * bounded by %globaltimer and, on expiry, records a code in the kernel's
+ * device status word and returns instead of hanging (a context that stays
+ * usable).  This probe exercises that path on purpose: one warp waits, for
+ * limit_ns (1 ms .. 5 s), on an mbarrier that nothing arrives on, then writes
+ * MT_STATUS_WAIT_PROBE (7) into *status (device int32, first error sticks)
+ * and exits.  MT_EINVAL for a null status or a limit out of range.
+ */
+enum { MT_STATUS_WAIT_PROBE = 7 };
+int mt_op_wait_probe(int32_t* status, int64_t limit_ns, void* stream);
+
+/*
  * Mixture-of-experts MLP pieces (the expert GEMMs run on mt_op_gemm /
  * mt_op_gemm_layout over each expert's rows).  MegaTrain's largest run
  * trains an MoE model (author's blog, the single-H200 gpt-oss 120B run;

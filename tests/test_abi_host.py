@@ -157,3 +157,12 @@ def test_chunked_mlp_shrinks_the_device_arena(lib):
     assert chunked > 0 and whole - chunked > 40e9
     assert chunked < 240e9
 
+
+
+def test_fault_injection_and_wait_probe_argument_checks(lib):
+    """Both entry points validate on the host before touching a handle or the device."""
+    from host_memory_streamed_gb300 import _lib
+    assert lib.mt_debug_inject(None, _lib.MT_INJECT_LOADER_FAIL, 0) == _lib.MT_EINVAL
+    assert lib.mt_op_wait_probe(None, 50_000_000, None) == _lib.MT_EINVAL
+    for limit in (0, 999_999, 5_000_000_001):
+        assert lib.mt_op_wait_probe(0x10000, limit, None) == _lib.MT_EINVAL
