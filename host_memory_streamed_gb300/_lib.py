@@ -32,7 +32,7 @@ class MtConfig(C.Structure):
         ("weight_decay", C.c_float),
         ("n_adam_threads", C.c_int32), ("n_pack_threads", C.c_int32), ("n_grad_slabs", C.c_int32),
         ("grad_slab_bytes", C.c_int64), ("stage_bytes", C.c_int64), ("timeout_ms", C.c_int64),
-        ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64),
+        ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64), ("n_experts", C.c_int32), ("top_k", C.c_int32),
     ]
 
 

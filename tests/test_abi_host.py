@@ -54,7 +54,9 @@ def test_required_device_bytes_positive_and_bounded(lib, name):
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=690), dict(ckpt_every=0),
                                  dict(vocab=0), dict(batch=0), dict(seq=3, batch=1), dict(mlp_chunk_rows=100),
-                                 dict(mlp_chunk_rows=128, flags=2)])
+                                 dict(mlp_chunk_rows=128, flags=2), dict(n_experts=12, top_k=2),
+                                 dict(n_experts=8, top_k=0), dict(n_experts=8, top_k=9), dict(n_experts=512, top_k=2),
+                                 dict(n_experts=8, top_k=2, mlp_chunk_rows=128)])
 def test_bad_config_rejected(lib, bad):
     s = mt_inputs.PRESETS["tiny"]
     assert lib.mt_required_device_bytes(C.byref(_cfg(s, **bad))) == -1
@@ -156,4 +158,18 @@ def test_chunked_mlp_shrinks_the_device_arena(lib):
     chunked = lib.mt_required_device_bytes(C.byref(_cfg(s, mlp_chunk_rows=65536)))
     assert chunked > 0 and whole - chunked > 40e9
     assert chunked < 240e9
+
+
+def test_moe_arena_grows_with_the_routed_pairs(lib):
+    """MoE layers: the device arena holds the routing, the permuted rows and the
+    experts' outputs of one layer pass, sized by tokens x top_k, and the same
+    per-layer weight buffers as the largest tile."""
+    s = mt_inputs.PRESETS["tiny"]
+    dense = lib.mt_required_device_bytes(C.byref(_cfg(s)))
+    k2 = lib.mt_required_device_bytes(C.byref(_cfg(s, n_experts=8, top_k=2)))
+    k4 = lib.mt_required_device_bytes(C.byref(_cfg(s, n_experts=8, top_k=4)))
+    assert 0 < dense < k2 < k4
+    T, d, F = s.batch * s.seq, s.d_model, s.ffn
+    # two more pairs per token add at least their rows of xp, yp, dyp, dxp (d each), ap (F), gup and dgup (2F)
+    assert k4 - k2 >= 2 * T * (4 * d + F + 4 * F) * 2
 

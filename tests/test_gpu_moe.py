@@ -91,3 +91,58 @@ def test_moe_mlp_deterministic():
     torch.cuda.synchronize()
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ MoE layers in the streamed step
+def _moe_shape(E, k):
+    import mt_inputs
+    return mt_inputs.PRESETS["tiny"].with_(n_experts=E, top_k=k, ffn=136)
+
+
+def _moe_run(s, steps=1, flags=0):
+    import mt_inputs
+    m = hms.StreamedDecoder.from_shape(s, flags=flags)
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    m.load_weights(params)
+    out = {"params0": params, "loss": [], "w": [], "g": [], "mv": []}
+    for n in range(1, steps + 1):
+        out["loss"].append(m.train_step(mt_inputs.step_tokens(s, n)))
+        out["w"].append(m.weights())
+        out["g"].append(m.grads())
+        out["mv"].append(m.moments())
+    m.close()
+    return out
+
+
+def test_moe_step_with_every_expert_matches_oracle():
+    """k = E: every token uses every expert, so no selection is involved and
+    the step must match the oracle within the library's usual tolerances."""
+    import mt_inputs
+    from oracle import OracleConfig
+    from tests import parity
+    s = _moe_shape(8, 8)
+    cfg = OracleConfig.from_shape(s)
+    r = _moe_run(s)
+    loss, grads = moe.moe_model_loss_and_grads(r["params0"], mt_inputs.step_tokens(s, 1), cfg, s.top_k)
+    assert abs(r["loss"][0] - loss) <= parity.LOSS_RTOL * abs(loss)
+    parity.assert_grads_close(r["g"][0], grads)
+    m, v = r["mv"][0]
+    parity.assert_adam_matches(r["w"][0], r["params0"], r["g"][0], m, v, 1, cfg)
+
+
+def test_moe_step_top2_streamed_equals_resident_and_loss_close():
+    """Top-2 of 16 experts: streamed == resident bit for bit (routing is
+    deterministic), and the loss is the oracle's (a near-tie routed
+    differently moves the loss by far less than the tolerance)."""
+    import mt_inputs
+    from oracle import OracleConfig
+    from tests import parity
+    s = _moe_shape(16, 2)
+    a = _moe_run(s, steps=2)
+    b = _moe_run(s, steps=2, flags=hms.MT_RESIDENT)
+    assert a["loss"] == b["loss"]
+    for (n, x), (_, y) in zip(parity.flat_named(a["w"][-1]), parity.flat_named(b["w"][-1])):
+        assert torch.equal(x, y), n
+    cfg = OracleConfig.from_shape(s)
+    loss, _ = moe.moe_model_loss_and_grads(a["params0"], mt_inputs.step_tokens(s, 1), cfg, s.top_k)
+    assert abs(a["loss"][0] - loss) <= parity.LOSS_RTOL * abs(loss)
