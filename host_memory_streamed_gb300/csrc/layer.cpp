@@ -132,6 +132,18 @@ int LayerTemplate::gemm(const GemmArgs& g) const {
   return rc;
 }
 
+// One grouped launch (an MoE layer's expert GEMMs); the statistics count the
+// FLOPs of the `rows` routed rows (padding and skipped tiles excluded).
+int LayerTemplate::gemm_grouped(const GemmArgs& g, const int32_t* offsets, int groups, int mode, long rows) const {
+  const int rc = launch_gemm_grouped(g, offsets, groups, mode, s);
+  const double flops = mode == kGemmGroupRows ? 2.0 * rows * g.N * g.K : 2.0 * g.M * g.N * rows;
+  stats->kernels += 1;
+  stats->gemms += 1;
+  stats->gemm_flops += flops;
+  trace("grouped gemm");
+  return rc;
+}
+
 namespace {
 GemmArgs mk(const bf16* A, long lda, const bf16* B, long ldb, int M, int N, int K, int epi, void* C, long ldc,
             int* status) {
@@ -303,38 +315,29 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
 
 // ------------------------------------------------------------------ MoE layers
 // The MLP half of an MoE decoder layer: router logits n2 W_r^T (FP32), top-k
-// routing and the stable sort of the (token, slot) pairs by expert, the
-// routed rows of n2 gathered per expert, each expert's gate/up (+SwiGLU) and
-// down GEMMs on its rows, and the gate-weighted combine with the residual h.
-// The per-expert row counts are needed on the host to size the GEMMs, so the
-// stream is synchronised once here.
+// routing and the stable sort of the (token, slot) pairs by expert (each
+// expert's rows padded to a multiple of 64 with zero rows), the routed rows of
+// n2 gathered, the experts' gate/up (+SwiGLU) and down GEMMs as one grouped
+// launch each (the per-expert row counts stay on the device), and the
+// gate-weighted combine with the residual h.
 int LayerTemplate::moe_forward(const LayerView& w, LayerActs& a, bf16* x_out) const {
   const Dims& D = dm;
   const long T = D.T;
   const int E = D.E, k = D.k, F = D.f, d = D.d;
-  const long P = T * k;
+  const long P = T * k, R = moe_rows_capacity(P, E, kMoeRowAlign);
   int rc = 0;
   rc |= gemm(mk(a.n2, d, w.wr, d, (int)T, E, d, kEpiF32, a.moe_logits, E, ws->status));
   rc |= launch_moe_topk(a.moe_logits, T, E, k, a.moe_idx, a.moe_gates, s) ? 1 : 0;
-  rc |= launch_moe_sort(a.moe_idx, P, E, ws->moe_scratch, a.moe_order, a.moe_pos, a.moe_off, s) ? 1 : 0;
-  rc |= launch_moe_gather(a.n2, d, a.moe_order, k, P, d, a.moe_xp, s) ? 1 : 0;
+  rc |= launch_moe_sort(a.moe_idx, P, E, kMoeRowAlign, ws->moe_scratch, a.moe_order, a.moe_pos, a.moe_off, s) ? 1 : 0;
+  rc |= launch_moe_gather(a.n2, d, a.moe_order, k, R, d, a.moe_xp, s) ? 1 : 0;
   stats->kernels += 5;
-  if (cudaMemcpyAsync(ws->moe_off_host, a.moe_off, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return 1;
-  const int32_t* off = ws->moe_off_host;
-  for (int e = 0; e < E; ++e) {
-    const int r0 = off[e], rows = off[e + 1] - off[e];
-    if (rows <= 0) continue;
-    GemmArgs g = mk(a.moe_xp + (long)r0 * d, d, w.wgu + (long)e * 2 * F * d, d, rows, 2 * F, d, kEpiSwiGLU,
-                    a.moe_ap + (long)r0 * F, F, ws->status);
-    g.C2 = a.moe_gup + (long)r0 * 2 * F;
-    g.ldc2 = 2L * F;
-    rc |= gemm(g);
-    rc |= gemm(mk(a.moe_ap + (long)r0 * F, F, w.wd + (long)e * d * F, F, rows, d, F, kEpiStoreBf16,
-                  a.moe_yp + (long)r0 * d, d, ws->status));
-  }
+  trace("moe routing");
+  GemmArgs g = mk(a.moe_xp, d, w.wgu, d, (int)R, 2 * F, d, kEpiSwiGLU, a.moe_ap, F, ws->status);
+  g.C2 = a.moe_gup;
+  g.ldc2 = 2L * F;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupRows, P);
+  rc |= gemm_grouped(mk(a.moe_ap, F, w.wd, F, (int)R, d, F, kEpiStoreBf16, a.moe_yp, d, ws->status), a.moe_off, E,
+                     kGemmGroupRows, P);
   if (x_out) {
     rc |= launch_moe_combine(a.moe_yp, a.moe_pos, a.moe_gates, T, k, d, a.h, x_out, s) ? 1 : 0;
     stats->kernels += 1;
@@ -343,59 +346,41 @@ int LayerTemplate::moe_forward(const LayerView& w, LayerActs& a, bf16* x_out) co
 }
 
 // Backward of moe_forward (its internals recomputed for this visit): dn2 into
-// ws->dn; the experts' and the router's weight gradients into gv.  Experts
-// that received no row get zero gradients.
+// ws->dn; the experts' and the router's weight gradients into gv.  Every
+// expert GEMM is one grouped launch; experts that received no row get zero
+// gradients from the grouped weight-gradient GEMM itself.
 int LayerTemplate::moe_backward(const LayerView& w, const LayerActs& a, const bf16* dx_out,
                                 const LayerView& gv) const {
   const Dims& D = dm;
   const long T = D.T;
   const int E = D.E, k = D.k, F = D.f, d = D.d;
+  const long P = T * k, R = moe_rows_capacity(P, E, kMoeRowAlign);
   const Workspace& W = *ws;
   int rc = 0;
   rc |= launch_moe_combine_bwd(dx_out, a.moe_yp, a.moe_pos, a.moe_gates, T, k, d, W.moe_dyp, W.moe_dgates, s) ? 1 : 0;
-  stats->kernels += 1;
-  // this layer's per-expert row offsets (its activations may be stored ones)
-  if (cudaMemcpyAsync(W.moe_off_host, a.moe_off, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost, s) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return 1;
-  const int32_t* off = W.moe_off_host;
-  for (int e = 0; e < E; ++e) {
-    const int r0 = off[e], rows = off[e + 1] - off[e];
-    bf16* gwd = gv.wd + (long)e * d * F;
-    bf16* gwgu = gv.wgu + (long)e * 2 * F * d;
-    if (rows <= 0) {
-      launch_zero(gwd, sizeof(bf16) * (size_t)d * F, s);
-      launch_zero(gwgu, sizeof(bf16) * (size_t)2 * F * d, s);
-      stats->kernels += 2;
-      continue;
-    }
-    // dW_d[e] = dY^T A over the expert's rows (both operands MN-major)
-    GemmArgs g = mk(W.moe_dyp + (long)r0 * d, d, a.moe_ap + (long)r0 * F, F, d, F, rows, kEpiStoreBf16, gwd, F,
-                    W.status);
-    g.a_mn = g.b_mn = true;
-    rc |= gemm(g);
-    // da = dY W_d[e] and, in the epilogue, the SwiGLU backward against the kept gate/up pairs
-    g = mk(W.moe_dyp + (long)r0 * d, d, w.wd + (long)e * d * F, F, rows, F, d, kEpiSwiGLUBwd,
-           W.moe_dgup + (long)r0 * 2 * F, 2L * F, W.status);
-    g.b_mn = true;
-    g.R = a.moe_gup + (long)r0 * 2 * F;
-    g.ldr = 2L * F;
-    rc |= gemm(g);
-    // dW_gu[e] = dGU^T Xp
-    g = mk(W.moe_dgup + (long)r0 * 2 * F, 2L * F, a.moe_xp + (long)r0 * d, d, 2 * F, d, rows, kEpiStoreBf16, gwgu, d,
-           W.status);
-    g.a_mn = g.b_mn = true;
-    rc |= gemm(g);
-    // dXp = dGU W_gu[e]
-    g = mk(W.moe_dgup + (long)r0 * 2 * F, 2L * F, w.wgu + (long)e * 2 * F * d, d, rows, d, 2 * F, kEpiStoreBf16,
-           W.moe_dxp + (long)r0 * d, d, W.status);
-    g.b_mn = true;
-    rc |= gemm(g);
-  }
+  rc |= launch_moe_zero_pads(a.moe_order, R, d, W.moe_dyp, s) ? 1 : 0;  // the padding rows enter the K sums
+  stats->kernels += 2;
+  // dW_d[e] = dY_e^T A_e over each expert's rows (both operands MN-major)
+  GemmArgs g = mk(W.moe_dyp, d, a.moe_ap, F, d, F, (int)R, kEpiStoreBf16, gv.wd, F, W.status);
+  g.a_mn = g.b_mn = true;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupK, P);
+  // da = dY W_d[e] and, in the epilogue, the SwiGLU backward against the kept gate/up pairs
+  g = mk(W.moe_dyp, d, w.wd, F, (int)R, F, d, kEpiSwiGLUBwd, W.moe_dgup, 2L * F, W.status);
+  g.b_mn = true;
+  g.R = a.moe_gup;
+  g.ldr = 2L * F;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupRows, P);
+  // dW_gu[e] = dGU_e^T Xp_e
+  g = mk(W.moe_dgup, 2L * F, a.moe_xp, d, 2 * F, d, (int)R, kEpiStoreBf16, gv.wgu, d, W.status);
+  g.a_mn = g.b_mn = true;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupK, P);
+  // dXp = dGU W_gu[e]
+  g = mk(W.moe_dgup, 2L * F, w.wgu, d, (int)R, d, 2 * F, kEpiStoreBf16, W.moe_dxp, d, W.status);
+  g.b_mn = true;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupRows, P);
   // router: ds = softmax backward over the selected logits; dW_r = ds^T n2; dn2 += ds W_r
   rc |= launch_moe_gate_bwd(a.moe_idx, a.moe_gates, W.moe_dgates, T, E, k, W.moe_ds, s) ? 1 : 0;
-  GemmArgs g = mk(W.moe_ds, E, a.n2, d, E, d, (int)T, kEpiStoreBf16, gv.wr, d, W.status);
+  g = mk(W.moe_ds, E, a.n2, d, E, d, (int)T, kEpiStoreBf16, gv.wr, d, W.status);
   g.a_mn = g.b_mn = true;
   rc |= gemm(g);
   g = mk(W.moe_ds, E, w.wr, d, (int)T, d, E, kEpiStoreBf16, W.moe_dn2r, d, W.status);

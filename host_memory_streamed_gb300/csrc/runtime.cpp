@@ -203,7 +203,7 @@ struct Plan {
 
 struct ActsSizes {
   int64_t n1, rstd, qkv, o, lse, h, n2, gu, a, x;
-  int64_t moe_logits, moe_pairs_i32, moe_off, moe_gates, moe_xp, moe_ap, moe_gup, moe_yp;  // MoE layers only
+  int64_t moe_logits, moe_pairs_i32, moe_rows_i32, moe_off, moe_gates, moe_xp, moe_ap, moe_gup, moe_yp;  // MoE only
   int64_t total;
 };
 
@@ -220,16 +220,18 @@ ActsSizes acts_sizes(const Dims& D) {
   s.gu = D.E ? 0 : align_up(D.Tc * 2L * D.f * 2, 256);  // one MLP row chunk (the whole step when unchunked)
   s.a = D.E ? 0 : align_up(D.Tc * (int64_t)D.f * 2, 256);
   const int64_t P = D.T * (int64_t)D.k;  // (token, slot) pairs of an MoE layer
+  const int64_t R = D.E ? moe_rows_capacity(P, D.E, kMoeRowAlign) : 0;  // permuted rows, padding included
   s.moe_logits = align_up(D.T * (int64_t)D.E * 4, 256);
   s.moe_pairs_i32 = align_up(P * 4, 256);
+  s.moe_rows_i32 = align_up(R * 4, 256);
   s.moe_off = align_up((D.E + 1) * 4L, 256);
   s.moe_gates = s.moe_pairs_i32;
-  s.moe_xp = align_up(P * D.d * 2, 256);
-  s.moe_ap = align_up(P * D.f * 2, 256);
-  s.moe_gup = align_up(P * 2L * D.f * 2, 256);
+  s.moe_xp = align_up(R * D.d * 2, 256);
+  s.moe_ap = align_up(R * D.f * 2, 256);
+  s.moe_gup = align_up(R * 2L * D.f * 2, 256);
   s.moe_yp = s.moe_xp;
-  const int64_t moe = D.E ? s.moe_logits + 3 * s.moe_pairs_i32 + s.moe_off + s.moe_gates + s.moe_xp + s.moe_ap +
-                                s.moe_gup + s.moe_yp
+  const int64_t moe = D.E ? s.moe_logits + 2 * s.moe_pairs_i32 + s.moe_rows_i32 + s.moe_off + s.moe_gates +
+                                s.moe_xp + s.moe_ap + s.moe_gup + s.moe_yp
                           : 0;
   s.total = s.n1 + 2 * s.rstd + s.qkv + s.o + s.lse + s.h + s.n2 + s.gu + s.a + moe;
   return s;
@@ -265,7 +267,7 @@ LayerActs carve_acts(uint8_t* p, const Dims& D, bf16* x) {
     a.moe_idx = reinterpret_cast<int32_t*>(p);
     p += s.moe_pairs_i32;
     a.moe_order = reinterpret_cast<int32_t*>(p);
-    p += s.moe_pairs_i32;
+    p += s.moe_rows_i32;
     a.moe_pos = reinterpret_cast<int32_t*>(p);
     p += s.moe_pairs_i32;
     a.moe_off = reinterpret_cast<int32_t*>(p);
@@ -328,10 +330,10 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.status = reinterpret_cast<int*>(at(256));
   w.head_chunk = hc;
   if (D.E) {
-    const int64_t P = T * (int64_t)D.k;
-    w.moe_dyp = reinterpret_cast<bf16*>(at(P * D.d * 2));
-    w.moe_dgup = reinterpret_cast<bf16*>(at(P * 2L * D.f * 2));
-    w.moe_dxp = reinterpret_cast<bf16*>(at(P * D.d * 2));
+    const int64_t P = T * (int64_t)D.k, R = moe_rows_capacity(P, D.E, kMoeRowAlign);
+    w.moe_dyp = reinterpret_cast<bf16*>(at(R * D.d * 2));
+    w.moe_dgup = reinterpret_cast<bf16*>(at(R * 2L * D.f * 2));
+    w.moe_dxp = reinterpret_cast<bf16*>(at(R * D.d * 2));
     w.moe_ds = reinterpret_cast<bf16*>(at(T * (int64_t)D.E * 2));
     w.moe_dn2r = reinterpret_cast<bf16*>(at(td));
     w.moe_dgates = reinterpret_cast<float*>(at(P * 4));
@@ -385,7 +387,6 @@ struct mt_model {
   std::vector<uint8_t*> slabs;
   int64_t slab_bytes = 0;
   float* pinned_scalars = nullptr;  // [0] loss, [1] status bits
-  int32_t* moe_off_host = nullptr;  // MoE layers: per-expert row offsets read back per layer pass
   int32_t* pinned_tok = nullptr;    // inp | tgt | emb_off | emb_pos | emb_rows
   int emb_u = 0;                    // number of distinct token ids of the step (rows of the compact dE)
   // micro-batches of the current step: pass micro_index of micro_count; gradients
@@ -1266,6 +1267,8 @@ const char* validate(const mt_config& c) {
   if (c.n_experts > 0) {
     if (c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts) return "top_k must be in 1 .. min(8, n_experts)";
     if (c.ffn % 8) return "MoE layers need ffn (the expert width) to be a multiple of 8";
+    if ((int64_t)c.batch * c.seq * c.top_k + 63LL * c.n_experts > 0x7fffffffLL)
+      return "MoE layers: batch * seq * top_k (plus padding) must fit int32 row positions";
     if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq)
       return "mlp_chunk_rows does not apply to MoE layers";
   }
@@ -1421,7 +1424,6 @@ void destroy(mt_model* m) {
     if (s) cudaFreeHost(s);
   if (m->pinned_scalars) cudaFreeHost(m->pinned_scalars);
   if (m->pinned_tok) cudaFreeHost(m->pinned_tok);
-  if (m->moe_off_host) cudaFreeHost(m->moe_off_host);
   for (auto t : m->tiles) std::free(t);
   delete m;
 }
@@ -1518,11 +1520,6 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_scalars), 256, cudaHostAllocDefault));
   const size_t ntok = (size_t)(3 * m->D.T + m->D.V + 1 + std::min<int64_t>(m->D.T, m->D.V));
   MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_tok), ntok * sizeof(int32_t), cudaHostAllocDefault));
-  if (m->D.E) {
-    MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->moe_off_host), (m->D.E + 1) * sizeof(int32_t),
-                        cudaHostAllocDefault));
-    m->ws.moe_off_host = m->moe_off_host;
-  }
 
   // RoPE tables (rotate-half; angle = s * theta^(-2i/hd)), computed in double
   {

@@ -48,6 +48,10 @@ struct TileLayout {
   bool has(const char* n) const;
 };
 
+// MoE layers pad each expert's permuted rows to a multiple of this (one K
+// block of the grouped weight-gradient GEMM).
+constexpr int kMoeRowAlign = 64;
+
 struct Dims {
   int L, d, Hq, Hkv, hd, f, V, B, S;
   int E = 0, k = 0;  // MoE layers: experts and experts per token (E = 0: dense)
@@ -124,8 +128,7 @@ struct Workspace {
   // MoE backward scratch
   bf16 *moe_dyp = nullptr, *moe_dgup = nullptr, *moe_dxp = nullptr, *moe_ds = nullptr, *moe_dn2r = nullptr;
   float* moe_dgates = nullptr;
-  int32_t* moe_scratch = nullptr;   // counting-sort scratch
-  int32_t* moe_off_host = nullptr;  // pinned host copy of the per-expert row offsets [E + 1]
+  int32_t* moe_scratch = nullptr;  // counting-sort scratch
 };
 
 // Counts what the launch sequences issued (for the step statistics).
@@ -158,6 +161,7 @@ struct LayerTemplate {
   }
 
   int gemm(const GemmArgs& g) const;
+  int gemm_grouped(const GemmArgs& g, const int32_t* offsets, int groups, int mode, long rows) const;
   // x -> x_out (x_out == nullptr: stop after the MLP activation).  keep_gu: also
   // store the gate/up pre-activations (needed by backward).
   int forward(const LayerView& w, LayerActs& a, bf16* x_out, bool keep_gu) const;
@@ -166,8 +170,8 @@ struct LayerTemplate {
   int backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, bf16* dx_in, const LayerView& gv) const;
   int mlp_backward_chunked(const LayerView& w, const LayerActs& a, const bf16* dx_out, const LayerView& gv) const;
   // MoE layers: the MLP half from n2 (and h for the residual) to x_out, and its
-  // backward from dx_out to dn2 in ws->dn (the per-expert row counts are read
-  // on the host, so both synchronise the compute stream once).
+  // backward from dx_out to dn2 in ws->dn; the per-expert row counts stay on
+  // the device (grouped GEMMs), so neither synchronises with the host.
   int moe_forward(const LayerView& w, LayerActs& a, bf16* x_out) const;
   int moe_backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, const LayerView& gv) const;
   // Final norm + LM head + cross-entropy, forward and backward in chunks.
