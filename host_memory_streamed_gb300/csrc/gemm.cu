@@ -773,17 +773,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      bool issued = false;  // any MMA at all (a grouped launch may leave a cluster without work)
       for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
+        // only kGroupK has a per-tile K; a group without rows has none, and its
+        // tiles skip the accumulator altogether (the epilogue stores zeros)
+        const int nk = GROUP == kGroupK ? pair_job<GROUP, B_MN>(tile, p, s_off, s_tstart, num_m, num_n, num_k).nk
+                                        : num_k;
+        if (GROUP == kGroupK && nk == 0) continue;
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1)) {
           set_status(p.status, kStatusGemmTimeout);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        // only kGroupK has a per-tile K (and a group without rows has none: its
-        // accumulator is left untouched and the epilogue stores zeros)
-        const int nk = GROUP == kGroupK ? pair_job<GROUP, B_MN>(tile, p, s_off, s_tstart, num_m, num_n, num_k).nk
-                                        : num_k;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase)) {
             set_status(p.status, kStatusGemmTimeout);
@@ -800,6 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          issued = true;
           tc_commit_pair_mc(&empty[stage], 0x3);
           if (++stage == P_STAGES) {
             stage = 0;
@@ -813,8 +816,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       // Every MMA issued above has completed (and stopped reading both CTAs'
       // shared memory and writing their TMEM) once this commit arrives.
-      tc_commit_pair(done);
-      if (!mbar_wait(done, 0)) set_status(p.status, kStatusGemmTimeout);
+      if (issued) {
+        tc_commit_pair(done);
+        if (!mbar_wait(done, 0)) set_status(p.status, kStatusGemmTimeout);
+      }
     }
   } else {
     const int quarter = warp & 3;
@@ -824,6 +829,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     for (int tile = cluster; tile < num_tiles; tile += num_clusters) {
       const PairJob jb = pair_job<GROUP, B_MN>(tile, p, s_off, s_tstart, num_m, num_n, num_k);
+      if (GROUP == kGroupK && jb.nk == 0) {
+        // a group without rows: the product is zero; no accumulator was used
+        EpiParams q = p;
+        q.M = jb.row_lim;
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          epilogue_chunk(q, jb.c_row0 + row_in_tile, jb.tn * BN + c * 32, v);
+        }
+        continue;
+      }
       if (!mbar_wait_warp(&tfull[acc], acc_phase)) {
         set_status(p.status, kStatusGemmTimeout);
         break;
@@ -835,16 +852,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       } else {
         EpiParams q = p;
         q.M = jb.row_lim;
-        if (jb.nk > 0) {
-          store_tile(q, tbase, jb.c_row0 + row_in_tile, jb.tn, xpose);
-        } else {  // no K at all: the product is zero
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0.f;
-            epilogue_chunk(q, jb.c_row0 + row_in_tile, jb.tn * BN + c * 32, v);
-          }
-        }
+        store_tile(q, tbase, jb.c_row0 + row_in_tile, jb.tn, xpose);
       }
       tc_fence_before();
       if (leader)
