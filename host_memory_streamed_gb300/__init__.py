@@ -53,7 +53,7 @@ class StreamedDecoder:
     def __init__(self, n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, batch, seq, *,
                  ckpt_every=1, rms_eps=1e-5, rope_theta=1e4, lr=1e-4, beta1=0.9, beta2=0.95, adam_eps=1e-8,
                  weight_decay=0.0, n_adam_threads=0, n_pack_threads=0, n_grad_slabs=0, grad_slab_bytes=0,
-                 stage_bytes=0, timeout_ms=0, flags=0, mlp_chunk_rows=0, device=None):
+                 stage_bytes=0, timeout_ms=0, flags=0, mlp_chunk_rows=0, n_experts=0, top_k=0, device=None):
         if not torch.cuda.is_available():
             raise RuntimeError("a CUDA device is required (the library has no CPU path)")
         self._L = _lib.lib()
@@ -64,7 +64,7 @@ class StreamedDecoder:
                          adam_eps=adam_eps, weight_decay=weight_decay, n_adam_threads=n_adam_threads,
                          n_pack_threads=n_pack_threads, n_grad_slabs=n_grad_slabs,
                          grad_slab_bytes=grad_slab_bytes, stage_bytes=stage_bytes, timeout_ms=timeout_ms,
-                         flags=flags, mlp_chunk_rows=mlp_chunk_rows).items():
+                         flags=flags, mlp_chunk_rows=mlp_chunk_rows, n_experts=n_experts, top_k=top_k).items():
             setattr(cfg, k, v)
         self.cfg = cfg
         self.device = torch.device(device or "cuda")
@@ -101,6 +101,8 @@ class StreamedDecoder:
 
     @classmethod
     def from_shape(cls, s, **kw):
+        kw.setdefault("n_experts", getattr(s, "n_experts", 0))
+        kw.setdefault("top_k", getattr(s, "top_k", 0))
         return cls(s.n_layers, s.d_model, s.n_heads, s.n_kv_heads, s.head_dim, s.ffn, s.vocab, s.batch, s.seq,
                    ckpt_every=s.ckpt_every, rms_eps=s.rms_eps, rope_theta=s.rope_theta, lr=s.lr, beta1=s.beta1,
                    beta2=s.beta2, adam_eps=s.adam_eps, weight_decay=s.weight_decay, **kw)
@@ -161,6 +163,12 @@ class StreamedDecoder:
             return {"E": named["E"], "gf": named["gf"]} if self.tied else {"E": named["E"]}
         if kind == 2:
             return {"gf": named["gf"], "wh": named["wh"]}
+        if "experts" in named:  # MoE layer: experts stacked, each expert's gate/up rows interleaved
+            ex = named["experts"]
+            wgu = torch.cat([torch.stack([e["wg"], e["wu"]], dim=1).reshape(-1, e["wg"].shape[1]) for e in ex], 0)
+            return {"g1": named["g1"], "wqkv": torch.cat([named["wq"], named["wk"], named["wv"]], 0),
+                    "wo": named["wo"], "g2": named["g2"], "wr": named["wr"], "wgu": wgu,
+                    "wd": torch.cat([e["wd"] for e in ex], 0)}
         wgu = torch.stack([named["wg"], named["wu"]], dim=1).reshape(-1, named["wg"].shape[1])
         return {"g1": named["g1"], "wqkv": torch.cat([named["wq"], named["wk"], named["wv"]], 0),
                 "wo": named["wo"], "g2": named["g2"], "wgu": wgu, "wd": named["wd"]}
@@ -172,6 +180,13 @@ class StreamedDecoder:
         c = self.cfg
         q, kv = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
         wqkv, wgu = slots["wqkv"], slots["wgu"]
+        if "wr" in slots:
+            E, F, d = c.n_experts, c.ffn, c.d_model
+            wgu = wgu.reshape(E, 2 * F, -1)
+            wd = slots["wd"].reshape(E, d, F)
+            return {"g1": slots["g1"], "wq": wqkv[:q], "wk": wqkv[q:q + kv], "wv": wqkv[q + kv:],
+                    "wo": slots["wo"], "g2": slots["g2"], "wr": slots["wr"],
+                    "experts": [{"wg": wgu[e, 0::2], "wu": wgu[e, 1::2], "wd": wd[e]} for e in range(E)]}
         return {"g1": slots["g1"], "wq": wqkv[:q], "wk": wqkv[q:q + kv], "wv": wqkv[q + kv:],
                 "wo": slots["wo"], "g2": slots["g2"], "wg": wgu[0::2], "wu": wgu[1::2], "wd": slots["wd"]}
 

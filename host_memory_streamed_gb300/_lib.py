@@ -20,6 +20,7 @@ MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
 EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE, EPI_SWIGLU_BWD = range(7)
 GEMM_A_MN, GEMM_B_MN = 1, 2  # operand layouts of mt_op_gemm_layout
+GEMM_GROUP_ROWS, GEMM_GROUP_K = 1, 2  # groupings of mt_op_gemm_grouped
 
 
 class MtConfig(C.Structure):
@@ -32,7 +33,7 @@ class MtConfig(C.Structure):
         ("weight_decay", C.c_float),
         ("n_adam_threads", C.c_int32), ("n_pack_threads", C.c_int32), ("n_grad_slabs", C.c_int32),
         ("grad_slab_bytes", C.c_int64), ("stage_bytes", C.c_int64), ("timeout_ms", C.c_int64),
-        ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64),
+        ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64), ("n_experts", C.c_int32), ("top_k", C.c_int32),
     ]
 
 
@@ -120,8 +121,12 @@ def lib():
         "mt_op_cross_entropy": (C.c_int, [vp, i64, i32, vp, f32, vp, vp, vp, vp]),
         "mt_op_embedding_fwd": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp]),
         "mt_op_embedding_bwd": (C.c_int, [vp, vp, vp, vp, i32, i32, vp]),
+        "mt_op_gemm_grouped": (C.c_int, [vp, i64, vp, i64, i32, i32, i32, i32, i32, vp, i32, i32, vp, i64, vp, i64,
+                                         vp, i64, vp, vp]),
         "mt_op_moe_sort_scratch_ints": (i64, [i64, i32]),
-        "mt_op_moe_route": (C.c_int, [vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "mt_op_moe_rows_capacity": (i64, [i64, i32, i32]),
+        "mt_op_moe_route": (C.c_int, [vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "mt_op_moe_zero_pads": (C.c_int, [vp, i64, i32, vp, vp]),
         "mt_op_moe_gather": (C.c_int, [vp, i64, vp, i32, i64, i32, vp, vp]),
         "mt_op_moe_combine": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp, vp]),
         "mt_op_moe_combine_bwd": (C.c_int, [vp, vp, vp, vp, i64, i32, i32, vp, vp, vp]),

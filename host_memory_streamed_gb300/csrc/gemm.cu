@@ -73,8 +73,27 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_STAGE = PHALF * BK * 2;  // 16 KB
 constexpr int P_B_STAGE = PHALF * BK * 2;  // 16 KB
 constexpr int P_GROUP_M = 8;           // pair-tile raster: 8 M-tiles share each B panel
-constexpr int P_SMEM_USED = P_STAGES * (P_A_STAGE + P_B_STAGE) + 1024 + 256 + XPOSE_BYTES;
+// Grouped launches (one GEMM per expert of a mixture-of-experts layer in one
+// launch) keep the group's row offsets and tile prefix in shared memory.
+constexpr int kMaxGroups = 256;
+constexpr int P_GROUP_TABLE = 2 * (kMaxGroups + 4) * 4;
+constexpr int P_SMEM_USED = P_STAGES * (P_A_STAGE + P_B_STAGE) + 1024 + 256 + XPOSE_BYTES + P_GROUP_TABLE;
 static_assert(P_SMEM_USED <= SMEM_BYTES, "pair shared memory plan exceeds 227 KB");
+
+// Grouping of a pair launch (a compile-time kernel parameter):
+//   kGroupNone  one GEMM.
+//   kGroupM     per group g the rows offsets[g] .. offsets[g+1] of A (K-major,
+//               one buffer for all groups) times group g's B (stacked: rows
+//               g*N .. of a K-major B, K rows g*K .. of an MN-major B); C rows
+//               are A's rows.  Tiles past a group's last row are computed and
+//               not stored.
+//   kGroupK     per group g, C[g*M .. g*M + M) = A_g^T B_g where A_g, B_g are
+//               the rows offsets[g] .. offsets[g+1] of two MN-major operands
+//               (the K range of group g).  A group with no rows stores zeros.
+//               Every group's row count must be a multiple of 64 (one K block)
+//               or its last block reads the next group's rows.
+enum : int { kGroupNone = 0, kGroupM = 1, kGroupK = 2 };
+static_assert((int)kGroupM == (int)kGemmGroupRows && (int)kGroupK == (int)kGemmGroupK, "grouping codes");
 
 struct EpiParams {
   int M, N, K;
@@ -91,6 +110,8 @@ struct EpiParams {
   int head_dim;
   int seq;
   int* status;
+  const int32_t* group_off;  // grouped launches: [groups + 1] row offsets on the device
+  int groups;
 };
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& tm, int& tn, int group_m = GROUP_M) {
@@ -519,6 +540,118 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// One output tile of a pair launch: where its operands start, how many K
+// blocks it takes and where its rows go.
+struct PairJob {
+  int tn;       // N tile: output columns tn*BN ..
+  int a_m0;     // first of the tile's 256 rows of A (a row of K-major A, a column of MN-major A)
+  int b_n0;     // first of the tile's 256 rows of B (likewise)
+  int k0;       // first K of both operands' blocks (0 for K-major A; a group's first row for kGroupK)
+  int b_k0;     // first K of B's blocks when it differs (an MN-major B stacked along K)
+  int nk;       // K blocks
+  int c_row0;   // output row of the tile's first row
+  int row_lim;  // output rows >= row_lim are computed and not stored
+};
+
+// Group g's clamped row offsets; rows = max(off[g+1] - off[g], 0).  The
+// clamp to [0, cap] keeps every load and store of a grouped launch inside
+// its operands whatever the device-computed offsets hold.
+template <int GROUP>
+__device__ __forceinline__ int group_tiles(int rows, int num_m, int num_n) {
+  return GROUP == kGroupM ? ((rows + PM - 1) / PM) * num_n : num_m * num_n;
+}
+
+// Grouped launches: one warp fills s_off[0..groups] (clamped offsets) and
+// s_tstart[0..groups] (exclusive prefix of the groups' tile counts; the last
+// entry is the launch's tile count).  Lane l holds groups 8l .. 8l+7.
+template <int GROUP>
+__device__ __forceinline__ void load_group_table(const EpiParams& p, int num_m, int num_n, int* s_off,
+                                                 int* s_tstart) {
+  const int lane = threadIdx.x & 31;
+  const int cap = GROUP == kGroupM ? p.M : p.K;
+  auto clamped = [&](int g) { return min(max(p.group_off[g], 0), cap); };
+  int cnt[8];
+  int sum = 0;
+  int prev = lane * 8 < p.groups ? clamped(lane * 8) : 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int g = lane * 8 + q;
+    int t = 0;
+    if (g < p.groups) {
+      const int next = clamped(g + 1);
+      s_off[g] = prev;
+      t = group_tiles<GROUP>(max(next - prev, 0), num_m, num_n);
+      prev = next;
+    }
+    cnt[q] = t;
+    sum += t;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - sum;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int g = lane * 8 + q;
+    if (g < p.groups) s_tstart[g] = run;
+    run += cnt[q];
+  }
+  if (lane == 31) s_tstart[p.groups] = incl;
+  if (lane == 0) s_off[p.groups] = clamped(p.groups);
+}
+
+template <int GROUP, bool B_MN>
+__device__ __forceinline__ PairJob pair_job(int tile, const EpiParams& p, const int* s_off, const int* s_tstart,
+                                            int num_m, int num_n, int num_k) {
+  PairJob j;
+  int tm, tn;
+  if constexpr (GROUP == kGroupNone) {
+    tile_coords(tile, num_m, num_n, tm, tn, P_GROUP_M);
+    j.a_m0 = tm * PM;
+    j.b_n0 = tn * BN;
+    j.k0 = j.b_k0 = 0;
+    j.nk = num_k;
+    j.c_row0 = tm * PM;
+    j.row_lim = p.M;
+  } else {
+    // the group holding this tile: s_tstart[lo] <= tile < s_tstart[hi]
+    // (groups without tiles share their start with the next group)
+    int lo = 0, hi = p.groups;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_tstart[mid] <= tile)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int g = lo;
+    const int r0 = s_off[g], rows = max(s_off[g + 1] - r0, 0);
+    if constexpr (GROUP == kGroupM) {
+      tile_coords(tile - s_tstart[g], (rows + PM - 1) / PM, num_n, tm, tn, P_GROUP_M);
+      j.a_m0 = r0 + tm * PM;
+      j.b_n0 = (B_MN ? 0 : g * p.N) + tn * BN;
+      j.k0 = 0;
+      j.b_k0 = B_MN ? g * p.K : 0;
+      j.nk = num_k;
+      j.c_row0 = j.a_m0;
+      j.row_lim = r0 + rows;
+    } else {
+      tile_coords(tile - s_tstart[g], num_m, num_n, tm, tn, P_GROUP_M);
+      j.a_m0 = tm * PM;
+      j.b_n0 = tn * BN;
+      j.k0 = j.b_k0 = r0;
+      j.nk = (rows + BK - 1) / BK;
+      j.c_row0 = g * p.M + tm * PM;
+      j.row_lim = g * p.M + p.M;
+    }
+  }
+  j.tn = tn;
+  return j;
+}
+
 // The CTA-pair kernel.  Roles per CTA as in gemm_bf16_tcgen05_kernel; the
 // MMA warp of the odd CTA only takes part in the TMEM allocation.
 //   full[s]    leading CTA only: the leader's producer arms it with both
@@ -528,7 +661,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 //   tempty[a]  leading CTA only: the 8 epilogue warps of the pair arrive.
 // Every wait is bounded; after a timeout each role stops, records
 // kStatusGemmTimeout and both CTAs still meet at the final cluster barrier.
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int GROUP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_bf16_tcgen05_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                   const __grid_constant__ CUtensorMap tmap_b, EpiParams p) {
@@ -542,6 +675,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  int* s_off = reinterpret_cast<int*>(sB + P_STAGES * P_B_STAGE + 256 + XPOSE_BYTES);  // grouped only
+  int* s_tstart = s_off + kMaxGroups + 4;
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -549,10 +684,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1;
   const int num_clusters = gridDim.x >> 1;
-  const int num_m = (p.M + PM - 1) / PM;
+  const int num_m = (p.M + PM - 1) / PM;  // kGroupM: not used (per group)
   const int num_n = (p.N + BN - 1) / BN;
-  const int num_tiles = num_m * num_n;
-  const int num_k = (p.K + BK - 1) / BK;
+  const int num_k = (p.K + BK - 1) / BK;  // kGroupK: not used (per group)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
@@ -572,10 +706,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tmem_alloc_pair(tmem_holder, TMEM_COLS);
     tmem_relinquish_pair();
   }
+  if constexpr (GROUP != kGroupNone)
+    if (warp == 2) load_group_table<GROUP>(p, num_m, num_n, s_off, s_tstart);
   tc_fence_before();
-  cluster_sync();  // barriers initialised in both CTAs before any remote use
+  cluster_sync();  // barriers initialised in both CTAs before any remote use (and the group table filled)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  const int num_tiles = GROUP == kGroupNone ? num_m * num_n : s_tstart[p.groups];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -586,9 +723,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int row0 = (int)rank * PHALF;
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
-        int tm, tn;
-        tile_coords(tile, num_m, num_n, tm, tn, P_GROUP_M);
-        for (int kb = 0; kb < num_k; ++kb) {
+        const PairJob jb = pair_job<GROUP, B_MN>(tile, p, s_off, s_tstart, num_m, num_n, num_k);
+        for (int kb = 0; kb < jb.nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             set_status(p.status, kStatusGemmTimeout);
             ok = false;
@@ -598,19 +734,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_STAGE + P_B_STAGE));
           uint8_t* a_dst = sA + stage * P_A_STAGE;
           uint8_t* b_dst = sB + stage * P_B_STAGE;
+          const int ka = jb.k0 + kb * BK, kbb = jb.b_k0 + kb * BK;
           if (A_MN) {
 #pragma unroll
             for (int i = 0; i < PHALF / 64; ++i)
-              tma_load_2d_pair(a_dst + i * (64 * BK * 2), &tmap_a, tm * PM + row0 + 64 * i, kb * BK, bar);
+              tma_load_2d_pair(a_dst + i * (64 * BK * 2), &tmap_a, jb.a_m0 + row0 + 64 * i, ka, bar);
           } else {
-            tma_load_2d_pair(a_dst, &tmap_a, kb * BK, tm * PM + row0, bar);
+            tma_load_2d_pair(a_dst, &tmap_a, ka, jb.a_m0 + row0, bar);
           }
           if (B_MN) {
 #pragma unroll
             for (int i = 0; i < PHALF / 64; ++i)
-              tma_load_2d_pair(b_dst + i * (64 * BK * 2), &tmap_b, tn * BN + row0 + 64 * i, kb * BK, bar);
+              tma_load_2d_pair(b_dst + i * (64 * BK * 2), &tmap_b, jb.b_n0 + row0 + 64 * i, kbb, bar);
           } else {
-            tma_load_2d_pair(b_dst, &tmap_b, kb * BK, tn * BN + row0, bar);
+            tma_load_2d_pair(b_dst, &tmap_b, kbb, jb.b_n0 + row0, bar);
           }
           pending[stage] = (int)phase;
           if (++stage == P_STAGES) {
@@ -636,14 +773,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      bool issued = false;  // any MMA at all (a grouped launch may leave a cluster without work)
       for (int tile = cluster; tile < num_tiles && ok; tile += num_clusters) {
+        // only kGroupK has a per-tile K; a group without rows has none, and its
+        // tiles skip the accumulator altogether (the epilogue stores zeros)
+        const int nk = GROUP == kGroupK ? pair_job<GROUP, B_MN>(tile, p, s_off, s_tstart, num_m, num_n, num_k).nk
+                                        : num_k;
+        if (GROUP == kGroupK && nk == 0) continue;
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1)) {
           set_status(p.status, kStatusGemmTimeout);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase)) {
             set_status(p.status, kStatusGemmTimeout);
             ok = false;
@@ -659,6 +802,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_bf16_pair(d_tmem, adesc + a_step * kk, bdesc + b_step * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          issued = true;
           tc_commit_pair_mc(&empty[stage], 0x3);
           if (++stage == P_STAGES) {
             stage = 0;
@@ -672,8 +816,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       // Every MMA issued above has completed (and stopped reading both CTAs'
       // shared memory and writing their TMEM) once this commit arrives.
-      tc_commit_pair(done);
-      if (!mbar_wait(done, 0)) set_status(p.status, kStatusGemmTimeout);
+      if (issued) {
+        tc_commit_pair(done);
+        if (!mbar_wait(done, 0)) set_status(p.status, kStatusGemmTimeout);
+      }
     }
   } else {
     const int quarter = warp & 3;
@@ -682,15 +828,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = cluster; tile < num_tiles; tile += num_clusters) {
-      int tm, tn;
-      tile_coords(tile, num_m, num_n, tm, tn, P_GROUP_M);
+      const PairJob jb = pair_job<GROUP, B_MN>(tile, p, s_off, s_tstart, num_m, num_n, num_k);
+      if (GROUP == kGroupK && jb.nk == 0) {
+        // a group without rows: the product is zero; no accumulator was used
+        EpiParams q = p;
+        q.M = jb.row_lim;
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          epilogue_chunk(q, jb.c_row0 + row_in_tile, jb.tn * BN + c * 32, v);
+        }
+        continue;
+      }
       if (!mbar_wait_warp(&tfull[acc], acc_phase)) {
         set_status(p.status, kStatusGemmTimeout);
         break;
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      store_tile(p, tbase, tm * PM + row_in_tile, tn, xpose);
+      if constexpr (GROUP == kGroupNone) {
+        store_tile(p, tbase, jb.c_row0 + row_in_tile, jb.tn, xpose);
+      } else {
+        EpiParams q = p;
+        q.M = jb.row_lim;
+        store_tile(q, tbase, jb.c_row0 + row_in_tile, jb.tn, xpose);
+      }
       tc_fence_before();
       if (leader)
         mbar_arrive_warp(&tempty[acc]);
@@ -813,12 +976,12 @@ namespace {
 
 // Clusters of two that fit on the device at once (one CTA per SM; SMs left
 // over by an odd GPC stay idle), or 0 when no pair can be placed.
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int GROUP = kGroupNone>
 int pair_clusters() {
   static int n = -1;
   static std::once_flag once;
   std::call_once(once, [] {
-    auto* k = gemm_bf16_tcgen05_pair_kernel<A_MN, B_MN>;
+    auto* k = gemm_bf16_tcgen05_pair_kernel<A_MN, B_MN, GROUP>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
       n = 0;
       return;
@@ -834,9 +997,9 @@ int pair_clusters() {
   return n;
 }
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, int GROUP = kGroupNone>
 int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& p, int clusters, cudaStream_t s) {
-  gemm_bf16_tcgen05_pair_kernel<A_MN, B_MN><<<2 * clusters, THREADS, SMEM_BYTES, s>>>(ta, tb, p);
+  gemm_bf16_tcgen05_pair_kernel<A_MN, B_MN, GROUP><<<2 * clusters, THREADS, SMEM_BYTES, s>>>(ta, tb, p);
   return launch_result();
 }
 
@@ -851,23 +1014,7 @@ int gemm_pair(const GemmArgs& g, const EpiParams& p, cudaStream_t s) {
   return launch_pair<A_MN, B_MN>(ta, tb, p, tiles < avail ? tiles : avail, s);
 }
 
-}  // namespace
-
-int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
-  if (gemm_check(g)) return -1;
-  static bool attr_done = false;
-  if (!attr_done) {
-    bool ok = cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<false, false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES) == cudaSuccess;
-    if (!ok) return -2;
-    attr_done = true;
-  }
+EpiParams epi_params(const GemmArgs& g) {
   EpiParams p;
   p.M = g.M;
   p.N = g.N;
@@ -885,6 +1032,78 @@ int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   p.head_dim = g.head_dim;
   p.seq = g.seq;
   p.status = g.status;
+  p.group_off = nullptr;
+  p.groups = 0;
+  return p;
+}
+
+template <bool A_MN, bool B_MN, int GROUP>
+int grouped_pair(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& p, long max_tiles, cudaStream_t s) {
+  const int avail = pair_clusters<A_MN, B_MN, GROUP>();
+  if (avail <= 0) return -2;
+  return launch_pair<A_MN, B_MN, GROUP>(ta, tb, p, (int)(max_tiles < avail ? max_tiles : avail), s);
+}
+
+}  // namespace
+
+const char* gemm_grouped_check(const GemmArgs& g, const int32_t* offsets, int groups, int mode) {
+  if (const char* e = gemm_check(g)) return e;
+  if (!offsets || (reinterpret_cast<uintptr_t>(offsets) & 3)) return "grouped gemm: offsets missing or misaligned";
+  if (groups < 1 || groups > kMaxGroups) return "grouped gemm: 1 <= groups <= 256";
+  if (mode == kGemmGroupRows) {
+    if (g.a_mn) return "grouped gemm (rows): A must be K-major";
+    if (g.epi == kEpiRope || g.epi == kEpiResidualBf16) return "grouped gemm (rows): no RoPE or residual epilogue";
+    if ((long)groups * (g.b_mn ? g.K : g.N) > 0x7fffffffL) return "grouped gemm (rows): stacked B too tall";
+  } else if (mode == kGemmGroupK) {
+    if (!g.a_mn || !g.b_mn) return "grouped gemm (K): both operands must be MN-major";
+    if (g.epi != kEpiStoreBf16 && g.epi != kEpiF32 && g.epi != kEpiF32Accumulate)
+      return "grouped gemm (K): store or FP32 epilogues only";
+    if ((long)groups * g.M > 0x7fffffffL) return "grouped gemm (K): stacked C too tall";
+  } else {
+    return "grouped gemm: unknown grouping";
+  }
+  return nullptr;
+}
+
+int launch_gemm_grouped(const GemmArgs& g, const int32_t* offsets, int groups, int mode, cudaStream_t stream) {
+  if (gemm_grouped_check(g, offsets, groups, mode)) return -1;
+  EpiParams p = epi_params(g);
+  p.group_off = offsets;
+  p.groups = groups;
+  const long num_n = (g.N + BN - 1) / BN;
+  CUtensorMap ta, tb;
+  if (mode == kGemmGroupRows) {
+    // A [M, K]: every group's rows; B stacked per group along N (K-major) or K (MN-major)
+    if (!make_tmap(&ta, g.A, g.M, g.K, g.lda, PHALF)) return -3;
+    if (g.b_mn ? !make_tmap(&tb, g.B, (long)groups * g.K, g.N, g.ldb, BK)
+               : !make_tmap(&tb, g.B, (long)groups * g.N, g.K, g.ldb, PHALF))
+      return -3;
+    const long max_tiles = ((g.M + PM - 1) / PM + groups) * num_n;  // each group adds at most one partial M tile
+    return g.b_mn ? grouped_pair<false, true, kGroupM>(ta, tb, p, max_tiles, stream)
+                  : grouped_pair<false, false, kGroupM>(ta, tb, p, max_tiles, stream);
+  }
+  // A stored [K, M], B stored [K, N]: K = every group's rows
+  if (!make_tmap(&ta, g.A, g.K, g.M, g.lda, BK) || !make_tmap(&tb, g.B, g.K, g.N, g.ldb, BK)) return -3;
+  const long tiles = (long)groups * ((g.M + PM - 1) / PM) * num_n;
+  return grouped_pair<true, true, kGroupK>(ta, tb, p, tiles, stream);
+}
+
+int launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+  if (gemm_check(g)) return -1;
+  static bool attr_done = false;
+  if (!attr_done) {
+    bool ok = cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<false, false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(gemm_bf16_tcgen05_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) == cudaSuccess;
+    if (!ok) return -2;
+    attr_done = true;
+  }
+  const EpiParams p = epi_params(g);
   // More than one 128-row tile of M: CTA pairs (256 x 256 tiles).
   if (g.M > BM) {
     int rc;

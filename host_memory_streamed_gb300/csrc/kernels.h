@@ -71,6 +71,22 @@ const char* gemm_check(const GemmArgs& g);
 // 0 on success; negative on a launch or descriptor error.
 int launch_gemm(const GemmArgs& g, cudaStream_t stream);
 
+// Grouped GEMM: one launch for a GEMM per group (the experts of an MoE layer)
+// whose row counts live on the device, offsets [groups + 1] (int32, first row
+// of each group, non-decreasing; values are clamped to the operand).
+//   kGemmGroupRows  C[r] = epi(A[r] B_g^T) for r in offsets[g] .. offsets[g+1]:
+//                   A [M, K] K-major holds every group's rows; B is group-
+//                   stacked, [groups * N, K] K-major or [groups * K, N]
+//                   MN-major; C (and R, C2) rows are A's rows.
+//   kGemmGroupK     C[g*M .. g*M + M) = A_g^T B_g with A stored [K, M] and B
+//                   stored [K, N] (both MN-major), A_g and B_g their rows
+//                   offsets[g] .. offsets[g+1]; every group's row count is a
+//                   multiple of 64 (zero rows as padding); an empty group's C
+//                   block is zero.
+enum GemmGroup : int { kGemmGroupRows = 1, kGemmGroupK = 2 };
+const char* gemm_grouped_check(const GemmArgs& g, const int32_t* offsets, int groups, int mode);
+int launch_gemm_grouped(const GemmArgs& g, const int32_t* offsets, int groups, int mode, cudaStream_t stream);
+
 // ----------------------------------------------------------------- attention
 struct AttnArgs {
   const bf16* qkv = nullptr;  // [B*S, ldqkv]: q heads, then k heads, then v heads (head_dim each)
@@ -139,11 +155,16 @@ const char* moe_check(long N, int E, int k, int d);
 // idx[n, j], gates[n, j] from FP32 router logits [N, E]: k largest, ties to the lower id; softmax over them.
 int launch_moe_topk(const float* logits, long N, int E, int k, int32_t* idx, float* gates, cudaStream_t s);
 // Stable counting sort of the pairs by expert: order[i] = pair at position i,
-// pos[p] = position of pair p, offsets[e] = first position of expert e (offsets[E] = P).
+// pos[p] = position of pair p, offsets[e] = first position of expert e.  Each
+// expert's positions are padded to a multiple of row_align (order = -1 at the
+// padding; offsets[E] = the padded total); order holds
+// moe_rows_capacity(P, E, row_align) entries.  row_align = 1: no padding.
 long moe_sort_scratch_ints(long P, int E);
-int launch_moe_sort(const int32_t* idx, long P, int E, int32_t* scratch, int32_t* order, int32_t* pos,
-                    int32_t* offsets, cudaStream_t s);
-// xp[i] = x[order[i] / k] (rows of d BF16 values; x rows ldx apart).
+long moe_rows_capacity(long P, int E, int row_align);
+int launch_moe_sort(const int32_t* idx, long P, int E, int row_align, int32_t* scratch, int32_t* order,
+                    int32_t* pos, int32_t* offsets, cudaStream_t s);
+// xp[i] = x[order[i] / k] for i < P (rows of d BF16 values; x rows ldx apart);
+// a zero row where order[i] < 0.
 int launch_moe_gather(const bf16* x, long ldx, const int32_t* order, int k, long P, int d, bf16* xp,
                       cudaStream_t s);
 // out[n] = res[n] + sum_j gates[n, j] yp[pos[n k + j]] (res may be null).
@@ -155,6 +176,8 @@ int launch_moe_combine_bwd(const bf16* dy, const bf16* yp, const int32_t* pos, c
 // ds [N, E] (BF16): softmax backward over the selected logits, zero elsewhere.
 int launch_moe_gate_bwd(const int32_t* idx, const float* gates, const float* dgates, long N, int E, int k, bf16* ds,
                         cudaStream_t s);
+// buf[i] = 0 (d BF16 values) for the rows i < P_rows with order[i] < 0.
+int launch_moe_zero_pads(const int32_t* order, long P_rows, int d, bf16* buf, cudaStream_t s);
 // dx[n] = dres[n] + sum_j dxp[pos[n k + j]] (dres may be null).
 int launch_moe_scatter_bwd(const bf16* dxp, const int32_t* pos, long N, int k, int d, const bf16* dres, bf16* dx,
                            cudaStream_t s);

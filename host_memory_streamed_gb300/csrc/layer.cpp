@@ -44,6 +44,8 @@ Dims dims_of(const mt_config& c) {
   d.Tc = (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < d.T) ? (long)c.mlp_chunk_rows : d.T;
   d.Dq = c.n_heads * c.head_dim;
   d.Dqkv = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  d.E = c.n_experts > 0 ? c.n_experts : 0;
+  d.k = d.E ? c.top_k : 0;
   return d;
 }
 
@@ -67,8 +69,14 @@ TileLayout make_layout(TileKind kind, const Dims& d, bool tied) {
     add("wqkv", d.Dqkv, d.d);
     add("wo", d.d, d.Dq);
     add("g2", d.d, 0);
-    add("wgu", 2L * d.f, d.d);
-    add("wd", d.d, d.f);
+    if (d.E) {  // MoE: router, then the experts stacked (expert e's rows at e * rows-per-expert)
+      add("wr", d.E, d.d);
+      add("wgu", (int64_t)d.E * 2L * d.f, d.d);
+      add("wd", (int64_t)d.E * d.d, d.f);
+    } else {
+      add("wgu", 2L * d.f, d.d);
+      add("wd", d.d, d.f);
+    }
   } else {
     add("gf", d.d, 0);
     add("wh", d.V, d.d);
@@ -91,7 +99,9 @@ TileLayout make_layout(TileKind kind, const Dims& d, bool tied) {
 
 LayerView bind_layer(const TileLayout& lay, void* base) {
   auto p = [&](const char* n) { return reinterpret_cast<bf16*>(static_cast<uint8_t*>(base) + lay.slot(n).offset); };
-  return LayerView{p("g1"), p("wqkv"), p("wo"), p("g2"), p("wgu"), p("wd")};
+  LayerView v{p("g1"), p("wqkv"), p("wo"), p("g2"), p("wgu"), p("wd")};
+  if (lay.has("wr")) v.wr = p("wr");
+  return v;
 }
 
 HeadView bind_head(const TileLayout& lay, void* base) {
@@ -119,6 +129,18 @@ int LayerTemplate::gemm(const GemmArgs& g) const {
   stats->gemms += 1;
   stats->gemm_flops += 2.0 * g.M * g.N * g.K;
   trace(g.a_mn || g.b_mn ? "gemm (MN-major operand)" : "gemm");
+  return rc;
+}
+
+// One grouped launch (an MoE layer's expert GEMMs); the statistics count the
+// FLOPs of the `rows` routed rows (padding and skipped tiles excluded).
+int LayerTemplate::gemm_grouped(const GemmArgs& g, const int32_t* offsets, int groups, int mode, long rows) const {
+  const int rc = launch_gemm_grouped(g, offsets, groups, mode, s);
+  const double flops = mode == kGemmGroupRows ? 2.0 * rows * g.N * g.K : 2.0 * g.M * g.N * rows;
+  stats->kernels += 1;
+  stats->gemms += 1;
+  stats->gemm_flops += flops;
+  trace("grouped gemm");
   return rc;
 }
 
@@ -176,6 +198,10 @@ int LayerTemplate::forward(const LayerView& w, LayerActs& a, bf16* x_out, bool k
   rc |= gemm(g);
   launch_rmsnorm_fwd(a.h, w.g2, a.n2, a.rstd2, T, D.d, eps, s);
   trace("rmsnorm_fwd");
+  if (D.E) {
+    stats->kernels += 3;
+    return rc | moe_forward(w, a, x_out);
+  }
   if (D.Tc < T) {
     // chunked MLP: the gate/up activations of one row chunk at a time.  An
     // internals-only pass (for backward) stops here: backward recomputes the
@@ -233,7 +259,9 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
     rc |= gemm(g);
   };
 
-  if (D.Tc < T) {
+  if (D.E) {
+    rc |= moe_backward(w, a, dx_out, gv);
+  } else if (D.Tc < T) {
     rc |= mlp_backward_chunked(w, a, dx_out, gv);
   } else {
   // x_out = h + a Wd^T
@@ -282,6 +310,84 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   trace("rmsnorm_bwd");
   launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g1, s);
   stats->kernels += 7;  // 2 x (rmsnorm bwd + colsum), attention delta + dK/dV + dQ
+  return rc;
+}
+
+// ------------------------------------------------------------------ MoE layers
+// The MLP half of an MoE decoder layer: router logits n2 W_r^T (FP32), top-k
+// routing and the stable sort of the (token, slot) pairs by expert (each
+// expert's rows padded to a multiple of 64 with zero rows), the routed rows of
+// n2 gathered, the experts' gate/up (+SwiGLU) and down GEMMs as one grouped
+// launch each (the per-expert row counts stay on the device), and the
+// gate-weighted combine with the residual h.
+int LayerTemplate::moe_forward(const LayerView& w, LayerActs& a, bf16* x_out) const {
+  const Dims& D = dm;
+  const long T = D.T;
+  const int E = D.E, k = D.k, F = D.f, d = D.d;
+  const long P = T * k, R = moe_rows_capacity(P, E, kMoeRowAlign);
+  int rc = 0;
+  rc |= gemm(mk(a.n2, d, w.wr, d, (int)T, E, d, kEpiF32, a.moe_logits, E, ws->status));
+  rc |= launch_moe_topk(a.moe_logits, T, E, k, a.moe_idx, a.moe_gates, s) ? 1 : 0;
+  rc |= launch_moe_sort(a.moe_idx, P, E, kMoeRowAlign, ws->moe_scratch, a.moe_order, a.moe_pos, a.moe_off, s) ? 1 : 0;
+  rc |= launch_moe_gather(a.n2, d, a.moe_order, k, R, d, a.moe_xp, s) ? 1 : 0;
+  stats->kernels += 5;
+  trace("moe routing");
+  GemmArgs g = mk(a.moe_xp, d, w.wgu, d, (int)R, 2 * F, d, kEpiSwiGLU, a.moe_ap, F, ws->status);
+  g.C2 = a.moe_gup;
+  g.ldc2 = 2L * F;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupRows, P);
+  rc |= gemm_grouped(mk(a.moe_ap, F, w.wd, F, (int)R, d, F, kEpiStoreBf16, a.moe_yp, d, ws->status), a.moe_off, E,
+                     kGemmGroupRows, P);
+  if (x_out) {
+    rc |= launch_moe_combine(a.moe_yp, a.moe_pos, a.moe_gates, T, k, d, a.h, x_out, s) ? 1 : 0;
+    stats->kernels += 1;
+  }
+  return rc;
+}
+
+// Backward of moe_forward (its internals recomputed for this visit): dn2 into
+// ws->dn; the experts' and the router's weight gradients into gv.  Every
+// expert GEMM is one grouped launch; experts that received no row get zero
+// gradients from the grouped weight-gradient GEMM itself.
+int LayerTemplate::moe_backward(const LayerView& w, const LayerActs& a, const bf16* dx_out,
+                                const LayerView& gv) const {
+  const Dims& D = dm;
+  const long T = D.T;
+  const int E = D.E, k = D.k, F = D.f, d = D.d;
+  const long P = T * k, R = moe_rows_capacity(P, E, kMoeRowAlign);
+  const Workspace& W = *ws;
+  int rc = 0;
+  rc |= launch_moe_combine_bwd(dx_out, a.moe_yp, a.moe_pos, a.moe_gates, T, k, d, W.moe_dyp, W.moe_dgates, s) ? 1 : 0;
+  rc |= launch_moe_zero_pads(a.moe_order, R, d, W.moe_dyp, s) ? 1 : 0;  // the padding rows enter the K sums
+  stats->kernels += 2;
+  // dW_d[e] = dY_e^T A_e over each expert's rows (both operands MN-major)
+  GemmArgs g = mk(W.moe_dyp, d, a.moe_ap, F, d, F, (int)R, kEpiStoreBf16, gv.wd, F, W.status);
+  g.a_mn = g.b_mn = true;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupK, P);
+  // da = dY W_d[e] and, in the epilogue, the SwiGLU backward against the kept gate/up pairs
+  g = mk(W.moe_dyp, d, w.wd, F, (int)R, F, d, kEpiSwiGLUBwd, W.moe_dgup, 2L * F, W.status);
+  g.b_mn = true;
+  g.R = a.moe_gup;
+  g.ldr = 2L * F;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupRows, P);
+  // dW_gu[e] = dGU_e^T Xp_e
+  g = mk(W.moe_dgup, 2L * F, a.moe_xp, d, 2 * F, d, (int)R, kEpiStoreBf16, gv.wgu, d, W.status);
+  g.a_mn = g.b_mn = true;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupK, P);
+  // dXp = dGU W_gu[e]
+  g = mk(W.moe_dgup, 2L * F, w.wgu, d, (int)R, d, 2 * F, kEpiStoreBf16, W.moe_dxp, d, W.status);
+  g.b_mn = true;
+  rc |= gemm_grouped(g, a.moe_off, E, kGemmGroupRows, P);
+  // router: ds = softmax backward over the selected logits; dW_r = ds^T n2; dn2 += ds W_r
+  rc |= launch_moe_gate_bwd(a.moe_idx, a.moe_gates, W.moe_dgates, T, E, k, W.moe_ds, s) ? 1 : 0;
+  g = mk(W.moe_ds, E, a.n2, d, E, d, (int)T, kEpiStoreBf16, gv.wr, d, W.status);
+  g.a_mn = g.b_mn = true;
+  rc |= gemm(g);
+  g = mk(W.moe_ds, E, w.wr, d, (int)T, d, E, kEpiStoreBf16, W.moe_dn2r, d, W.status);
+  g.b_mn = true;
+  rc |= gemm(g);
+  rc |= launch_moe_scatter_bwd(W.moe_dxp, a.moe_pos, T, k, d, W.moe_dn2r, W.dn, s) ? 1 : 0;
+  stats->kernels += 2;
   return rc;
 }
 

@@ -102,10 +102,12 @@ __global__ void moe_hist_kernel(const int32_t* __restrict__ idx, long P, int E, 
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[(long)blockIdx.x * E + e] = h[e];
 }
 
-// Pass 2 (one block): base[b * E + e] = pairs before (e, b) in expert-major
-// order; offsets[e] = first position of expert e, offsets[E] = P.
-__global__ void moe_scan_kernel(const int32_t* __restrict__ counts, int nblk, int E, int32_t* __restrict__ base,
-                                int32_t* __restrict__ offsets) {
+// Pass 2 (one block): base[b * E + e] = position of the first pair of (e, b)
+// in expert-major order; offsets[e] = first position of expert e.  Each
+// expert's range is padded to a multiple of row_align positions (order = -1
+// there); offsets[E] = the padded total.
+__global__ void moe_scan_kernel(const int32_t* __restrict__ counts, int nblk, int E, int row_align,
+                                int32_t* __restrict__ base, int32_t* __restrict__ offsets) {
   if (threadIdx.x != 0) return;  // nblk * E is small (thousands): one thread keeps the order plain
   int32_t run = 0;
   for (int e = 0; e < E; ++e) {
@@ -114,6 +116,7 @@ __global__ void moe_scan_kernel(const int32_t* __restrict__ counts, int nblk, in
       base[(long)b * E + e] = run;
       run += counts[(long)b * E + e];
     }
+    run = (run + row_align - 1) / row_align * row_align;
   }
   offsets[E] = run;
 }
@@ -147,16 +150,30 @@ __global__ void moe_place_kernel(const int32_t* __restrict__ idx, long P, int E,
   }
 }
 
-// xp[i] = x[order[i] / k]: 16-byte copies, one warp per row.
+// xp[i] = x[order[i] / k], a zero row where order[i] < 0 (padding): 16-byte
+// copies, one warp per row.
 __global__ void moe_gather_kernel(const bf16* __restrict__ x, long ldx, const int32_t* __restrict__ order, int k,
                                   long P, int d, bf16* __restrict__ xp) {
   const long i = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x & 31;
   if (i >= P) return;
-  const long n = order[i] / k;
-  const uint4* src = reinterpret_cast<const uint4*>(x + n * ldx);
+  const int32_t o = order[i];
   uint4* dst = reinterpret_cast<uint4*>(xp + i * (long)d);
+  if (o < 0) {
+    for (int c = lane; c < d / 8; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (long)(o / k) * ldx);
   for (int c = lane; c < d / 8; c += 32) dst[c] = src[c];
+}
+
+// buf[i] = 0 for the padding rows (order[i] < 0), one warp per row.
+__global__ void moe_zero_pads_kernel(const int32_t* __restrict__ order, long P, int d, bf16* __restrict__ buf) {
+  const long i = ((long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  if (i >= P || order[i] >= 0) return;
+  uint4* dst = reinterpret_cast<uint4*>(buf + i * (long)d);
+  for (int c = lane; c < d / 8; c += 32) dst[c] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // out[n] = res[n] + sum_j gates[n, j] * yp[pos[n*k + j]] (FP32, slot order).
@@ -232,6 +249,7 @@ __global__ void moe_scatter_bwd_kernel(const bf16* __restrict__ dxp, const int32
 
 const char* moe_check(long N, int E, int k, int d) {
   if (N <= 0 || d <= 0) return "moe: empty shape";
+  if (N * (long)k + 255L * E > 0x7fffffffL) return "moe: too many (token, slot) pairs for int32 positions";
   if (E < 1 || E > 256) return "moe: 1 <= n_experts <= 256";
   if (k < 1 || k > 8 || k > E) return "moe: 1 <= top_k <= min(8, n_experts)";
   if (d % 8) return "moe: d_model must be a multiple of 8";
@@ -245,14 +263,24 @@ int launch_moe_topk(const float* logits, long N, int E, int k, int32_t* idx, flo
 
 long moe_sort_scratch_ints(long P, int E) { return ((P + kMoeSortBlock - 1) / kMoeSortBlock) * (long)E * 2; }
 
-int launch_moe_sort(const int32_t* idx, long P, int E, int32_t* scratch, int32_t* order, int32_t* pos,
-                    int32_t* offsets, cudaStream_t s) {
+long moe_rows_capacity(long P, int E, int row_align) { return P + (long)(row_align - 1) * E; }
+
+int launch_moe_sort(const int32_t* idx, long P, int E, int row_align, int32_t* scratch, int32_t* order,
+                    int32_t* pos, int32_t* offsets, cudaStream_t s) {
   const int nblk = (int)((P + kMoeSortBlock - 1) / kMoeSortBlock);
   int32_t* counts = scratch;
   int32_t* base = scratch + (long)nblk * E;
+  if (row_align > 1 &&
+      cudaMemsetAsync(order, 0xff, sizeof(int32_t) * moe_rows_capacity(P, E, row_align), s) != cudaSuccess)
+    return launch_result();
   moe_hist_kernel<<<nblk, 256, E * sizeof(int32_t), s>>>(idx, P, E, counts);
-  moe_scan_kernel<<<1, 32, 0, s>>>(counts, nblk, E, base, offsets);
+  moe_scan_kernel<<<1, 32, 0, s>>>(counts, nblk, E, row_align, base, offsets);
   moe_place_kernel<<<nblk, 32, E * sizeof(int32_t), s>>>(idx, P, E, base, order, pos);
+  return launch_result();
+}
+
+int launch_moe_zero_pads(const int32_t* order, long P_rows, int d, bf16* buf, cudaStream_t s) {
+  moe_zero_pads_kernel<<<(unsigned)((P_rows * 32 + 255) / 256), 256, 0, s>>>(order, P_rows, d, buf);
   return launch_result();
 }
 

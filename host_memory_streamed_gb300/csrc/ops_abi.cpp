@@ -87,6 +87,34 @@ int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, in
   return op_cuda(mt::launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
 }
 
+int mt_op_gemm_grouped(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M, int32_t N, int32_t K,
+                       int32_t layout, int32_t grouping, const int32_t* offsets, int32_t groups, int32_t epilogue,
+                       void* C, int64_t ldc, const void* R, int64_t ldr, void* C2, int64_t ldc2, int32_t* status,
+                       void* stream) {
+  mt::GemmArgs g;
+  g.A = static_cast<const mt::bf16*>(A);
+  g.lda = lda;
+  g.B = static_cast<const mt::bf16*>(B);
+  g.ldb = ldb;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.a_mn = (layout & 1) != 0;
+  g.b_mn = (layout & 2) != 0;
+  g.epi = epilogue;
+  g.C = C;
+  g.ldc = ldc;
+  g.R = static_cast<const mt::bf16*>(R);
+  g.ldr = ldr;
+  g.C2 = static_cast<mt::bf16*>(C2);
+  g.ldc2 = ldc2;
+  g.status = status;
+  if (layout & ~3) return op_fail("gemm: layout must be a combination of MT_GEMM_A_MN and MT_GEMM_B_MN");
+  if (const char* e = mt::gemm_grouped_check(g, offsets, groups, grouping)) return op_fail(e);
+  return op_cuda(mt::launch_gemm_grouped(g, offsets, groups, grouping, static_cast<cudaStream_t>(stream)),
+                 "grouped gemm");
+}
+
 }  // extern "C"
 
 extern "C" {
@@ -207,13 +235,26 @@ int mt_op_wait_probe(int32_t* status, int64_t limit_ns, void* stream) {
 
 int64_t mt_op_moe_sort_scratch_ints(int64_t P, int32_t E) { return mt::moe_sort_scratch_ints(P, E); }
 
-int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_t* idx, float* gates, int32_t* order,
-                    int32_t* pos, int32_t* offsets, int32_t* scratch, void* stream) {
+int64_t mt_op_moe_rows_capacity(int64_t P, int32_t E, int32_t row_align) {
+  if (P < 0 || E < 1 || row_align < 1 || row_align > 256) return -1;
+  return mt::moe_rows_capacity(P, E, row_align);
+}
+
+int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_t row_align, int32_t* idx,
+                    float* gates, int32_t* order, int32_t* pos, int32_t* offsets, int32_t* scratch, void* stream) {
   if (const char* e = mt::moe_check(N, E, k, 8)) return op_fail(e);
+  if (row_align < 1 || row_align > 256) return op_fail("moe route: row_align must be in 1 .. 256");
   if (!logits || !idx || !gates || !order || !pos || !offsets || !scratch) return op_fail("moe route: null pointer");
   auto s = static_cast<cudaStream_t>(stream);
   if (mt::launch_moe_topk(logits, N, E, k, idx, gates, s)) return op_cuda(-4, "moe top-k");
-  return op_cuda(mt::launch_moe_sort(idx, N * k, E, scratch, order, pos, offsets, s), "moe sort");
+  return op_cuda(mt::launch_moe_sort(idx, N * k, E, row_align, scratch, order, pos, offsets, s), "moe sort");
+}
+
+int mt_op_moe_zero_pads(const int32_t* order, int64_t P_rows, int32_t d, void* buf, void* stream) {
+  if (P_rows <= 0 || d <= 0 || d % 8 || !order || !buf) return op_fail("moe zero pads: bad shape");
+  return op_cuda(mt::launch_moe_zero_pads(order, P_rows, d, static_cast<mt::bf16*>(buf),
+                                          static_cast<cudaStream_t>(stream)),
+                 "moe zero pads");
 }
 
 int mt_op_moe_gather(const void* x, int64_t ldx, const int32_t* order, int32_t k, int64_t P, int32_t d, void* xp,

@@ -203,6 +203,7 @@ struct Plan {
 
 struct ActsSizes {
   int64_t n1, rstd, qkv, o, lse, h, n2, gu, a, x;
+  int64_t moe_logits, moe_pairs_i32, moe_rows_i32, moe_off, moe_gates, moe_xp, moe_ap, moe_gup, moe_yp;  // MoE only
   int64_t total;
 };
 
@@ -216,9 +217,23 @@ ActsSizes acts_sizes(const Dims& D) {
   s.lse = align_up((int64_t)D.B * D.Hq * D.S * 4, 256);
   s.h = s.x;
   s.n2 = s.x;
-  s.gu = align_up(D.Tc * 2L * D.f * 2, 256);  // one MLP row chunk (the whole step when unchunked)
-  s.a = align_up(D.Tc * (int64_t)D.f * 2, 256);
-  s.total = s.n1 + 2 * s.rstd + s.qkv + s.o + s.lse + s.h + s.n2 + s.gu + s.a;
+  s.gu = D.E ? 0 : align_up(D.Tc * 2L * D.f * 2, 256);  // one MLP row chunk (the whole step when unchunked)
+  s.a = D.E ? 0 : align_up(D.Tc * (int64_t)D.f * 2, 256);
+  const int64_t P = D.T * (int64_t)D.k;  // (token, slot) pairs of an MoE layer
+  const int64_t R = D.E ? moe_rows_capacity(P, D.E, kMoeRowAlign) : 0;  // permuted rows, padding included
+  s.moe_logits = align_up(D.T * (int64_t)D.E * 4, 256);
+  s.moe_pairs_i32 = align_up(P * 4, 256);
+  s.moe_rows_i32 = align_up(R * 4, 256);
+  s.moe_off = align_up((D.E + 1) * 4L, 256);
+  s.moe_gates = s.moe_pairs_i32;
+  s.moe_xp = align_up(R * D.d * 2, 256);
+  s.moe_ap = align_up(R * D.f * 2, 256);
+  s.moe_gup = align_up(R * 2L * D.f * 2, 256);
+  s.moe_yp = s.moe_xp;
+  const int64_t moe = D.E ? s.moe_logits + 2 * s.moe_pairs_i32 + s.moe_rows_i32 + s.moe_off + s.moe_gates +
+                                s.moe_xp + s.moe_ap + s.moe_gup + s.moe_yp
+                          : 0;
+  s.total = s.n1 + 2 * s.rstd + s.qkv + s.o + s.lse + s.h + s.n2 + s.gu + s.a + moe;
   return s;
 }
 
@@ -245,6 +260,28 @@ LayerActs carve_acts(uint8_t* p, const Dims& D, bf16* x) {
   a.gu = reinterpret_cast<bf16*>(p);
   p += s.gu;
   a.a = reinterpret_cast<bf16*>(p);
+  p += s.a;
+  if (D.E) {
+    a.moe_logits = reinterpret_cast<float*>(p);
+    p += s.moe_logits;
+    a.moe_idx = reinterpret_cast<int32_t*>(p);
+    p += s.moe_pairs_i32;
+    a.moe_order = reinterpret_cast<int32_t*>(p);
+    p += s.moe_rows_i32;
+    a.moe_pos = reinterpret_cast<int32_t*>(p);
+    p += s.moe_pairs_i32;
+    a.moe_off = reinterpret_cast<int32_t*>(p);
+    p += s.moe_off;
+    a.moe_gates = reinterpret_cast<float*>(p);
+    p += s.moe_gates;
+    a.moe_xp = reinterpret_cast<bf16*>(p);
+    p += s.moe_xp;
+    a.moe_ap = reinterpret_cast<bf16*>(p);
+    p += s.moe_ap;
+    a.moe_gup = reinterpret_cast<bf16*>(p);
+    p += s.moe_gup;
+    a.moe_yp = reinterpret_cast<bf16*>(p);
+  }
   return a;
 }
 
@@ -265,7 +302,7 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.dx_a = reinterpret_cast<bf16*>(at(td));
   w.dx_b = reinterpret_cast<bf16*>(at(td));
   w.dh = reinterpret_cast<bf16*>(at(td));
-  w.dgu = reinterpret_cast<bf16*>(at(D.Tc * 2L * D.f * 2));
+  w.dgu = reinterpret_cast<bf16*>(at(D.E ? 0 : D.Tc * 2L * D.f * 2));
   w.dn = reinterpret_cast<bf16*>(at(td));
   w.dout = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dq * 2));
   w.dqkv = reinterpret_cast<bf16*>(at(T * (int64_t)D.Dqkv * 2));
@@ -292,6 +329,16 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.rope_sin = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
   w.status = reinterpret_cast<int*>(at(256));
   w.head_chunk = hc;
+  if (D.E) {
+    const int64_t P = T * (int64_t)D.k, R = moe_rows_capacity(P, D.E, kMoeRowAlign);
+    w.moe_dyp = reinterpret_cast<bf16*>(at(R * D.d * 2));
+    w.moe_dgup = reinterpret_cast<bf16*>(at(R * 2L * D.f * 2));
+    w.moe_dxp = reinterpret_cast<bf16*>(at(R * D.d * 2));
+    w.moe_ds = reinterpret_cast<bf16*>(at(T * (int64_t)D.E * 2));
+    w.moe_dn2r = reinterpret_cast<bf16*>(at(td));
+    w.moe_dgates = reinterpret_cast<float*>(at(P * 4));
+    w.moe_scratch = reinterpret_cast<int32_t*>(at(moe_sort_scratch_ints(P, D.E) * 4));
+  }
   return w;
 }
 
@@ -1257,6 +1304,16 @@ const char* validate(const mt_config& c) {
   if (((int64_t)c.batch * c.seq) % 8) return "batch * seq must be a multiple of 8";
   if (c.ckpt_every < 1) return "ckpt_every must be >= 1";
   if (c.mlp_chunk_rows < 0 || c.mlp_chunk_rows % 128) return "mlp_chunk_rows must be a multiple of 128 (0 = unchunked)";
+  if (c.n_experts < 0 || c.n_experts > 256 || c.n_experts % 8)
+    return "n_experts must be 0 (dense) or a multiple of 8 up to 256";
+  if (c.n_experts > 0) {
+    if (c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts) return "top_k must be in 1 .. min(8, n_experts)";
+    if (c.ffn % 8) return "MoE layers need ffn (the expert width) to be a multiple of 8";
+    if ((int64_t)c.batch * c.seq * c.top_k + 63LL * c.n_experts > 0x7fffffffLL)
+      return "MoE layers: batch * seq * top_k (plus padding) must fit int32 row positions";
+    if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq)
+      return "mlp_chunk_rows does not apply to MoE layers";
+  }
   if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq && (c.flags & MT_STORE_ACTS))
     return "a chunked MLP keeps no per-layer gate/up activations: not combinable with MT_STORE_ACTS";
   if (c.grad_slab_bytes > 0 && align_up(c.grad_slab_bytes, kPage) < 2LL * c.d_model)

@@ -48,8 +48,13 @@ struct TileLayout {
   bool has(const char* n) const;
 };
 
+// MoE layers pad each expert's permuted rows to a multiple of this (one K
+// block of the grouped weight-gradient GEMM).
+constexpr int kMoeRowAlign = 64;
+
 struct Dims {
   int L, d, Hq, Hkv, hd, f, V, B, S;
+  int E = 0, k = 0;  // MoE layers: experts and experts per token (E = 0: dense)
   long T;       // B*S
   long Tc;      // rows per MLP chunk (T when the MLP runs on the whole step at once)
   int Dq;       // Hq*hd
@@ -66,6 +71,7 @@ TileLayout make_layout(TileKind kind, const Dims& d, bool tied = false);
 // in a gradient buffer): pointers only, no storage (the "Bind" of a template).
 struct LayerView {
   bf16 *g1, *wqkv, *wo, *g2, *wgu, *wd;
+  bf16* wr = nullptr;  // MoE layers: router [E, d]; wgu/wd then stack the experts
 };
 struct HeadView {
   bf16 *gf, *wh;
@@ -86,6 +92,11 @@ struct LayerActs {
   float* rstd2;
   bf16* gu;      // may be null in plain forward
   bf16* a;
+  // MoE layers: router logits, routing, the permuted rows and the experts' outputs
+  float* moe_logits = nullptr;  // [T, E]
+  int32_t *moe_idx = nullptr, *moe_order = nullptr, *moe_pos = nullptr, *moe_off = nullptr;
+  float* moe_gates = nullptr;   // [T, k]
+  bf16 *moe_xp = nullptr, *moe_ap = nullptr, *moe_gup = nullptr, *moe_yp = nullptr;
 };
 
 struct Workspace {
@@ -114,6 +125,10 @@ struct Workspace {
   float *rope_cos, *rope_sin;  // [S, hd/2]
   int* status;
   long head_chunk;  // rows per LM-head chunk
+  // MoE backward scratch
+  bf16 *moe_dyp = nullptr, *moe_dgup = nullptr, *moe_dxp = nullptr, *moe_ds = nullptr, *moe_dn2r = nullptr;
+  float* moe_dgates = nullptr;
+  int32_t* moe_scratch = nullptr;  // counting-sort scratch
 };
 
 // Counts what the launch sequences issued (for the step statistics).
@@ -146,6 +161,7 @@ struct LayerTemplate {
   }
 
   int gemm(const GemmArgs& g) const;
+  int gemm_grouped(const GemmArgs& g, const int32_t* offsets, int groups, int mode, long rows) const;
   // x -> x_out (x_out == nullptr: stop after the MLP activation).  keep_gu: also
   // store the gate/up pre-activations (needed by backward).
   int forward(const LayerView& w, LayerActs& a, bf16* x_out, bool keep_gu) const;
@@ -153,6 +169,11 @@ struct LayerTemplate {
   // layer's gradients into gv (BF16, tile layout).
   int backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, bf16* dx_in, const LayerView& gv) const;
   int mlp_backward_chunked(const LayerView& w, const LayerActs& a, const bf16* dx_out, const LayerView& gv) const;
+  // MoE layers: the MLP half from n2 (and h for the residual) to x_out, and its
+  // backward from dx_out to dn2 in ws->dn; the per-expert row counts stay on
+  // the device (grouped GEMMs), so neither synchronises with the host.
+  int moe_forward(const LayerView& w, LayerActs& a, bf16* x_out) const;
+  int moe_backward(const LayerView& w, const LayerActs& a, const bf16* dx_out, const LayerView& gv) const;
   // Final norm + LM head + cross-entropy, forward and backward in chunks.
   int head(const HeadView& w, const bf16* x_L, bf16* dx_L, const HeadView& gv) const;
   int embed_fwd(const bf16* E, bf16* x0) const;

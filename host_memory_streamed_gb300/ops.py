@@ -77,6 +77,48 @@ def wait_probe(status, limit_ns):
     _chk(_lib.lib().mt_op_wait_probe(status.data_ptr(), int(limit_ns), _stream()))
 
 
+def gemm_grouped_rows(A, B, offsets, out, b_mn=False, epilogue=_lib.EPI_STORE_BF16, residual=None, out2=None,
+                      status=None):
+    """One launch, per group g: out[r] = epilogue(A[r] @ B[g]^T) for the rows r
+    in offsets[g] .. offsets[g+1] (device int32 [G + 1]).  A [R, K]; B [G, N, K]
+    (or [G, K, N] when b_mn); out has A's rows (SwiGLU: N/2 columns, SwiGLU
+    backward: 2N columns against residual = the gate/up pairs)."""
+    _need(A, BF16, "A")
+    _need(B, BF16, "B")
+    _need(offsets, I32, "offsets")
+    _need(out, F32 if epilogue in (_lib.EPI_F32, _lib.EPI_F32_ACCUMULATE) else BF16, "out")
+    _need(residual, BF16, "residual")
+    _need(out2, BF16, "out2")
+    _need(status, I32, "status")
+    G = B.shape[0]
+    K, N = (B.shape[1], B.shape[2]) if b_mn else (B.shape[2], B.shape[1])
+    if B.stride(0) != B.shape[1] * B.stride(1) or offsets.numel() != G + 1:
+        raise ValueError("gemm_grouped_rows: B must stack its groups contiguously, offsets must have G + 1 entries")
+    _chk(_lib.lib().mt_op_gemm_grouped(A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(1), A.shape[0], N, K,
+                                       _lib.GEMM_B_MN if b_mn else 0, _lib.GEMM_GROUP_ROWS, offsets.data_ptr(), G,
+                                       epilogue, out.data_ptr(), out.stride(0), _ptr(residual),
+                                       residual.stride(0) if residual is not None else 0, _ptr(out2),
+                                       out2.stride(0) if out2 is not None else 0, _ptr(status), _stream()))
+
+
+def gemm_grouped_k(A, B, offsets, out, epilogue=_lib.EPI_STORE_BF16, status=None):
+    """One launch, per group g: out[g] = A[rows]^T @ B[rows] over the rows
+    offsets[g] .. offsets[g+1] (each a multiple of 64 long; an empty group
+    gives zeros).  A [R, M], B [R, N], out [G, M, N]."""
+    _need(A, BF16, "A")
+    _need(B, BF16, "B")
+    _need(offsets, I32, "offsets")
+    _need(out, F32 if epilogue in (_lib.EPI_F32, _lib.EPI_F32_ACCUMULATE) else BF16, "out")
+    _need(status, I32, "status")
+    G, M, N = out.shape
+    if out.stride(0) != M * out.stride(1) or offsets.numel() != G + 1:
+        raise ValueError("gemm_grouped_k: out must stack its groups contiguously, offsets must have G + 1 entries")
+    _chk(_lib.lib().mt_op_gemm_grouped(A.data_ptr(), A.stride(0), B.data_ptr(), B.stride(0), M, N, A.shape[0],
+                                       _lib.GEMM_A_MN | _lib.GEMM_B_MN, _lib.GEMM_GROUP_K, offsets.data_ptr(), G,
+                                       epilogue, out.data_ptr(), out.stride(1), None, 0, None, 0, _ptr(status),
+                                       _stream()))
+
+
 def attention_fwd(qkv, batch, seq, n_heads, n_kv_heads, head_dim, o, lse, status=None):
     _need(qkv, BF16, "qkv")
     _need(o, BF16, "o")
@@ -156,20 +198,33 @@ def embedding_bwd(row_offsets, positions, dx, dE):
 
 
 # ------------------------------------------------------------------ mixture of experts
-def moe_route(logits, k):
-    """FP32 router logits [N, E] -> (idx [N, k], gates [N, k], order [N k], pos [N k], offsets [E + 1])."""
+def moe_route(logits, k, row_align=1):
+    """FP32 router logits [N, E] -> (idx [N, k], gates [N, k], order [R], pos [N k], offsets [E + 1]).
+
+    Each expert's positions are padded to a multiple of row_align (order = -1
+    there); R = N k + (row_align - 1) E."""
     _need(logits, F32, "logits")
     N, E = logits.shape
     dev = logits.device
+    R = int(_lib.lib().mt_op_moe_rows_capacity(N * k, E, row_align))
+    if R < 0:
+        raise ValueError("moe_route: row_align must be in 1 .. 256")
     idx = torch.empty(N, k, device=dev, dtype=I32)
     gates = torch.empty(N, k, device=dev, dtype=F32)
-    order = torch.empty(N * k, device=dev, dtype=I32)
+    order = torch.empty(R, device=dev, dtype=I32)
     pos = torch.empty(N * k, device=dev, dtype=I32)
     offsets = torch.empty(E + 1, device=dev, dtype=I32)
     scratch = torch.empty(int(_lib.lib().mt_op_moe_sort_scratch_ints(N * k, E)), device=dev, dtype=I32)
-    _chk(_lib.lib().mt_op_moe_route(logits.data_ptr(), N, E, k, idx.data_ptr(), gates.data_ptr(), order.data_ptr(),
-                                    pos.data_ptr(), offsets.data_ptr(), scratch.data_ptr(), _stream()))
+    _chk(_lib.lib().mt_op_moe_route(logits.data_ptr(), N, E, k, row_align, idx.data_ptr(), gates.data_ptr(),
+                                    order.data_ptr(), pos.data_ptr(), offsets.data_ptr(), scratch.data_ptr(),
+                                    _stream()))
     return idx, gates, order, pos, offsets
+
+
+def moe_zero_pads(order, buf):
+    """buf[i] = 0 for the padding rows (order[i] = -1)."""
+    _need(buf, BF16, "buf")
+    _chk(_lib.lib().mt_op_moe_zero_pads(order.data_ptr(), order.numel(), buf.shape[1], buf.data_ptr(), _stream()))
 
 
 def moe_gather(x, order, k):
@@ -193,7 +248,7 @@ def moe_combine(yp, pos, gates, residual=None):
 def moe_combine_bwd(dy, yp, pos, gates):
     N, k = gates.shape
     d = dy.shape[1]
-    dyp = torch.empty(N * k, d, device=dy.device, dtype=BF16)
+    dyp = torch.empty(yp.shape[0], d, device=dy.device, dtype=BF16)
     dgates = torch.empty(N, k, device=dy.device, dtype=F32)
     _chk(_lib.lib().mt_op_moe_combine_bwd(dy.data_ptr(), yp.data_ptr(), pos.data_ptr(), gates.data_ptr(), N, k, d,
                                           dyp.data_ptr(), dgates.data_ptr(), _stream()))
@@ -217,53 +272,46 @@ def moe_scatter_bwd(dxp, pos, N, k, dres=None):
 
 
 def moe_mlp_forward(x, wr, wgu, wd, k):
-    """The MoE MLP on the device from the pieces above and the tcgen05 GEMM:
-    x [N, d] BF16, wr [E, d], wgu [E, 2F, d] (gate/up rows interleaved),
-    wd [E, d, F].  Returns (y [N, d] BF16, saved tensors for the backward).
-    The expert loop reads the per-expert row counts on the host."""
+    """The MoE MLP on the device from the pieces above and the grouped tcgen05
+    GEMM, with no host read of the routing: x [N, d] BF16, wr [E, d], wgu
+    [E, 2F, d] (gate/up rows interleaved), wd [E, d, F].  Returns (y [N, d]
+    BF16, saved tensors for the backward).  Each expert's rows are padded to a
+    multiple of 64 with zero rows (the weight-gradient GEMM's K block)."""
     N, d = x.shape
     E, twoF, _ = wgu.shape
     Fh = twoF // 2
     logits = torch.empty(N, E, device=x.device, dtype=F32)
     gemm(x, wr, logits, _lib.EPI_F32)
-    idx, gates, order, pos, offsets = moe_route(logits, k)
+    idx, gates, order, pos, offsets = moe_route(logits, k, row_align=64)
     xp = moe_gather(x, order, k)
-    P = N * k
-    ap = torch.empty(P, Fh, device=x.device, dtype=BF16)
-    gup = torch.empty(P, twoF, device=x.device, dtype=BF16)
-    yp = torch.empty(P, d, device=x.device, dtype=BF16)
-    off = offsets.cpu().tolist()
-    for e in range(E):
-        r0, r1 = off[e], off[e + 1]
-        if r1 == r0:
-            continue
-        gemm(xp[r0:r1], wgu[e], ap[r0:r1], _lib.EPI_SWIGLU, out2=gup[r0:r1])
-        gemm(ap[r0:r1], wd[e], yp[r0:r1])
+    R = order.numel()
+    ap = torch.empty(R, Fh, device=x.device, dtype=BF16)
+    gup = torch.empty(R, twoF, device=x.device, dtype=BF16)
+    yp = torch.empty(R, d, device=x.device, dtype=BF16)
+    gemm_grouped_rows(xp, wgu, offsets, ap, epilogue=_lib.EPI_SWIGLU, out2=gup)
+    gemm_grouped_rows(ap, wd, offsets, yp)
     y = moe_combine(yp, pos, gates)
-    return y, dict(idx=idx, gates=gates, order=order, pos=pos, off=off, xp=xp, ap=ap, gup=gup, yp=yp)
+    return y, dict(idx=idx, gates=gates, order=order, pos=pos, offsets=offsets, xp=xp, ap=ap, gup=gup, yp=yp)
 
 
 def moe_mlp_backward(dy, x, wr, wgu, wd, k, saved):
-    """Gradients of the MoE MLP: (dx, dwr, dwgu [E, 2F, d], dwd [E, d, F])."""
+    """Gradients of the MoE MLP: (dx, dwr, dwgu [E, 2F, d], dwd [E, d, F]).
+    Every expert GEMM is one grouped launch; experts without rows get zero
+    gradients."""
     N, d = x.shape
     E, twoF, _ = wgu.shape
-    Fh = twoF // 2
+    offsets, order = saved["offsets"], saved["order"]
     dyp, dgates = moe_combine_bwd(dy, saved["yp"], saved["pos"], saved["gates"])
-    P = N * k
-    dgup = torch.empty(P, twoF, device=x.device, dtype=BF16)
-    dxp = torch.empty(P, d, device=x.device, dtype=BF16)
-    dwgu = torch.zeros_like(wgu)
-    dwd = torch.zeros_like(wd)
-    off = saved["off"]
-    for e in range(E):
-        r0, r1 = off[e], off[e + 1]
-        if r1 == r0:
-            continue
-        gemm_layout(dyp[r0:r1], saved["ap"][r0:r1], dwd[e], a_mn=True, b_mn=True)
-        gemm_layout(dyp[r0:r1], wd[e], dgup[r0:r1], b_mn=True, epilogue=_lib.EPI_SWIGLU_BWD,
-                    residual=saved["gup"][r0:r1])
-        gemm_layout(dgup[r0:r1], saved["xp"][r0:r1], dwgu[e], a_mn=True, b_mn=True)
-        gemm_layout(dgup[r0:r1], wgu[e], dxp[r0:r1], b_mn=True)
+    moe_zero_pads(order, dyp)
+    R = order.numel()
+    dgup = torch.empty(R, twoF, device=x.device, dtype=BF16)
+    dxp = torch.empty(R, d, device=x.device, dtype=BF16)
+    dwgu = torch.empty_like(wgu)
+    dwd = torch.empty_like(wd)
+    gemm_grouped_k(dyp, saved["ap"], offsets, dwd)
+    gemm_grouped_rows(dyp, wd, offsets, dgup, b_mn=True, epilogue=_lib.EPI_SWIGLU_BWD, residual=saved["gup"])
+    gemm_grouped_k(dgup, saved["xp"], offsets, dwgu)
+    gemm_grouped_rows(dgup, wgu, offsets, dxp, b_mn=True)
     ds = moe_gate_bwd(saved["idx"], saved["gates"], dgates, E)
     dwr = torch.empty_like(wr)
     gemm_layout(ds, x, dwr, a_mn=True, b_mn=True)
@@ -271,4 +319,3 @@ def moe_mlp_backward(dy, x, wr, wgu, wd, k, saved):
     gemm_layout(ds, wr, dx_router, b_mn=True)
     dx = moe_scatter_bwd(dxp, saved["pos"], N, k, dres=dx_router)
     return dx, dwr, dwgu, dwd
-

@@ -116,6 +116,15 @@ typedef struct {
                                 activations exist one chunk at a time (long sequences); the W_gu and W_d
                                 gradients then accumulate in FP32 across chunks.  0 = the whole step at
                                 once.  Not combinable with MT_STORE_ACTS. */
+  int32_t n_experts;         /* 0: dense decoder layers.  > 0: every layer's MLP is a top-k mixture of
+                                n_experts SwiGLU experts of width ffn (a multiple of 8, at most 256):
+                                router logits x W_r^T, per token the top_k largest (ties to the lower
+                                expert id), gates = softmax over them, output = the gate-weighted sum of
+                                the chosen experts.  A layer tile then holds g1, wqkv, wo, g2, wr
+                                [n_experts, d], wgu [n_experts * 2 ffn, d] (each expert's gate/up rows
+                                interleaved) and wd [n_experts * d, ffn].  Not combinable with
+                                mlp_chunk_rows. */
+  int32_t top_k;             /* experts per token (1 .. min(8, n_experts)); ignored when n_experts = 0 */
 } mt_config;
 
 typedef struct mt_model mt_model;

@@ -69,6 +69,40 @@ int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, in
                       int32_t layout, int32_t epilogue, void* C, int64_t ldc, const void* R, int64_t ldr,
                       int32_t* status, void* stream);
 
+/* Groupings of mt_op_gemm_grouped. */
+enum { MT_GEMM_GROUP_ROWS = 1, MT_GEMM_GROUP_K = 2 };
+
+/*
+ * One launch for a GEMM per group (the experts of a mixture-of-experts layer)
+ * whose sizes are only known on the device: offsets (device int32
+ * [groups + 1], non-decreasing, groups 1..256) give each group's first row of
+ * a shared buffer.  No host synchronisation.  Values outside the operand are
+ * clamped to it, so no offsets can make the kernel read or write out of
+ * bounds.
+ *
+ * MT_GEMM_GROUP_ROWS (layout 0 or MT_GEMM_B_MN): for every group g and row r
+ *   in offsets[g] .. offsets[g+1]:  C[r] = epilogue(A[r] B_g^T).
+ *   A [M, K] K-major (M = the buffer's rows, all groups); B_g is group g's
+ *   block of a stacked B: rows g*N .. g*N + N of a K-major [groups*N, K] B, or
+ *   (MT_GEMM_B_MN) rows g*K .. g*K + K of a [groups*K, N] B.  C, R, C2 have
+ *   A's rows.  Epilogues MT_EPI_STORE_BF16, MT_EPI_F32, MT_EPI_F32_ACCUMULATE,
+ *   MT_EPI_SWIGLU (C2 optional), MT_EPI_SWIGLU_BWD.
+ * MT_GEMM_GROUP_K (layout MT_GEMM_A_MN | MT_GEMM_B_MN): for every group g,
+ *   C[g*M .. g*M + M) = A_g^T B_g, where A is stored [K, M], B stored [K, N]
+ *   (K = the buffer's rows, all groups) and A_g, B_g are their rows
+ *   offsets[g] .. offsets[g+1].  Each group's row count must be a multiple
+ *   of 64 (pad with zero rows: mt_op_moe_route with row_align 64); a group
+ *   without rows gets a zero block.  Epilogues MT_EPI_STORE_BF16, MT_EPI_F32,
+ *   MT_EPI_F32_ACCUMULATE.  This is the weight gradient of every expert in
+ *   one launch.
+ * Alignment rules as mt_op_gemm.  Errors: MT_EINVAL for unsupported
+ * arguments (nothing launched), MT_ECUDA for a failed launch.
+ */
+int mt_op_gemm_grouped(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M, int32_t N, int32_t K,
+                       int32_t layout, int32_t grouping, const int32_t* offsets, int32_t groups, int32_t epilogue,
+                       void* C, int64_t ldc, const void* R, int64_t ldr, void* C2, int64_t ldc2, int32_t* status,
+                       void* stream);
+
 /*
  * Causal grouped-query attention forward (flash style, one pass over keys).
  * qkv: [batch*seq, ldqkv] BF16 rows (token t = b*seq + s) holding n_heads query
@@ -166,20 +200,27 @@ enum { MT_STATUS_WAIT_PROBE = 7 };
 int mt_op_wait_probe(int32_t* status, int64_t limit_ns, void* stream);
 
 /*
- * Mixture-of-experts MLP pieces (the expert GEMMs run on mt_op_gemm /
- * mt_op_gemm_layout over each expert's rows).  MegaTrain's largest run
- * trains an MoE model (author's blog, the single-H200 gpt-oss 120B run;
- * podcast transcript, the 120B GPT-OSS run); the pages give no formula for
- * the MoE layer, so this is the plainest top-k reading.  N tokens, E experts (1..256),
+ * Mixture-of-experts MLP pieces (the expert GEMMs run on mt_op_gemm_grouped,
+ * or mt_op_gemm / mt_op_gemm_layout over each expert's rows).  MegaTrain's
+ * largest run trains an MoE model (author's blog, the single-H200 gpt-oss
+ * 120B run; podcast transcript, the 120B GPT-OSS run); the pages give no
+ * formula for the MoE layer, so this is the plainest top-k reading.  N
+ * tokens, E experts (1..256),
  * top k (1..min(8, E)), pairs p = n*k + j (P = N*k), d a multiple of 8.
  * Routing: per token the k largest router logits (ties to the lower expert
  * id), gates = softmax over them; the pairs are then sorted by expert, stably.
  *
  * mt_op_moe_route: logits FP32 [N, E] -> idx int32 [N, k], gates FP32 [N, k],
- *   order int32 [P] (pair at each position), pos int32 [P] (position of each
- *   pair), offsets int32 [E + 1] (first position of each expert, offsets[E] =
- *   P); scratch: mt_op_moe_sort_scratch_ints(P, E) int32 values.
- * mt_op_moe_gather: xp[i] = x[order[i] / k] (BF16 rows, x rows ldx apart).
+ *   order int32 [R] (pair at each position, -1 at padding), pos int32 [P]
+ *   (position of each pair), offsets int32 [E + 1] (first position of each
+ *   expert; offsets[E] = the positions used); scratch:
+ *   mt_op_moe_sort_scratch_ints(P, E) int32 values.  Each expert's positions
+ *   are padded to a multiple of row_align (1..256; 1 = no padding, R = P; 64
+ *   for the grouped weight-gradient GEMM); R = mt_op_moe_rows_capacity(P, E,
+ *   row_align) = P + (row_align - 1) E.
+ * mt_op_moe_gather: xp[i] = x[order[i] / k] for i < P rows (BF16 rows, x rows
+ *   ldx apart), a zero row where order[i] = -1.
+ * mt_op_moe_zero_pads: buf[i] = 0 for the rows i < P_rows with order[i] = -1.
  * mt_op_moe_combine: out[n] = res[n] + sum_j gates[n, j] yp[pos[n k + j]]
  *   (BF16 rows, FP32 sums in slot order; res may be NULL).
  * mt_op_moe_combine_bwd: dyp[pos[p]] = gates[p] dy[n] (BF16),
@@ -189,8 +230,10 @@ int mt_op_wait_probe(int32_t* status, int64_t limit_ns, void* stream);
  * mt_op_moe_scatter_bwd: dx[n] = dres[n] + sum_j dxp[pos[n k + j]] (dres may be NULL).
  */
 int64_t mt_op_moe_sort_scratch_ints(int64_t P, int32_t E);
-int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_t* idx, float* gates, int32_t* order,
-                    int32_t* pos, int32_t* offsets, int32_t* scratch, void* stream);
+int64_t mt_op_moe_rows_capacity(int64_t P, int32_t E, int32_t row_align);
+int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_t row_align, int32_t* idx,
+                    float* gates, int32_t* order, int32_t* pos, int32_t* offsets, int32_t* scratch, void* stream);
+int mt_op_moe_zero_pads(const int32_t* order, int64_t P_rows, int32_t d, void* buf, void* stream);
 int mt_op_moe_gather(const void* x, int64_t ldx, const int32_t* order, int32_t k, int64_t P, int32_t d, void* xp,
                      void* stream);
 int mt_op_moe_combine(const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k, int32_t d,

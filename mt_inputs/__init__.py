@@ -61,6 +61,8 @@ class ModelShape:
     beta2: float = 0.95
     adam_eps: float = 1e-8
     weight_decay: float = 0.0
+    n_experts: int = 0  # > 0: every layer's MLP is a top_k mixture of n_experts SwiGLU experts of width ffn
+    top_k: int = 0
 
     def with_(self, **kw) -> "ModelShape":
         return replace(self, **kw)
@@ -129,6 +131,19 @@ def layer_weights(s: ModelShape, layer: int, gain_jitter: float = 0.0) -> dict:
     return out
 
 
+def moe_layer_weights(s: ModelShape, layer: int, gain_jitter: float = 0.0) -> dict:
+    """Weights of MoE decoder layer ``layer``: the attention half as in
+    ``layer_weights``, the router ``wr`` [E, d] and ``experts``, a list of
+    {'wg', 'wu' [ffn, d], 'wd' [d, ffn]}."""
+    gen = torch.Generator().manual_seed(5000 + layer + 1)
+    dense = layer_weights(s, layer, gain_jitter)
+    out = {k: dense[k] for k in ("g1", "wq", "wk", "wv", "wo", "g2")}
+    out["wr"] = _matrix(gen, (s.n_experts, s.d_model), std=0.2)
+    out["experts"] = [{"wg": _matrix(gen, (s.ffn, s.d_model)), "wu": _matrix(gen, (s.ffn, s.d_model)),
+                       "wd": _matrix(gen, (s.d_model, s.ffn))} for _ in range(s.n_experts)]
+    return out
+
+
 def head_weights(s: ModelShape, gain_jitter: float = 0.0) -> dict:
     gen = torch.Generator().manual_seed(1000 + s.n_layers + 1)
     return {"gf": _gain(gen, s.d_model, gain_jitter), "wh": _matrix(gen, (s.vocab, s.d_model))}
@@ -138,7 +153,8 @@ def model_weights(s: ModelShape, gain_jitter: float = 0.0) -> dict:
     """All BF16 weights: {'embed': {...}, 'layers': [{...}, ...], 'head': {...}}."""
     return {
         "embed": embed_weights(s),
-        "layers": [layer_weights(s, i, gain_jitter) for i in range(s.n_layers)],
+        "layers": [(moe_layer_weights if s.n_experts else layer_weights)(s, i, gain_jitter)
+                   for i in range(s.n_layers)],
         "head": head_weights(s, gain_jitter),
     }
 

@@ -34,10 +34,12 @@ from __future__ import annotations
 
 import torch
 
-from .decoder import (OracleConfig, causal_gqa_attention, causal_gqa_attention_backward, rms_norm,
-                      rms_norm_backward, rope, rope_backward, swiglu, swiglu_backward)
+from .decoder import (OracleConfig, causal_gqa_attention, causal_gqa_attention_backward, head_loss_and_backward,
+                      head_weight, rms_norm, rms_norm_backward, rope, rope_backward, rope_cos_sin, swiglu,
+                      swiglu_backward)
 
-__all__ = ["moe_route", "moe_mlp_forward", "moe_mlp_backward", "moe_layer_forward", "moe_layer_backward"]
+__all__ = ["moe_route", "moe_mlp_forward", "moe_mlp_backward", "moe_layer_forward", "moe_layer_backward",
+           "moe_model_loss_and_grads"]
 
 
 def moe_route(x, wr, k):
@@ -154,4 +156,35 @@ def moe_layer_backward(dx_out, c, lw, cfg: OracleConfig, cos, sin, k):
     dn1 = dq @ lw["wq"] + dk @ lw["wk"] + dv @ lw["wv"]
     dx_n, g["g1"] = rms_norm_backward(dn1, c["x"], lw["g1"], c["rstd1"])
     return dh + dx_n, g
+
+
+def moe_model_loss_and_grads(params, tokens, cfg: OracleConfig, k, dtype=torch.float64):
+    """``model_loss_and_grads`` of a decoder whose layers are all MoE layers
+    (``params["layers"][i]`` as ``moe_layer_forward`` takes them); the
+    embedding, the final norm, the LM head (tied or not) and the loss as in
+    the dense model."""
+    f = lambda t: t.to(dtype)
+    p = {"embed": {n: f(t) for n, t in params["embed"].items()},
+         "layers": [{n: ([{m: f(u) for m, u in e.items()} for e in t] if n == "experts" else f(t))
+                     for n, t in lw.items()} for lw in params["layers"]],
+         "head": {n: f(t) for n, t in params["head"].items()}}
+    tokens = tokens.long()
+    inp, tgt = tokens[:, :-1], tokens[:, 1:]
+    S = inp.shape[1]
+    cos, sin = rope_cos_sin(S, cfg.head_dim, cfg.rope_theta, dtype)
+    x = p["embed"]["E"][inp]
+    caches = []
+    for lw in p["layers"]:
+        x, c = moe_layer_forward(x, lw, cfg, cos, sin, k)
+        caches.append(c)
+    tied = "wh" not in p["head"]
+    loss, dx, head_g = head_loss_and_backward(x, {"gf": p["head"]["gf"], "wh": head_weight(p)}, tgt, cfg)
+    layer_g = [None] * len(p["layers"])
+    for i in reversed(range(len(p["layers"]))):
+        dx, layer_g[i] = moe_layer_backward(dx, caches[i], p["layers"][i], cfg, cos, sin, k)
+    dE = torch.zeros_like(p["embed"]["E"])
+    dE.index_add_(0, inp.reshape(-1), dx.reshape(-1, cfg.d_model))
+    if tied:
+        dE += head_g.pop("wh")
+    return float(loss), {"embed": {"E": dE}, "layers": layer_g, "head": head_g}
 

@@ -30,6 +30,13 @@ D = torch.float64
 def flat_named(tree):
     out = [("embed.E", tree["embed"]["E"])]
     for i, lw in enumerate(tree["layers"]):
+        if "experts" in lw:  # MoE layer
+            for k in ("g1", "wq", "wk", "wv", "wo", "g2", "wr"):
+                out.append((f"layers.{i}.{k}", lw[k]))
+            for e, ew in enumerate(lw["experts"]):
+                for k in ("wg", "wu", "wd"):
+                    out.append((f"layers.{i}.experts.{e}.{k}", ew[k]))
+            continue
         for k in mt_inputs.LAYER_TENSORS:
             out.append((f"layers.{i}.{k}", lw[k]))
     out.append(("head.gf", tree["head"]["gf"]))

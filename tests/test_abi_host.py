@@ -54,7 +54,9 @@ def test_required_device_bytes_positive_and_bounded(lib, name):
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(n_kv_heads=3), dict(ffn=690), dict(ckpt_every=0),
                                  dict(vocab=0), dict(batch=0), dict(seq=3, batch=1), dict(mlp_chunk_rows=100),
-                                 dict(mlp_chunk_rows=128, flags=2)])
+                                 dict(mlp_chunk_rows=128, flags=2), dict(n_experts=12, top_k=2),
+                                 dict(n_experts=8, top_k=0), dict(n_experts=8, top_k=9), dict(n_experts=512, top_k=2),
+                                 dict(n_experts=8, top_k=2, mlp_chunk_rows=128)])
 def test_bad_config_rejected(lib, bad):
     s = mt_inputs.PRESETS["tiny"]
     assert lib.mt_required_device_bytes(C.byref(_cfg(s, **bad))) == -1
@@ -166,3 +168,53 @@ def test_fault_injection_and_wait_probe_argument_checks(lib):
     assert lib.mt_op_wait_probe(None, 50_000_000, None) == _lib.MT_EINVAL
     for limit in (0, 999_999, 5_000_000_001):
         assert lib.mt_op_wait_probe(0x10000, limit, None) == _lib.MT_EINVAL
+
+
+def test_moe_arena_grows_with_the_routed_pairs(lib):
+    """MoE layers: the device arena holds the routing, the permuted rows and the
+    experts' outputs of one layer pass, sized by tokens x top_k, and the same
+    per-layer weight buffers as the largest tile."""
+    s = mt_inputs.PRESETS["tiny"]
+    dense = lib.mt_required_device_bytes(C.byref(_cfg(s)))
+    k2 = lib.mt_required_device_bytes(C.byref(_cfg(s, n_experts=8, top_k=2)))
+    k4 = lib.mt_required_device_bytes(C.byref(_cfg(s, n_experts=8, top_k=4)))
+    assert 0 < dense < k2 < k4
+    T, d, F = s.batch * s.seq, s.d_model, s.ffn
+    # two more pairs per token add at least their rows of xp, yp, dyp, dxp (d each), ap (F), gup and dgup (2F)
+    assert k4 - k2 >= 2 * T * (4 * d + F + 4 * F) * 2
+
+
+def test_grouped_gemm_rejects_bad_arguments_before_any_launch(lib):
+    """mt_op_gemm_grouped validates on the host and returns MT_EINVAL without
+    touching the device (the pointers below are never dereferenced)."""
+    from host_memory_streamed_gb300 import _lib
+    A, B, Cp, off = 0x10000, 0x20000, 0x30000, 0x40000
+
+    def call(layout=0, grouping=_lib.GEMM_GROUP_ROWS, offsets=off, groups=8, epi=_lib.EPI_STORE_BF16, M=1024,
+             N=256, K=128, lda=128, ldb=128, ldc=256):
+        return lib.mt_op_gemm_grouped(A, lda, B, ldb, M, N, K, layout, grouping, offsets, groups, epi, Cp, ldc,
+                                      None, 0, None, 0, None, None)
+
+    bad = [
+        dict(groups=0), dict(groups=257), dict(offsets=None), dict(offsets=off + 2),
+        dict(grouping=3), dict(layout=_lib.GEMM_A_MN),                            # rows grouping wants K-major A
+        dict(epi=_lib.EPI_ROPE), dict(epi=_lib.EPI_RESIDUAL_BF16),
+        dict(grouping=_lib.GEMM_GROUP_K, layout=_lib.GEMM_B_MN),                  # K grouping wants both MN-major
+        dict(grouping=_lib.GEMM_GROUP_K, layout=3, epi=_lib.EPI_SWIGLU, lda=1024, ldb=256),
+        dict(K=100),                                                              # K-major K not a multiple of 8
+        dict(layout=4),
+    ]
+    for kw in bad:
+        assert call(**kw) == _lib.MT_EINVAL, kw
+        assert lib.mt_op_last_error()
+
+
+def test_moe_padding_capacity_and_route_checks(lib):
+    from host_memory_streamed_gb300 import _lib
+    assert lib.mt_op_moe_rows_capacity(1000, 8, 1) == 1000
+    assert lib.mt_op_moe_rows_capacity(1000, 8, 64) == 1000 + 63 * 8
+    assert lib.mt_op_moe_rows_capacity(1000, 8, 0) == -1 and lib.mt_op_moe_rows_capacity(1000, 8, 257) == -1
+    p = 0x10000
+    for row_align in (0, 300):
+        assert lib.mt_op_moe_route(p, 100, 8, 2, row_align, p, p, p, p, p, p, None) == _lib.MT_EINVAL
+    assert lib.mt_op_moe_zero_pads(p, 0, 64, p, None) == _lib.MT_EINVAL

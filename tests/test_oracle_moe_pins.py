@@ -184,3 +184,28 @@ def test_moe_layer_finite_differences():
         an = float((dx * ux).sum()) + sum(float((g[n] * uw[n]).sum()) for n in names) + \
             sum(float((g["experts"][i][n] * ue[i][n]).sum()) for i in range(E) for n in ("wg", "wu", "wd"))
         assert abs(fd - an) <= 1e-6 * abs(an) + 1e-9, (fd, an)
+
+
+def test_moe_model_with_one_expert_is_the_dense_model():
+    """A whole model of single-expert MoE layers (the dense MLP as the expert)
+    has the dense model's loss and gradients."""
+    import mt_inputs
+    from oracle import OracleConfig
+    s = mt_inputs.PRESETS["tiny"].with_(n_layers=2, d_model=64, n_heads=4, n_kv_heads=2, head_dim=16, ffn=48,
+                                        vocab=50, batch=2, seq=10)
+    cfg = OracleConfig.from_shape(s)
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    tokens = mt_inputs.step_tokens(s, 1)
+    loss, grads = oracle.model_loss_and_grads(params, tokens, cfg)
+    mp = dict(params, layers=[{**{n: lw[n] for n in ("g1", "wq", "wk", "wv", "wo", "g2")},
+                               "wr": torch.zeros(1, s.d_model, dtype=torch.bfloat16),
+                               "experts": [{"wg": lw["wg"], "wu": lw["wu"], "wd": lw["wd"]}]}
+                              for lw in params["layers"]])
+    loss_m, grads_m = moe.moe_model_loss_and_grads(mp, tokens, cfg, 1)
+    assert abs(loss_m - loss) <= 1e-12 * abs(loss)
+    assert torch.allclose(grads_m["embed"]["E"], grads["embed"]["E"], rtol=1e-10, atol=1e-14)
+    for gl_m, gl in zip(grads_m["layers"], grads["layers"]):
+        for n in ("g1", "wq", "wk", "wv", "wo", "g2"):
+            assert torch.allclose(gl_m[n], gl[n], rtol=1e-10, atol=1e-14), n
+        for n in ("wg", "wu", "wd"):
+            assert torch.allclose(gl_m["experts"][0][n], gl[n], rtol=1e-10, atol=1e-14), n
