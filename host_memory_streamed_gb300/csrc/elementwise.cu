@@ -6,7 +6,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cfloat>
+#include <mutex>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -141,13 +143,170 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_bwd_kernel(const bf16* __
   for (int c = threadIdx.x; c < d; c += RMS_THREADS) dg_partial[(long)blockIdx.x * d + c] = dg_acc[c];
 }
 
-// out[c] = sum_p partial[p, c], p ascending; one thread per column.
-__global__ void colsum_bf16_kernel(const float* __restrict__ partial, long nparts, int d, bf16* __restrict__ out) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= d) return;
-  float s = 0.f;
-  for (long p = 0; p < nparts; ++p) s += partial[p * d + c];
-  out[c] = __float2bfloat16_rn(s);
+// Backward with the columns held in registers: each thread owns VPT 16-byte
+// vectors (8 columns each) of every row, vector i = threadIdx.x + k*blockDim.x
+// for k < VPT, so the gain and the block's gain-gradient sums for those
+// columns stay in registers for all of the block's rows.  The block's
+// kRmsRowsPerBlock rows go two at a time; with PREFETCH (one vector per
+// thread, where the registers allow it) the next pair's dy, x and dres
+// vectors are requested before the current pair is reduced, so loads stay in
+// flight while the block waits on its reduction barrier.  The
+// two rows' dot products are reduced together (warp butterfly, then the
+// warps' sums in warp order from a double-buffered shared slot: one barrier
+// per pair of rows).  No shared-memory accumulator and no barrier per row,
+// unlike rmsnorm_bwd_kernel, which remains for rows wider than
+// kRmsBwdRegMaxVectors vectors.
+constexpr int kRmsBwdRegMaxVectors = 1024;  // d <= 8192
+
+template <int VPT>
+struct RmsPair {
+  uint4 dy[2][VPT], x[2][VPT], r[2][VPT];
+  float rs[2];
+};
+
+template <int VPT>
+__device__ __forceinline__ void rms_load_pair(RmsPair<VPT>& p, const bf16* __restrict__ dy,
+                                              const bf16* __restrict__ x, const float* __restrict__ rstd,
+                                              const bf16* __restrict__ dres, long row, int nr, int nv) {
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const long off = (row + j) * (long)nv;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      const bool ok = i < nv && j < nr;
+      p.dy[j][k] = ok ? reinterpret_cast<const uint4*>(dy)[off + i] : zero;
+      p.x[j][k] = ok ? reinterpret_cast<const uint4*>(x)[off + i] : zero;
+      p.r[j][k] = (ok && dres) ? reinterpret_cast<const uint4*>(dres)[off + i] : zero;
+    }
+  }
+  p.rs[0] = nr > 0 ? rstd[row] : 0.f;
+  p.rs[1] = nr > 1 ? rstd[row + 1] : 0.f;
+}
+
+template <int VPT, bool PREFETCH>
+__global__ void __launch_bounds__(VPT == 1 ? 640 : (VPT == 2 ? 384 : 256)) rmsnorm_bwd_rows_kernel(
+    const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ g,
+    const float* __restrict__ rstd, const bf16* __restrict__ dres, bf16* __restrict__ dx,
+    float* __restrict__ dg_partial, long rows, int d) {
+  __shared__ float red[2][2][32];  // [buffer][row of the pair][warp]
+  const int nv = d / 8;
+  const int nthreads = blockDim.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32, nwarps = nthreads / 32;
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  float wf[VPT][8], acc[VPT][8];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int i = threadIdx.x + k * nthreads;
+    if (i < nv) {
+      unpack8(gr[i], wf[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wf[k][e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
+  }
+  const long r0 = (long)blockIdx.x * kRmsRowsPerBlock;
+  const long r1 = min(rows, r0 + kRmsRowsPerBlock);
+  auto pair_rows = [&](long row) { return row >= r1 ? 0 : (row + 1 < r1 ? 2 : 1); };
+  RmsPair<VPT> cur, nxt;
+  if (PREFETCH) rms_load_pair<VPT>(cur, dy, x, rstd, dres, r0, pair_rows(r0), nv);
+  int buf = 0;
+  for (long row = r0; row < r1; row += 2) {
+    const int nr = pair_rows(row);
+    if (PREFETCH)
+      rms_load_pair<VPT>(nxt, dy, x, rstd, dres, row + 2, pair_rows(row + 2), nv);
+    else
+      rms_load_pair<VPT>(cur, dy, x, rstd, dres, row, nr, nv);
+    float dot[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        float xf[8], df[8];
+        unpack8(cur.x[j][k], xf);
+        unpack8(cur.dy[j][k], df);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = xf[e] * cur.rs[j];
+          dot[j] += df[e] * wf[k][e] * xh;
+          acc[k][e] += df[e] * xh;  // zero for a missing second row (dy = 0)
+        }
+      }
+    }
+    dot[0] = warp_sum(dot[0]);
+    dot[1] = warp_sum(dot[1]);
+    if (lane == 0) {
+      red[buf][0][warp] = dot[0];
+      red[buf][1][warp] = dot[1];
+    }
+    __syncthreads();
+    float t0 = 0.f, t1 = 0.f;
+    for (int w = 0; w < nwarps; ++w) {
+      t0 += red[buf][0][w];
+      t1 += red[buf][1][w];
+    }
+    // the next pair writes the other buffer; this one is rewritten only after
+    // the next pair's barrier, which every thread reaches after reading it
+    buf ^= 1;
+    const float mean[2] = {t0 / (float)d, t1 / (float)d};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (j >= nr) break;
+      const long off = (row + j) * (long)nv;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int i = threadIdx.x + k * nthreads;
+        if (i >= nv) continue;
+        float xf[8], df[8], rf[8], out[8];
+        unpack8(cur.x[j][k], xf);
+        unpack8(cur.dy[j][k], df);
+        unpack8(cur.r[j][k], rf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[e] = rf[e] + cur.rs[j] * (df[e] * wf[k][e] - xf[e] * cur.rs[j] * mean[j]);
+        reinterpret_cast<uint4*>(dx)[off + i] = pack8(out);
+      }
+    }
+    if (PREFETCH) cur = nxt;
+  }
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int i = threadIdx.x + k * nthreads;
+    if (i < nv) {
+      float4* dst = reinterpret_cast<float4*>(dg_partial + (long)blockIdx.x * d + (long)i * 8);
+      dst[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+      dst[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+    }
+  }
+}
+
+// out[c] = sum_p partial[p, c] in a fixed order: the parts split into
+// kColsumSlices consecutive slices, each summed in ascending order by one warp
+// over 32 adjacent columns (128-byte loads), then the slice sums in slice
+// order.  One block per 32 columns.
+constexpr int kColsumSlices = 8;
+__global__ void __launch_bounds__(32 * kColsumSlices) colsum_bf16_kernel(const float* __restrict__ partial,
+                                                                       long nparts, int d, bf16* __restrict__ out) {
+  __shared__ float acc[kColsumSlices][32];
+  const int lane = threadIdx.x & 31, sl = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
+  const long per = (nparts + kColsumSlices - 1) / kColsumSlices;
+  const long p0 = sl * per, p1 = min(nparts, p0 + per);
+  float v = 0.f;
+  if (c < d) {
+#pragma unroll 8
+    for (long p = p0; p < p1; ++p) v += partial[p * d + c];
+  }
+  acc[sl][lane] = v;
+  __syncthreads();
+  if (sl == 0 && c < d) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < kColsumSlices; ++k) t += acc[k][lane];
+    out[c] = __float2bfloat16_rn(t);
+  }
 }
 
 // ---------------------------------------------------------------- SwiGLU backward
@@ -431,17 +590,44 @@ void launch_rmsnorm_fwd(const bf16* x, const bf16* g, bf16* y, float* rstd, long
   rmsnorm_fwd_kernel<<<(unsigned)rows, RMS_THREADS, 0, s>>>(x, g, y, rstd, d, eps);
 }
 
+long rmsnorm_bwd_max_d() {
+  static long maxd = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    // widths the register kernel takes need no dynamic shared memory; beyond
+    // them rmsnorm_bwd_kernel keeps d floats in shared memory
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      optin = 48 * 1024;
+    const long smem_d = ((long)optin - 32 * (long)sizeof(float)) / (long)sizeof(float) / 8 * 8;
+    maxd = std::max<long>(smem_d, 8L * kRmsBwdRegMaxVectors);
+  });
+  return maxd;
+}
+
 void launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
                         bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s) {
   if (rows <= 0) return;
   const unsigned nb = blocks_for(rows, kRmsRowsPerBlock);
-  const size_t shm = (size_t)d * sizeof(float);
-  if (shm > 48 * 1024) cudaFuncSetAttribute(rmsnorm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
-  rmsnorm_bwd_kernel<<<nb, RMS_THREADS, shm, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+  const int nv = d / 8;
+  auto threads = [&](int vpt) { return (int)((nv + vpt * 32 - 1) / (vpt * 32) * 32); };
+  if (nv <= 640) {
+    rmsnorm_bwd_rows_kernel<1, true><<<nb, threads(1), 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+  } else if (nv <= 768) {
+    rmsnorm_bwd_rows_kernel<2, false><<<nb, threads(2), 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+  } else if (nv <= kRmsBwdRegMaxVectors) {
+    rmsnorm_bwd_rows_kernel<4, false><<<nb, threads(4), 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+  } else {
+    const size_t shm = (size_t)d * sizeof(float);
+    if (shm > 48 * 1024)
+      cudaFuncSetAttribute(rmsnorm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
+    rmsnorm_bwd_kernel<<<nb, RMS_THREADS, shm, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+  }
 }
 
 void launch_colsum_bf16(const float* partial, long nparts, int d, bf16* out, cudaStream_t s) {
-  colsum_bf16_kernel<<<blocks_for(d, 256), 256, 0, s>>>(partial, nparts, d, out);
+  colsum_bf16_kernel<<<blocks_for(d, 32), 32 * kColsumSlices, 0, s>>>(partial, nparts, d, out);
 }
 
 void launch_swiglu_bwd(const bf16* da, const bf16* gu, bf16* dgu, long rows, int f, cudaStream_t s) {

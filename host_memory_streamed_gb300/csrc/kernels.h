@@ -123,6 +123,9 @@ void launch_rmsnorm_fwd(const bf16* x, const bf16* g, bf16* y, float* rstd, long
 constexpr int kRmsRowsPerBlock = 64;
 void launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
                         bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s);
+// Largest d the backward launches on this device (its shared-memory plan for
+// d > 8192 keeps d floats per block).
+long rmsnorm_bwd_max_d();
 // out[c] = bf16(sum_p partial[p, c]) in a fixed order.
 void launch_colsum_bf16(const float* partial, long nparts, int d, bf16* out, cudaStream_t s);
 // gu [rows, 2f] interleaved (gate, up); da [rows, f] -> dgu [rows, 2f] interleaved.

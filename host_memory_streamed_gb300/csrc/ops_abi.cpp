@@ -3,6 +3,7 @@
 // kernel sequence and return without synchronising.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -174,12 +175,16 @@ int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_
 }
 
 int64_t mt_op_rmsnorm_bwd_scratch_floats(int64_t rows, int32_t d) {
-  return ((rows + mt::kRmsRowsPerBlock - 1) / mt::kRmsRowsPerBlock) * (int64_t)d;
+  if (rows < 0 || d <= 0) return -1;
+  const int64_t parts = rows / mt::kRmsRowsPerBlock + (rows % mt::kRmsRowsPerBlock != 0);
+  if (parts > INT64_MAX / d) return -1;
+  return parts * (int64_t)d;
 }
 
 int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float* rstd, const void* dres, void* dx,
                       void* dg, float* scratch, int64_t rows, int32_t d, void* stream) {
-  if (d <= 0 || d % 8) return op_fail("rmsnorm: d must be a positive multiple of 8");
+  if (d <= 0 || d % 8 || rows < 0) return op_fail("rmsnorm: d must be a positive multiple of 8 and rows >= 0");
+  if (d > mt::rmsnorm_bwd_max_d()) return op_fail("rmsnorm backward: d exceeds the widest row this device takes");
   auto s = static_cast<cudaStream_t>(stream);
   mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
                          static_cast<const mt::bf16*>(g), rstd, static_cast<const mt::bf16*>(dres),

@@ -15,6 +15,7 @@
 // without ordering) race on the array and must be serialised by the caller.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <map>
 #include <mutex>
 #include <string>
@@ -66,10 +67,16 @@ extern "C" int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const vo
     mt::set_op_error("rmsnorm (no-alloc): d must be a positive multiple of 8 and rows >= 0");
     return MT_EINVAL;
   }
-  const long nparts = (long)((rows + mt::kRmsRowsPerBlock - 1) / mt::kRmsRowsPerBlock);
-  if (nparts * (long)d > mt::kNoAllocScratchFloats) {
-    mt::set_op_error("rmsnorm (no-alloc): ceil(rows/64) * d = " + std::to_string(nparts * (long)d) +
-                     " exceeds the fixed scratch of " + std::to_string(mt::kNoAllocScratchFloats) +
+  if (d > mt::rmsnorm_bwd_max_d()) {
+    mt::set_op_error("rmsnorm (no-alloc): d = " + std::to_string(d) + " exceeds the widest row this device takes (" +
+                     std::to_string(mt::rmsnorm_bwd_max_d()) + ")");
+    return MT_EINVAL;
+  }
+  // partial-sum rows, computed without overflow for any rows >= 0
+  const int64_t nparts = rows / mt::kRmsRowsPerBlock + (rows % mt::kRmsRowsPerBlock != 0);
+  if (nparts > mt::kNoAllocScratchFloats / d) {
+    mt::set_op_error("rmsnorm (no-alloc): ceil(rows/64) * d exceeds the fixed scratch of " +
+                     std::to_string(mt::kNoAllocScratchFloats) +
                      " floats; use mt_op_rmsnorm_bwd with a caller buffer");
     return MT_EINVAL;
   }

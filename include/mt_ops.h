@@ -133,11 +133,15 @@ int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
 /* y = x * rsqrt(mean(x^2) + eps) * g over rows of d (d % 8 == 0); rstd: FP32 [rows]. */
 int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_t rows, int32_t d, float eps,
                       void* stream);
-/* FP32 scratch elements mt_op_rmsnorm_bwd needs. */
+/* FP32 scratch elements mt_op_rmsnorm_bwd needs: ceil(rows/64) * d; -1 when
+ * rows < 0, d <= 0 or the product does not fit in int64. */
 int64_t mt_op_rmsnorm_bwd_scratch_floats(int64_t rows, int32_t d);
 /*
  * dx = dres + d(rmsnorm)/dx^T dy (dres may be NULL); dg [d] BF16 = sum over rows
- * of dy * x * rstd, reduced in a fixed order.
+ * of dy * x * rstd, reduced in a fixed order (per 64-row block, then over the
+ * blocks).  d % 8 == 0; rows wider than 8192 keep d floats in shared memory per
+ * block, so d beyond what the device's shared memory holds (about 58K on this
+ * part) returns MT_EINVAL.
  */
 int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float* rstd, const void* dres, void* dx,
                       void* dg, float* scratch, int64_t rows, int32_t d, void* stream);
@@ -176,7 +180,8 @@ int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, co
  * The gain-gradient partial sums go to a fixed array in the library's own
  * device memory (16 MiB, 4,194,304 floats) that every GPU loading the library
  * keeps until the process exits.  The call requires ceil(rows/64) * d <=
- * 4,194,304 and returns MT_EINVAL otherwise (message in mt_op_last_error()).
+ * 4,194,304 and d within mt_op_rmsnorm_bwd's limit, and returns MT_EINVAL
+ * otherwise, before launching anything (message in mt_op_last_error()).
  * It calls no cudaMalloc, cudaFree or allocating library routine.  The first
  * call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call

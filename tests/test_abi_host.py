@@ -218,3 +218,11 @@ def test_moe_padding_capacity_and_route_checks(lib):
     for row_align in (0, 300):
         assert lib.mt_op_moe_route(p, 100, 8, 2, row_align, p, p, p, p, p, p, None) == _lib.MT_EINVAL
     assert lib.mt_op_moe_zero_pads(p, 0, 64, p, None) == _lib.MT_EINVAL
+
+
+def test_rmsnorm_scratch_size_is_overflow_safe(lib):
+    f = lib.mt_op_rmsnorm_bwd_scratch_floats
+    assert f(130, 64) == 3 * 64 and f(128, 64) == 2 * 64 and f(0, 64) == 0
+    assert f(-1, 64) == -1 and f(10, 0) == -1
+    assert f((1 << 63) - 1, 1 << 20) == -1  # the product does not fit in int64
+    assert f((1 << 63) - 1, 8) == ((1 << 63) - 1 + 63) // 64 * 8
