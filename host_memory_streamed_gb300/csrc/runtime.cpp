@@ -44,11 +44,30 @@
 #include <thread>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
 #include <sys/resource.h>
 #include <sys/syscall.h>
 #include <unistd.h>
 
 #include "runtime.h"
+
+namespace {
+// NVTX ranges for timeline profilers (no-ops unless one is attached): one per
+// visit on the compute thread, per weight upload on the loader thread, per
+// gradient evacuation on the D2H thread, per accumulated slab and per Adam task.
+struct NvtxRange {
+  explicit NvtxRange(const char* fmt, int a = 0, int b = 0) {
+    char name[64];
+    std::snprintf(name, sizeof name, fmt, a, b);
+    nvtxRangePushA(name);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+const char* const kVisitRangeFmt[] = {"embed fwd", "layer fwd %d (tile %d)", "head", "recompute %d (tile %d)",
+                                      "layer bwd %d (tile %d)", "embed bwd"};
+}  // namespace
 
 namespace mt {
 namespace {
@@ -571,6 +590,7 @@ void loader_main(mt_model* m) {
                          [&] { return m->abort_flag.load() || m->stop_threads; });
           break;
         }
+        NvtxRange range("h2d visit %d (tile %d)", v, x.tile);
         if (x.prev_user >= 0) {
           wait_flag(m, m->rec_free, x.prev_user, "buffer free");
           MT_CK(cudaStreamWaitEvent(m->s_h2d, m->ev_free[x.prev_user], 0));
@@ -628,6 +648,7 @@ void d2h_main(mt_model* m) {
       if (inject_now(m, MT_INJECT_D2H_FAIL, v)) throw injected("D2H", v);
       const Visit& x = m->visits[v];
       const TileLayout& lay = m->layouts[x.tile];
+      NvtxRange range("d2h visit %d (tile %d)", v, x.tile);
       MT_CK(cudaStreamWaitEvent(m->s_d2h, m->ev_grads[v], 0));
       MT_CK(cudaEventRecord(m->ev_d2h_a[v], m->s_d2h));
       const uint8_t* src = m->gbuf[x.gbuf];
@@ -679,6 +700,7 @@ void submit_adam_range(mt_model* m, int tile, int64_t g_off, int64_t g_bytes) {
       float* mm = reinterpret_cast<float*>(base + lay.off_m + 2 * t.offset) + b;
       float* vv = reinterpret_cast<float*>(base + lay.off_v + 2 * t.offset) + b;
       m->adam_pool->submit([=] {
+        NvtxRange range("adam (tile %d)", tile);
         const auto t0 = Clock::now();
         adam_range(w, g, mm, vv, (size_t)c, h);
         m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
@@ -817,6 +839,7 @@ void accum_main(mt_model* m) {
       m->acc_q.pop_front();
     }
     try {
+      NvtxRange range("accumulate visit %d (tile %d)", j.visit, j.tile);
       wait_event(m, m->ev_slab[j.slab], "gradient slab copy");
       if (inject_now(m, MT_INJECT_ACCUM_FAIL, j.visit)) throw injected("accumulator", j.visit);
       const bool head = m->visits[j.visit].kind == kHead;
@@ -943,19 +966,23 @@ void prepare_tokens(mt_model* m, const int32_t* tokens) {
 
 // ------------------------------------------------------------------ FLOP accounting
 // layer_fwd: one layer's forward; layer_internal: the internals that a
-// backward visit recomputes (the forward without the down projection, whose
-// output the backward does not need); head_fwd: the LM head's forward.
-// Attention counts the causal half of QK^T and PV; a backward counts as two
-// forwards (the usual convention for the model FLOPs).
+// backward visit recomputes (for a dense layer the forward without the down
+// projection, whose output the backward does not need; an MoE layer recomputes
+// its experts' outputs too, for the gate gradient); head_fwd: the LM head's
+// forward.  Attention counts the causal half of QK^T and PV; a backward counts
+// as two forwards (the usual convention for the model FLOPs).  MoE layers count
+// the router and k experts per token (not the rows padding each expert's
+// group to a multiple of 64).
 struct Flops {
   double layer_fwd, layer_internal, head_fwd;
 };
 Flops flop_model(const Dims& D) {
   const double T = (double)D.T;
-  const double down = 2.0 * T * (double)D.f * D.d;
-  const double lin = (double)D.d * D.Dqkv + (double)D.Dq * D.d + (double)D.d * 2.0 * D.f + (double)D.f * D.d;
+  const double attn_lin = (double)D.d * D.Dqkv + (double)D.Dq * D.d;
+  const double mlp = D.E ? D.k * 3.0 * D.d * D.f + (double)D.d * D.E : 3.0 * D.d * D.f;
   const double attn = 4.0 * D.B * D.Hq * D.hd * ((double)D.S * (D.S + 1) / 2.0);
-  const double fwd = 2.0 * T * lin + attn;
+  const double fwd = 2.0 * T * (attn_lin + mlp) + attn;
+  const double down = D.E ? 0.0 : 2.0 * T * (double)D.f * D.d;
   return Flops{fwd, fwd - down, 2.0 * T * (double)D.d * D.V};
 }
 
@@ -1052,6 +1079,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     for (int v = 0; v < (int)m->visits.size(); ++v) {
       check_abort(m);
       const Visit& x = m->visits[v];
+      NvtxRange range(kVisitRangeFmt[x.kind], x.layer, x.tile);
       if (m->trace)
         std::fprintf(stderr, "[mt trace] visit %d (tile %d, layer %d, buffer %d, h2d %d) starts\n", v, x.tile,
                      x.layer, x.buf, (int)x.h2d);

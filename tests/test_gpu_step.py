@@ -158,6 +158,22 @@ def test_statistics_account_for_streamed_bytes():
     assert st["step"] == 1 and st["gemm_launches"] > 0
 
 
+@pytest.mark.parametrize("K", [1, 2])
+def test_executed_flops_are_the_launched_gemms_plus_attention(K):
+    """flops_executed counts what the schedule launches: every GEMM launch
+    (2*M*N*K each, recorded per launch under MT_TIME_KERNELS) plus causal
+    attention once per forward visit, boundary recompute and backward visit's
+    internal recompute, and twice per layer backward."""
+    s = SHAPES["gqa128"].with_(ckpt_every=K)
+    st = _run(s, flags=hms.MT_TIME_KERNELS)["stats"]
+    plan = hms.plan_schedule(s.n_layers, K)
+    kinds = (hms._lib.VISIT_LAYER_FWD, hms._lib.VISIT_RECOMPUTE, hms._lib.VISIT_LAYER_BWD)
+    n_attn = sum(1 for v in plan if v["kind"] in kinds) + 2 * s.n_layers
+    attn = 4.0 * s.batch * s.n_heads * s.head_dim * s.seq * (s.seq + 1) / 2
+    assert st["gemm_launches"] > 0
+    assert st["flops_executed"] == pytest.approx(st["gemm_flops"] + n_attn * attn, rel=1e-9)
+
+
 def test_nonfinite_loss_skips_every_update():
     """A non-finite loss is seen before any gradient lands: the step reports
     MT_ENONFINITE and no weight is updated."""
