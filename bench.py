@@ -39,6 +39,10 @@ sys.path.insert(0, ROOT)
 import mt_inputs  # noqa: E402
 
 METRIC = "streamed train tokens/s and MFU on 1 GB300; % of step roofline; H2D/D2H overlap"
+# Workloads whose description fixes no checkpoint interval: their layers keep
+# their internals in device memory where it holds them (no recompute).  The
+# others follow their stated interval (every layer, every 2 layers).
+KEEP_AUTO_WORKLOADS = ("14b", "70b")
 NOMINAL_BF16_PFLOPS = 2.25
 
 
@@ -197,6 +201,79 @@ def link_bandwidth(device, nbytes=1 << 30):
     return best
 
 
+def _union(iv):
+    """Sorted, merged copy of a list of (start, end) intervals."""
+    out = []
+    for a, b in sorted(iv):
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return out
+
+
+def _measure(iv):
+    return sum(b - a for a, b in iv)
+
+
+def _intersect(u, w):
+    """Total length of the intersection of two merged interval lists."""
+    i = j = 0
+    tot = 0.0
+    while i < len(u) and j < len(w):
+        a, b = max(u[i][0], w[j][0]), min(u[i][1], w[j][1])
+        if b > a:
+            tot += b - a
+        if u[i][1] < w[j][1]:
+            i += 1
+        else:
+            j += 1
+    return tot
+
+
+def traced_overlap(model, toks, device):
+    """Copy/compute overlap from a device timeline of whole steps.
+
+    The steps run under torch.profiler's CUDA activity tracing (CUPTI), which
+    records every kernel and every memcpy of the process with device start and
+    end times, the library's included.  overlap = |(H2D u D2H) n kernels| /
+    |H2D u D2H| over the union of the intervals; the H2D and D2H streams are
+    also reported on their own."""
+    import tempfile
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize(device)
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for t in toks:
+            model.train_step(t)
+        torch.cuda.synchronize(device)
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "trace.json")
+        prof.export_chrome_trace(path)
+        with open(path) as f:
+            ev = json.load(f).get("traceEvents", [])
+    kern, h2d, d2h = [], [], []
+    for e in ev:
+        if e.get("ph") != "X" or "dur" not in e:
+            continue
+        iv = (float(e["ts"]), float(e["ts"]) + float(e["dur"]))
+        cat, name = e.get("cat", ""), e.get("name", "")
+        if cat == "kernel":
+            kern.append(iv)
+        elif cat == "gpu_memcpy" and "HtoD" in name:
+            h2d.append(iv)
+        elif cat == "gpu_memcpy" and "DtoH" in name:
+            d2h.append(iv)
+    K, H, G = _union(kern), _union(h2d), _union(d2h)
+    C = _union(h2d + d2h)
+    tc = _measure(C)
+    return {"method": "torch.profiler CUDA activity (CUPTI) device timeline; |(H2D u D2H) n kernels| / |H2D u D2H|",
+            "steps": len(toks), "kernels": len(kern), "h2d_copies": len(h2d), "d2h_copies": len(d2h),
+            "copy_ms": tc / 1e3, "kernel_ms": _measure(K) / 1e3,
+            "overlap": _intersect(C, K) / tc if tc else None,
+            "h2d_overlap": _intersect(H, K) / _measure(H) if H else None,
+            "d2h_overlap": _intersect(G, K) / _measure(G) if G else None}
+
+
 def load_synthetic_weights(model, s, device):
     """N(0, 0.02) BF16 weights drawn on the GPU from per-tile seeds (1000 + tile), gains 1."""
     for i in range(model.n_tiles):
@@ -321,8 +398,14 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the depth (0 = preset, truncated to host RAM)")
     ap.add_argument("--mlp-chunk-rows", type=int, default=-1,
                     help="MLP row chunk (0 = whole step; default: chunk only when the device arena would not fit)")
+    ap.add_argument("--keep-layers", default="preset",
+                    help="layers whose internals stay on the device from forward to backward: a number, 'auto' "
+                         "(as many as fit) or 'preset' (auto where the workload fixes no checkpoint interval, "
+                         "else 0)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-trace-overlap", action="store_true",
+                    help="skip the two extra steps traced for the copy/compute overlap")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -361,11 +444,18 @@ def main():
     # replicas share the host's cores: split the Adam workers (3/4 of the cores, the library's
     # own default for one process) between them instead of oversubscribing
     adam_threads = max(2, (os.cpu_count() or 4) * 3 // 4 // world) if world > 1 else 0
+    keep = args.keep_layers
+    if keep == "preset":
+        keep = "auto" if s.name in KEEP_AUTO_WORKLOADS else 0
+    elif keep != "auto":
+        keep = int(keep)
+    if chunk:
+        keep = 0  # a chunked MLP keeps no per-layer activations
     model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device, mlp_chunk_rows=chunk,
-                                           n_adam_threads=adam_threads)
+                                           n_adam_threads=adam_threads, keep_layers=keep)
     load_synthetic_weights(model, s, device)
     init_s = time.perf_counter() - t_init
-    toks = token_batches(s, args.warmup + args.steps, device)
+    toks = token_batches(s, args.warmup + args.steps + 2, device)
     host_toks = [t.cpu().pin_memory() for t in toks]
     s_comp = model.streams[0]
 
@@ -412,6 +502,13 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         e2e_elapsed = float(t[0])
     e2e = world * args.steps * tokens_per_step / e2e_elapsed
+    model_keep = model.keep_layers
+    overlap_trace = None
+    if not args.no_trace_overlap and rank == 0:
+        try:
+            overlap_trace = traced_overlap(model, toks[args.warmup + args.steps:], device)
+        except Exception as e:  # the profiler is a measurement aid, not the product
+            overlap_trace = {"error": f"{type(e).__name__}: {e}"}
     model.close()
     del model
 
@@ -440,6 +537,7 @@ def main():
         "config": {"workload": s.name, "layers": s.n_layers, "layers_preset": full_layers, "d_model": s.d_model,
                    "heads": f"{s.n_heads}q/{s.n_kv_heads}kv x {s.head_dim}", "ffn": s.ffn, "vocab": s.vocab,
                    "batch": s.batch, "seq": s.seq, "ckpt_every": s.ckpt_every,
+                   "keep_layers": model_keep,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (weights streamed per layer, activations > 129 MB)",
                    "mlp_chunk_rows": chunk or None,
@@ -460,7 +558,8 @@ def main():
         "overlap": {"copy_ms_per_step": copy_ms / args.steps, "compute_stall_on_weights_ms_per_step":
                     stall_ms / args.steps,
                     "hidden_frac": (1.0 - stall_ms / copy_ms) if copy_ms else None,
-                    "method": "CUDA events: copy windows on the H2D/D2H streams vs compute-stream waits"},
+                    "method": "CUDA events: copy windows on the H2D/D2H streams vs compute-stream waits",
+                    "traced": overlap_trace},
         "roofline": {"bound": "tensor", "kernel": "gemm_bf16_tcgen05", "achieved": achieved, "peak": p_sust,
                      "unit": "TFLOP/s", "frac": (achieved / p_sust) if achieved else None,
                      "traffic": gemm_traffic_per_launch() if s.name == "14b" else None,

@@ -24,16 +24,16 @@ __all__ = ["StreamedDecoder", "MtError", "ops", "plan_schedule", "MT_RESIDENT", 
 LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
 
 
-def plan_schedule(n_layers: int, ckpt_every: int = 1, flags: int = 0) -> list[dict]:
+def plan_schedule(n_layers: int, ckpt_every: int = 1, flags: int = 0, keep_layers: int = 0) -> list[dict]:
     """The visit order of one training step (``mt_plan_schedule``): a list of
     dicts with kind, tile, layer, buf, h2d, buf_wait, gbuf, gbuf_wait.  Host
     only; needs no GPU."""
     lib = _lib.lib()
-    n = lib.mt_plan_schedule(n_layers, ckpt_every, flags, None, 0)
+    n = lib.mt_plan_schedule(n_layers, ckpt_every, keep_layers, flags, None, 0)
     if n < 0:
         raise MtError(n, "mt_plan_schedule: bad arguments")
     out = (_lib.MtVisit * n)()
-    lib.mt_plan_schedule(n_layers, ckpt_every, flags, out, n)
+    lib.mt_plan_schedule(n_layers, ckpt_every, keep_layers, flags, out, n)
     return [{f: getattr(v, f) for f, _ in _lib.MtVisit._fields_} for v in out]
 
 
@@ -53,7 +53,11 @@ class StreamedDecoder:
     def __init__(self, n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, batch, seq, *,
                  ckpt_every=1, rms_eps=1e-5, rope_theta=1e4, lr=1e-4, beta1=0.9, beta2=0.95, adam_eps=1e-8,
                  weight_decay=0.0, n_adam_threads=0, n_pack_threads=0, n_grad_slabs=0, grad_slab_bytes=0,
-                 stage_bytes=0, timeout_ms=0, flags=0, mlp_chunk_rows=0, n_experts=0, top_k=0, device=None):
+                 stage_bytes=0, timeout_ms=0, flags=0, mlp_chunk_rows=0, n_experts=0, top_k=0, keep_layers=0,
+                 device=None):
+        """keep_layers: how many of the last layers keep their internals on the
+        device from forward to backward (no recompute for them); "auto" keeps as
+        many as fit in the device's free memory (less ``KEEP_MARGIN``)."""
         if not torch.cuda.is_available():
             raise RuntimeError("a CUDA device is required (the library has no CPU path)")
         self._L = _lib.lib()
@@ -68,6 +72,8 @@ class StreamedDecoder:
             setattr(cfg, k, v)
         self.cfg = cfg
         self.device = torch.device(device or "cuda")
+        cfg.keep_layers = self.fit_keep_layers(cfg, self.device) if keep_layers == "auto" else int(keep_layers)
+        self.keep_layers = min(int(cfg.keep_layers), n_layers)
         need = self._L.mt_required_device_bytes(C.byref(cfg))
         if need < 0:
             raise MtError(need, self._L.mt_last_error(None).decode())
@@ -84,6 +90,37 @@ class StreamedDecoder:
         self.infos = [self.tile_info(i) for i in range(self.n_tiles)]
         # tied embeddings: tile 0 holds E and gf, and there is no head tile
         self.tied = bool(flags & MT_TIE_EMBEDDINGS)
+
+    KEEP_MARGIN = 6 << 30  # device bytes left free when keep_layers is "auto"
+
+    @classmethod
+    def fit_keep_layers(cls, cfg, device) -> int:
+        """The most layers whose internals fit, with the rest of the arena, in
+        the device's free memory less KEEP_MARGIN (0 when none does)."""
+        torch.cuda.empty_cache()  # blocks torch caches count as used
+        free, _ = torch.cuda.mem_get_info(device)
+        budget = free - cls.KEEP_MARGIN
+        lib = _lib.lib()
+
+        def need(k):
+            c = _lib.MtConfig.from_buffer_copy(cfg)
+            c.keep_layers = k
+            n = lib.mt_required_device_bytes(C.byref(c))
+            if n < 0:
+                raise MtError(n, lib.mt_last_error(None).decode())
+            return n
+        lo, hi = 0, int(cfg.n_layers)
+        if need(hi) <= budget:  # every layer kept also drops the checkpoints and block buffers
+            return hi
+        if need(0) > budget:
+            return 0
+        while lo < hi:  # largest k with need(k) <= budget (need grows with k)
+            mid = (lo + hi + 1) // 2
+            if need(mid) <= budget:
+                lo = mid
+            else:
+                hi = mid - 1
+        return lo
 
     @staticmethod
     def required_device_bytes(s, **kw) -> int:

@@ -34,6 +34,7 @@ class MtConfig(C.Structure):
         ("n_adam_threads", C.c_int32), ("n_pack_threads", C.c_int32), ("n_grad_slabs", C.c_int32),
         ("grad_slab_bytes", C.c_int64), ("stage_bytes", C.c_int64), ("timeout_ms", C.c_int64),
         ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64), ("n_experts", C.c_int32), ("top_k", C.c_int32),
+        ("keep_layers", C.c_int32),
     ]
 
 
@@ -88,7 +89,7 @@ def lib():
     sig = {
         "mt_required_device_bytes": (i64, [C.POINTER(MtConfig)]),
         "mt_init_model": (C.c_int, [C.POINTER(MtConfig), vp, sz, vp, vp, vp, C.POINTER(vp)]),
-        "mt_plan_schedule": (i32, [i32, i32, C.c_uint32, C.POINTER(MtVisit), i32]),
+        "mt_plan_schedule": (i32, [i32, i32, i32, C.c_uint32, C.POINTER(MtVisit), i32]),
         "mt_debug_inject": (C.c_int, [vp, i32, i32]),
         "mt_op_wait_probe": (C.c_int, [vp, i64, vp]),
         "mt_tile_count": (C.c_int, [vp]),

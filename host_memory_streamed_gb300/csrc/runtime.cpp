@@ -162,16 +162,19 @@ struct Visit {
   int prev_gbuf_user = -1;
 };
 
-std::vector<Visit> build_schedule(int L, int K, bool store_acts, bool single_buffer, int head_tile) {
+// keep_from: layers keep_from .. L-1 keep their internals from the forward
+// (their backward visits recompute nothing); layers 0 .. keep_from-1 form the
+// checkpoint blocks of K layers.
+std::vector<Visit> build_schedule(int L, int K, int keep_from, bool single_buffer, int head_tile) {
   std::vector<Visit> v;
   v.push_back({kEmbedFwd, 0, -1});
   for (int i = 0; i < L; ++i) v.push_back({kLayerFwd, i + 1, i});
   v.push_back({kHead, head_tile, -1});
-  const int nblk = (L + K - 1) / K;
+  for (int j = L - 1; j >= keep_from; --j) v.push_back({kLayerBwd, j + 1, j});
+  const int nblk = (keep_from + K - 1) / K;
   for (int b = nblk - 1; b >= 0; --b) {
-    const int s = b * K, e = std::min(L, s + K);
-    if (!store_acts)
-      for (int j = s; j < e - 1; ++j) v.push_back({kRecompute, j + 1, j});
+    const int s = b * K, e = std::min(keep_from, s + K);
+    for (int j = s; j < e - 1; ++j) v.push_back({kRecompute, j + 1, j});
     for (int j = e - 1; j >= s; --j) v.push_back({kLayerBwd, j + 1, j});
   }
   v.push_back({kEmbedBwd, 0, -1});
@@ -371,6 +374,7 @@ struct mt_model {
   int device = 0;
   int K = 1;
   bool resident_mode = false, store_acts = false, single_buffer = false, debug = false, time_kernels = false;
+  int keep_from = 0;  // first layer whose internals stay on the device (L: none); stored[i - keep_from]
   bool trace = false;
   bool visit_log = false;
   bool tied = false;   // MT_TIE_EMBEDDINGS: the head's weight is tile 0's E
@@ -988,8 +992,8 @@ Flops flop_model(const Dims& D) {
 
 // ------------------------------------------------------------------ the step
 bf16* x_fwd_loc(mt_model* m, int i) {
-  if (m->store_acts) return i < m->D.L ? m->stored[i].x : m->xtmp[m->D.L % 2];
-  return (i < m->D.L && i % m->K == 0) ? m->ckpt[i / m->K] : m->xtmp[i % 2];
+  if (i < m->D.L && i >= m->keep_from) return m->stored[i - m->keep_from].x;
+  return (i < m->keep_from && i % m->K == 0) ? m->ckpt[i / m->K] : m->xtmp[i % 2];
 }
 
 int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev, size_t n_tokens, float* loss_out) {
@@ -1119,9 +1123,10 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
           break;
         case kLayerFwd: {
           const int i = x.layer;
-          LayerActs a = m->store_acts ? m->stored[i] : m->acts;
+          const bool kept = i >= m->keep_from;
+          LayerActs a = kept ? m->stored[i - m->keep_from] : m->acts;
           a.x = x_fwd_loc(m, i);
-          rc = tmpl.forward(bind_layer(lay, wb), a, x_fwd_loc(m, i + 1), m->store_acts);
+          rc = tmpl.forward(bind_layer(lay, wb), a, x_fwd_loc(m, i + 1), kept);
           break;
         }
         case kHead:
@@ -1138,8 +1143,8 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
         case kLayerBwd: {
           const int j = x.layer;
           LayerActs a;
-          if (m->store_acts) {
-            a = m->stored[j];
+          if (j >= m->keep_from) {
+            a = m->stored[j - m->keep_from];
           } else {
             const int s = j / m->K * m->K;
             a = m->acts;
@@ -1265,7 +1270,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     int n_fwd = 0, n_internal = 0;
     for (const auto& x : m->visits) {
       if (x.kind == kLayerFwd || x.kind == kRecompute) ++n_fwd;
-      if (x.kind == kLayerBwd && !m->store_acts) ++n_internal;
+      if (x.kind == kLayerBwd && x.layer < m->keep_from) ++n_internal;
     }
     st.flops_model = (int64_t)(3.0 * (D.L * fm.layer_fwd + fm.head_fwd));
     st.flops_executed = (int64_t)(n_fwd * fm.layer_fwd + n_internal * fm.layer_internal + 2.0 * D.L * fm.layer_fwd +
@@ -1342,8 +1347,10 @@ const char* validate(const mt_config& c) {
     if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq)
       return "mlp_chunk_rows does not apply to MoE layers";
   }
-  if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq && (c.flags & MT_STORE_ACTS))
-    return "a chunked MLP keeps no per-layer gate/up activations: not combinable with MT_STORE_ACTS";
+  if (c.keep_layers < 0) return "keep_layers must be >= 0";
+  if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq &&
+      ((c.flags & MT_STORE_ACTS) || c.keep_layers > 0))
+    return "a chunked MLP keeps no per-layer gate/up activations: not combinable with MT_STORE_ACTS or keep_layers";
   if (c.grad_slab_bytes > 0 && align_up(c.grad_slab_bytes, kPage) < 2LL * c.d_model)
     return "grad_slab_bytes must hold one embedding row (2 * d_model bytes)";
   if (!(c.rms_eps > 0) || !(c.rope_theta > 0) || !(c.lr >= 0) || !(c.beta1 >= 0 && c.beta1 < 1) ||
@@ -1366,6 +1373,12 @@ mt_config with_defaults(const mt_config& in) {
   c.grad_slab_bytes = align_up(c.grad_slab_bytes, kPage);
   c.stage_bytes = align_up(c.stage_bytes, kPage);
   return c;
+}
+
+// First layer that keeps its internals on the device (n_layers: none).
+int keep_from_of(const mt_config& c) {
+  if (c.flags & MT_STORE_ACTS) return 0;
+  return std::max(0, c.n_layers - std::max(0, c.keep_layers));
 }
 
 // Lay out the device arena; with base == nullptr only the byte count is computed.
@@ -1392,15 +1405,17 @@ int64_t plan_arena(mt_model* m, uint8_t* base) {
   m->ckpt.clear();
   m->blockbuf.clear();
   m->stored.clear();
-  if (m->store_acts) {
-    for (int i = 0; i < D.L; ++i) {
-      uint8_t* x = at(xb);
-      uint8_t* p = at(as.total);
-      m->stored.push_back(base ? carve_acts(p, D, reinterpret_cast<bf16*>(x)) : LayerActs{});
-    }
-  } else {
-    for (int i = 0; i < (D.L + m->K - 1) / m->K; ++i) m->ckpt.push_back(reinterpret_cast<bf16*>(at(xb)));
-    for (int i = 0; i < m->K - 1; ++i) m->blockbuf.push_back(reinterpret_cast<bf16*>(at(xb)));
+  // kept layers: their input and internals, one set each
+  for (int i = m->keep_from; i < D.L; ++i) {
+    uint8_t* x = at(xb);
+    uint8_t* p = at(as.total);
+    m->stored.push_back(base ? carve_acts(p, D, reinterpret_cast<bf16*>(x)) : LayerActs{});
+  }
+  // recomputed layers: their block checkpoints, the block buffers and one
+  // shared set of internals
+  if (m->keep_from > 0) {
+    for (int i = 0; i < (m->keep_from + m->K - 1) / m->K; ++i) m->ckpt.push_back(reinterpret_cast<bf16*>(at(xb)));
+    for (int i = 0; i < std::min(m->K, m->keep_from) - 1; ++i) m->blockbuf.push_back(reinterpret_cast<bf16*>(at(xb)));
     uint8_t* p = at(as.total);
     if (base) m->acts = carve_acts(p, D, nullptr);
   }
@@ -1505,6 +1520,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->K = m->cfg.ckpt_every;
   m->resident_mode = m->cfg.flags & MT_RESIDENT;
   m->store_acts = m->cfg.flags & MT_STORE_ACTS;
+  m->keep_from = keep_from_of(m->cfg);
   m->single_buffer = m->cfg.flags & MT_NO_DOUBLE_BUFFER;
   m->debug = m->cfg.flags & MT_DEBUG_CHECKS;
   m->time_kernels = m->cfg.flags & MT_TIME_KERNELS;
@@ -1526,7 +1542,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->arena_used = plan_arena(m, m->arena);
 
   // visit schedule
-  m->visits = build_schedule(m->D.L, m->K, m->store_acts, m->single_buffer, m->head_tile);
+  m->visits = build_schedule(m->D.L, m->K, m->keep_from, m->single_buffer, m->head_tile);
   if (m->resident_mode)
     for (auto& x : m->visits) x.h2d = false;
   const int nv = (int)m->visits.size();
@@ -1626,10 +1642,12 @@ using mt::MtError;
 
 extern "C" {
 
-int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, uint32_t flags, mt_visit* out, int32_t cap) {
-  if (n_layers < 1 || ckpt_every < 1 || cap < 0) return MT_EINVAL;
+int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, int32_t keep_layers, uint32_t flags, mt_visit* out,
+                         int32_t cap) {
+  if (n_layers < 1 || ckpt_every < 1 || keep_layers < 0 || cap < 0) return MT_EINVAL;
   const bool tied = flags & MT_TIE_EMBEDDINGS;
-  const auto v = mt::build_schedule(n_layers, ckpt_every, flags & MT_STORE_ACTS, flags & MT_NO_DOUBLE_BUFFER,
+  const int keep_from = (flags & MT_STORE_ACTS) ? 0 : std::max(0, n_layers - keep_layers);
+  const auto v = mt::build_schedule(n_layers, ckpt_every, keep_from, flags & MT_NO_DOUBLE_BUFFER,
                                     tied ? 0 : n_layers + 1);
   for (int i = 0; out && i < (int)v.size() && i < cap; ++i) {
     const mt::Visit& x = v[i];
@@ -1650,6 +1668,7 @@ int64_t mt_required_device_bytes(const mt_config* cfg) {
   tmp.K = tmp.cfg.ckpt_every;
   tmp.resident_mode = tmp.cfg.flags & MT_RESIDENT;
   tmp.store_acts = tmp.cfg.flags & MT_STORE_ACTS;
+  tmp.keep_from = mt::keep_from_of(tmp.cfg);
   mt::build_layouts(&tmp);
   return mt::plan_arena(&tmp, nullptr);
 }
@@ -1852,7 +1871,7 @@ int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, 
     MT_CK(cudaMemcpyAsync(wb, m->tiles[tile] + lay.off_w, (size_t)lay.w_bytes, cudaMemcpyHostToDevice, m->s_comp));
     LaunchStats ls;
     LayerTemplate tmpl{D, m->cfg.rms_eps, m->s_comp, &m->ws, &ls};
-    LayerActs a = m->store_acts ? m->stored[layer] : m->acts;
+    LayerActs a = layer >= m->keep_from ? m->stored[layer - m->keep_from] : m->acts;
     a.x = reinterpret_cast<bf16*>(const_cast<void*>(x_in));
     int rc = tmpl.forward(bind_layer(lay, wb), a, reinterpret_cast<bf16*>(x_out), dx_out != nullptr);
     if (dx_out) {

@@ -75,7 +75,8 @@ enum {
 /* mt_config.flags */
 enum {
   MT_RESIDENT = 1u << 0,          /* upload every tile's W once; no streaming (test path) */
-  MT_STORE_ACTS = 1u << 1,        /* keep every layer's internals from forward; no recompute (test path) */
+  MT_STORE_ACTS = 1u << 1,        /* keep every layer's internals from forward; no recompute (keep_layers =
+                                     n_layers) */
   MT_NO_DOUBLE_BUFFER = 1u << 2,  /* one device weight buffer: no H2D/compute overlap (ablation) */
   MT_DEBUG_CHECKS = 1u << 3,      /* NaN/Inf scan of every gradient tile; host event-order asserts */
   MT_TIME_KERNELS = 1u << 4,      /* CUDA-event timing of every GEMM launch (mt_get_step_stats) */
@@ -125,6 +126,17 @@ typedef struct {
                                 interleaved) and wd [n_experts * d, ffn].  Not combinable with
                                 mlp_chunk_rows. */
   int32_t top_k;             /* experts per token (1 .. min(8, n_experts)); ignored when n_experts = 0 */
+  int32_t keep_layers;       /* the last keep_layers decoder layers keep their internals (normalised
+                                inputs, q/k/v, attention output and log-sum-exp, residual, gate/up and
+                                SwiGLU activations) in device memory from their forward to their
+                                backward, so their backward visits recompute nothing; the other layers
+                                follow the ckpt_every block schedule.  Checkpointing trades device memory
+                                for recompute (hyper.ai summary, 实验 ablation: checkpoint interval 1
+                                cuts the largest batch 96 -> 32); a device with the memory for every
+                                layer's internals needs no recompute.  0 = every layer recomputed;
+                                >= n_layers = every layer kept (as MT_STORE_ACTS).  Each kept layer adds
+                                its stored set to mt_required_device_bytes.  Not combinable with
+                                mlp_chunk_rows. */
 } mt_config;
 
 typedef struct mt_model mt_model;
@@ -194,7 +206,8 @@ enum {
   MT_VISIT_LAYER_FWD = 1, /* layer forward; x_i kept when i % ckpt_every == 0 */
   MT_VISIT_HEAD = 2,      /* final norm + LM head + cross-entropy, forward and backward */
   MT_VISIT_RECOMPUTE = 3, /* layer forward again inside a checkpoint block (backward pass) */
-  MT_VISIT_LAYER_BWD = 4, /* layer backward (its internals recomputed from x_i in the same visit) */
+  MT_VISIT_LAYER_BWD = 4, /* layer backward (its internals recomputed from x_i in the same visit unless the
+                             layer keeps them from its forward) */
   MT_VISIT_EMBED_BWD = 5  /* embedding gradient rows (no weights needed on the device) */
 };
 typedef struct {
@@ -210,18 +223,21 @@ typedef struct {
 
 /*
  * The visit order one mt_train_step runs for n_layers decoder layers,
- * checkpoint interval ckpt_every (K) and flags (MT_STORE_ACTS,
- * MT_NO_DOUBLE_BUFFER and MT_TIE_EMBEDDINGS matter; MT_RESIDENT models use the
- * same order with every tile resident).  Host only, no handle: the forward
- * visits every layer in order, the head follows, then the checkpoint blocks
- * run in reverse (per block [s, e): layers s .. e-2 recomputed, then layers
- * e-1 .. s backward), then the embedding gradient (MegaTrain paperlayer.ai
- * summary, §3 "Execution workflow" and §A.3 "Block-wise recomputation").  A
- * tile still held by one of the two buffers is not streamed again.  Writes at
- * most cap visits to out (out may be NULL) and returns the number of visits,
- * or MT_EINVAL for n_layers < 1, ckpt_every < 1 or cap < 0.
+ * checkpoint interval ckpt_every (K), keep_layers (mt_config.keep_layers) and
+ * flags (MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER and MT_TIE_EMBEDDINGS matter;
+ * MT_RESIDENT models use the same order with every tile resident).  Host
+ * only, no handle: the forward visits every layer in order, the head
+ * follows, then the kept layers' backward visits (last layer first), then
+ * the remaining layers' checkpoint blocks in reverse (per block [s, e):
+ * layers s .. e-2 recomputed, then layers e-1 .. s backward), then the
+ * embedding gradient (MegaTrain paperlayer.ai summary, §3 "Execution
+ * workflow" and §A.3 "Block-wise recomputation").  A tile still held by one
+ * of the two buffers is not streamed again.  Writes at most cap visits to out
+ * (out may be NULL) and returns the number of visits, or MT_EINVAL for
+ * n_layers < 1, ckpt_every < 1, keep_layers < 0 or cap < 0.
  */
-int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, uint32_t flags, mt_visit* out, int32_t cap);
+int32_t mt_plan_schedule(int32_t n_layers, int32_t ckpt_every, int32_t keep_layers, uint32_t flags, mt_visit* out,
+                         int32_t cap);
 
 /*
  * Host-side fault injection, for tests of failure detection that fault no

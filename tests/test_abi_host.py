@@ -56,7 +56,8 @@ def test_required_device_bytes_positive_and_bounded(lib, name):
                                  dict(vocab=0), dict(batch=0), dict(seq=3, batch=1), dict(mlp_chunk_rows=100),
                                  dict(mlp_chunk_rows=128, flags=2), dict(n_experts=12, top_k=2),
                                  dict(n_experts=8, top_k=0), dict(n_experts=8, top_k=9), dict(n_experts=512, top_k=2),
-                                 dict(n_experts=8, top_k=2, mlp_chunk_rows=128)])
+                                 dict(n_experts=8, top_k=2, mlp_chunk_rows=128), dict(keep_layers=-1),
+                                 dict(keep_layers=1, mlp_chunk_rows=128)])
 def test_bad_config_rejected(lib, bad):
     s = mt_inputs.PRESETS["tiny"]
     assert lib.mt_required_device_bytes(C.byref(_cfg(s, **bad))) == -1
@@ -226,3 +227,16 @@ def test_rmsnorm_scratch_size_is_overflow_safe(lib):
     assert f(-1, 64) == -1 and f(10, 0) == -1
     assert f((1 << 63) - 1, 1 << 20) == -1  # the product does not fit in int64
     assert f((1 << 63) - 1, 8) == ((1 << 63) - 1 + 63) // 64 * 8
+
+
+def test_kept_layers_add_their_internals_to_the_arena(lib):
+    """Each kept layer adds one stored set (its input and internals) to the
+    device arena; keeping every layer drops the checkpoints and the shared set
+    and equals MT_STORE_ACTS."""
+    import host_memory_streamed_gb300 as hms
+    s = mt_inputs.PRESETS["tiny"].with_(n_layers=4)
+    need = [lib.mt_required_device_bytes(C.byref(_cfg(s, keep_layers=k))) for k in range(5)]
+    step = need[2] - need[1]
+    assert step > 0 and need[3] - need[2] == step
+    assert need[4] == lib.mt_required_device_bytes(C.byref(_cfg(s, flags=hms.MT_STORE_ACTS)))
+    assert lib.mt_required_device_bytes(C.byref(_cfg(s, keep_layers=9))) == need[4]

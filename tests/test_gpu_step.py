@@ -91,6 +91,20 @@ def test_recompute_equals_stored_activations_bitexact():
     _equal_trees(a["g"][-1], b["g"][-1])
 
 
+@pytest.mark.parametrize("K,keep", [(1, 1), (1, 2), (2, 1), (2, 2), (3, 2), (1, 3)])
+def test_kept_layers_equal_recompute_bitexact(K, keep):
+    """The last `keep` layers keep their internals from the forward (no
+    recompute in their backward); the result is the recompute schedule's, bit
+    for bit, and the executed-FLOP count drops by their internal recompute."""
+    s = SHAPES["gqa128"].with_(ckpt_every=K)
+    a = _run(s, steps=2)
+    b = _run(s, steps=2, keep_layers=keep)
+    assert a["loss"] == b["loss"]
+    _equal_trees(a["w"][-1], b["w"][-1])
+    _equal_trees(a["g"][-1], b["g"][-1])
+    assert b["stats"]["flops_executed"] < a["stats"]["flops_executed"]
+
+
 @pytest.mark.parametrize("variant", ["ckpt2", "ckpt3", "single_buffer", "small_chunks"])
 def test_schedule_variants_bitexact(variant):
     s = SHAPES["gqa128"]

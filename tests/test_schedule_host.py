@@ -22,14 +22,17 @@ def built():
     build.build()
 
 
-def expected_order(L, K, store_acts=False):
-    """(kind, layer) of every visit, written out from the description."""
+def expected_order(L, K, store_acts=False, keep=0):
+    """(kind, layer) of every visit, written out from the description: the
+    kept layers (the last `keep`, or all with stored activations) go backward
+    without recompute, the others in checkpoint blocks of K."""
     v = [(EF, -1)] + [(LF, i) for i in range(L)] + [(HD, -1)]
-    starts = list(range(0, L, K))
+    L0 = 0 if store_acts else max(0, L - keep)
+    v += [(LB, j) for j in range(L - 1, L0 - 1, -1)]
+    starts = list(range(0, L0, K))
     for s in reversed(starts):
-        e = min(L, s + K)
-        if not store_acts:
-            v += [(RC, j) for j in range(s, e - 1)]
+        e = min(L0, s + K)
+        v += [(RC, j) for j in range(s, e - 1)]
         v += [(LB, j) for j in range(e - 1, s - 1, -1)]
     return v + [(EB, -1)]
 
@@ -131,7 +134,33 @@ def test_gradient_buffers_rotate(L, K):
 
 def test_bad_arguments_and_counting_call():
     lib = _lib.lib()
-    assert lib.mt_plan_schedule(0, 1, 0, None, 0) == _lib.MT_EINVAL
-    assert lib.mt_plan_schedule(4, 0, 0, None, 0) == _lib.MT_EINVAL
-    assert lib.mt_plan_schedule(4, 1, 0, None, -1) == _lib.MT_EINVAL
-    assert lib.mt_plan_schedule(4, 1, 0, None, 0) == len(expected_order(4, 1))
+    assert lib.mt_plan_schedule(0, 1, 0, 0, None, 0) == _lib.MT_EINVAL
+    assert lib.mt_plan_schedule(4, 0, 0, 0, None, 0) == _lib.MT_EINVAL
+    assert lib.mt_plan_schedule(4, 1, -1, 0, None, 0) == _lib.MT_EINVAL
+    assert lib.mt_plan_schedule(4, 1, 0, 0, None, -1) == _lib.MT_EINVAL
+    assert lib.mt_plan_schedule(4, 1, 0, 0, None, 0) == len(expected_order(4, 1))
+
+
+@pytest.mark.parametrize("L,K,keep", [(1, 1, 1), (5, 1, 2), (5, 2, 3), (7, 3, 2), (8, 4, 8), (8, 4, 20),
+                                      (48, 1, 48), (48, 1, 30), (24, 2, 5)])
+def test_kept_layers_go_backward_without_recompute(L, K, keep):
+    """The last `keep` layers keep their internals: their backward visits come
+    right after the head with no recompute; the rest keep the block schedule.
+    keep >= L is the stored-activations schedule."""
+    v = hms.plan_schedule(L, K, 0, keep)
+    assert [(x["kind"], x["layer"]) for x in v] == expected_order(L, K, keep=keep)
+    L0 = max(0, L - keep)
+    n_rc = sum(x["kind"] == RC for x in v)
+    assert n_rc == L0 - (L0 + K - 1) // K
+    if keep >= L:
+        assert v == hms.plan_schedule(L, K, hms.MT_STORE_ACTS)
+    # every layer still has exactly one forward and one backward visit
+    assert sorted(x["layer"] for x in v if x["kind"] == LB) == list(range(L))
+    # the buffers hold what each visit binds (as in the block schedule)
+    held = [None, None]
+    for x in v:
+        if x["kind"] == EB:
+            continue
+        if x["h2d"]:
+            held[x["buf"]] = x["tile"]
+        assert held[x["buf"]] == x["tile"]
