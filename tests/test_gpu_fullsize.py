@@ -23,7 +23,7 @@ import torch
 import mt_inputs
 import oracle
 from oracle import OracleConfig
-from tests import parity
+from tests import bounds, parity
 
 pytestmark = pytest.mark.gpu
 
@@ -154,6 +154,12 @@ def test_attention_full_length_sampled_rows_and_keys(name):
             assert float((lse_g - lse_r).abs().max()) < 1e-4 * max(1.0, float(lse_r.abs().max())), (name, b, h)
             c, r = cos_rel(dqkv[idx, h * hd:(h + 1) * hd], dq_r)
             assert r < 1e-2, (name, b, h, "dq", r)
+            # element-wise, each sampled row against its own bound
+            do_h = do[seq][:, h * hd:(h + 1) * hd]
+            rb = [bounds.attention_row(q, k, v, do_h, i) for i in rows]
+            bounds.check(o[idx, h * hd:(h + 1) * hd], o_r, torch.stack([x[0] for x in rb]), f"{name} o (b{b} h{h})")
+            bounds.check(dqkv[idx, h * hd:(h + 1) * hd], dq_r, torch.stack([x[1] for x in rb]),
+                         f"{name} dq (b{b} h{h})")
         for j in sorted({h * Hkv // Hq for h in hs}):
             heads = range(j * G, (j + 1) * G)
             qs = torch.stack([x[:, h * hd:(h + 1) * hd] for h in heads]).to(D)
@@ -167,6 +173,9 @@ def test_attention_full_length_sampled_rows_and_keys(name):
                 dvs.append(dv_r)
                 gk.append(dqkv[b * S + key, (Hq + j) * hd:(Hq + j + 1) * hd])
                 gv.append(dqkv[b * S + key, (Hq + Hkv + j) * hd:(Hq + Hkv + j + 1) * hd])
+                bk, bv = bounds.attention_key(qs, k, v, dos, key)
+                bounds.check(gk[-1], dk_r, bk, f"{name} dk (b{b} kv{j} key {key})")
+                bounds.check(gv[-1], dv_r, bv, f"{name} dv (b{b} kv{j} key {key})")
             _, r = cos_rel(torch.stack(gk), torch.stack(dks))
             assert r < 1e-2, (name, b, j, "dk", r)
             _, r = cos_rel(torch.stack(gv), torch.stack(dvs))
@@ -240,19 +249,29 @@ def test_full_width_model_matches_oracle(name):
     finally:
         m.close()
     assert all(c >= parity.GRAD_COS for c, _ in rep.values()), rep
+    names = ["embed"] + [f"layer{j}" for j in range(s.n_layers)] + ["head"]
+    for (i, k), (c, r) in sorted(rep.items()):
+        print(f"{name} {names[i]}.{k}: cos {c:.6f} rel {r:.4f}")
     over = {key: r for key, (c, r) in rep.items() if r > parity.GRAD_RTOL}
     if over:
-        # Beyond the target's normwise bound: allowed only as far as BF16
-        # storage between kernels forces it.  The storage-precision model (the
-        # same step in FP32 with BF16 rounding where the library stores BF16,
-        # no kernels) bounds the error every implementation of that precision
-        # shows; the library may add at most 10 % on top.
+        # The target's normwise bound is not met for these tensors.  Reading
+        # R8: BF16 tensor-core operands (the normalised activations and q/k/v
+        # feeding the BF16 GEMMs and attention) force this error on any
+        # implementation that stores them in BF16; the storage-precision model
+        # (the same step in FP32, rounded to BF16 exactly where the library
+        # stores BF16, no kernels) shows it on the same inputs.  The test
+        # reports the case as an expected failure of the target, and fails
+        # outright if the library's error is not that storage error (more
+        # than 10 % above the model's).
         from tests import precision_model as pm
         assert s.batch == 1
         _, gm = pm.Model(pm.ALL).loss_and_grads(params, tokens, cfg)
-        names = ["embed"] + [f"layer{j}" for j in range(s.n_layers)] + ["head"]
-        for (i, k), r in over.items():
+        lines = []
+        for (i, k), r in sorted(over.items()):
             tree = gm["embed"] if i == 0 else (gm["head"] if i == s.n_layers + 1 else gm["layers"][i - 1])
             _, r_model = cos_rel(tree[k], m._tile_named(grads, i)[k])
-            print(f"{names[i]}.{k}: library {r:.4f}, storage-precision model {r_model:.4f}")
+            lines.append(f"{names[i]}.{k}: library {r:.4f}, storage-precision model {r_model:.4f}")
+            print(lines[-1])
             assert r <= 1.1 * r_model, (names[i], k, r, r_model)
+        pytest.xfail("normwise gradient error above 2e-2 from BF16 storage of tensor-core operands: " +
+                     "; ".join(lines))

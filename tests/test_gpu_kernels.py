@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import oracle
+from tests import bounds
 
 pytestmark = pytest.mark.gpu
 
@@ -57,17 +58,27 @@ def test_gemm_residual_accumulate_swiglu_rope():
     A, B, R = rnd((M, K), g), rnd((N, K), g), rnd((M, N), g)
     Ad, Bd = A.to(DEV), B.to(DEV)
     ref = A.to(D) @ B.to(D).T
+    err = bounds.gemm_err(A, B, K)  # the FP32 accumulator's error, element-wise
     out = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
     ops.gemm(Ad, Bd, out, _lib.EPI_RESIDUAL_BF16, residual=R.to(DEV))
     assert rel(out, ref + R.to(D)) < 4e-3
+    bounds.check(out, ref + R.to(D), bounds.store_bf16(ref + R.to(D), err), "residual epilogue")
     acc = torch.full((M, N), 0.5, device=DEV)
     ops.gemm(Ad, Bd, acc, _lib.EPI_F32_ACCUMULATE)
     assert rel(acc, ref + 0.5) < 1e-6
+    bounds.check(acc, ref + 0.5, bounds.MARGIN * (err + 2.0 ** -23 * (ref + 0.5).abs()), "FP32 += epilogue")
     a = torch.empty(M, N // 2, device=DEV, dtype=torch.bfloat16)
     gu = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
     ops.gemm(Ad, Bd, a, _lib.EPI_SWIGLU, out2=gu)
-    assert rel(a, oracle.swiglu(ref[:, 0::2], ref[:, 1::2])) < 4e-3
+    a_ref = oracle.swiglu(ref[:, 0::2], ref[:, 1::2])
+    assert rel(a, a_ref) < 4e-3
     assert rel(gu, ref) < 4e-3
+    gt, up = ref[:, 0::2], ref[:, 1::2]
+    sg = torch.sigmoid(gt)
+    a_in = (sg * (1 + gt * (1 - sg))).abs() * up.abs() * err[:, 0::2] + (gt * sg).abs() * err[:, 1::2] + \
+        8 * 2.0 ** -23 * a_ref.abs()
+    bounds.check(a, a_ref, bounds.store_bf16(a_ref, a_in), "SwiGLU epilogue")
+    bounds.check(gu, ref, bounds.store_bf16(ref, err), "SwiGLU epilogue's stored gate/up")
     cos, sin = rope_tables(S, hd)
     ro = torch.empty(M, N, device=DEV, dtype=torch.bfloat16)
     ops.gemm(Ad, Bd, ro, _lib.EPI_ROPE, rope_cos=cos, rope_sin=sin, rope_cols=3 * hd, head_dim=hd, seq=S)
@@ -77,6 +88,16 @@ def test_gemm_residual_accumulate_swiglu_rope():
     x = ref[:, :3 * hd].reshape(B_, S_, 3, hd)
     expect = torch.cat([oracle.rope(x, c64, s64).reshape(M, 3 * hd), ref[:, 3 * hd:]], 1)
     assert rel(ro, expect) < 4e-3
+    # rotated columns: |cos| e_1 + |sin| e_2 from the accumulator, a few FP32
+    # roundings of the products (and of the FP32 tables), then BF16
+    h = hd // 2
+    e = err[:, :3 * hd].reshape(B_, S_, 3, hd)
+    xa = x.abs()
+    ca, sa = c64.abs()[None, :, None, :], s64.abs()[None, :, None, :]
+    e_rot = torch.cat([ca * e[..., :h] + sa * e[..., h:], ca * e[..., h:] + sa * e[..., :h]], -1) + \
+        8 * 2.0 ** -23 * torch.cat([ca * xa[..., :h] + sa * xa[..., h:], ca * xa[..., h:] + sa * xa[..., :h]], -1)
+    e_all = torch.cat([e_rot.reshape(M, 3 * hd), err[:, 3 * hd:]], 1)
+    bounds.check(ro, expect, bounds.store_bf16(expect, e_all), "RoPE epilogue")
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 344, 256), (256, 688, 512), (33, 40, 64)])
@@ -93,6 +114,9 @@ def test_gemm_swiglu_backward_epilogue(M, N, K):
     dg, du = oracle.swiglu_backward(da, gu.to(D)[:, 0::2], gu.to(D)[:, 1::2])
     assert rel(dgu.cpu()[:, 0::2], dg) < 4e-3
     assert rel(dgu.cpu()[:, 1::2], du) < 4e-3
+    bg, bu = bounds.swiglu_bwd(dg, du, da, gu[:, 0::2], gu[:, 1::2], da_err=bounds.gemm_err(dY, W, K))
+    bounds.check(dgu.cpu()[:, 0::2], dg, bg, "SwiGLU-backward epilogue dgate")
+    bounds.check(dgu.cpu()[:, 1::2], du, bu, "SwiGLU-backward epilogue dup")
 
 
 # Both kernels (single CTA for M <= 128, CTA pairs with 256 x 256 tiles above)
@@ -193,6 +217,48 @@ def test_attention_forward_backward_vs_oracle(B, S, Hq, Hkv, hd):
             assert float(a.abs().max()) < 1e-2 * float(do.to(D).abs().max()), name
         else:
             assert rel(a, b_) < 1e-2, (name, rel(a, b_))
+    # element-wise: every output, query head and key head against its bound
+    _attention_elementwise(o.cpu().to(D), got, q, k, v, do.to(D).reshape(B, S, Hq, hd), o_ref, dq, dk, dv)
+
+
+def _attention_elementwise(o, got, q, k, v, do, o_ref, dq, dk, dv, rope=None):
+    """|gpu - oracle| <= bound for o, dq, dk, dv, element by element (bounds
+    from tests/bounds.py: BF16 P and dS operands, FP32 sums, BF16 outputs).
+    rope = (cos, sin): the backward's outputs are the inverse-rotated grads."""
+    B, S, Hq, hd = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    T = B * S
+    bo = torch.empty(B, S, Hq, hd, dtype=D)
+    e_dq = torch.empty(B, S, Hq, hd, dtype=D)
+    e_dk = torch.zeros(B, S, Hkv, hd, dtype=D)
+    e_dv = torch.zeros(B, S, Hkv, hd, dtype=D)
+    for b in range(B):
+        for h in range(Hq):
+            j = h // G
+            r = bounds.attention_head(q[b, :, h], k[b, :, j], v[b, :, j], do[b, :, h])
+            bo[b, :, h] = r["bo"]
+            e_dq[b, :, h] = r["e_dq"]
+            e_dk[b, :, j] += r["e_dk"]
+            e_dv[b, :, j] += r["e_dv"]
+    bounds.check(o, o_ref.reshape(T, -1), bo.reshape(T, -1), "attention o")
+    dq, dk, dv = dq.reshape(B, S, Hq, hd), dk.reshape(B, S, Hkv, hd), dv.reshape(B, S, Hkv, hd)
+    if rope is not None:
+        c, s_ = rope
+        h2 = hd // 2
+        ca, sa = c.abs()[None, :, None, :], s_.abs()[None, :, None, :]
+
+        def rot_err(e, x):
+            xa = x.abs()
+            return torch.cat([ca * e[..., :h2] + sa * e[..., h2:], ca * e[..., h2:] + sa * e[..., :h2]], -1) + \
+                8 * 2.0 ** -23 * torch.cat([ca * xa[..., :h2] + sa * xa[..., h2:],
+                                            ca * xa[..., h2:] + sa * xa[..., :h2]], -1)
+        e_dq, e_dk = rot_err(e_dq, dq), rot_err(e_dk, dk)
+        dq, dk = oracle.rope_backward(dq, c, s_), oracle.rope_backward(dk, c, s_)
+    for name, a, ref, e in (("dq", got[:, :Hq * hd], dq, e_dq), ("dk", got[:, Hq * hd:(Hq + Hkv) * hd], dk, e_dk),
+                            ("dv", got[:, (Hq + Hkv) * hd:], dv, e_dv)):
+        ref = ref.reshape(T, -1)
+        bounds.check(a, ref, bounds.MARGIN * (e.reshape(T, -1) + bounds.U * ref.abs()), f"attention {name}")
 
 
 def test_attention_backward_with_rope_gives_unrotated_grads():
@@ -218,6 +284,10 @@ def test_attention_backward_with_rope_gives_unrotated_grads():
     got = dqkv.cpu().to(D)
     assert rel(got[:, :Hq * hd], oracle.rope_backward(dq, c64, s64).reshape(T, -1)) < 1e-2
     assert rel(got[:, Hq * hd:(Hq + Hkv) * hd], oracle.rope_backward(dk, c64, s64).reshape(T, -1)) < 1e-2
+    o_ref, _ = oracle.causal_gqa_attention(q, k, v)
+    _, _, dv = oracle.causal_gqa_attention_backward(do.to(D).reshape(B, S, Hq, hd), q, k, v, probs)
+    _attention_elementwise(o.cpu().to(D), got, q, k, v, do.to(D).reshape(B, S, Hq, hd), o_ref, dq, dk, dv,
+                           rope=(c64, s64))
 
 
 def test_attention_backward_deterministic():
@@ -256,6 +326,11 @@ def test_rmsnorm_vs_oracle(rows, d):
     assert rel(rstd, rr.reshape(-1)) < 1e-6
     assert rel(dx, dxr + dres.to(D)) < 4e-3
     assert rel(dg, dgr) < 4e-3
+    assert float(((rstd.cpu().to(D) - rr.reshape(-1)) / rr.reshape(-1)).abs().max()) < 1e-6
+    bounds.check(y, yr, bounds.rmsnorm_fwd(yr, x, w, rstd.cpu()), "rmsnorm y")
+    bdx, bdg = bounds.rmsnorm_bwd(dxr + dres.to(D), dgr, dy, x, w, rstd.cpu(), dres)
+    bounds.check(dx, dxr + dres.to(D), bdx, "rmsnorm dx")
+    bounds.check(dg, dgr, bdg, "rmsnorm dg")
 
 
 @pytest.mark.parametrize("rows,f", [(256, 688), (300, 5632), (5, 7)])
@@ -268,6 +343,9 @@ def test_swiglu_backward_vs_oracle(rows, f):
     dg, du = oracle.swiglu_backward(da.to(D), gu.to(D)[:, 0::2], gu.to(D)[:, 1::2])
     assert rel(dgu.cpu()[:, 0::2], dg) < 4e-3
     assert rel(dgu.cpu()[:, 1::2], du) < 4e-3
+    bg, bu = bounds.swiglu_bwd(dg, du, da, gu[:, 0::2], gu[:, 1::2])
+    bounds.check(dgu.cpu()[:, 0::2], dg, bg, "swiglu backward dgate")
+    bounds.check(dgu.cpu()[:, 1::2], du, bu, "swiglu backward dup")
 
 
 @pytest.mark.parametrize("rows,V", [(256, 1024), (64, 152064), (10, 40)])
@@ -286,6 +364,7 @@ def test_cross_entropy_vs_oracle(rows, V):
     p = torch.softmax(zd, -1)
     p[torch.arange(rows), y.long()] -= 1
     assert rel(dz, p / rows) < 4e-3
+    bounds.check(dz, p / rows, bounds.cross_entropy_dz(p / rows, z, y, 1.0 / rows), "cross-entropy dz")
     assert int(st.item()) == 0
 
 
@@ -307,6 +386,7 @@ def test_embedding_forward_exact_backward_deterministic_sum():
     assert torch.equal(x.cpu(), E[tok.long()])
     ref = torch.zeros(V, d, dtype=D).index_add_(0, tok.long(), dx.to(D))
     assert rel(dE, ref) < 4e-3
+    bounds.check(dE, ref, bounds.embedding_bwd(ref, tok, dx, V), "embedding backward")
     assert torch.all(dE.cpu()[torch.bincount(tok.long(), minlength=V) == 0] == 0)
     bad = tok.clone()
     bad[3] = V + 5
