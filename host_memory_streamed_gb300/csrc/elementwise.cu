@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <cfloat>
+#include <map>
 #include <mutex>
 
 #include "kernels.h"
@@ -146,8 +147,10 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_bwd_kernel(const bf16* __
 // Backward with the columns held in registers: each thread owns VPT 16-byte
 // vectors (8 columns each) of every row, vector i = threadIdx.x + k*blockDim.x
 // for k < VPT, so the gain and the block's gain-gradient sums for those
-// columns stay in registers for all of the block's rows.  The block's
-// kRmsRowsPerBlock rows go two at a time; with PREFETCH (one vector per
+// columns stay in registers for all of the block's rows.  The grid is one
+// wave (every block resident at once), each block taking an equal run of
+// rows_per_block >= kRmsRowsPerBlock rows, so no partial wave idles the
+// memory system at the end.  A block's rows go two at a time; with PREFETCH (one vector per
 // thread, where the registers allow it) the next pair's dy, x and dres
 // vectors are requested before the current pair is reduced, so loads stay in
 // flight while the block waits on its reduction barrier.  The
@@ -189,7 +192,7 @@ template <int VPT, bool PREFETCH>
 __global__ void __launch_bounds__(VPT == 1 ? 640 : (VPT == 2 ? 384 : 256)) rmsnorm_bwd_rows_kernel(
     const bf16* __restrict__ dy, const bf16* __restrict__ x, const bf16* __restrict__ g,
     const float* __restrict__ rstd, const bf16* __restrict__ dres, bf16* __restrict__ dx,
-    float* __restrict__ dg_partial, long rows, int d) {
+    float* __restrict__ dg_partial, long rows, int d, long rows_per_block) {
   __shared__ float red[2][2][32];  // [buffer][row of the pair][warp]
   const int nv = d / 8;
   const int nthreads = blockDim.x;
@@ -208,8 +211,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 640 : (VPT == 2 ? 384 : 256)) rmsno
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
   }
-  const long r0 = (long)blockIdx.x * kRmsRowsPerBlock;
-  const long r1 = min(rows, r0 + kRmsRowsPerBlock);
+  const long r0 = (long)blockIdx.x * rows_per_block;
+  const long r1 = min(rows, r0 + rows_per_block);
   auto pair_rows = [&](long row) { return row >= r1 ? 0 : (row + 1 < r1 ? 2 : 1); };
   RmsPair<VPT> cur, nxt;
   if (PREFETCH) rms_load_pair<VPT>(cur, dy, x, rstd, dres, r0, pair_rows(r0), nv);
@@ -606,24 +609,56 @@ long rmsnorm_bwd_max_d() {
   return maxd;
 }
 
-void launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
-                        bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s) {
-  if (rows <= 0) return;
-  const unsigned nb = blocks_for(rows, kRmsRowsPerBlock);
+namespace {
+// Blocks of a register-kernel variant, at a given block size, that fit on the
+// device at once (0 when the device cannot say).
+template <int VPT, bool PF>
+int resident_rows_blocks(int threads) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find(threads);
+  if (it != cache.end()) return it->second;
+  int dev = 0, sms = 0, per = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, rmsnorm_bwd_rows_kernel<VPT, PF>, threads, 0) !=
+          cudaSuccess)
+    sms = per = 0;
+  return cache[threads] = sms * per;
+}
+
+template <int VPT, bool PF>
+long launch_rows_variant(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres, bf16* dx,
+                         float* dg_partial, long rows, int d, cudaStream_t s) {
   const int nv = d / 8;
-  auto threads = [&](int vpt) { return (int)((nv + vpt * 32 - 1) / (vpt * 32) * 32); };
-  if (nv <= 640) {
-    rmsnorm_bwd_rows_kernel<1, true><<<nb, threads(1), 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
-  } else if (nv <= 768) {
-    rmsnorm_bwd_rows_kernel<2, false><<<nb, threads(2), 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
-  } else if (nv <= kRmsBwdRegMaxVectors) {
-    rmsnorm_bwd_rows_kernel<4, false><<<nb, threads(4), 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
-  } else {
-    const size_t shm = (size_t)d * sizeof(float);
-    if (shm > 48 * 1024)
-      cudaFuncSetAttribute(rmsnorm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
-    rmsnorm_bwd_kernel<<<nb, RMS_THREADS, shm, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
-  }
+  const int threads = (nv + VPT * 32 - 1) / (VPT * 32) * 32;
+  // one block per kRmsRowsPerBlock rows at most (the scratch the callers size),
+  // and no more blocks than are resident at once at this block size
+  long nb = (rows + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock;
+  const int wave = resident_rows_blocks<VPT, PF>(threads);
+  if (wave > 0 && nb > wave) nb = wave;
+  const long rpb = (rows + nb - 1) / nb;
+  nb = (rows + rpb - 1) / rpb;
+  rmsnorm_bwd_rows_kernel<VPT, PF><<<(unsigned)nb, threads, 0, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d,
+                                                                     rpb);
+  return nb;
+}
+}  // namespace
+
+long launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
+                        bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s) {
+  if (rows <= 0) return 0;
+  const int nv = d / 8;
+  if (nv <= 640) return launch_rows_variant<1, true>(dy, x, g, rstd, dres, dx, dg_partial, rows, d, s);
+  if (nv <= 768) return launch_rows_variant<2, false>(dy, x, g, rstd, dres, dx, dg_partial, rows, d, s);
+  if (nv <= kRmsBwdRegMaxVectors)
+    return launch_rows_variant<4, false>(dy, x, g, rstd, dres, dx, dg_partial, rows, d, s);
+  const unsigned nb = blocks_for(rows, kRmsRowsPerBlock);
+  const size_t shm = (size_t)d * sizeof(float);
+  if (shm > 48 * 1024) cudaFuncSetAttribute(rmsnorm_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shm);
+  rmsnorm_bwd_kernel<<<nb, RMS_THREADS, shm, s>>>(dy, x, g, rstd, dres, dx, dg_partial, rows, d);
+  return nb;
 }
 
 void launch_colsum_bf16(const float* partial, long nparts, int d, bf16* out, cudaStream_t s) {

@@ -118,10 +118,11 @@ int launch_attn_bwd(const AttnArgs& a, cudaStream_t stream);
 void launch_rmsnorm_fwd(const bf16* x, const bf16* g, bf16* y, float* rstd, long rows, int d, float eps,
                         cudaStream_t s);
 // dx = dres + rstd * (dy*g - xhat * mean(dy*g*xhat)), xhat = x*rstd.
-// dg_partial[blk, d] = sum over the rows of block blk of dy * xhat
-// (blocks of kRmsRowsPerBlock rows); reduce with launch_colsum_bf16.
+// dg_partial[blk, d] = sum over the rows of block blk of dy * xhat; returns
+// the number of blocks (partial rows), at most ceil(rows / kRmsRowsPerBlock)
+// (the scratch callers provide); reduce them with launch_colsum_bf16.
 constexpr int kRmsRowsPerBlock = 64;
-void launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
+long launch_rmsnorm_bwd(const bf16* dy, const bf16* x, const bf16* g, const float* rstd, const bf16* dres,
                         bf16* dx, float* dg_partial, long rows, int d, cudaStream_t s);
 // Largest d the backward launches on this device (its shared-memory plan for
 // d > 8192 keeps d floats per block).

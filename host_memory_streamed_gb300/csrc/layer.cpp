@@ -279,9 +279,11 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   dgrad(W.dgu, 2 * D.f, w.wgu, D.d, W.dn);
   }
   // dh = dx_out + RMSNorm2^T dn2 ; dg2
-  launch_rmsnorm_bwd(W.dn, a.h, w.g2, a.rstd2, dx_out, W.dh, W.dg_partial, T, D.d, s);
-  trace("rmsnorm_bwd");
-  launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g2, s);
+  {
+    const long parts = launch_rmsnorm_bwd(W.dn, a.h, w.g2, a.rstd2, dx_out, W.dh, W.dg_partial, T, D.d, s);
+    trace("rmsnorm_bwd");
+    launch_colsum_bf16(W.dg_partial, parts, D.d, gv.g2, s);
+  }
   // h = x + o Wo^T
   wgrad(W.dh, D.d, a.o, D.Dq, gv.wo);
   dgrad(W.dh, D.d, w.wo, D.Dq, W.dout);
@@ -306,9 +308,11 @@ int LayerTemplate::backward(const LayerView& w, const LayerActs& a, const bf16* 
   trace("attention_bwd");
   wgrad(W.dqkv, D.Dqkv, a.n1, D.d, gv.wqkv);
   dgrad(W.dqkv, D.Dqkv, w.wqkv, D.d, W.dn);
-  launch_rmsnorm_bwd(W.dn, a.x, w.g1, a.rstd1, W.dh, dx_in, W.dg_partial, T, D.d, s);
-  trace("rmsnorm_bwd");
-  launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.g1, s);
+  {
+    const long parts = launch_rmsnorm_bwd(W.dn, a.x, w.g1, a.rstd1, W.dh, dx_in, W.dg_partial, T, D.d, s);
+    trace("rmsnorm_bwd");
+    launch_colsum_bf16(W.dg_partial, parts, D.d, gv.g1, s);
+  }
   stats->kernels += 7;  // 2 x (rmsnorm bwd + colsum), attention delta + dK/dV + dQ
   return rc;
 }
@@ -468,8 +472,10 @@ int LayerTemplate::head(const HeadView& w, const bf16* x_L, bf16* dx_L, const He
   trace("f32_to_bf16");
   launch_mean_loss(W.loss_rows, T, inv_n, W.loss, s);
   trace("mean_loss");
-  launch_rmsnorm_bwd(W.dnf, x_L, w.gf, W.rstd_f, nullptr, dx_L, W.dg_partial, T, D.d, s);
-  launch_colsum_bf16(W.dg_partial, (T + kRmsRowsPerBlock - 1) / kRmsRowsPerBlock, D.d, gv.gf, s);
+  {
+    const long parts = launch_rmsnorm_bwd(W.dnf, x_L, w.gf, W.rstd_f, nullptr, dx_L, W.dg_partial, T, D.d, s);
+    launch_colsum_bf16(W.dg_partial, parts, D.d, gv.gf, s);
+  }
   stats->kernels += 4;
   return rc;
 }

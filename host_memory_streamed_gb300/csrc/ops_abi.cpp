@@ -186,11 +186,11 @@ int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float*
   if (d <= 0 || d % 8 || rows < 0) return op_fail("rmsnorm: d must be a positive multiple of 8 and rows >= 0");
   if (d > mt::rmsnorm_bwd_max_d()) return op_fail("rmsnorm backward: d exceeds the widest row this device takes");
   auto s = static_cast<cudaStream_t>(stream);
-  mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
-                         static_cast<const mt::bf16*>(g), rstd, static_cast<const mt::bf16*>(dres),
-                         static_cast<mt::bf16*>(dx), scratch, rows, d, s);
-  mt::launch_colsum_bf16(scratch, (rows + mt::kRmsRowsPerBlock - 1) / mt::kRmsRowsPerBlock, d,
-                         static_cast<mt::bf16*>(dg), s);
+  const long parts = mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
+                                            static_cast<const mt::bf16*>(g), rstd,
+                                            static_cast<const mt::bf16*>(dres), static_cast<mt::bf16*>(dx), scratch,
+                                            rows, d, s);
+  mt::launch_colsum_bf16(scratch, parts, d, static_cast<mt::bf16*>(dg), s);
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "rmsnorm backward");
 }
 

@@ -87,10 +87,12 @@ extern "C" int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const vo
     return MT_ECUDA;
   }
   auto s = static_cast<cudaStream_t>(stream);
-  mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
-                         static_cast<const mt::bf16*>(g), rstd, static_cast<const mt::bf16*>(dres),
-                         static_cast<mt::bf16*>(dx), scratch, rows, d, s);
-  mt::launch_colsum_bf16(scratch, nparts, d, static_cast<mt::bf16*>(dg), s);
+  // the kernel writes at most nparts partial rows (fewer when its grid is capped at one wave)
+  const long parts = mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
+                                            static_cast<const mt::bf16*>(g), rstd,
+                                            static_cast<const mt::bf16*>(dres), static_cast<mt::bf16*>(dx), scratch,
+                                            rows, d, s);
+  mt::launch_colsum_bf16(scratch, parts, d, static_cast<mt::bf16*>(dg), s);
   if (cudaPeekAtLastError() != cudaSuccess) {
     mt::set_op_error(std::string("rmsnorm (no-alloc): launch failed: ") + cudaGetErrorString(cudaGetLastError()));
     return MT_ECUDA;

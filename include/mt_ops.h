@@ -138,7 +138,7 @@ int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_
 int64_t mt_op_rmsnorm_bwd_scratch_floats(int64_t rows, int32_t d);
 /*
  * dx = dres + d(rmsnorm)/dx^T dy (dres may be NULL); dg [d] BF16 = sum over rows
- * of dy * x * rstd, reduced in a fixed order (per 64-row block, then over the
+ * of dy * x * rstd, reduced in a fixed order (per block of rows, then over the
  * blocks).  d % 8 == 0; rows wider than 8192 keep d floats in shared memory per
  * block, so d beyond what the device's shared memory holds (about 58K on this
  * part) returns MT_EINVAL.
