@@ -231,47 +231,28 @@ def _intersect(u, w):
     return tot
 
 
-def traced_overlap(model, toks, device):
-    """Copy/compute overlap from a device timeline of whole steps.
+def timeline_overlap(tl):
+    """Copy/compute overlap of one step from its device timeline.
 
-    The steps run under torch.profiler's CUDA activity tracing (CUPTI), which
-    records every kernel and every memcpy of the process with device start and
-    end times, the library's included.  overlap = |(H2D u D2H) n kernels| /
-    |H2D u D2H| over the union of the intervals; the H2D and D2H streams are
-    also reported on their own."""
-    import tempfile
-    from torch.profiler import ProfilerActivity, profile
-    torch.cuda.synchronize(device)
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        for t in toks:
-            model.train_step(t)
-        torch.cuda.synchronize(device)
-    with tempfile.TemporaryDirectory() as d:
-        path = os.path.join(d, "trace.json")
-        prof.export_chrome_trace(path)
-        with open(path) as f:
-            ev = json.load(f).get("traceEvents", [])
-    kern, h2d, d2h = [], [], []
-    for e in ev:
-        if e.get("ph") != "X" or "dur" not in e:
-            continue
-        iv = (float(e["ts"]), float(e["ts"]) + float(e["dur"]))
-        cat, name = e.get("cat", ""), e.get("name", "")
-        if cat == "kernel":
-            kern.append(iv)
-        elif cat == "gpu_memcpy" and "HtoD" in name:
-            h2d.append(iv)
-        elif cat == "gpu_memcpy" and "DtoH" in name:
-            d2h.append(iv)
-    K, H, G = _union(kern), _union(h2d), _union(d2h)
-    C = _union(h2d + d2h)
-    tc = _measure(C)
-    return {"method": "torch.profiler CUDA activity (CUPTI) device timeline; |(H2D u D2H) n kernels| / |H2D u D2H|",
-            "steps": len(toks), "kernels": len(kern), "h2d_copies": len(h2d), "d2h_copies": len(d2h),
-            "copy_ms": tc / 1e3, "kernel_ms": _measure(K) / 1e3,
-            "overlap": _intersect(C, K) / tc if tc else None,
-            "h2d_overlap": _intersect(H, K) / _measure(H) if H else None,
-            "d2h_overlap": _intersect(G, K) / _measure(G) if G else None}
+    tl: (kind, visit, t0_ms, t1_ms) spans from mt_get_timeline -- each visit's
+    compute-stream span and every chunk copy on the H2D and D2H streams, timed
+    by CUDA events around each copy.  overlap = |(H2D u D2H) n compute| /
+    |H2D u D2H| over the unions of the spans; each direction is also reported
+    on its own."""
+    from host_memory_streamed_gb300 import _lib
+    comp = _union([(a, b) for k, _, a, b in tl if k == _lib.SPAN_COMPUTE])
+    h2d = _union([(a, b) for k, _, a, b in tl if k == _lib.SPAN_H2D])
+    d2h = _union([(a, b) for k, _, a, b in tl if k == _lib.SPAN_D2H])
+    cp = _union(h2d + d2h)
+    tc = _measure(cp)
+    return {"method": "device timeline (CUDA events around every chunk copy and every visit's compute span); "
+                      "|(H2D u D2H) n compute| / |H2D u D2H|",
+            "h2d_chunks": sum(1 for k, *_ in tl if k == _lib.SPAN_H2D),
+            "d2h_chunks": sum(1 for k, *_ in tl if k == _lib.SPAN_D2H),
+            "copy_ms": tc, "compute_ms": _measure(comp),
+            "overlap": _intersect(cp, comp) / tc if tc else None,
+            "h2d_overlap": _intersect(h2d, comp) / _measure(h2d) if h2d else None,
+            "d2h_overlap": _intersect(d2h, comp) / _measure(d2h) if d2h else None}
 
 
 def load_synthetic_weights(model, s, device):
@@ -402,10 +383,16 @@ def main():
                     help="layers whose internals stay on the device from forward to backward: a number, 'auto' "
                          "(as many as fit) or 'preset' (auto where the workload fixes no checkpoint interval, "
                          "else 0)")
+    ap.add_argument("--sync-adam", action="store_true",
+                    help="each step waits for all of its Adam updates (default: they finish during the next "
+                         "step, each before its tile is uploaded; the timed regions wait for all of them)")
+    ap.add_argument("--slab-grads", action="store_true",
+                    help="gradients through the pinned slabs and the accumulator's copy (default: straight into "
+                         "the page-locked G sections of the tiles)")
+    ap.add_argument("--no-double-buffer", action="store_true",
+                    help="ablation: one device weight buffer, so no upload overlaps compute")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-trace-overlap", action="store_true",
-                    help="skip the two extra steps traced for the copy/compute overlap")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -451,11 +438,13 @@ def main():
         keep = int(keep)
     if chunk:
         keep = 0  # a chunked MLP keeps no per-layer activations
-    model = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS, device=device, mlp_chunk_rows=chunk,
+    flags = hms.MT_TIME_KERNELS | (hms.MT_NO_DOUBLE_BUFFER if args.no_double_buffer else 0) | \
+        (0 if args.sync_adam else hms.MT_ASYNC_ADAM) | (0 if args.slab_grads else hms.MT_DIRECT_GRADS)
+    model = hms.StreamedDecoder.from_shape(s, flags=flags, device=device, mlp_chunk_rows=chunk,
                                            n_adam_threads=adam_threads, keep_layers=keep)
     load_synthetic_weights(model, s, device)
     init_s = time.perf_counter() - t_init
-    toks = token_batches(s, args.warmup + args.steps + 2, device)
+    toks = token_batches(s, args.warmup + args.steps, device)
     host_toks = [t.cpu().pin_memory() for t in toks]
     s_comp = model.streams[0]
 
@@ -463,6 +452,7 @@ def main():
         model.train_step(toks[i])
     # ---- timed region: device-resident tokens
     stats = []
+    model.sync()  # no Adam work of the warm-up steps inside the timed region
     if pg:
         pg.barrier()
     torch.cuda.synchronize(device)
@@ -473,8 +463,10 @@ def main():
         for i in range(args.steps):
             losses.append(model.train_step(toks[args.warmup + i]))
             stats.append(model.stats())
+        model.sync()  # every Adam update of the timed steps inside the timed region
         e1.record(s_comp)
         torch.cuda.synchronize(device)
+    overlap_tl = timeline_overlap(model.timeline())  # the last timed step
     if pg:
         pg.barrier()
     elapsed = e0.elapsed_time(e1) / 1e3
@@ -494,6 +486,7 @@ def main():
     f0.record(s_comp)
     for i in range(args.steps):
         model.train_step(host_toks[args.warmup + i])
+    model.sync()
     f1.record(s_comp)
     torch.cuda.synchronize(device)
     e2e_elapsed = f0.elapsed_time(f1) / 1e3
@@ -503,12 +496,6 @@ def main():
         e2e_elapsed = float(t[0])
     e2e = world * args.steps * tokens_per_step / e2e_elapsed
     model_keep = model.keep_layers
-    overlap_trace = None
-    if not args.no_trace_overlap and rank == 0:
-        try:
-            overlap_trace = traced_overlap(model, toks[args.warmup + args.steps:], device)
-        except Exception as e:  # the profiler is a measurement aid, not the product
-            overlap_trace = {"error": f"{type(e).__name__}: {e}"}
     model.close()
     del model
 
@@ -537,7 +524,9 @@ def main():
         "config": {"workload": s.name, "layers": s.n_layers, "layers_preset": full_layers, "d_model": s.d_model,
                    "heads": f"{s.n_heads}q/{s.n_kv_heads}kv x {s.head_dim}", "ffn": s.ffn, "vocab": s.vocab,
                    "batch": s.batch, "seq": s.seq, "ckpt_every": s.ckpt_every,
-                   "keep_layers": model_keep,
+                   "keep_layers": model_keep, "double_buffer": not args.no_double_buffer,
+                   "adam": "sync" if args.sync_adam else "async (finished inside the timed region)",
+                   "grads": "pinned slabs + accumulator copy" if args.slab_grads else "direct into page-locked G",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (weights streamed per layer, activations > 129 MB)",
                    "mlp_chunk_rows": chunk or None,
@@ -559,7 +548,7 @@ def main():
                     stall_ms / args.steps,
                     "hidden_frac": (1.0 - stall_ms / copy_ms) if copy_ms else None,
                     "method": "CUDA events: copy windows on the H2D/D2H streams vs compute-stream waits",
-                    "traced": overlap_trace},
+                    "timeline": overlap_tl},
         "roofline": {"bound": "tensor", "kernel": "gemm_bf16_tcgen05", "achieved": achieved, "peak": p_sust,
                      "unit": "TFLOP/s", "frac": (achieved / p_sust) if achieved else None,
                      "traffic": gemm_traffic_per_launch() if s.name == "14b" else None,

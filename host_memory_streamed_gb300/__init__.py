@@ -13,13 +13,13 @@ import ctypes as C
 import torch
 
 from . import _lib
-from ._lib import (MT_DEBUG_CHECKS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V, MT_PART_W,
-                   MT_RESIDENT, MT_STORE_ACTS, MT_TIE_EMBEDDINGS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG,
+from ._lib import (MT_ASYNC_ADAM, MT_DEBUG_CHECKS, MT_DIRECT_GRADS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V,
+                   MT_PART_W, MT_RESIDENT, MT_STORE_ACTS, MT_TIE_EMBEDDINGS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG,
                    ERROR_NAMES)
 
 __all__ = ["StreamedDecoder", "MtError", "ops", "plan_schedule", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
            "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_VISIT_LOG", "MT_TIE_EMBEDDINGS", "MT_PART_W",
-           "MT_PART_G", "MT_PART_M", "MT_PART_V"]
+           "MT_PART_G", "MT_PART_M", "MT_PART_V", "MT_ASYNC_ADAM", "MT_DIRECT_GRADS"]
 
 LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
 
@@ -335,6 +335,20 @@ class StreamedDecoder:
         p = lambda t: None if t is None else t.data_ptr()
         torch.cuda.current_stream(self.device).synchronize()
         self._check(self._L.mt_layer_pass(self._h, int(layer), p(x_in), p(dx_out), p(x_out), p(dx_in)))
+
+    def timeline(self) -> list[tuple[int, int, float, float]]:
+        """(kind, visit, t0_ms, t1_ms) spans of the last step (``mt_get_timeline``;
+        MT_TIME_KERNELS): compute per visit, H2D and D2H per chunk copy."""
+        n = self._L.mt_get_timeline(self._h, None, 0)
+        if n < 0:
+            raise MtError(int(n), "mt_get_timeline failed")
+        out = (_lib.MtInterval * max(1, n))()
+        n = self._L.mt_get_timeline(self._h, out, n)
+        return [(out[i].kind, out[i].visit, out[i].t0_ms, out[i].t1_ms) for i in range(n)]
+
+    def sync(self):
+        """Wait for every pending Adam update (``mt_sync``; MT_ASYNC_ADAM)."""
+        self._check(self._L.mt_sync(self._h))
 
     def stats(self) -> dict:
         st = _lib.MtStepStats()

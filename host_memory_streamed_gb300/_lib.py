@@ -15,7 +15,7 @@ ERROR_NAMES = {0: "MT_OK", -1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_ECUDA", -4:
                -5: "MT_ESTATE", -6: "MT_ENONFINITE", -7: "MT_EINTERNAL"}
 
 MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG, \
-    MT_TIE_EMBEDDINGS = 1, 2, 4, 8, 16, 32, 64, 128
+    MT_TIE_EMBEDDINGS, MT_ASYNC_ADAM, MT_DIRECT_GRADS = 1, 2, 4, 8, 16, 32, 64, 128, 256, 512
 MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
 EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE, EPI_SWIGLU_BWD = range(7)
@@ -46,6 +46,13 @@ class MtTensorDesc(C.Structure):
 class MtTileDesc(C.Structure):
     _fields_ = [("kind", C.c_int32), ("n_tensors", C.c_int32), ("n_params", C.c_int64),
                 ("w_bytes", C.c_int64), ("tile_bytes", C.c_int64), ("tensors", MtTensorDesc * 8)]
+
+
+class MtInterval(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("visit", C.c_int32), ("t0_ms", C.c_double), ("t1_ms", C.c_double)]
+
+
+SPAN_COMPUTE, SPAN_H2D, SPAN_D2H = 0, 1, 2
 
 
 class MtVisit(C.Structure):
@@ -105,6 +112,8 @@ def lib():
         "mt_get_step_stats": (C.c_int, [vp, C.POINTER(MtStepStats)]),
         "mt_get_step": (i64, [vp]),
         "mt_set_step": (C.c_int, [vp, i64]),
+        "mt_sync": (C.c_int, [vp]),
+        "mt_get_timeline": (i64, [vp, C.POINTER(MtInterval), i64]),
         "mt_last_error": (C.c_char_p, [vp]),
         "mt_free": (None, [vp]),
         "mt_adam_host": (C.c_int, [vp, vp, vp, vp, sz, i64, f32, f32, f32, f32, f32]),
@@ -133,6 +142,7 @@ def lib():
         "mt_op_moe_combine_bwd": (C.c_int, [vp, vp, vp, vp, i64, i32, i32, vp, vp, vp]),
         "mt_op_moe_gate_bwd": (C.c_int, [vp, vp, vp, i64, i32, i32, vp, vp]),
         "mt_op_moe_scatter_bwd": (C.c_int, [vp, vp, i64, i32, i32, vp, vp, vp]),
+        "mt_op_flag_nonfinite": (C.c_int, [vp, i64, vp, vp]),
         "mt_op_rmsnorm_bwd_noalloc": (C.c_int, [vp, vp, vp, vp, vp, vp, vp, i64, i32, vp]),
     }
     for name, (res, args) in sig.items():

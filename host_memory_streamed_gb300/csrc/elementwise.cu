@@ -570,6 +570,25 @@ __global__ void check_finite_kernel(const bf16* __restrict__ p, long n, int* sta
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x % 32) == 0) set_status(status, kStatusNonFinite);
 }
 
+// *flag = 1 when any of the n BF16 values holds NaN or Inf (exponent bits all
+// ones); 16-byte loads, grid-strided.  Every writer stores the same value.
+__global__ void flag_nonfinite_kernel(const bf16* __restrict__ p, long n, int* flag) {
+  const long nvec = n / 8;
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+  bool bad = false;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (long)gridDim.x * blockDim.x) {
+    const uint4 q = v[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      bad |= ((w[k] & 0x7F80u) == 0x7F80u) | ((w[k] & 0x7F800000u) == 0x7F800000u);
+  }
+  if (blockIdx.x == 0)
+    for (long i = nvec * 8 + threadIdx.x; i < n; i += blockDim.x)
+      bad |= (reinterpret_cast<const unsigned short*>(p)[i] & 0x7F80u) == 0x7F80u;
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x % 32) == 0) *flag = 1;
+}
+
 inline unsigned blocks_for(long n, int per) { return (unsigned)((n + per - 1) / per); }
 
 // Failure-detection probe (see launch_wait_probe): the barrier expects one
@@ -722,6 +741,13 @@ void launch_check_finite(const bf16* p, long n, int* status, cudaStream_t s) {
   unsigned nb = blocks_for(n, 256);
   if (nb > 152u * 16u) nb = 152u * 16u;
   check_finite_kernel<<<nb, 256, 0, s>>>(p, n, status);
+}
+
+void launch_flag_nonfinite(const bf16* p, long n, int* flag, cudaStream_t s) {
+  if (n <= 0) return;
+  unsigned nb = blocks_for((n + 7) / 8, 256);
+  if (nb > 152u * 8u) nb = 152u * 8u;
+  flag_nonfinite_kernel<<<nb, 256, 0, s>>>(p, n, flag);
 }
 
 int launch_wait_probe(int* status, uint64_t limit_ns, cudaStream_t s) {

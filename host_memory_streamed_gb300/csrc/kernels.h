@@ -152,6 +152,8 @@ void launch_f32_to_bf16(const float* src, bf16* dst, long n, cudaStream_t s);
 void launch_zero(void* p, size_t bytes, cudaStream_t s);
 // status |= kStatusNonFinite when any of the n BF16 values is NaN or Inf.
 void launch_check_finite(const bf16* p, long n, int* status, cudaStream_t s);
+// *flag = 1 if any of the n values is NaN or Inf (p 16-byte aligned).
+void launch_flag_nonfinite(const bf16* p, long n, int* flag, cudaStream_t s);
 
 // ----------------------------------------------------------------- mixture of experts (moe.cu)
 // N tokens, E experts (<= 256), top k (<= 8), pairs p = n*k + j, P = N*k.

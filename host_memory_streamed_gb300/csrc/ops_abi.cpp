@@ -194,6 +194,13 @@ int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float*
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "rmsnorm backward");
 }
 
+int mt_op_flag_nonfinite(const void* p, int64_t n, int32_t* flag, void* stream) {
+  if (n < 0 || !flag || (n > 0 && (!p || (reinterpret_cast<uintptr_t>(p) & 15))))
+    return op_fail("flag_nonfinite: n >= 0, a flag and a 16-byte aligned p are required");
+  mt::launch_flag_nonfinite(static_cast<const mt::bf16*>(p), n, flag, static_cast<cudaStream_t>(stream));
+  return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "flag_nonfinite");
+}
+
 int mt_op_swiglu_bwd(const void* da, const void* gu, void* dgu, int64_t rows, int32_t f, void* stream) {
   if (f <= 0) return op_fail("swiglu: f must be positive");
   mt::launch_swiglu_bwd(static_cast<const mt::bf16*>(da), static_cast<const mt::bf16*>(gu),

@@ -38,6 +38,7 @@
 #include <cstring>
 #include <deque>
 #include <functional>
+#include <map>
 #include <memory>
 #include <mutex>
 #include <string>
@@ -103,10 +104,12 @@ class Pool {
     cv_.notify_all();
     for (auto& t : th_) t.join();
   }
-  void submit(std::function<void()> f) {
+  // Tasks run in ascending key order (equal keys in submission order).
+  void submit(std::function<void()> f, int key = 0) {
     {
       std::lock_guard<std::mutex> g(mu_);
-      q_.push_back(std::move(f));
+      q_[key].push_back(std::move(f));
+      ++queued_;
       ++pending_;
     }
     cv_.notify_one();
@@ -124,10 +127,13 @@ class Pool {
       std::function<void()> f;
       {
         std::unique_lock<std::mutex> g(mu_);
-        cv_.wait(g, [this] { return stop_ || !q_.empty(); });
-        if (stop_ && q_.empty()) return;
-        f = std::move(q_.front());
-        q_.pop_front();
+        cv_.wait(g, [this] { return stop_ || queued_ > 0; });
+        if (stop_ && queued_ == 0) return;
+        auto it = q_.begin();
+        f = std::move(it->second.front());
+        it->second.pop_front();
+        if (it->second.empty()) q_.erase(it);
+        --queued_;
       }
       f();
       {
@@ -137,10 +143,10 @@ class Pool {
     }
   }
   std::vector<std::thread> th_;
-  std::deque<std::function<void()>> q_;
+  std::map<int, std::deque<std::function<void()>>> q_;
   std::mutex mu_;
   std::condition_variable cv_, done_cv_;
-  int64_t pending_ = 0;
+  int64_t pending_ = 0, queued_ = 0;
   bool stop_ = false;
 };
 
@@ -350,6 +356,7 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
   w.rope_cos = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
   w.rope_sin = reinterpret_cast<float*>(at((int64_t)D.S * (D.hd / 2) * 4));
   w.status = reinterpret_cast<int*>(at(256));
+  w.grad_flags = reinterpret_cast<int*>(at((3LL * D.L + 8) * 4));  // more than the visits of any schedule
   w.head_chunk = hc;
   if (D.E) {
     const int64_t P = T * (int64_t)D.k, R = moe_rows_capacity(P, D.E, kMoeRowAlign);
@@ -428,6 +435,11 @@ struct mt_model {
   cudaEvent_t ev_stage[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> ev_slab;
   cudaEvent_t ev_t0 = nullptr, ev_t1 = nullptr;
+  // MT_TIME_KERNELS timeline: an event pair around every H2D and D2H chunk copy
+  std::vector<cudaEvent_t> tl_h2d, tl_d2h;
+  std::vector<int> tl_h2d_visit, tl_d2h_visit;
+  int tl_h2d_n = 0;
+  std::atomic<int> tl_d2h_n{0};
 
   // host handshakes
   std::mutex mu;
@@ -453,11 +465,25 @@ struct mt_model {
     int64_t off, bytes;
     bool last;
     bool rows;  // compact embedding gradient: the slab holds whole rows of emb_rows, from row off / (2 d)
+    bool direct;  // MT_DIRECT_GRADS: the chunk was copied straight into the tile's G (slab memory unused)
   };
   std::deque<AccJob> acc_q;
   std::vector<int> free_slabs;
   int acc_tiles_done = 0;
   std::atomic<int64_t> adam_us{0};
+  // Adam tasks not yet finished, per tile (MT_ASYNC_ADAM: a step may return
+  // with some pending; a tile's are waited for before it is uploaded or read)
+  bool async_adam = false;
+  // MT_DIRECT_GRADS: the tiles' G sections are page-locked and gradient
+  // chunks land in them directly; a device check flags non-finite values of
+  // each gradient visit (grad_flags, copied to pinned_flags before the chunks)
+  bool direct_grads = false;
+  std::vector<int> g_registered;
+  int* grad_flags = nullptr;     // device [visits]
+  int* pinned_flags = nullptr;   // host, pinned [visits]
+  std::mutex adam_mu;
+  std::condition_variable adam_cv;
+  std::vector<int> adam_pending;
   std::chrono::steady_clock::time_point last_grads_landed;
 
   // stats
@@ -569,6 +595,57 @@ void pack_copy(mt_model* m, uint8_t* dst, const uint8_t* src, int64_t n) {
   if (!m->pack_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "packer copy timed out"};
 }
 
+// Every Adam task goes through here: counted per tile, queued with the tile
+// index as its priority (the next step uploads tiles in index order, so the
+// tile needed first is updated first).
+void submit_adam_task(mt_model* m, int tile, std::function<void()> fn) {
+  {
+    std::lock_guard<std::mutex> g(m->adam_mu);
+    ++m->adam_pending[tile];
+  }
+  m->adam_pool->submit(
+      [m, tile, fn = std::move(fn)] {
+        NvtxRange range("adam (tile %d)", tile);
+        fn();
+        std::lock_guard<std::mutex> g(m->adam_mu);
+        if (--m->adam_pending[tile] == 0) m->adam_cv.notify_all();
+      },
+      tile);
+}
+
+// Bounded wait until tile `tile` has no Adam task pending (all tiles: -1).
+void wait_adam(mt_model* m, int tile) {
+  std::unique_lock<std::mutex> g(m->adam_mu);
+  auto idle = [&] {
+    if (tile >= 0) return m->adam_pending[tile] == 0;
+    for (int c : m->adam_pending)
+      if (c) return false;
+    return true;
+  };
+  if (!m->adam_cv.wait_for(g, std::chrono::milliseconds(m->cfg.timeout_ms), idle))
+    throw MtError{MT_ETIMEDOUT, "timed out waiting for the Adam update of tile " + std::to_string(tile)};
+}
+
+// Entry points that read or overwrite tiles wait for their pending Adam
+// tasks (tile, or -1 for all).  A failure of a task that ran after its step
+// returned is reported by the next waiting call that can fail.
+int settle_adam(mt_model* m, int tile, bool report_failure) {
+  if (!m->async_adam) return MT_OK;
+  try {
+    wait_adam(m, tile);
+  } catch (const MtError& e) {
+    m->err = e.msg;
+    m->broken = true;
+    return e.code;
+  }
+  if (report_failure && m->abort_flag && m->worker_code) {
+    m->err = "an Adam update that ran after its step returned failed: " + m->worker_msg;
+    m->broken = true;
+    return m->worker_code;
+  }
+  return MT_OK;
+}
+
 // ------------------------------------------------------------------ loader (H2D stream)
 void loader_main(mt_model* m) {
   cudaSetDevice(m->device);
@@ -599,6 +676,7 @@ void loader_main(mt_model* m) {
           wait_flag(m, m->rec_free, x.prev_user, "buffer free");
           MT_CK(cudaStreamWaitEvent(m->s_h2d, m->ev_free[x.prev_user], 0));
         }
+        if (m->async_adam) wait_adam(m, x.tile);  // the previous step's update of this tile
         MT_CK(cudaEventRecord(m->ev_h2d_a[v], m->s_h2d));
         const TileLayout& lay = m->layouts[x.tile];
         const uint8_t* src = m->tiles[x.tile] + lay.off_w;
@@ -609,7 +687,13 @@ void loader_main(mt_model* m) {
           const int k = si++ & 1;
           wait_event(m, m->ev_stage[k], "pinned staging buffer");
           pack_copy(m, m->stage[k], src + off, c);
+          const int tl = m->time_kernels && 2 * m->tl_h2d_n + 1 < (int)m->tl_h2d.size() ? m->tl_h2d_n++ : -1;
+          if (tl >= 0) {
+            m->tl_h2d_visit[tl] = v;
+            MT_CK(cudaEventRecord(m->tl_h2d[2 * tl], m->s_h2d));
+          }
           MT_CK(cudaMemcpyAsync(dst + off, m->stage[k], (size_t)c, cudaMemcpyHostToDevice, m->s_h2d));
+          if (tl >= 0) MT_CK(cudaEventRecord(m->tl_h2d[2 * tl + 1], m->s_h2d));
           MT_CK(cudaEventRecord(m->ev_stage[k], m->s_h2d));
         }
         MT_CK(cudaEventRecord(m->ev_h2d_b[v], m->s_h2d));
@@ -661,14 +745,32 @@ void d2h_main(mt_model* m) {
       const int64_t row_b = 2LL * m->D.d;
       const int64_t n = rows ? (int64_t)m->emb_u * row_b : lay.w_bytes;
       const int64_t chunk = rows ? m->slab_bytes / row_b * row_b : m->slab_bytes;
+      // Direct landing (first pass of a step): the chunks go into the tile's
+      // page-locked G and the slab is only a token bounding the chunks in
+      // flight; the visit's device non-finite flag travels first.
+      const bool direct = m->direct_grads && !rows && m->micro_index == 0;
+      uint8_t* gdst = m->tiles[x.tile] + lay.off_g;
+      if (direct)
+        MT_CK(cudaMemcpyAsync(m->pinned_flags + v, m->grad_flags + v, sizeof(int), cudaMemcpyDeviceToHost, m->s_d2h));
       for (int64_t off = 0; off < n; off += chunk) {
         const int64_t c = std::min(chunk, n - off);
         const int s = acquire_slab(m);
-        MT_CK(cudaMemcpyAsync(m->slabs[s], src + off, (size_t)c, cudaMemcpyDeviceToHost, m->s_d2h));
+        int tl = -1;
+        if (m->time_kernels) {
+          tl = m->tl_d2h_n++;
+          if (2 * tl + 1 >= (int)m->tl_d2h.size()) tl = -1;
+        }
+        if (tl >= 0) {
+          m->tl_d2h_visit[tl] = v;
+          MT_CK(cudaEventRecord(m->tl_d2h[2 * tl], m->s_d2h));
+        }
+        MT_CK(cudaMemcpyAsync(direct ? gdst + off : m->slabs[s], src + off, (size_t)c, cudaMemcpyDeviceToHost,
+                              m->s_d2h));
+        if (tl >= 0) MT_CK(cudaEventRecord(m->tl_d2h[2 * tl + 1], m->s_d2h));
         MT_CK(cudaEventRecord(m->ev_slab[s], m->s_d2h));
         {
           std::lock_guard<std::mutex> g(m->mu);
-          m->acc_q.push_back({s, v, x.tile, off, c, off + c >= n, rows});
+          m->acc_q.push_back({s, v, x.tile, off, c, off + c >= n, rows, direct});
         }
         m->cv.notify_all();
       }
@@ -703,8 +805,7 @@ void submit_adam_range(mt_model* m, int tile, int64_t g_off, int64_t g_bytes) {
       const uint16_t* g = reinterpret_cast<const uint16_t*>(base + lay.off_g + t.offset) + b;
       float* mm = reinterpret_cast<float*>(base + lay.off_m + 2 * t.offset) + b;
       float* vv = reinterpret_cast<float*>(base + lay.off_v + 2 * t.offset) + b;
-      m->adam_pool->submit([=] {
-        NvtxRange range("adam (tile %d)", tile);
+      submit_adam_task(m, tile, [=] {
         const auto t0 = Clock::now();
         adam_range(w, g, mm, vv, (size_t)c, h);
         m->adam_us += (int64_t)(ms_since(t0) * 1000.0);
@@ -731,7 +832,7 @@ void submit_untouched_embed(mt_model* m) {
   constexpr int kRowsPerTask = 64;
   for (int v0 = 0; v0 < V; v0 += kRowsPerTask) {
     const int v1 = std::min(V, v0 + kRowsPerTask);
-    m->adam_pool->submit([=] {
+    submit_adam_task(m, 0, [=] {
       const auto t0 = Clock::now();
       for (int v = v0; v < v1; ++v) {
         if (off[v + 1] > off[v]) continue;
@@ -764,7 +865,7 @@ void submit_tied_head_adam(mt_model* m) {
   constexpr int kRowsPerTask = 64;
   for (int v0 = 0; v0 < V; v0 += kRowsPerTask) {
     const int v1 = std::min(V, v0 + kRowsPerTask);
-    m->adam_pool->submit([=] {
+    submit_adam_task(m, 0, [=] {
       const auto t0 = Clock::now();
       for (int v = v0; v < v1; ++v) {
         if (off[v + 1] > off[v]) continue;
@@ -817,7 +918,7 @@ void submit_adam_embed_rows(mt_model* m, int tile, int64_t u0, int64_t nrows) {
   const int64_t per = std::max<int64_t>(8, (1 << 18) / d);
   for (int64_t a = 0; a < nrows; a += per) {
     const int64_t b = std::min(nrows, a + per);
-    m->adam_pool->submit([=] {
+    submit_adam_task(m, tile, [=] {
       const auto t0 = Clock::now();
       for (int64_t k = a; k < b; ++k) {
         const int64_t e = (int64_t)rows[u0 + k] * d;
@@ -880,24 +981,29 @@ void accum_main(mt_model* m) {
         continue;
       }
       const TileLayout& lay = m->layouts[j.tile];
-      uint16_t* dst = reinterpret_cast<uint16_t*>(m->tiles[j.tile] + lay.off_g + j.off);
-      const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
-      // the copy (and NaN/Inf scan) of one slab is split over the accumulator pool
-      const int64_t n = j.bytes / 2;
-      const int nt = m->acc_pool->size();
-      const bool add = m->micro_index > 0;
-      const int64_t piece = std::max<int64_t>(1 << 18, align_up((n + nt - 1) / nt, 2048));
-      std::atomic<bool> fin{true};
-      for (int64_t b = 0; b < n; b += piece) {
-        const int64_t c = std::min(piece, n - b);
-        m->acc_pool->submit([=, &fin] {
-          const bool okc = add ? add_grad_check_finite(dst + b, src + b, (size_t)c)
-                               : copy_grad_check_finite(dst + b, src + b, (size_t)c);
-          if (!okc) fin = false;
-        });
+      if (j.direct) {
+        // already in the tile; the device flag (copied before the chunks) says whether it is finite
+        if (m->pinned_flags[j.visit]) m->nonfinite = true;
+      } else {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(m->tiles[j.tile] + lay.off_g + j.off);
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
+        // the copy (and NaN/Inf scan) of one slab is split over the accumulator pool
+        const int64_t n = j.bytes / 2;
+        const int nt = m->acc_pool->size();
+        const bool add = m->micro_index > 0;
+        const int64_t piece = std::max<int64_t>(1 << 18, align_up((n + nt - 1) / nt, 2048));
+        std::atomic<bool> fin{true};
+        for (int64_t b = 0; b < n; b += piece) {
+          const int64_t c = std::min(piece, n - b);
+          m->acc_pool->submit([=, &fin] {
+            const bool okc = add ? add_grad_check_finite(dst + b, src + b, (size_t)c)
+                                 : copy_grad_check_finite(dst + b, src + b, (size_t)c);
+            if (!okc) fin = false;
+          });
+        }
+        if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
+        if (!fin) m->nonfinite = true;
       }
-      if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
-      if (!fin) m->nonfinite = true;
       {
         std::lock_guard<std::mutex> g(m->mu);
         m->free_slabs.push_back(j.slab);
@@ -906,7 +1012,7 @@ void accum_main(mt_model* m) {
       if (!m->nonfinite && m->last_pass()) {
         if (inject_now(m, MT_INJECT_ADAM_FAIL, j.visit)) {
           const int v = j.visit;
-          m->adam_pool->submit([m, v] { worker_fail(m, injected("Adam", v)); });
+          submit_adam_task(m, j.tile, [m, v] { worker_fail(m, injected("Adam", v)); });
         } else if (!(head && m->tied)) {
           submit_adam_range(m, j.tile, j.off, j.bytes);
         } else if (j.last && m->micro_count == 1) {
@@ -1022,6 +1128,13 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       MT_CK(cudaStreamSynchronize(m->s_comp));
       tokens_host = host_tok.data();
     }
+    if (m->async_adam) {
+      // The previous step's embedding Adam reads that step's token tables,
+      // which this step overwrites; and a deferred task that failed fails
+      // this call before the per-step state is reset.
+      wait_adam(m, 0);
+      check_abort(m);
+    }
     // reset per-step state
     {
       std::lock_guard<std::mutex> g(m->mu);
@@ -1037,6 +1150,8 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       m->worker_code = 0;
       m->worker_msg.clear();
       m->acc_tiles_done = 0;
+      m->tl_h2d_n = 0;
+      m->tl_d2h_n = 0;
       m->d2h_q.clear();
       m->acc_q.clear();
     }
@@ -1055,6 +1170,8 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       for (size_t t = 0; t < m->tiles.size(); ++t)
         MT_CK(cudaMemcpyAsync(m->resident + m->resident_off[t], m->tiles[t] + m->layouts[t].off_w,
                               (size_t)m->layouts[t].w_bytes, cudaMemcpyHostToDevice, m->s_comp));
+    if (m->direct_grads)
+      MT_CK(cudaMemsetAsync(m->ws.grad_flags, 0, sizeof(int) * m->visits.size(), m->s_comp));
     MT_CK(cudaEventRecord(m->ev_t0, m->s_comp));
     const auto t_ev0 = Clock::now();
     {
@@ -1185,6 +1302,8 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
           launch_check_finite(reinterpret_cast<bf16*>(gb),
                               x.kind == kEmbedBwd ? (int64_t)m->emb_u * D.d : lay.w_bytes / 2, m->ws.status,
                               m->s_comp);
+        if (m->direct_grads && x.kind != kEmbedBwd && m->micro_index == 0)
+          launch_flag_nonfinite(reinterpret_cast<bf16*>(gb), lay.w_bytes / 2, m->grad_flags + v, m->s_comp);
         MT_CK(cudaEventRecord(m->ev_grads[v], m->s_comp));
         {
           std::lock_guard<std::mutex> g(m->mu);
@@ -1209,7 +1328,10 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       if (!ok) throw MtError{MT_ETIMEDOUT, "timed out waiting for gradient accumulation"};
     }
     const auto t_grads_done = Clock::now();
-    if (!m->adam_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "timed out waiting for Adam"};
+    // MT_ASYNC_ADAM: the step returns with Adam tasks still running; each
+    // tile's finish before it is uploaded again or read through the API
+    if (!m->async_adam && !m->adam_pool->wait_idle(m->cfg.timeout_ms))
+      throw MtError{MT_ETIMEDOUT, "timed out waiting for Adam"};
     const auto adam_end = Clock::now();
     check_abort(m);
     MT_CK(cudaStreamSynchronize(m->s_h2d));
@@ -1476,7 +1598,8 @@ void destroy(mt_model* m) {
     // work may still be running against the pinned buffers: leak them rather than free memory in use
     std::fprintf(stderr, "mt_free: streams still busy after %lld ms; pinned buffers are leaked\n",
                  (long long)m->cfg.timeout_ms);
-    for (auto t : m->tiles) std::free(t);
+    for (size_t t = 0; t < m->tiles.size(); ++t)  // page-locked gradient sections are leaked with them
+      if (t >= m->g_registered.size() || !m->g_registered[t]) std::free(m->tiles[t]);
     delete m;
     return;
   }
@@ -1499,6 +1622,8 @@ void destroy(mt_model* m) {
   kill(m->ev_vis_b);
   kill(m->ev_slab);
   kill(m->gemm_events);
+  kill(m->tl_h2d);
+  kill(m->tl_d2h);
   for (auto& e : m->ev_stage)
     if (e) cudaEventDestroy(e);
   if (m->ev_t0) cudaEventDestroy(m->ev_t0);
@@ -1509,6 +1634,9 @@ void destroy(mt_model* m) {
     if (s) cudaFreeHost(s);
   if (m->pinned_scalars) cudaFreeHost(m->pinned_scalars);
   if (m->pinned_tok) cudaFreeHost(m->pinned_tok);
+  if (m->pinned_flags) cudaFreeHost(m->pinned_flags);
+  for (size_t t = 0; t < m->g_registered.size(); ++t)
+    if (m->g_registered[t]) cudaHostUnregister(m->tiles[t] + m->layouts[t].off_g);
   for (auto t : m->tiles) std::free(t);
   delete m;
 }
@@ -1520,6 +1648,8 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->K = m->cfg.ckpt_every;
   m->resident_mode = m->cfg.flags & MT_RESIDENT;
   m->store_acts = m->cfg.flags & MT_STORE_ACTS;
+  m->async_adam = m->cfg.flags & MT_ASYNC_ADAM;
+  m->direct_grads = m->cfg.flags & MT_DIRECT_GRADS;
   m->keep_from = keep_from_of(m->cfg);
   m->single_buffer = m->cfg.flags & MT_NO_DOUBLE_BUFFER;
   m->debug = m->cfg.flags & MT_DEBUG_CHECKS;
@@ -1533,6 +1663,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->s_h2d = static_cast<cudaStream_t>(sh);
   m->s_d2h = static_cast<cudaStream_t>(sd);
   build_layouts(m);
+  m->adam_pending.assign(m->layouts.size(), 0);
   const int64_t need = plan_arena(m, nullptr);
   if (!arena || (reinterpret_cast<uintptr_t>(arena) & 255)) throw MtError{MT_EINVAL, "device arena must be 256-byte aligned"};
   if ((int64_t)arena_bytes < need)
@@ -1604,6 +1735,42 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
     m->free_slabs.push_back(i);
   }
   MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_scalars), 256, cudaHostAllocDefault));
+  if (m->time_kernels) {
+    // one event pair per chunk copy of a step, both directions
+    int64_t nh = 0, nd = 0;
+    for (const auto& x : m->visits) {
+      const int64_t wb = m->layouts[x.tile].w_bytes;
+      if (x.h2d) nh += (wb + m->stage_bytes - 1) / m->stage_bytes;
+      if (x.grads) {
+        const int64_t row_b = 2LL * m->D.d;
+        const int64_t rows_chunk = std::max<int64_t>(1, m->slab_bytes / row_b) * row_b;
+        nd += x.kind == kEmbedBwd ? (std::min<int64_t>(m->D.T, m->D.V) * row_b + rows_chunk - 1) / rows_chunk
+                                  : (wb + m->slab_bytes - 1) / m->slab_bytes;
+      }
+    }
+    m->tl_h2d.assign(2 * nh, nullptr);
+    m->tl_d2h.assign(2 * nd, nullptr);
+    m->tl_h2d_visit.assign(nh, -1);
+    m->tl_d2h_visit.assign(nd, -1);
+    for (auto& e : m->tl_h2d) MT_CK(cudaEventCreate(&e));
+    for (auto& e : m->tl_d2h) MT_CK(cudaEventCreate(&e));
+  }
+  if (m->direct_grads) {
+    // page-lock each tile's G section so gradient chunks can land in it
+    m->g_registered.assign(m->tiles.size(), 0);
+    for (size_t t = 0; t < m->tiles.size(); ++t) {
+      const TileLayout& lay = m->layouts[t];
+      if (cudaHostRegister(m->tiles[t] + lay.off_g, (size_t)(lay.off_m - lay.off_g), cudaHostRegisterDefault) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        throw MtError{MT_ENOMEM, "could not page-lock the gradient section of tile " + std::to_string(t)};
+      }
+      m->g_registered[t] = 1;
+    }
+    m->grad_flags = m->ws.grad_flags;
+    MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_flags), sizeof(int) * (3 * m->D.L + 8),
+                        cudaHostAllocDefault));
+  }
   const size_t ntok = (size_t)(3 * m->D.T + m->D.V + 1 + std::min<int64_t>(m->D.T, m->D.V));
   MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_tok), ntok * sizeof(int32_t), cudaHostAllocDefault));
 
@@ -1754,6 +1921,7 @@ int mt_load_layer_tile(mt_model* m, int tile, int part, const void* src, size_t 
     m->err = "null source";
     return MT_EINVAL;
   }
+  if (int rc = mt::settle_adam(m, tile, false)) return rc;
   std::memcpy(m->tiles[tile] + off, src, (size_t)n);
   if (part == MT_PART_W) m->w_loaded[tile] = 1;
   return MT_OK;
@@ -1766,6 +1934,7 @@ int mt_get_layer_tile(mt_model* m, int tile, int part, void* dst, size_t nbytes)
     m->err = "null destination";
     return MT_EINVAL;
   }
+  if (int rc = mt::settle_adam(m, tile, false)) return rc;
   std::memcpy(dst, m->tiles[tile] + off, (size_t)n);
   return MT_OK;
 }
@@ -1795,6 +1964,7 @@ int mt_apply_adam(mt_model* m) {
     m->err = "handle is unusable after an earlier CUDA or internal error: " + m->err;
     return MT_ESTATE;
   }
+  if (int rc = settle_adam(m, -1, true)) return rc;
   for (size_t t = 0; t < m->tiles.size(); ++t) submit_adam_range(m, (int)t, 0, m->layouts[t].w_bytes);
   if (!m->adam_pool->wait_idle(m->cfg.timeout_ms)) {
     m->err = "timed out waiting for Adam";
@@ -1858,6 +2028,7 @@ int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, 
     return MT_ESTATE;
   }
   const int tile = layer + 1;
+  if (int rc = settle_adam(m, tile, true)) return rc;
   if (!m->w_loaded[tile]) {
     m->err = "tile " + std::to_string(tile) + " has no weights loaded";
     return MT_ESTATE;
@@ -1914,8 +2085,33 @@ int64_t mt_get_step(const mt_model* m) { return m ? m->step : MT_EINVAL; }
 
 int mt_set_step(mt_model* m, int64_t step) {
   if (!m || step < 0) return MT_EINVAL;
+  if (int rc = mt::settle_adam(m, -1, false)) return rc;
   m->step = step;
   return MT_OK;
+}
+
+int64_t mt_get_timeline(const mt_model* m, mt_interval* out, int64_t cap) {
+  if (!m || cap < 0) return MT_EINVAL;
+  if (!m->time_kernels) return 0;
+  std::vector<mt_interval> iv;
+  auto add = [&](int32_t kind, int32_t visit, cudaEvent_t a, cudaEvent_t b) {
+    float t0 = 0.f, t1 = 0.f;
+    if (cudaEventElapsedTime(&t0, m->ev_t0, a) == cudaSuccess && cudaEventElapsedTime(&t1, m->ev_t0, b) == cudaSuccess)
+      iv.push_back(mt_interval{kind, visit, (double)t0, (double)t1});
+    else
+      cudaGetLastError();
+  };
+  for (int v = 0; v < (int)m->visits.size(); ++v) add(MT_SPAN_COMPUTE, v, m->ev_vis_a[v], m->ev_vis_b[v]);
+  for (int k = 0; k < m->tl_h2d_n; ++k) add(MT_SPAN_H2D, m->tl_h2d_visit[k], m->tl_h2d[2 * k], m->tl_h2d[2 * k + 1]);
+  const int nd = std::min<int>(m->tl_d2h_n.load(), (int)m->tl_d2h_visit.size());
+  for (int k = 0; k < nd; ++k) add(MT_SPAN_D2H, m->tl_d2h_visit[k], m->tl_d2h[2 * k], m->tl_d2h[2 * k + 1]);
+  for (int64_t i = 0; out && i < (int64_t)iv.size() && i < cap; ++i) out[i] = iv[i];
+  return (int64_t)iv.size();
+}
+
+int mt_sync(mt_model* m) {
+  if (!m) return MT_EINVAL;
+  return mt::settle_adam(m, -1, true);
 }
 
 const char* mt_last_error(const mt_model* m) { return m ? m->err.c_str() : mt::g_init_error.c_str(); }

@@ -124,6 +124,7 @@ struct Workspace {
   int32_t* tokens_dev;  // [B, S+1] (device-token entry point)
   float *rope_cos, *rope_sin;  // [S, hd/2]
   int* status;
+  int* grad_flags;  // [3 L + 8]: one non-finite flag per gradient visit (direct gradient landing)
   long head_chunk;  // rows per LM-head chunk
   // MoE backward scratch
   bf16 *moe_dyp = nullptr, *moe_dgup = nullptr, *moe_dxp = nullptr, *moe_ds = nullptr, *moe_dn2r = nullptr;

@@ -86,6 +86,24 @@ enum {
   MT_VISIT_LOG = 1u << 6,         /* after each step print one line per visit to stderr: the compute-stream
                                      gap before it, its compute-stream time, and how long the stream and the
                                      issuing host thread waited for its weights and its gradient buffer */
+  MT_ASYNC_ADAM = 1u << 8,        /* mt_train_step returns once the step's gradients have landed in their tiles
+                                     and leaves the Adam updates still running on the CPU workers; each
+                                     tile's update finishes before the next step uploads that tile and
+                                     before any call reads or writes it (mt_get_layer_tile,
+                                     mt_load_layer_tile, mt_layer_pass, mt_apply_adam, mt_set_step;
+                                     mt_sync waits for all).  Updates run lowest tile first, the order in
+                                     which the next step needs them, so the host's memory bandwidth, which
+                                     the backward's gradient traffic saturates, finishes the updates of the
+                                     upper layers during the next forward (paperlayer.ai summary §3: CPU
+                                     updates run concurrently with the GPU).  The results are those of the
+                                     synchronous step, bit for bit. */
+  MT_DIRECT_GRADS = 1u << 9,      /* gradient chunks of the first (or only) micro-batch land straight in the
+                                     tiles' G sections, which mt_init_model page-locks, instead of passing
+                                     through the pinned slabs and the accumulator's copy: half the host
+                                     memory traffic of the gradient path, and no host copy between the D2H
+                                     stream and the device gradient buffers' reuse.  A device check flags
+                                     non-finite gradients per visit (the slab path checks on the host).
+                                     Later micro-batches and the embedding rows keep the slab path. */
   MT_TIE_EMBEDDINGS = 1u << 7     /* the LM head's weight is the embedding table E (paperlayer.ai summary
                                      §A.1, tied embeddings: one shared host region, update readiness
                                      tracked).  Tile 0 holds E and the final norm gain gf; there is no head
@@ -350,6 +368,28 @@ int mt_layer_pass(mt_model* m, int layer, const void* x_in, const void* dx_out, 
 int mt_get_layer_tile(mt_model* m, int tile, int part, void* dst, size_t nbytes);
 
 int mt_get_step_stats(const mt_model* m, mt_step_stats* out);
+
+/*
+ * Device timeline of the last step (MT_TIME_KERNELS; 0 intervals otherwise):
+ * each visit's compute-stream span and every chunk copy on the H2D and D2H
+ * streams, in milliseconds from the step's first compute-stream event (a copy
+ * issued before it may start slightly earlier, i.e. at a negative time).
+ * Writes at most cap intervals to out (out may be NULL) and returns the count.
+ */
+enum { MT_SPAN_COMPUTE = 0, MT_SPAN_H2D = 1, MT_SPAN_D2H = 2 };
+typedef struct {
+  int32_t kind;   /* MT_SPAN_* */
+  int32_t visit;  /* the visit the span belongs to (mt_plan_schedule order) */
+  double t0_ms, t1_ms;
+} mt_interval;
+int64_t mt_get_timeline(const mt_model* m, mt_interval* out, int64_t cap);
+
+/*
+ * Wait until every Adam update of the steps run so far has finished
+ * (MT_ASYNC_ADAM; returns at once otherwise).  Returns the error of an
+ * update that failed after its step had returned, else MT_OK.
+ */
+int mt_sync(mt_model* m);
 int64_t mt_get_step(const mt_model* m);       /* Adam step counter t (0 before the first step) */
 int mt_set_step(mt_model* m, int64_t step);  /* for resume */
 const char* mt_last_error(const mt_model* m);

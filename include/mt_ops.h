@@ -205,6 +205,14 @@ enum { MT_STATUS_WAIT_PROBE = 7 };
 int mt_op_wait_probe(int32_t* status, int64_t limit_ns, void* stream);
 
 /*
+ * *flag = 1 if any of the n BF16 values at p (16-byte aligned) is NaN or Inf;
+ * *flag is left as it is otherwise (the caller zeroes it).  The device check
+ * behind MT_DIRECT_GRADS (no counterpart in the pages: their host copy of each
+ * gradient slab is where a non-finite value would be seen).
+ */
+int mt_op_flag_nonfinite(const void* p, int64_t n, int32_t* flag, void* stream);
+
+/*
  * Mixture-of-experts MLP pieces (the expert GEMMs run on mt_op_gemm_grouped,
  * or mt_op_gemm / mt_op_gemm_layout over each expert's rows).  MegaTrain's
  * largest run trains an MoE model (author's blog, the single-H200 gpt-oss

@@ -94,3 +94,21 @@ def test_an_injection_arms_one_step_only():
     m.debug_inject(_lib.MT_INJECT_NONE, 0)
     m.train_step(mt_inputs.step_tokens(SHAPE, 2))
     m.close()
+
+
+def test_adam_failure_after_an_async_step_returns_is_reported():
+    """MT_ASYNC_ADAM: a step may return before its Adam updates finish; an
+    injected Adam failure then surfaces at the next call that waits for them
+    (mt_sync here), never silently."""
+    m = hms.StreamedDecoder.from_shape(SHAPE, flags=_lib.MT_ASYNC_ADAM)
+    m.load_weights(mt_inputs.model_weights(SHAPE))
+    m.debug_inject(_lib.MT_INJECT_ADAM_FAIL, 2)
+    tokens = mt_inputs.step_tokens(SHAPE, 1)
+    with pytest.raises(hms.MtError) as ei:
+        m.train_step(tokens)
+        m.sync()
+    assert ei.value.code == _lib.MT_EINTERNAL and "injected" in str(ei.value)
+    m.weights()  # the tiles are still readable
+    with pytest.raises(hms.MtError):
+        m.train_step(tokens)
+    m.close()

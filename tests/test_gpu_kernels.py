@@ -445,3 +445,24 @@ def test_attention_long_sequence_step_scale():
     g = torch.Generator().manual_seed(32)
     qkv = (torch.randn(B * S, (Hq + 2 * Hkv) * hd, generator=g) * 1.4).to(torch.bfloat16)
     assert _attention_vs_oracle(qkv, B, S, Hq, Hkv, hd) < 5e-3
+
+
+@pytest.mark.parametrize("n", [8, 4096, 1 << 20, 1000003])
+def test_flag_nonfinite(n):
+    """The device non-finite check: clean data leaves the flag at 0; one NaN,
+    +Inf or -Inf anywhere (first, middle, in the ragged tail, last) sets it."""
+    L = _lib.lib()
+    g = torch.Generator().manual_seed(n)
+    x = rnd((n,), g).to(DEV)
+    flag = torch.zeros(1, device=DEV, dtype=torch.int32)
+    assert L.mt_op_flag_nonfinite(x.data_ptr(), n, flag.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    for pos in sorted({0, n // 2, n - 1, (n // 8) * 8 if n % 8 else n - 1}):
+        for bad in (float("nan"), float("inf"), float("-inf")):
+            y = x.clone()
+            y[pos] = bad
+            flag.zero_()
+            assert L.mt_op_flag_nonfinite(y.data_ptr(), n, flag.data_ptr(), None) == 0
+            torch.cuda.synchronize()
+            assert int(flag.item()) == 1, (pos, bad)

@@ -105,6 +105,100 @@ def test_kept_layers_equal_recompute_bitexact(K, keep):
     assert b["stats"]["flops_executed"] < a["stats"]["flops_executed"]
 
 
+@pytest.mark.parametrize("name,keep", [("tiny", 0), ("gqa128", 3)])
+def test_async_adam_equals_synchronous_bitexact(name, keep):
+    """MT_ASYNC_ADAM lets a step return while its Adam updates still run; the
+    next step waits per tile, reads wait too, so three steps give the
+    synchronous step's weights, gradients and moments bit for bit."""
+    s = SHAPES[name]
+    a = _run(s, steps=3, keep_layers=keep)
+    b = _run(s, steps=3, flags=hms.MT_ASYNC_ADAM, keep_layers=keep)
+    assert a["loss"] == b["loss"]
+    for n in range(3):
+        _equal_trees(a["w"][n], b["w"][n])
+        _equal_trees(a["g"][n], b["g"][n])
+        for x, y in zip(a["mv"][n], b["mv"][n]):
+            _equal_trees(x, y)
+
+
+@pytest.mark.parametrize("name,flags,keep", [("tiny", 0, 0), ("gqa128", hms.MT_ASYNC_ADAM, 3),
+                                             ("tiny", hms.MT_TIE_EMBEDDINGS, 0)])
+def test_direct_gradient_landing_equals_slab_path_bitexact(name, flags, keep):
+    """MT_DIRECT_GRADS: gradient chunks land straight in the page-locked G
+    sections (no slab copy); weights, gradients and moments are the slab
+    path's bit for bit over three steps."""
+    s = SHAPES[name]
+    a = _run(s, steps=3, flags=flags, keep_layers=keep)
+    b = _run(s, steps=3, flags=flags | hms.MT_DIRECT_GRADS, keep_layers=keep)
+    assert a["loss"] == b["loss"]
+    for n in range(3):
+        _equal_trees(a["w"][n], b["w"][n])
+        _equal_trees(a["g"][n], b["g"][n])
+        for x, y in zip(a["mv"][n], b["mv"][n]):
+            _equal_trees(x, y)
+
+
+def test_direct_gradient_landing_nonfinite_step_updates_nothing():
+    """A non-finite value in the forward (an infinite weight) with direct
+    gradient landing: MT_ENONFINITE and no weight updated."""
+    s = SHAPES["tiny"]
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    params["layers"][0]["wq"][0, 0] = float("inf")
+    m = hms.StreamedDecoder.from_shape(s, flags=hms.MT_DIRECT_GRADS)
+    m.load_weights(params)
+    with pytest.raises(hms.MtError) as e:
+        m.train_step(mt_inputs.step_tokens(s, 1))
+    assert e.value.code == hms._lib.MT_ENONFINITE
+    _equal_trees(m.weights(), params)
+    m.close()
+
+
+def test_direct_gradient_landing_with_micro_batches_matches_oracle():
+    """The first micro-batch lands directly, the second adds through the slabs."""
+    s = SHAPES["gqa128"]
+    cfg = OracleConfig.from_shape(s)
+    params = mt_inputs.model_weights(s, gain_jitter=0.1)
+    t1, t2 = mt_inputs.step_tokens(s, 1), mt_inputs.step_tokens(s, 2)
+    m = hms.StreamedDecoder.from_shape(s, flags=hms.MT_DIRECT_GRADS | hms.MT_ASYNC_ADAM)
+    m.load_weights(params)
+    loss = m.train_step_micro(torch.stack([t1, t2]))
+    g, w = m.grads(), m.weights()
+    mm, vv = m.moments()
+    m.close()
+    loss_ref, grads = oracle.model_loss_and_grads(params, torch.cat([t1, t2]), cfg)
+    assert abs(loss - loss_ref) <= parity.LOSS_RTOL * abs(loss_ref)
+    parity.assert_grads_close(g, grads)
+    parity.assert_adam_matches(w, params, g, mm, vv, 1, cfg)
+
+
+def test_timeline_spans_every_visit_and_chunk_copy():
+    """mt_get_timeline: one compute span per visit and one span per chunk copy
+    in each direction, each with t1 >= t0; the copies of a visit's weights
+    end before that visit's compute starts (Weights-Ready)."""
+    s = SHAPES["gqa128"]
+    stage, slab = 64 << 10, 32 << 10
+    m = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS | hms.MT_DIRECT_GRADS, stage_bytes=stage,
+                                       grad_slab_bytes=slab, n_grad_slabs=4)
+    m.load_weights(mt_inputs.model_weights(s))
+    m.train_step(mt_inputs.step_tokens(s, 1))
+    tl = m.timeline()
+    plan = hms.plan_schedule(s.n_layers, s.ckpt_every)
+    m.close()
+    L = hms._lib
+    comp = [x for x in tl if x[0] == L.SPAN_COMPUTE]
+    h2d = [x for x in tl if x[0] == L.SPAN_H2D]
+    d2h = [x for x in tl if x[0] == L.SPAN_D2H]
+    assert len(comp) == len(plan)
+    wb = [info["w_bytes"] for info in m.infos]
+    assert len(h2d) == sum(-(-wb[v["tile"]] // stage) for v in plan if v["h2d"])
+    layer_grads = [v for v in plan if v["kind"] in (L.VISIT_LAYER_BWD, L.VISIT_HEAD)]
+    assert len(d2h) >= sum(-(-wb[v["tile"]] // slab) for v in layer_grads)
+    assert all(t1 >= t0 for _, _, t0, t1 in tl)
+    start = {v: t0 for k, v, t0, _ in comp}
+    for _, v, _, t1 in h2d:
+        assert t1 <= start[v] + 1e-3, v
+
+
 @pytest.mark.parametrize("variant", ["ckpt2", "ckpt3", "single_buffer", "small_chunks"])
 def test_schedule_variants_bitexact(variant):
     s = SHAPES["gqa128"]
