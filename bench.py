@@ -255,6 +255,19 @@ def timeline_overlap(tl):
             "d2h_overlap": _intersect(d2h, comp) / _measure(d2h) if d2h else None}
 
 
+def host_bandwidth(nbytes=2 << 30):
+    """Host memory GB/s (read + write) of a large torch CPU copy on all cores."""
+    a = torch.ones(nbytes, dtype=torch.uint8)
+    b = torch.zeros(nbytes, dtype=torch.uint8)
+    best = 0.0
+    for _ in range(3):
+        t0 = time.perf_counter()
+        b.copy_(a)
+        best = max(best, 2 * nbytes / (time.perf_counter() - t0) / 1e9)
+    del a, b
+    return best
+
+
 def load_synthetic_weights(model, s, device):
     """N(0, 0.02) BF16 weights drawn on the GPU from per-tile seeds (1000 + tile), gains 1."""
     for i in range(model.n_tiles):
@@ -344,6 +357,87 @@ def cpu_sample(s, repeats=1):
             "cpu": cpu, "sample_seconds": ts + ta, "layer_seconds": t_layer}
 
 
+def gemm_case(args, s):
+    """One GEMM kind of the workload's step at its full shape, repeated: a small
+    case (a few GB on the device) for DRAM-traffic counters of the GEMM kernel.
+    gate_up: a = SwiGLU(n2 W_gu^T) with the gate/up pairs kept (M = T, N = 2 ffn,
+    K = d); dw_gu: dW_gu = dGU^T n2, both operands MN-major (M = 2 ffn, N = d,
+    K = T).  Prints one JSON line with the launch's FLOPs and algorithmic bytes."""
+    from host_memory_streamed_gb300 import _lib, ops
+    device = torch.device("cuda", 0)
+    T, d, f = s.batch * s.seq, s.d_model, s.ffn
+    g = torch.Generator(device=device).manual_seed(5)
+    rnd = lambda *shape: (torch.randn(*shape, generator=g, device=device) * 0.02).to(torch.bfloat16)
+    if args.gemm_case == "gate_up":
+        A, B = rnd(T, d), rnd(2 * f, d)
+        out = torch.empty(T, f, device=device, dtype=torch.bfloat16)
+        gu = torch.empty(T, 2 * f, device=device, dtype=torch.bfloat16)
+        run = lambda: ops.gemm(A, B, out, _lib.EPI_SWIGLU, out2=gu)
+        M, N, K = T, 2 * f, d
+        alg = 2 * (A.numel() + B.numel() + out.numel() + gu.numel())
+    else:
+        A, B = rnd(T, 2 * f), rnd(T, d)
+        out = torch.empty(2 * f, d, device=device, dtype=torch.bfloat16)
+        run = lambda: ops.gemm_layout(A, B, out, a_mn=True, b_mn=True)
+        M, N, K = 2 * f, d, T
+        alg = 2 * (A.numel() + B.numel() + out.numel())
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"gemm_case": args.gemm_case, "workload": s.name, "M": M, "N": N, "K": K,
+                      "flops_per_launch": 2.0 * M * N * K, "algorithmic_bytes_per_launch": alg,
+                      "ms_per_launch": ms, "tflops": 2.0 * M * N * K / (ms * 1e-3) / 1e12}), flush=True)
+
+
+def attention_case(args, s):
+    """The attention kernels alone at the workload's batch, sequence and heads
+    (q/k/v of standard deviation 1.4, the scale the decoder produces): forward,
+    then backward (delta, dK/dV, dQ), CUDA events around each.  Prints one JSON
+    line; FLOPs are the causal forward's (4 hd S(S+1)/2 per batch and head) and
+    2.5x that for the backward, the usual convention."""
+    from host_memory_streamed_gb300 import ops
+    device = torch.device("cuda", 0)
+    B, S, Hq, Hkv, hd = s.batch, s.seq, s.n_heads, s.n_kv_heads, s.head_dim
+    T, ld = B * S, (Hq + 2 * Hkv) * hd
+    g = torch.Generator(device=device).manual_seed(1)
+    qkv = (torch.randn(T, ld, device=device, generator=g) * 1.4).to(torch.bfloat16)
+    do = torch.randn(T, Hq * hd, device=device, generator=g).to(torch.bfloat16)
+    o = torch.empty(T, Hq * hd, device=device, dtype=torch.bfloat16)
+    lse = torch.empty(B * Hq * S, device=device)
+    delta = torch.empty(B * Hq * S, device=device)
+    dqkv = torch.empty(T, ld, device=device, dtype=torch.bfloat16)
+    st = torch.zeros(1, device=device, dtype=torch.int32)
+    for _ in range(args.warmup):
+        ops.attention_fwd(qkv, B, S, Hq, Hkv, hd, o, lse, st)
+        ops.attention_bwd(qkv, B, S, Hq, Hkv, hd, o, lse, do, delta, dqkv, status=st)
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf = tb = 0.0
+    for _ in range(args.steps):
+        ev[0].record()
+        ops.attention_fwd(qkv, B, S, Hq, Hkv, hd, o, lse, st)
+        ev[1].record()
+        ops.attention_bwd(qkv, B, S, Hq, Hkv, hd, o, lse, do, delta, dqkv, status=st)
+        ev[2].record()
+        torch.cuda.synchronize(device)
+        tf += ev[0].elapsed_time(ev[1])
+        tb += ev[1].elapsed_time(ev[2])
+    if int(st.item()) != 0:
+        raise SystemExit(f"attention kernels reported status {int(st.item())}")
+    tf, tb = tf / args.steps, tb / args.steps
+    fl = 4.0 * B * Hq * hd * S * (S + 1) / 2
+    print(json.dumps({"attention_case": s.name, "B": B, "S": S, "heads": f"{Hq}q/{Hkv}kv x {hd}",
+                      "fwd_ms": tf, "bwd_ms": tb, "fwd_tflops": fl / (tf * 1e-3) / 1e12,
+                      "bwd_tflops_model": 2.5 * fl / (tb * 1e-3) / 1e12}), flush=True)
+
+
 def run_reference(args, s, rank):
     """The reference arm: the oracle timed on the host cores.  A step is one
     bounded sample (cpu_sample); ms_per_step is its measured wall time and
@@ -391,6 +485,10 @@ def main():
                          "the page-locked G sections of the tiles)")
     ap.add_argument("--no-double-buffer", action="store_true",
                     help="ablation: one device weight buffer, so no upload overlaps compute")
+    ap.add_argument("--gemm-case", choices=["gate_up", "dw_gu"], default=None,
+                    help="run one GEMM kind of the step at full shape (a small case for DRAM counters) and exit")
+    ap.add_argument("--attention-case", action="store_true",
+                    help="run the attention kernels alone at the workload's shape and exit")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -405,6 +503,12 @@ def main():
         s = s.with_(n_layers=args.layers)
     if args.impl == "reference":
         run_reference(args, s, rank)
+        return
+    if args.gemm_case:
+        gemm_case(args, s)
+        return
+    if args.attention_case:
+        attention_case(args, s)
         return
 
     import host_memory_streamed_gb300 as hms
@@ -422,6 +526,7 @@ def main():
 
     peaks, peak_kind = measured_peaks()
     h2d_bw, d2h_bw = link_bandwidth(device)
+    host_bw = host_bandwidth()
 
     chunk = args.mlp_chunk_rows
     if chunk < 0:
@@ -496,6 +601,7 @@ def main():
         e2e_elapsed = float(t[0])
     e2e = world * args.steps * tokens_per_step / e2e_elapsed
     model_keep = model.keep_layers
+    n_params = sum(info["n_params"] for info in model.infos)
     model.close()
     del model
 
@@ -565,6 +671,16 @@ def main():
         "losses": losses, "init_seconds": init_s,
         "device_memory": dev_mem,
     }
+    # Host memory traffic of a step: every uploaded byte is read from the
+    # pageable tile, written to pinned staging and read by the DMA; every
+    # gradient byte is written by the DMA (and, through the slabs, read and
+    # written again by the accumulator); Adam reads and writes 22 bytes per
+    # parameter (BF16 w and g, FP32 m and v; w, m, v written back).
+    host_bytes = 3 * st["h2d_bytes"] + (3 if args.slab_grads else 1) * st["d2h_bytes"] + 22 * n_params
+    line["host_memory"] = {"bytes_per_step": host_bytes, "gbs_measured": host_bw,
+                           "t_ms": 1e3 * host_bytes / (host_bw * 1e9),
+                           "frac_of_step": host_bytes / (host_bw * 1e9) / (ms_step * 1e-3),
+                           "method": "torch CPU copy of 2 GiB, read + write bytes, all cores"}
     line["clocks"] = clk.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = {k: v for k, v in cpu_sample(s).items() if k not in ("layer_seconds", "sample_seconds")}
