@@ -598,8 +598,6 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint64_t* p_ready = bar + 7;    // P^T stored (256 softmax threads)
   uint64_t* ds_ready = bar + 8;   // dS^T stored (256)
   uint64_t* ld_ready = bar + 9;   // [2] lse/delta of a block staged (256)
-  uint64_t* st_read = bar + 11;   // every softmax thread has read its S^T columns (256)
-  uint64_t* dpt_read = bar + 12;  // ... and its dP^T columns (256)
   uint64_t* acc_full = bar + 13;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 14);
   __shared__ volatile int abort_flag;
@@ -627,8 +625,6 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     mbar_init(dpt_full, 1);
     mbar_init(p_ready, kSoftmaxWarps);
     mbar_init(ds_ready, kSoftmaxWarps);
-    mbar_init(st_read, kSoftmaxWarps);
-    mbar_init(dpt_read, kSoftmaxWarps);
     mbar_init(acc_full, 1);
     fence_barrier_init();
     tma_prefetch_desc(&tm_qkv);
@@ -696,8 +692,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         const int qs = it & 1;
         const uint64_t bd = smem_desc_mnmajor_sw128(sB + qs * C::TILE, C::BOX);
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk)
-          tc_mma_bf16_ts(acc, src + kk * 8, bd + (uint64_t)(kk * (2048 >> 4)), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 128 / 16; ++kk)  // queries 64.. sit at columns 96..127
+          tc_mma_bf16_ts(acc, src + kk * 8 + (kk >= 4 ? 64 : 0), bd + (uint64_t)(kk * (2048 >> 4)), id_acc,
+                         (it > 0 || kk > 0) ? 1u : 0u);
       };
       if (ok && total > 0) {
         ok = mbar_wait(&qd_full[0], 0);
@@ -779,8 +776,6 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       tmem_ld_32x32b_x32(tST + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_ld_32x32b_x32(tST + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld_regs(sv);
-      tc_fence_before();
-      mbar_arrive_warp(st_read);
       // Queries past the sequence end have lse = +inf (P = 0) and delta = 0;
       // only the diagonal block (q0 == k0) needs the key > query mask.
       const bool diag = q0 == k0;
@@ -801,12 +796,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) pk[j] = pack2bf(pf[2 * j], pf[2 * j + 1]);
-      if (!mbar_wait_warp(st_read, ph)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st_packed32(tST + lane_off + hf * 32, pk);
+      // P^T over the first 32 of this half's own 64 S^T columns (half 0:
+      // 0..31, half 1: 96..127): no other thread reads them, so no barrier
+      tmem_st_packed32(tST + lane_off + hf * 96, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(p_ready);
@@ -833,14 +825,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
                                   pf[c + 3] * (__uint_as_float(dp[c4 * 4 + 3]) - dv[3]));
         }
       }
-      tc_fence_before();
-      mbar_arrive_warp(dpt_read);
-      if (!mbar_wait_warp(dpt_read, ph)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st_packed32(tDPT + lane_off + hf * 32, pk);
+      tmem_st_packed32(tDPT + lane_off + hf * 96, pk);  // dS^T likewise over this half's dP^T columns
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(ds_ready);
@@ -1052,8 +1037,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         const uint32_t src = tmem + 128u * (uint32_t)(j & 1);
         const uint64_t kd = smem_desc_mnmajor_sw128(sK + (j % NK) * C::TILE, C::BOX);
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk)
-          tc_mma_bf16_ts(tdQ, src + kk * 8, kd + (uint64_t)(kk * (2048 >> 4)), id_dq, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 128 / 16; ++kk)  // keys 64.. sit at columns 96..127
+          tc_mma_bf16_ts(tdQ, src + kk * 8 + (kk >= 4 ? 64 : 0), kd + (uint64_t)(kk * (2048 >> 4)), id_dq,
+                         (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&k_empty[j % NK]);
       }
       if (ok) {
@@ -1116,13 +1102,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive_warp(sd_read);
-      if (!mbar_wait_warp(sd_read, ph)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st_packed32(tS + lane_off + hf * 32, pk);
+      mbar_arrive_warp(sd_read);  // dP_{j+1} may overwrite dP_j once every warp has read it
+      // dS over the first 32 of this half's own 64 S columns (half 0: 0..31,
+      // half 1: 96..127): no other thread reads them, so no barrier
+      tmem_st_packed32(tS + lane_off + hf * 96, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&ds_ready[j & 1]);
