@@ -62,12 +62,13 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def gemm_traffic_per_launch():
-    """DRAM bytes per GEMM launch of the 14B step from the committed ncu summary
-    (profiles/gemm_dram_14b_step.md), or None when gemm.cu has changed since
-    the counters were taken (the summary records the source's SHA-256)."""
+def gemm_traffic_per_flop():
+    """DRAM bytes per GEMM FLOP of the GEMM kernel from the committed ncu
+    summary of two full-shape 14B GEMM kinds (profiles/gemm_dram_14b_shapes.md),
+    or None when gemm.cu has changed since the counters were taken (the
+    summary records the source's SHA-256)."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "gemm_dram_14b_step.md")
+    prof = os.path.join(ROOT, "profiles", "gemm_dram_14b_shapes.md")
     src = os.path.join(ROOT, "host_memory_streamed_gb300", "csrc", "gemm.cu")
     if not (os.path.exists(prof) and os.path.exists(src)):
         return None
@@ -77,9 +78,9 @@ def gemm_traffic_per_launch():
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if fields.get("gemm.cu sha256") != digest or "traffic bytes per launch" not in fields:
+    if fields.get("gemm.cu sha256") != digest or "traffic bytes per GEMM flop" not in fields:
         return None
-    return float(fields["traffic bytes per launch"])
+    return float(fields["traffic bytes per GEMM flop"])
 
 
 def mem_available_bytes():
@@ -657,7 +658,10 @@ def main():
                     "timeline": overlap_tl},
         "roofline": {"bound": "tensor", "kernel": "gemm_bf16_tcgen05", "achieved": achieved, "peak": p_sust,
                      "unit": "TFLOP/s", "frac": (achieved / p_sust) if achieved else None,
-                     "traffic": gemm_traffic_per_launch() if s.name == "14b" else None,
+                     "traffic": (gemm_traffic_per_flop() * gemm_flops / max(1, gemm_launches)
+                                 if s.name == "14b" and gemm_traffic_per_flop() else None),
+                     "traffic_basis": "DRAM bytes per FLOP of two full-shape 14B GEMM kinds (ncu, "
+                                      "profiles/gemm_dram_14b_shapes.md) x this step's FLOPs per GEMM launch",
                      "peak_kind": f"bf16_tflops_sustained ({peak_kind}) -- timed inside a long step",
                      "launches": gemm_launches, "flops_per_launch": gemm_flops / max(1, gemm_launches),
                      "ms_per_launch": gemm_ms / max(1, gemm_launches)},
