@@ -484,6 +484,9 @@ def main():
     ap.add_argument("--slab-grads", action="store_true",
                     help="gradients through the pinned slabs and the accumulator's copy (default: straight into "
                          "the page-locked G sections of the tiles)")
+    ap.add_argument("--staged-weights", action="store_true",
+                    help="weights through the packer's pinned staging chunks (default: each upload's DMA reads "
+                         "the page-locked W section of the tile)")
     ap.add_argument("--no-double-buffer", action="store_true",
                     help="ablation: one device weight buffer, so no upload overlaps compute")
     ap.add_argument("--gemm-case", choices=["gate_up", "dw_gu"], default=None,
@@ -545,7 +548,8 @@ def main():
     if chunk:
         keep = 0  # a chunked MLP keeps no per-layer activations
     flags = hms.MT_TIME_KERNELS | (hms.MT_NO_DOUBLE_BUFFER if args.no_double_buffer else 0) | \
-        (0 if args.sync_adam else hms.MT_ASYNC_ADAM) | (0 if args.slab_grads else hms.MT_DIRECT_GRADS)
+        (0 if args.sync_adam else hms.MT_ASYNC_ADAM) | (0 if args.slab_grads else hms.MT_DIRECT_GRADS) | \
+        (0 if args.staged_weights else hms.MT_DIRECT_WEIGHTS)
     model = hms.StreamedDecoder.from_shape(s, flags=flags, device=device, mlp_chunk_rows=chunk,
                                            n_adam_threads=adam_threads, keep_layers=keep)
     load_synthetic_weights(model, s, device)
@@ -634,6 +638,8 @@ def main():
                    "keep_layers": model_keep, "double_buffer": not args.no_double_buffer,
                    "adam": "sync" if args.sync_adam else "async (finished inside the timed region)",
                    "grads": "pinned slabs + accumulator copy" if args.slab_grads else "direct into page-locked G",
+                   "weights": "packer copy into pinned staging + DMA" if args.staged_weights
+                   else "DMA from page-locked W",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (weights streamed per layer, activations > 129 MB)",
                    "mlp_chunk_rows": chunk or None,
@@ -680,7 +686,7 @@ def main():
     # gradient byte is written by the DMA (and, through the slabs, read and
     # written again by the accumulator); Adam reads and writes 22 bytes per
     # parameter (BF16 w and g, FP32 m and v; w, m, v written back).
-    host_bytes = 3 * st["h2d_bytes"] + (3 if args.slab_grads else 1) * st["d2h_bytes"] + 22 * n_params
+    host_bytes = (3 if args.staged_weights else 1) * st["h2d_bytes"] + (3 if args.slab_grads else 1) * st["d2h_bytes"] + 22 * n_params
     line["host_memory"] = {"bytes_per_step": host_bytes, "gbs_measured": host_bw,
                            "t_ms": 1e3 * host_bytes / (host_bw * 1e9),
                            "frac_of_step": host_bytes / (host_bw * 1e9) / (ms_step * 1e-3),

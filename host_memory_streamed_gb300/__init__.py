@@ -13,13 +13,13 @@ import ctypes as C
 import torch
 
 from . import _lib
-from ._lib import (MT_ASYNC_ADAM, MT_DEBUG_CHECKS, MT_DIRECT_GRADS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V,
+from ._lib import (MT_ASYNC_ADAM, MT_DEBUG_CHECKS, MT_DIRECT_GRADS, MT_DIRECT_WEIGHTS, MT_NO_DOUBLE_BUFFER, MT_PART_G, MT_PART_M, MT_PART_V,
                    MT_PART_W, MT_RESIDENT, MT_STORE_ACTS, MT_TIE_EMBEDDINGS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG,
                    ERROR_NAMES)
 
 __all__ = ["StreamedDecoder", "MtError", "ops", "plan_schedule", "MT_RESIDENT", "MT_STORE_ACTS", "MT_NO_DOUBLE_BUFFER",
            "MT_DEBUG_CHECKS", "MT_TIME_KERNELS", "MT_TRACE", "MT_VISIT_LOG", "MT_TIE_EMBEDDINGS", "MT_PART_W",
-           "MT_PART_G", "MT_PART_M", "MT_PART_V", "MT_ASYNC_ADAM", "MT_DIRECT_GRADS"]
+           "MT_PART_G", "MT_PART_M", "MT_PART_V", "MT_ASYNC_ADAM", "MT_DIRECT_GRADS", "MT_DIRECT_WEIGHTS"]
 
 LAYER_NAMES = ("g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
 

@@ -15,7 +15,7 @@ ERROR_NAMES = {0: "MT_OK", -1: "MT_EINVAL", -2: "MT_ENOMEM", -3: "MT_ECUDA", -4:
                -5: "MT_ESTATE", -6: "MT_ENONFINITE", -7: "MT_EINTERNAL"}
 
 MT_RESIDENT, MT_STORE_ACTS, MT_NO_DOUBLE_BUFFER, MT_DEBUG_CHECKS, MT_TIME_KERNELS, MT_TRACE, MT_VISIT_LOG, \
-    MT_TIE_EMBEDDINGS, MT_ASYNC_ADAM, MT_DIRECT_GRADS = 1, 2, 4, 8, 16, 32, 64, 128, 256, 512
+    MT_TIE_EMBEDDINGS, MT_ASYNC_ADAM, MT_DIRECT_GRADS, MT_DIRECT_WEIGHTS = 1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024
 MT_PART_W, MT_PART_G, MT_PART_M, MT_PART_V = 0, 1, 2, 3
 
 EPI_STORE_BF16, EPI_RESIDUAL_BF16, EPI_F32, EPI_F32_ACCUMULATE, EPI_SWIGLU, EPI_ROPE, EPI_SWIGLU_BWD = range(7)

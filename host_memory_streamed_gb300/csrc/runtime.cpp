@@ -478,7 +478,10 @@ struct mt_model {
   // chunks land in them directly; a device check flags non-finite values of
   // each gradient visit (grad_flags, copied to pinned_flags before the chunks)
   bool direct_grads = false;
-  std::vector<int> g_registered;
+  // page-locked range of each tile (MT_DIRECT_GRADS: its G section; MT_DIRECT_WEIGHTS: its W
+  // section; both: W and G as one range), nullptr where nothing is registered
+  std::vector<uint8_t*> host_reg;
+  bool direct_weights = false;
   int* grad_flags = nullptr;     // device [visits]
   int* pinned_flags = nullptr;   // host, pinned [visits]
   std::mutex adam_mu;
@@ -682,19 +685,27 @@ void loader_main(mt_model* m) {
         const uint8_t* src = m->tiles[x.tile] + lay.off_w;
         uint8_t* dst = m->wbuf[x.buf];
         const int64_t n = lay.w_bytes;
+        // Staged: a packer copy into one of the two pinned staging chunks, then its
+        // DMA.  Direct (MT_DIRECT_WEIGHTS): the DMA reads the page-locked W section
+        // itself, chunk by chunk, so nothing on the host touches the bytes.
         for (int64_t off = 0; off < n; off += m->stage_bytes) {
           const int64_t c = std::min(m->stage_bytes, n - off);
-          const int k = si++ & 1;
-          wait_event(m, m->ev_stage[k], "pinned staging buffer");
-          pack_copy(m, m->stage[k], src + off, c);
+          const uint8_t* from = src + off;
+          const int k = si & 1;
+          if (!m->direct_weights) {
+            ++si;
+            wait_event(m, m->ev_stage[k], "pinned staging buffer");
+            pack_copy(m, m->stage[k], src + off, c);
+            from = m->stage[k];
+          }
           const int tl = m->time_kernels && 2 * m->tl_h2d_n + 1 < (int)m->tl_h2d.size() ? m->tl_h2d_n++ : -1;
           if (tl >= 0) {
             m->tl_h2d_visit[tl] = v;
             MT_CK(cudaEventRecord(m->tl_h2d[2 * tl], m->s_h2d));
           }
-          MT_CK(cudaMemcpyAsync(dst + off, m->stage[k], (size_t)c, cudaMemcpyHostToDevice, m->s_h2d));
+          MT_CK(cudaMemcpyAsync(dst + off, from, (size_t)c, cudaMemcpyHostToDevice, m->s_h2d));
           if (tl >= 0) MT_CK(cudaEventRecord(m->tl_h2d[2 * tl + 1], m->s_h2d));
-          MT_CK(cudaEventRecord(m->ev_stage[k], m->s_h2d));
+          if (!m->direct_weights) MT_CK(cudaEventRecord(m->ev_stage[k], m->s_h2d));
         }
         MT_CK(cudaEventRecord(m->ev_h2d_b[v], m->s_h2d));
         MT_CK(cudaEventRecord(m->ev_ready[v], m->s_h2d));
@@ -1598,8 +1609,8 @@ void destroy(mt_model* m) {
     // work may still be running against the pinned buffers: leak them rather than free memory in use
     std::fprintf(stderr, "mt_free: streams still busy after %lld ms; pinned buffers are leaked\n",
                  (long long)m->cfg.timeout_ms);
-    for (size_t t = 0; t < m->tiles.size(); ++t)  // page-locked gradient sections are leaked with them
-      if (t >= m->g_registered.size() || !m->g_registered[t]) std::free(m->tiles[t]);
+    for (size_t t = 0; t < m->tiles.size(); ++t)  // page-locked tiles are leaked with them
+      if (t >= m->host_reg.size() || !m->host_reg[t]) std::free(m->tiles[t]);
     delete m;
     return;
   }
@@ -1635,8 +1646,8 @@ void destroy(mt_model* m) {
   if (m->pinned_scalars) cudaFreeHost(m->pinned_scalars);
   if (m->pinned_tok) cudaFreeHost(m->pinned_tok);
   if (m->pinned_flags) cudaFreeHost(m->pinned_flags);
-  for (size_t t = 0; t < m->g_registered.size(); ++t)
-    if (m->g_registered[t]) cudaHostUnregister(m->tiles[t] + m->layouts[t].off_g);
+  for (uint8_t* r : m->host_reg)
+    if (r) cudaHostUnregister(r);
   for (auto t : m->tiles) std::free(t);
   delete m;
 }
@@ -1650,6 +1661,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   m->store_acts = m->cfg.flags & MT_STORE_ACTS;
   m->async_adam = m->cfg.flags & MT_ASYNC_ADAM;
   m->direct_grads = m->cfg.flags & MT_DIRECT_GRADS;
+  m->direct_weights = m->cfg.flags & MT_DIRECT_WEIGHTS;
   m->keep_from = keep_from_of(m->cfg);
   m->single_buffer = m->cfg.flags & MT_NO_DOUBLE_BUFFER;
   m->debug = m->cfg.flags & MT_DEBUG_CHECKS;
@@ -1755,18 +1767,21 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
     for (auto& e : m->tl_h2d) MT_CK(cudaEventCreate(&e));
     for (auto& e : m->tl_d2h) MT_CK(cudaEventCreate(&e));
   }
-  if (m->direct_grads) {
-    // page-lock each tile's G section so gradient chunks can land in it
-    m->g_registered.assign(m->tiles.size(), 0);
+  if (m->direct_grads || m->direct_weights) {
+    // page-lock the sections the DMA engines read (W) or write (G) in place
+    m->host_reg.assign(m->tiles.size(), nullptr);
     for (size_t t = 0; t < m->tiles.size(); ++t) {
       const TileLayout& lay = m->layouts[t];
-      if (cudaHostRegister(m->tiles[t] + lay.off_g, (size_t)(lay.off_m - lay.off_g), cudaHostRegisterDefault) !=
-          cudaSuccess) {
+      const int64_t lo = m->direct_weights ? lay.off_w : lay.off_g;
+      const int64_t hi = m->direct_grads ? lay.off_m : lay.off_w + lay.w_bytes;
+      if (cudaHostRegister(m->tiles[t] + lo, (size_t)(hi - lo), cudaHostRegisterDefault) != cudaSuccess) {
         cudaGetLastError();
-        throw MtError{MT_ENOMEM, "could not page-lock the gradient section of tile " + std::to_string(t)};
+        throw MtError{MT_ENOMEM, "could not page-lock tile " + std::to_string(t) + " for direct copies"};
       }
-      m->g_registered[t] = 1;
+      m->host_reg[t] = m->tiles[t] + lo;
     }
+  }
+  if (m->direct_grads) {
     m->grad_flags = m->ws.grad_flags;
     MT_CK(cudaHostAlloc(reinterpret_cast<void**>(&m->pinned_flags), sizeof(int) * (3 * m->D.L + 8),
                         cudaHostAllocDefault));

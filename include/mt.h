@@ -104,6 +104,14 @@ enum {
                                      stream and the device gradient buffers' reuse.  A device check flags
                                      non-finite gradients per visit (the slab path checks on the host).
                                      Later micro-batches and the embedding rows keep the slab path. */
+  MT_DIRECT_WEIGHTS = 1u << 10,   /* each upload's DMA reads the tile's W section in place, which
+                                     mt_init_model page-locks, instead of a packer copy into the two
+                                     pinned staging chunks followed by their DMA: a third of the host
+                                     memory traffic of the weight path, and no host thread on it.  The
+                                     tile's bytes must not change while its copy is queued, which the
+                                     step already guarantees (its Adam update finishes before the
+                                     upload is enqueued, MT_ASYNC_ADAM included).  With MT_DIRECT_GRADS
+                                     the W and G sections are page-locked as one range per tile. */
   MT_TIE_EMBEDDINGS = 1u << 7     /* the LM head's weight is the embedding table E (paperlayer.ai summary
                                      §A.1, tied embeddings: one shared host region, update readiness
                                      tracked).  Tile 0 holds E and the final norm gain gf; there is no head

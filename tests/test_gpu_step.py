@@ -138,6 +138,25 @@ def test_direct_gradient_landing_equals_slab_path_bitexact(name, flags, keep):
             _equal_trees(x, y)
 
 
+@pytest.mark.parametrize("name,flags,keep", [("tiny", 0, 0),
+                                             ("gqa128", hms.MT_ASYNC_ADAM | hms.MT_DIRECT_GRADS, 3),
+                                             ("tiny", hms.MT_TIE_EMBEDDINGS | hms.MT_DIRECT_GRADS, 0)])
+def test_direct_weight_upload_equals_staged_path_bitexact(name, flags, keep):
+    """MT_DIRECT_WEIGHTS: each upload's DMA reads the page-locked W section in
+    place, in chunks smaller than a tile; losses, weights, gradients and
+    moments are the staged path's bit for bit over three steps (so every
+    upload read the weights after that tile's previous Adam update)."""
+    s = SHAPES[name]
+    a = _run(s, steps=3, flags=flags, keep_layers=keep, stage_bytes=48 << 10)
+    b = _run(s, steps=3, flags=flags | hms.MT_DIRECT_WEIGHTS, keep_layers=keep, stage_bytes=48 << 10)
+    assert a["loss"] == b["loss"]
+    for n in range(3):
+        _equal_trees(a["w"][n], b["w"][n])
+        _equal_trees(a["g"][n], b["g"][n])
+        for x, y in zip(a["mv"][n], b["mv"][n]):
+            _equal_trees(x, y)
+
+
 def test_direct_gradient_landing_nonfinite_step_updates_nothing():
     """A non-finite value in the forward (an infinite weight) with direct
     gradient landing: MT_ENONFINITE and no weight updated."""
@@ -171,13 +190,15 @@ def test_direct_gradient_landing_with_micro_batches_matches_oracle():
     parity.assert_adam_matches(w, params, g, mm, vv, 1, cfg)
 
 
-def test_timeline_spans_every_visit_and_chunk_copy():
+@pytest.mark.parametrize("direct_weights", [0, hms.MT_DIRECT_WEIGHTS])
+def test_timeline_spans_every_visit_and_chunk_copy(direct_weights):
     """mt_get_timeline: one compute span per visit and one span per chunk copy
     in each direction, each with t1 >= t0; the copies of a visit's weights
     end before that visit's compute starts (Weights-Ready)."""
     s = SHAPES["gqa128"]
     stage, slab = 64 << 10, 32 << 10
-    m = hms.StreamedDecoder.from_shape(s, flags=hms.MT_TIME_KERNELS | hms.MT_DIRECT_GRADS, stage_bytes=stage,
+    flags = hms.MT_TIME_KERNELS | hms.MT_DIRECT_GRADS | direct_weights
+    m = hms.StreamedDecoder.from_shape(s, flags=flags, stage_bytes=stage,
                                        grad_slab_bytes=slab, n_grad_slabs=4)
     m.load_weights(mt_inputs.model_weights(s))
     m.train_step(mt_inputs.step_tokens(s, 1))
