@@ -16,9 +16,11 @@ cannot hold all 48 layers' tiles the depth is truncated to what fits and the
 JSON says so.  With `--impl reference` the CPU oracle is timed instead on a
 bounded sample of the same workload (see `cpu_sample`).
 
-N > 1 (torchrun): one independent replica per GPU, no collective on the data
-path (the method is single-GPU); value = all ranks' tokens / the slowest
-rank's time.
+N > 1 (torchrun): N data-parallel replicas of one model, one per GPU, each on
+its own batch, whose gradients the runtime sums in host shared memory (one
+copy of the host tiles; no collective on the data path); value = all ranks'
+tokens / the slowest rank's time.  --independent-replicas runs N unrelated
+models instead.
 """
 from __future__ import annotations
 
@@ -288,11 +290,11 @@ def load_synthetic_weights(model, s, device):
         del raw
 
 
-def token_batches(s, steps, device):
+def token_batches(s, steps, device, rank=0):
     gen = torch.Generator(device=device)
     out = []
     for n in range(steps):
-        gen.manual_seed(2000 + n + 1)
+        gen.manual_seed(2000 + n + 1 + 100003 * rank)
         out.append(torch.randint(0, s.vocab, (s.batch, s.seq + 1), generator=gen, device=device, dtype=torch.int32))
     return out
 
@@ -487,6 +489,12 @@ def main():
     ap.add_argument("--staged-weights", action="store_true",
                     help="weights through the packer's pinned staging chunks (default: each upload's DMA reads "
                          "the page-locked W section of the tile)")
+    ap.add_argument("--share-device", action="store_true",
+                    help="every rank on cuda:0: exercises the N > 1 path on one GPU (the ranks only meet on the "
+                         "host); the throughput it prints is not an N-GPU figure")
+    ap.add_argument("--independent-replicas", action="store_true",
+                    help="N > 1: N unrelated models, one per GPU (default: one model, N data-parallel replicas "
+                         "summing their gradients on the host)")
     ap.add_argument("--no-double-buffer", action="store_true",
                     help="ablation: one device weight buffer, so no upload overlaps compute")
     ap.add_argument("--gemm-case", choices=["gate_up", "dw_gu"], default=None,
@@ -518,14 +526,15 @@ def main():
     import host_memory_streamed_gb300 as hms
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
-    device = torch.device("cuda", local)
+    device = torch.device("cuda", 0 if args.share_device else local)
     torch.cuda.set_device(device)
     pg = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
         pg = dist
-    L = fit_depth(s, n_replicas=world) if not args.layers else s.n_layers
+    group = world > 1 and not args.independent_replicas
+    L = fit_depth(s, n_replicas=1 if group else world) if not args.layers else s.n_layers
     s = s.with_(n_layers=L)
 
     peaks, peak_kind = measured_peaks()
@@ -540,6 +549,8 @@ def main():
     # replicas share the host's cores: split the Adam workers (3/4 of the cores, the library's
     # own default for one process) between them instead of oversubscribing
     adam_threads = max(2, (os.cpu_count() or 4) * 3 // 4 // world) if world > 1 else 0
+    if group:  # the last replica runs every Adam update of the group
+        adam_threads = 0 if rank == world - 1 else 2
     keep = args.keep_layers
     if keep == "preset":
         keep = "auto" if s.name in KEEP_AUTO_WORKLOADS else 0
@@ -550,11 +561,17 @@ def main():
     flags = hms.MT_TIME_KERNELS | (hms.MT_NO_DOUBLE_BUFFER if args.no_double_buffer else 0) | \
         (0 if args.sync_adam else hms.MT_ASYNC_ADAM) | (0 if args.slab_grads else hms.MT_DIRECT_GRADS) | \
         (0 if args.staged_weights else hms.MT_DIRECT_WEIGHTS)
+    kw = {}
+    if group:
+        from host_memory_streamed_gb300 import replicas
+        kw["replica_group"] = (replicas.shared_group_name("mt-bench"), rank, world)
     model = hms.StreamedDecoder.from_shape(s, flags=flags, device=device, mlp_chunk_rows=chunk,
-                                           n_adam_threads=adam_threads, keep_layers=keep)
-    load_synthetic_weights(model, s, device)
+                                           n_adam_threads=adam_threads, keep_layers=keep, **kw)
+    if not group or rank == 0:  # a group's tiles are shared: one replica writes them
+        load_synthetic_weights(model, s, device)
+    model.barrier()
     init_s = time.perf_counter() - t_init
-    toks = token_batches(s, args.warmup + args.steps, device)
+    toks = token_batches(s, args.warmup + args.steps, device, rank)
     host_toks = [t.cpu().pin_memory() for t in toks]
     s_comp = model.streams[0]
 
@@ -567,7 +584,7 @@ def main():
         pg.barrier()
     torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(device.index) as clk:
         e0.record(s_comp)
         losses = []
         for i in range(args.steps):
@@ -640,7 +657,8 @@ def main():
                    "grads": "pinned slabs + accumulator copy" if args.slab_grads else "direct into page-locked G",
                    "weights": "packer copy into pinned staging + DMA" if args.staged_weights
                    else "DMA from page-locked W",
-                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "parallelism": ("data-parallel replica group" if group else "independent replicas")
+                   if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (weights streamed per layer, activations > 129 MB)",
                    "mlp_chunk_rows": chunk or None,
                    "truncated": s.n_layers < full_layers,

@@ -54,10 +54,14 @@ class StreamedDecoder:
                  ckpt_every=1, rms_eps=1e-5, rope_theta=1e4, lr=1e-4, beta1=0.9, beta2=0.95, adam_eps=1e-8,
                  weight_decay=0.0, n_adam_threads=0, n_pack_threads=0, n_grad_slabs=0, grad_slab_bytes=0,
                  stage_bytes=0, timeout_ms=0, flags=0, mlp_chunk_rows=0, n_experts=0, top_k=0, keep_layers=0,
-                 device=None):
+                 replica_group=None, device=None):
         """keep_layers: how many of the last layers keep their internals on the
         device from forward to backward (no recompute for them); "auto" keeps as
-        many as fit in the device's free memory (less ``KEEP_MARGIN``)."""
+        many as fit in the device's free memory (less ``KEEP_MARGIN``).
+
+        replica_group: ``(name, rank, n)`` makes this handle replica ``rank`` of
+        ``n`` data-parallel replicas of one model whose host tiles live once, in
+        the shared-memory segment ``name`` (see ``replicas``)."""
         if not torch.cuda.is_available():
             raise RuntimeError("a CUDA device is required (the library has no CPU path)")
         self._L = _lib.lib()
@@ -70,6 +74,9 @@ class StreamedDecoder:
                          grad_slab_bytes=grad_slab_bytes, stage_bytes=stage_bytes, timeout_ms=timeout_ms,
                          flags=flags, mlp_chunk_rows=mlp_chunk_rows, n_experts=n_experts, top_k=top_k).items():
             setattr(cfg, k, v)
+        if replica_group is not None:
+            name, rank, n = replica_group
+            cfg.replica_name, cfg.replica_rank, cfg.n_replicas = name.encode(), int(rank), int(n)
         self.cfg = cfg
         self.device = torch.device(device or "cuda")
         cfg.keep_layers = self.fit_keep_layers(cfg, self.device) if keep_layers == "auto" else int(keep_layers)
@@ -309,7 +316,7 @@ class StreamedDecoder:
         """Forward and backward of one step without the optimizer: the tiles'
         G sections receive the gradient of the mean loss over these tokens
         (host int32 [B, S+1]); weights, moments and the step are unchanged.
-        Returns the loss.  See ``apply_adam`` and ``replicas.replica_step``."""
+        Returns the loss.  See ``apply_adam``."""
         loss = C.c_float()
         tok = tokens.to(torch.int32).contiguous()
         if tok.is_cuda:
@@ -349,6 +356,11 @@ class StreamedDecoder:
     def sync(self):
         """Wait for every pending Adam update (``mt_sync``; MT_ASYNC_ADAM)."""
         self._check(self._L.mt_sync(self._h))
+
+    def barrier(self):
+        """Replica group: wait until every replica has called ``barrier`` as
+        often as this one (``mt_replica_barrier``); no-op outside a group."""
+        self._check(self._L.mt_replica_barrier(self._h))
 
     def stats(self) -> dict:
         st = _lib.MtStepStats()

@@ -34,7 +34,8 @@ class MtConfig(C.Structure):
         ("n_adam_threads", C.c_int32), ("n_pack_threads", C.c_int32), ("n_grad_slabs", C.c_int32),
         ("grad_slab_bytes", C.c_int64), ("stage_bytes", C.c_int64), ("timeout_ms", C.c_int64),
         ("flags", C.c_uint32), ("mlp_chunk_rows", C.c_int64), ("n_experts", C.c_int32), ("top_k", C.c_int32),
-        ("keep_layers", C.c_int32),
+        ("keep_layers", C.c_int32), ("replica_rank", C.c_int32), ("n_replicas", C.c_int32),
+        ("replica_name", C.c_char * 48),
     ]
 
 
@@ -112,6 +113,7 @@ def lib():
         "mt_get_step_stats": (C.c_int, [vp, C.POINTER(MtStepStats)]),
         "mt_get_step": (i64, [vp]),
         "mt_set_step": (C.c_int, [vp, i64]),
+        "mt_replica_barrier": (C.c_int, [vp]),
         "mt_sync": (C.c_int, [vp]),
         "mt_get_timeline": (i64, [vp, C.POINTER(MtInterval), i64]),
         "mt_last_error": (C.c_char_p, [vp]),

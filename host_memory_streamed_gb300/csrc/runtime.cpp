@@ -29,6 +29,15 @@
 // §A.4 (stateless templates, ping-pong binding, no CUDA graphs); hyper.ai
 // summary 方法 ¶2-6 (block recompute order, JIT packer thread, Weights-Ready
 // event before Bind); author's blog (per-block F/W/G figure).
+//
+// Replica group (n_replicas >= 2): one process per GPU, every process mapping
+// one shared-memory segment that holds a control block and all host tiles.
+// Each replica runs the step above on its own batch; its accumulator adds a
+// gradient chunk into the shared G only when the chunk's turn counter says
+// replicas 0 .. r-1 have added theirs, and the last replica's Adam pool
+// updates each chunk once its own addition is in.  Each tile's finished
+// update is published in the control block, and every replica's loader waits
+// for it before uploading that tile for the next step.
 #include <atomic>
 #include <chrono>
 #include <cmath>
@@ -46,7 +55,11 @@
 #include <vector>
 
 #include <nvtx3/nvToolsExt.h>
+#include <errno.h>
+#include <fcntl.h>
+#include <sys/mman.h>
 #include <sys/resource.h>
+#include <sys/stat.h>
 #include <sys/syscall.h>
 #include <unistd.h>
 
@@ -374,6 +387,34 @@ Workspace carve_ws(uint8_t* base, const Dims& D, Plan& P) {
 }  // namespace
 }  // namespace mt
 
+// ====================================================================== replica group control block
+namespace mt {
+constexpr int kMaxReplicas = 64;
+constexpr uint64_t kGroupMagic = 0x3170756f72477453ull;
+
+// At the start of the shared segment; the turn counters [n_chunks], the
+// published Adam steps [tiles] and the loaded flags [tiles] follow it.  All
+// counters are read and written with atomic builtins (lock-free, address-free
+// on both host architectures), so they work across processes.
+struct GroupHeader {
+  uint64_t magic;
+  int64_t total_bytes, n_chunks, slab_bytes, n_tiles;
+  int32_t n_replicas, ready, attached, failed;
+  int64_t steps_done;      // step completions of all replicas, cumulative
+  int64_t nonfinite_step;  // s + 1 once group step s has seen a non-finite loss or gradient
+  int64_t emb_turn;        // embedding rows of step s: replica r adds once it reads s * n + r
+  int64_t barrier_count;   // mt_replica_barrier arrivals, cumulative
+  float loss[2][kMaxReplicas];  // each replica's scaled loss, by step parity
+};
+
+template <class T>
+inline T aload(const T* p) { return __atomic_load_n(p, __ATOMIC_ACQUIRE); }
+template <class T>
+inline void astore(T* p, T v) { __atomic_store_n(p, v, __ATOMIC_RELEASE); }
+template <class T>
+inline T aadd(T* p, T v) { return __atomic_add_fetch(p, v, __ATOMIC_ACQ_REL); }
+}  // namespace mt
+
 // ====================================================================== the handle
 struct mt_model {
   mt_config cfg{};
@@ -489,6 +530,22 @@ struct mt_model {
   std::vector<int> adam_pending;
   std::chrono::steady_clock::time_point last_grads_landed;
 
+  // replica group (n_replicas >= 2); micro_index / micro_count are rank / n
+  struct Group {
+    int rank = 0, n = 0;
+    uint8_t* base = nullptr;  // the mapped segment
+    size_t bytes = 0;
+    mt::GroupHeader* h = nullptr;
+    int64_t* turn = nullptr;       // per gradient chunk
+    int64_t* adam_done = nullptr;  // per tile: s + 1 once step s's update of the tile has finished
+    int32_t* loaded = nullptr;     // per tile: W loaded by some replica
+    std::vector<int64_t> chunk_base;  // first chunk index of each tile
+    int64_t s = 0;                    // group steps run (the current step while one runs)
+    int64_t barriers = 0;             // mt_replica_barrier calls of this replica
+    std::vector<int64_t> final_val;   // last replica: value to publish once the tile's Adam tasks finish
+  } grp;
+  bool group() const { return grp.n >= 2; }
+
   // stats
   mt_step_stats stats{};
   mt::LaunchStats ls;
@@ -516,6 +573,7 @@ void worker_fail(mt_model* m, const MtError& e) {
     }
     m->abort_flag = true;
   }
+  if (m->group()) astore(&m->grp.h->failed, 1);  // the other replicas' waits fail too
   m->cv.notify_all();
 }
 
@@ -583,6 +641,66 @@ void set_flag(mt_model* m, std::vector<char>& vec, int i) {
   m->cv.notify_all();
 }
 
+// ------------------------------------------------------------------ replica group waits and turns
+// Bounded poll of a condition in the shared control block; fails at once when
+// another replica has failed or this replica's step was aborted.
+template <class F>
+void group_wait(mt_model* m, F ready, const char* what) {
+  const auto t0 = Clock::now();
+  for (int spin = 0; !ready(); ++spin) {
+    if (aload(&m->grp.h->failed))
+      throw MtError{MT_EINTERNAL, std::string("another replica of the group failed (waiting for ") + what + ")"};
+    check_abort(m);
+    if (ms_since(t0) > (double)m->cfg.timeout_ms)
+      throw MtError{MT_ETIMEDOUT, std::string("timed out waiting for ") + what};
+    if (spin < 64) std::this_thread::yield();
+    else std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+void group_set_nonfinite(mt_model* m) {
+  m->nonfinite = true;
+  if (m->group()) astore(&m->grp.h->nonfinite_step, m->grp.s + 1);
+}
+
+// Whether this step has seen a non-finite value on this replica or, in a
+// group, on any replica whose contribution this one has waited for.
+bool step_nonfinite(mt_model* m) {
+  return m->nonfinite || (m->group() && aload(&m->grp.h->nonfinite_step) == m->grp.s + 1);
+}
+
+int64_t* group_chunk_turn(mt_model* m, int tile, int64_t off) {
+  return m->grp.turn + m->grp.chunk_base[tile] + off / m->slab_bytes;
+}
+
+// Replica r may write a gradient chunk of step s once the chunk's counter reads
+// s * n + r (replicas 0 .. r-1 have added theirs); it then sets s * n + r + 1.
+void group_take_turn(mt_model* m, int64_t* slot) {
+  const int64_t want = m->grp.s * m->grp.n + m->grp.rank;
+  group_wait(m, [&] { return aload(slot) >= want; }, "the previous replica's gradient chunk");
+  if (aload(slot) != want) throw MtError{MT_EINTERNAL, "replica group: a gradient turn counter is ahead of this step"};
+}
+
+void group_pass_turn(mt_model* m, int64_t* slot) {
+  astore(slot, m->grp.s * m->grp.n + m->grp.rank + 1);
+}
+
+// Last replica: every Adam task of `tile` for this step has been submitted;
+// publish the tile's update once they have finished.
+void group_tile_final(mt_model* m, int tile) {
+  std::lock_guard<std::mutex> g(m->adam_mu);
+  if (m->adam_pending[tile] == 0) astore(&m->grp.adam_done[tile], m->grp.s + 1);
+  else m->grp.final_val[tile] = m->grp.s + 1;
+}
+
+// Wait until the last replica has published the update of `tile` (-1: every
+// tile) for the steps before group step v.
+void group_wait_adam(mt_model* m, int tile, int64_t v) {
+  const int lo = tile < 0 ? 0 : tile, hi = tile < 0 ? (int)m->tiles.size() : tile + 1;
+  for (int t = lo; t < hi; ++t)
+    group_wait(m, [&] { return aload(&m->grp.adam_done[t]) >= v; }, "the Adam update of a tile (last replica)");
+}
+
 // Multi-threaded pageable -> pinned copy (the JIT packer).
 void pack_copy(mt_model* m, uint8_t* dst, const uint8_t* src, int64_t n) {
   const int nt = m->pack_pool->size();
@@ -611,7 +729,13 @@ void submit_adam_task(mt_model* m, int tile, std::function<void()> fn) {
         NvtxRange range("adam (tile %d)", tile);
         fn();
         std::lock_guard<std::mutex> g(m->adam_mu);
-        if (--m->adam_pending[tile] == 0) m->adam_cv.notify_all();
+        if (--m->adam_pending[tile] == 0) {
+          m->adam_cv.notify_all();
+          if (m->group() && m->grp.final_val[tile]) {
+            astore(&m->grp.adam_done[tile], m->grp.final_val[tile]);
+            m->grp.final_val[tile] = 0;
+          }
+        }
       },
       tile);
 }
@@ -633,9 +757,10 @@ void wait_adam(mt_model* m, int tile) {
 // tasks (tile, or -1 for all).  A failure of a task that ran after its step
 // returned is reported by the next waiting call that can fail.
 int settle_adam(mt_model* m, int tile, bool report_failure) {
-  if (!m->async_adam) return MT_OK;
+  if (!m->async_adam && !m->group()) return MT_OK;
   try {
-    wait_adam(m, tile);
+    if (m->group()) group_wait_adam(m, tile, m->grp.s);
+    else wait_adam(m, tile);
   } catch (const MtError& e) {
     m->err = e.msg;
     m->broken = true;
@@ -654,11 +779,13 @@ void loader_main(mt_model* m) {
   cudaSetDevice(m->device);
   int64_t gen = 0;
   while (true) {
+    int64_t gs = 0;  // group step of this step
     {
       std::unique_lock<std::mutex> g(m->mu);
       m->cv.wait(g, [&] { return m->stop_threads || m->step_gen > gen; });
       if (m->stop_threads) return;
       gen = m->step_gen;
+      gs = m->grp.s;
     }
     try {
       int si = 0;
@@ -679,7 +806,8 @@ void loader_main(mt_model* m) {
           wait_flag(m, m->rec_free, x.prev_user, "buffer free");
           MT_CK(cudaStreamWaitEvent(m->s_h2d, m->ev_free[x.prev_user], 0));
         }
-        if (m->async_adam) wait_adam(m, x.tile);  // the previous step's update of this tile
+        if (m->group()) group_wait_adam(m, x.tile, gs);  // the previous step's update, on the last replica
+        else if (m->async_adam) wait_adam(m, x.tile);  // the previous step's update of this tile
         MT_CK(cudaEventRecord(m->ev_h2d_a[v], m->s_h2d));
         const TileLayout& lay = m->layouts[x.tile];
         const uint8_t* src = m->tiles[x.tile] + lay.off_w;
@@ -960,15 +1088,21 @@ void accum_main(mt_model* m) {
       if (inject_now(m, MT_INJECT_ACCUM_FAIL, j.visit)) throw injected("accumulator", j.visit);
       const bool head = m->visits[j.visit].kind == kHead;
       if (head && j.off == 0) {
-        if (!std::isfinite(m->pinned_scalars[0])) m->nonfinite = true;
+        if (!std::isfinite(m->pinned_scalars[0])) group_set_nonfinite(m);
         if (!m->tied) submit_untouched_embed(m);
       }
       if (j.rows) {
+        // replica group: the rows of replica r add once replicas 0 .. r-1 have added all of theirs
+        if (m->group()) group_take_turn(m, &m->grp.h->emb_turn);
         std::atomic<bool> fin{true};
         accumulate_embed_rows(m, j, fin, m->tied || m->micro_index > 0);
         if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
-        if (!fin) m->nonfinite = true;
-        if (!m->nonfinite && m->last_pass()) {
+        if (!fin) group_set_nonfinite(m);
+        if (m->group() && j.last) {
+          if (m->grp.rank == 0) wait_adam(m, 0);  // the zeroed rows that no token of this replica uses
+          group_pass_turn(m, &m->grp.h->emb_turn);
+        }
+        if (!step_nonfinite(m) && m->last_pass()) {
           if (m->micro_count == 1) {
             submit_adam_embed_rows(m, j.tile, j.off / (2LL * m->D.d), j.bytes / (2LL * m->D.d));
           } else if (j.last) {  // every row may have been touched by some micro-batch: one dense update
@@ -980,6 +1114,7 @@ void accum_main(mt_model* m) {
             }
           }
         }
+        if (m->group() && j.last && m->last_pass()) group_tile_final(m, j.tile);
         {
           std::lock_guard<std::mutex> g(m->mu);
           m->free_slabs.push_back(j.slab);
@@ -992,9 +1127,11 @@ void accum_main(mt_model* m) {
         continue;
       }
       const TileLayout& lay = m->layouts[j.tile];
+      int64_t* turn = m->group() ? group_chunk_turn(m, j.tile, j.off) : nullptr;
+      if (turn) group_take_turn(m, turn);
       if (j.direct) {
         // already in the tile; the device flag (copied before the chunks) says whether it is finite
-        if (m->pinned_flags[j.visit]) m->nonfinite = true;
+        if (m->pinned_flags[j.visit]) group_set_nonfinite(m);
       } else {
         uint16_t* dst = reinterpret_cast<uint16_t*>(m->tiles[j.tile] + lay.off_g + j.off);
         const uint16_t* src = reinterpret_cast<const uint16_t*>(m->slabs[j.slab]);
@@ -1013,14 +1150,15 @@ void accum_main(mt_model* m) {
           });
         }
         if (!m->acc_pool->wait_idle(m->cfg.timeout_ms)) throw MtError{MT_ETIMEDOUT, "gradient accumulation timed out"};
-        if (!fin) m->nonfinite = true;
+        if (!fin) group_set_nonfinite(m);
       }
+      if (turn) group_pass_turn(m, turn);
       {
         std::lock_guard<std::mutex> g(m->mu);
         m->free_slabs.push_back(j.slab);
       }
       m->cv.notify_all();
-      if (!m->nonfinite && m->last_pass()) {
+      if (!step_nonfinite(m) && m->last_pass()) {
         if (inject_now(m, MT_INJECT_ADAM_FAIL, j.visit)) {
           const int v = j.visit;
           submit_adam_task(m, j.tile, [m, v] { worker_fail(m, injected("Adam", v)); });
@@ -1032,6 +1170,7 @@ void accum_main(mt_model* m) {
           submit_tied_head_adam(m);
         }
       }
+      if (m->group() && j.last && m->last_pass()) group_tile_final(m, j.tile);
       if (j.last) {
         {
           std::lock_guard<std::mutex> g(m->mu);
@@ -1113,6 +1252,22 @@ bf16* x_fwd_loc(mt_model* m, int i) {
   return (i < m->keep_from && i % m->K == 0) ? m->ckpt[i / m->K] : m->xtmp[i % 2];
 }
 
+// Replica group, once this replica's gradients are all in the shared tiles:
+// wait for every replica to get there, then take the global loss (the
+// replicas' scaled losses summed in rank order, as mt_train_step_micro sums
+// its micro-batches) and the group's non-finite verdict for the step.
+void group_finish_step(mt_model* m) {
+  auto& g = m->grp;
+  const int64_t s = g.s;
+  g.h->loss[s & 1][g.rank] = m->pinned_scalars[0];
+  aadd(&g.h->steps_done, (int64_t)1);
+  group_wait(m, [&] { return aload(&g.h->steps_done) >= (s + 1) * g.n; }, "every replica to finish the step");
+  float loss = 0.f;
+  for (int r = 0; r < g.n; ++r) loss += g.h->loss[s & 1][r];
+  m->pinned_scalars[0] = loss;
+  if (aload(&g.h->nonfinite_step) == s + 1) m->nonfinite = true;
+}
+
 int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev, size_t n_tokens, float* loss_out) {
   const Dims& D = m->D;
   if (m->broken) {
@@ -1124,10 +1279,15 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
     return MT_EINVAL;
   }
   for (size_t t = 0; t < m->tiles.size(); ++t)
-    if (!m->w_loaded[t]) {
+    if (!(m->group() ? aload(&m->grp.loaded[t]) != 0 : m->w_loaded[t] != 0)) {
       m->err = "tile " + std::to_string(t) + " has no weights loaded";
       return MT_ESTATE;
     }
+  if (m->group() && aload(&m->grp.h->failed)) {
+    m->err = "a replica of the group failed; the group is unusable";
+    m->broken = true;
+    return MT_ESTATE;
+  }
   const auto wall0 = Clock::now();
   int code = MT_OK;
   try {
@@ -1166,7 +1326,7 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       m->d2h_q.clear();
       m->acc_q.clear();
     }
-    if (m->micro_index == 0) m->nonfinite = false;
+    if (m->micro_index == 0 || m->group()) m->nonfinite = false;
     m->adam_us = 0;
     m->ls = LaunchStats{};
     m->ls.time_gemms = m->time_kernels;
@@ -1339,10 +1499,12 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
       if (!ok) throw MtError{MT_ETIMEDOUT, "timed out waiting for gradient accumulation"};
     }
     const auto t_grads_done = Clock::now();
+    if (m->group()) group_finish_step(m);
     // MT_ASYNC_ADAM: the step returns with Adam tasks still running; each
     // tile's finish before it is uploaded again or read through the API
     if (!m->async_adam && !m->adam_pool->wait_idle(m->cfg.timeout_ms))
       throw MtError{MT_ETIMEDOUT, "timed out waiting for Adam"};
+    if (m->group() && !m->async_adam) group_wait_adam(m, -1, m->grp.s + 1);
     const auto adam_end = Clock::now();
     check_abort(m);
     MT_CK(cudaStreamSynchronize(m->s_h2d));
@@ -1422,7 +1584,8 @@ int run_step(mt_model* m, const int32_t* tokens_host, const int32_t* tokens_dev,
         throw MtError{MT_EINVAL, "device status " + std::to_string(status) + " (index out of range)"};
       }
     }
-    if (m->last_pass()) m->step += 1;
+    if (m->last_pass() || m->group()) m->step += 1;
+    if (m->group()) m->grp.s += 1;
     st.step = m->step;
     st.step_ms = ms_since(wall0);
     auto span = [](Clock::time_point a, Clock::time_point b) {
@@ -1481,6 +1644,20 @@ const char* validate(const mt_config& c) {
       return "mlp_chunk_rows does not apply to MoE layers";
   }
   if (c.keep_layers < 0) return "keep_layers must be >= 0";
+  if (c.n_replicas < 0 || c.n_replicas > kMaxReplicas) return "n_replicas must be in 0 .. 64";
+  if (c.n_replicas >= 2) {
+    if (c.replica_rank < 0 || c.replica_rank >= c.n_replicas) return "replica_rank must be in 0 .. n_replicas - 1";
+    const size_t len = strnlen(c.replica_name, sizeof(c.replica_name));
+    if (len == 0 || len == sizeof(c.replica_name)) return "replica_name must be a non-empty NUL-terminated name";
+    for (size_t i = 0; i < len; ++i) {
+      const char ch = c.replica_name[i];
+      if (!((ch >= 'a' && ch <= 'z') || (ch >= 'A' && ch <= 'Z') || (ch >= '0' && ch <= '9') || ch == '_' ||
+            ch == '-' || ch == '.'))
+        return "replica_name may hold letters, digits, '_', '-' and '.' only";
+    }
+    if (c.flags & MT_RESIDENT) return "a replica group streams its weights: MT_RESIDENT does not apply";
+    if (c.flags & MT_TIE_EMBEDDINGS) return "a replica group does not support MT_TIE_EMBEDDINGS";
+  }
   if (c.mlp_chunk_rows > 0 && c.mlp_chunk_rows < (int64_t)c.batch * c.seq &&
       ((c.flags & MT_STORE_ACTS) || c.keep_layers > 0))
     return "a chunked MLP keeps no per-layer gate/up activations: not combinable with MT_STORE_ACTS or keep_layers";
@@ -1587,6 +1764,110 @@ void parallel_zero(uint8_t* p, int64_t n, int nthreads) {
   for (auto& t : th) t.join();
 }
 
+// Replica group: map the shared segment (control block, then every tile on a
+// page boundary) and point the tiles into it.  Replica 0 creates it (fresh
+// shared memory reads as zeros, so the tiles start zeroed) and removes the
+// name once all n replicas have attached; the others open it once it exists
+// with the expected size and its control block is marked ready.
+void group_attach(mt_model* m) {
+  auto& g = m->grp;
+  const mt_config& c = m->cfg;
+  const int rank = c.replica_rank, n = c.n_replicas;  // the handle's group fields are set once attached
+  const int64_t nt = (int64_t)m->layouts.size();
+  g.chunk_base.assign(nt + 1, 0);
+  for (int64_t t = 0; t < nt; ++t)
+    g.chunk_base[t + 1] = g.chunk_base[t] + (m->layouts[t].w_bytes + m->slab_bytes - 1) / m->slab_bytes;
+  const int64_t n_chunks = g.chunk_base[nt];
+  const int64_t head = align_up((int64_t)sizeof(GroupHeader) + 8 * n_chunks + 12 * nt, kPage);
+  std::vector<int64_t> tile_off(nt);
+  int64_t total = head;
+  for (int64_t t = 0; t < nt; ++t) {
+    tile_off[t] = total;
+    total += align_up(m->layouts[t].tile_bytes, kPage);
+  }
+  const std::string name = std::string("/") + c.replica_name;
+  const auto t0 = Clock::now();
+  auto expired = [&] { return ms_since(t0) > (double)c.timeout_ms; };
+  int fd = -1;
+  if (rank == 0) {
+    shm_unlink(name.c_str());  // a leftover of a group that never finished attaching
+    fd = shm_open(name.c_str(), O_CREAT | O_EXCL | O_RDWR, 0600);
+    if (fd < 0) throw MtError{MT_ENOMEM, "shm_open(" + name + "): " + std::strerror(errno)};
+    if (ftruncate(fd, (off_t)total) != 0) {
+      const int e = errno;
+      close(fd);
+      shm_unlink(name.c_str());
+      throw MtError{MT_ENOMEM, "sizing the replica group's shared memory to " + std::to_string(total) +
+                                   " bytes: " + std::strerror(e)};
+    }
+  } else {
+    while (true) {
+      fd = shm_open(name.c_str(), O_RDWR, 0);
+      if (fd >= 0) {
+        struct stat st {};
+        if (fstat(fd, &st) == 0 && st.st_size == (off_t)total) break;
+        close(fd);
+        fd = -1;
+      }
+      if (expired())
+        throw MtError{MT_ETIMEDOUT, "replica " + std::to_string(rank) + ": no shared segment " + name + " of " +
+                                        std::to_string(total) + " bytes appeared (is replica 0 running with the "
+                                        "same config?)"};
+      std::this_thread::sleep_for(std::chrono::milliseconds(1));
+    }
+  }
+  void* p = mmap(nullptr, (size_t)total, PROT_READ | PROT_WRITE, MAP_SHARED, fd, 0);
+  const int map_errno = errno;
+  close(fd);
+  if (p == MAP_FAILED) {
+    if (rank == 0) shm_unlink(name.c_str());
+    throw MtError{MT_ENOMEM, std::string("mapping the replica group's shared memory: ") + std::strerror(map_errno)};
+  }
+  g.base = static_cast<uint8_t*>(p);
+  g.bytes = (size_t)total;
+  g.h = reinterpret_cast<GroupHeader*>(g.base);
+  g.turn = reinterpret_cast<int64_t*>(g.base + sizeof(GroupHeader));
+  g.adam_done = g.turn + n_chunks;
+  g.loaded = reinterpret_cast<int32_t*>(g.adam_done + nt);
+  g.final_val.assign(nt, 0);
+  GroupHeader* h = g.h;
+  if (rank == 0) {
+    h->total_bytes = total;
+    h->n_chunks = n_chunks;
+    h->slab_bytes = m->slab_bytes;
+    h->n_tiles = nt;
+    h->n_replicas = n;
+    h->magic = kGroupMagic;
+    astore(&h->ready, 1);
+  } else {
+    while (!aload(&h->ready)) {
+      if (expired()) throw MtError{MT_ETIMEDOUT, "replica group: the control block was never marked ready"};
+      std::this_thread::sleep_for(std::chrono::milliseconds(1));
+    }
+    if (h->magic != kGroupMagic || h->total_bytes != total || h->n_chunks != n_chunks ||
+        h->slab_bytes != m->slab_bytes || h->n_tiles != nt || h->n_replicas != n)
+      throw MtError{MT_EINVAL, "replica group: this replica's config differs from replica 0's"};
+  }
+  if (aadd(&h->attached, 1) > n)
+    throw MtError{MT_EINVAL, "replica group: more replicas attached than n_replicas (a reused replica_name?)"};
+  if (rank == 0) {
+    while (aload(&h->attached) < n) {
+      if (expired()) {
+        shm_unlink(name.c_str());
+        throw MtError{MT_ETIMEDOUT, "replica group: only " + std::to_string(aload(&h->attached)) + " of " +
+                                        std::to_string(n) + " replicas attached"};
+      }
+      std::this_thread::sleep_for(std::chrono::milliseconds(1));
+    }
+    shm_unlink(name.c_str());
+  }
+  for (int64_t t = 0; t < nt; ++t) m->tiles[t] = g.base + tile_off[t];
+  m->micro_index = rank;  // replica r adds its gradients as micro-batch r of the group's step
+  m->micro_count = n;
+  g.rank = rank;
+  g.n = n;
+}
+
 void destroy(mt_model* m) {
   if (!m) return;
   {
@@ -1609,8 +1890,9 @@ void destroy(mt_model* m) {
     // work may still be running against the pinned buffers: leak them rather than free memory in use
     std::fprintf(stderr, "mt_free: streams still busy after %lld ms; pinned buffers are leaked\n",
                  (long long)m->cfg.timeout_ms);
-    for (size_t t = 0; t < m->tiles.size(); ++t)  // page-locked tiles are leaked with them
-      if (t >= m->host_reg.size() || !m->host_reg[t]) std::free(m->tiles[t]);
+    if (!m->grp.base)
+      for (size_t t = 0; t < m->tiles.size(); ++t)  // page-locked tiles are leaked with them
+        if (t >= m->host_reg.size() || !m->host_reg[t]) std::free(m->tiles[t]);
     delete m;
     return;
   }
@@ -1648,7 +1930,11 @@ void destroy(mt_model* m) {
   if (m->pinned_flags) cudaFreeHost(m->pinned_flags);
   for (uint8_t* r : m->host_reg)
     if (r) cudaHostUnregister(r);
-  for (auto t : m->tiles) std::free(t);
+  if (m->grp.base) {
+    munmap(m->grp.base, m->grp.bytes);
+  } else {
+    for (auto t : m->tiles) std::free(t);
+  }
   delete m;
 }
 
@@ -1726,17 +2012,21 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   // host tiles: pageable, page aligned, zeroed (first touch spread over threads)
   m->tiles.assign(m->layouts.size(), nullptr);
   m->w_loaded.assign(m->layouts.size(), 0);
-  for (size_t t = 0; t < m->layouts.size(); ++t) {
-    m->tiles[t] = static_cast<uint8_t*>(std::aligned_alloc(kPage, (size_t)m->layouts[t].tile_bytes));
-    if (!m->tiles[t]) throw MtError{MT_ENOMEM, "host tile allocation failed"};
-    parallel_zero(m->tiles[t], m->layouts[t].tile_bytes, std::min(16, m->cfg.n_adam_threads));
+  m->slab_bytes = std::min<int64_t>(m->cfg.grad_slab_bytes, m->max_w_bytes);
+  if (m->cfg.n_replicas >= 2) {
+    group_attach(m);
+  } else {
+    for (size_t t = 0; t < m->layouts.size(); ++t) {
+      m->tiles[t] = static_cast<uint8_t*>(std::aligned_alloc(kPage, (size_t)m->layouts[t].tile_bytes));
+      if (!m->tiles[t]) throw MtError{MT_ENOMEM, "host tile allocation failed"};
+      parallel_zero(m->tiles[t], m->layouts[t].tile_bytes, std::min(16, m->cfg.n_adam_threads));
+    }
   }
   // pinned staging, slabs, scalars, token buffers
   m->stage_bytes = std::min<int64_t>(m->cfg.stage_bytes, m->max_w_bytes);
   for (auto& s : m->stage)
     if (cudaHostAlloc(reinterpret_cast<void**>(&s), (size_t)m->stage_bytes, cudaHostAllocDefault) != cudaSuccess)
       throw MtError{MT_ENOMEM, "pinned staging allocation failed"};
-  m->slab_bytes = std::min<int64_t>(m->cfg.grad_slab_bytes, m->max_w_bytes);
   m->slabs.assign(m->cfg.n_grad_slabs, nullptr);
   m->ev_slab.assign(m->cfg.n_grad_slabs, nullptr);
   for (int i = 0; i < m->cfg.n_grad_slabs; ++i) {
@@ -1868,10 +2158,12 @@ int mt_init_model(const mt_config* cfg, void* device_arena, size_t arena_bytes, 
     mt::init_model(m, *cfg, device_arena, arena_bytes, stream_comp, stream_h2d, stream_d2h);
   } catch (const MtError& e) {
     mt::g_init_error = e.msg;
+    if (m->grp.h) mt::astore(&m->grp.h->failed, 1);  // the other replicas stop waiting for this one
     mt::destroy(m);
     return e.code;
   } catch (const std::exception& e) {
     mt::g_init_error = e.what();
+    if (m->grp.h) mt::astore(&m->grp.h->failed, 1);
     mt::destroy(m);
     return MT_EINTERNAL;
   }
@@ -1938,7 +2230,10 @@ int mt_load_layer_tile(mt_model* m, int tile, int part, const void* src, size_t 
   }
   if (int rc = mt::settle_adam(m, tile, false)) return rc;
   std::memcpy(m->tiles[tile] + off, src, (size_t)n);
-  if (part == MT_PART_W) m->w_loaded[tile] = 1;
+  if (part == MT_PART_W) {
+    m->w_loaded[tile] = 1;
+    if (m->group()) mt::astore(&m->grp.loaded[tile], 1);
+  }
   return MT_OK;
 }
 
@@ -1964,8 +2259,18 @@ int mt_train_step_device_tokens(mt_model* m, const int32_t* tokens_dev, size_t n
   return mt::run_step(m, nullptr, tokens_dev, n_tokens, loss_out);
 }
 
+namespace {
+// Entry points whose accumulation or update pattern a replica group does not have.
+int refuse_in_group(mt_model* m, const char* what) {
+  m->err = std::string(what) + " is not available to a replica of a group (each group step is one mt_train_step "
+                               "on every replica)";
+  return MT_ESTATE;
+}
+}  // namespace
+
 int mt_train_step_grads(mt_model* m, const int32_t* tokens, size_t n_tokens, float* loss_out) {
   if (!m || !tokens) return MT_EINVAL;
+  if (m->group()) return refuse_in_group(m, "mt_train_step_grads");
   m->grads_only = true;
   const int code = mt::run_step(m, tokens, nullptr, n_tokens, loss_out);
   m->grads_only = false;
@@ -1975,6 +2280,7 @@ int mt_train_step_grads(mt_model* m, const int32_t* tokens, size_t n_tokens, flo
 int mt_apply_adam(mt_model* m) {
   using namespace mt;
   if (!m) return MT_EINVAL;
+  if (m->group()) return refuse_in_group(m, "mt_apply_adam");
   if (m->broken) {
     m->err = "handle is unusable after an earlier CUDA or internal error: " + m->err;
     return MT_ESTATE;
@@ -1992,6 +2298,7 @@ int mt_apply_adam(mt_model* m) {
 
 int mt_train_step_micro(mt_model* m, const int32_t* tokens, size_t n_tokens, int32_t n_micro, float* loss_out) {
   if (!m || !tokens || n_micro < 1) return MT_EINVAL;
+  if (m->group()) return refuse_in_group(m, "mt_train_step_micro");
   const size_t per = (size_t)m->D.B * (m->D.S + 1);
   if (n_tokens != per * (size_t)n_micro) {
     m->err = "n_tokens must equal n_micro * batch * (seq + 1)";
@@ -2097,6 +2404,22 @@ int mt_get_step_stats(const mt_model* m, mt_step_stats* out) {
 }
 
 int64_t mt_get_step(const mt_model* m) { return m ? m->step : MT_EINVAL; }
+
+int mt_replica_barrier(mt_model* m) {
+  using namespace mt;
+  if (!m) return MT_EINVAL;
+  if (!m->group()) return MT_OK;
+  try {
+    const int64_t k = ++m->grp.barriers;
+    GroupHeader* h = m->grp.h;
+    aadd(&h->barrier_count, (int64_t)1);
+    group_wait(m, [&] { return aload(&h->barrier_count) >= k * m->grp.n; }, "every replica to reach the barrier");
+  } catch (const MtError& e) {
+    m->err = e.msg;
+    return e.code;
+  }
+  return MT_OK;
+}
 
 int mt_set_step(mt_model* m, int64_t step) {
   if (!m || step < 0) return MT_EINVAL;

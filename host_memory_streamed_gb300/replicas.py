@@ -1,48 +1,57 @@
-"""Data-parallel replicas with a host-side gradient sum.
+"""Data-parallel replicas of one model, one process per GPU, summed on the host.
 
-One process per GPU, each with its own ``StreamedDecoder`` and its own share of
-the global batch (equal token counts).  A replica step is
+The MegaTrain pages leave several GPUs as future work (author's blog, planned
+projects).  Here every replica is a ``StreamedDecoder`` opened with
+``replica_group=(name, rank, n)``: the n processes map one shared-memory
+segment that holds the host tiles (W, G, M, V exist once), each streams the
+weights from it and trains on its own batch, and the runtime's accumulator
+adds each replica's gradient chunks into the shared G in rank order, the last
+replica running Adam on every chunk as soon as its sum is complete, while the
+backward goes on (paperlayer.ai summary §A.3, background accumulator over the
+gradient slabs).  No collective runs on the data path, and no GPU reads
+another's memory.
 
-  1. ``train_step_grads``: forward and backward of the local batch; every host
-     tile's G section holds the BF16 gradient of the local mean loss;
-  2. the gradients of all replicas are averaged on the host, tile by tile
-     (``torch.distributed`` all-reduce of FP32 copies over the given process
-     group, gloo on the host), and written back into each tile's G;
-  3. ``apply_adam``: every replica applies the same Adam step to the same
-     averaged gradient, so the replicas' weights stay identical.
+A group step is one ``train_step`` on every replica; it returns the loss of
+the global batch (the mean over every replica's tokens) on each.  The result
+equals ``train_step_micro`` of one model over the replicas' batches stacked in
+rank order, bit for bit.
 
-The mean over replicas of the local mean losses' gradients is the gradient of
-the mean loss over the global batch.  This is the host-side gradient sum that
-the MegaTrain pages leave as future work for several GPUs (one GPU per
-process; no device-side collective, no peer access between GPUs).
+    name = replicas.group_name()      # made once, handed to every process
+    m = replicas.open_replica(shape, name, rank, n)
+    if rank == 0:
+        m.load_weights(params)        # the tiles are shared: one replica writes
+    m.barrier()
+    loss = m.train_step(local_tokens)
 """
 from __future__ import annotations
 
-import torch
-import torch.distributed as dist
+import os
+import secrets
 
-from ._lib import MT_PART_G
-
-
-def allreduce_mean_bf16_(raw: torch.Tensor, group=None) -> None:
-    """In place: the BF16 values held in the uint8 buffer ``raw`` become the
-    mean over the group's ranks, summed in FP32 and rounded to BF16 once."""
-    bf = raw.view(torch.bfloat16)
-    acc = bf.to(torch.float32)
-    dist.all_reduce(acc, op=dist.ReduceOp.SUM, group=group)
-    acc /= dist.get_world_size(group)
-    bf.copy_(acc.to(torch.bfloat16))
+from . import StreamedDecoder
 
 
-def replica_step(model, tokens: torch.Tensor, group=None) -> float:
-    """One data-parallel step of this replica on its local ``tokens``; returns
-    the mean loss over all replicas' tokens (the same value on every rank)."""
-    loss = model.train_step_grads(tokens)
-    for i in range(model.n_tiles):
-        g = model.get_tile(i, MT_PART_G)
-        allreduce_mean_bf16_(g, group)
-        model.load_tile(i, MT_PART_G, g)
-    model.apply_adam()
-    t = torch.tensor([loss], dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
-    return float(t) / dist.get_world_size(group)
+def group_name(prefix: str = "mt-group") -> str:
+    """A shared-memory name for a new group (unique per call); pass it to
+    every replica.  Replica 0 removes the name once all have attached."""
+    return f"{prefix}-{os.getpid()}-{secrets.token_hex(6)}"
+
+
+def shared_group_name(prefix: str = "mt-group", group=None) -> str:
+    """``group_name`` made on rank 0 of an initialised torch.distributed
+    process group and broadcast to its ranks (host-side agreement only)."""
+    import torch.distributed as dist
+    obj = [group_name(prefix) if dist.get_rank(group) == 0 else None]
+    dist.broadcast_object_list(obj, src=0, group=group)
+    return obj[0]
+
+
+def open_replica(shape, name: str, rank: int, n: int, **kw) -> StreamedDecoder:
+    """Replica ``rank`` of ``n`` of the model ``shape``; returns once all n
+    replicas have attached to the group ``name``."""
+    return StreamedDecoder.from_shape(shape, replica_group=(name, rank, n), **kw)
+
+
+def replica_step(model: StreamedDecoder, tokens) -> float:
+    """One group step on this replica's ``tokens``; the global batch's loss."""
+    return model.train_step(tokens)

@@ -163,6 +163,36 @@ typedef struct {
                                 >= n_layers = every layer kept (as MT_STORE_ACTS).  Each kept layer adds
                                 its stored set to mt_required_device_bytes.  Not combinable with
                                 mlp_chunk_rows. */
+  int32_t replica_rank;      /* replica group: this process's rank, 0 .. n_replicas - 1 */
+  int32_t n_replicas;        /* 0 or 1: a model of its own.  2 .. 64: one of n_replicas data-parallel
+                                replicas of ONE model, one process per GPU, each training on its own
+                                batch of batch x seq tokens (the future multi-GPU work of the MegaTrain
+                                pages: author's blog, planned projects).  The replicas map one
+                                shared-memory segment (replica_name) that holds every host tile, so W,
+                                M and V exist once on the host.  Each replica streams the weights from
+                                it; its gradient chunks are summed into the shared G in rank order,
+                                replica r adding a chunk once replicas 0 .. r-1 have added theirs, with
+                                each replica's cross-entropy scaled by 1 / n_replicas: the additions of
+                                mt_train_step_micro with micro-batch r = replica r, so the result is that
+                                call's bit for bit.  The last replica runs Adam on each chunk as it
+                                completes (paperlayer.ai summary §A.3: a background accumulator drains
+                                the gradient slabs and the CPU update overlaps the backward); every
+                                replica's next upload of a tile waits for its update.  mt_train_step
+                                returns the loss of the global batch (every replica's mean, averaged)
+                                on every replica, after all have finished the step, and MT_ENONFINITE on
+                                every replica if any saw a non-finite value.  Every replica calls
+                                mt_init_model with the same config apart from replica_rank;
+                                mt_init_model returns once all have attached.  Tiles are written
+                                (mt_load_layer_tile) by one replica while no step runs, and read
+                                (mt_get_layer_tile) while no replica runs a step: the replicas meet at
+                                mt_replica_barrier.  A failure on
+                                one replica makes the others' waits fail (MT_EINTERNAL) and leaves every
+                                handle of the group unusable.  Not combinable with MT_RESIDENT or
+                                MT_TIE_EMBEDDINGS; mt_train_step_micro, mt_train_step_grads and
+                                mt_apply_adam return MT_ESTATE. */
+  char replica_name[48];     /* the group's shared-memory name (letters, digits, '_', '-', '.'; NUL
+                                terminated), new for each group: replica 0 creates the segment and
+                                removes the name once every replica has attached */
 } mt_config;
 
 typedef struct mt_model mt_model;
@@ -400,6 +430,16 @@ int64_t mt_get_timeline(const mt_model* m, mt_interval* out, int64_t cap);
 int mt_sync(mt_model* m);
 int64_t mt_get_step(const mt_model* m);       /* Adam step counter t (0 before the first step) */
 int mt_set_step(mt_model* m, int64_t step);  /* for resume */
+
+/*
+ * Replica group (mt_config.n_replicas >= 2): return once every replica of the
+ * group has called mt_replica_barrier as many times as this one (bounded by
+ * timeout_ms; MT_EINTERNAL at once if another replica has failed).  Used
+ * between one replica's mt_load_layer_tile calls and the group's first step.
+ * Returns MT_OK at once for a handle that is not in a group.
+ */
+int mt_replica_barrier(mt_model* m);
+
 const char* mt_last_error(const mt_model* m);
 void mt_free(mt_model* m);
 
