@@ -491,6 +491,7 @@ struct TbParams {
   const float* sin_t;
   float sl2;    // scale * log2(e)
   float scale;  // 1/sqrt(hd)
+  int ld_bulk;  // lse/delta rows 16-byte aligned (S % 4 == 0): whole query blocks arrive by bulk copy
   int* status;
 };
 
@@ -572,7 +573,7 @@ struct TkvCfg {
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_Q = OFF_V + TILE;                 // QSTAGES tiles
   static constexpr int OFF_DO = OFF_Q + QSTAGES * TILE;      // QSTAGES tiles
-  static constexpr int OFF_LD = OFF_DO + QSTAGES * TILE;     // [QSTAGES][lse*log2e 128 | delta 128]
+  static constexpr int OFF_LD = OFF_DO + QSTAGES * TILE;     // [QSTAGES][lse 128 | delta 128]
   static constexpr int OFF_BAR = OFF_LD + QSTAGES * 256 * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
 };
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint64_t* dpt_full = bar + 6;   // dP^T of the current block computed
   uint64_t* p_ready = bar + 7;    // P^T stored (256 softmax threads)
   uint64_t* ds_ready = bar + 8;   // dS^T stored (256)
-  uint64_t* ld_ready = bar + 9;   // [2] lse/delta of a block staged (256)
+  uint64_t* ld_ready = bar + 9;   // lse/delta of a ragged block staged by the softmax threads (256)
   uint64_t* acc_full = bar + 13;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 14);
   __shared__ volatile int abort_flag;
@@ -619,8 +620,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
-      mbar_init(&ld_ready[i], kSoftmaxWarps);
     }
+    mbar_init(ld_ready, kSoftmaxWarps);
     mbar_init(st_full, 1);
     mbar_init(dpt_full, 1);
     mbar_init(p_ready, kSoftmaxWarps);
@@ -642,6 +643,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
 
   auto head_of = [&](int it) { return kvh * G + it / per_head; };
   auto q0_of = [&](int it) { return (qb_first + it % per_head) * 128; };
+  // lse and delta of a whole query block come with its Q and dO tiles (bulk
+  // copies); a ragged last block is staged by the softmax threads
+  auto bulk_ld = [&](int q0) { return p.ld_bulk && q0 + 128 <= S; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -660,11 +664,17 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           break;
         }
         const int h = head_of(it), q0 = q0_of(it);
-        mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE);
+        const bool bulk = bulk_ld(q0);
+        mbar_arrive_expect_tx(&qd_full[st], 2 * C::TILE + (bulk ? 1024 : 0));
 #pragma unroll
         for (int i = 0; i < HD / 64; ++i) {
           tma_load_2d(sQ + st * C::TILE + i * C::BOX, &tm_qkv, h * HD + 64 * i, row0 + q0, &qd_full[st]);
           tma_load_2d(sdO + st * C::TILE + i * C::BOX, &tm_do, h * HD + 64 * i, row0 + q0, &qd_full[st]);
+        }
+        if (bulk) {
+          const long idx = ((long)b * p.Hq + h) * S + q0;
+          bulk_load_1d(sLD + st * 256, p.lse + idx, 512, &qd_full[st]);
+          bulk_load_1d(sLD + st * 256 + 128, p.delta + idx, 512, &qd_full[st]);
         }
         pend[st] = (it >> 1) & 1;
       }
@@ -752,22 +762,39 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     const int key = k0 + r;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
+    int staged = 0;  // ragged blocks staged so far (ld_ready's phase)
     for (int it = 0; it < total; ++it) {
       const int st = it & 1;
       const uint32_t ph = it & 1;
       const int h = head_of(it), q0 = q0_of(it);
-      // stage lse (log2 units) and delta of the 128 queries once for all rows
       float* ld = sLD + st * 256;
-      {
+      if (bulk_ld(q0)) {
+        // the block's Q/dO barrier also covers its lse/delta copies
+        if (!mbar_wait_warp(&qd_full[st], (it >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+      } else {
+        // stage lse and delta of the 128 queries once for all rows; queries
+        // past the end get lse = +inf (P = 0) and delta = 0.  The slot's
+        // previous block (it - 2) has been read by every softmax thread: this
+        // thread has seen dP^T of block it - 1, which the MMA warp issues only
+        // after all dS^T of block it - 2 are stored.  No copy targets it: the
+        // TMA fills a slot only for whole blocks.
         const int t = tid & 127, q = q0 + t;
         const long idx = ((long)b * p.Hq + h) * S + q;
         if (tid < 128)
-          ld[t] = q < S ? p.lse[idx] * kLog2eF : INFINITY;
+          ld[t] = q < S ? p.lse[idx] : INFINITY;
         else
           ld[128 + t] = q < S ? p.delta[idx] : 0.f;
+        mbar_arrive_warp(ld_ready);
+        if (!mbar_wait_warp(ld_ready, staged & 1)) {
+          ok = false;
+          break;
+        }
+        ++staged;
       }
-      mbar_arrive_warp(&ld_ready[st]);
-      if (!mbar_wait_warp(&ld_ready[st], (it >> 1) & 1) || !mbar_wait_warp(st_full, ph)) {
+      if (!mbar_wait_warp(st_full, ph)) {
         ok = false;
         break;
       }
@@ -785,7 +812,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l4 = lse4[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float lv[4] = {l4.x * kLog2eF, l4.y * kLog2eF, l4.z * kLog2eF, l4.w * kLog2eF};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c4 * 4 + e;
@@ -1164,6 +1191,8 @@ int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
   p.sin_t = x.rope_sin;
   p.scale = 1.0f / sqrtf((float)HD);
   p.sl2 = p.scale * kLog2eF;
+  p.ld_bulk = x.seq % 4 == 0 && (reinterpret_cast<uintptr_t>(x.lse) & 15) == 0 &&
+              (reinterpret_cast<uintptr_t>(x.delta) & 15) == 0;
   p.status = x.status;
   dim3 g1((x.seq + 127) / 128, x.batch * x.n_kv_heads);
   attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_qkv, tm_do, p);

@@ -189,6 +189,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, in
       : "memory");
 }
 
+// Contiguous copy of `bytes` from global to shared memory, completing on
+// `bar`; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // The same load issued by either CTA of a pair, completing on a barrier that
 // may sit in the peer CTA (`bar` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* desc, int x, int y, uint32_t bar) {
