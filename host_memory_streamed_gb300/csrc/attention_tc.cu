@@ -471,8 +471,10 @@ int launch_attn_fwd_tc(const AttnArgs& x, cudaStream_t s) {
 // The tensor core runs dV_i, S^T_{i+1}, dK_i, dP^T_{i+1} in that order, so
 // each score block is overwritten only after its probabilities were used.
 // dQ kernel: one CTA per (128-query block, query head, batch), streaming
-// 128-key blocks of K and V (2 stages): S = Q K^T (double-buffered in TMEM),
-// dP = dO V^T, dS = P * (dP - delta) -> BF16 over S's columns, dQ += dS K.
+// 128-key blocks of K (3 stages) and V (2 stages): S = Q K^T, dP = dO V^T
+// (two TMEM buffers), dS = P * (dP - delta) -> BF16 over dP's columns,
+// dQ += dS K.  S is released as soon as every softmax thread holds its row in
+// registers, so S_{j+1} and dP_{j+1} run while the softmax works on block j.
 // dK and dQ are scaled by 1/sqrt(hd) and leave through the inverse RoPE
 // rotation when tables are given.
 // ============================================================================
@@ -916,11 +918,11 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   uint64_t* k_empty = bar + 1 + NK;           // [NK]
   uint64_t* v_full = bar + 1 + 2 * NK;        // [NV]
   uint64_t* v_empty = bar + 1 + 2 * NK + NV;  // [NV]
-  uint64_t* s_full = bar + 1 + 2 * NK + 2 * NV;  // [2] S of block j in TMEM buffer j & 1
-  uint64_t* dp_full = bar + 3 + 2 * NK + 2 * NV;
-  uint64_t* sd_read = bar + 4 + 2 * NK + 2 * NV;  // every softmax warp has read its S and dP columns
-  // [2] dS_j stored.  Two barriers: the softmax may finish block j + 1 before
-  // the MMA thread starts waiting for block j (dP_{j+1} is issued first).
+  uint64_t* s_full = bar + 1 + 2 * NK + 2 * NV;   // S of the current block computed
+  uint64_t* s_read = bar + 2 + 2 * NK + 2 * NV;   // every softmax warp holds its S row in registers
+  uint64_t* dp_full = bar + 3 + 2 * NK + 2 * NV;  // [2] dP of block j in TMEM buffer j & 1
+  // [2] dS_j stored (over dP buffer j & 1).  Two barriers: the softmax may
+  // finish block j + 1 before the MMA thread starts waiting for block j.
   uint64_t* ds_ready = bar + 5 + 2 * NK + 2 * NV;
   uint64_t* acc_full = bar + 7 + 2 * NK + 2 * NV;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar + 8 + 2 * NK + 2 * NV);
@@ -946,9 +948,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
-    mbar_init(dp_full, 1);
-    mbar_init(sd_read, kSoftmaxWarps);
+    mbar_init(s_full, 1);
+    mbar_init(s_read, kSoftmaxWarps);
+    for (int i = 0; i < 2; ++i) mbar_init(&dp_full[i], 1);
     mbar_init(&ds_ready[0], kSoftmaxWarps);
     mbar_init(&ds_ready[1], kSoftmaxWarps);
     mbar_init(acc_full, 1);
@@ -964,8 +966,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // TMEM columns: S[2] 0 / 128, dP 256, dQ 384 (HD columns)
-  const uint32_t tDP = tmem + 256, tdQ = tmem + 384;
+  // TMEM columns: S 0, dP[2] 128 / 256 (dS over them), dQ 384 (HD columns)
+  const uint32_t tS = tmem, tdQ = tmem + 384;
+  auto tDP = [&](int j) { return tmem + 128u + 128u * (uint32_t)(j & 1); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1026,33 +1029,30 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       auto issue_s = [&](int j) {
         if (!mbar_wait(&k_full[j % NK], (j / NK) & 1)) return false;
         tc_fence_after();
-        issue_scores(sQ, sK + (j % NK) * C::TILE, tmem + 128u * (uint32_t)(j & 1));
-        tc_commit(&s_full[j & 1]);
+        issue_scores(sQ, sK + (j % NK) * C::TILE, tS);
+        tc_commit(s_full);
         return true;
       };
+      // dP_j into buffer j & 1, whose dS_{j-2} the dQ MMAs issued before have read
       auto issue_dp = [&](int j) {
         if (!mbar_wait(&v_full[j % NV], (j / NV) & 1)) return false;
         tc_fence_after();
-        issue_scores(sdO, sV + (j % NV) * C::TILE, tDP);
-        tc_commit(dp_full);
+        issue_scores(sdO, sV + (j % NV) * C::TILE, tDP(j));
+        tc_commit(&dp_full[j & 1]);
         tc_commit(&v_empty[j % NV]);
         return true;
       };
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < n_kb; ++j) {
-        const uint32_t ph = j & 1;
-        // S_{j+1} into the other buffer, whose dS_{j-1} the dQ MMAs issued before have read
-        if (j + 1 < n_kb && !issue_s(j + 1)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(sd_read, ph)) {
+        // S_{j+1} once every softmax thread holds S_j in registers, dP_{j+1}
+        // into the other buffer: both run while the softmax works on block j
+        if (!mbar_wait(s_read, j & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (j + 1 < n_kb && !issue_dp(j + 1)) {  // dP_{j+1}: every thread has read dP_j
+        if (j + 1 < n_kb && (!issue_s(j + 1) || !issue_dp(j + 1))) {
           ok = false;
           break;
         }
@@ -1061,7 +1061,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t src = tmem + 128u * (uint32_t)(j & 1);
+        const uint32_t src = tDP(j);
         const uint64_t kd = smem_desc_mnmajor_sw128(sK + (j % NK) * C::TILE, C::BOX);
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)  // keys 64.. sit at columns 96..127
@@ -1089,9 +1089,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
     const float Dr = valid ? p.delta[li] : 0.f;
     bool ok = true;
     for (int j = 0; j < n_kb; ++j) {
-      const uint32_t ph = j & 1;
-      const uint32_t tS = tmem + 128u * (uint32_t)(j & 1);
-      if (!mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1)) {
+      const uint32_t tD = tDP(j);
+      if (!mbar_wait_warp(s_full, j & 1)) {
         ok = false;
         break;
       }
@@ -1100,6 +1099,8 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       tmem_ld_32x32b_x32(tS + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
       tmem_ld_32x32b_x32(tS + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
       tmem_wait_ld_regs(sv);
+      tc_fence_before();
+      mbar_arrive_warp(s_read);  // S_{j+1} may overwrite S_j
       // Rows past the sequence end have L2 = +inf (P = 0); only the diagonal
       // block (key block j == query block) needs the key > query mask.
       const int k0 = j * 128;
@@ -1111,7 +1112,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
         if (diag && k0 + hf * 64 + c > qrow) pr = 0.f;
         pf[c] = pr;
       }
-      if (!mbar_wait_warp(dp_full, ph)) {
+      if (!mbar_wait_warp(&dp_full[j & 1], (j >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -1120,7 +1121,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t dp[32];
-        tmem_ld_32x32b_x32(tDP + lane_off + hf * 64 + half * 32, dp);
+        tmem_ld_32x32b_x32(tD + lane_off + hf * 64 + half * 32, dp);
         tmem_wait_ld_regs(dp);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -1128,11 +1129,9 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
           pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[2 * e]) - Dr), pf[c + 1] * (__uint_as_float(dp[2 * e + 1]) - Dr));
         }
       }
-      tc_fence_before();
-      mbar_arrive_warp(sd_read);  // dP_{j+1} may overwrite dP_j once every warp has read it
-      // dS over the first 32 of this half's own 64 S columns (half 0: 0..31,
-      // half 1: 96..127): no other thread reads them, so no barrier
-      tmem_st_packed32(tS + lane_off + hf * 96, pk);
+      // dS over the first 32 of this half's own 64 dP columns (half 0: 0..31,
+      // half 1: 96..127), which this thread has read: no barrier
+      tmem_st_packed32(tD + lane_off + hf * 96, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&ds_ready[j & 1]);
