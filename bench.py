@@ -489,6 +489,8 @@ def main():
     ap.add_argument("--staged-weights", action="store_true",
                     help="weights through the packer's pinned staging chunks (default: each upload's DMA reads "
                          "the page-locked W section of the tile)")
+    ap.add_argument("--adam-threads", type=int, default=0,
+                    help="CPU Adam workers (0: the library's default, 3/4 of the hardware threads)")
     ap.add_argument("--share-device", action="store_true",
                     help="every rank on cuda:0: exercises the N > 1 path on one GPU (the ranks only meet on the "
                          "host); the throughput it prints is not an N-GPU figure")
@@ -551,6 +553,8 @@ def main():
     adam_threads = max(2, (os.cpu_count() or 4) * 3 // 4 // world) if world > 1 else 0
     if group:  # the last replica runs every Adam update of the group
         adam_threads = 0 if rank == world - 1 else 2
+    if args.adam_threads:
+        adam_threads = args.adam_threads
     keep = args.keep_layers
     if keep == "preset":
         keep = "auto" if s.name in KEEP_AUTO_WORKLOADS else 0
