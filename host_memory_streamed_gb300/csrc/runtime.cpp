@@ -519,6 +519,9 @@ struct mt_model {
   // chunks land in them directly; a device check flags non-finite values of
   // each gradient visit (grad_flags, copied to pinned_flags before the chunks)
   bool direct_grads = false;
+  // a model's own host tiles: one anonymous mapping (nullptr in a replica group)
+  uint8_t* tile_map = nullptr;
+  size_t tile_map_bytes = 0;
   // page-locked range of each tile (MT_DIRECT_GRADS: its G section; MT_DIRECT_WEIGHTS: its W
   // section; both: W and G as one range), nullptr where nothing is registered
   std::vector<uint8_t*> host_reg;
@@ -1868,6 +1871,44 @@ void group_attach(mt_model* m) {
   g.n = n;
 }
 
+// Size of a transparent huge page on this host (2 MiB when the kernel does not say).
+int64_t huge_page_bytes() {
+  int64_t v = 0;
+  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+    long long x = 0;
+    if (std::fscanf(f, "%lld", &x) == 1) v = x;
+    std::fclose(f);
+  }
+  return v >= kPage && (v & (v - 1)) == 0 ? v : (2LL << 20);
+}
+
+// Host tiles of a model of its own: one anonymous mapping holding every tile
+// on a page boundary, started on a huge-page boundary and advised for
+// transparent huge pages (where the kernel grants them: fewer translations for
+// the CPU Adam workers' streaming and shorter page lists for the DMA engines'
+// in-place copies).  First touch, which zeroes, is spread over threads.
+void alloc_tiles(mt_model* m) {
+  const int64_t huge = huge_page_bytes();
+  std::vector<int64_t> off(m->layouts.size());
+  int64_t total = 0;
+  for (size_t t = 0; t < m->layouts.size(); ++t) {
+    off[t] = total;
+    total += align_up(m->layouts[t].tile_bytes, kPage);
+  }
+  const size_t map_bytes = (size_t)(total + huge);
+  void* p = mmap(nullptr, map_bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (p == MAP_FAILED)
+    throw MtError{MT_ENOMEM, "host tile allocation of " + std::to_string(total) + " bytes failed"};
+  m->tile_map = static_cast<uint8_t*>(p);
+  m->tile_map_bytes = map_bytes;
+  uint8_t* base = reinterpret_cast<uint8_t*>(align_up((int64_t)reinterpret_cast<uintptr_t>(p), huge));
+  madvise(base, (size_t)total, MADV_HUGEPAGE);  // advisory: a refusal leaves ordinary pages
+  for (size_t t = 0; t < m->layouts.size(); ++t) {
+    m->tiles[t] = base + off[t];
+    parallel_zero(m->tiles[t], m->layouts[t].tile_bytes, std::min(16, m->cfg.n_adam_threads));
+  }
+}
+
 void destroy(mt_model* m) {
   if (!m) return;
   {
@@ -1890,10 +1931,7 @@ void destroy(mt_model* m) {
     // work may still be running against the pinned buffers: leak them rather than free memory in use
     std::fprintf(stderr, "mt_free: streams still busy after %lld ms; pinned buffers are leaked\n",
                  (long long)m->cfg.timeout_ms);
-    if (!m->grp.base)
-      for (size_t t = 0; t < m->tiles.size(); ++t)  // page-locked tiles are leaked with them
-        if (t >= m->host_reg.size() || !m->host_reg[t]) std::free(m->tiles[t]);
-    delete m;
+    delete m;  // the tile mapping (page-locked in parts) is leaked with the buffers
     return;
   }
   auto kill = [](std::vector<cudaEvent_t>& v) {
@@ -1930,11 +1968,8 @@ void destroy(mt_model* m) {
   if (m->pinned_flags) cudaFreeHost(m->pinned_flags);
   for (uint8_t* r : m->host_reg)
     if (r) cudaHostUnregister(r);
-  if (m->grp.base) {
-    munmap(m->grp.base, m->grp.bytes);
-  } else {
-    for (auto t : m->tiles) std::free(t);
-  }
+  if (m->grp.base) munmap(m->grp.base, m->grp.bytes);
+  if (m->tile_map) munmap(m->tile_map, m->tile_map_bytes);
   delete m;
 }
 
@@ -2016,11 +2051,7 @@ void init_model(mt_model* m, const mt_config& cin, void* arena, size_t arena_byt
   if (m->cfg.n_replicas >= 2) {
     group_attach(m);
   } else {
-    for (size_t t = 0; t < m->layouts.size(); ++t) {
-      m->tiles[t] = static_cast<uint8_t*>(std::aligned_alloc(kPage, (size_t)m->layouts[t].tile_bytes));
-      if (!m->tiles[t]) throw MtError{MT_ENOMEM, "host tile allocation failed"};
-      parallel_zero(m->tiles[t], m->layouts[t].tile_bytes, std::min(16, m->cfg.n_adam_threads));
-    }
+    alloc_tiles(m);
   }
   // pinned staging, slabs, scalars, token buffers
   m->stage_bytes = std::min<int64_t>(m->cfg.stage_bytes, m->max_w_bytes);
