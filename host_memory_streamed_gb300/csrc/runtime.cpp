@@ -1828,6 +1828,7 @@ void group_attach(mt_model* m) {
   }
   g.base = static_cast<uint8_t*>(p);
   g.bytes = (size_t)total;
+  madvise(p, (size_t)total, MADV_HUGEPAGE);  // as for a model's own tiles; shared memory may decline
   g.h = reinterpret_cast<GroupHeader*>(g.base);
   g.turn = reinterpret_cast<int64_t*>(g.base + sizeof(GroupHeader));
   g.adam_done = g.turn + n_chunks;
