@@ -205,13 +205,11 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
           return false;
         }
         tc_fence_after();
+        const uint64_t da = smem_desc_kmajor_sw128(sQ), db = smem_desc_kmajor_sw128(sK + s * C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const int box = kk >> 2, off = (kk & 3) * 32;
-          const uint64_t a = smem_desc_kmajor_sw128(sQ + box * C::BOX + off);
-          const uint64_t bb = smem_desc_kmajor_sw128(sK + s * C::KV_BYTES + box * C::BOX + off);
-          tc_mma_bf16(tmem + 128u * (uint32_t)(j & 1), a, bb, id_qk, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma_bf16(tmem + 128u * (uint32_t)(j & 1), da + desc_step(kk, C::BOX), db + desc_step(kk, C::BOX), id_qk,
+                      kk > 0 ? 1u : 0u);
         tc_commit(&s_full[j & 1]);
         return true;
       };
@@ -692,12 +690,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       // S^T (or dP^T with V, dO) of block it into TMEM columns dst
       auto issue_scores = [&](int it, const uint8_t* sA, const uint8_t* sB, uint32_t dst) {
         const int qs = it & 1;
+        const uint64_t da = smem_desc_kmajor_sw128(sA), db = smem_desc_kmajor_sw128(sB + qs * C::TILE);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const int box = kk >> 2, off = (kk & 3) * 32;
-          tc_mma_bf16(dst, smem_desc_kmajor_sw128(sA + box * C::BOX + off),
-                      smem_desc_kmajor_sw128(sB + qs * C::TILE + box * C::BOX + off), id_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma_bf16(dst, da + desc_step(kk, C::BOX), db + desc_step(kk, C::BOX), id_s, kk > 0 ? 1u : 0u);
       };
       // acc += (TMEM operand at src) x (tile of block it, MN-major)
       auto issue_acc = [&](int it, uint32_t src, const uint8_t* sB, uint32_t acc) {
@@ -1019,12 +1015,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       bool ok = mbar_wait(q_full, 0);
       // scores of block j: A (Q or dO) x B-tile^T into TMEM columns dst
       auto issue_scores = [&](const uint8_t* sA, const uint8_t* sBt, uint32_t dst) {
+        const uint64_t da = smem_desc_kmajor_sw128(sA), db = smem_desc_kmajor_sw128(sBt);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const int box = kk >> 2, off = (kk & 3) * 32;
-          tc_mma_bf16(dst, smem_desc_kmajor_sw128(sA + box * C::BOX + off),
-                      smem_desc_kmajor_sw128(sBt + box * C::BOX + off), id_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma_bf16(dst, da + desc_step(kk, C::BOX), db + desc_step(kk, C::BOX), id_s, kk > 0 ? 1u : 0u);
       };
       auto issue_s = [&](int j) {
         if (!mbar_wait(&k_full[j % NK], (j / NK) & 1)) return false;

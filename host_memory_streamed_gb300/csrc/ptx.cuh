@@ -336,6 +336,15 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(const void* tile) {
   return d;
 }
 
+// Descriptor offset of the K = 16 slice kk of a K-major SW128 tile made of
+// 64-column boxes box_bytes apart: slice kk sits in box kk / 4 at byte
+// (kk % 4) * 32 of each 128-byte row.  The start-address field holds
+// address / 16 and shared addresses stay below 2^18, so a descriptor of the
+// slice is the tile's descriptor plus this constant.
+__host__ __device__ constexpr uint64_t desc_step(int kk, int box_bytes) {
+  return (uint64_t)(((kk >> 2) * box_bytes + (kk & 3) * 32) >> 4);
+}
+
 // Descriptor for an MN-major operand tile (M or N contiguous) written by TMA
 // as 64-element-wide boxes with 128-byte swizzling: each box is rows of 128
 // bytes (one K index per row), 8-row swizzle atoms 1024 bytes apart along K
