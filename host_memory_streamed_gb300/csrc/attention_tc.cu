@@ -269,8 +269,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       tc_fence_after();
       uint32_t x[TA_BN];
 #pragma unroll
-      for (int c = 0; c < TA_BN / 32; ++c)
-        tmem_ld_32x32b_x32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(x + c * 32));
+      for (int c = 0; c < TA_BN / 64; ++c)
+        tmem_ld_32x32b_x64(tS + c * 64, *reinterpret_cast<uint32_t(*)[64]>(x + c * 64));
       tmem_wait_ld_regs(x);
       const int k0 = j * TA_BN;
       if (k0 + TA_BN - 1 > q0) {  // block touches the diagonal
@@ -798,8 +798,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
       tc_fence_after();
       uint32_t sv[64];
-      tmem_ld_32x32b_x32(tST + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_ld_32x32b_x32(tST + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_ld_32x32b_x64(tST + lane_off + hf * 64, sv);  // one wide load: less TMEM traffic contention
       tmem_wait_ld_regs(sv);
       // Queries past the sequence end have lse = +inf (P = 0) and delta = 0;
       // only the diagonal block (q0 == k0) needs the key > query mask.
@@ -1090,8 +1089,7 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
       tc_fence_after();
       uint32_t sv[64];
-      tmem_ld_32x32b_x32(tS + lane_off + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_ld_32x32b_x32(tS + lane_off + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_ld_32x32b_x64(tS + lane_off + hf * 64, sv);  // one wide load: less TMEM traffic contention
       tmem_wait_ld_regs(sv);
       tc_fence_before();
       mbar_arrive_warp(s_read);  // S_{j+1} may overwrite S_j
