@@ -833,20 +833,18 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
       tc_fence_after();
       const float4* del4 = reinterpret_cast<const float4*>(ld + 128 + hf * 64);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t dp[32];
-        tmem_ld_32x32b_x32(tDPT + lane_off + hf * 64 + half * 32, dp);
+      {
+        uint32_t dp[64];
+        tmem_ld_32x32b_x64(tDPT + lane_off + hf * 64, dp);
         tmem_wait_ld_regs(dp);
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = del4[half * 8 + c4];
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 d4 = del4[c4];
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          const int c = half * 32 + c4 * 4;
-          pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[c4 * 4]) - dv[0]),
-                              pf[c + 1] * (__uint_as_float(dp[c4 * 4 + 1]) - dv[1]));
-          pk[c / 2 + 1] = pack2bf(pf[c + 2] * (__uint_as_float(dp[c4 * 4 + 2]) - dv[2]),
-                                  pf[c + 3] * (__uint_as_float(dp[c4 * 4 + 3]) - dv[3]));
+          const int c = c4 * 4;
+          pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[c]) - dv[0]), pf[c + 1] * (__uint_as_float(dp[c + 1]) - dv[1]));
+          pk[c / 2 + 1] =
+              pack2bf(pf[c + 2] * (__uint_as_float(dp[c + 2]) - dv[2]), pf[c + 3] * (__uint_as_float(dp[c + 3]) - dv[3]));
         }
       }
       tmem_st_packed32(tDPT + lane_off + hf * 96, pk);  // dS^T likewise over this half's dP^T columns
@@ -1110,16 +1108,13 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
       }
       tc_fence_after();
       uint32_t pk[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t dp[32];
-        tmem_ld_32x32b_x32(tD + lane_off + hf * 64 + half * 32, dp);
+      {
+        uint32_t dp[64];
+        tmem_ld_32x32b_x64(tD + lane_off + hf * 64, dp);
         tmem_wait_ld_regs(dp);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = half * 32 + 2 * e;
-          pk[c / 2] = pack2bf(pf[c] * (__uint_as_float(dp[2 * e]) - Dr), pf[c + 1] * (__uint_as_float(dp[2 * e + 1]) - Dr));
-        }
+        for (int e = 0; e < 32; ++e)
+          pk[e] = pack2bf(pf[2 * e] * (__uint_as_float(dp[2 * e]) - Dr), pf[2 * e + 1] * (__uint_as_float(dp[2 * e + 1]) - Dr));
       }
       // dS over the first 32 of this half's own 64 dP columns (half 0: 0..31,
       // half 1: 96..127), which this thread has read: no barrier
