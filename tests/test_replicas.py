@@ -22,6 +22,8 @@ SHAPES = {
     # GQA, head_dim 128, ragged sequence, 3 layers
     "gqa128": mt_inputs.PRESETS["tiny"].with_(n_layers=3, d_model=256, n_heads=4, n_kv_heads=2, head_dim=128,
                                               ffn=344, vocab=520, batch=2, seq=180),
+    # mixture-of-experts layers: 8 experts, top-2, grouped expert GEMMs
+    "moe": mt_inputs.PRESETS["tiny"].with_(n_experts=8, top_k=2, ffn=136),
 }
 
 
@@ -161,6 +163,7 @@ CASES = {
     # asynchronous Adam, direct gradient landing on replica 0, weights read in place
     "gqa128-async-direct": dict(shape="gqa128", steps=3, keep=3, slab=32 << 10, stage=48 << 10, all_read=True,
                                 flags=256 | 512 | 1024),
+    "moe-async-direct": dict(shape="moe", steps=2, flags=256 | 512 | 1024),
 }
 
 
