@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <type_traits>
@@ -51,6 +52,30 @@ constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
+// Order of the CTAs of a causal grid whose x is the block along the sequence
+// (x = 0 the longest causal work) and whose y is a row of blocks that share
+// operands (a head or a kv-head group).  The block scheduler starts CTAs in
+// linear block order; taken row by row, every row's longest CTA would start
+// up to one row's span late and the kernel would end on one of them.  The
+// grid is cut into chunks of `chunk` rows and, within a chunk, walks
+// x-major: the x = 0 CTAs of all its rows first, then x = 1, ...  So the
+// longest CTAs of a chunk start first and short ones fill the end, while the
+// CTAs running at one time still come from a few rows, whose shared
+// operands stay in L2.  chunk = 1 is plain row-by-row order.
+__device__ __forceinline__ void causal_cta_order(int chunk, int& x, int& y) {
+  const int nx = (int)gridDim.x, ny = (int)gridDim.y;
+  const int lin = (int)blockIdx.y * nx + (int)blockIdx.x;  // < nx * ny
+  const int y0 = lin / (chunk * nx) * chunk;              // first row of this CTA's chunk
+  const int cy = min(chunk, ny - y0);                     // rows in the chunk (the last may be short)
+  const int idx = lin - y0 * nx;                          // < cy * nx
+  x = idx / cy;
+  y = y0 + idx % cy;
+}
+
+// Rows per chunk for a grid of nx x ny CTAs: about 256 CTAs (1.7 waves of
+// one CTA per SM) per chunk, at least one row.
+inline int causal_chunk_rows(int nx, int ny) { return std::max(1, std::min(ny, 256 / std::max(1, nx))); }
+
 template <int HD>
 struct TaCfg {
   static constexpr int BOX = 128 * 128;          // one 64-column box of 128 rows, bytes
@@ -70,6 +95,7 @@ struct TaParams {
   long ldo;
   float* lse;
   float sl2;  // softmax scale * log2(e)
+  int chunk;  // rows of the grid per chunk of the CTA order (causal_cta_order)
   int* status;
 };
 
@@ -126,8 +152,10 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest causal rows first
-  const int b = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
+  int bx, by;
+  causal_cta_order(p.chunk, bx, by);
+  const int qb = gridDim.x - 1 - bx;  // longest causal rows first
+  const int b = by / p.Hq, h = by % p.Hq;
   const int kvh = h * p.Hkv / p.Hq;
   const int S = p.S;
   const int q0 = qb * TA_BM;
@@ -434,6 +462,7 @@ int launch_tc(const AttnArgs& x, cudaStream_t s) {
   p.sl2 = kLog2eF / sqrtf((float)HD);
   p.status = x.status;
   dim3 grid((x.seq + TA_BM - 1) / TA_BM, x.batch * x.n_heads);
+  p.chunk = causal_chunk_rows((int)grid.x, (int)grid.y);
   attn_fwd_tc_kernel<HD><<<grid, TA_THREADS, C::SMEM, s>>>(tm, p);
   return launch_result();
 }
@@ -492,6 +521,8 @@ struct TbParams {
   float sl2;    // scale * log2(e)
   float scale;  // 1/sqrt(hd)
   int ld_bulk;  // lse/delta rows 16-byte aligned (S % 4 == 0): whole query blocks arrive by bulk copy
+  int chunk_kv;  // rows per chunk of the dK/dV grid's CTA order (causal_cta_order)
+  int chunk_q;   // the same for the dQ grid
   int* status;
 };
 
@@ -604,12 +635,14 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int b = blockIdx.y / p.Hkv, kvh = blockIdx.y % p.Hkv;
+  int kb, gy;  // key block (0 = the most query blocks) and (batch, kv head) row
+  causal_cta_order(p.chunk_kv, kb, gy);
+  const int b = gy / p.Hkv, kvh = gy % p.Hkv;
   const int S = p.S;
-  const int k0 = blockIdx.x * 128;
+  const int k0 = kb * 128;
   const int row0 = b * S;
   const int G = p.Hq / p.Hkv;
-  const int qb_first = blockIdx.x;
+  const int qb_first = kb;
   const int n_qb = (S + 127) / 128;
   const int per_head = n_qb - qb_first;
   const int total = per_head * G;
@@ -922,8 +955,10 @@ __global__ void __launch_bounds__(TB_THREADS, 1)
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int qb = gridDim.x - 1 - blockIdx.x;  // longest causal rows first
-  const int b = blockIdx.y / p.Hq, h = blockIdx.y % p.Hq;
+  int bx, by;
+  causal_cta_order(p.chunk_q, bx, by);
+  const int qb = gridDim.x - 1 - bx;  // longest causal rows first
+  const int b = by / p.Hq, h = by % p.Hq;
   const int kvh = h * p.Hkv / p.Hq;
   const int S = p.S;
   const int q0 = qb * 128;
@@ -1181,8 +1216,10 @@ int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
               (reinterpret_cast<uintptr_t>(x.delta) & 15) == 0;
   p.status = x.status;
   dim3 g1((x.seq + 127) / 128, x.batch * x.n_kv_heads);
-  attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_qkv, tm_do, p);
   dim3 g2((x.seq + 127) / 128, x.batch * x.n_heads);
+  p.chunk_kv = causal_chunk_rows((int)g1.x, (int)g1.y);
+  p.chunk_q = causal_chunk_rows((int)g2.x, (int)g2.y);
+  attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_qkv, tm_do, p);
   attn_bwd_dq_tc_kernel<HD><<<g2, TB_THREADS, Bq::SMEM, s>>>(tm_qkv, tm_do, p);
   return launch_result();
 }
