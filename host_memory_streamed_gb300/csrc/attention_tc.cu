@@ -72,9 +72,14 @@ __device__ __forceinline__ void causal_cta_order(int chunk, int& x, int& y) {
   y = y0 + idx % cy;
 }
 
-// Rows per chunk for a grid of nx x ny CTAs: about 256 CTAs (1.7 waves of
-// one CTA per SM) per chunk, at least one row.
-inline int causal_chunk_rows(int nx, int ny) { return std::max(1, std::min(ny, 256 / std::max(1, nx))); }
+// Rows per chunk for a grid of nx x ny CTAs: about `ctas` CTAs per chunk, at
+// least one row.  The backward kernels take 256 (1.7 waves of one CTA per
+// SM): their longest CTAs run hundreds of key or query blocks and need the
+// wider chunk to balance.  The forward's CTAs are short, and 128 (fewer
+// heads' K/V in L2 at a time) measured faster at every width tried.
+inline int causal_chunk_rows(int nx, int ny, int ctas) {
+  return std::max(1, std::min(ny, ctas / std::max(1, nx)));
+}
 
 template <int HD>
 struct TaCfg {
@@ -462,7 +467,7 @@ int launch_tc(const AttnArgs& x, cudaStream_t s) {
   p.sl2 = kLog2eF / sqrtf((float)HD);
   p.status = x.status;
   dim3 grid((x.seq + TA_BM - 1) / TA_BM, x.batch * x.n_heads);
-  p.chunk = causal_chunk_rows((int)grid.x, (int)grid.y);
+  p.chunk = causal_chunk_rows((int)grid.x, (int)grid.y, 128);
   attn_fwd_tc_kernel<HD><<<grid, TA_THREADS, C::SMEM, s>>>(tm, p);
   return launch_result();
 }
@@ -1217,8 +1222,8 @@ int launch_bwd_tc(const AttnArgs& x, cudaStream_t s) {
   p.status = x.status;
   dim3 g1((x.seq + 127) / 128, x.batch * x.n_kv_heads);
   dim3 g2((x.seq + 127) / 128, x.batch * x.n_heads);
-  p.chunk_kv = causal_chunk_rows((int)g1.x, (int)g1.y);
-  p.chunk_q = causal_chunk_rows((int)g2.x, (int)g2.y);
+  p.chunk_kv = causal_chunk_rows((int)g1.x, (int)g1.y, 256);
+  p.chunk_q = causal_chunk_rows((int)g2.x, (int)g2.y, 256);
   attn_bwd_dkdv_tc_kernel<HD><<<g1, TB_THREADS, A::SMEM, s>>>(tm_qkv, tm_do, p);
   attn_bwd_dq_tc_kernel<HD><<<g2, TB_THREADS, Bq::SMEM, s>>>(tm_qkv, tm_do, p);
   return launch_result();

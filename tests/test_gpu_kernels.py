@@ -170,10 +170,11 @@ def test_gemm_deterministic():
 # ------------------------------------------------------------------ attention
 # S % 4 == 0 brings whole query blocks' lse/delta by bulk copy in the dK/dV
 # kernel and stages ragged ones by thread: 512 (all whole, GQA 4), 452 and 200
-# (whole blocks, then a ragged one), 333 / 257 / 1 (all staged).  The kernels
-# start their CTAs in chunks of about 256 / (query blocks) rows of the grid;
-# 180 query heads and 90 kv-head rows over three query blocks (chunks of 85
-# rows) leave a short last chunk in every kernel.
+# (whole blocks, then a ragged one), 333 / 257 / 1 (all staged).  The
+# backward kernels start their CTAs in chunks of 256 / (query blocks) rows of
+# the grid, the forward in chunks of 128 / (query blocks): 180 query heads and
+# 90 kv-head rows over three query blocks (chunks of 85 and 42 rows) leave a
+# short last chunk in every kernel.
 ATTN = [(2, 128, 4, 4, 64), (1, 200, 4, 2, 128), (2, 333, 6, 2, 64), (1, 1, 2, 1, 128), (1, 257, 10, 2, 128),
         (1, 64, 8, 1, 64), (2, 512, 8, 2, 128), (1, 452, 4, 1, 128), (2, 300, 90, 45, 64)]
 
