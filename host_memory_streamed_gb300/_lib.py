@@ -102,6 +102,7 @@ def lib():
         "mt_op_wait_probe": (C.c_int, [vp, i64, vp]),
         "mt_tile_count": (C.c_int, [vp]),
         "mt_tile_info": (C.c_int, [vp, C.c_int, C.POINTER(MtTileDesc)]),
+        "mt_plan_tile_info": (C.c_int, [C.POINTER(MtConfig), C.c_int, C.POINTER(MtTileDesc)]),
         "mt_load_layer_tile": (C.c_int, [vp, C.c_int, C.c_int, vp, sz]),
         "mt_train_step": (C.c_int, [vp, vp, sz, fp]),
         "mt_train_step_device_tokens": (C.c_int, [vp, vp, sz, fp]),

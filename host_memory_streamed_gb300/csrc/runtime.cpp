@@ -2212,9 +2212,7 @@ int mt_debug_inject(mt_model* m, int32_t what, int32_t visit) {
 
 int mt_tile_count(const mt_model* m) { return m ? (int)m->layouts.size() : MT_EINVAL; }
 
-int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out) {
-  if (!m || !out || tile < 0 || tile >= (int)m->layouts.size()) return MT_EINVAL;
-  const auto& L = m->layouts[tile];
+static void fill_tile_desc(const mt::TileLayout& L, mt_tile_desc* out) {
   std::memset(out, 0, sizeof(*out));
   out->kind = L.kind;
   out->n_tensors = (int)L.tensors.size();
@@ -2230,7 +2228,39 @@ int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out) {
     out->tensors[i].offset = t.offset;
     out->tensors[i].numel = t.numel;
   }
+}
+
+int mt_tile_info(const mt_model* m, int tile, mt_tile_desc* out) {
+  if (!m || !out || tile < 0 || tile >= (int)m->layouts.size()) return MT_EINVAL;
+  fill_tile_desc(m->layouts[tile], out);
   return MT_OK;
+}
+
+int mt_plan_tile_info(const mt_config* cfg, int tile, mt_tile_desc* out) {
+  if (!cfg) {
+    mt::g_init_error = "null config";
+    return MT_EINVAL;
+  }
+  if (const char* e = mt::validate(*cfg)) {
+    mt::g_init_error = e;
+    return MT_EINVAL;
+  }
+  try {
+    mt_model tmp;
+    tmp.cfg = mt::with_defaults(*cfg);
+    tmp.D = mt::dims_of(tmp.cfg);
+    mt::build_layouts(&tmp);
+    const int n = (int)tmp.layouts.size();
+    if (tile < 0 || tile >= n) {
+      mt::g_init_error = "tile index out of range";
+      return MT_EINVAL;
+    }
+    if (out) fill_tile_desc(tmp.layouts[tile], out);
+    return n;
+  } catch (const std::exception& e) {
+    mt::g_init_error = e.what();
+    return MT_EINTERNAL;
+  }
 }
 
 static int part_span(mt_model* m, int tile, int part, size_t nbytes, int64_t* off, int64_t* n) {

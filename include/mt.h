@@ -245,6 +245,18 @@ typedef struct {
 int64_t mt_required_device_bytes(const mt_config* cfg);
 
 /*
+ * Host tile layout of this config without a handle (no GPU involved), to size
+ * host memory before mt_init_model: fills *out (if not NULL) with the
+ * description mt_tile_info gives for tile `tile` once the handle exists, and
+ * returns the number of tiles (> 0).  The tile store is the pages' 12 bytes
+ * per parameter (BF16 W and G, FP32 M and V) plus section and sub-tensor
+ * alignment (paperlayer.ai §2 "Training memory", §A.1 "Layer-Contiguous
+ * Tiling").  MT_EINVAL for an invalid config or a tile index outside
+ * [0, tiles); the text is in mt_last_error(NULL).
+ */
+int mt_plan_tile_info(const mt_config* cfg, int tile, mt_tile_desc* out);
+
+/*
  * Create a handle.  device_arena: a device allocation of at least
  * mt_required_device_bytes(cfg) bytes, 256-byte aligned; stream_*:
  * cudaStream_t values (compute, host-to-device, device-to-host), distinct and

@@ -1,7 +1,7 @@
 """Host-side checks of libmt.so that need no GPU: the library loads and exports
 every symbol the headers declare, the CPU Adam matches the oracle, the tile
-layout keeps the 12-bytes-per-parameter accounting, and bad configurations are
-rejected with MT_EINVAL."""
+layout (queried without a handle) keeps the pages' 12-bytes-per-parameter
+accounting, and bad configurations are rejected with MT_EINVAL."""
 import ctypes as C
 import os
 
@@ -105,20 +105,98 @@ def test_cpu_adam_rejects_bad_step(lib):
                             0.0) != 0
 
 
-def test_tile_layout_accounting():
-    """Layer tiles hold W (BF16) | G (BF16) | M (FP32) | V (FP32), each section
-    page aligned: 12 bytes per parameter plus padding (the pages' 12P
-    accounting, 70B -> at least 840 GB)."""
-    for name in ("1.3b", "14b", "70b"):
-        s = mt_inputs.PRESETS[name]
-        shapes = mt_inputs.layer_tensor_shapes(s)
-        n = sum(int(torch.tensor(v).prod()) for v in shapes.values())
-        per_layer = 12 * n
-        total = s.n_layers * per_layer + 12 * (2 * s.vocab * s.d_model + s.d_model)
-        if name == "70b":
-            assert total >= 840e9
-        if name == "14b":
-            assert abs(n - 275261440) == 0
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", name)):
+        line = line.split("#")[0].split()
+        if line:
+            vals[line[0]] = int(line[1])
+    return vals
+
+
+def _plan_tiles(lib, shape, **kw):
+    """Every tile's layout from the library, without a handle."""
+    from host_memory_streamed_gb300 import _lib
+    cfg = _cfg(shape, **kw)
+    n = lib.mt_plan_tile_info(C.byref(cfg), 0, None)
+    assert n > 0, lib.mt_last_error(None)
+    out = []
+    for t in range(n):
+        d = _lib.MtTileDesc()
+        assert lib.mt_plan_tile_info(C.byref(cfg), t, C.byref(d)) == n
+        out.append(d)
+    return out
+
+
+@pytest.mark.parametrize("name,kw", [("1.3b", {}), ("14b", {}), ("70b", {}), ("1.3b", {"flags": 128}),
+                                     ("1.3b", {"n_experts": 8, "top_k": 2})])
+def test_tile_layout_accounting(lib, name, kw):
+    """The library's host tiles (queried through the C-ABI, no GPU) hold W
+    (BF16) | G (BF16) | M (FP32) | V (FP32): the pages' bytes per parameter
+    (tests/golden/persistent_state.txt) plus section and sub-tensor padding,
+    every tensor where the layout documents it, with the parameter count of
+    the architecture; tiles in the documented order (embedding, layers, head;
+    no head tile when the embedding is tied)."""
+    gold = _golden("persistent_state.txt")
+    per_param = gold["state_bytes_per_param"]
+    assert per_param == gold["weight_bytes_per_param"] + gold["grad_bytes_per_param"] + \
+        gold["moment_bytes_per_param"]
+    s = mt_inputs.PRESETS[name]
+    tied = bool(kw.get("flags", 0) & 128)
+    E = kw.get("n_experts", 0)
+    tiles = _plan_tiles(lib, s, **kw)
+    assert len(tiles) == s.n_layers + (1 if tied else 2)
+    d, dq, dqkv = s.d_model, s.n_heads * s.head_dim, (s.n_heads + 2 * s.n_kv_heads) * s.head_dim
+    if E:
+        layer = [("g1", d, 0), ("wqkv", dqkv, d), ("wo", d, dq), ("g2", d, 0), ("wr", E, d),
+                 ("wgu", E * 2 * s.ffn, d), ("wd", E * d, s.ffn)]
+    else:
+        layer = [("g1", d, 0), ("wqkv", dqkv, d), ("wo", d, dq), ("g2", d, 0), ("wgu", 2 * s.ffn, d),
+                 ("wd", d, s.ffn)]
+    expect = [[("E", s.vocab, d)] + ([("gf", d, 0)] if tied else [])] + [layer] * s.n_layers
+    if not tied:
+        expect.append([("gf", d, 0), ("wh", s.vocab, d)])
+    total_params = total_bytes = 0
+    for i, (t, ex) in enumerate(zip(tiles, expect)):
+        assert t.kind == (0 if i == 0 else (1 if i <= s.n_layers else 2))
+        assert t.n_tensors == len(ex)
+        end = 0
+        for k, (nm, r, c) in enumerate(ex):
+            x = t.tensors[k]
+            assert x.name.decode() == nm and x.ndim == (2 if c else 1)
+            assert (x.shape[0], x.shape[1]) == (r, c) and x.numel == (r * c if c else r)
+            assert x.offset % 256 == 0 and x.offset >= end  # 256-byte sub-tensors, in order, no overlap
+            end = x.offset + 2 * x.numel
+        assert t.n_params == sum(r * c if c else r for _, r, c in ex)
+        # W and G: BF16 per parameter; M and V: FP32 per parameter; 4 KB sections
+        assert t.w_bytes % 4096 == 0 and end <= t.w_bytes < end + 4096
+        assert t.tile_bytes == 2 * t.w_bytes + 2 * (2 * t.w_bytes)  # W, G + M, V at twice the bytes
+        assert per_param * t.n_params <= t.tile_bytes
+        # padding: at most 255 bytes per sub-tensor plus 4 KB per W section, times six W-sized sections
+        assert t.tile_bytes <= per_param * t.n_params + 6 * (256 * t.n_tensors + 4096)
+        total_params += t.n_params
+        total_bytes += t.tile_bytes
+    if name == "14b" and not kw:
+        assert tiles[1].n_params == 275261440
+    if name == "70b":
+        # the pages' 70B figure, at this shape's 70.55 B parameters
+        assert total_params >= gold["params_70b"]
+        assert total_bytes >= gold["state_bytes_70b"]
+        assert total_bytes <= per_param * total_params * 1.0001
+
+
+def test_plan_tile_info_rejects_bad_arguments(lib):
+    from host_memory_streamed_gb300 import _lib
+    s = mt_inputs.PRESETS["tiny"]
+    cfg = _cfg(s)
+    n = lib.mt_plan_tile_info(C.byref(cfg), 0, None)
+    assert n == s.n_layers + 2
+    d = _lib.MtTileDesc()
+    for t in (-1, n):
+        assert lib.mt_plan_tile_info(C.byref(cfg), t, C.byref(d)) == -1
+        assert "tile index" in lib.mt_last_error(None).decode()
+    assert lib.mt_plan_tile_info(C.byref(_cfg(s, n_heads=3, n_kv_heads=2)), 0, C.byref(d)) == -1
+    assert lib.mt_plan_tile_info(None, 0, C.byref(d)) == -1
 
 
 def test_header_documents_every_entry_point():
