@@ -37,6 +37,17 @@ def plan_schedule(n_layers: int, ckpt_every: int = 1, flags: int = 0, keep_layer
     return [{f: getattr(v, f) for f, _ in _lib.MtVisit._fields_} for v in out]
 
 
+def _tile_dict(d) -> dict:
+    """An ``mt_tile_desc`` as a dict: kind, n_params, w_bytes, tile_bytes and
+    the tensors by name (shape, byte offset in the W section, numel)."""
+    tensors = {}
+    for k in range(d.n_tensors):
+        t = d.tensors[k]
+        shape = (t.shape[0], t.shape[1]) if t.ndim == 2 else (t.shape[0],)
+        tensors[t.name.decode()] = dict(shape=shape, offset=t.offset, numel=t.numel)
+    return dict(kind=d.kind, n_params=d.n_params, w_bytes=d.w_bytes, tile_bytes=d.tile_bytes, tensors=tensors)
+
+
 class MtError(RuntimeError):
     def __init__(self, code, msg):
         super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
@@ -130,18 +141,43 @@ class StreamedDecoder:
         return lo
 
     @staticmethod
-    def required_device_bytes(s, **kw) -> int:
-        """Device arena bytes a model of shape ``s`` (and the given options) needs."""
+    def _shape_cfg(s, kw):
         cfg = _lib.MtConfig()
         for k in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "batch", "seq",
                   "ckpt_every", "rms_eps", "rope_theta", "lr", "beta1", "beta2", "adam_eps", "weight_decay"):
             setattr(cfg, k, getattr(s, k))
         for k, v in kw.items():
             setattr(cfg, k, v)
+        return cfg
+
+    @staticmethod
+    def required_device_bytes(s, **kw) -> int:
+        """Device arena bytes a model of shape ``s`` (and the given options) needs."""
+        cfg = StreamedDecoder._shape_cfg(s, kw)
         need = _lib.lib().mt_required_device_bytes(C.byref(cfg))
         if need < 0:
             raise MtError(need, _lib.lib().mt_last_error(None).decode())
         return int(need)
+
+    @staticmethod
+    def plan_tiles(s, **kw) -> list[dict]:
+        """The host tiles a model of shape ``s`` (and the given options) will
+        have, as ``tile_info`` describes them, without a handle or a GPU
+        (``mt_plan_tile_info``); their ``tile_bytes`` sum to the host memory
+        the tile store takes."""
+        cfg = StreamedDecoder._shape_cfg(s, kw)
+        lib = _lib.lib()
+        n = lib.mt_plan_tile_info(C.byref(cfg), 0, None)
+        if n < 0:
+            raise MtError(n, lib.mt_last_error(None).decode())
+        out = []
+        for i in range(n):
+            d = _lib.MtTileDesc()
+            rc = lib.mt_plan_tile_info(C.byref(cfg), i, C.byref(d))
+            if rc < 0:
+                raise MtError(rc, lib.mt_last_error(None).decode())
+            out.append(_tile_dict(d))
+        return out
 
     @classmethod
     def from_shape(cls, s, **kw):
@@ -179,12 +215,7 @@ class StreamedDecoder:
     def tile_info(self, i):
         d = _lib.MtTileDesc()
         self._check(self._L.mt_tile_info(self._h, i, C.byref(d)))
-        tensors = {}
-        for k in range(d.n_tensors):
-            t = d.tensors[k]
-            shape = (t.shape[0], t.shape[1]) if t.ndim == 2 else (t.shape[0],)
-            tensors[t.name.decode()] = dict(shape=shape, offset=t.offset, numel=t.numel)
-        return dict(kind=d.kind, n_params=d.n_params, w_bytes=d.w_bytes, tile_bytes=d.tile_bytes, tensors=tensors)
+        return _tile_dict(d)
 
     def _part_bytes(self, i, part):
         w = self.infos[i]["w_bytes"]

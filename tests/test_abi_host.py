@@ -318,3 +318,21 @@ def test_kept_layers_add_their_internals_to_the_arena(lib):
     assert step > 0 and need[3] - need[2] == step
     assert need[4] == lib.mt_required_device_bytes(C.byref(_cfg(s, flags=hms.MT_STORE_ACTS)))
     assert lib.mt_required_device_bytes(C.byref(_cfg(s, keep_layers=9))) == need[4]
+
+
+def test_binding_plans_the_tiles_without_a_gpu(lib):
+    """``StreamedDecoder.plan_tiles`` returns the tiles the C-ABI describes; at
+    the 14B shape they take 12 bytes per parameter plus under 0.01 % of
+    padding (177 GB)."""
+    import host_memory_streamed_gb300 as hms
+    s = mt_inputs.PRESETS["14b"]
+    tiles = hms.StreamedDecoder.plan_tiles(s)
+    assert len(tiles) == s.n_layers + 2
+    assert list(tiles[1]["tensors"]) == ["g1", "wqkv", "wo", "g2", "wgu", "wd"]
+    assert tiles[1]["tensors"]["wgu"]["shape"] == (2 * s.ffn, s.d_model)
+    params = sum(t["n_params"] for t in tiles)
+    host = sum(t["tile_bytes"] for t in tiles)
+    assert 12 * params <= host <= 12 * params * 1.0001
+    assert 176e9 < host < 178e9
+    with pytest.raises(hms.MtError):
+        hms.StreamedDecoder.plan_tiles(s, n_kv_heads=7)
