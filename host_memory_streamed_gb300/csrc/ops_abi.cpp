@@ -162,6 +162,8 @@ int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
   a.status = status;
   if (const char* e = mt::attn_check(a)) return op_fail(e);
   if (!dout || !delta || !dqkv) return op_fail("attention backward: null dout, delta or dqkv");
+  if ((reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dqkv)) & 15)
+    return op_fail("attention backward: dout and dqkv must be 16-byte aligned");
   if ((rope_cos == nullptr) != (rope_sin == nullptr)) return op_fail("attention backward: cos and sin go together");
   return op_cuda(mt::launch_attn_bwd(a, static_cast<cudaStream_t>(stream)), "attention backward");
 }

@@ -110,7 +110,9 @@ int mt_op_gemm_grouped(const void* A, int64_t lda, const void* B, int64_t ldb, i
  * columns each (q, k already rotated).  Query head h reads kv head
  * h*n_kv_heads/n_heads.  o: [batch*seq, ldo] BF16; lse: FP32
  * [batch, n_heads, seq] natural-log log-sum-exp of each score row (scores
- * scaled by 1/sqrt(head_dim)).  head_dim 64 or 128; n_heads % n_kv_heads == 0.
+ * scaled by 1/sqrt(head_dim)).  head_dim 64 or 128; n_heads % n_kv_heads == 0;
+ * batch, seq > 0; ldqkv, ldo multiples of 8 and at least the row widths;
+ * qkv and o 16-byte aligned (TMA); otherwise MT_EINVAL before any launch.
  * A wait inside the kernel that runs out writes a nonzero code to *status.
  */
 int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
@@ -123,7 +125,10 @@ int mt_op_attention_fwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
  * [batch, n_heads, seq] (overwritten).  When rope_cos/rope_sin ([seq,
  * head_dim/2] FP32) are given, dq and dk are passed back through the inverse
  * rotate-half rotation (gradient w.r.t. the unrotated projections).
- * Deterministic: no atomics, fixed accumulation order.
+ * Deterministic: no atomics, fixed accumulation order.  The forward's
+ * argument rules apply, and dout and dqkv must be non-null and 16-byte
+ * aligned, delta non-null, rope_cos and rope_sin both given or both NULL;
+ * otherwise MT_EINVAL before any launch.
  */
 int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t seq, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, const void* o, int64_t ldo, const float* lse,

@@ -336,3 +336,38 @@ def test_binding_plans_the_tiles_without_a_gpu(lib):
     assert 176e9 < host < 178e9
     with pytest.raises(hms.MtError):
         hms.StreamedDecoder.plan_tiles(s, n_kv_heads=7)
+
+
+_ATT = dict(ldqkv=(4 + 2 * 2) * 64, batch=2, seq=100, n_heads=4, n_kv_heads=2, head_dim=64, ldo=4 * 64)
+
+
+@pytest.mark.parametrize("bad,msg", [
+    (dict(head_dim=96, ldqkv=8 * 96, ldo=4 * 96), "head_dim"),
+    (dict(n_kv_heads=3, ldqkv=10 * 64), "multiple of n_kv_heads"),
+    (dict(seq=0), "empty"),
+    (dict(batch=-1), "empty"),
+    (dict(ldqkv=8 * 64 - 8), "ldqkv too small"),
+    (dict(ldo=4 * 64 + 4), "multiples of 8"),
+    (dict(qkv=0), "null"),
+    (dict(o=0x10008), "misaligned"),
+    (dict(dout=0), "null dout"),
+    (dict(dqkv=0x20008), "16-byte aligned"),
+    (dict(rope_cos=0x30000), "cos and sin"),
+])
+def test_attention_ops_reject_bad_arguments_before_any_launch(lib, bad, msg):
+    """The attention entry points check shapes, leading dimensions, pointers
+    and alignment on the host and return MT_EINVAL with a message; nothing is
+    launched (these run without a GPU; the pointers are never dereferenced)."""
+    from host_memory_streamed_gb300 import _lib
+    a = dict(_ATT, qkv=0x10000, o=0x20000, lse=0x30000, dout=0x40000, delta=0x50000, dqkv=0x60000,
+             rope_cos=None, rope_sin=None)
+    a.update(bad)
+    fwd_only = {"dout", "dqkv", "rope_cos"}.isdisjoint(bad)
+    if fwd_only:
+        rc = lib.mt_op_attention_fwd(a["qkv"], a["ldqkv"], a["batch"], a["seq"], a["n_heads"], a["n_kv_heads"],
+                                     a["head_dim"], a["o"], a["ldo"], a["lse"], None, None)
+        assert rc == _lib.MT_EINVAL and msg in lib.mt_op_last_error().decode()
+    rc = lib.mt_op_attention_bwd(a["qkv"], a["ldqkv"], a["batch"], a["seq"], a["n_heads"], a["n_kv_heads"],
+                                 a["head_dim"], a["o"], a["ldo"], a["lse"], a["dout"], a["delta"], a["dqkv"],
+                                 a["rope_cos"], a["rope_sin"], None, None)
+    assert rc == _lib.MT_EINVAL and msg in lib.mt_op_last_error().decode()
