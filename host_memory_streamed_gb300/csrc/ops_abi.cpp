@@ -19,6 +19,9 @@ int op_fail(const char* msg) {
   g_op_error = msg ? msg : "unknown error";
   return MT_EINVAL;
 }
+// 16-byte aligned (NULL counts as aligned: null checks are separate)
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+constexpr int64_t kMaxGridRows = 0x7fffffff;  // one CTA per row: grid.x limit
 int op_cuda(int rc, const char* what) {
   if (rc == 0) return MT_OK;
   g_op_error = std::string(what) + ": launch failed (" + (rc == -4 ? mt::last_launch_error() : "bad descriptor or attributes") + ")";
@@ -171,6 +174,9 @@ int mt_op_attention_bwd(const void* qkv, int64_t ldqkv, int32_t batch, int32_t s
 int mt_op_rmsnorm_fwd(const void* x, const void* g, void* y, float* rstd, int64_t rows, int32_t d, float eps,
                       void* stream) {
   if (d <= 0 || d % 8) return op_fail("rmsnorm: d must be a positive multiple of 8");
+  if (rows < 0 || rows > kMaxGridRows) return op_fail("rmsnorm: rows must be in 0 .. 2^31 - 1");
+  if (rows > 0 && (!x || !g || !y || !rstd)) return op_fail("rmsnorm: null x, g, y or rstd");
+  if (!al16(x) || !al16(g) || !al16(y)) return op_fail("rmsnorm: x, g and y must be 16-byte aligned");
   mt::launch_rmsnorm_fwd(static_cast<const mt::bf16*>(x), static_cast<const mt::bf16*>(g),
                          static_cast<mt::bf16*>(y), rstd, rows, d, eps, static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "rmsnorm forward");
@@ -186,6 +192,10 @@ int64_t mt_op_rmsnorm_bwd_scratch_floats(int64_t rows, int32_t d) {
 int mt_op_rmsnorm_bwd(const void* dy, const void* x, const void* g, const float* rstd, const void* dres, void* dx,
                       void* dg, float* scratch, int64_t rows, int32_t d, void* stream) {
   if (d <= 0 || d % 8 || rows < 0) return op_fail("rmsnorm: d must be a positive multiple of 8 and rows >= 0");
+  if (!dg || (rows > 0 && (!dy || !x || !g || !rstd || !dx || !scratch)))
+    return op_fail("rmsnorm backward: null dy, x, g, rstd, dx, dg or scratch");
+  if (!al16(dy) || !al16(x) || !al16(g) || !al16(dres) || !al16(dx))
+    return op_fail("rmsnorm backward: dy, x, g, dres and dx must be 16-byte aligned");
   if (d > mt::rmsnorm_bwd_max_d()) return op_fail("rmsnorm backward: d exceeds the widest row this device takes");
   auto s = static_cast<cudaStream_t>(stream);
   const long parts = mt::launch_rmsnorm_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(x),
@@ -204,7 +214,10 @@ int mt_op_flag_nonfinite(const void* p, int64_t n, int32_t* flag, void* stream) 
 }
 
 int mt_op_swiglu_bwd(const void* da, const void* gu, void* dgu, int64_t rows, int32_t f, void* stream) {
-  if (f <= 0) return op_fail("swiglu: f must be positive");
+  if (f <= 0 || rows < 0) return op_fail("swiglu: f must be positive and rows >= 0");
+  if (rows > 0 && (!da || !gu || !dgu)) return op_fail("swiglu: null da, gu or dgu");
+  if (f % 8 == 0 && (!al16(da) || !al16(gu) || !al16(dgu)))
+    return op_fail("swiglu: with f % 8 == 0, da, gu and dgu must be 16-byte aligned");
   mt::launch_swiglu_bwd(static_cast<const mt::bf16*>(da), static_cast<const mt::bf16*>(gu),
                         static_cast<mt::bf16*>(dgu), rows, f, static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "swiglu backward");
@@ -212,6 +225,8 @@ int mt_op_swiglu_bwd(const void* da, const void* gu, void* dgu, int64_t rows, in
 
 int mt_op_transpose(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t ldd,
                     void* stream) {
+  if (rows < 0 || cols < 0 || lds < cols || ldd < rows) return op_fail("transpose: bad shape or leading dimension");
+  if (rows > 0 && cols > 0 && (!src || !dst)) return op_fail("transpose: null src or dst");
   mt::launch_transpose(static_cast<const mt::bf16*>(src), rows, cols, lds, static_cast<mt::bf16*>(dst), ldd,
                        static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "transpose");
@@ -220,6 +235,9 @@ int mt_op_transpose(const void* src, int64_t rows, int64_t cols, int64_t lds, vo
 int mt_op_cross_entropy(const float* z, int64_t rows, int32_t vocab, const int32_t* tgt, float inv_n, void* dz,
                         float* loss_rows, int32_t* status, void* stream) {
   if (vocab <= 0) return op_fail("cross entropy: vocab must be positive");
+  if (rows < 0 || rows > kMaxGridRows) return op_fail("cross entropy: rows must be in 0 .. 2^31 - 1");
+  if (rows > 0 && (!z || !tgt || !dz || !loss_rows)) return op_fail("cross entropy: null z, tgt, dz or loss_rows");
+  if (!al16(z) || !al16(dz)) return op_fail("cross entropy: z and dz must be 16-byte aligned");
   mt::launch_cross_entropy(z, rows, vocab, tgt, inv_n, static_cast<mt::bf16*>(dz), loss_rows, status,
                            static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "cross entropy");
@@ -227,7 +245,10 @@ int mt_op_cross_entropy(const float* z, int64_t rows, int32_t vocab, const int32
 
 int mt_op_embedding_fwd(const int32_t* tok, const void* E, void* x, int64_t T, int32_t d, int32_t V,
                         int32_t* status, void* stream) {
-  if (d % 8) return op_fail("embedding: d must be a multiple of 8");
+  if (d <= 0 || d % 8 || V <= 0) return op_fail("embedding: d must be a positive multiple of 8 and V positive");
+  if (T < 0 || T > kMaxGridRows) return op_fail("embedding: T must be in 0 .. 2^31 - 1");
+  if (T > 0 && (!tok || !E || !x)) return op_fail("embedding: null tok, E or x");
+  if (!al16(E) || !al16(x)) return op_fail("embedding: E and x must be 16-byte aligned");
   mt::launch_embed_fwd(tok, static_cast<const mt::bf16*>(E), static_cast<mt::bf16*>(x), T, d, V, status,
                        static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "embedding forward");
@@ -235,7 +256,9 @@ int mt_op_embedding_fwd(const int32_t* tok, const void* E, void* x, int64_t T, i
 
 int mt_op_embedding_bwd(const int32_t* row_offsets, const int32_t* positions, const void* dx, void* dE, int32_t V,
                         int32_t d, void* stream) {
-  if (d % 8) return op_fail("embedding: d must be a multiple of 8");
+  if (d <= 0 || d % 8 || V <= 0) return op_fail("embedding: d must be a positive multiple of 8 and V positive");
+  if (!row_offsets || !positions || !dx || !dE) return op_fail("embedding backward: null pointer");
+  if (!al16(dx) || !al16(dE)) return op_fail("embedding backward: dx and dE must be 16-byte aligned");
   mt::launch_embed_bwd(row_offsets, positions, static_cast<const mt::bf16*>(dx), static_cast<mt::bf16*>(dE), V, d,
                        static_cast<cudaStream_t>(stream));
   return op_cuda(cudaPeekAtLastError() == cudaSuccess ? 0 : -1, "embedding backward");

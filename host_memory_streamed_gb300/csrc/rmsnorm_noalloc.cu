@@ -67,6 +67,15 @@ extern "C" int mt_op_rmsnorm_bwd_noalloc(const void* dy, const void* x, const vo
     mt::set_op_error("rmsnorm (no-alloc): d must be a positive multiple of 8 and rows >= 0");
     return MT_EINVAL;
   }
+  if (!dg || (rows > 0 && (!dy || !x || !g || !rstd || !dx))) {
+    mt::set_op_error("rmsnorm (no-alloc): null dy, x, g, rstd, dx or dg");
+    return MT_EINVAL;
+  }
+  if ((reinterpret_cast<uintptr_t>(dy) | reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) |
+       reinterpret_cast<uintptr_t>(dres) | reinterpret_cast<uintptr_t>(dx)) & 15) {
+    mt::set_op_error("rmsnorm (no-alloc): dy, x, g, dres and dx must be 16-byte aligned");
+    return MT_EINVAL;
+  }
   if (d > mt::rmsnorm_bwd_max_d()) {
     mt::set_op_error("rmsnorm (no-alloc): d = " + std::to_string(d) + " exceeds the widest row this device takes (" +
                      std::to_string(mt::rmsnorm_bwd_max_d()) + ")");

@@ -8,6 +8,15 @@
  * asynchronous: they enqueue work and return.  Arguments are validated on the
  * host: an unsupported shape, alignment or mode returns MT_EINVAL before
  * anything is launched, with the reason in mt_op_last_error() (per thread).
+ * Buffers the kernels move in 16-byte vectors must be 16-byte aligned (the
+ * RMSNorm rows and gain, the SwiGLU buffers when f % 8 == 0, the embedding
+ * table and rows, cross-entropy's z and dz, the attention buffers, the GEMM
+ * operands).  The elementwise kernels (RMSNorm, SwiGLU, transpose,
+ * cross-entropy, embedding forward) take zero rows or tokens: they launch
+ * nothing over rows and return MT_OK, and their row buffers may then be NULL
+ * (RMSNorm's gain gradient dg [d] is still written, as zeros).  GEMM and
+ * attention take non-empty shapes only.  Row counts that index the grid (one
+ * CTA per row) must be below 2^31.
  * A launch failure returns MT_ECUDA.  Kernels that can detect a problem at
  * run time (a bounded wait that expired, a token id out of range) write a
  * nonzero code into *status (device int, first error sticks) when `status`

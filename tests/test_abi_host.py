@@ -371,3 +371,58 @@ def test_attention_ops_reject_bad_arguments_before_any_launch(lib, bad, msg):
                                  a["head_dim"], a["o"], a["ldo"], a["lse"], a["dout"], a["delta"], a["dqkv"],
                                  a["rope_cos"], a["rope_sin"], None, None)
     assert rc == _lib.MT_EINVAL and msg in lib.mt_op_last_error().decode()
+
+
+A0, A1, A2, A3, A4, A5, A6 = (0x100000 * (i + 1) for i in range(7))  # 16-byte aligned stand-ins, never read
+ODD = 0x100008  # 8-byte aligned only
+
+
+@pytest.mark.parametrize("call,msg", [
+    (lambda L: L.mt_op_rmsnorm_fwd(A0, A1, A2, A3, 10, 12, 1e-5, None), "multiple of 8"),
+    (lambda L: L.mt_op_rmsnorm_fwd(A0, A1, A2, A3, -1, 64, 1e-5, None), "rows"),
+    (lambda L: L.mt_op_rmsnorm_fwd(A0, A1, A2, A3, 1 << 31, 64, 1e-5, None), "rows"),
+    (lambda L: L.mt_op_rmsnorm_fwd(None, A1, A2, A3, 10, 64, 1e-5, None), "null"),
+    (lambda L: L.mt_op_rmsnorm_fwd(A0, A1, ODD, A3, 10, 64, 1e-5, None), "16-byte"),
+    (lambda L: L.mt_op_rmsnorm_bwd(A0, A1, A2, A3, None, A4, A5, None, 10, 64, None), "null"),
+    (lambda L: L.mt_op_rmsnorm_bwd(A0, A1, A2, A3, None, A4, None, A6, 0, 64, None), "null"),
+    (lambda L: L.mt_op_rmsnorm_bwd(A0, A1, A2, A3, ODD, A4, A5, A6, 10, 64, None), "16-byte"),
+    (lambda L: L.mt_op_rmsnorm_bwd_noalloc(A0, A1, A2, None, None, A4, A5, 10, 64, None), "null"),
+    (lambda L: L.mt_op_rmsnorm_bwd_noalloc(ODD, A1, A2, A3, None, A4, A5, 10, 64, None), "16-byte"),
+    (lambda L: L.mt_op_swiglu_bwd(A0, A1, A2, -1, 16, None), "rows"),
+    (lambda L: L.mt_op_swiglu_bwd(A0, None, A2, 4, 16, None), "null"),
+    (lambda L: L.mt_op_swiglu_bwd(A0, A1, ODD, 4, 16, None), "16-byte"),
+    (lambda L: L.mt_op_transpose(A0, 4, 10, 9, A1, 4, None), "leading dimension"),
+    (lambda L: L.mt_op_transpose(A0, 4, 10, 10, A1, 3, None), "leading dimension"),
+    (lambda L: L.mt_op_transpose(None, 4, 10, 10, A1, 4, None), "null"),
+    (lambda L: L.mt_op_cross_entropy(A0, 4, 0, A1, 0.25, A2, A3, None, None), "vocab"),
+    (lambda L: L.mt_op_cross_entropy(A0, 4, 64, None, 0.25, A2, A3, None, None), "null"),
+    (lambda L: L.mt_op_cross_entropy(ODD, 4, 64, A1, 0.25, A2, A3, None, None), "16-byte"),
+    (lambda L: L.mt_op_embedding_fwd(A0, A1, A2, 5, 60, 100, None, None), "multiple of 8"),
+    (lambda L: L.mt_op_embedding_fwd(A0, A1, A2, 5, 64, 0, None, None), "V positive"),
+    (lambda L: L.mt_op_embedding_fwd(A0, None, A2, 5, 64, 100, None, None), "null"),
+    (lambda L: L.mt_op_embedding_fwd(A0, ODD, A2, 5, 64, 100, None, None), "16-byte"),
+    (lambda L: L.mt_op_embedding_bwd(A0, None, A2, A3, 100, 64, None), "null"),
+    (lambda L: L.mt_op_embedding_bwd(A0, A1, A2, ODD, 100, 64, None), "16-byte"),
+    (lambda L: L.mt_op_gemm(None, 64, A1, 64, 256, 256, 64, 0, A2, 256, None, 0, None, 0, None, None, 0, 0, 0,
+                            None, None), "null A or B"),
+    (lambda L: L.mt_op_gemm(A0, 64, A1, 64, 256, 256, 64, 0, ODD, 256, None, 0, None, 0, None, None, 0, 0, 0,
+                            None, None), "C not 16-byte"),
+    (lambda L: L.mt_op_gemm(A0, 64, A1, 64, 0, 256, 64, 0, A2, 256, None, 0, None, 0, None, None, 0, 0, 0,
+                            None, None), "positive"),
+    (lambda L: L.mt_op_gemm(A0, 60, A1, 64, 256, 256, 60, 0, A2, 256, None, 0, None, 0, None, None, 0, 0, 0,
+                            None, None), "multiple of 8"),
+    (lambda L: L.mt_op_gemm(A0, 64, A1, 64, 256, 256, 64, 1, A2, 256, None, 0, None, 0, None, None, 0, 0, 0,
+                            None, None), "residual"),
+    (lambda L: L.mt_op_gemm(A0, 64, A1, 64, 256, 256, 64, 5, A2, 256, None, 0, None, 0, None, None, 256, 128, 64,
+                            None, None), "RoPE tables"),
+    (lambda L: L.mt_op_gemm(A0, 64, A1, 64, 256, 256, 64, 9, A2, 256, None, 0, None, 0, None, None, 0, 0, 0,
+                            None, None), "unknown epilogue"),
+])
+def test_elementwise_ops_reject_bad_arguments_before_any_launch(lib, call, msg):
+    """Each per-kernel entry point checks sizes, pointers and the alignment
+    its 16-byte vector accesses need on the host, returning MT_EINVAL with a
+    message (no launch: these run without a GPU and the pointers are never
+    dereferenced)."""
+    from host_memory_streamed_gb300 import _lib
+    assert call(lib) == _lib.MT_EINVAL
+    assert msg in lib.mt_op_last_error().decode()
