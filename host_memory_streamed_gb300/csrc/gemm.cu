@@ -938,7 +938,6 @@ const char* gemm_check(const GemmArgs& g) {
   if (g.K % 8 && !(g.a_mn && g.b_mn)) return "gemm: K must be a multiple of 8 (16-byte TMA rows)";
   if (g.lda % 8 || g.ldb % 8) return "gemm: lda/ldb must be multiples of 8 elements";
   if (g.lda < (g.a_mn ? g.M : g.K) || g.ldb < (g.b_mn ? g.N : g.K)) return "gemm: lda/ldb smaller than a row";
-  if (!g.A || !g.B) return "gemm: null A or B";
   if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.B)) & 15) return "gemm: A/B not 16-byte aligned";
   if (!g.C) return "gemm: null output";
   if (reinterpret_cast<uintptr_t>(g.C) & 15) return "gemm: C not 16-byte aligned";

@@ -62,6 +62,7 @@ int mt_op_gemm(const void* A, int64_t lda, const void* B, int64_t ldb, int32_t M
   g.head_dim = head_dim;
   g.seq = seq;
   g.status = status;
+  if (!A || !B) return op_fail("gemm: null A or B");
   if (const char* e = mt::gemm_check(g)) return op_fail(e);
   return op_cuda(mt::launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
 }
@@ -87,6 +88,7 @@ int mt_op_gemm_layout(const void* A, int64_t lda, const void* B, int64_t ldb, in
   g.status = status;
   if (layout & ~3) return op_fail("gemm: layout must be a combination of MT_GEMM_A_MN and MT_GEMM_B_MN");
   if (epilogue == MT_EPI_SWIGLU || epilogue == MT_EPI_ROPE) return op_fail("gemm_layout: use mt_op_gemm for SwiGLU/RoPE");
+  if (!A || !B) return op_fail("gemm: null A or B");
   if (const char* e = mt::gemm_check(g)) return op_fail(e);
   return op_cuda(mt::launch_gemm(g, static_cast<cudaStream_t>(stream)), "gemm");
 }
