@@ -116,6 +116,7 @@ int mt_op_gemm_grouped(const void* A, int64_t lda, const void* B, int64_t ldb, i
   g.ldc2 = ldc2;
   g.status = status;
   if (layout & ~3) return op_fail("gemm: layout must be a combination of MT_GEMM_A_MN and MT_GEMM_B_MN");
+  if (!A || !B) return op_fail("gemm: null A or B");
   if (const char* e = mt::gemm_grouped_check(g, offsets, groups, grouping)) return op_fail(e);
   return op_cuda(mt::launch_gemm_grouped(g, offsets, groups, grouping, static_cast<cudaStream_t>(stream)),
                  "grouped gemm");
