@@ -292,6 +292,7 @@ int mt_op_moe_route(const float* logits, int64_t N, int32_t E, int32_t k, int32_
 
 int mt_op_moe_zero_pads(const int32_t* order, int64_t P_rows, int32_t d, void* buf, void* stream) {
   if (P_rows <= 0 || d <= 0 || d % 8 || !order || !buf) return op_fail("moe zero pads: bad shape");
+  if (!al16(buf)) return op_fail("moe zero pads: buf must be 16-byte aligned");
   return op_cuda(mt::launch_moe_zero_pads(order, P_rows, d, static_cast<mt::bf16*>(buf),
                                           static_cast<cudaStream_t>(stream)),
                  "moe zero pads");
@@ -300,6 +301,8 @@ int mt_op_moe_zero_pads(const int32_t* order, int64_t P_rows, int32_t d, void* b
 int mt_op_moe_gather(const void* x, int64_t ldx, const int32_t* order, int32_t k, int64_t P, int32_t d, void* xp,
                      void* stream) {
   if (P <= 0 || k < 1 || d <= 0 || d % 8 || ldx % 8 || ldx < d) return op_fail("moe gather: bad shape");
+  if (!x || !order || !xp) return op_fail("moe gather: null x, order or xp");
+  if (!al16(x) || !al16(xp)) return op_fail("moe gather: x and xp must be 16-byte aligned");
   return op_cuda(mt::launch_moe_gather(static_cast<const mt::bf16*>(x), ldx, order, k, P, d,
                                        static_cast<mt::bf16*>(xp), static_cast<cudaStream_t>(stream)),
                  "moe gather");
@@ -308,6 +311,7 @@ int mt_op_moe_gather(const void* x, int64_t ldx, const int32_t* order, int32_t k
 int mt_op_moe_combine(const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k, int32_t d,
                       const void* res, void* out, void* stream) {
   if (const char* e = mt::moe_check(N, k, k, d)) return op_fail(e);
+  if (!yp || !pos || !gates || !out) return op_fail("moe combine: null yp, pos, gates or out");
   return op_cuda(mt::launch_moe_combine(static_cast<const mt::bf16*>(yp), pos, gates, N, k, d,
                                         static_cast<const mt::bf16*>(res), static_cast<mt::bf16*>(out),
                                         static_cast<cudaStream_t>(stream)),
@@ -317,6 +321,7 @@ int mt_op_moe_combine(const void* yp, const int32_t* pos, const float* gates, in
 int mt_op_moe_combine_bwd(const void* dy, const void* yp, const int32_t* pos, const float* gates, int64_t N, int32_t k,
                           int32_t d, void* dyp, float* dgates, void* stream) {
   if (const char* e = mt::moe_check(N, k, k, d)) return op_fail(e);
+  if (!dy || !yp || !pos || !gates || !dyp || !dgates) return op_fail("moe combine backward: null pointer");
   return op_cuda(mt::launch_moe_combine_bwd(static_cast<const mt::bf16*>(dy), static_cast<const mt::bf16*>(yp), pos,
                                             gates, N, k, d, static_cast<mt::bf16*>(dyp), dgates,
                                             static_cast<cudaStream_t>(stream)),
@@ -326,6 +331,7 @@ int mt_op_moe_combine_bwd(const void* dy, const void* yp, const int32_t* pos, co
 int mt_op_moe_gate_bwd(const int32_t* idx, const float* gates, const float* dgates, int64_t N, int32_t E, int32_t k,
                        void* ds, void* stream) {
   if (const char* e = mt::moe_check(N, E, k, 8)) return op_fail(e);
+  if (!idx || !gates || !dgates || !ds) return op_fail("moe gate backward: null pointer");
   return op_cuda(mt::launch_moe_gate_bwd(idx, gates, dgates, N, E, k, static_cast<mt::bf16*>(ds),
                                          static_cast<cudaStream_t>(stream)),
                  "moe gate backward");
@@ -334,6 +340,7 @@ int mt_op_moe_gate_bwd(const int32_t* idx, const float* gates, const float* dgat
 int mt_op_moe_scatter_bwd(const void* dxp, const int32_t* pos, int64_t N, int32_t k, int32_t d, const void* dres,
                           void* dx, void* stream) {
   if (const char* e = mt::moe_check(N, k, k, d)) return op_fail(e);
+  if (!dxp || !pos || !dx) return op_fail("moe scatter backward: null dxp, pos or dx");
   return op_cuda(mt::launch_moe_scatter_bwd(static_cast<const mt::bf16*>(dxp), pos, N, k, d,
                                             static_cast<const mt::bf16*>(dres), static_cast<mt::bf16*>(dx),
                                             static_cast<cudaStream_t>(stream)),

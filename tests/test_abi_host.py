@@ -417,6 +417,13 @@ ODD = 0x100008  # 8-byte aligned only
                             None, None), "RoPE tables"),
     (lambda L: L.mt_op_gemm(A0, 64, A1, 64, 256, 256, 64, 9, A2, 256, None, 0, None, 0, None, None, 0, 0, 0,
                             None, None), "unknown epilogue"),
+    (lambda L: L.mt_op_moe_gather(A0, 64, None, 2, 10, 64, A2, None), "null"),
+    (lambda L: L.mt_op_moe_gather(ODD, 64, A1, 2, 10, 64, A2, None), "16-byte"),
+    (lambda L: L.mt_op_moe_zero_pads(A0, 10, 64, ODD, None), "16-byte"),
+    (lambda L: L.mt_op_moe_combine(A0, None, A2, 5, 2, 64, None, A4, None), "null"),
+    (lambda L: L.mt_op_moe_combine_bwd(A0, A1, A2, A3, 5, 2, 64, A5, None, None), "null"),
+    (lambda L: L.mt_op_moe_gate_bwd(A0, A1, None, 5, 8, 2, A4, None), "null"),
+    (lambda L: L.mt_op_moe_scatter_bwd(A0, A1, 5, 2, 64, None, None, None), "null"),
 ])
 def test_elementwise_ops_reject_bad_arguments_before_any_launch(lib, call, msg):
     """Each per-kernel entry point checks sizes, pointers and the alignment
