@@ -2,7 +2,8 @@
 // cores: S = Q K^T and O += P V with tcgen05.mma, S and O accumulated in
 // TMEM, Q/K/V tiles brought in by TMA.
 //
-// One CTA per (128 queries, query head, batch); 10 warps:
+// One CTA per (128 queries, query head, batch), started longest causal row
+// first within chunks of a few heads (causal_cta_order); 10 warps:
 //   warp 0      TMA: Q once; K and V blocks of 128 keys into a 3-stage ring
 //               (one tensor map over the packed q|k|v projection buffer).
 //   warp 1      MMA (one thread): S_j = Q K_j^T into TMEM buffer j%2; once
